@@ -1,0 +1,90 @@
+"""Seeded synthetic inputs shared by the tests, the benchmark and the smoke
+check. Holds none of the decode arithmetic: only random draws, dtype casts
+and host copies.
+
+Recipe: every matrix bf16(N(0, 0.02)); norm gains bf16(1 + N(0, 0.05)); drawn
+from one torch generator seeded `seed` in the fixed order embed, then per
+layer attn_norm, wq, wk, wv, wo, mlp_norm, w_gate, w_up, w_down, then
+final_norm. Prompt tokens are uniform in [0, vocab) from a CPU generator
+(seed 1, sequence b of a batch: seed 100 + b). Pre-filled cache entries are
+bf16(N(0, 1)) from seed 2.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from .configs import ModelShape
+
+LAYER_KEYS = ("attn_norm", "wq", "wk", "wv", "wo", "mlp_norm", "w_gate", "w_up", "w_down")
+
+
+def layer_shapes(s: ModelShape) -> dict:
+    d, F = s.d_model, s.ffn_dim
+    return {
+        "attn_norm": (d,), "wq": (s.q_dim, d), "wk": (s.kv_dim, d), "wv": (s.kv_dim, d),
+        "wo": (d, s.q_dim), "mlp_norm": (d,), "w_gate": (F, d), "w_up": (F, d),
+        "w_down": (d, F),
+    }
+
+
+def _normal(shape, std, mean, gen, device):
+    t = torch.randn(shape, generator=gen, device=device, dtype=torch.float32)
+    if std != 1.0:
+        t.mul_(std)
+    if mean != 0.0:
+        t.add_(mean)
+    return t.to(torch.bfloat16)
+
+
+def make_weights(s: ModelShape, device="cpu", seed: int = 0) -> dict:
+    """Random-init bf16 weights of shape `s` on `device`."""
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    w = {"embed": _normal((s.vocab, s.d_model), 0.02, 0.0, gen, device), "layers": []}
+    for _ in range(s.n_layers):
+        lw = {}
+        for k, shp in layer_shapes(s).items():
+            if k.endswith("norm"):
+                lw[k] = _normal(shp, 0.05, 1.0, gen, device)
+            else:
+                lw[k] = _normal(shp, 0.02, 0.0, gen, device)
+        w["layers"].append(lw)
+    w["final_norm"] = _normal((s.d_model,), 0.05, 1.0, gen, device)
+    return w
+
+
+def prompt_tokens(vocab: int, n: int, seq: int = 0) -> torch.Tensor:
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(1 if seq == 0 else 100 + seq)
+    return torch.randint(0, vocab, (n,), generator=gen, dtype=torch.int64).to(torch.int32)
+
+
+def kv_cache(s: ModelShape, max_seq: int, batch: int = 1, device="cpu") -> tuple:
+    """Zeroed bf16 caches [L][B][Hkv][max_seq][hd]."""
+    shape = (s.n_layers, batch, s.n_kv_heads, max_seq, s.head_dim)
+    return (torch.zeros(shape, dtype=torch.bfloat16, device=device),
+            torch.zeros(shape, dtype=torch.bfloat16, device=device))
+
+
+def prefill_cache(k: torch.Tensor, v: torch.Tensor, n_positions: int, seed: int = 2) -> None:
+    """Fill positions [0, n_positions) of both caches with bf16(N(0,1))."""
+    gen = torch.Generator(device=k.device)
+    gen.manual_seed(seed)
+    shape = k[:, :, :, :n_positions, :].shape
+    k[:, :, :, :n_positions, :] = _normal(shape, 1.0, 0.0, gen, k.device)
+    v[:, :, :, :n_positions, :] = _normal(shape, 1.0, 0.0, gen, k.device)
+
+
+def bf16_bits(t: torch.Tensor) -> np.ndarray:
+    """Host copy of a bf16 tensor as its raw uint16 bit patterns."""
+    return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def host_weights(w: dict) -> dict:
+    """The same weights as host uint16 bit arrays (what the oracle reads)."""
+    return {
+        "embed": bf16_bits(w["embed"]),
+        "final_norm": bf16_bits(w["final_norm"]),
+        "layers": [{k: bf16_bits(v) for k, v in lw.items()} for lw in w["layers"]],
+    }
