@@ -1,0 +1,400 @@
+#!/usr/bin/env python3
+"""Batch-1 decode benchmark of the megakernel on the Llama-1B shape.
+
+One step = one greedy decode token (one megakernel launch) of the Llama-1B
+shaped model (16 layers, d 2048, 32/8 heads x 64, SwiGLU 8192, vocab 128256,
+tied embedding) with random bf16 weights, after a 128-token seeded prompt:
+the timed steps are positions 128..128+K-1 with the token fed back on the
+device. Weights (2.47 GB) exceed L2, so every step streams them from HBM.
+
+Prints ONE JSON line (rank 0). `--impl reference` times the fp64 CPU oracle
+on the host cores instead (a bounded sample of the same workload).
+With torchrun (--gpus N > 1) every rank runs an independent replica.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "llama1b"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=128)
+    ap.add_argument("--warmup", type=int, default=8)
+    ap.add_argument("--impl", default="mk", choices=["mk", "reference"])
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--no-comparators", action="store_true",
+                    help="skip the unfused-chain timings")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="budget of the oracle CPU-baseline sample")
+    return ap.parse_args()
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def algorithmic_bytes(shape, pos: int) -> int:
+    """Weights read by one step + keys/values attended over (positions 0..pos)."""
+    return shape.step_weight_bytes() + shape.kv_read_bytes(pos + 1)
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            d = json.load(open(path))
+            for k in ("hbm_gbs", "hbm_GBs", "hbm_copy_gbs"):
+                if k in d and d[k]:
+                    return float(d[k]), "of measured"
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, "of fallback"
+
+
+def kernel_sha() -> str:
+    h = hashlib.sha256()
+    for f in ("mk_kernel.cu", "mk_plan.h", "mk_host.cpp"):
+        h.update(open(os.path.join(ROOT, "decode_megakernel_llama_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic():
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "megakernel_llama1b_traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        d = json.load(open(path))
+        if d.get("kernel_sha") == kernel_sha():
+            return int(d["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu: int):
+        self.gpu = gpu
+        self.p = None
+
+    def __enter__(self):
+        try:
+            self.p = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.p = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.p is not None:
+            self.p.terminate()
+            try:
+                out, _ = self.p.communicate(timeout=5)
+            except Exception:
+                self.p.kill()
+                out = ""
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def oracle_sample(shape, host_w, budget_s: float, threads: int | None = None):
+    """Times the oracle's decode step on a bounded sample; returns (us_per_token, n, threads)."""
+    import oracle
+    from decode_megakernel_llama_gb300 import synth
+    if threads:
+        oracle.set_threads(threads)
+    cfg = oracle.OracleConfig(shape.n_layers, shape.d_model, shape.n_heads, shape.n_kv_heads,
+                              shape.head_dim, shape.ffn_dim, shape.vocab, shape.rms_eps,
+                              shape.rope_theta)
+    m = oracle.OracleModel(cfg, host_w, 64)
+    prompt = [int(t) for t in synth.prompt_tokens(shape.vocab, 64)]
+    n, t_total = 0, 0.0
+    while n < 64:
+        t0 = time.perf_counter()
+        m.decode_step(prompt[n], n)
+        t_total += time.perf_counter() - t0
+        n += 1
+        if t_total >= budget_s:
+            break
+    return 1e6 * t_total / n, n, oracle.get_threads()
+
+
+def run_reference(args, ws, rank):
+    """The oracle as it stands, on the host cores: W untimed then K timed
+    decode steps (one token each) of the same workload shape."""
+    if rank != 0:
+        return
+    import oracle
+    from decode_megakernel_llama_gb300 import synth
+    from decode_megakernel_llama_gb300.configs import WORKLOADS
+    oracle.build()
+    wl = WORKLOADS[args.workload]
+    shape = wl.shape
+    K, W = args.steps, args.warmup
+    host_w = synth.host_weights(synth.make_weights(shape, "cpu", 0))
+    oracle.set_threads(os.cpu_count() or 1)
+    cfg = oracle.OracleConfig(shape.n_layers, shape.d_model, shape.n_heads, shape.n_kv_heads,
+                              shape.head_dim, shape.ffn_dim, shape.vocab, shape.rms_eps,
+                              shape.rope_theta)
+    m = oracle.OracleModel(cfg, host_w, K + W)
+    tok = int(synth.prompt_tokens(shape.vocab, 1)[0])
+    for pos in range(W):
+        _, tok = m.decode_step(tok, pos)
+    t0 = time.perf_counter()
+    for pos in range(W, W + K):
+        _, tok = m.decode_step(tok, pos)
+    us = 1e6 * (time.perf_counter() - t0) / K
+    thr = oracle.get_threads()
+    line = {
+        "impl": "reference", "metric": "batch-1 decode us/token (Llama-1B shape) and achieved HBM GB/s vs peak",
+        "value": us, "unit": "us/token", "n_gpus": ws, "steps": K,
+        "warmup": W, "ms_per_step": us / 1e3, "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{wl.name}: Llama-1B shape, batch 1, greedy decode steps at "
+                               f"positions {W}..{W + K - 1} (fp64 CPU oracle)"},
+        "cpu_baseline": {"value": us, "unit": "us/token", "cores": thr, "kind": "oracle",
+                         "sample": f"{K} timed oracle decode steps after {W} warm-up steps"},
+        "e2e": {"value": us, "unit": "us/token", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_mk(args, ws, rank, local):
+    import torch
+    import torch.distributed as dist
+
+    from decode_megakernel_llama_gb300 import _lib, synth
+    from decode_megakernel_llama_gb300.build import build
+    from decode_megakernel_llama_gb300.configs import WORKLOADS
+
+    if ws > 1 and not dist.is_initialized():
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0 or ws == 1:
+        build()
+    if ws > 1:
+        dist.barrier()
+    wl = WORKLOADS[args.workload]
+    shape = wl.shape
+    K, W = args.steps, args.warmup
+    P = wl.prompt_len
+    if W < 3:
+        raise SystemExit("--warmup must be >= 3")
+    max_seq = P + max(K, wl.decode_steps)
+    w = synth.make_weights(shape, dev, 0)
+    kc, vc = synth.kv_cache(shape, max_seq, 1, dev)
+    mk = _lib.Megakernel(shape, w, kc, vc)
+    prompt = synth.prompt_tokens(shape.vocab, P)
+    stream = torch.cuda.current_stream(dev)
+    tok = torch.zeros(1, dtype=torch.int32, device=dev)
+    logits = torch.empty(shape.vocab, dtype=torch.float32, device=dev)
+
+    def run_prompt(step_fn):
+        for i in range(P):
+            step_fn(int(prompt[i]), i)
+
+    # prompt through the decode step (its last W steps are the warm-up)
+    run_prompt(lambda t, i: mk.step(t, i, tok, None, stream))
+    torch.cuda.synchronize()
+    if mk.status() != 0:
+        raise SystemExit("megakernel status error during the prompt")
+    tok.fill_(int(prompt[-1]))
+
+    # keep the clocks sampled under load around the timed region
+    def timed_decode():
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        if ws > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        start.record(stream)
+        for s in range(K):
+            mk.step_dev(tok, P + s, tok, None, stream)
+        end.record(stream)
+        torch.cuda.synchronize()
+        return start.elapsed_time(end)  # ms
+
+    with ClockSampler(local) as clk:
+        t_end = time.time() + 1.0
+        while time.time() < t_end:      # load the GPU before the timed region
+            for s in range(W):
+                mk.step_dev(tok, P + s, tok, None, stream)
+            torch.cuda.synchronize()
+        # W warm-up steps on the exact positions, then the timed K
+        for s in range(W):
+            mk.step_dev(tok, P + s, tok, None, stream)
+        ms = timed_decode()
+    if mk.status() != 0:
+        raise SystemExit("megakernel status error during timing")
+    t_max = ms
+    if ws > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        t_max = float(t.item())
+    us_per_tok_launch = 1e3 * ms / K                  # this rank's per-launch average
+    value = 1e3 * t_max / (K * ws)                     # aggregate us per token
+
+    # ---- end to end: the public call with host buffers (token H2D, token D2H)
+    h_in = torch.zeros(1, dtype=torch.int32).pin_memory()
+    h_out = torch.zeros(1, dtype=torch.int32).pin_memory()
+    h_in[0] = int(prompt[-1])
+    for s in range(W):
+        mk.step_host(h_in, P + s, h_out, None, stream)
+        h_in[0] = int(h_out[0])
+    if ws > 1:
+        dist.barrier()
+    t0 = time.perf_counter()
+    for s in range(K):
+        mk.step_host(h_in, P + s, h_out, None, stream)
+        h_in[0] = int(h_out[0])
+    e2e_s = time.perf_counter() - t0
+    e2e_val = 1e6 * e2e_s / K
+    if ws > 1:
+        t = torch.tensor([e2e_s], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_val = 1e6 * float(t.item()) / (K * ws)
+
+    # ---- comparators: the same kernels as an unfused chain (and as a graph)
+    comp = None
+    if not args.no_comparators:
+        torch.cuda.synchronize()
+        for s in range(W):
+            mk.step_unfused(int(prompt[-1]), P + s, tok, None, stream)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for s in range(K):
+            mk.step_unfused(int(prompt[-1]), P + s, tok, None, stream)
+        b.record(stream)
+        torch.cuda.synchronize()
+        unfused_us = 1e3 * a.elapsed_time(b) / K
+        graph_us = None
+        try:
+            g = torch.cuda.CUDAGraph()
+            cs = torch.cuda.Stream(dev)
+            cs.wait_stream(stream)
+            with torch.cuda.stream(cs):
+                mk.step_unfused(int(prompt[-1]), P, tok, None, cs)  # warm the capture stream
+            torch.cuda.synchronize()
+            with torch.cuda.graph(g, stream=cs):
+                mk.step_unfused(int(prompt[-1]), P, tok, None, cs)
+            for _ in range(W):
+                g.replay()
+            torch.cuda.synchronize()
+            a.record(stream)
+            for _ in range(K):
+                g.replay()
+            b.record(stream)
+            torch.cuda.synchronize()
+            graph_us = 1e3 * a.elapsed_time(b) / K
+        except Exception as e:  # capture support is a comparator, not the product
+            graph_us = f"unavailable: {type(e).__name__}"
+        if mk.status() != 0:
+            raise SystemExit("status error in comparators")
+        comp = {"unfused_chain_us_per_token": unfused_us,
+                "unfused_chain_graph_us_per_token": graph_us,
+                "unfused_launches_per_token": 5 * shape.n_layers + 1,
+                "megakernel_speedup_vs_unfused": unfused_us / us_per_tok_launch}
+
+    # ---- roofline of the megakernel (the only kernel)
+    mean_bytes = sum(algorithmic_bytes(shape, P + s) for s in range(K)) / K
+    achieved = mean_bytes / (us_per_tok_launch * 1e-6) / 1e9
+    peak, peak_kind = measured_peak()
+    roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+            "frac": achieved / peak, "peak_source": peak_kind,
+            "traffic": committed_traffic(), "bytes_per_launch": mean_bytes,
+            "kernel": "mk_megakernel"}
+
+    # ---- oracle on the host cores (rank 0 at N=1 only)
+    cpu = None
+    if rank == 0 and ws == 1:
+        import oracle
+        oracle.build()
+        host_w = synth.host_weights(w)
+        us, n, thr = oracle_sample(shape, host_w, args.cpu_seconds, os.cpu_count())
+        cpu = {"value": us, "unit": "us/token", "cores": thr, "kind": "oracle",
+               "sample": f"{n} oracle decode steps (positions 0..{n - 1}) of the same model, "
+                         f"{thr} OpenMP threads"}
+
+    if rank == 0:
+        line = {
+            "metric": "batch-1 decode us/token (Llama-1B shape) and achieved HBM GB/s vs peak",
+            "value": value, "unit": "us/token", "n_gpus": ws, "steps": K, "warmup": W,
+            "ms_per_step": t_max / K, "higher_is_better": False, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"{wl.name}: Llama-1B shape (16 layers, d 2048, 32 q / 8 kv heads "
+                                   f"x 64, SwiGLU 8192, vocab 128256 tied), batch 1, {P}-token prompt, "
+                                   f"timed decode positions {P}..{P + K - 1}",
+                       "l2": "inputs larger than L2: 2.47 GB of weights streamed every step",
+                       "parallelism": f"replicas x{ws}"},
+            "tokens_per_s": 1e6 / value,
+            "achieved_hbm_gbs": achieved,
+            "roofline": roof,
+            "e2e": {"value": e2e_val, "unit": "us/token", "h2d_bytes_per_step": 4,
+                    "d2h_bytes_per_step": 4},
+            "gpu_launches": K,
+            "clocks": clk.summary(),
+            "comparators": comp,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    mk.close()
+    if ws > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    ws, rank, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, ws, rank)
+    else:
+        run_mk(args, ws, rank, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,211 @@
+"""Thin ctypes binding of libmk.so (include/mk.h): argument marshalling only.
+
+Every step of the decode path runs in the library's CUDA kernels; this module
+only turns torch tensors into device pointers and sizes. If the library is
+missing it raises instead of falling back to anything else.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "_build", "libmk.so")
+HEADER = os.path.join(os.path.dirname(PKG), "include", "mk.h")
+
+MK_OK = 0
+MK_ERR_INVALID_ARG = -1
+MK_ERR_CUDA = -2
+MK_ERR_LAUNCH = -3
+MK_ERR_UNSUPPORTED = -4
+MK_ERR_TIMEOUT = -5
+MK_ERR_NOMEM = -6
+MK_INSTR_WORDS = 16
+
+
+class MKError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"mk error {code}: {msg}")
+        self.code = code
+
+
+class mk_config(ctypes.Structure):
+    _fields_ = [("n_layers", ctypes.c_int32), ("d_model", ctypes.c_int32),
+                ("n_heads", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("ffn_dim", ctypes.c_int32),
+                ("vocab", ctypes.c_int32), ("max_seq", ctypes.c_int32),
+                ("max_batch", ctypes.c_int32), ("attn_splits", ctypes.c_int32),
+                ("rms_eps", ctypes.c_float), ("rope_theta", ctypes.c_float)]
+
+
+class mk_layer_weights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("attn_norm", "wq", "wk", "wv", "wo", "mlp_norm",
+                                               "w_gate", "w_up", "w_down")]
+
+
+class mk_weights(ctypes.Structure):
+    _fields_ = [("embed", ctypes.c_void_p), ("final_norm", ctypes.c_void_p),
+                ("layers", ctypes.POINTER(mk_layer_weights))]
+
+
+class mk_kv_cache(ctypes.Structure):
+    _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p)]
+
+
+_lib = None
+_VP = ctypes.c_void_p
+_I32 = ctypes.c_int32
+_PI32 = ctypes.POINTER(ctypes.c_int32)
+
+
+def load(path: str = LIB_PATH):
+    """Loads libmk.so (built by decode_megakernel_llama_gb300.build)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is missing: run decode_megakernel_llama_gb300.build.build() "
+                          "(there is no fallback implementation)")
+    L = ctypes.CDLL(path)
+    L.mk_last_error.restype = ctypes.c_char_p
+    L.mk_create.argtypes = [ctypes.POINTER(mk_config), ctypes.POINTER(mk_weights),
+                            ctypes.POINTER(mk_kv_cache), ctypes.POINTER(_VP)]
+    L.mk_decode_step.argtypes = [_VP, _I32, _I32, _VP, _VP, _VP]
+    L.mk_decode_step_dev.argtypes = [_VP, _VP, _I32, _VP, _VP, _VP]
+    L.mk_decode_step_host.argtypes = [_VP, _PI32, _I32, _VP, _PI32, _VP]
+    L.mk_decode_step_unfused.argtypes = [_VP, _I32, _I32, _VP, _VP, _VP]
+    L.mk_get_status.argtypes = [_VP]
+    L.mk_set_wait_timeout.argtypes = [_VP, ctypes.c_uint64]
+    L.mk_set_trace.argtypes = [_VP, _I32]
+    L.mk_read_trace.argtypes = [_VP, ctypes.POINTER(ctypes.c_int64), _I32]
+    L.mk_plan_size.argtypes = [_VP, _PI32, _PI32]
+    L.mk_plan_inspect.argtypes = [ctypes.POINTER(mk_config), _I32, _PI32, _I32, _PI32, _PI32]
+    L.mk_destroy.argtypes = [_VP]
+    L.mk_destroy.restype = None
+    _lib = L
+    return L
+
+
+def declared_symbols(header: str = HEADER) -> list[str]:
+    """Function names declared in include/mk.h."""
+    text = open(header).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mk_[a-z_0-9]+)\s*\(", text)))
+
+
+def check(rc: int) -> int:
+    if rc < 0:
+        raise MKError(rc, load().mk_last_error().decode())
+    return rc
+
+
+def make_config(shape, max_seq: int, max_batch: int = 1, attn_splits: int = 0) -> mk_config:
+    return mk_config(shape.n_layers, shape.d_model, shape.n_heads, shape.n_kv_heads,
+                     shape.head_dim, shape.ffn_dim, shape.vocab, int(max_seq), int(max_batch),
+                     int(attn_splits), float(shape.rms_eps), float(shape.rope_theta))
+
+
+def plan_inspect(shape, n_sm: int, max_seq: int, attn_splits: int = 0):
+    """Host-only plan: returns (instr int32 [n, 16] as list of lists, queue lengths, n_counters)."""
+    import numpy as np
+    L = load()
+    cfg = make_config(shape, max_seq, 1, attn_splits)
+    qlen = (ctypes.c_int32 * n_sm)()
+    nctr = ctypes.c_int32(0)
+    n = check(L.mk_plan_inspect(ctypes.byref(cfg), n_sm, None, 0, qlen, ctypes.byref(nctr)))
+    buf = np.zeros((n, MK_INSTR_WORDS), dtype=np.int32)
+    check(L.mk_plan_inspect(ctypes.byref(cfg), n_sm,
+                            buf.ctypes.data_as(_PI32), n, qlen, ctypes.byref(nctr)))
+    return buf, np.array(list(qlen), dtype=np.int64), int(nctr.value)
+
+
+def _stream_ptr(stream) -> int:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream)
+
+
+class Megakernel:
+    """One model bound to the decode megakernel (owns an mk_handle).
+
+    weights: dict from synth.make_weights on a CUDA device (bf16 tensors).
+    k_cache, v_cache: bf16 CUDA tensors [L][max_batch][Hkv][max_seq][hd].
+    """
+
+    def __init__(self, shape, weights: dict, k_cache, v_cache, attn_splits: int = 0):
+        L = load()
+        self.shape = shape
+        self.max_seq = int(k_cache.shape[3])
+        self.max_batch = int(k_cache.shape[1])
+        self._keep = (weights, k_cache, v_cache)
+        self.cfg = make_config(shape, self.max_seq, self.max_batch, attn_splits)
+        layers = (mk_layer_weights * shape.n_layers)()
+        for i, lw in enumerate(weights["layers"]):
+            for k in ("attn_norm", "wq", "wk", "wv", "wo", "mlp_norm", "w_gate", "w_up", "w_down"):
+                setattr(layers[i], k, lw[k].data_ptr())
+        self._layers = layers
+        w = mk_weights(weights["embed"].data_ptr(), weights["final_norm"].data_ptr(),
+                       ctypes.cast(layers, ctypes.POINTER(mk_layer_weights)))
+        kv = mk_kv_cache(k_cache.data_ptr(), v_cache.data_ptr())
+        h = _VP()
+        check(L.mk_create(ctypes.byref(self.cfg), ctypes.byref(w), ctypes.byref(kv), ctypes.byref(h)))
+        self.h = h
+
+    def step(self, token: int, pos: int, out_token, logits=None, stream=None) -> None:
+        check(load().mk_decode_step(self.h, int(token), int(pos),
+                                    logits.data_ptr() if logits is not None else None,
+                                    out_token.data_ptr(), _stream_ptr(stream)))
+
+    def step_dev(self, d_token, pos: int, out_token, logits=None, stream=None) -> None:
+        check(load().mk_decode_step_dev(self.h, d_token.data_ptr(), int(pos),
+                                        logits.data_ptr() if logits is not None else None,
+                                        out_token.data_ptr(), _stream_ptr(stream)))
+
+    def step_unfused(self, token: int, pos: int, out_token, logits=None, stream=None) -> None:
+        check(load().mk_decode_step_unfused(self.h, int(token), int(pos),
+                                            logits.data_ptr() if logits is not None else None,
+                                            out_token.data_ptr(), _stream_ptr(stream)))
+
+    def step_host(self, host_token, pos: int, host_out_token, host_logits=None, stream=None) -> None:
+        """host_token / host_out_token: pinned int32 CPU tensors [1]; host_logits: pinned
+        float32 CPU tensor [vocab] or None."""
+        check(load().mk_decode_step_host(
+            self.h, ctypes.cast(host_token.data_ptr(), _PI32), int(pos),
+            host_logits.data_ptr() if host_logits is not None else None,
+            ctypes.cast(host_out_token.data_ptr(), _PI32), _stream_ptr(stream)))
+
+    def status(self) -> int:
+        return load().mk_get_status(self.h)
+
+    def set_wait_timeout(self, ns: int) -> None:
+        check(load().mk_set_wait_timeout(self.h, int(ns)))
+
+    def set_trace(self, on: bool) -> None:
+        check(load().mk_set_trace(self.h, 1 if on else 0))
+
+    def read_trace(self):
+        import numpy as np
+        n_sm, n_instr = ctypes.c_int32(), ctypes.c_int32()
+        check(load().mk_plan_size(self.h, ctypes.byref(n_sm), ctypes.byref(n_instr)))
+        buf = np.zeros((max(1, n_instr.value), 5), dtype=np.int64)
+        n = check(load().mk_read_trace(self.h, buf.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
+                                       buf.shape[0]))
+        return buf[:n]
+
+    def plan_size(self):
+        n_sm, n_instr = ctypes.c_int32(), ctypes.c_int32()
+        check(load().mk_plan_size(self.h, ctypes.byref(n_sm), ctypes.byref(n_instr)))
+        return n_sm.value, n_instr.value
+
+    def close(self) -> None:
+        if getattr(self, "h", None):
+            load().mk_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -1,0 +1,682 @@
+// mk_host.cpp — host scheduler and C ABI of the decode megakernel.
+//
+// The scheduler plans, once per model, one instruction sequence per SM and a
+// dependency count for every instruction ("Revolution der
+// KI-Beschleunigung: Wie ein Low-Latency Megakernel den Llama-1B Turbo
+// zündet", dasgeld.co: sequences pre-planned on the host and reused for many
+// forward passes without recompiling; counters in global memory that tell
+// an instruction when its inputs are ready). The plan is uploaded in
+// mk_create and every decode step is then one launch of the interpreter.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <numeric>
+#include <string>
+#include <vector>
+
+#include "../../include/mk.h"
+#include "mk_plan.h"
+
+extern "C" cudaError_t mk_kernel_configure(void);
+extern "C" cudaError_t mk_kernel_launch(const mk::Params *p, int n_sm, int cooperative,
+                                        cudaStream_t stream);
+extern "C" cudaError_t mk_kernel_occupancy(int *blocks_per_sm);
+
+namespace {
+
+thread_local std::string g_err;
+
+int fail(int code, const std::string &msg) {
+    g_err = msg;
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char *what) {
+    return fail(e == cudaErrorMemoryAllocation ? MK_ERR_NOMEM : MK_ERR_CUDA,
+                std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+using mk::Geo;
+using mk::Instr;
+
+// ---------------------------------------------------------------------------
+// Tile geometry for an input length K (see Geo in mk_plan.h).
+// ---------------------------------------------------------------------------
+bool make_geo(int K, Geo &g) {
+    if (K <= 0 || K % 256 != 0 || K > 16384) return false;
+    int sw = 1;
+    while (K / sw > 2048 || (K / sw) % 256 != 0) {
+        sw *= 2;
+        if (sw > mk::kConsumerWarps) return false;
+    }
+    g.K = K;
+    g.sw = sw;
+    g.rw = mk::kConsumerWarps / sw;
+    g.kslice = K / sw;
+    g.nx = g.kslice / 32;
+    const int row_bytes = K * 2;
+    g.m = mk::kPageBytes / (g.rw * row_bytes);
+    if (g.m < 1) return false;
+    g.rt = g.rw * g.m;
+    g.pad = 0;
+    return true;
+}
+
+struct Plan {
+    int n_sm = 0, S = 1, ppt = 0, n_lm = 0, n_stages = 0;
+    mk::CtrLayout cl{};
+    Geo geo_qkv{}, geo_o{}, geo_gu{}, geo_down{}, geo_lm{};
+    std::vector<std::vector<Instr>> q;
+    size_t n_instr() const {
+        size_t n = 0;
+        for (auto &v : q) n += v.size();
+        return n;
+    }
+};
+
+int check_config(const mk_config *c) {
+    if (!c) return fail(MK_ERR_INVALID_ARG, "config is NULL");
+    if (c->n_layers < 1 || c->n_layers > 4096 || c->d_model < 1 || c->n_heads < 1 ||
+        c->n_kv_heads < 1 || c->head_dim < 1 || c->ffn_dim < 1 || c->vocab < 1 || c->max_seq < 1 ||
+        c->max_batch < 1 || c->attn_splits < 0)
+        return fail(MK_ERR_INVALID_ARG, "config has a non-positive size");
+    if (!(c->rms_eps >= 0.f) || !(c->rope_theta > 0.f))
+        return fail(MK_ERR_INVALID_ARG, "rms_eps must be >= 0 and rope_theta > 0");
+    if (c->head_dim != 64 && c->head_dim != 128)
+        return fail(MK_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
+    if (c->n_heads % c->n_kv_heads != 0)
+        return fail(MK_ERR_INVALID_ARG, "n_heads must be a multiple of n_kv_heads");
+    const int G = c->n_heads / c->n_kv_heads, hd = c->head_dim;
+    if (G > mk::kMaxG || G * hd + hd + mk::kConsumerWarps * G * (hd + 2) > mk::kXbufFloats)
+        return fail(MK_ERR_UNSUPPORTED, "too many query heads per kv head for the attention scratch");
+    const int qd = c->n_heads * hd;
+    if (c->d_model % 256 || qd % 256 || c->ffn_dim % 256)
+        return fail(MK_ERR_UNSUPPORTED, "d_model, n_heads*head_dim and ffn_dim must be multiples of 256");
+    if (c->d_model > mk::kXbufFloats || qd > mk::kXbufFloats)
+        return fail(MK_ERR_UNSUPPORTED, "d_model and n_heads*head_dim must be <= 5120");
+    if (c->ffn_dim > 16384) return fail(MK_ERR_UNSUPPORTED, "ffn_dim must be <= 16384");
+    const double kv_elems = (double)c->n_layers * c->max_batch * c->n_kv_heads * c->max_seq * hd;
+    if (kv_elems * 2 > 9.0e18) return fail(MK_ERR_INVALID_ARG, "KV cache too large");
+    return MK_OK;
+}
+
+// Balanced contiguous split of N rows of one stage across the SMs. The
+// N % n_sm extra rows go to the SMs with the least bytes so far, so the
+// per-SM byte totals over the whole step stay even.
+struct Chunk {
+    int sm, r0, n;
+};
+
+std::vector<Chunk> split_rows(int N, double cost_per_row, std::vector<double> &load, int max_rows) {
+    const int n_sm = (int)load.size();
+    const int base = N / n_sm, extra = N % n_sm;
+    std::vector<int> order(n_sm);
+    std::iota(order.begin(), order.end(), 0);
+    std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return load[a] < load[b]; });
+    std::vector<int> cnt(n_sm, base);
+    for (int i = 0; i < extra; ++i) cnt[order[i]] += 1;
+    std::vector<Chunk> out;
+    int r = 0;
+    for (int sm = 0; sm < n_sm; ++sm) {
+        int left = cnt[sm];
+        load[sm] += left * cost_per_row;
+        while (left > 0) {
+            const int n = std::min(left, max_rows);
+            out.push_back({sm, r, n});
+            r += n;
+            left -= n;
+        }
+    }
+    return out;
+}
+
+int build_plan(const mk_config *c, int n_sm, Plan &P) {
+    int rc = check_config(c);
+    if (rc) return rc;
+    if (n_sm < 1 || n_sm > 4096) return fail(MK_ERR_INVALID_ARG, "bad SM count");
+    const int L = c->n_layers, d = c->d_model, Hq = c->n_heads, Hkv = c->n_kv_heads,
+              hd = c->head_dim, F = c->ffn_dim, V = c->vocab, G = Hq / Hkv;
+    const int qd = Hq * hd, kvd = Hkv * hd;
+    P = Plan();
+    P.n_sm = n_sm;
+    if (!make_geo(d, P.geo_qkv) || !make_geo(qd, P.geo_o) || !make_geo(d, P.geo_gu) ||
+        !make_geo(F, P.geo_down) || !make_geo(d, P.geo_lm))
+        return fail(MK_ERR_UNSUPPORTED, "no tile geometry for these input lengths");
+    if (P.geo_gu.rt < 2 || P.geo_gu.rt % 2)
+        return fail(MK_ERR_UNSUPPORTED, "gate/up tile needs an even row count");
+    P.ppt = (mk::kPageBytes / 2) / (hd * 2);
+    const int max_tiles = (c->max_seq + P.ppt - 1) / P.ppt;
+    int S = std::max(1, std::min(n_sm / Hkv, max_tiles));
+    if (c->attn_splits > 0) S = std::min(c->attn_splits, std::max(1, max_tiles));
+    P.S = S;
+    P.n_stages = mk::kStagesPerLayer * L + 1;
+    auto &cl = P.cl;
+    cl.qkv_grp = 0;
+    cl.merge = cl.qkv_grp + L * Hkv;
+    cl.attn_done = cl.merge + L * Hkv;
+    cl.oproj_done = cl.attn_done + L;
+    cl.gateup_done = cl.oproj_done + L;
+    cl.down_done = cl.gateup_done + L;
+    cl.lm_arrive = cl.down_done + L;
+    cl.total = cl.lm_arrive + 1;
+
+    P.q.assign(n_sm, {});
+    std::vector<double> load(n_sm, 0.0);
+    auto mk_instr = [](int op, int layer, int stage) {
+        Instr in;
+        std::memset(&in, 0, sizeof in);
+        in.op = op;
+        in.layer = layer;
+        in.stage = stage;
+        in.wait_ctr = -1;
+        return in;
+    };
+    auto set_bytes = [](Instr &in, long long b) {
+        in.bytes_lo = (int32_t)(b & 0xFFFFFFFFll);
+        in.bytes_hi = (int32_t)(b >> 32);
+    };
+    const int cap_qkv = mk::kRedCap / P.geo_qkv.sw, cap_o = mk::kRedCap / P.geo_o.sw,
+              cap_gu = mk::kRedCap / (2 * P.geo_gu.sw), cap_down = mk::kRedCap / P.geo_down.sw,
+              cap_lm = mk::kRedCap / P.geo_lm.sw;
+    int prev_down = 0;
+    for (int l = 0; l < L; ++l) {
+        const int st = mk::kStagesPerLayer * l;
+        // ---- QKV: rows of [Wq; Wk; Wv]
+        std::vector<int> touch(Hkv, 0);
+        const int mat_start[4] = {0, qd, qd + kvd, qd + 2 * kvd};
+        for (const Chunk &ch : split_rows(qd + 2 * kvd, 2.0 * d, load, cap_qkv)) {
+            int r = ch.r0, end = ch.r0 + ch.n;
+            while (r < end) {
+                int mat = r < mat_start[1] ? 0 : (r < mat_start[2] ? 1 : 2);
+                int e = std::min(end, mat_start[mat + 1]);
+                Instr in = mk_instr(mk::OP_QKV, l, st);
+                in.mat = mat;
+                in.a0 = r - mat_start[mat];
+                in.a1 = e - r;
+                int h0 = in.a0 / hd, h1 = (in.a0 + in.a1 - 1) / hd;
+                int g0 = mat == 0 ? h0 / G : h0, g1 = mat == 0 ? h1 / G : h1;
+                in.sig_ctr = cl.qkv_grp + l * Hkv + g0;
+                in.sig_n = g1 - g0 + 1;
+                for (int g = g0; g <= g1; ++g) touch[g] += 1;
+                if (l > 0) {
+                    in.wait_ctr = cl.down_done + (l - 1);
+                    in.wait_target = prev_down;
+                }
+                set_bytes(in, 2ll * in.a1 * d);
+                P.q[ch.sm].push_back(in);
+                r = e;
+            }
+        }
+        // ---- attention: Hkv x S splits, each to the least-loaded SM
+        const double attn_cost = 2.0 * 2.0 * hd * std::ceil((double)c->max_seq / S) + 4096.0;
+        for (int h = 0; h < Hkv; ++h)
+            for (int s = 0; s < S; ++s) {
+                int sm = (int)(std::min_element(load.begin(), load.end()) - load.begin());
+                load[sm] += attn_cost;
+                Instr in = mk_instr(mk::OP_ATTN, l, st + 1);
+                in.a0 = h;
+                in.a1 = s;
+                in.wait_ctr = cl.qkv_grp + l * Hkv + h;
+                in.wait_target = touch[h];
+                P.q[sm].push_back(in);
+            }
+        // ---- O-projection + residual
+        int n_o = 0;
+        for (const Chunk &ch : split_rows(d, 2.0 * qd, load, cap_o)) {
+            Instr in = mk_instr(mk::OP_OPROJ, l, st + 2);
+            in.a0 = ch.r0;
+            in.a1 = ch.n;
+            in.wait_ctr = cl.attn_done + l;
+            in.wait_target = Hkv;
+            in.sig_ctr = cl.oproj_done + l;
+            in.sig_n = 1;
+            set_bytes(in, 2ll * ch.n * qd);
+            P.q[ch.sm].push_back(in);
+            ++n_o;
+        }
+        // ---- gate/up + SiLU
+        int n_gu = 0;
+        for (const Chunk &ch : split_rows(F, 4.0 * d, load, cap_gu)) {
+            Instr in = mk_instr(mk::OP_GATEUP, l, st + 3);
+            in.a0 = ch.r0;
+            in.a1 = ch.n;
+            in.wait_ctr = cl.oproj_done + l;
+            in.wait_target = n_o;
+            in.sig_ctr = cl.gateup_done + l;
+            in.sig_n = 1;
+            set_bytes(in, 4ll * ch.n * d);
+            P.q[ch.sm].push_back(in);
+            ++n_gu;
+        }
+        // ---- down + residual
+        int n_down = 0;
+        for (const Chunk &ch : split_rows(d, 2.0 * F, load, cap_down)) {
+            Instr in = mk_instr(mk::OP_DOWN, l, st + 4);
+            in.a0 = ch.r0;
+            in.a1 = ch.n;
+            in.wait_ctr = cl.gateup_done + l;
+            in.wait_target = n_gu;
+            in.sig_ctr = cl.down_done + l;
+            in.sig_n = 1;
+            set_bytes(in, 2ll * ch.n * F);
+            P.q[ch.sm].push_back(in);
+            ++n_down;
+        }
+        prev_down = n_down;
+    }
+    // ---- final norm + tied LM head + argmax
+    int slot = 0;
+    for (const Chunk &ch : split_rows(V, 2.0 * d, load, cap_lm)) {
+        Instr in = mk_instr(mk::OP_LMHEAD, L, mk::kStagesPerLayer * L);
+        in.layer = 0;
+        in.a0 = ch.r0;
+        in.a1 = ch.n;
+        in.wait_ctr = cl.down_done + (L - 1);
+        in.wait_target = prev_down;
+        in.slot = slot++;
+        set_bytes(in, 2ll * ch.n * d);
+        P.q[ch.sm].push_back(in);
+    }
+    P.n_lm = slot;
+    return MK_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Device-side handle
+// ---------------------------------------------------------------------------
+struct DevBump {
+    char *base = nullptr;
+    size_t off = 0;
+    size_t take(size_t bytes) {
+        size_t o = off;
+        off += (bytes + 255) & ~size_t(255);
+        return o;
+    }
+    template <class T>
+    T *at(size_t o) const {
+        return reinterpret_cast<T *>(base + o);
+    }
+};
+
+}  // namespace
+
+struct mk_handle {
+    mk_config cfg;
+    Plan plan;
+    int device = 0;
+    mk::Params base{};     // everything but the per-step fields
+    void *dev_mem = nullptr;
+    mk::LayerW *d_layers = nullptr;
+    int32_t *d_tok_in = nullptr;   // host path: token staged here
+    int32_t *d_tok_out = nullptr;  // host path: greedy token
+    float *d_logits = nullptr;     // host path: logits
+    int32_t *d_status = nullptr;
+    uint32_t *d_ctr = nullptr, *d_exit = nullptr;
+    int32_t *d_abort = nullptr;
+    size_t ctr_bytes = 0;
+    unsigned long long timeout_ns = 2000000000ull;
+    long long *d_trace = nullptr;
+    int trace_cap = 0;
+    bool trace_on = false;
+    std::vector<int> qlen;
+};
+
+namespace {
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int launch(mk_handle *h, int32_t token, const int32_t *d_token, int32_t position, float *out_logits,
+           int32_t *out_token, cudaStream_t stream, bool unfused) {
+    if (!h) return fail(MK_ERR_INVALID_ARG, "handle is NULL");
+    if (!out_token) return fail(MK_ERR_INVALID_ARG, "out_token is NULL");
+    if (position < 0 || position >= h->cfg.max_seq)
+        return fail(MK_ERR_INVALID_ARG, "position outside [0, max_seq)");
+    if (!d_token && (token < 0 || token >= h->cfg.vocab))
+        return fail(MK_ERR_INVALID_ARG, "token_id outside [0, vocab)");
+    mk::Params p = h->base;
+    p.token = token;
+    p.d_token = d_token;
+    p.pos = position;
+    p.out_logits = out_logits;
+    p.out_token = out_token;
+    p.timeout_ns = h->timeout_ns;
+    p.trace = h->trace_on ? h->d_trace : nullptr;
+    p.trace_cap = h->trace_cap;
+    cudaError_t e = cudaSetDevice(h->device);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaSetDevice");
+    if (!unfused) {
+        p.stage_lo = 0;
+        p.stage_hi = h->plan.n_stages;
+        p.reset_at_exit = 1;
+        e = mk_kernel_launch(&p, h->plan.n_sm, 1, stream);
+        if (e == cudaErrorCooperativeLaunchTooLarge)
+            return fail(MK_ERR_LAUNCH, "persistent grid cannot be co-resident on this device");
+        if (e != cudaSuccess) return cuda_fail(e, "megakernel launch");
+        return MK_OK;
+    }
+    for (int s = 0; s < h->plan.n_stages; ++s) {
+        p.stage_lo = s;
+        p.stage_hi = s + 1;
+        p.reset_at_exit = (s == h->plan.n_stages - 1);
+        e = mk_kernel_launch(&p, h->plan.n_sm, 0, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "stage launch");
+    }
+    return MK_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *mk_last_error(void) { return g_err.c_str(); }
+
+int mk_plan_inspect(const mk_config *config, int32_t n_sm, int32_t *out_instr, int32_t cap,
+                    int32_t *out_queue_len, int32_t *out_n_counters) {
+    Plan P;
+    int rc = build_plan(config, n_sm, P);
+    if (rc) return rc;
+    const size_t n = P.n_instr();
+    if (out_queue_len)
+        for (int s = 0; s < n_sm; ++s) out_queue_len[s] = (int32_t)P.q[s].size();
+    if (out_n_counters) *out_n_counters = P.cl.total;
+    if (out_instr) {
+        if ((size_t)cap < n) return fail(MK_ERR_INVALID_ARG, "cap smaller than the plan");
+        size_t k = 0;
+        for (int s = 0; s < n_sm; ++s)
+            for (const Instr &in : P.q[s]) std::memcpy(out_instr + 16 * (k++), &in, sizeof(Instr));
+    }
+    return (int)n;
+}
+
+int mk_create(const mk_config *config, const mk_weights *w, const mk_kv_cache *kv,
+              mk_handle **out) {
+    if (!out) return fail(MK_ERR_INVALID_ARG, "out is NULL");
+    *out = nullptr;
+    int rc = check_config(config);
+    if (rc) return rc;
+    if (!w || !w->embed || !w->final_norm || !w->layers || !kv || !kv->k || !kv->v)
+        return fail(MK_ERR_INVALID_ARG, "a weight or cache pointer is NULL");
+    const mk_config &c = *config;
+    if (!aligned16(w->embed) || !aligned16(w->final_norm) || !aligned16(kv->k) || !aligned16(kv->v))
+        return fail(MK_ERR_INVALID_ARG, "weights and caches must be 16-byte aligned");
+    for (int l = 0; l < c.n_layers; ++l) {
+        const mk_layer_weights &lw = w->layers[l];
+        const void *ps[9] = {lw.attn_norm, lw.wq, lw.wk, lw.wv, lw.wo,
+                             lw.mlp_norm, lw.w_gate, lw.w_up, lw.w_down};
+        for (const void *q : ps) {
+            if (!q) return fail(MK_ERR_INVALID_ARG, "a layer weight pointer is NULL");
+            if (!aligned16(q)) return fail(MK_ERR_INVALID_ARG, "layer weights must be 16-byte aligned");
+        }
+    }
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    cudaDeviceProp prop;
+    e = cudaGetDeviceProperties(&prop, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDeviceProperties");
+    if (!(prop.major == 10 && prop.minor == 3))
+        return fail(MK_ERR_UNSUPPORTED, "built for sm_103 (GB300); this device is sm_" +
+                                            std::to_string(prop.major) + std::to_string(prop.minor));
+    int coop = 0;
+    cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
+    if (!coop) return fail(MK_ERR_UNSUPPORTED, "device has no cooperative launch");
+    e = mk_kernel_configure();
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+    int bps = 0;
+    e = mk_kernel_occupancy(&bps);
+    if (e != cudaSuccess) return cuda_fail(e, "occupancy query");
+    if (bps < 1) return fail(MK_ERR_LAUNCH, "megakernel CTA does not fit on an SM");
+
+    mk_handle *h = new (std::nothrow) mk_handle();
+    if (!h) return fail(MK_ERR_NOMEM, "host allocation failed");
+    h->cfg = c;
+    h->device = dev;
+    rc = build_plan(config, prop.multiProcessorCount, h->plan);
+    if (rc) {
+        delete h;
+        return rc;
+    }
+    const Plan &P = h->plan;
+    const int L = c.n_layers, d = c.d_model, Hq = c.n_heads, Hkv = c.n_kv_heads, hd = c.head_dim,
+              F = c.ffn_dim, V = c.vocab;
+    const size_t n_instr = P.n_instr();
+    // ---- flat queues and stage index
+    std::vector<Instr> flat;
+    flat.reserve(n_instr);
+    std::vector<int32_t> qbeg((size_t)P.n_sm * (P.n_stages + 1));
+    h->qlen.resize(P.n_sm);
+    for (int s = 0; s < P.n_sm; ++s) {
+        const int base = (int)flat.size();
+        h->qlen[s] = (int)P.q[s].size();
+        int k = 0;
+        for (int st = 0; st <= P.n_stages; ++st) {
+            while (k < (int)P.q[s].size() && P.q[s][k].stage < st) ++k;
+            qbeg[(size_t)s * (P.n_stages + 1) + st] = base + k;
+        }
+        flat.insert(flat.end(), P.q[s].begin(), P.q[s].end());
+    }
+    // ---- RoPE table: angle pos * theta^(-2i/hd), in double
+    std::vector<float> rope((size_t)c.max_seq * hd);
+    for (int pos = 0; pos < c.max_seq; ++pos)
+        for (int i = 0; i < hd / 2; ++i) {
+            const double inv_freq = std::pow((double)c.rope_theta, -2.0 * i / (double)hd);
+            const double a = (double)pos * inv_freq;
+            rope[((size_t)pos * (hd / 2) + i) * 2] = (float)std::cos(a);
+            rope[((size_t)pos * (hd / 2) + i) * 2 + 1] = (float)std::sin(a);
+        }
+    // ---- one device allocation, carved up
+    DevBump b;
+    const size_t o_layers = b.take(sizeof(mk::LayerW) * L);
+    const size_t o_x = b.take(sizeof(float) * d);
+    const size_t o_qkv = b.take(sizeof(float) * (size_t)L * (Hq + 2 * Hkv) * hd);
+    const size_t o_part = b.take(sizeof(float) * (size_t)L * Hq * P.S * (hd + 2));
+    const size_t o_att = b.take(sizeof(float) * (size_t)L * Hq * hd);
+    const size_t o_h = b.take(sizeof(float) * (size_t)L * F);
+    const size_t o_lm = b.take(sizeof(unsigned long long) * P.n_lm);
+    const size_t o_ctr = b.take(sizeof(uint32_t) * P.cl.total);
+    const size_t o_exit = b.take(sizeof(uint32_t));
+    const size_t o_status = b.take(sizeof(int32_t));
+    const size_t o_abort = b.take(sizeof(int32_t));
+    const size_t o_tin = b.take(sizeof(int32_t));
+    const size_t o_tout = b.take(sizeof(int32_t));
+    const size_t o_logits = b.take(sizeof(float) * V);
+    const size_t o_rope = b.take(sizeof(float) * rope.size());
+    const size_t o_instr = b.take(sizeof(Instr) * flat.size());
+    const size_t o_qbeg = b.take(sizeof(int32_t) * qbeg.size());
+    e = cudaMalloc(&h->dev_mem, b.off);
+    if (e != cudaSuccess) {
+        delete h;
+        return cuda_fail(e, "cudaMalloc(scratch)");
+    }
+    b.base = static_cast<char *>(h->dev_mem);
+    std::vector<mk::LayerW> lws(L);
+    for (int l = 0; l < L; ++l) {
+        const mk_layer_weights &lw = w->layers[l];
+        lws[l] = {(const uint16_t *)lw.attn_norm, (const uint16_t *)lw.wq, (const uint16_t *)lw.wk,
+                  (const uint16_t *)lw.wv, (const uint16_t *)lw.wo, (const uint16_t *)lw.mlp_norm,
+                  (const uint16_t *)lw.w_gate, (const uint16_t *)lw.w_up, (const uint16_t *)lw.w_down};
+    }
+    bool ok = cudaMemset(h->dev_mem, 0, b.off) == cudaSuccess &&
+              cudaMemcpy(b.at<char>(o_layers), lws.data(), sizeof(mk::LayerW) * L, cudaMemcpyHostToDevice) == cudaSuccess &&
+              cudaMemcpy(b.at<char>(o_rope), rope.data(), sizeof(float) * rope.size(), cudaMemcpyHostToDevice) == cudaSuccess &&
+              cudaMemcpy(b.at<char>(o_instr), flat.data(), sizeof(Instr) * flat.size(), cudaMemcpyHostToDevice) == cudaSuccess &&
+              cudaMemcpy(b.at<char>(o_qbeg), qbeg.data(), sizeof(int32_t) * qbeg.size(), cudaMemcpyHostToDevice) == cudaSuccess &&
+              cudaDeviceSynchronize() == cudaSuccess;
+    if (!ok) {
+        e = cudaGetLastError();
+        cudaFree(h->dev_mem);
+        delete h;
+        return cuda_fail(e, "uploading the plan");
+    }
+    h->d_layers = b.at<mk::LayerW>(o_layers);
+    h->d_tok_in = b.at<int32_t>(o_tin);
+    h->d_tok_out = b.at<int32_t>(o_tout);
+    h->d_logits = b.at<float>(o_logits);
+    h->d_status = b.at<int32_t>(o_status);
+    h->d_ctr = b.at<uint32_t>(o_ctr);
+    h->d_exit = b.at<uint32_t>(o_exit);
+    h->d_abort = b.at<int32_t>(o_abort);
+
+    mk::Params &p = h->base;
+    p.L = L; p.d = d; p.Hq = Hq; p.Hkv = Hkv; p.hd = hd; p.F = F; p.V = V;
+    p.max_seq = c.max_seq; p.max_batch = c.max_batch; p.S = P.S; p.G = Hq / Hkv; p.ppt = P.ppt;
+    p.eps = c.rms_eps;
+    p.n_lm = P.n_lm; p.n_stages = P.n_stages;
+    p.geo_qkv = P.geo_qkv; p.geo_o = P.geo_o; p.geo_gu = P.geo_gu; p.geo_down = P.geo_down;
+    p.geo_lm = P.geo_lm;
+    p.cl = P.cl;
+    p.embed = (const uint16_t *)w->embed;
+    p.final_norm = (const uint16_t *)w->final_norm;
+    p.layers = h->d_layers;
+    p.kc = (uint16_t *)kv->k;
+    p.vc = (uint16_t *)kv->v;
+    p.x = b.at<float>(o_x);
+    p.qkv = b.at<float>(o_qkv);
+    p.part = b.at<float>(o_part);
+    p.att = b.at<float>(o_att);
+    p.h = b.at<float>(o_h);
+    p.lm_part = b.at<unsigned long long>(o_lm);
+    p.ctr = h->d_ctr;
+    p.exit_ctr = h->d_exit;
+    p.status = h->d_status;
+    p.abort_flag = h->d_abort;
+    p.rope = b.at<float>(o_rope);
+    p.instr = b.at<Instr>(o_instr);
+    p.q_begin = b.at<int32_t>(o_qbeg);
+    h->ctr_bytes = o_tin - o_ctr;  // counters, exit, status, abort
+    if (getenv("MK_LOG")) {
+        size_t mx = 0, mn = (size_t)-1;
+        for (auto &q : P.q) { mx = std::max(mx, q.size()); mn = std::min(mn, q.size()); }
+        fprintf(stderr, "[mk] plan: %d SMs, %zu instructions (%zu..%zu per SM), %d splits, %d counters\n",
+                P.n_sm, n_instr, mn, mx, P.S, P.cl.total);
+    }
+    *out = h;
+    return MK_OK;
+}
+
+int mk_decode_step(mk_handle *h, int32_t token_id, int32_t position, float *out_logits,
+                   int32_t *out_token, void *stream) {
+    return launch(h, token_id, nullptr, position, out_logits, out_token, (cudaStream_t)stream, false);
+}
+
+int mk_decode_step_dev(mk_handle *h, const int32_t *d_token_id, int32_t position, float *out_logits,
+                       int32_t *out_token, void *stream) {
+    if (!d_token_id) return fail(MK_ERR_INVALID_ARG, "d_token_id is NULL");
+    return launch(h, 0, d_token_id, position, out_logits, out_token, (cudaStream_t)stream, false);
+}
+
+int mk_decode_step_unfused(mk_handle *h, int32_t token_id, int32_t position, float *out_logits,
+                           int32_t *out_token, void *stream) {
+    return launch(h, token_id, nullptr, position, out_logits, out_token, (cudaStream_t)stream, true);
+}
+
+int mk_decode_step_host(mk_handle *h, const int32_t *host_token, int32_t position,
+                        float *host_logits, int32_t *host_out_token, void *stream) {
+    if (!h || !host_token || !host_out_token)
+        return fail(MK_ERR_INVALID_ARG, "handle or host token pointer is NULL");
+    if (*host_token < 0 || *host_token >= h->cfg.vocab)
+        return fail(MK_ERR_INVALID_ARG, "token_id outside [0, vocab)");
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e = cudaSetDevice(h->device);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaSetDevice");
+    e = cudaMemcpyAsync(h->d_tok_in, host_token, sizeof(int32_t), cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(e, "token upload");
+    int rc = launch(h, 0, h->d_tok_in, position, host_logits ? h->d_logits : nullptr, h->d_tok_out, s,
+                    false);
+    if (rc) return rc;
+    e = cudaMemcpyAsync(host_out_token, h->d_tok_out, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
+    if (e != cudaSuccess) return cuda_fail(e, "token download");
+    if (host_logits) {
+        e = cudaMemcpyAsync(host_logits, h->d_logits, sizeof(float) * h->cfg.vocab,
+                            cudaMemcpyDeviceToHost, s);
+        if (e != cudaSuccess) return cuda_fail(e, "logits download");
+    }
+    e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    return MK_OK;
+}
+
+int mk_get_status(mk_handle *h) {
+    if (!h) return fail(MK_ERR_INVALID_ARG, "handle is NULL");
+    cudaError_t e = cudaSetDevice(h->device);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+    int32_t st = 0;
+    e = cudaMemcpy(&st, h->d_status, sizeof st, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "status read");
+    if (st == mk::DS_OK) return MK_OK;
+    // a failed step leaves counters mid-way: clear them with the status
+    e = cudaMemset(h->d_ctr, 0, h->ctr_bytes);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "status reset");
+    if (st == mk::DS_BAD_TOKEN) return fail(MK_ERR_INVALID_ARG, "device token outside [0, vocab)");
+    return fail(MK_ERR_TIMEOUT, "an in-kernel dependency wait timed out");
+}
+
+int mk_set_wait_timeout(mk_handle *h, uint64_t timeout_ns) {
+    if (!h || timeout_ns == 0) return fail(MK_ERR_INVALID_ARG, "bad handle or zero timeout");
+    h->timeout_ns = timeout_ns;
+    return MK_OK;
+}
+
+int mk_set_trace(mk_handle *h, int32_t enable) {
+    if (!h) return fail(MK_ERR_INVALID_ARG, "handle is NULL");
+    if (enable && !h->d_trace) {
+        int cap = 0;
+        for (int q : h->qlen) cap = std::max(cap, q);
+        cap = std::max(cap, 1);
+        cudaError_t e = cudaSetDevice(h->device);
+        if (e == cudaSuccess)
+            e = cudaMalloc(&h->d_trace, sizeof(long long) * 5 * (size_t)cap * h->plan.n_sm);
+        if (e == cudaSuccess)
+            e = cudaMemset(h->d_trace, 0, sizeof(long long) * 5 * (size_t)cap * h->plan.n_sm);
+        if (e != cudaSuccess) {
+            h->d_trace = nullptr;
+            return cuda_fail(e, "trace buffer");
+        }
+        h->trace_cap = cap;
+    }
+    h->trace_on = enable != 0;
+    return MK_OK;
+}
+
+int mk_read_trace(mk_handle *h, int64_t *host_out, int32_t cap) {
+    if (!h || !host_out || cap < 0) return fail(MK_ERR_INVALID_ARG, "bad arguments");
+    if (!h->d_trace) return 0;
+    std::vector<long long> buf(5 * (size_t)h->trace_cap * h->plan.n_sm);
+    cudaError_t e = cudaSetDevice(h->device);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e == cudaSuccess)
+        e = cudaMemcpy(buf.data(), h->d_trace, sizeof(long long) * buf.size(), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "trace read");
+    int n = 0;
+    for (int s = 0; s < h->plan.n_sm; ++s)
+        for (int i = 0; i < h->qlen[s] && i < h->trace_cap; ++i) {
+            if (n >= cap) return n;
+            std::memcpy(host_out + 5 * (size_t)n, &buf[5 * ((size_t)s * h->trace_cap + i)],
+                        5 * sizeof(long long));
+            ++n;
+        }
+    return n;
+}
+
+int mk_plan_size(const mk_handle *h, int32_t *n_sm, int32_t *n_instr) {
+    if (!h) return fail(MK_ERR_INVALID_ARG, "handle is NULL");
+    if (n_sm) *n_sm = h->plan.n_sm;
+    if (n_instr) *n_instr = (int32_t)h->plan.n_instr();
+    return MK_OK;
+}
+
+void mk_destroy(mk_handle *h) {
+    if (!h) return;
+    cudaSetDevice(h->device);
+    cudaDeviceSynchronize();
+    if (h->d_trace) cudaFree(h->d_trace);
+    if (h->dev_mem) cudaFree(h->dev_mem);
+    delete h;
+}
+
+}  // extern "C"

@@ -1,0 +1,121 @@
+// mk_plan.h — instruction format, tile geometry and kernel parameters shared
+// by the host scheduler (mk_host.cpp) and the persistent interpreter kernel
+// (mk_kernel.cu).
+//
+// The design follows the megakernel article ("Revolution der
+// KI-Beschleunigung: Wie ein Low-Latency Megakernel den Llama-1B Turbo
+// zündet", dasgeld.co): the host plans one instruction sequence per SM once
+// (internal-infrastructure paragraph), the kernel interprets it, and
+// instructions wait on / bump dependency counters in global memory
+// (synchronisation paragraph).
+#pragma once
+#include <stdint.h>
+
+namespace mk {
+
+// ---- fixed kernel geometry ------------------------------------------------
+constexpr int kConsumerWarps = 8;                    // compute warps per CTA
+constexpr int kConsumerThreads = kConsumerWarps * 32;
+constexpr int kThreads = kConsumerThreads + 32;      // + one producer (TMA) warp
+constexpr int kPageBytes = 32768;                    // one shared-memory page
+constexpr int kPages = 6;                            // pages in the ring
+constexpr int kRedCap = 2048;                        // floats of per-row partials
+constexpr int kXbufFloats = 5120;                    // staged input vector / attention scratch
+constexpr int kMaxG = 8;                             // max query heads per kv head
+
+constexpr int kSmemPages = 0;
+constexpr int kSmemXbuf = kSmemPages + kPages * kPageBytes;
+constexpr int kSmemRed = kSmemXbuf + kXbufFloats * 4;
+constexpr int kSmemBars = kSmemRed + kRedCap * 4;
+constexpr int kSmemMisc = kSmemBars + 2 * kPages * 8;
+constexpr int kSmemBytes = kSmemMisc + 256;
+
+// ---- opcodes ------------------------------------------------------------
+enum Op : int32_t {
+    OP_QKV = 1,     // rows of Wq|Wk|Wv on RMSNorm(x): writes raw q,k,v
+    OP_ATTN = 2,    // one KV split of one kv head: RoPE, KV append, partial softmax, LSE merge
+    OP_OPROJ = 3,   // rows of Wo on the attention output, + residual
+    OP_GATEUP = 4,  // rows of Wg and Wu on RMSNorm(x), silu(g)*u
+    OP_DOWN = 5,    // rows of Wd on h, + residual
+    OP_LMHEAD = 6,  // rows of the tied embedding on RMSNorm(x), logits + block argmax
+};
+constexpr int kStagesPerLayer = 5;
+
+// One instruction = 16 int32 (64 bytes).
+struct Instr {
+    int32_t op, layer;
+    int32_t a0, a1;         // GEMV: first row, row count.  ATTN: kv head, split
+    int32_t mat;            // QKV: 0 q, 1 k, 2 v
+    int32_t wait_ctr;       // counter to wait on (-1: none)
+    int32_t wait_target;    // ... until it reaches this value
+    int32_t sig_ctr, sig_n; // counters [sig_ctr, sig_ctr+sig_n) to bump by 1 when done
+    int32_t stage;          // topological stage (QKV(l)=5l ... LMHEAD=5L)
+    int32_t slot;           // LMHEAD: argmax partial slot
+    int32_t bytes_lo, bytes_hi;  // weight bytes streamed (host bookkeeping)
+    int32_t pad[3];
+};
+static_assert(sizeof(Instr) == 64, "Instr must be 64 bytes");
+
+// Tile geometry of one GEMV operand shape (input length K).
+// A warp owns rows of a tile (row group rg) and a K-slice (ks):
+//   sw = K-slices per row, rw = 8/sw row groups, m rows per warp per tile,
+//   rt = rw*m rows per tile, nx = floats of the input each lane keeps.
+struct Geo {
+    int32_t K, sw, rw, m, rt, nx, kslice, pad;
+};
+
+struct LayerW {
+    const uint16_t *attn_norm, *wq, *wk, *wv, *wo, *mlp_norm, *w_gate, *w_up, *w_down;
+};
+
+// Counter index layout (all uint32 in one device array).
+struct CtrLayout {
+    int32_t qkv_grp;   // + l*Hkv + h : QKV instructions of group h done
+    int32_t merge;     // + l*Hkv + h : attention splits arrived
+    int32_t attn_done; // + l        : kv heads merged
+    int32_t oproj_done, gateup_done, down_done;  // + l
+    int32_t lm_arrive; // LM-head instructions arrived
+    int32_t total;
+};
+
+struct Params {
+    // shape
+    int32_t L, d, Hq, Hkv, hd, F, V, max_seq, max_batch, S, G, ppt;
+    float eps;
+    int32_t n_lm, n_stages;
+    Geo geo_qkv, geo_o, geo_gu, geo_down, geo_lm;
+    CtrLayout cl;
+    // weights (borrowed)
+    const uint16_t *embed, *final_norm;
+    const LayerW *layers;   // device array [L]
+    uint16_t *kc, *vc;      // KV caches
+    // scratch (library-owned)
+    float *x;               // [d] residual stream
+    float *qkv;             // [L][(Hq+2Hkv)*hd] raw projections
+    float *part;            // [L][Hq][S][hd+2] split partials (o, m, l)
+    float *att;             // [L][Hq*hd] merged attention output
+    float *h;               // [L][F] silu(g)*u
+    unsigned long long *lm_part;  // [n_lm] packed (value, ~index)
+    uint32_t *ctr;          // dependency counters
+    uint32_t *exit_ctr;     // CTAs done with the step
+    int32_t *status;        // 0 ok, else error code (sticky until read)
+    int32_t *abort_flag;
+    const float *rope;      // [max_seq][hd/2][2] cos, sin
+    const Instr *instr;     // flat queues
+    const int32_t *q_begin; // [n_sm][n_stages+1] first instruction index with stage >= s
+    // this launch
+    int32_t stage_lo, stage_hi, reset_at_exit;
+    int32_t token;
+    const int32_t *d_token; // if non-null, overrides token
+    int32_t pos;
+    float *out_logits;      // nullable
+    int32_t *out_token;
+    unsigned long long timeout_ns;
+    long long *trace;       // nullable: [n_sm][trace_cap][5]
+    int32_t trace_cap;
+};
+
+// Device status codes written to *status.
+enum DevStatus : int32_t { DS_OK = 0, DS_TIMEOUT = 1, DS_BAD_TOKEN = 2 };
+
+}  // namespace mk

