@@ -59,11 +59,14 @@ _I32 = ctypes.c_int32
 _PI32 = ctypes.POINTER(ctypes.c_int32)
 
 
-def load(path: str = LIB_PATH):
-    """Loads libmk.so (built by decode_megakernel_llama_gb300.build)."""
+def load(path: str | None = None):
+    """Loads libmk.so (built by decode_megakernel_llama_gb300.build). The
+    environment variable MK_LIB selects another build of the same library
+    (e.g. the address-checked one)."""
     global _lib
     if _lib is not None:
         return _lib
+    path = path or os.environ.get("MK_LIB") or LIB_PATH
     if not os.path.exists(path):
         raise ImportError(f"{path} is missing: run decode_megakernel_llama_gb300.build.build() "
                           "(there is no fallback implementation)")
@@ -81,6 +84,7 @@ def load(path: str = LIB_PATH):
     L.mk_read_trace.argtypes = [_VP, ctypes.POINTER(ctypes.c_int64), _I32]
     L.mk_plan_size.argtypes = [_VP, _PI32, _PI32]
     L.mk_plan_inspect.argtypes = [ctypes.POINTER(mk_config), _I32, _PI32, _I32, _PI32, _PI32]
+    L.mk_debug_read.argtypes = [_VP, ctypes.POINTER(ctypes.c_uint64)]
     L.mk_destroy.argtypes = [_VP]
     L.mk_destroy.restype = None
     _lib = L
@@ -193,6 +197,12 @@ class Megakernel:
         n = check(load().mk_read_trace(self.h, buf.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
                                        buf.shape[0]))
         return buf[:n]
+
+    def debug_read(self):
+        """(checked_build, [site, address, bytes, block<<32|thread])."""
+        out = (ctypes.c_uint64 * 4)()
+        rc = check(load().mk_debug_read(self.h, out))
+        return rc == 1, list(out)
 
     def plan_size(self):
         n_sm, n_instr = ctypes.c_int32(), ctypes.c_int32()

@@ -10,6 +10,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libmk.so")
+LIB_CHECKED = os.path.join(BUILD, "libmk_checked.so")
 SOURCES = ["mk_kernel.cu", "mk_host.cpp"]
 DEPS = SOURCES + ["mk_plan.h"]
 
@@ -26,23 +27,29 @@ def flags() -> list[str]:
             "-Xcompiler", "-fPIC", "-Xcompiler", "-O2", f"-I{os.path.join(ROOT, 'include')}"]
 
 
-def _stale() -> bool:
-    if not os.path.exists(LIB):
+def _stale(lib: str) -> bool:
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     deps = [os.path.join(CSRC, s) for s in DEPS] + [os.path.join(ROOT, "include", "mk.h")]
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    if not force and not _stale():
-        return LIB
+def build(force: bool = False, verbose: bool = False, checked: bool = False) -> str:
+    """checked=True builds libmk_checked.so: every device-side access is
+    validated against the registered buffers (slow; for diagnosing faults)."""
+    lib = LIB_CHECKED if checked else LIB
+    if not force and not _stale(lib):
+        return lib
     os.makedirs(BUILD, exist_ok=True)
     nv = nvcc()
     procs, objs = [], []
+    tag = ".chk" if checked else ""
     for s in SOURCES:
-        obj = os.path.join(BUILD, s + ".o")
+        obj = os.path.join(BUILD, s + tag + ".o")
         extra = ["-Xptxas", "-v"] if (verbose and s.endswith(".cu")) else []
+        if checked:
+            extra += ["-DMK_CHECKED"]
         cmd = [nv, *flags(), *extra, "-c", os.path.join(CSRC, s), "-o", obj]
         procs.append((cmd, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)))
         objs.append(obj)
@@ -52,13 +59,14 @@ def build(force: bool = False, verbose: bool = False) -> str:
             print(out.decode(errors="replace"))
         if pr.returncode:
             raise RuntimeError(f"compile failed: {' '.join(cmd)}")
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     subprocess.run([nv, "-shared", "-gencode", "arch=compute_103a,code=sm_103a", "-o", tmp, *objs],
                    check=True)
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
     import sys
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv,
+                checked="--checked" in sys.argv))

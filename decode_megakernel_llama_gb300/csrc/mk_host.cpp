@@ -486,6 +486,9 @@ int mk_create(const mk_config *config, const mk_weights *w, const mk_kv_cache *k
     const size_t o_rope = b.take(sizeof(float) * rope.size());
     const size_t o_instr = b.take(sizeof(Instr) * flat.size());
     const size_t o_qbeg = b.take(sizeof(int32_t) * qbeg.size());
+    const int n_ranges = 5 + 9 * L;
+    const size_t o_ranges = b.take(sizeof(unsigned long long) * 2 * n_ranges);
+    const size_t o_dbg = b.take(sizeof(unsigned long long) * 4);
     e = cudaMalloc(&h->dev_mem, b.off);
     if (e != cudaSuccess) {
         delete h;
@@ -499,7 +502,33 @@ int mk_create(const mk_config *config, const mk_weights *w, const mk_kv_cache *k
                   (const uint16_t *)lw.wv, (const uint16_t *)lw.wo, (const uint16_t *)lw.mlp_norm,
                   (const uint16_t *)lw.w_gate, (const uint16_t *)lw.w_up, (const uint16_t *)lw.w_down};
     }
+    // valid byte ranges for the address self-checks of an MK_CHECKED build
+    std::vector<unsigned long long> ranges;
+    auto add_range = [&](const void *ptr, size_t bytes) {
+        ranges.push_back((unsigned long long)(uintptr_t)ptr);
+        ranges.push_back((unsigned long long)(uintptr_t)ptr + bytes);
+    };
+    const size_t kv_bytes = (size_t)L * c.max_batch * Hkv * c.max_seq * hd * 2;
+    add_range(h->dev_mem, b.off);
+    add_range(kv->k, kv_bytes);
+    add_range(kv->v, kv_bytes);
+    add_range(w->embed, (size_t)V * d * 2);
+    add_range(w->final_norm, (size_t)d * 2);
+    for (int l = 0; l < L; ++l) {
+        const mk_layer_weights &lw = w->layers[l];
+        const int qd = Hq * hd, kvd = Hkv * hd;
+        add_range(lw.attn_norm, (size_t)d * 2);
+        add_range(lw.wq, (size_t)qd * d * 2);
+        add_range(lw.wk, (size_t)kvd * d * 2);
+        add_range(lw.wv, (size_t)kvd * d * 2);
+        add_range(lw.wo, (size_t)d * qd * 2);
+        add_range(lw.mlp_norm, (size_t)d * 2);
+        add_range(lw.w_gate, (size_t)F * d * 2);
+        add_range(lw.w_up, (size_t)F * d * 2);
+        add_range(lw.w_down, (size_t)d * F * 2);
+    }
     bool ok = cudaMemset(h->dev_mem, 0, b.off) == cudaSuccess &&
+              cudaMemcpy(b.at<char>(o_ranges), ranges.data(), sizeof(unsigned long long) * ranges.size(), cudaMemcpyHostToDevice) == cudaSuccess &&
               cudaMemcpy(b.at<char>(o_layers), lws.data(), sizeof(mk::LayerW) * L, cudaMemcpyHostToDevice) == cudaSuccess &&
               cudaMemcpy(b.at<char>(o_rope), rope.data(), sizeof(float) * rope.size(), cudaMemcpyHostToDevice) == cudaSuccess &&
               cudaMemcpy(b.at<char>(o_instr), flat.data(), sizeof(Instr) * flat.size(), cudaMemcpyHostToDevice) == cudaSuccess &&
@@ -546,6 +575,9 @@ int mk_create(const mk_config *config, const mk_weights *w, const mk_kv_cache *k
     p.rope = b.at<float>(o_rope);
     p.instr = b.at<Instr>(o_instr);
     p.q_begin = b.at<int32_t>(o_qbeg);
+    p.n_ranges = n_ranges;
+    p.ranges = b.at<unsigned long long>(o_ranges);
+    p.dbg = b.at<unsigned long long>(o_dbg);
     h->ctr_bytes = o_tin - o_ctr;  // counters, exit, status, abort
     if (getenv("MK_LOG")) {
         size_t mx = 0, mn = (size_t)-1;
@@ -661,6 +693,20 @@ int mk_read_trace(mk_handle *h, int64_t *host_out, int32_t cap) {
             ++n;
         }
     return n;
+}
+
+int mk_debug_read(mk_handle *h, uint64_t *host_out4) {
+    if (!h || !host_out4) return fail(MK_ERR_INVALID_ARG, "bad arguments");
+    cudaError_t e = cudaSetDevice(h->device);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e == cudaSuccess)
+        e = cudaMemcpy(host_out4, h->base.dbg, 4 * sizeof(uint64_t), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "debug read");
+#ifdef MK_CHECKED
+    return 1;
+#else
+    return 0;
+#endif
 }
 
 int mk_plan_size(const mk_handle *h, int32_t *n_sm, int32_t *n_instr) {

@@ -144,6 +144,53 @@ __device__ __forceinline__ float warp_sum(float v) {
 
 __device__ __forceinline__ float ldcg(const float *p) { return __ldcg(p); }
 
+// ---------------------------------------------------------------------------
+// Address self-checks. A build with MK_CHECKED validates every global access
+// against the byte ranges the host registered (weights, caches, scratch,
+// outputs) and every computed shared-memory access against the CTA's
+// allocation; the first violation is recorded in p.dbg and the access is
+// skipped. Without MK_CHECKED the checks compile to `true`.
+// ---------------------------------------------------------------------------
+extern __shared__ __align__(1024) uint8_t mk_smem[];
+
+#ifdef MK_CHECKED
+__device__ __noinline__ void chk_record(const Params &p, int site, uintptr_t a, size_t bytes) {
+    if (p.dbg && atomicCAS(p.dbg, 0ull, (unsigned long long)site) == 0ull) {
+        p.dbg[1] = a;
+        p.dbg[2] = bytes;
+        p.dbg[3] = ((unsigned long long)blockIdx.x << 32) | threadIdx.x;
+        __threadfence();
+    }
+}
+__device__ __noinline__ bool chk_global(const Params &p, const void *ptr, size_t bytes, int site) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(ptr);
+    for (int i = 0; i < p.n_ranges; ++i)
+        if (a >= p.ranges[2 * i] && a + bytes <= p.ranges[2 * i + 1]) return true;
+    if (p.out_logits && a >= (uintptr_t)p.out_logits && a + bytes <= (uintptr_t)(p.out_logits + p.V))
+        return true;
+    if (p.out_token && a >= (uintptr_t)p.out_token && a + bytes <= (uintptr_t)(p.out_token + 1))
+        return true;
+    if (p.d_token && a >= (uintptr_t)p.d_token && a + bytes <= (uintptr_t)(p.d_token + 1))
+        return true;
+    if (p.trace && a >= (uintptr_t)p.trace &&
+        a + bytes <= (uintptr_t)(p.trace + (size_t)gridDim.x * p.trace_cap * 5))
+        return true;
+    chk_record(p, site, a, bytes);
+    return false;
+}
+__device__ __noinline__ bool chk_shared(const Params &p, const void *ptr, size_t bytes, int site) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(ptr), b = reinterpret_cast<uintptr_t>(mk_smem);
+    if (__isShared(ptr) && a >= b && a + bytes <= b + kSmemBytes) return true;
+    chk_record(p, site, a, bytes);
+    return false;
+}
+#define CHK(ptr, bytes, site) chk_global(p, (ptr), (bytes), (site))
+#define CHKS(ptr, bytes, site) chk_shared(p, (ptr), (bytes), (site))
+#else
+#define CHK(ptr, bytes, site) true
+#define CHKS(ptr, bytes, site) true
+#endif
+
 // Orderable key for the argmax: larger value wins, then lower index.
 __device__ __forceinline__ unsigned long long argmax_key(float v, uint32_t idx) {
     uint32_t u = __float_as_uint(v);
@@ -174,6 +221,7 @@ struct Ctx {
 // Bounded spin of one thread on a global counter. Returns false on abort or
 // timeout (after recording the timeout).
 __device__ bool wait_counter(const Params &p, const uint32_t *c, uint32_t target) {
+    if (!CHK(c, 4, 29)) return false;
     if (ld_acquire(c) >= target) return true;
     uint64_t t0 = gtimer();
     for (uint32_t it = 1;; ++it) {
@@ -208,6 +256,13 @@ __device__ bool wait_bar(const Params &p, uint64_t *bar, uint32_t parity) {
 
 __device__ __forceinline__ Instr load_instr(const Params &p, int i) {
     Instr in;
+    if (!CHK(p.instr + i, sizeof(Instr), 1)) {
+        memset(&in, 0, sizeof in);
+        in.wait_ctr = -1;
+        in.op = OP_QKV;
+        in.a1 = 0;
+        return in;
+    }
     const int4 *src = reinterpret_cast<const int4 *>(p.instr + i);
     int4 *dst = reinterpret_cast<int4 *>(&in);
 #pragma unroll
@@ -288,9 +343,13 @@ __device__ void producer(const Params &p, const Ctx &cx, int qb, int qe) {
                 size_t base = ((size_t)(in.layer * p.max_batch) * p.Hkv + in.a0) * p.max_seq * p.hd +
                               (size_t)ts * p.hd;
                 uint32_t bytes = (uint32_t)n * p.hd * 2;
-                mbar_expect_tx(&cx.full[pg], 2 * bytes);
-                bulk_g2s(dst, p.kc + base, bytes, &cx.full[pg], pol);
-                bulk_g2s(dst + kPageBytes / 2, p.vc + base, bytes, &cx.full[pg], pol);
+                const bool ok = CHK(p.kc + base, bytes, 3) && CHK(p.vc + base, bytes, 4) &&
+                                CHKS(dst, kPageBytes / 2 + bytes, 40);
+                mbar_expect_tx(&cx.full[pg], ok ? 2 * bytes : 0);
+                if (ok) {
+                    bulk_g2s(dst, p.kc + base, bytes, &cx.full[pg], pol);
+                    bulk_g2s(dst + kPageBytes / 2, p.vc + base, bytes, &cx.full[pg], pol);
+                }
             } else {
                 const Geo &g = geo_of(p, in.op);
                 const int per = (in.op == OP_GATEUP) ? g.rt / 2 : g.rt;
@@ -300,10 +359,15 @@ __device__ void producer(const Params &p, const Ctx &cx, int qb, int qe) {
                 const uint32_t bytes = (uint32_t)rows * g.K * 2;
                 if (in.op == OP_GATEUP) {
                     const LayerW *lw = p.layers + in.layer;
-                    mbar_expect_tx(&cx.full[pg], 2 * bytes);
-                    bulk_g2s(dst, lw->w_gate + row0 * g.K, bytes, &cx.full[pg], pol);
-                    bulk_g2s(dst + (size_t)per * g.K * 2, lw->w_up + row0 * g.K, bytes, &cx.full[pg],
-                             pol);
+                    const bool ok = CHK(lw->w_gate + row0 * g.K, bytes, 5) &&
+                                    CHK(lw->w_up + row0 * g.K, bytes, 6) &&
+                                    CHKS(dst, (size_t)per * g.K * 2 + bytes, 41);
+                    mbar_expect_tx(&cx.full[pg], ok ? 2 * bytes : 0);
+                    if (ok) {
+                        bulk_g2s(dst, lw->w_gate + row0 * g.K, bytes, &cx.full[pg], pol);
+                        bulk_g2s(dst + (size_t)per * g.K * 2, lw->w_up + row0 * g.K, bytes,
+                                 &cx.full[pg], pol);
+                    }
                 } else {
                     const uint16_t *W;
                     const LayerW *lw = p.layers + in.layer;
@@ -313,8 +377,9 @@ __device__ void producer(const Params &p, const Ctx &cx, int qb, int qe) {
                         case OP_DOWN: W = lw->w_down; break;
                         default: W = p.embed; break;
                     }
-                    mbar_expect_tx(&cx.full[pg], bytes);
-                    bulk_g2s(dst, W + row0 * g.K, bytes, &cx.full[pg], pol);
+                    const bool ok = CHK(W + row0 * g.K, bytes, 7) && CHKS(dst, bytes, 42);
+                    mbar_expect_tx(&cx.full[pg], ok ? bytes : 0);
+                    if (ok) bulk_g2s(dst, W + row0 * g.K, bytes, &cx.full[pg], pol);
                 }
             }
             cx.misc->n_issued = t + 1;
@@ -364,11 +429,13 @@ __device__ void gemv_tiles(const Params &p, const Ctx &cx, const Instr &in, cons
 #pragma unroll
     for (int c = 0; c < NX / 8; ++c) {
         const int idx = sbase + (c * 32 + lane) * 8;
-        float4 u, v;
+        float4 u = make_float4(0.f, 0.f, 0.f, 0.f), v = u;
         if (xglobal) {
-            u = __ldcg(reinterpret_cast<const float4 *>(xsrc + idx));
-            v = __ldcg(reinterpret_cast<const float4 *>(xsrc + idx + 4));
-        } else {
+            if (CHK(xsrc + idx, 32, 8)) {
+                u = __ldcg(reinterpret_cast<const float4 *>(xsrc + idx));
+                v = __ldcg(reinterpret_cast<const float4 *>(xsrc + idx + 4));
+            }
+        } else if (CHKS(xsrc + idx, 32, 43)) {
             u = *reinterpret_cast<const float4 *>(xsrc + idx);
             v = *reinterpret_cast<const float4 *>(xsrc + idx + 4);
         }
@@ -401,8 +468,10 @@ __device__ void gemv_tiles(const Params &p, const Ctx &cx, const Instr &in, cons
                 if (valid) {
                     const uint4 *w = reinterpret_cast<const uint4 *>(page + r * row_bytes) +
                                      (sbase / 8) + lane;
-                    float acc = warp_sum(dot_row<NX>(w, xr));
-                    if (lane == 0) cx.red[out_i * g.sw + ks] = acc;
+                    const bool ok = CHKS(w, 16, 44) && CHKS(w + (NX / 8 - 1) * 32, 16, 45);
+                    float acc = warp_sum(ok ? dot_row<NX>(w, xr) : 0.f);
+                    if (lane == 0 && CHKS(cx.red + out_i * g.sw + ks, 4, 46))
+                        cx.red[out_i * g.sw + ks] = acc;
                 }
             }
         }
@@ -419,14 +488,16 @@ __device__ void stage_input(const Params &p, const Ctx &cx, const float *src,
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     float ss = 0.f;
     for (int i = tid * 4; i < n; i += kConsumerThreads * 4) {
-        float4 v;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
         if (src_bf16) {
-            uint2 b = __ldg(reinterpret_cast<const uint2 *>(src_bf16 + i));
-            v = make_float4(bf_lo(b.x), bf_hi(b.x), bf_lo(b.y), bf_hi(b.y));
-        } else {
+            if (CHK(src_bf16 + i, 8, 9)) {
+                uint2 b = __ldg(reinterpret_cast<const uint2 *>(src_bf16 + i));
+                v = make_float4(bf_lo(b.x), bf_hi(b.x), bf_lo(b.y), bf_hi(b.y));
+            }
+        } else if (CHK(src + i, 16, 10)) {
             v = __ldcg(reinterpret_cast<const float4 *>(src + i));
         }
-        *reinterpret_cast<float4 *>(cx.xbuf + i) = v;
+        if (CHKS(cx.xbuf + i, 16, 47)) *reinterpret_cast<float4 *>(cx.xbuf + i) = v;
         ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
     }
     if (!gain) {
@@ -440,11 +511,13 @@ __device__ void stage_input(const Params &p, const Ctx &cx, const float *src,
 #pragma unroll
     for (int w = 0; w < kConsumerWarps; ++w) tot += cx.misc->red8[w];
     const float rstd = 1.0f / sqrtf(tot / (float)n + p.eps);
-    for (int i = tid; i < n; i += kConsumerThreads) cx.xbuf[i] = cx.xbuf[i] * rstd * bf16f(__ldg(gain + i));
+    for (int i = tid; i < n; i += kConsumerThreads)
+        if (CHK(gain + i, 2, 11)) cx.xbuf[i] = cx.xbuf[i] * rstd * bf16f(__ldg(gain + i));
     consumer_sync();
 }
 
 __device__ __forceinline__ int current_token(const Params &p) {
+    if (p.d_token && !CHK(p.d_token, 4, 33)) return -1;
     return p.d_token ? *(volatile const int32_t *)p.d_token : p.token;
 }
 
@@ -506,7 +579,7 @@ __device__ void do_gemv(const Params &p, const Ctx &cx, const Instr &in, uint32_
             for (int i = tid; i < n; i += kConsumerThreads) {
                 float v = 0.f;
                 for (int s = 0; s < sw; ++s) v += cx.red[i * sw + s];
-                dst[i] = v;
+                if (CHK(dst + i, 4, 12)) dst[i] = v;
             }
             break;
         }
@@ -515,9 +588,14 @@ __device__ void do_gemv(const Params &p, const Ctx &cx, const Instr &in, uint32_
             for (int i = tid; i < n; i += kConsumerThreads) {
                 float v = 0.f;
                 for (int s = 0; s < sw; ++s) v += cx.red[i * sw + s];
-                const float res = (l == 0) ? bf16f(__ldg(p.embed + (size_t)tok * p.d + r0 + i))
-                                           : ldcg(p.x + r0 + i);
-                p.x[r0 + i] = res + v;
+                float res = 0.f;
+                if (l == 0) {
+                    if (CHK(p.embed + (size_t)tok * p.d + r0 + i, 2, 13))
+                        res = bf16f(__ldg(p.embed + (size_t)tok * p.d + r0 + i));
+                } else if (CHK(p.x + r0 + i, 4, 14)) {
+                    res = ldcg(p.x + r0 + i);
+                }
+                if (CHK(p.x + r0 + i, 4, 15)) p.x[r0 + i] = res + v;
             }
             break;
         }
@@ -529,7 +607,7 @@ __device__ void do_gemv(const Params &p, const Ctx &cx, const Instr &in, uint32_
                     gv += cx.red[i * sw + s];
                     uv += cx.red[(n + i) * sw + s];
                 }
-                dst[i] = gv / (1.0f + expf(-gv)) * uv;
+                if (CHK(dst + i, 4, 16)) dst[i] = gv / (1.0f + expf(-gv)) * uv;
             }
             break;
         }
@@ -537,7 +615,7 @@ __device__ void do_gemv(const Params &p, const Ctx &cx, const Instr &in, uint32_
             for (int i = tid; i < n; i += kConsumerThreads) {
                 float v = 0.f;
                 for (int s = 0; s < sw; ++s) v += cx.red[i * sw + s];
-                p.x[r0 + i] = ldcg(p.x + r0 + i) + v;
+                if (CHK(p.x + r0 + i, 4, 17)) p.x[r0 + i] = ldcg(p.x + r0 + i) + v;
             }
             break;
         }
@@ -546,7 +624,7 @@ __device__ void do_gemv(const Params &p, const Ctx &cx, const Instr &in, uint32_
             for (int i = tid; i < n; i += kConsumerThreads) {
                 float v = 0.f;
                 for (int s = 0; s < sw; ++s) v += cx.red[i * sw + s];
-                if (p.out_logits) p.out_logits[r0 + i] = v;
+                if (p.out_logits && CHK(p.out_logits + r0 + i, 4, 18)) p.out_logits[r0 + i] = v;
                 const unsigned long long k = argmax_key(v, (uint32_t)(r0 + i));
                 best = k > best ? k : best;
             }
@@ -561,16 +639,18 @@ __device__ void do_gemv(const Params &p, const Ctx &cx, const Instr &in, uint32_
             if (tid == 0) {
                 unsigned long long b = 0ull;
                 for (int w = 0; w < kConsumerWarps; ++w) b = cx.misc->best8[w] > b ? cx.misc->best8[w] : b;
-                p.lm_part[in.slot] = b;
+                if (CHK(p.lm_part + in.slot, 8, 19)) p.lm_part[in.slot] = b;
                 __threadfence();
-                const uint32_t old = atom_acq_rel_add(p.ctr + p.cl.lm_arrive, 1u);
+                const uint32_t old = CHK(p.ctr + p.cl.lm_arrive, 4, 31)
+                                         ? atom_acq_rel_add(p.ctr + p.cl.lm_arrive, 1u) : 0u;
                 if (old == (uint32_t)p.n_lm - 1u) {
                     unsigned long long g2 = 0ull;
                     for (int s = 0; s < p.n_lm; ++s) {
-                        const unsigned long long v = __ldcg(p.lm_part + s);
+                        const unsigned long long v = CHK(p.lm_part + s, 8, 20) ? __ldcg(p.lm_part + s) : 0ull;
                         g2 = v > g2 ? v : g2;
                     }
-                    *p.out_token = (int32_t)(0xFFFFFFFFu - (uint32_t)(g2 & 0xFFFFFFFFull));
+                    if (CHK(p.out_token, 4, 21))
+                        *p.out_token = (int32_t)(0xFFFFFFFFu - (uint32_t)(g2 & 0xFFFFFFFFull));
                 }
             }
             break;
@@ -716,6 +796,9 @@ __device__ void do_attn_hd(const Params &p, const Ctx &cx, const Instr &in, uint
         for (int idx = tid; idx < G * (HD / 2); idx += kConsumerThreads) {
             const int g = idx / (HD / 2), i = idx % (HD / 2);
             const float *qh = qkv + (size_t)(kvh * G + g) * HD;
+            if (!(CHK(qh + i, 4, 22) && CHK(qh + i + HD / 2, 4, 22) && CHK(rope + 2 * i, 8, 28) &&
+                  CHKS(qs + g * HD + i + HD / 2, 4, 48)))
+                continue;
             const float a = ldcg(qh + i), b = ldcg(qh + i + HD / 2);
             const float c = rope[2 * i], s = rope[2 * i + 1];
             qs[g * HD + i] = (a * c - b * s) * qscale;
@@ -727,6 +810,12 @@ __device__ void do_attn_hd(const Params &p, const Ctx &cx, const Instr &in, uint
             const size_t cache_off = (((size_t)l * p.max_batch) * p.Hkv + kvh) * p.max_seq * HD +
                                      (size_t)p.pos * HD;
             for (int i = tid; i < HD / 2; i += kConsumerThreads) {
+                if (!(CHK(kh + i, 4, 23) && CHK(kh + i + HD / 2, 4, 23) && CHK(vh + i, 4, 23) &&
+                      CHK(vh + i + HD / 2, 4, 23) && CHK(p.kc + cache_off + i, 2, 24) &&
+                      CHK(p.kc + cache_off + i + HD / 2, 2, 24) && CHK(p.vc + cache_off + i, 2, 24) &&
+                      CHK(p.vc + cache_off + i + HD / 2, 2, 24) && CHK(rope + 2 * i, 8, 28) &&
+                      CHKS(vnew + i + HD / 2, 2, 49)))
+                    continue;
                 const float a = ldcg(kh + i), b = ldcg(kh + i + HD / 2);
                 const float c = rope[2 * i], s = rope[2 * i + 1];
                 const uint16_t k0 = f2bf(a * c - b * s), k1 = f2bf(b * c + a * s);
@@ -762,7 +851,8 @@ __device__ void do_attn_hd(const Params &p, const Ctx &cx, const Instr &in, uint
             if (n > p.ppt) n = p.ppt;
             int np = n - warp * PPW;
             np = np > PPW ? PPW : np;
-            if (np > 0) {
+            if (np > 0 && CHKS(cx.pages + (size_t)pg * kPageBytes + (size_t)(warp * PPW + np) * HD * 2 - 2, 2, 50) &&
+                CHKS(pbuf + PPW * kMaxG - 1, 4, 51)) {
                 const uint16_t *Kp = reinterpret_cast<const uint16_t *>(cx.pages + (size_t)pg * kPageBytes) +
                                      (size_t)warp * PPW * HD;
                 const uint16_t *Vp = reinterpret_cast<const uint16_t *>(cx.pages + (size_t)pg * kPageBytes +
@@ -779,6 +869,7 @@ __device__ void do_attn_hd(const Params &p, const Ctx &cx, const Instr &in, uint
         if (r.has_new && warp == kConsumerWarps - 1) attn_chunk<HD>(st, knew, vnew, 1, qs, G, pbuf);
         // warp states -> shared
         float *my = wst + (size_t)warp * G * (HD + 2);
+        if (!CHKS(my + G * (HD + 2) - 1, 4, 52)) my = wst;
         for (int g = 0; g < G; ++g) {
 #pragma unroll
             for (int e = 0; e < DPL; ++e) my[g * (HD + 2) + lane * DPL + e] = st.o[g][e];
@@ -804,14 +895,16 @@ __device__ void do_attn_hd(const Params &p, const Ctx &cx, const Instr &in, uint
                     if (mw != -INFINITY) acc += wst[(w * G + g) * (HD + 2) + src] * exp2f(mw - M);
                 }
             }
-            dst[((size_t)g * p.S + split) * (HD + 2) + e] = acc;
+            if (CHK(dst + ((size_t)g * p.S + split) * (HD + 2) + e, 4, 25))
+                dst[((size_t)g * p.S + split) * (HD + 2) + e] = acc;
         }
     }
     consumer_sync();
     // arrival; the last split of this kv head merges all active splits
     if (tid == 0) {
         __threadfence();
-        const uint32_t old = atom_acq_rel_add(p.ctr + p.cl.merge + l * p.Hkv + kvh, 1u);
+        const uint32_t old = CHK(p.ctr + p.cl.merge + l * p.Hkv + kvh, 4, 31)
+                                 ? atom_acq_rel_add(p.ctr + p.cl.merge + l * p.Hkv + kvh, 1u) : 0u;
         cx.misc->flag = (old == (uint32_t)p.S - 1u);
     }
     consumer_sync();
@@ -822,6 +915,8 @@ __device__ void do_attn_hd(const Params &p, const Ctx &cx, const Instr &in, uint
         for (int idx = tid; idx < G * HD; idx += kConsumerThreads) {
             const int g = idx / HD, e = idx % HD;
             const float *sg = src + (size_t)g * p.S * (HD + 2);
+            if (!(CHK(sg, 4, 26) && CHK(sg + (size_t)seff * (HD + 2) - 1, 4, 26) && CHK(out + idx, 4, 27)))
+                continue;
             float M = -INFINITY;
             for (int s = 0; s < seff; ++s) M = fmaxf(M, ldcg(sg + (size_t)s * (HD + 2) + HD));
             float num = 0.f, den = 0.f;
@@ -837,7 +932,7 @@ __device__ void do_attn_hd(const Params &p, const Ctx &cx, const Instr &in, uint
         consumer_sync();
         if (tid == 0) {
             __threadfence();
-            red_release_add(p.ctr + p.cl.attn_done + l, 1u);
+            if (CHK(p.ctr + p.cl.attn_done + l, 4, 30)) red_release_add(p.ctr + p.cl.attn_done + l, 1u);
         }
     }
 }
@@ -878,9 +973,10 @@ __device__ void consumer(const Params &p, const Ctx &cx, int qb, int qe) {
         if (tid == 0) {
             if (in.sig_n > 0) {
                 __threadfence();
-                for (int c = 0; c < in.sig_n; ++c) red_release_add(p.ctr + in.sig_ctr + c, 1u);
+                for (int c = 0; c < in.sig_n; ++c)
+                    if (CHK(p.ctr + in.sig_ctr + c, 4, 30)) red_release_add(p.ctr + in.sig_ctr + c, 1u);
             }
-            if (trace && (i - qb) < p.trace_cap) {
+            if (trace && (i - qb) < p.trace_cap && CHK(trace + (size_t)(i - qb) * 5, 40, 34)) {
                 long long *rec = trace + (size_t)(i - qb) * 5;
                 rec[0] = blockIdx.x;
                 rec[1] = in.op;
@@ -893,8 +989,11 @@ __device__ void consumer(const Params &p, const Ctx &cx, int qb, int qe) {
     if (bad && tid == 0) cx.misc->aborted = 1;
 }
 
-__global__ void __launch_bounds__(kThreads, 1) mk_megakernel(const __grid_constant__ Params p) {
-    extern __shared__ __align__(1024) uint8_t smem[];
+__global__ void __launch_bounds__(kThreads, 1) mk_megakernel(const Params prm) {
+    uint8_t *smem = mk_smem;
+    // Launch parameters are copied to shared memory once; every device
+    // function reads them from there (no generic pointer into param space).
+    Params *sp = reinterpret_cast<Params *>(smem + kSmemParams);
     Ctx cx;
     cx.pages = smem + kSmemPages;
     cx.xbuf = reinterpret_cast<float *>(smem + kSmemXbuf);
@@ -904,6 +1003,7 @@ __global__ void __launch_bounds__(kThreads, 1) mk_megakernel(const __grid_consta
     cx.misc = reinterpret_cast<Misc *>(smem + kSmemMisc);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (tid == 0) {
+        *sp = prm;
         for (int i = 0; i < kPages; ++i) {
             mbar_init(&cx.full[i], 1);
             mbar_init(&cx.empty[i], kConsumerWarps);
@@ -915,9 +1015,12 @@ __global__ void __launch_bounds__(kThreads, 1) mk_megakernel(const __grid_consta
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
     __syncthreads();
+    const Params &p = *sp;
     const int *qrow = p.q_begin + (size_t)blockIdx.x * (p.n_stages + 1);
-    const int qb = __ldg(qrow + p.stage_lo), qe = __ldg(qrow + p.stage_hi);
-    bool run = *(volatile int32_t *)p.status == DS_OK;
+    bool run = CHK(qrow + p.stage_lo, 4, 2) && CHK(qrow + p.stage_hi, 4, 2) &&
+               CHK(p.status, 4, 32) && CHK(p.abort_flag, 4, 32) && CHK(p.exit_ctr, 4, 32);
+    const int qb = run ? __ldg(qrow + p.stage_lo) : 0, qe = run ? __ldg(qrow + p.stage_hi) : 0;
+    run = run && *(volatile int32_t *)p.status == DS_OK;
     if (run) {
         const int tok = current_token(p);
         if (tok < 0 || tok >= p.V) {
@@ -949,7 +1052,8 @@ __global__ void __launch_bounds__(kThreads, 1) mk_megakernel(const __grid_consta
         }
     }
     // End of step: the last CTA out resets the counters for the next step.
-    if (p.reset_at_exit && tid == 0) {
+    if (p.reset_at_exit && tid == 0 && CHK(p.exit_ctr, 4, 32) &&
+        CHK(p.ctr + p.cl.total - 1, 4, 32)) {
         __threadfence();
         const uint32_t old = atomicAdd(p.exit_ctr, 1u);
         if (old == gridDim.x - 1) {

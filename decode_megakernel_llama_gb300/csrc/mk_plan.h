@@ -28,7 +28,8 @@ constexpr int kSmemXbuf = kSmemPages + kPages * kPageBytes;
 constexpr int kSmemRed = kSmemXbuf + kXbufFloats * 4;
 constexpr int kSmemBars = kSmemRed + kRedCap * 4;
 constexpr int kSmemMisc = kSmemBars + 2 * kPages * 8;
-constexpr int kSmemBytes = kSmemMisc + 256;
+constexpr int kSmemParams = kSmemMisc + 256;      // shared copy of the launch parameters
+constexpr int kSmemBytes = kSmemParams + 1024;
 
 // ---- opcodes ------------------------------------------------------------
 enum Op : int32_t {
@@ -42,7 +43,7 @@ enum Op : int32_t {
 constexpr int kStagesPerLayer = 5;
 
 // One instruction = 16 int32 (64 bytes).
-struct Instr {
+struct alignas(16) Instr {
     int32_t op, layer;
     int32_t a0, a1;         // GEMV: first row, row count.  ATTN: kv head, split
     int32_t mat;            // QKV: 0 q, 1 k, 2 v
@@ -113,7 +114,12 @@ struct Params {
     unsigned long long timeout_ns;
     long long *trace;       // nullable: [n_sm][trace_cap][5]
     int32_t trace_cap;
+    // address self-checks (only read by a build with MK_CHECKED defined)
+    int32_t n_ranges;
+    const unsigned long long *ranges;  // [n_ranges][2] valid [begin, end) byte ranges
+    unsigned long long *dbg;           // first violation: site, address, bytes, block/thread
 };
+static_assert(sizeof(Params) <= 1024, "Params must fit its shared-memory slot");
 
 // Device status codes written to *status.
 enum DevStatus : int32_t { DS_OK = 0, DS_TIMEOUT = 1, DS_BAD_TOKEN = 2 };

@@ -140,10 +140,18 @@ int mk_set_wait_timeout(mk_handle *h, uint64_t timeout_ns);
  * mk_read_trace copies out (see mk_read_trace). */
 int mk_set_trace(mk_handle *h, int32_t enable);
 
-/* Copies the trace of the last traced step to host_out (int64 quadruples
- * {sm, instruction op, wait-start ns, start ns, end ns} = 5 int64 each) and
- * returns the number of records (or a negative status). cap = records. */
+/* Copies the trace of the last traced step to host_out: records of 5 int64
+ * {sm, instruction op, wait-start ns, start ns, end ns}, SM after SM in queue
+ * order; returns the number of records (or a negative status). cap = records. */
 int mk_read_trace(mk_handle *h, int64_t *host_out, int32_t cap);
+
+/* Diagnostics of a library built with MK_CHECKED (every device-side global
+ * and shared-memory access is validated against the registered buffers; the
+ * first violation is recorded and the access skipped). Copies the record
+ * {site, address, bytes, (block << 32) | thread} to host_out4 (site 0 = none)
+ * after synchronising the device. Returns 1 for a checked build, 0 for a
+ * normal build (whose record is always zero), or a negative status. */
+int mk_debug_read(mk_handle *h, uint64_t *host_out4);
 
 /* Number of streaming multiprocessors (persistent CTAs) the plan uses and
  * the number of instructions in the plan. */
