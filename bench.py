@@ -40,6 +40,10 @@ def parse():
                     help="skip the unfused-chain timings")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="budget of the oracle CPU-baseline sample")
+    ap.add_argument("--profile", action="store_true",
+                    help="only W warm-up and K decode steps (for ncu captures); prints one line")
+    ap.add_argument("--trace", default=None,
+                    help="also record one traced step and write its summary (JSON) here")
     return ap.parse_args()
 
 
@@ -236,6 +240,14 @@ def run_mk(args, ws, rank, local):
         for i in range(P):
             step_fn(int(prompt[i]), i)
 
+    if args.profile:
+        for s in range(W + K):
+            mk.step(int(prompt[s % P]), s, tok, None, stream)
+        torch.cuda.synchronize()
+        print(json.dumps({"profile": True, "status": mk.status(), "launches": W + K}), flush=True)
+        mk.close()
+        return
+
     # prompt through the decode step (its last W steps are the warm-up)
     run_prompt(lambda t, i: mk.step(t, i, tok, None, stream))
     torch.cuda.synchronize()
@@ -338,6 +350,19 @@ def run_mk(args, ws, rank, local):
                 "unfused_chain_graph_us_per_token": graph_us,
                 "unfused_launches_per_token": 5 * shape.n_layers + 1,
                 "megakernel_speedup_vs_unfused": unfused_us / us_per_tok_launch}
+
+    # ---- optional per-instruction trace of one step
+    if args.trace:
+        from decode_megakernel_llama_gb300 import trace as mktrace
+        mk.set_trace(True)
+        mk.step_dev(tok, P, tok, None, stream)
+        torch.cuda.synchronize()
+        rec = mk.read_trace()
+        mk.set_trace(False)
+        summ = mktrace.summarize(rec)
+        with open(args.trace, "w") as f:
+            json.dump(summ, f, indent=1)
+        mktrace.to_chrome(rec, os.path.splitext(args.trace)[0] + ".chrome.json")
 
     # ---- roofline of the megakernel (the only kernel)
     mean_bytes = sum(algorithmic_bytes(shape, P + s) for s in range(K)) / K

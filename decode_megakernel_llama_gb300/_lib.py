@@ -131,6 +131,16 @@ def _stream_ptr(stream) -> int:
     return int(stream.cuda_stream)
 
 
+def _weights_struct(shape, weights: dict):
+    layers = (mk_layer_weights * shape.n_layers)()
+    for i, lw in enumerate(weights["layers"]):
+        for k in ("attn_norm", "wq", "wk", "wv", "wo", "mlp_norm", "w_gate", "w_up", "w_down"):
+            setattr(layers[i], k, lw[k].data_ptr())
+    w = mk_weights(weights["embed"].data_ptr(), weights["final_norm"].data_ptr(),
+                   ctypes.cast(layers, ctypes.POINTER(mk_layer_weights)))
+    return w, layers
+
+
 class Megakernel:
     """One model bound to the decode megakernel (owns an mk_handle).
 
@@ -145,13 +155,8 @@ class Megakernel:
         self.max_batch = int(k_cache.shape[1])
         self._keep = (weights, k_cache, v_cache)
         self.cfg = make_config(shape, self.max_seq, self.max_batch, attn_splits)
-        layers = (mk_layer_weights * shape.n_layers)()
-        for i, lw in enumerate(weights["layers"]):
-            for k in ("attn_norm", "wq", "wk", "wv", "wo", "mlp_norm", "w_gate", "w_up", "w_down"):
-                setattr(layers[i], k, lw[k].data_ptr())
+        w, layers = _weights_struct(shape, weights)
         self._layers = layers
-        w = mk_weights(weights["embed"].data_ptr(), weights["final_norm"].data_ptr(),
-                       ctypes.cast(layers, ctypes.POINTER(mk_layer_weights)))
         kv = mk_kv_cache(k_cache.data_ptr(), v_cache.data_ptr())
         h = _VP()
         check(L.mk_create(ctypes.byref(self.cfg), ctypes.byref(w), ctypes.byref(kv), ctypes.byref(h)))

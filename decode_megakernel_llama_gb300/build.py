@@ -12,7 +12,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libmk.so")
 LIB_CHECKED = os.path.join(BUILD, "libmk_checked.so")
 SOURCES = ["mk_kernel.cu", "mk_host.cpp"]
-DEPS = SOURCES + ["mk_plan.h"]
+DEPS = SOURCES + ["mk_plan.h", "mk_internal.h"]
 
 
 def nvcc() -> str:

@@ -285,48 +285,275 @@ int build_plan(const mk_config *c, int n_sm, Plan &P) {
 }
 
 // ---------------------------------------------------------------------------
-// Device-side handle
+// Device image of a plan: where every buffer lives in one scratch region and
+// the host arrays uploaded into it. Shared by mk_create (cudaMalloc'd region)
+// and mk_decode_step_noalloc (a static device array).
 // ---------------------------------------------------------------------------
 struct DevBump {
-    char *base = nullptr;
     size_t off = 0;
     size_t take(size_t bytes) {
         size_t o = off;
         off += (bytes + 255) & ~size_t(255);
         return o;
     }
-    template <class T>
-    T *at(size_t o) const {
-        return reinterpret_cast<T *>(base + o);
-    }
 };
 
 }  // namespace
 
+#include "mk_internal.h"
+
+namespace mkint {
+
+struct ImageImpl {
+    Plan plan;
+};
+
+int check_inputs(const mk_config *config, const mk_weights *w, const mk_kv_cache *kv) {
+    int rc = check_config(config);
+    if (rc) return rc;
+    if (!w || !w->embed || !w->final_norm || !w->layers || !kv || !kv->k || !kv->v)
+        return fail(MK_ERR_INVALID_ARG, "a weight or cache pointer is NULL");
+    auto al = [](const void *q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; };
+    if (!al(w->embed) || !al(w->final_norm) || !al(kv->k) || !al(kv->v))
+        return fail(MK_ERR_INVALID_ARG, "weights and caches must be 16-byte aligned");
+    for (int l = 0; l < config->n_layers; ++l) {
+        const mk_layer_weights &lw = w->layers[l];
+        const void *ps[9] = {lw.attn_norm, lw.wq, lw.wk, lw.wv, lw.wo,
+                             lw.mlp_norm, lw.w_gate, lw.w_up, lw.w_down};
+        for (const void *q : ps) {
+            if (!q) return fail(MK_ERR_INVALID_ARG, "a layer weight pointer is NULL");
+            if (!al(q)) return fail(MK_ERR_INVALID_ARG, "layer weights must be 16-byte aligned");
+        }
+    }
+    return MK_OK;
+}
+
+int check_device(int *dev, int *n_sm) {
+    cudaError_t e = cudaGetDevice(dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    int major = 0, minor = 0, coop = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, *dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, *dev);
+    cudaDeviceGetAttribute(n_sm, cudaDevAttrMultiProcessorCount, *dev);
+    cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, *dev);
+    if (!(major == 10 && minor == 3))
+        return fail(MK_ERR_UNSUPPORTED, "built for sm_103 (GB300); this device is sm_" +
+                                            std::to_string(major) + std::to_string(minor));
+    if (!coop) return fail(MK_ERR_UNSUPPORTED, "device has no cooperative launch");
+    e = mk_kernel_configure();
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+    int bps = 0;
+    e = mk_kernel_occupancy(&bps);
+    if (e != cudaSuccess) return cuda_fail(e, "occupancy query");
+    if (bps < 1) return fail(MK_ERR_LAUNCH, "megakernel CTA does not fit on an SM");
+    return MK_OK;
+}
+
+int make_image(const mk_config *config, const mk_weights *w, int n_sm, Image &im) {
+    im = Image();
+    im.impl = std::make_shared<ImageImpl>();
+    Plan &P = im.impl->plan;
+    int rc = build_plan(config, n_sm, P);
+    if (rc) return rc;
+    const mk_config &c = *config;
+    const int L = c.n_layers, d = c.d_model, Hq = c.n_heads, Hkv = c.n_kv_heads, hd = c.head_dim,
+              F = c.ffn_dim, V = c.vocab;
+    im.n_sm = P.n_sm;
+    im.n_stages = P.n_stages;
+    im.n_instr = P.n_instr();
+    // flat queues and stage index
+    im.flat.reserve(im.n_instr);
+    im.qbeg.assign((size_t)P.n_sm * (P.n_stages + 1), 0);
+    im.qlen.resize(P.n_sm);
+    for (int s = 0; s < P.n_sm; ++s) {
+        const int base = (int)im.flat.size();
+        im.qlen[s] = (int)P.q[s].size();
+        int k = 0;
+        for (int st = 0; st <= P.n_stages; ++st) {
+            while (k < (int)P.q[s].size() && P.q[s][k].stage < st) ++k;
+            im.qbeg[(size_t)s * (P.n_stages + 1) + st] = base + k;
+        }
+        im.flat.insert(im.flat.end(), P.q[s].begin(), P.q[s].end());
+    }
+    // RoPE table: angle pos * theta^(-2i/hd), computed in double
+    im.rope.assign((size_t)c.max_seq * hd, 0.f);
+    for (int pos = 0; pos < c.max_seq; ++pos)
+        for (int i = 0; i < hd / 2; ++i) {
+            const double inv_freq = std::pow((double)c.rope_theta, -2.0 * i / (double)hd);
+            const double a = (double)pos * inv_freq;
+            im.rope[((size_t)pos * (hd / 2) + i) * 2] = (float)std::cos(a);
+            im.rope[((size_t)pos * (hd / 2) + i) * 2 + 1] = (float)std::sin(a);
+        }
+    im.lws.resize(L);
+    for (int l = 0; l < L; ++l) {
+        const mk_layer_weights &lw = w->layers[l];
+        im.lws[l] = {(const uint16_t *)lw.attn_norm, (const uint16_t *)lw.wq, (const uint16_t *)lw.wk,
+                     (const uint16_t *)lw.wv, (const uint16_t *)lw.wo, (const uint16_t *)lw.mlp_norm,
+                     (const uint16_t *)lw.w_gate, (const uint16_t *)lw.w_up, (const uint16_t *)lw.w_down};
+    }
+    // layout of the scratch region; [o_ctr, o_zero_end) must be zero before a step
+    DevBump b;
+    im.o_ctr = b.take(sizeof(uint32_t) * P.cl.total);
+    im.o_exit = b.take(sizeof(uint32_t));
+    im.o_status = b.take(sizeof(int32_t));
+    im.o_abort = b.take(sizeof(int32_t));
+    im.o_dbg = b.take(sizeof(unsigned long long) * 4);
+    im.o_zero_end = b.off;
+    im.o_layers = b.take(sizeof(mk::LayerW) * L);
+    im.o_x = b.take(sizeof(float) * d);
+    im.o_qkv = b.take(sizeof(float) * (size_t)L * (Hq + 2 * Hkv) * hd);
+    im.o_part = b.take(sizeof(float) * (size_t)L * Hq * P.S * (hd + 2));
+    im.o_att = b.take(sizeof(float) * (size_t)L * Hq * hd);
+    im.o_h = b.take(sizeof(float) * (size_t)L * F);
+    im.o_lm = b.take(sizeof(unsigned long long) * P.n_lm);
+    im.o_tin = b.take(sizeof(int32_t));
+    im.o_tout = b.take(sizeof(int32_t));
+    im.o_logits = b.take(sizeof(float) * V);
+    im.o_rope = b.take(sizeof(float) * im.rope.size());
+    im.o_instr = b.take(sizeof(Instr) * im.flat.size());
+    im.o_qbeg = b.take(sizeof(int32_t) * im.qbeg.size());
+    im.n_ranges = 5 + 9 * L;
+    im.o_ranges = b.take(sizeof(unsigned long long) * 2 * im.n_ranges);
+    im.total = b.off;
+    return MK_OK;
+}
+
+void fill_params(const Image &im, const mk_config *config, const mk_weights *w,
+                 const mk_kv_cache *kv, char *base, mk::Params &p) {
+    const Plan &P = im.impl->plan;
+    const mk_config &c = *config;
+    p = mk::Params();
+    p.L = c.n_layers; p.d = c.d_model; p.Hq = c.n_heads; p.Hkv = c.n_kv_heads; p.hd = c.head_dim;
+    p.F = c.ffn_dim; p.V = c.vocab; p.max_seq = c.max_seq; p.max_batch = c.max_batch;
+    p.S = P.S; p.G = c.n_heads / c.n_kv_heads; p.ppt = P.ppt; p.eps = c.rms_eps;
+    p.n_lm = P.n_lm; p.n_stages = P.n_stages;
+    p.geo_qkv = P.geo_qkv; p.geo_o = P.geo_o; p.geo_gu = P.geo_gu; p.geo_down = P.geo_down;
+    p.geo_lm = P.geo_lm;
+    p.cl = P.cl;
+    p.embed = (const uint16_t *)w->embed;
+    p.final_norm = (const uint16_t *)w->final_norm;
+    p.layers = reinterpret_cast<const mk::LayerW *>(base + im.o_layers);
+    p.kc = (uint16_t *)kv->k;
+    p.vc = (uint16_t *)kv->v;
+    p.x = reinterpret_cast<float *>(base + im.o_x);
+    p.qkv = reinterpret_cast<float *>(base + im.o_qkv);
+    p.part = reinterpret_cast<float *>(base + im.o_part);
+    p.att = reinterpret_cast<float *>(base + im.o_att);
+    p.h = reinterpret_cast<float *>(base + im.o_h);
+    p.lm_part = reinterpret_cast<unsigned long long *>(base + im.o_lm);
+    p.ctr = reinterpret_cast<uint32_t *>(base + im.o_ctr);
+    p.exit_ctr = reinterpret_cast<uint32_t *>(base + im.o_exit);
+    p.status = reinterpret_cast<int32_t *>(base + im.o_status);
+    p.abort_flag = reinterpret_cast<int32_t *>(base + im.o_abort);
+    p.rope = reinterpret_cast<const float *>(base + im.o_rope);
+    p.instr = reinterpret_cast<const Instr *>(base + im.o_instr);
+    p.q_begin = reinterpret_cast<const int32_t *>(base + im.o_qbeg);
+    p.n_ranges = im.n_ranges;
+    p.ranges = reinterpret_cast<const unsigned long long *>(base + im.o_ranges);
+    p.dbg = reinterpret_cast<unsigned long long *>(base + im.o_dbg);
+    p.timeout_ns = 2000000000ull;
+}
+
+int upload_image(const Image &im, const mk_config *config, const mk_weights *w,
+                 const mk_kv_cache *kv, char *base, cudaStream_t s) {
+    const mk_config &c = *config;
+    const int L = c.n_layers, d = c.d_model, Hq = c.n_heads, Hkv = c.n_kv_heads, hd = c.head_dim,
+              F = c.ffn_dim, V = c.vocab;
+    // valid byte ranges for the address self-checks of an MK_CHECKED build
+    std::vector<unsigned long long> ranges;
+    auto add_range = [&](const void *ptr, size_t bytes) {
+        ranges.push_back((unsigned long long)(uintptr_t)ptr);
+        ranges.push_back((unsigned long long)(uintptr_t)ptr + bytes);
+    };
+    const size_t kv_bytes = (size_t)L * c.max_batch * Hkv * c.max_seq * hd * 2;
+    add_range(base, im.total);
+    add_range(kv->k, kv_bytes);
+    add_range(kv->v, kv_bytes);
+    add_range(w->embed, (size_t)V * d * 2);
+    add_range(w->final_norm, (size_t)d * 2);
+    const int qd = Hq * hd, kvd = Hkv * hd;
+    for (int l = 0; l < L; ++l) {
+        const mk_layer_weights &lw = w->layers[l];
+        add_range(lw.attn_norm, (size_t)d * 2);
+        add_range(lw.wq, (size_t)qd * d * 2);
+        add_range(lw.wk, (size_t)kvd * d * 2);
+        add_range(lw.wv, (size_t)kvd * d * 2);
+        add_range(lw.wo, (size_t)d * qd * 2);
+        add_range(lw.mlp_norm, (size_t)d * 2);
+        add_range(lw.w_gate, (size_t)F * d * 2);
+        add_range(lw.w_up, (size_t)F * d * 2);
+        add_range(lw.w_down, (size_t)d * F * 2);
+    }
+    struct Up {
+        size_t off;
+        const void *src;
+        size_t bytes;
+    } ups[] = {
+        {im.o_ranges, ranges.data(), sizeof(unsigned long long) * ranges.size()},
+        {im.o_layers, im.lws.data(), sizeof(mk::LayerW) * im.lws.size()},
+        {im.o_rope, im.rope.data(), sizeof(float) * im.rope.size()},
+        {im.o_instr, im.flat.data(), sizeof(Instr) * im.flat.size()},
+        {im.o_qbeg, im.qbeg.data(), sizeof(int32_t) * im.qbeg.size()},
+    };
+    cudaError_t e = cudaMemsetAsync(base, 0, im.total, s);
+    for (const Up &u : ups)
+        if (e == cudaSuccess) e = cudaMemcpyAsync(base + u.off, u.src, u.bytes, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "uploading the plan");
+    return MK_OK;
+}
+
+int launch_step(const mk::Params &base, int n_sm, int n_stages, int32_t token,
+                const int32_t *d_token, int32_t position, float *out_logits, int32_t *out_token,
+                cudaStream_t stream, bool unfused) {
+    mk::Params p = base;
+    p.token = token;
+    p.d_token = d_token;
+    p.pos = position;
+    p.out_logits = out_logits;
+    p.out_token = out_token;
+    cudaError_t e;
+    if (!unfused) {
+        p.stage_lo = 0;
+        p.stage_hi = n_stages;
+        p.reset_at_exit = 1;
+        e = mk_kernel_launch(&p, n_sm, 1, stream);
+        if (e == cudaErrorCooperativeLaunchTooLarge)
+            return fail(MK_ERR_LAUNCH, "persistent grid cannot be co-resident on this device");
+        if (e != cudaSuccess) return cuda_fail(e, "megakernel launch");
+        return MK_OK;
+    }
+    for (int s = 0; s < n_stages; ++s) {
+        p.stage_lo = s;
+        p.stage_hi = s + 1;
+        p.reset_at_exit = (s == n_stages - 1);
+        e = mk_kernel_launch(&p, n_sm, 0, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "stage launch");
+    }
+    return MK_OK;
+}
+
+int set_error(int code, const char *msg) { return fail(code, msg); }
+
+}  // namespace mkint
+
 struct mk_handle {
     mk_config cfg;
-    Plan plan;
+    mkint::Image im;
     int device = 0;
     mk::Params base{};     // everything but the per-step fields
     void *dev_mem = nullptr;
-    mk::LayerW *d_layers = nullptr;
     int32_t *d_tok_in = nullptr;   // host path: token staged here
     int32_t *d_tok_out = nullptr;  // host path: greedy token
     float *d_logits = nullptr;     // host path: logits
-    int32_t *d_status = nullptr;
-    uint32_t *d_ctr = nullptr, *d_exit = nullptr;
-    int32_t *d_abort = nullptr;
-    size_t ctr_bytes = 0;
+    size_t zero_bytes = 0;         // counters .. debug record
     unsigned long long timeout_ns = 2000000000ull;
     long long *d_trace = nullptr;
     int trace_cap = 0;
     bool trace_on = false;
-    std::vector<int> qlen;
 };
 
 namespace {
-
-bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int launch(mk_handle *h, int32_t token, const int32_t *d_token, int32_t position, float *out_logits,
            int32_t *out_token, cudaStream_t stream, bool unfused) {
@@ -336,35 +563,14 @@ int launch(mk_handle *h, int32_t token, const int32_t *d_token, int32_t position
         return fail(MK_ERR_INVALID_ARG, "position outside [0, max_seq)");
     if (!d_token && (token < 0 || token >= h->cfg.vocab))
         return fail(MK_ERR_INVALID_ARG, "token_id outside [0, vocab)");
+    cudaError_t e = cudaSetDevice(h->device);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaSetDevice");
     mk::Params p = h->base;
-    p.token = token;
-    p.d_token = d_token;
-    p.pos = position;
-    p.out_logits = out_logits;
-    p.out_token = out_token;
     p.timeout_ns = h->timeout_ns;
     p.trace = h->trace_on ? h->d_trace : nullptr;
     p.trace_cap = h->trace_cap;
-    cudaError_t e = cudaSetDevice(h->device);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaSetDevice");
-    if (!unfused) {
-        p.stage_lo = 0;
-        p.stage_hi = h->plan.n_stages;
-        p.reset_at_exit = 1;
-        e = mk_kernel_launch(&p, h->plan.n_sm, 1, stream);
-        if (e == cudaErrorCooperativeLaunchTooLarge)
-            return fail(MK_ERR_LAUNCH, "persistent grid cannot be co-resident on this device");
-        if (e != cudaSuccess) return cuda_fail(e, "megakernel launch");
-        return MK_OK;
-    }
-    for (int s = 0; s < h->plan.n_stages; ++s) {
-        p.stage_lo = s;
-        p.stage_hi = s + 1;
-        p.reset_at_exit = (s == h->plan.n_stages - 1);
-        e = mk_kernel_launch(&p, h->plan.n_sm, 0, stream);
-        if (e != cudaSuccess) return cuda_fail(e, "stage launch");
-    }
-    return MK_OK;
+    return mkint::launch_step(p, h->im.n_sm, h->im.n_stages, token, d_token, position, out_logits,
+                              out_token, stream, unfused);
 }
 
 }  // namespace
@@ -395,195 +601,42 @@ int mk_create(const mk_config *config, const mk_weights *w, const mk_kv_cache *k
               mk_handle **out) {
     if (!out) return fail(MK_ERR_INVALID_ARG, "out is NULL");
     *out = nullptr;
-    int rc = check_config(config);
+    int rc = mkint::check_inputs(config, w, kv);
     if (rc) return rc;
-    if (!w || !w->embed || !w->final_norm || !w->layers || !kv || !kv->k || !kv->v)
-        return fail(MK_ERR_INVALID_ARG, "a weight or cache pointer is NULL");
-    const mk_config &c = *config;
-    if (!aligned16(w->embed) || !aligned16(w->final_norm) || !aligned16(kv->k) || !aligned16(kv->v))
-        return fail(MK_ERR_INVALID_ARG, "weights and caches must be 16-byte aligned");
-    for (int l = 0; l < c.n_layers; ++l) {
-        const mk_layer_weights &lw = w->layers[l];
-        const void *ps[9] = {lw.attn_norm, lw.wq, lw.wk, lw.wv, lw.wo,
-                             lw.mlp_norm, lw.w_gate, lw.w_up, lw.w_down};
-        for (const void *q : ps) {
-            if (!q) return fail(MK_ERR_INVALID_ARG, "a layer weight pointer is NULL");
-            if (!aligned16(q)) return fail(MK_ERR_INVALID_ARG, "layer weights must be 16-byte aligned");
-        }
-    }
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-    cudaDeviceProp prop;
-    e = cudaGetDeviceProperties(&prop, dev);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDeviceProperties");
-    if (!(prop.major == 10 && prop.minor == 3))
-        return fail(MK_ERR_UNSUPPORTED, "built for sm_103 (GB300); this device is sm_" +
-                                            std::to_string(prop.major) + std::to_string(prop.minor));
-    int coop = 0;
-    cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
-    if (!coop) return fail(MK_ERR_UNSUPPORTED, "device has no cooperative launch");
-    e = mk_kernel_configure();
-    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
-    int bps = 0;
-    e = mk_kernel_occupancy(&bps);
-    if (e != cudaSuccess) return cuda_fail(e, "occupancy query");
-    if (bps < 1) return fail(MK_ERR_LAUNCH, "megakernel CTA does not fit on an SM");
-
+    int dev = 0, n_sm = 0;
+    rc = mkint::check_device(&dev, &n_sm);
+    if (rc) return rc;
     mk_handle *h = new (std::nothrow) mk_handle();
     if (!h) return fail(MK_ERR_NOMEM, "host allocation failed");
-    h->cfg = c;
+    h->cfg = *config;
     h->device = dev;
-    rc = build_plan(config, prop.multiProcessorCount, h->plan);
+    rc = mkint::make_image(config, w, n_sm, h->im);
     if (rc) {
         delete h;
         return rc;
     }
-    const Plan &P = h->plan;
-    const int L = c.n_layers, d = c.d_model, Hq = c.n_heads, Hkv = c.n_kv_heads, hd = c.head_dim,
-              F = c.ffn_dim, V = c.vocab;
-    const size_t n_instr = P.n_instr();
-    // ---- flat queues and stage index
-    std::vector<Instr> flat;
-    flat.reserve(n_instr);
-    std::vector<int32_t> qbeg((size_t)P.n_sm * (P.n_stages + 1));
-    h->qlen.resize(P.n_sm);
-    for (int s = 0; s < P.n_sm; ++s) {
-        const int base = (int)flat.size();
-        h->qlen[s] = (int)P.q[s].size();
-        int k = 0;
-        for (int st = 0; st <= P.n_stages; ++st) {
-            while (k < (int)P.q[s].size() && P.q[s][k].stage < st) ++k;
-            qbeg[(size_t)s * (P.n_stages + 1) + st] = base + k;
-        }
-        flat.insert(flat.end(), P.q[s].begin(), P.q[s].end());
-    }
-    // ---- RoPE table: angle pos * theta^(-2i/hd), in double
-    std::vector<float> rope((size_t)c.max_seq * hd);
-    for (int pos = 0; pos < c.max_seq; ++pos)
-        for (int i = 0; i < hd / 2; ++i) {
-            const double inv_freq = std::pow((double)c.rope_theta, -2.0 * i / (double)hd);
-            const double a = (double)pos * inv_freq;
-            rope[((size_t)pos * (hd / 2) + i) * 2] = (float)std::cos(a);
-            rope[((size_t)pos * (hd / 2) + i) * 2 + 1] = (float)std::sin(a);
-        }
-    // ---- one device allocation, carved up
-    DevBump b;
-    const size_t o_layers = b.take(sizeof(mk::LayerW) * L);
-    const size_t o_x = b.take(sizeof(float) * d);
-    const size_t o_qkv = b.take(sizeof(float) * (size_t)L * (Hq + 2 * Hkv) * hd);
-    const size_t o_part = b.take(sizeof(float) * (size_t)L * Hq * P.S * (hd + 2));
-    const size_t o_att = b.take(sizeof(float) * (size_t)L * Hq * hd);
-    const size_t o_h = b.take(sizeof(float) * (size_t)L * F);
-    const size_t o_lm = b.take(sizeof(unsigned long long) * P.n_lm);
-    const size_t o_ctr = b.take(sizeof(uint32_t) * P.cl.total);
-    const size_t o_exit = b.take(sizeof(uint32_t));
-    const size_t o_status = b.take(sizeof(int32_t));
-    const size_t o_abort = b.take(sizeof(int32_t));
-    const size_t o_tin = b.take(sizeof(int32_t));
-    const size_t o_tout = b.take(sizeof(int32_t));
-    const size_t o_logits = b.take(sizeof(float) * V);
-    const size_t o_rope = b.take(sizeof(float) * rope.size());
-    const size_t o_instr = b.take(sizeof(Instr) * flat.size());
-    const size_t o_qbeg = b.take(sizeof(int32_t) * qbeg.size());
-    const int n_ranges = 5 + 9 * L;
-    const size_t o_ranges = b.take(sizeof(unsigned long long) * 2 * n_ranges);
-    const size_t o_dbg = b.take(sizeof(unsigned long long) * 4);
-    e = cudaMalloc(&h->dev_mem, b.off);
+    cudaError_t e = cudaMalloc(&h->dev_mem, h->im.total);
     if (e != cudaSuccess) {
         delete h;
         return cuda_fail(e, "cudaMalloc(scratch)");
     }
-    b.base = static_cast<char *>(h->dev_mem);
-    std::vector<mk::LayerW> lws(L);
-    for (int l = 0; l < L; ++l) {
-        const mk_layer_weights &lw = w->layers[l];
-        lws[l] = {(const uint16_t *)lw.attn_norm, (const uint16_t *)lw.wq, (const uint16_t *)lw.wk,
-                  (const uint16_t *)lw.wv, (const uint16_t *)lw.wo, (const uint16_t *)lw.mlp_norm,
-                  (const uint16_t *)lw.w_gate, (const uint16_t *)lw.w_up, (const uint16_t *)lw.w_down};
-    }
-    // valid byte ranges for the address self-checks of an MK_CHECKED build
-    std::vector<unsigned long long> ranges;
-    auto add_range = [&](const void *ptr, size_t bytes) {
-        ranges.push_back((unsigned long long)(uintptr_t)ptr);
-        ranges.push_back((unsigned long long)(uintptr_t)ptr + bytes);
-    };
-    const size_t kv_bytes = (size_t)L * c.max_batch * Hkv * c.max_seq * hd * 2;
-    add_range(h->dev_mem, b.off);
-    add_range(kv->k, kv_bytes);
-    add_range(kv->v, kv_bytes);
-    add_range(w->embed, (size_t)V * d * 2);
-    add_range(w->final_norm, (size_t)d * 2);
-    for (int l = 0; l < L; ++l) {
-        const mk_layer_weights &lw = w->layers[l];
-        const int qd = Hq * hd, kvd = Hkv * hd;
-        add_range(lw.attn_norm, (size_t)d * 2);
-        add_range(lw.wq, (size_t)qd * d * 2);
-        add_range(lw.wk, (size_t)kvd * d * 2);
-        add_range(lw.wv, (size_t)kvd * d * 2);
-        add_range(lw.wo, (size_t)d * qd * 2);
-        add_range(lw.mlp_norm, (size_t)d * 2);
-        add_range(lw.w_gate, (size_t)F * d * 2);
-        add_range(lw.w_up, (size_t)F * d * 2);
-        add_range(lw.w_down, (size_t)d * F * 2);
-    }
-    bool ok = cudaMemset(h->dev_mem, 0, b.off) == cudaSuccess &&
-              cudaMemcpy(b.at<char>(o_ranges), ranges.data(), sizeof(unsigned long long) * ranges.size(), cudaMemcpyHostToDevice) == cudaSuccess &&
-              cudaMemcpy(b.at<char>(o_layers), lws.data(), sizeof(mk::LayerW) * L, cudaMemcpyHostToDevice) == cudaSuccess &&
-              cudaMemcpy(b.at<char>(o_rope), rope.data(), sizeof(float) * rope.size(), cudaMemcpyHostToDevice) == cudaSuccess &&
-              cudaMemcpy(b.at<char>(o_instr), flat.data(), sizeof(Instr) * flat.size(), cudaMemcpyHostToDevice) == cudaSuccess &&
-              cudaMemcpy(b.at<char>(o_qbeg), qbeg.data(), sizeof(int32_t) * qbeg.size(), cudaMemcpyHostToDevice) == cudaSuccess &&
-              cudaDeviceSynchronize() == cudaSuccess;
-    if (!ok) {
-        e = cudaGetLastError();
+    char *base = static_cast<char *>(h->dev_mem);
+    rc = mkint::upload_image(h->im, config, w, kv, base, nullptr);
+    if (rc) {
         cudaFree(h->dev_mem);
         delete h;
-        return cuda_fail(e, "uploading the plan");
+        return rc;
     }
-    h->d_layers = b.at<mk::LayerW>(o_layers);
-    h->d_tok_in = b.at<int32_t>(o_tin);
-    h->d_tok_out = b.at<int32_t>(o_tout);
-    h->d_logits = b.at<float>(o_logits);
-    h->d_status = b.at<int32_t>(o_status);
-    h->d_ctr = b.at<uint32_t>(o_ctr);
-    h->d_exit = b.at<uint32_t>(o_exit);
-    h->d_abort = b.at<int32_t>(o_abort);
-
-    mk::Params &p = h->base;
-    p.L = L; p.d = d; p.Hq = Hq; p.Hkv = Hkv; p.hd = hd; p.F = F; p.V = V;
-    p.max_seq = c.max_seq; p.max_batch = c.max_batch; p.S = P.S; p.G = Hq / Hkv; p.ppt = P.ppt;
-    p.eps = c.rms_eps;
-    p.n_lm = P.n_lm; p.n_stages = P.n_stages;
-    p.geo_qkv = P.geo_qkv; p.geo_o = P.geo_o; p.geo_gu = P.geo_gu; p.geo_down = P.geo_down;
-    p.geo_lm = P.geo_lm;
-    p.cl = P.cl;
-    p.embed = (const uint16_t *)w->embed;
-    p.final_norm = (const uint16_t *)w->final_norm;
-    p.layers = h->d_layers;
-    p.kc = (uint16_t *)kv->k;
-    p.vc = (uint16_t *)kv->v;
-    p.x = b.at<float>(o_x);
-    p.qkv = b.at<float>(o_qkv);
-    p.part = b.at<float>(o_part);
-    p.att = b.at<float>(o_att);
-    p.h = b.at<float>(o_h);
-    p.lm_part = b.at<unsigned long long>(o_lm);
-    p.ctr = h->d_ctr;
-    p.exit_ctr = h->d_exit;
-    p.status = h->d_status;
-    p.abort_flag = h->d_abort;
-    p.rope = b.at<float>(o_rope);
-    p.instr = b.at<Instr>(o_instr);
-    p.q_begin = b.at<int32_t>(o_qbeg);
-    p.n_ranges = n_ranges;
-    p.ranges = b.at<unsigned long long>(o_ranges);
-    p.dbg = b.at<unsigned long long>(o_dbg);
-    h->ctr_bytes = o_tin - o_ctr;  // counters, exit, status, abort
+    mkint::fill_params(h->im, config, w, kv, base, h->base);
+    h->d_tok_in = reinterpret_cast<int32_t *>(base + h->im.o_tin);
+    h->d_tok_out = reinterpret_cast<int32_t *>(base + h->im.o_tout);
+    h->d_logits = reinterpret_cast<float *>(base + h->im.o_logits);
+    h->zero_bytes = h->im.o_zero_end - h->im.o_ctr;
     if (getenv("MK_LOG")) {
         size_t mx = 0, mn = (size_t)-1;
-        for (auto &q : P.q) { mx = std::max(mx, q.size()); mn = std::min(mn, q.size()); }
-        fprintf(stderr, "[mk] plan: %d SMs, %zu instructions (%zu..%zu per SM), %d splits, %d counters\n",
-                P.n_sm, n_instr, mn, mx, P.S, P.cl.total);
+        for (int q : h->im.qlen) { mx = std::max(mx, (size_t)q); mn = std::min(mn, (size_t)q); }
+        fprintf(stderr, "[mk] plan: %d SMs, %zu instructions (%zu..%zu per SM), %d splits, %zu scratch bytes\n",
+                h->im.n_sm, h->im.n_instr, mn, mx, h->base.S, h->im.total);
     }
     *out = h;
     return MK_OK;
@@ -637,11 +690,11 @@ int mk_get_status(mk_handle *h) {
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
     int32_t st = 0;
-    e = cudaMemcpy(&st, h->d_status, sizeof st, cudaMemcpyDeviceToHost);
+    e = cudaMemcpy(&st, h->base.status, sizeof st, cudaMemcpyDeviceToHost);
     if (e != cudaSuccess) return cuda_fail(e, "status read");
     if (st == mk::DS_OK) return MK_OK;
     // a failed step leaves counters mid-way: clear them with the status
-    e = cudaMemset(h->d_ctr, 0, h->ctr_bytes);
+    e = cudaMemset(h->base.ctr, 0, h->zero_bytes);
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return cuda_fail(e, "status reset");
     if (st == mk::DS_BAD_TOKEN) return fail(MK_ERR_INVALID_ARG, "device token outside [0, vocab)");
@@ -658,13 +711,13 @@ int mk_set_trace(mk_handle *h, int32_t enable) {
     if (!h) return fail(MK_ERR_INVALID_ARG, "handle is NULL");
     if (enable && !h->d_trace) {
         int cap = 0;
-        for (int q : h->qlen) cap = std::max(cap, q);
+        for (int q : h->im.qlen) cap = std::max(cap, q);
         cap = std::max(cap, 1);
         cudaError_t e = cudaSetDevice(h->device);
         if (e == cudaSuccess)
-            e = cudaMalloc(&h->d_trace, sizeof(long long) * 5 * (size_t)cap * h->plan.n_sm);
+            e = cudaMalloc(&h->d_trace, sizeof(long long) * 5 * (size_t)cap * h->im.n_sm);
         if (e == cudaSuccess)
-            e = cudaMemset(h->d_trace, 0, sizeof(long long) * 5 * (size_t)cap * h->plan.n_sm);
+            e = cudaMemset(h->d_trace, 0, sizeof(long long) * 5 * (size_t)cap * h->im.n_sm);
         if (e != cudaSuccess) {
             h->d_trace = nullptr;
             return cuda_fail(e, "trace buffer");
@@ -678,15 +731,15 @@ int mk_set_trace(mk_handle *h, int32_t enable) {
 int mk_read_trace(mk_handle *h, int64_t *host_out, int32_t cap) {
     if (!h || !host_out || cap < 0) return fail(MK_ERR_INVALID_ARG, "bad arguments");
     if (!h->d_trace) return 0;
-    std::vector<long long> buf(5 * (size_t)h->trace_cap * h->plan.n_sm);
+    std::vector<long long> buf(5 * (size_t)h->trace_cap * h->im.n_sm);
     cudaError_t e = cudaSetDevice(h->device);
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e == cudaSuccess)
         e = cudaMemcpy(buf.data(), h->d_trace, sizeof(long long) * buf.size(), cudaMemcpyDeviceToHost);
     if (e != cudaSuccess) return cuda_fail(e, "trace read");
     int n = 0;
-    for (int s = 0; s < h->plan.n_sm; ++s)
-        for (int i = 0; i < h->qlen[s] && i < h->trace_cap; ++i) {
+    for (int s = 0; s < h->im.n_sm; ++s)
+        for (int i = 0; i < h->im.qlen[s] && i < h->trace_cap; ++i) {
             if (n >= cap) return n;
             std::memcpy(host_out + 5 * (size_t)n, &buf[5 * ((size_t)s * h->trace_cap + i)],
                         5 * sizeof(long long));
@@ -711,8 +764,8 @@ int mk_debug_read(mk_handle *h, uint64_t *host_out4) {
 
 int mk_plan_size(const mk_handle *h, int32_t *n_sm, int32_t *n_instr) {
     if (!h) return fail(MK_ERR_INVALID_ARG, "handle is NULL");
-    if (n_sm) *n_sm = h->plan.n_sm;
-    if (n_instr) *n_instr = (int32_t)h->plan.n_instr();
+    if (n_sm) *n_sm = h->im.n_sm;
+    if (n_instr) *n_instr = (int32_t)h->im.n_instr;
     return MK_OK;
 }
 
