@@ -85,6 +85,8 @@ def load(path: str | None = None):
     L.mk_plan_size.argtypes = [_VP, _PI32, _PI32]
     L.mk_plan_inspect.argtypes = [ctypes.POINTER(mk_config), _I32, _PI32, _I32, _PI32, _PI32]
     L.mk_debug_read.argtypes = [_VP, ctypes.POINTER(ctypes.c_uint64)]
+    L.mk_decode_step_noalloc.argtypes = [ctypes.POINTER(mk_config), ctypes.POINTER(mk_weights),
+                                         ctypes.POINTER(mk_kv_cache), _I32, _I32, _VP, _VP, _VP]
     L.mk_destroy.argtypes = [_VP]
     L.mk_destroy.restype = None
     _lib = L
@@ -139,6 +141,19 @@ def _weights_struct(shape, weights: dict):
     w = mk_weights(weights["embed"].data_ptr(), weights["final_norm"].data_ptr(),
                    ctypes.cast(layers, ctypes.POINTER(mk_layer_weights)))
     return w, layers
+
+
+def decode_step_noalloc(shape, weights: dict, k_cache, v_cache, token: int, pos: int, out_token,
+                        logits=None, attn_splits: int = 0, stream=None) -> None:
+    """mk_decode_step_noalloc: one decode step without a handle and without
+    any device allocation (scratch lives in the library's static array)."""
+    cfg = make_config(shape, int(k_cache.shape[3]), int(k_cache.shape[1]), attn_splits)
+    w, layers = _weights_struct(shape, weights)
+    kv = mk_kv_cache(k_cache.data_ptr(), v_cache.data_ptr())
+    check(load().mk_decode_step_noalloc(ctypes.byref(cfg), ctypes.byref(w), ctypes.byref(kv),
+                                        int(token), int(pos),
+                                        logits.data_ptr() if logits is not None else None,
+                                        out_token.data_ptr(), _stream_ptr(stream)))
 
 
 class Megakernel:

@@ -11,7 +11,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libmk.so")
 LIB_CHECKED = os.path.join(BUILD, "libmk_checked.so")
-SOURCES = ["mk_kernel.cu", "mk_host.cpp"]
+SOURCES = ["mk_kernel.cu", "mk_host.cpp", "mk_noalloc.cu"]
 DEPS = SOURCES + ["mk_plan.h", "mk_internal.h"]
 
 

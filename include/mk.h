@@ -125,6 +125,34 @@ int mk_decode_step_host(mk_handle *h, const int32_t *host_token, int32_t positio
 int mk_decode_step_unfused(mk_handle *h, int32_t token_id, int32_t position,
                            float *out_logits, int32_t *out_token, void *stream);
 
+/* The decode step of mk_decode_step for callers that cannot allocate device
+ * memory (a host framework that owns all device memory through its own pool,
+ * a plugin that may only use the buffers it is handed, code that must not
+ * trigger an allocation's implicit synchronisation). There is no handle: the
+ * caller passes the model every call, and the kernel's scratch (instruction
+ * queues, dependency counters, activations, attention partials, RoPE table)
+ * lives in one file-scope device array of 16 MiB that every GPU loading this
+ * library holds until the process exits. No counterpart in the megakernel
+ * article: it is an interface addition of this library.
+ *   - Allocates no device memory: no cudaMalloc, cudaFree or allocating
+ *     library routine. Host-side planning uses ordinary host memory.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current) and plans and uploads
+ *     the instruction queues; later calls with the same config, weight and
+ *     cache pointers reuse them and only clear the counters before the
+ *     launch. Make the first call (and any call with new inputs) before
+ *     capturing a stream.
+ *   - Every call shares the one array and it keeps the last call's contents;
+ *     calls whose kernels overlap on the GPU (different streams, or a second
+ *     model while the first still runs) race on it.
+ *   - Returns MK_ERR_INVALID_ARG with a message if the model needs more
+ *     scratch than the array holds (use mk_create then). A device-side wait
+ *     timeout is not reported by this asynchronous call.
+ * Arguments are those of mk_create plus those of mk_decode_step. */
+int mk_decode_step_noalloc(const mk_config *config, const mk_weights *weights,
+                           const mk_kv_cache *kv, int32_t token_id, int32_t position,
+                           float *out_logits, int32_t *out_token, void *stream);
+
 /* Device-side status of the last steps. Synchronises the handle's device,
  * returns MK_OK or MK_ERR_TIMEOUT (a bounded in-kernel wait expired; the step
  * that hit it produced undefined outputs) and resets it. After a timeout the
