@@ -355,7 +355,7 @@ def run_mk(args, ws, rank, local):
     if args.trace:
         from decode_megakernel_llama_gb300 import trace as mktrace
         mk.set_trace(True)
-        mk.step_dev(tok, P, tok, None, stream)
+        mk.step_dev(tok, P + K // 2, tok, None, stream)  # a position in the middle of the timed range
         torch.cuda.synchronize()
         rec = mk.read_trace()
         mk.set_trace(False)

@@ -213,7 +213,7 @@ class Megakernel:
         import numpy as np
         n_sm, n_instr = ctypes.c_int32(), ctypes.c_int32()
         check(load().mk_plan_size(self.h, ctypes.byref(n_sm), ctypes.byref(n_instr)))
-        buf = np.zeros((max(1, n_instr.value), 5), dtype=np.int64)
+        buf = np.zeros((max(1, n_instr.value), 8), dtype=np.int64)
         n = check(load().mk_read_trace(self.h, buf.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
                                        buf.shape[0]))
         return buf[:n]

@@ -12,6 +12,7 @@
 #include <algorithm>
 #include <cmath>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <numeric>
 #include <string>
@@ -45,10 +46,10 @@ using mk::Instr;
 // ---------------------------------------------------------------------------
 // Tile geometry for an input length K (see Geo in mk_plan.h).
 // ---------------------------------------------------------------------------
-bool make_geo(int K, Geo &g) {
+bool make_geo(int K, Geo &g, int max_nx = 32) {
     if (K <= 0 || K % 256 != 0 || K > 16384) return false;
     int sw = 1;
-    while (K / sw > 2048 || (K / sw) % 256 != 0) {
+    while (K / sw > 32 * max_nx || (K / sw) % 256 != 0) {
         sw *= 2;
         if (sw > mk::kConsumerWarps) return false;
     }
@@ -90,14 +91,15 @@ int check_config(const mk_config *c) {
     if (c->n_heads % c->n_kv_heads != 0)
         return fail(MK_ERR_INVALID_ARG, "n_heads must be a multiple of n_kv_heads");
     const int G = c->n_heads / c->n_kv_heads, hd = c->head_dim;
-    if (G > mk::kMaxG || G * hd + hd + mk::kConsumerWarps * G * (hd + 2) > mk::kXbufFloats)
+    if (G > 4 || G * hd + hd + mk::kConsumerWarps * G * (hd + 2) > mk::kXbufFloats)
         return fail(MK_ERR_UNSUPPORTED, "too many query heads per kv head for the attention scratch");
     const int qd = c->n_heads * hd;
     if (c->d_model % 256 || qd % 256 || c->ffn_dim % 256)
         return fail(MK_ERR_UNSUPPORTED, "d_model, n_heads*head_dim and ffn_dim must be multiples of 256");
-    if (c->d_model > mk::kXbufFloats || qd > mk::kXbufFloats)
-        return fail(MK_ERR_UNSUPPORTED, "d_model and n_heads*head_dim must be <= 5120");
-    if (c->ffn_dim > 16384) return fail(MK_ERR_UNSUPPORTED, "ffn_dim must be <= 16384");
+    if (c->d_model > mk::kMaxStaged || qd > mk::kMaxStaged)
+        return fail(MK_ERR_UNSUPPORTED, "d_model and n_heads*head_dim must be <= 4096");
+    if (c->n_layers > 127) return fail(MK_ERR_UNSUPPORTED, "at most 127 layers (activation tag versions)");
+    if (c->ffn_dim > mk::kMaxStagedLong) return fail(MK_ERR_UNSUPPORTED, "ffn_dim must be <= 8192");
     const double kv_elems = (double)c->n_layers * c->max_batch * c->n_kv_heads * c->max_seq * hd;
     if (kv_elems * 2 > 9.0e18) return fail(MK_ERR_INVALID_ARG, "KV cache too large");
     return MK_OK;
@@ -110,14 +112,17 @@ struct Chunk {
     int sm, r0, n;
 };
 
-std::vector<Chunk> split_rows(int N, double cost_per_row, std::vector<double> &load, int max_rows) {
+std::vector<Chunk> split_rows(int N, double cost_per_row, std::vector<double> &load, int max_rows,
+                              const std::vector<char> *excluded = nullptr) {
     const int n_sm = (int)load.size();
-    const int base = N / n_sm, extra = N % n_sm;
-    std::vector<int> order(n_sm);
-    std::iota(order.begin(), order.end(), 0);
+    std::vector<int> order;
+    for (int sm = 0; sm < n_sm; ++sm)
+        if (!excluded || !(*excluded)[sm]) order.push_back(sm);
+    const int n_use = (int)order.size();
+    const int base = N / n_use, extra = N % n_use;
     std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return load[a] < load[b]; });
-    std::vector<int> cnt(n_sm, base);
-    for (int i = 0; i < extra; ++i) cnt[order[i]] += 1;
+    std::vector<int> cnt(n_sm, 0);
+    for (int i = 0; i < n_use; ++i) cnt[order[i]] = base + (i < extra ? 1 : 0);
     std::vector<Chunk> out;
     int r = 0;
     for (int sm = 0; sm < n_sm; ++sm) {
@@ -148,7 +153,7 @@ int build_plan(const mk_config *c, int n_sm, Plan &P) {
     if (P.geo_gu.rt < 2 || P.geo_gu.rt % 2)
         return fail(MK_ERR_UNSUPPORTED, "gate/up tile needs an even row count");
     P.ppt = (mk::kPageBytes / 2) / (hd * 2);
-    const int max_tiles = (c->max_seq + P.ppt - 1) / P.ppt;
+    const int max_tiles = (c->max_seq + P.ppt * mk::kMinSplitTiles - 1) / (P.ppt * mk::kMinSplitTiles);
     int S = std::max(1, std::min(n_sm / Hkv, max_tiles));
     if (c->attn_splits > 0) S = std::min(c->attn_splits, std::max(1, max_tiles));
     P.S = S;
@@ -178,16 +183,37 @@ int build_plan(const mk_config *c, int n_sm, Plan &P) {
         in.bytes_lo = (int32_t)(b & 0xFFFFFFFFll);
         in.bytes_hi = (int32_t)(b >> 32);
     };
-    const int cap_qkv = mk::kRedCap / P.geo_qkv.sw, cap_o = mk::kRedCap / P.geo_o.sw,
-              cap_gu = mk::kRedCap / (2 * P.geo_gu.sw), cap_down = mk::kRedCap / P.geo_down.sw,
+    const int cap_qkv = mk::kRedCap / P.geo_qkv.sw,
+              cap_o = std::min(mk::kRedCap / P.geo_o.sw, mk::kResidFloats),
+              cap_gu = mk::kRedCap / (2 * P.geo_gu.sw),
+              cap_down = std::min(mk::kDredFloats / P.geo_down.sw, mk::kResidFloats),
               cap_lm = mk::kRedCap / P.geo_lm.sw;
+    // Short contexts: the attention of a layer runs on SMs that get no QKV
+    // rows, so it starts as soon as q/k/v are published and its cached
+    // keys/values are prefetched at the start of the layer. Long contexts
+    // spread attention (and its KV streaming) over every SM instead.
+    const double attn_cost = 2.0 * 2.0 * hd * std::ceil((double)c->max_seq / S) + 4096.0;
+    const bool dedicated_attn = Hkv * S * 4 <= n_sm;
     int prev_down = 0;
     for (int l = 0; l < L; ++l) {
         const int st = mk::kStagesPerLayer * l;
+        // ---- attention SMs of this layer (least loaded first)
+        std::vector<int> attn_sm;
+        std::vector<char> excluded(n_sm, 0);
+        if (dedicated_attn) {
+            std::vector<int> order(n_sm);
+            std::iota(order.begin(), order.end(), 0);
+            std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return load[a] < load[b]; });
+            for (int i = 0; i < Hkv * S; ++i) {
+                attn_sm.push_back(order[i]);
+                excluded[order[i]] = 1;
+            }
+        }
         // ---- QKV: rows of [Wq; Wk; Wv]
         std::vector<int> touch(Hkv, 0);
         const int mat_start[4] = {0, qd, qd + kvd, qd + 2 * kvd};
-        for (const Chunk &ch : split_rows(qd + 2 * kvd, 2.0 * d, load, cap_qkv)) {
+        for (const Chunk &ch : split_rows(qd + 2 * kvd, 2.0 * d, load, cap_qkv,
+                                          dedicated_attn ? &excluded : nullptr)) {
             int r = ch.r0, end = ch.r0 + ch.n;
             while (r < end) {
                 int mat = r < mat_start[1] ? 0 : (r < mat_start[2] ? 1 : 2);
@@ -210,11 +236,11 @@ int build_plan(const mk_config *c, int n_sm, Plan &P) {
                 r = e;
             }
         }
-        // ---- attention: Hkv x S splits, each to the least-loaded SM
-        const double attn_cost = 2.0 * 2.0 * hd * std::ceil((double)c->max_seq / S) + 4096.0;
+        // ---- attention: Hkv x S splits
         for (int h = 0; h < Hkv; ++h)
             for (int s = 0; s < S; ++s) {
-                int sm = (int)(std::min_element(load.begin(), load.end()) - load.begin());
+                int sm = dedicated_attn ? attn_sm[h * S + s]
+                                        : (int)(std::min_element(load.begin(), load.end()) - load.begin());
                 load[sm] += attn_cost;
                 Instr in = mk_instr(mk::OP_ATTN, l, st + 1);
                 in.a0 = h;
@@ -400,11 +426,12 @@ int make_image(const mk_config *config, const mk_weights *w, int n_sm, Image &im
     im.o_dbg = b.take(sizeof(unsigned long long) * 4);
     im.o_zero_end = b.off;
     im.o_layers = b.take(sizeof(mk::LayerW) * L);
-    im.o_x = b.take(sizeof(float) * d);
-    im.o_qkv = b.take(sizeof(float) * (size_t)L * (Hq + 2 * Hkv) * hd);
-    im.o_part = b.take(sizeof(float) * (size_t)L * Hq * P.S * (hd + 2));
-    im.o_att = b.take(sizeof(float) * (size_t)L * Hq * hd);
-    im.o_h = b.take(sizeof(float) * (size_t)L * F);
+    im.o_epoch = b.take(sizeof(uint32_t));
+    im.o_x = b.take(8 * (size_t)d);  // tagged words {value, tag}
+    im.o_qkv = b.take(8 * (size_t)L * (Hq + 2 * Hkv) * hd);
+    im.o_part = b.take(8 * (size_t)L * Hq * P.S * (hd + 2));
+    im.o_att = b.take(8 * (size_t)L * Hq * hd);
+    im.o_h = b.take(8 * (size_t)L * F);
     im.o_lm = b.take(sizeof(unsigned long long) * P.n_lm);
     im.o_tin = b.take(sizeof(int32_t));
     im.o_tout = b.take(sizeof(int32_t));
@@ -435,11 +462,12 @@ void fill_params(const Image &im, const mk_config *config, const mk_weights *w,
     p.layers = reinterpret_cast<const mk::LayerW *>(base + im.o_layers);
     p.kc = (uint16_t *)kv->k;
     p.vc = (uint16_t *)kv->v;
-    p.x = reinterpret_cast<float *>(base + im.o_x);
-    p.qkv = reinterpret_cast<float *>(base + im.o_qkv);
-    p.part = reinterpret_cast<float *>(base + im.o_part);
-    p.att = reinterpret_cast<float *>(base + im.o_att);
-    p.h = reinterpret_cast<float *>(base + im.o_h);
+    p.xll = reinterpret_cast<uint2 *>(base + im.o_x);
+    p.qkvll = reinterpret_cast<uint2 *>(base + im.o_qkv);
+    p.partll = reinterpret_cast<uint2 *>(base + im.o_part);
+    p.attll = reinterpret_cast<uint2 *>(base + im.o_att);
+    p.hll = reinterpret_cast<uint2 *>(base + im.o_h);
+    p.epoch = reinterpret_cast<uint32_t *>(base + im.o_epoch);
     p.lm_part = reinterpret_cast<unsigned long long *>(base + im.o_lm);
     p.ctr = reinterpret_cast<uint32_t *>(base + im.o_ctr);
     p.exit_ctr = reinterpret_cast<uint32_t *>(base + im.o_exit);
@@ -452,6 +480,12 @@ void fill_params(const Image &im, const mk_config *config, const mk_weights *w,
     p.ranges = reinterpret_cast<const unsigned long long *>(base + im.o_ranges);
     p.dbg = reinterpret_cast<unsigned long long *>(base + im.o_dbg);
     p.timeout_ns = 2000000000ull;
+    p.l2_lookahead = 0;
+    if (const char *env = getenv("MK_L2_LOOKAHEAD_KB")) p.l2_lookahead = strtoull(env, nullptr, 10) << 10;
+    p.max_inflight = 3;
+    if (const char *env = getenv("MK_MAX_INFLIGHT")) p.max_inflight = atoi(env);
+    if (p.max_inflight < 1) p.max_inflight = 1;
+    if (p.max_inflight > mk::kPages) p.max_inflight = mk::kPages;
 }
 
 int upload_image(const Image &im, const mk_config *config, const mk_weights *w,
@@ -715,9 +749,9 @@ int mk_set_trace(mk_handle *h, int32_t enable) {
         cap = std::max(cap, 1);
         cudaError_t e = cudaSetDevice(h->device);
         if (e == cudaSuccess)
-            e = cudaMalloc(&h->d_trace, sizeof(long long) * 5 * (size_t)cap * h->im.n_sm);
+            e = cudaMalloc(&h->d_trace, sizeof(long long) * mk::kTraceWords * (size_t)cap * h->im.n_sm);
         if (e == cudaSuccess)
-            e = cudaMemset(h->d_trace, 0, sizeof(long long) * 5 * (size_t)cap * h->im.n_sm);
+            e = cudaMemset(h->d_trace, 0, sizeof(long long) * mk::kTraceWords * (size_t)cap * h->im.n_sm);
         if (e != cudaSuccess) {
             h->d_trace = nullptr;
             return cuda_fail(e, "trace buffer");
@@ -731,7 +765,7 @@ int mk_set_trace(mk_handle *h, int32_t enable) {
 int mk_read_trace(mk_handle *h, int64_t *host_out, int32_t cap) {
     if (!h || !host_out || cap < 0) return fail(MK_ERR_INVALID_ARG, "bad arguments");
     if (!h->d_trace) return 0;
-    std::vector<long long> buf(5 * (size_t)h->trace_cap * h->im.n_sm);
+    std::vector<long long> buf(mk::kTraceWords * (size_t)h->trace_cap * h->im.n_sm);
     cudaError_t e = cudaSetDevice(h->device);
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e == cudaSuccess)
@@ -741,8 +775,9 @@ int mk_read_trace(mk_handle *h, int64_t *host_out, int32_t cap) {
     for (int s = 0; s < h->im.n_sm; ++s)
         for (int i = 0; i < h->im.qlen[s] && i < h->trace_cap; ++i) {
             if (n >= cap) return n;
-            std::memcpy(host_out + 5 * (size_t)n, &buf[5 * ((size_t)s * h->trace_cap + i)],
-                        5 * sizeof(long long));
+            std::memcpy(host_out + mk::kTraceWords * (size_t)n,
+                        &buf[mk::kTraceWords * ((size_t)s * h->trace_cap + i)],
+                        mk::kTraceWords * sizeof(long long));
             ++n;
         }
     return n;

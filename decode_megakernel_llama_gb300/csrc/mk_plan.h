@@ -5,9 +5,14 @@
 // The design follows the megakernel article ("Revolution der
 // KI-Beschleunigung: Wie ein Low-Latency Megakernel den Llama-1B Turbo
 // zündet", dasgeld.co): the host plans one instruction sequence per SM once
-// (internal-infrastructure paragraph), the kernel interprets it, and
-// instructions wait on / bump dependency counters in global memory
-// (synchronisation paragraph).
+// (internal-infrastructure paragraph), the kernel interprets it, and every
+// instruction waits for exactly the data it consumes through flags kept in
+// global memory (synchronisation paragraph). Here the flag travels inside
+// each activation word: an element is stored as {float value, 32-bit tag}
+// in one 8-byte write, the tag naming the decode step and the version of the
+// tensor, and a consumer polls the words it needs until all carry the tag it
+// expects. The plan's per-instruction dependency counts (wait_ctr /
+// wait_target) describe the same edges for the host-side validator.
 #pragma once
 #include <stdint.h>
 
@@ -20,16 +25,30 @@ constexpr int kThreads = kConsumerThreads + 32;      // + one producer (TMA) war
 constexpr int kPageBytes = 32768;                    // one shared-memory page
 constexpr int kPages = 6;                            // pages in the ring
 constexpr int kRedCap = 2048;                        // floats of per-row partials
-constexpr int kXbufFloats = 5120;                    // staged input vector / attention scratch
-constexpr int kMaxG = 8;                             // max query heads per kv head
+constexpr int kXbufFloats = 6144;                    // staged input (4096 fp32 + 4096 bf16 gains) / attention scratch
+constexpr int kMaxStaged = 4096;                     // max normed input length staged with its gains
+constexpr int kMaxStagedLong = 8192;                 // max un-normed input length (down projection)
+constexpr int kResidFloats = 256;                    // residual rows of one O-proj / down instruction
+constexpr int kDredFloats = 256;                     // per-row partials of one down instruction
+constexpr int kMaxG = 8;                             // max query heads per kv head (1,2,3,4,6,8)
+constexpr int kTraceWords = 8;                       // int64 per trace record
+constexpr int kMinSplitTiles = 4;                    // an attention split gets >= 4 KV tiles
+constexpr int kMergeBatch = 1;                       // splits read together by the merge
 
 constexpr int kSmemPages = 0;
 constexpr int kSmemXbuf = kSmemPages + kPages * kPageBytes;
+// The partials buffer `red` is the top 8 KB of the 32 KB staging area: ops
+// that stage at most kXbufFloats floats use both; the down projection stages
+// up to 8192 floats over both and keeps its partials in `dred`.
 constexpr int kSmemRed = kSmemXbuf + kXbufFloats * 4;
-constexpr int kSmemBars = kSmemRed + kRedCap * 4;
+constexpr int kSmemResid = kSmemXbuf + kMaxStagedLong * 4;
+constexpr int kSmemDred = kSmemResid + kResidFloats * 4;
+constexpr int kSmemBars = kSmemDred + kDredFloats * 4;
 constexpr int kSmemMisc = kSmemBars + 2 * kPages * 8;
 constexpr int kSmemParams = kSmemMisc + 256;      // shared copy of the launch parameters
-constexpr int kSmemBytes = kSmemParams + 1024;
+constexpr int kParamsSlot = 640;
+constexpr int kSmemBytes = kSmemParams + kParamsSlot;
+static_assert(kSmemBytes <= 232448, "shared memory of one CTA exceeds 227 KB");
 
 // ---- opcodes ------------------------------------------------------------
 enum Op : int32_t {
@@ -90,12 +109,13 @@ struct Params {
     const uint16_t *embed, *final_norm;
     const LayerW *layers;   // device array [L]
     uint16_t *kc, *vc;      // KV caches
-    // scratch (library-owned)
-    float *x;               // [d] residual stream
-    float *qkv;             // [L][(Hq+2Hkv)*hd] raw projections
-    float *part;            // [L][Hq][S][hd+2] split partials (o, m, l)
-    float *att;             // [L][Hq*hd] merged attention output
-    float *h;               // [L][F] silu(g)*u
+    // scratch (library-owned); activations are tagged words {value, tag}
+    uint2 *xll;             // [d] residual stream (versions 2l+1 after O-proj l, 2l+2 after down l)
+    uint2 *qkvll;           // [L][(Hq+2Hkv)*hd] raw projections
+    uint2 *partll;          // [L][Hq][S][hd+2] split partials (o, m, l)
+    uint2 *attll;           // [L][Hq*hd] attention output
+    uint2 *hll;             // [L][F] silu(g)*u
+    uint32_t *epoch;        // decode-step counter (tags carry it); advanced by the last CTA
     unsigned long long *lm_part;  // [n_lm] packed (value, ~index)
     uint32_t *ctr;          // dependency counters
     uint32_t *exit_ctr;     // CTAs done with the step
@@ -112,14 +132,16 @@ struct Params {
     float *out_logits;      // nullable
     int32_t *out_token;
     unsigned long long timeout_ns;
-    long long *trace;       // nullable: [n_sm][trace_cap][5]
+    long long *trace;       // nullable: [n_sm][trace_cap][kTraceWords]
     int32_t trace_cap;
+    unsigned long long l2_lookahead;  // bytes per SM prefetched into L2 beyond the smem ring
+    int32_t max_inflight;             // tiles per SM whose copies may be outstanding at once
     // address self-checks (only read by a build with MK_CHECKED defined)
     int32_t n_ranges;
     const unsigned long long *ranges;  // [n_ranges][2] valid [begin, end) byte ranges
     unsigned long long *dbg;           // first violation: site, address, bytes, block/thread
 };
-static_assert(sizeof(Params) <= 1024, "Params must fit its shared-memory slot");
+static_assert(sizeof(Params) <= kParamsSlot, "Params must fit its shared-memory slot");
 
 // Device status codes written to *status.
 enum DevStatus : int32_t { DS_OK = 0, DS_TIMEOUT = 1, DS_BAD_TOKEN = 2 };

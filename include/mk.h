@@ -54,10 +54,11 @@ typedef enum mk_status {
     MK_ERR_NOMEM = -6        /* device or host allocation failed */
 } mk_status;
 
-/* Model shape. Requirements: d_model, n_heads*head_dim and ffn_dim are
- * multiples of 256 and at most 16384; head_dim is 64 or 128; n_heads is a
- * multiple of n_kv_heads; d_model <= 4096. rms_eps is added to the mean
- * square inside the square root; rope_theta is the RoPE base. */
+/* Model shape. Requirements: d_model and n_heads*head_dim are each one of
+ * 256, 512, 768, 1024, 1536, 2048, 3072, 4096, and ffn_dim one of those or
+ * 6144, 8192 (a row is split over 1, 2, 4 or 8 warps in slices of 256..1024); head_dim is 64 or 128; n_heads is a multiple of n_kv_heads, at
+ * most 4 query heads per kv head; at most 127 layers. rms_eps is added to
+ * the mean square inside the square root; rope_theta is the RoPE base. */
 typedef struct mk_config {
     int32_t n_layers, d_model, n_heads, n_kv_heads, head_dim, ffn_dim, vocab;
     int32_t max_seq;     /* positions in the KV cache per sequence */
@@ -168,9 +169,13 @@ int mk_set_wait_timeout(mk_handle *h, uint64_t timeout_ns);
  * mk_read_trace copies out (see mk_read_trace). */
 int mk_set_trace(mk_handle *h, int32_t enable);
 
-/* Copies the trace of the last traced step to host_out: records of 5 int64
- * {sm, instruction op, wait-start ns, start ns, end ns}, SM after SM in queue
- * order; returns the number of records (or a negative status). cap = records. */
+/* Copies the trace of the last traced step to host_out: records of 8 int64
+ * {sm, instruction op, start - tile wait, start ns, phase0 ns, phase1 ns,
+ * phase2 ns, end ns}, SM after SM in queue order; "tile wait" is the time
+ * the instruction spent waiting for its weight / KV tiles to land. Phases of
+ * a GEMV instruction: input polled (and normalised), tiles done, epilogue
+ * written; of an attention instruction: q/k/v polled, tiles done, output
+ * written. Returns the number of records (or a negative status). cap = records. */
 int mk_read_trace(mk_handle *h, int64_t *host_out, int32_t cap);
 
 /* Diagnostics of a library built with MK_CHECKED (every device-side global

@@ -184,4 +184,5 @@ def test_trace_records_every_instruction(tiny):
     n_sm, n_instr = tiny.mk.plan_size()
     assert len(tr) == n_instr
     assert set(np.unique(tr[:, 1])) <= {1, 2, 3, 4, 5, 6}
-    assert (tr[:, 2] <= tr[:, 3]).all() and (tr[:, 3] <= tr[:, 4]).all()
+    assert (tr[:, 2] <= tr[:, 3]).all() and (tr[:, 3] <= tr[:, 7]).all()  # tile wait >= 0
+    assert ((tr[:, 4] >= tr[:, 3]) & (tr[:, 6] <= tr[:, 7])).all()
