@@ -360,13 +360,15 @@ __device__ bool wait_bar(const Params &p, uint64_t *bar, uint32_t parity) {
     }
 }
 
-// Consumer wait for tile t's page to be full; on traced steps thread 0 adds
-// the time it waited to the instruction's tile_wait.
-__device__ __forceinline__ bool wait_tile(const Params &p, const Ctx &cx, uint32_t t) {
+// Consumer wait for page pg to be full in the phase of parity par; on traced
+// steps thread 0 adds the time it waited to the instruction's tile_wait.
+__device__ __forceinline__ bool wait_tile(const Params &p, const Ctx &cx, int pg, uint32_t par,
+                                          bool tracing) {
+    if (!tracing) return wait_bar(p, &cx.full[pg], par);
     uint64_t t0 = 0;
-    if (p.trace && threadIdx.x == 0) t0 = gtimer();
-    const bool ok = wait_bar(p, &cx.full[t % kPages], (t / kPages) & 1);
-    if (p.trace && threadIdx.x == 0) cx.misc->tile_wait += (long long)(gtimer() - t0);
+    if (threadIdx.x == 0) t0 = gtimer();
+    const bool ok = wait_bar(p, &cx.full[pg], par);
+    if (threadIdx.x == 0) cx.misc->tile_wait += (long long)(gtimer() - t0);
     return ok;
 }
 
@@ -573,30 +575,6 @@ __device__ void producer(const Params &p, const Ctx &cx, int qb, int qe) {
 // GEMV instructions
 // ---------------------------------------------------------------------------
 
-// Dot product of one warp-slice of a bf16 row (in shared memory) with the
-// lane's nx input floats. Element e of chunk c of this lane is input index
-// (c*32 + lane)*8 + e of the slice.
-template <int NX>
-__device__ __forceinline__ float dot_row(const uint4 *w, const float *xr) {
-    uint4 wv[NX / 8];
-#pragma unroll
-    for (int c = 0; c < NX / 8; ++c) wv[c] = w[c * 32];
-    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-#pragma unroll
-    for (int c = 0; c < NX / 8; ++c) {
-        const float *x = xr + c * 8;
-        a0 = fmaf(bf_lo(wv[c].x), x[0], a0);
-        a1 = fmaf(bf_lo(wv[c].y), x[2], a1);
-        a2 = fmaf(bf_lo(wv[c].z), x[4], a2);
-        a3 = fmaf(bf_lo(wv[c].w), x[6], a3);
-        a0 = fmaf(bf_hi(wv[c].x), x[1], a0);
-        a1 = fmaf(bf_hi(wv[c].y), x[3], a1);
-        a2 = fmaf(bf_hi(wv[c].z), x[5], a2);
-        a3 = fmaf(bf_hi(wv[c].w), x[7], a3);
-    }
-    return (a0 + a1) + (a2 + a3);
-}
-
 // Polls this thread's nc chunks of 8 tagged elements (chunk c at element
 // (c*256 + tid)*8 of src) with all loads of a poll in flight together, then
 // stores them to xbuf. Returns false on abort/timeout.
@@ -620,7 +598,9 @@ __device__ __forceinline__ bool stage_chunks(const Params &p, const Ctx &cx, con
 }
 
 // Two rows at once: both rows' weights are loaded before any FMA so the two
-// dependent chains overlap.
+// dependent chains overlap. Element e of chunk c of this lane is input index
+// (c*32 + lane)*8 + e of the warp's K-slice; each 32-bit weight word holds
+// elements (2k, 2k+1), multiplied as a pair with one packed fp32 FMA.
 template <int NX>
 __device__ __forceinline__ void dot_rows2(const uint4 *wa, const uint4 *wb, const float *xr,
                                           float &ra, float &rb) {
@@ -630,29 +610,22 @@ __device__ __forceinline__ void dot_rows2(const uint4 *wa, const uint4 *wb, cons
         va[c] = wa[c * 32];
         vb[c] = wb[c * 32];
     }
-    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f, b0 = 0.f, b1 = 0.f, b2 = 0.f, b3 = 0.f;
+    float2 a[4], b[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) a[k] = b[k] = make_float2(0.f, 0.f);
 #pragma unroll
     for (int c = 0; c < NX / 8; ++c) {
-        const float *x = xr + c * 8;
-        a0 = fmaf(bf_lo(va[c].x), x[0], a0);
-        b0 = fmaf(bf_lo(vb[c].x), x[0], b0);
-        a1 = fmaf(bf_lo(va[c].y), x[2], a1);
-        b1 = fmaf(bf_lo(vb[c].y), x[2], b1);
-        a2 = fmaf(bf_lo(va[c].z), x[4], a2);
-        b2 = fmaf(bf_lo(vb[c].z), x[4], b2);
-        a3 = fmaf(bf_lo(va[c].w), x[6], a3);
-        b3 = fmaf(bf_lo(vb[c].w), x[6], b3);
-        a0 = fmaf(bf_hi(va[c].x), x[1], a0);
-        b0 = fmaf(bf_hi(vb[c].x), x[1], b0);
-        a1 = fmaf(bf_hi(va[c].y), x[3], a1);
-        b1 = fmaf(bf_hi(vb[c].y), x[3], b1);
-        a2 = fmaf(bf_hi(va[c].z), x[5], a2);
-        b2 = fmaf(bf_hi(vb[c].z), x[5], b2);
-        a3 = fmaf(bf_hi(va[c].w), x[7], a3);
-        b3 = fmaf(bf_hi(vb[c].w), x[7], b3);
+        const uint32_t ua[4] = {va[c].x, va[c].y, va[c].z, va[c].w};
+        const uint32_t ub[4] = {vb[c].x, vb[c].y, vb[c].z, vb[c].w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float2 x2 = make_float2(xr[c * 8 + 2 * k], xr[c * 8 + 2 * k + 1]);
+            a[k] = __ffma2_rn(make_float2(bf_lo(ua[k]), bf_hi(ua[k])), x2, a[k]);
+            b[k] = __ffma2_rn(make_float2(bf_lo(ub[k]), bf_hi(ub[k])), x2, b[k]);
+        }
     }
-    ra = (a0 + a1) + (a2 + a3);
-    rb = (b0 + b1) + (b2 + b3);
+    ra = ((a[0].x + a[0].y) + (a[1].x + a[1].y)) + ((a[2].x + a[2].y) + (a[3].x + a[3].y));
+    rb = ((b[0].x + b[0].y) + (b[1].x + b[1].y)) + ((b[2].x + b[2].y) + (b[3].x + b[3].y));
 }
 
 // Warp sums of two values at once: after the call lanes 0-15 hold the sum of
@@ -798,56 +771,68 @@ __device__ void gemv_instr(const Params &p, const Ctx &cx, const Instr &in, cons
         }
     }
     phase_stamp(p, cx, 0);
-    // tiles
+    // Tiles. Warp (rg, ks) owns rows rg*M .. rg*M+M-1 of every tile (M = 64/NX
+    // for every geometry the host plans) and K-slice ks. Everything the loop
+    // needs is copied into registers first: values read through `p` or `g`
+    // live in shared memory and would be reloaded after every barrier op.
+    constexpr int M = 64 / NX;
+    const int sw = g.sw;
     const int per = gu ? g.rt / 2 : g.rt;
     const int nt = (n + per - 1) / per;
-    const size_t row_bytes = (size_t)g.K * 2;
-    for (int j = 0; j < nt; ++j, ++t) {
-        const int pg = t % kPages;
-        if (!bad && !wait_tile(p, cx, t)) bad = true;
-        if (!bad) {
-            const uint8_t *page = cx.pages + (size_t)pg * kPageBytes;
-            // this warp's rows of the tile, two at a time
-            for (int mi = 0; mi < g.m; mi += 2) {
-                int out_i[2];
-                bool valid[2];
+    const int row_u4 = g.K / 8;  // 16-byte chunks per row
+    const bool tracing = p.trace != nullptr;
+    const uint4 *pages = reinterpret_cast<const uint4 *>(cx.pages);
+    const int woff = rg * M * row_u4 + sbase / 8 + lane;
+    const bool second = (lane & 16) != 0;  // lanes 16-31 hold the second row's sum
+    // row r of a tile is output row j*per + roff[r] (+ n for the up half of a gate/up tile)
+    int roff[M], obase[M];
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int r = rg * g.m + mi + h;  // row of the tile
-                    if (mi + h >= g.m) {
-                        valid[h] = false;
-                        out_i[h] = 0;
-                    } else if (gu) {
-                        const int up = r >= per;
-                        const int rr = j * per + (up ? r - per : r);
-                        valid[h] = rr < n;
-                        out_i[h] = up ? n + rr : rr;
-                    } else {
-                        out_i[h] = j * per + r;
-                        valid[h] = out_i[h] < n;
-                    }
-                }
-                if (!valid[0] && !valid[1]) continue;
-                const int r0t = rg * g.m + mi;
-                const uint4 *wa = reinterpret_cast<const uint4 *>(page + r0t * row_bytes) + (sbase / 8) + lane;
-                // an invalid second row reads the first row again (in bounds)
-                const uint4 *wb = valid[1] ? reinterpret_cast<const uint4 *>(page + (r0t + 1) * row_bytes) +
-                                                 (sbase / 8) + lane
-                                           : wa;
-                const bool ok = CHKS(wa, 16, 44) && CHKS(wa + (NX / 8 - 1) * 32, 16, 45) &&
-                                CHKS(wb, 16, 44) && CHKS(wb + (NX / 8 - 1) * 32, 16, 45);
+    for (int q = 0; q < M; ++q) {
+        const int r = rg * M + q;
+        const bool up = gu && r >= per;
+        roff[q] = up ? r - per : r;
+        obase[q] = up ? n : 0;
+    }
+    int pg = (int)(t % kPages);
+    uint32_t par = (t / kPages) & 1u;
+    for (int j = 0; j < nt; ++j) {
+        if (!bad && !wait_tile(p, cx, pg, par, tracing)) bad = true;
+        bad = __any_sync(0xFFFFFFFFu, bad);  // warp-uniform from here on
+        bool released = false;
+        if (!bad) {
+            const uint4 *page = pages + pg * (kPageBytes / 16) + woff;
+#pragma unroll
+            for (int q = 0; q < M; q += 2) {
+                const int row0 = j * per + roff[q], row1 = j * per + roff[q + 1];
+                const bool v0 = row0 < n, v1 = row1 < n;
+                if (!v0 && !v1) continue;
+                const uint4 *wa = page + q * row_u4;
+                const uint4 *wb = v1 ? wa + row_u4 : wa;  // an invalid second row re-reads the first
                 float ra = 0.f, rb = 0.f;
-                if (ok) dot_rows2<NX>(wa, wb, xr, ra, rb);
-                const float v = warp_sum2(ra, rb);
-                // lanes 0-15 hold the first row's sum, 16-31 the second's
-                const bool second = (lane & 16) != 0;
-                const bool vh = second ? valid[1] : valid[0];
-                const int oh = second ? out_i[1] : out_i[0];
-                if ((lane & 15) == 0 && vh && CHKS(red + oh * g.sw + ks, 4, 46)) red[oh * g.sw + ks] = v;
+                if (CHKS(wa, 16, 44) && CHKS(wa + (NX / 8 - 1) * 32, 16, 45) && CHKS(wb, 16, 44) &&
+                    CHKS(wb + (NX / 8 - 1) * 32, 16, 45))
+                    dot_rows2<NX>(wa, wb, xr, ra, rb);
+                // with one row pair per warp the page is free once the weights are in registers
+                if (M == 2) {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&cx.empty[pg]);
+                    released = true;
+                }
+                const float sum = warp_sum2(ra, rb);
+                const bool vh = second ? v1 : v0;
+                const int oh = second ? obase[q + 1] + row1 : obase[q] + row0;
+                if ((lane & 15) == 0 && vh && CHKS(red + oh * sw + ks, 4, 46)) red[oh * sw + ks] = sum;
             }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&cx.empty[pg]);
+        if (!released) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&cx.empty[pg]);
+        }
+        ++t;
+        if (++pg == kPages) {
+            pg = 0;
+            par ^= 1u;
+        }
     }
 }
 
@@ -1139,7 +1124,7 @@ __device__ void do_attn_hd(const Params &p, const Ctx &cx, const Instr &in, uint
     const int nt = (r.t1 - r.t0 + p.ppt - 1) / p.ppt;
     for (int j = 0; j < nt; ++j, ++t) {
         const int pg = t % kPages;
-        if (!bad && !wait_tile(p, cx, t)) bad = true;
+        if (!bad && !wait_tile(p, cx, pg, (t / kPages) & 1, p.trace != nullptr)) bad = true;
         const int chunk = warp - (j % SLOTS) * CPT;
         if (!bad && chunk >= 0 && chunk < CPT) {
             const int ts = r.t0 + j * p.ppt;
