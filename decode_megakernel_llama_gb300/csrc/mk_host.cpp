@@ -209,32 +209,38 @@ int build_plan(const mk_config *c, int n_sm, Plan &P) {
                 excluded[order[i]] = 1;
             }
         }
-        // ---- QKV: rows of [Wq; Wk; Wv]
+        // ---- QKV: rows of the stacked [Wq; Wk; Wv] (an instruction may span
+        // two of the matrices; its tiles are copied from both)
         std::vector<int> touch(Hkv, 0);
-        const int mat_start[4] = {0, qd, qd + kvd, qd + 2 * kvd};
+        auto group_of = [&](int row) {  // kv group whose attention reads stacked row `row`
+            if (row < qd) return (row / hd) / G;
+            if (row < qd + kvd) return (row - qd) / hd;
+            return (row - qd - kvd) / hd;
+        };
         for (const Chunk &ch : split_rows(qd + 2 * kvd, 2.0 * d, load, cap_qkv,
                                           dedicated_attn ? &excluded : nullptr)) {
-            int r = ch.r0, end = ch.r0 + ch.n;
-            while (r < end) {
-                int mat = r < mat_start[1] ? 0 : (r < mat_start[2] ? 1 : 2);
-                int e = std::min(end, mat_start[mat + 1]);
-                Instr in = mk_instr(mk::OP_QKV, l, st);
-                in.mat = mat;
-                in.a0 = r - mat_start[mat];
-                in.a1 = e - r;
-                int h0 = in.a0 / hd, h1 = (in.a0 + in.a1 - 1) / hd;
-                int g0 = mat == 0 ? h0 / G : h0, g1 = mat == 0 ? h1 / G : h1;
-                in.sig_ctr = cl.qkv_grp + l * Hkv + g0;
-                in.sig_n = g1 - g0 + 1;
-                for (int g = g0; g <= g1; ++g) touch[g] += 1;
-                if (l > 0) {
-                    in.wait_ctr = cl.down_done + (l - 1);
-                    in.wait_target = prev_down;
+            Instr in = mk_instr(mk::OP_QKV, l, st);
+            in.mat = 0;
+            in.a0 = ch.r0;
+            in.a1 = ch.n;
+            std::vector<char> hit(Hkv, 0);
+            for (int r = ch.r0; r < ch.r0 + ch.n; ++r) hit[group_of(r)] = 1;
+            int g0 = Hkv, g1 = -1;
+            for (int g = 0; g < Hkv; ++g)
+                if (hit[g]) {
+                    g0 = std::min(g0, g);
+                    g1 = std::max(g1, g);
                 }
-                set_bytes(in, 2ll * in.a1 * d);
-                P.q[ch.sm].push_back(in);
-                r = e;
+            // signal every group in [g0, g1] (a span crossing matrices may cover extra groups)
+            in.sig_ctr = cl.qkv_grp + l * Hkv + g0;
+            in.sig_n = g1 - g0 + 1;
+            for (int g = g0; g <= g1; ++g) touch[g] += 1;
+            if (l > 0) {
+                in.wait_ctr = cl.down_done + (l - 1);
+                in.wait_target = prev_down;
             }
+            set_bytes(in, 2ll * in.a1 * d);
+            P.q[ch.sm].push_back(in);
         }
         // ---- attention: Hkv x S splits
         for (int h = 0; h < Hkv; ++h)

@@ -321,7 +321,10 @@ __device__ __forceinline__ bool ll_read_n(const Params &p, const uint2 *const *s
 }
 
 // Waits for NC chunks of 8 tagged elements, chunk c at base + c*stride
-// (16-byte aligned), all loads of a poll in flight together.
+// (16-byte aligned), all loads of a poll in flight together. While the
+// producers are still running it polls a single word (the thread's last
+// element) so that waiting CTAs put one 8-byte load per thread and round on
+// L2 instead of their whole slice.
 template <int NC>
 __device__ __forceinline__ bool ll_read_chunks(const Params &p, const uint2 *base, int stride,
                                                uint32_t tag, float *out) {
@@ -329,6 +332,9 @@ __device__ __forceinline__ bool ll_read_chunks(const Params &p, const uint2 *bas
     for (int c = 0; c < NC; ++c)
         if (!CHK(base + (size_t)c * stride, 64, 38)) return false;
     Spin sp;
+    const uint2 *sentinel = base + (size_t)(NC - 1) * stride + 7;
+    while (ll_ld8(sentinel).y != tag)
+        if (!sp.keep_going(p)) return false;
     while (true) {
         uint4 v[NC * 4];
 #pragma unroll
@@ -375,6 +381,11 @@ __device__ __forceinline__ bool wait_tile(const Params &p, const Ctx &cx, int pg
 // Trace stamp of an intra-instruction phase (thread 0, traced steps only).
 __device__ __forceinline__ void phase_stamp(const Params &p, const Ctx &cx, int k) {
     if (p.trace && threadIdx.x == 0) cx.misc->phase[k] = (long long)gtimer();
+}
+
+// Pulls the 64-byte record of instruction i into L1 ahead of its load_instr.
+__device__ __forceinline__ void prefetch_instr(const Params &p, int i) {
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(p.instr + i));
 }
 
 __device__ __forceinline__ Instr load_instr(const Params &p, int i) {
@@ -490,9 +501,23 @@ __device__ __forceinline__ TileCopy tile_copy(const Params &p, const Instr &in, 
             c.bytes1 = c.bytes0;
             c.dst1 = (uint32_t)per * g.K * 2;
             break;
-        case OP_QKV:
-            c.src0 = (in.mat == 0 ? lw->wq : (in.mat == 1 ? lw->wk : lw->wv)) + row0 * g.K;
+        case OP_QKV: {
+            // rows of the stacked [Wq; Wk; Wv]; a tile crosses at most one boundary
+            const size_t qd = (size_t)p.Hq * p.hd, kvd = (size_t)p.Hkv * p.hd;
+            const size_t end = row0 + (size_t)rows;
+            const int m0 = row0 < qd ? 0 : (row0 < qd + kvd ? 1 : 2);
+            const size_t start0 = m0 == 0 ? 0 : (m0 == 1 ? qd : qd + kvd);
+            const size_t bound = m0 == 0 ? qd : (m0 == 1 ? qd + kvd : qd + 2 * kvd);
+            const uint16_t *mats[3] = {lw->wq, lw->wk, lw->wv};
+            c.src0 = mats[m0] + (row0 - start0) * g.K;
+            if (end > bound && m0 < 2) {
+                c.bytes0 = (uint32_t)((bound - row0) * g.K * 2);
+                c.src1 = mats[m0 + 1];
+                c.bytes1 = (uint32_t)((end - bound) * g.K * 2);
+                c.dst1 = c.bytes0;
+            }
             break;
+        }
         case OP_OPROJ: c.src0 = lw->wo + row0 * g.K; break;
         case OP_DOWN: c.src0 = lw->w_down + row0 * g.K; break;
         default: c.src0 = p.embed + row0 * g.K; break;
@@ -543,6 +568,7 @@ __device__ void producer(const Params &p, const Ctx &cx, int qb, int qe) {
     const uint32_t back = (uint32_t)p.max_inflight;
     for (int i = qb; i < qe; ++i) {
         const Instr in = load_instr(p, i);
+        if (i + 1 < qe) prefetch_instr(p, i + 1);
         const int nt = num_tiles(p, in);
         for (int j = 0; j < nt; ++j, ++t) {
             const int pg = t % kPages;
@@ -855,8 +881,7 @@ __device__ void do_gemv(const Params &p, const Ctx &cx, const Instr &in, uint32_
     const float *red = in.op == OP_DOWN ? cx.dred : cx.red;
     switch (in.op) {
         case OP_QKV: {
-            uint2 *dst = p.qkvll + (size_t)l * (p.Hq + 2 * p.Hkv) * p.hd +
-                         (in.mat == 0 ? 0 : (in.mat == 1 ? p.Hq * p.hd : (p.Hq + p.Hkv) * p.hd)) + r0;
+            uint2 *dst = p.qkvll + (size_t)l * (p.Hq + 2 * p.Hkv) * p.hd + r0;  // stacked q | k | v
             for (int i = tid; i < n; i += kConsumerThreads) {
                 float v = 0.f;
                 for (int s = 0; s < sw; ++s) v += red[i * sw + s];
@@ -910,14 +935,30 @@ __device__ void do_gemv(const Params &p, const Ctx &cx, const Instr &in, uint32_
                 // the last LM-head instruction to arrive reduces all block maxima
                 const uint32_t old = CHK(p.ctr + p.cl.lm_arrive, 4, 31)
                                          ? atom_acq_rel_add(p.ctr + p.cl.lm_arrive, 1u) : 0u;
-                if (old == (uint32_t)p.n_lm - 1u) {
-                    unsigned long long g2 = 0ull;
-                    for (int s = 0; s < p.n_lm; ++s) {
-                        const unsigned long long v = CHK(p.lm_part + s, 8, 20) ? __ldcg(p.lm_part + s) : 0ull;
-                        g2 = v > g2 ? v : g2;
-                    }
+                const bool last = old == (uint32_t)p.n_lm - 1u;
+                if (last) __threadfence();
+                cx.misc->flag = last ? 1 : 0;
+            }
+            consumer_sync();
+            if (cx.misc->flag) {
+                // all consumer threads load the block maxima at once
+                unsigned long long g2 = 0ull;
+                for (int s = tid; s < p.n_lm; s += kConsumerThreads) {
+                    const unsigned long long v = CHK(p.lm_part + s, 8, 20) ? __ldcg(p.lm_part + s) : 0ull;
+                    g2 = v > g2 ? v : g2;
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    const unsigned long long other = __shfl_xor_sync(0xFFFFFFFFu, g2, o);
+                    g2 = other > g2 ? other : g2;
+                }
+                if ((tid & 31) == 0) cx.misc->best8[warp] = g2;
+                consumer_sync();
+                if (tid == 0) {
+                    unsigned long long b = 0ull;
+                    for (int w = 0; w < kConsumerWarps; ++w) b = cx.misc->best8[w] > b ? cx.misc->best8[w] : b;
                     if (CHK(p.out_token, 4, 21))
-                        *p.out_token = (int32_t)(0xFFFFFFFFu - (uint32_t)(g2 & 0xFFFFFFFFull));
+                        *p.out_token = (int32_t)(0xFFFFFFFFu - (uint32_t)(b & 0xFFFFFFFFull));
                 }
             }
             break;
@@ -1284,6 +1325,7 @@ __device__ void consumer(const Params &p, const Ctx &cx, int qb, int qe, int q0)
     long long *trace = p.trace ? p.trace + (size_t)blockIdx.x * p.trace_cap * kTraceWords : nullptr;
     for (int i = qb; i < qe && !bad; ++i) {
         const Instr in = load_instr(p, i);
+        if (i + 1 < qe) prefetch_instr(p, i + 1);
         const uint64_t ts = trace ? gtimer() : 0;
         if (trace && tid == 0) {
             cx.misc->phase[0] = cx.misc->phase[1] = cx.misc->phase[2] = (long long)ts;

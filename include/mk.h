@@ -199,8 +199,10 @@ int mk_plan_size(const mk_handle *h, int32_t *n_sm, int32_t *n_instr);
  *   {op, layer, a0, a1, mat, wait_ctr, wait_target, sig_ctr, sig_n, stage,
  *    slot, bytes_lo, bytes_hi, 0, 0, 0}
  * op: 1 QKV, 2 ATTN, 3 OPROJ, 4 GATEUP, 5 DOWN, 6 LMHEAD. For GEMV ops
- * a0/a1 = first row / row count (QKV rows within matrix `mat`: 0 q, 1 k, 2 v);
- * for ATTN a0 = kv head, a1 = split index. wait_ctr < 0: no wait.        */
+ * a0/a1 = first row / row count (QKV rows of the stacked [Wq; Wk; Wv],
+ * mat = 0); for ATTN a0 = kv head, a1 = split index. The wait/signal fields
+ * describe the dependency DAG as counts (wait_ctr < 0: no wait); the kernel
+ * itself waits on the tagged activation words those producers write.    */
 #define MK_INSTR_WORDS 16
 int mk_plan_inspect(const mk_config *config, int32_t n_sm, int32_t *out_instr, int32_t cap,
                     int32_t *out_queue_len, int32_t *out_n_counters);

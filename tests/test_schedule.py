@@ -49,21 +49,18 @@ def cover(intervals, total):
 def test_every_output_row_exactly_once(shape, n_sm, max_seq):
     instr, _, _ = plan(shape, n_sm, max_seq)
     hd = shape.head_dim
-    rows = {0: shape.n_heads * hd, 1: shape.n_kv_heads * hd, 2: shape.n_kv_heads * hd}
+    stacked = (shape.n_heads + 2 * shape.n_kv_heads) * hd  # rows of [Wq; Wk; Wv]
     by = defaultdict(list)
     for r in instr:
         op, l = int(r[F_OP]), int(r[F_LAYER])
-        if op == OP_QKV:
-            by[(op, l, int(r[F_MAT]))].append((int(r[F_A0]), int(r[F_A1])))
-        elif op == OP_ATTN:
+        if op == OP_ATTN:
             by[(op, l, int(r[F_A0]))].append((int(r[F_A1]), 1))
         else:
             by[(op, l)].append((int(r[F_A0]), int(r[F_A1])))
     S = len(by[(OP_ATTN, 0, 0)])
     assert S >= 1
     for l in range(shape.n_layers):
-        for m in range(3):
-            cover(by[(OP_QKV, l, m)], rows[m])
+        cover(by[(OP_QKV, l)], stacked)
         for h in range(shape.n_kv_heads):
             cover(by[(OP_ATTN, l, h)], S)
         cover(by[(OP_OPROJ, l)], shape.d_model)
@@ -203,8 +200,7 @@ def test_tile_copies_stay_in_bounds(shape, n_sm, max_seq):
     d, F, hd = shape.d_model, shape.ffn_dim, shape.head_dim
     qd, kvd = shape.n_heads * hd, shape.n_kv_heads * hd
     G = {OP_QKV: geo(d), OP_OPROJ: geo(qd), OP_GATEUP: geo(d), OP_DOWN: geo(F), OP_LMHEAD: geo(d)}
-    mat_rows = {(OP_QKV, 0): qd, (OP_QKV, 1): kvd, (OP_QKV, 2): kvd, (OP_OPROJ, 0): d,
-                (OP_GATEUP, 0): F, (OP_DOWN, 0): d, (OP_LMHEAD, 0): shape.vocab}
+    mat_rows = {OP_QKV: qd + 2 * kvd, OP_OPROJ: d, OP_GATEUP: F, OP_DOWN: d, OP_LMHEAD: shape.vocab}
     assert d <= STAGED and qd <= STAGED and F <= STAGED_LONG
     ppt = (PAGE // 2) // (hd * 2)
     S = sum(1 for r in instr if r[F_OP] == OP_ATTN and r[F_LAYER] == 0 and r[F_A0] == 0)
@@ -224,7 +220,7 @@ def test_tile_copies_stay_in_bounds(shape, n_sm, max_seq):
         per = g["rt"] // 2 if op == OP_GATEUP else g["rt"]
         assert per >= 1 and g["m"] >= 1 and g["nx"] in (8, 16, 24, 32)
         n, a0 = int(r[F_A1]), int(r[F_A0])
-        nrows = mat_rows[(op, int(r[F_MAT]) if op == OP_QKV else 0)]
+        nrows = mat_rows[op]
         nt = -(-n // per)
         for j in range(nt):
             rows = min(per, n - j * per)
@@ -234,6 +230,13 @@ def test_tile_copies_stay_in_bounds(shape, n_sm, max_seq):
             assert (row0 + rows) <= nrows
             dst1 = per * g["K"] * 2 if op == OP_GATEUP else 0
             assert dst1 + nbytes <= PAGE
+            if op == OP_QKV:
+                # a stacked-QKV tile crossing a matrix boundary is two copies
+                for b in (qd, qd + kvd):
+                    if row0 < b < row0 + rows:
+                        assert ((b - row0) * g["K"] * 2) % 16 == 0
+                        assert ((row0 + rows - b) * g["K"] * 2) % 16 == 0
+                assert sum(row0 < b < row0 + rows for b in (qd, qd + kvd)) <= 1
         # per-row partials fit their reduction buffer, residual rows theirs
         outs = 2 * n if op == OP_GATEUP else n
         assert outs * g["sw"] <= (DREDCAP if op == OP_DOWN else REDCAP)
