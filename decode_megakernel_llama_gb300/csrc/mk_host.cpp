@@ -91,7 +91,7 @@ int check_config(const mk_config *c) {
     if (c->n_heads % c->n_kv_heads != 0)
         return fail(MK_ERR_INVALID_ARG, "n_heads must be a multiple of n_kv_heads");
     const int G = c->n_heads / c->n_kv_heads, hd = c->head_dim;
-    if (G > 4 || G * hd + hd + mk::kConsumerWarps * G * (hd + 2) > mk::kXbufFloats)
+    if (G > 4 || G * hd + hd + mk::kConsumerWarps * G * (hd + 4) > mk::kXbufFloats)
         return fail(MK_ERR_UNSUPPORTED, "too many query heads per kv head for the attention scratch");
     const int qd = c->n_heads * hd;
     if (c->d_model % 256 || qd % 256 || c->ffn_dim % 256)

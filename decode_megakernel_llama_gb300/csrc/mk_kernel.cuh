@@ -1,0 +1,1518 @@
+#pragma once
+// mk_kernel.cuh — the persistent decode megakernel (sm_103a), device code.
+// Included by mk_kernel_hd64.cu and mk_kernel_hd128.cu, which instantiate it.
+//
+// One CTA per SM interprets that SM's instruction queue (planned on the host,
+// see mk_host.cpp). The design is the one described in "Revolution der
+// KI-Beschleunigung: Wie ein Low-Latency Megakernel den Llama-1B Turbo
+// zündet" (dasgeld.co), rebuilt for GB300:
+//   * the whole decode step is one launch; stages that used to be separate
+//     kernels are instructions (megakernel paragraphs);
+//   * every instruction waits for exactly the data it consumes through flags
+//     in global memory (synchronisation paragraph): each activation element
+//     is a tagged 8-byte word {value, step/version tag}; consumers poll the
+//     words they read, so an edge costs one round trip and producers never
+//     wait for write acknowledgements;
+//   * shared memory is a ring of pages: a producer warp streams the next
+//     instructions' weights (and cached keys/values) into free pages with
+//     cp.async.bulk while the consumer warps compute, across dependency
+//     waits, so HBM keeps streaming during synchronisation (shared-memory
+//     paging paragraph);
+//   * bf16 weights, fp32 accumulation (latency paragraph).
+//
+// CTA layout: warps 0..7 are consumers (GEMV / attention math), warp 8 lane 0
+// is the producer that issues bulk copies. Page p has a "full" mbarrier
+// (producer -> consumers, completed by the copy's transaction bytes) and an
+// "empty" mbarrier (8 consumer warps -> producer).
+//
+// Every wait is bounded (%globaltimer): on expiry the CTA records a timeout
+// in the status word, raises the abort flag that all CTAs poll, waits for
+// its own copies in flight and returns. Nothing traps. Counters remain only
+// for the LM head's global argmax and for the end of the step.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "mk_plan.h"
+
+namespace mk {
+
+extern __shared__ __align__(1024) uint8_t mk_smem[];
+
+// Everything below has internal linkage: each instance translation unit
+// carries its own copy.
+namespace {
+
+// ---------------------------------------------------------------------------
+// PTX helpers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// Bulk (non-tensor) copy global -> this CTA's shared memory, completing
+// `bytes` transaction bytes on `bar`. 16-byte aligned addresses and size.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar,
+                                         uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(pol)
+        : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_acquire(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void red_release_add(uint32_t *p, uint32_t v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t atom_acq_rel_add(uint32_t *p, uint32_t v) {
+    uint32_t old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;"
+                 : "=r"(old)
+                 : "l"(p), "r"(v)
+                 : "memory");
+    return old;
+}
+
+__device__ __forceinline__ uint64_t gtimer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void consumer_sync() {
+    asm volatile("bar.sync 1, %0;" ::"n"(kConsumerThreads) : "memory");
+}
+
+// Consumer barrier that also returns whether any consumer thread passed
+// `pred` = true, so failure decisions stay uniform across the warps.
+__device__ __forceinline__ bool consumer_sync_any(bool pred) {
+    uint32_t cnt;
+    asm volatile(
+        "{\n\t.reg .pred q;\n\t"
+        "setp.ne.u32 q, %2, 0;\n\t"
+        "bar.red.popc.u32 %0, 1, %1, q;\n\t}"
+        : "=r"(cnt)
+        : "n"(kConsumerThreads), "r"((uint32_t)pred)
+        : "memory");
+    return cnt != 0;
+}
+
+__device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
+__device__ __forceinline__ float bf16f(uint16_t b) { return __uint_as_float(uint32_t(b) << 16); }
+
+// fp32 -> bf16, round to nearest even (finite inputs; NaN kept quiet).
+__device__ __forceinline__ uint16_t f2bf(float f) {
+    uint32_t u = __float_as_uint(f);
+    if ((u & 0x7F800000u) == 0x7F800000u) return uint16_t((u >> 16) | ((u & 0xFFFFu) ? 0x40u : 0u));
+    u += 0x7FFFu + ((u >> 16) & 1u);
+    return uint16_t(u >> 16);
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ float ldcg(const float *p) { return __ldcg(p); }
+
+// ---------------------------------------------------------------------------
+// Address self-checks. A build with MK_CHECKED validates every global access
+// against the byte ranges the host registered (weights, caches, scratch,
+// outputs) and every computed shared-memory access against the CTA's
+// allocation; the first violation is recorded in p.dbg and the access is
+// skipped. Without MK_CHECKED the checks compile to `true`.
+// ---------------------------------------------------------------------------
+
+#ifdef MK_CHECKED
+__device__ __noinline__ void chk_record(const Params &p, int site, uintptr_t a, size_t bytes) {
+    if (p.dbg && atomicCAS(p.dbg, 0ull, (unsigned long long)site) == 0ull) {
+        p.dbg[1] = a;
+        p.dbg[2] = bytes;
+        p.dbg[3] = ((unsigned long long)blockIdx.x << 32) | threadIdx.x;
+        __threadfence();
+    }
+}
+__device__ __noinline__ bool chk_global(const Params &p, const void *ptr, size_t bytes, int site) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(ptr);
+    for (int i = 0; i < p.n_ranges; ++i)
+        if (a >= p.ranges[2 * i] && a + bytes <= p.ranges[2 * i + 1]) return true;
+    if (p.out_logits && a >= (uintptr_t)p.out_logits && a + bytes <= (uintptr_t)(p.out_logits + p.V))
+        return true;
+    if (p.out_token && a >= (uintptr_t)p.out_token && a + bytes <= (uintptr_t)(p.out_token + 1))
+        return true;
+    if (p.d_token && a >= (uintptr_t)p.d_token && a + bytes <= (uintptr_t)(p.d_token + 1))
+        return true;
+    if (p.trace && a >= (uintptr_t)p.trace &&
+        a + bytes <= (uintptr_t)(p.trace + (size_t)gridDim.x * p.trace_cap * kTraceWords))
+        return true;
+    chk_record(p, site, a, bytes);
+    return false;
+}
+__device__ __noinline__ bool chk_shared(const Params &p, const void *ptr, size_t bytes, int site) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(ptr), b = reinterpret_cast<uintptr_t>(mk_smem);
+    if (__isShared(ptr) && a >= b && a + bytes <= b + kSmemBytes) return true;
+    chk_record(p, site, a, bytes);
+    return false;
+}
+#define CHK(ptr, bytes, site) chk_global(p, (ptr), (bytes), (site))
+#define CHKS(ptr, bytes, site) chk_shared(p, (ptr), (bytes), (site))
+#else
+#define CHK(ptr, bytes, site) true
+#define CHKS(ptr, bytes, site) true
+#endif
+
+// Orderable key for the argmax: larger value wins, then lower index.
+__device__ __forceinline__ unsigned long long argmax_key(float v, uint32_t idx) {
+    uint32_t u = __float_as_uint(v);
+    u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    return (static_cast<unsigned long long>(u) << 32) | (0xFFFFFFFFu - idx);
+}
+
+// ---------------------------------------------------------------------------
+// Tagged activation words. Every activation element lives in global memory as
+// {float bits, tag} and is written with ONE relaxed 8-byte store, read with
+// relaxed 8-byte (or paired 8-byte) loads; each 8-byte access is single-copy
+// atomic, so a reader that sees the expected tag sees the value written with
+// it. The tag is (step epoch << 8) | version, so data of an
+// earlier step, or an earlier version of the in-place residual stream, never
+// matches. A consumer therefore needs no counter and no separate acquire:
+// polling the words it consumes is its dependency wait, and a producer never
+// waits for its writes to be acknowledged.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void ll_store(uint2 *dst, float v, uint32_t tag) {
+    const unsigned long long w =
+        ((unsigned long long)tag << 32) | (unsigned long long)__float_as_uint(v);
+    asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(dst), "l"(w) : "memory");
+}
+
+// Two tagged elements; each 64-bit half is read single-copy atomically.
+__device__ __forceinline__ uint4 ll_ld16(const uint2 *src) {
+    unsigned long long a, b;
+    asm volatile("ld.relaxed.gpu.global.v2.b64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(src) : "memory");
+    return make_uint4((uint32_t)a, (uint32_t)(a >> 32), (uint32_t)b, (uint32_t)(b >> 32));
+}
+
+__device__ __forceinline__ uint2 ll_ld8(const uint2 *src) {  // one tagged element
+    unsigned long long a;
+    asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(a) : "l"(src) : "memory");
+    return make_uint2((uint32_t)a, (uint32_t)(a >> 32));
+}
+
+// ---------------------------------------------------------------------------
+// Shared state
+// ---------------------------------------------------------------------------
+struct Misc {
+    float red8[kConsumerWarps];
+    unsigned long long best8[kConsumerWarps];
+    volatile int32_t flag;      // broadcast slot
+    volatile int32_t aborted;   // this CTA gave up
+    volatile uint32_t n_issued; // tiles issued by the producer
+    uint32_t ep8;               // this step's epoch << 8
+    int32_t staged_key;         // (op << 16 | layer) whose input xbuf holds, -1 none
+    float staged_ss;            // its sum of squares
+    long long phase[3];         // trace: intra-instruction phase stamps
+    long long tile_wait;        // trace: ns thread 0 spent waiting for tiles to land
+};
+
+struct Ctx {
+    uint8_t *pages;
+    float *xbuf;
+    float *red;
+    float *resid;
+    float *dred;
+    uint64_t *full, *empty;
+    Misc *misc;
+};
+
+// Bounded spinning: every 16th call checks the abort flag and the clock; on
+// expiry it records a timeout, raises the abort flag and tells the caller to
+// give up.
+struct Spin {
+    uint64_t t0 = 0;
+    uint32_t it = 0;
+    __device__ __forceinline__ bool keep_going(const Params &p) {
+        if ((++it & 15u) != 0) return true;
+        if (*(volatile int32_t *)p.abort_flag) return false;
+        const uint64_t now = gtimer();
+        if (t0 == 0) {
+            t0 = now;
+            return true;
+        }
+        if (now - t0 > p.timeout_ns) {
+            atomicCAS(p.status, DS_OK, DS_TIMEOUT);
+            atomicExch(p.abort_flag, 1);
+            return false;
+        }
+        return true;
+    }
+};
+
+// Waits for one tagged element. Returns false on abort/timeout.
+__device__ __forceinline__ bool ll_read1(const Params &p, const uint2 *src, uint32_t tag, float &out) {
+    if (!CHK(src, 8, 37)) return false;
+    Spin sp;
+    while (true) {
+        const uint2 v = ll_ld8(src);
+        if (v.y == tag) {
+            out = __uint_as_float(v.x);
+            return true;
+        }
+        if (!sp.keep_going(p)) return false;
+    }
+}
+
+// Waits for N independent tagged elements (any addresses), all loads of a
+// poll in flight together. Returns false on abort/timeout.
+template <int N>
+__device__ __forceinline__ bool ll_read_n(const Params &p, const uint2 *const *src, uint32_t tag,
+                                          float *out) {
+#pragma unroll
+    for (int k = 0; k < N; ++k)
+        if (!CHK(src[k], 8, 37)) return false;
+    Spin sp;
+    while (true) {
+        uint2 v[N];
+#pragma unroll
+        for (int k = 0; k < N; ++k) v[k] = ll_ld8(src[k]);
+        bool ok = true;
+#pragma unroll
+        for (int k = 0; k < N; ++k) ok = ok && v[k].y == tag;
+        if (ok) {
+#pragma unroll
+            for (int k = 0; k < N; ++k) out[k] = __uint_as_float(v[k].x);
+            return true;
+        }
+        if (!sp.keep_going(p)) return false;
+    }
+}
+
+// Waits for NC chunks of 8 tagged elements, chunk c at base + c*stride
+// (16-byte aligned), all loads of a poll in flight together. While the
+// producers are still running it polls a single word (the thread's last
+// element) so that waiting CTAs put one 8-byte load per thread and round on
+// L2 instead of their whole slice.
+template <int NC>
+__device__ __forceinline__ bool ll_read_chunks(const Params &p, const uint2 *base, int stride,
+                                               uint32_t tag, float *out) {
+#pragma unroll
+    for (int c = 0; c < NC; ++c)
+        if (!CHK(base + (size_t)c * stride, 64, 38)) return false;
+    Spin sp;
+    const uint2 *sentinel = base + (size_t)(NC - 1) * stride + 7;
+    while (ll_ld8(sentinel).y != tag)
+        if (!sp.keep_going(p)) return false;
+    while (true) {
+        uint4 v[NC * 4];
+#pragma unroll
+        for (int c = 0; c < NC; ++c)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) v[c * 4 + k] = ll_ld16(base + (size_t)c * stride + 2 * k);
+        bool ok = true;
+#pragma unroll
+        for (int k = 0; k < NC * 4; ++k) ok = ok && v[k].y == tag && v[k].w == tag;
+        if (ok) {
+#pragma unroll
+            for (int k = 0; k < NC * 4; ++k) {
+                out[2 * k] = __uint_as_float(v[k].x);
+                out[2 * k + 1] = __uint_as_float(v[k].z);
+            }
+            return true;
+        }
+        if (!sp.keep_going(p)) return false;
+    }
+}
+
+// Bounded wait on an mbarrier phase.
+__device__ bool wait_bar(const Params &p, uint64_t *bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    Spin sp;
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (!sp.keep_going(p)) return false;
+    }
+}
+
+// Consumer wait for page pg to be full in the phase of parity par; on traced
+// steps thread 0 adds the time it waited to the instruction's tile_wait.
+__device__ __forceinline__ bool wait_tile(const Params &p, const Ctx &cx, int pg, uint32_t par,
+                                          bool tracing) {
+    if (!tracing) return wait_bar(p, &cx.full[pg], par);
+    uint64_t t0 = 0;
+    if (threadIdx.x == 0) t0 = gtimer();
+    const bool ok = wait_bar(p, &cx.full[pg], par);
+    if (threadIdx.x == 0) cx.misc->tile_wait += (long long)(gtimer() - t0);
+    return ok;
+}
+
+// Trace stamp of an intra-instruction phase (thread 0, traced steps only).
+__device__ __forceinline__ void phase_stamp(const Params &p, const Ctx &cx, int k) {
+    if (p.trace && threadIdx.x == 0) cx.misc->phase[k] = (long long)gtimer();
+}
+
+// Pulls the 64-byte record of instruction i into L1 ahead of its load_instr.
+__device__ __forceinline__ void prefetch_instr(const Params &p, int i) {
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(p.instr + i));
+}
+
+__device__ __forceinline__ Instr load_instr(const Params &p, int i) {
+    Instr in;
+    if (!CHK(p.instr + i, sizeof(Instr), 1)) {
+        memset(&in, 0, sizeof in);
+        in.wait_ctr = -1;
+        in.op = OP_QKV;
+        return in;
+    }
+    const int4 *src = reinterpret_cast<const int4 *>(p.instr + i);
+    int4 *dst = reinterpret_cast<int4 *>(&in);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) dst[k] = __ldg(src + k);
+    return in;
+}
+
+__device__ __forceinline__ const Geo &geo_of(const Params &p, int op) {
+    switch (op) {
+        case OP_QKV: return p.geo_qkv;
+        case OP_OPROJ: return p.geo_o;
+        case OP_GATEUP: return p.geo_gu;
+        case OP_DOWN: return p.geo_down;
+        default: return p.geo_lm;
+    }
+}
+
+__device__ __forceinline__ int current_token(const Params &p) {
+    if (p.d_token && !CHK(p.d_token, 4, 33)) return -1;
+    return p.d_token ? *(volatile const int32_t *)p.d_token : p.token;
+}
+
+// ---------------------------------------------------------------------------
+// Attention split bookkeeping (identical on producer and consumer side).
+// Cached positions [0, pos) are cut into seff <= S contiguous chunks of at
+// least one tile; the last active split also owns the new position `pos`
+// and merges the splits.
+// ---------------------------------------------------------------------------
+struct AttnRange {
+    int active, t0, t1, has_new;
+};
+
+__device__ __forceinline__ int attn_seff(const Params &p) {
+    const int per = p.ppt * kMinSplitTiles;
+    int need = (p.pos + per - 1) / per;
+    if (need < 1) need = 1;
+    return need < p.S ? need : p.S;
+}
+
+__device__ __forceinline__ AttnRange attn_range(const Params &p, int split) {
+    AttnRange r;
+    const int seff = attn_seff(p);
+    r.active = split < seff;
+    const int chunk = (p.pos + seff - 1) / seff;
+    r.t0 = split * chunk;
+    if (r.t0 > p.pos) r.t0 = p.pos;
+    r.t1 = r.t0 + chunk;
+    if (r.t1 > p.pos) r.t1 = p.pos;
+    r.has_new = (split == seff - 1);
+    return r;
+}
+
+__device__ __forceinline__ int num_tiles(const Params &p, const Instr &in) {
+    if (in.op == OP_ATTN) {
+        const AttnRange r = attn_range(p, in.a1);
+        if (!r.active) return 0;
+        return (r.t1 - r.t0 + p.ppt - 1) / p.ppt;
+    }
+    const Geo &g = geo_of(p, in.op);
+    const int per = (in.op == OP_GATEUP) ? g.rt / 2 : g.rt;
+    return (in.a1 + per - 1) / per;
+}
+
+// ---------------------------------------------------------------------------
+// Tile copies: tile j of an instruction is one or two contiguous global
+// ranges copied into one page.
+// ---------------------------------------------------------------------------
+struct TileCopy {
+    const void *src0, *src1;
+    uint32_t bytes0, bytes1;  // bytes1 == 0: single copy
+    uint32_t dst1;            // page offset of the second copy
+};
+
+__device__ __forceinline__ TileCopy tile_copy(const Params &p, const Instr &in, int j) {
+    TileCopy c;
+    c.src1 = nullptr;
+    c.bytes1 = 0;
+    c.dst1 = 0;
+    if (in.op == OP_ATTN) {
+        const AttnRange r = attn_range(p, in.a1);
+        const int ts = r.t0 + j * p.ppt;
+        int n = r.t1 - ts;
+        if (n > p.ppt) n = p.ppt;
+        const size_t base = ((size_t)(in.layer * p.max_batch) * p.Hkv + in.a0) * p.max_seq * p.hd +
+                            (size_t)ts * p.hd;
+        c.bytes0 = c.bytes1 = (uint32_t)n * p.hd * 2;
+        c.src0 = p.kc + base;
+        c.src1 = p.vc + base;
+        c.dst1 = kPageBytes / 2;
+        return c;
+    }
+    const Geo &g = geo_of(p, in.op);
+    const int per = (in.op == OP_GATEUP) ? g.rt / 2 : g.rt;
+    int rows = in.a1 - j * per;
+    if (rows > per) rows = per;
+    const size_t row0 = (size_t)in.a0 + (size_t)j * per;
+    const LayerW *lw = p.layers + in.layer;
+    c.bytes0 = (uint32_t)rows * g.K * 2;
+    switch (in.op) {
+        case OP_GATEUP:
+            c.src0 = lw->w_gate + row0 * g.K;
+            c.src1 = lw->w_up + row0 * g.K;
+            c.bytes1 = c.bytes0;
+            c.dst1 = (uint32_t)per * g.K * 2;
+            break;
+        case OP_QKV: {
+            // rows of the stacked [Wq; Wk; Wv]; a tile crosses at most one boundary
+            const size_t qd = (size_t)p.Hq * p.hd, kvd = (size_t)p.Hkv * p.hd;
+            const size_t end = row0 + (size_t)rows;
+            const int m0 = row0 < qd ? 0 : (row0 < qd + kvd ? 1 : 2);
+            const size_t start0 = m0 == 0 ? 0 : (m0 == 1 ? qd : qd + kvd);
+            const size_t bound = m0 == 0 ? qd : (m0 == 1 ? qd + kvd : qd + 2 * kvd);
+            const uint16_t *mats[3] = {lw->wq, lw->wk, lw->wv};
+            c.src0 = mats[m0] + (row0 - start0) * g.K;
+            if (end > bound && m0 < 2) {
+                c.bytes0 = (uint32_t)((bound - row0) * g.K * 2);
+                c.src1 = mats[m0 + 1];
+                c.bytes1 = (uint32_t)((end - bound) * g.K * 2);
+                c.dst1 = c.bytes0;
+            }
+            break;
+        }
+        case OP_OPROJ: c.src0 = lw->wo + row0 * g.K; break;
+        case OP_DOWN: c.src0 = lw->w_down + row0 * g.K; break;
+        default: c.src0 = p.embed + row0 * g.K; break;
+    }
+    return c;
+}
+
+__device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Producer: walks the same queue as the consumers and issues every tile into
+// the page ring. Optionally a second cursor prefetches tiles up to
+// p.l2_lookahead bytes beyond the ring into L2.
+// ---------------------------------------------------------------------------
+struct PrefetchCursor {
+    int i, j, nt;
+    unsigned long long bytes;  // bytes of all tiles before (i, j)
+};
+
+__device__ void prefetch_until(const Params &p, PrefetchCursor &pc, int qe, unsigned long long limit,
+                               unsigned long long filled) {
+    while (pc.i < qe && pc.bytes < limit) {
+        if (pc.j >= pc.nt) {
+            ++pc.i;
+            pc.j = 0;
+            if (pc.i < qe) pc.nt = num_tiles(p, load_instr(p, pc.i));
+            continue;
+        }
+        const Instr in = load_instr(p, pc.i);
+        const TileCopy c = tile_copy(p, in, pc.j);
+        if (pc.bytes >= filled) {  // tiles already in the ring need no prefetch
+            if (CHK(c.src0, c.bytes0, 35)) prefetch_l2(c.src0, c.bytes0);
+            if (c.bytes1 && CHK(c.src1, c.bytes1, 36)) prefetch_l2(c.src1, c.bytes1);
+        }
+        pc.bytes += c.bytes0 + c.bytes1;
+        ++pc.j;
+    }
+}
+
+__device__ void producer(const Params &p, const Ctx &cx, int qb, int qe) {
+    const uint64_t pol = policy_evict_first();
+    const unsigned long long la = p.l2_lookahead;
+    PrefetchCursor pc{qb, 0, qb < qe ? num_tiles(p, load_instr(p, qb)) : 0, 0ull};
+    unsigned long long filled = 0;  // bytes issued into the ring
+    uint32_t t = 0;
+    const uint32_t back = (uint32_t)p.max_inflight;
+    for (int i = qb; i < qe; ++i) {
+        const Instr in = load_instr(p, i);
+        if (i + 1 < qe) prefetch_instr(p, i + 1);
+        const int nt = num_tiles(p, in);
+        for (int j = 0; j < nt; ++j, ++t) {
+            const int pg = t % kPages;
+            if (la) prefetch_until(p, pc, qe, filled + la, filled);
+            if (t >= kPages && !wait_bar(p, &cx.empty[pg], ((t / kPages) - 1) & 1)) {
+                cx.misc->aborted = 1;
+                return;
+            }
+            // at most `back` tiles in flight
+            if (t >= back && !wait_bar(p, &cx.full[(t - back) % kPages], ((t - back) / kPages) & 1)) {
+                cx.misc->aborted = 1;
+                return;
+            }
+            uint8_t *dst = cx.pages + (size_t)pg * kPageBytes;
+            const TileCopy c = tile_copy(p, in, j);
+            const bool ok = CHK(c.src0, c.bytes0, 3) && (!c.bytes1 || CHK(c.src1, c.bytes1, 4)) &&
+                            CHKS(dst, c.bytes0, 40) && (!c.bytes1 || CHKS(dst + c.dst1, c.bytes1, 41));
+            mbar_expect_tx(&cx.full[pg], ok ? c.bytes0 + c.bytes1 : 0u);
+            if (ok) {
+                bulk_g2s(dst, c.src0, c.bytes0, &cx.full[pg], pol);
+                if (c.bytes1) bulk_g2s(dst + c.dst1, c.src1, c.bytes1, &cx.full[pg], pol);
+            }
+            filled += c.bytes0 + c.bytes1;
+            cx.misc->n_issued = t + 1;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// GEMV instructions
+// ---------------------------------------------------------------------------
+
+// Polls this thread's nc chunks of 8 tagged elements (chunk c at element
+// (c*256 + tid)*8 of src) with all loads of a poll in flight together, then
+// stores them to xbuf. Returns false on abort/timeout.
+template <int NC>
+__device__ __forceinline__ bool stage_chunks(const Params &p, const Ctx &cx, const uint2 *src,
+                                             uint32_t tag, float &ss) {
+    const int i0 = threadIdx.x * 8;
+    float v[NC * 8];
+    if (!ll_read_chunks<NC>(p, src + i0, kConsumerThreads * 8, tag, v)) return false;
+#pragma unroll
+    for (int c = 0; c < NC; ++c) {
+        float *dst = cx.xbuf + i0 + c * kConsumerThreads * 8;
+        if (!CHKS(dst, 32, 47)) return false;
+        *reinterpret_cast<float4 *>(dst) = make_float4(v[c * 8], v[c * 8 + 1], v[c * 8 + 2], v[c * 8 + 3]);
+        *reinterpret_cast<float4 *>(dst + 4) =
+            make_float4(v[c * 8 + 4], v[c * 8 + 5], v[c * 8 + 6], v[c * 8 + 7]);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) ss = fmaf(v[c * 8 + e], v[c * 8 + e], ss);
+    }
+    return true;
+}
+
+// Two rows at once: both rows' weights are loaded before any FMA so the two
+// dependent chains overlap. Element e of chunk c of this lane is input index
+// (c*32 + lane)*8 + e of the warp's K-slice; each 32-bit weight word holds
+// elements (2k, 2k+1), multiplied as a pair with one packed fp32 FMA.
+template <int NX>
+__device__ __forceinline__ void dot_rows2(const uint4 *wa, const uint4 *wb, const float *xr,
+                                          float &ra, float &rb) {
+    uint4 va[NX / 8], vb[NX / 8];
+#pragma unroll
+    for (int c = 0; c < NX / 8; ++c) {
+        va[c] = wa[c * 32];
+        vb[c] = wb[c * 32];
+    }
+    float2 a[4], b[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) a[k] = b[k] = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int c = 0; c < NX / 8; ++c) {
+        const uint32_t ua[4] = {va[c].x, va[c].y, va[c].z, va[c].w};
+        const uint32_t ub[4] = {vb[c].x, vb[c].y, vb[c].z, vb[c].w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float2 x2 = make_float2(xr[c * 8 + 2 * k], xr[c * 8 + 2 * k + 1]);
+            a[k] = __ffma2_rn(make_float2(bf_lo(ua[k]), bf_hi(ua[k])), x2, a[k]);
+            b[k] = __ffma2_rn(make_float2(bf_lo(ub[k]), bf_hi(ub[k])), x2, b[k]);
+        }
+    }
+    ra = ((a[0].x + a[0].y) + (a[1].x + a[1].y)) + ((a[2].x + a[2].y) + (a[3].x + a[3].y));
+    rb = ((b[0].x + b[0].y) + (b[1].x + b[1].y)) + ((b[2].x + b[2].y) + (b[3].x + b[3].y));
+}
+
+// Warp sums of two values at once: after the call lanes 0-15 hold the sum of
+// a, lanes 16-31 the sum of b (5 shuffles instead of 10).
+__device__ __forceinline__ float warp_sum2(float a, float b) {
+    const bool hi = (threadIdx.x & 16) != 0;
+    const float send = hi ? a : b;
+    float v = (hi ? b : a) + __shfl_xor_sync(0xFFFFFFFFu, send, 16);
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    return v;
+}
+
+// Stages an input vector of K elements into xbuf (K <= kMaxStaged with
+// gains, K <= kMaxStagedLong without): tagged words polled until they carry
+// `tag` (or a bf16 row when src_bf is set), the norm gains copied to shared
+// memory in the same round trip. Returns the sum of squares of the whole
+// vector (valid in every thread) and false on abort/timeout (uniform across
+// the consumer warps).
+__device__ bool stage_input(const Params &p, const Ctx &cx, const uint2 *src, const uint16_t *src_bf,
+                            uint32_t tag, int K, const uint16_t *gain, float &ss_out) {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    uint16_t *gbuf = reinterpret_cast<uint16_t *>(cx.xbuf + kMaxStaged);
+    bool ok = src != nullptr || src_bf != nullptr;
+    float ss = 0.f;
+    if (gain) {
+        for (int i = tid * 8; i < K; i += kConsumerThreads * 8)
+            if (CHK(gain + i, 16, 11) && CHKS(gbuf + i, 16, 53))
+                *reinterpret_cast<uint4 *>(gbuf + i) = __ldg(reinterpret_cast<const uint4 *>(gain + i));
+    }
+    if (src_bf) {
+        for (int i = tid * 8; i < K; i += kConsumerThreads * 8) {
+            uint4 b = make_uint4(0u, 0u, 0u, 0u);
+            if (CHK(src_bf + i, 16, 9)) b = __ldg(reinterpret_cast<const uint4 *>(src_bf + i));
+            const float v[8] = {bf_lo(b.x), bf_hi(b.x), bf_lo(b.y), bf_hi(b.y),
+                                bf_lo(b.z), bf_hi(b.z), bf_lo(b.w), bf_hi(b.w)};
+            if (CHKS(cx.xbuf + i, 32, 47)) {
+                *reinterpret_cast<float4 *>(cx.xbuf + i) = make_float4(v[0], v[1], v[2], v[3]);
+                *reinterpret_cast<float4 *>(cx.xbuf + i + 4) = make_float4(v[4], v[5], v[6], v[7]);
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) ss = fmaf(v[e], v[e], ss);
+        }
+    } else if (ok) {
+        // chunks of this thread that lie inside the vector
+        const int nc = (K - tid * 8 + kConsumerThreads * 8 - 1) / (kConsumerThreads * 8);
+        switch (nc) {
+            case 0: break;
+            case 1: ok = stage_chunks<1>(p, cx, src, tag, ss); break;
+            case 2: ok = stage_chunks<2>(p, cx, src, tag, ss); break;
+            case 3: ok = stage_chunks<3>(p, cx, src, tag, ss); break;
+            default: ok = stage_chunks<4>(p, cx, src, tag, ss); break;
+        }
+    }
+    ss = warp_sum(ss);
+    if (lane == 0) cx.misc->red8[warp] = ss;
+    ok = !consumer_sync_any(!ok);
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) tot += cx.misc->red8[w];
+    ss_out = tot;
+    return ok;
+}
+
+// One GEMV instruction: rows [a0, a0+a1) of its matrix times the input
+// vector, with the op's prologue (RMSNorm) and epilogue (residual,
+// SiLU-gate, logits + block argmax). Per-row partial dot products go to
+// red[out_index * sw + ks].
+template <int NX>
+__device__ void gemv_instr(const Params &p, const Ctx &cx, const Instr &in, const Geo &g,
+                           uint32_t &t, bool &bad) {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int rg = warp / g.sw, ks = warp % g.sw;
+    const int l = in.layer, n = in.a1, r0 = in.a0;
+    const LayerW *lw = p.layers + l;
+    const bool gu = in.op == OP_GATEUP;
+    const uint32_t ep8 = cx.misc->ep8;
+    const uint2 *src = nullptr;
+    const uint16_t *src_bf = nullptr, *gain = nullptr;
+    uint32_t tag = ep8;
+    switch (in.op) {
+        case OP_QKV:
+            gain = lw->attn_norm;
+            if (l == 0)
+                src_bf = p.embed + (size_t)current_token(p) * p.d;
+            else {
+                src = p.xll;
+                tag = ep8 | (uint32_t)(2 * l);
+            }
+            break;
+        case OP_GATEUP: gain = lw->mlp_norm; src = p.xll; tag = ep8 | (uint32_t)(2 * l + 1); break;
+        case OP_LMHEAD: gain = p.final_norm; src = p.xll; tag = ep8 | (uint32_t)(2 * p.L); break;
+        case OP_OPROJ: src = p.attll + (size_t)l * p.Hq * p.hd; break;
+        default: src = p.hll + (size_t)l * p.F; break;  // OP_DOWN
+    }
+    // residual rows of this instruction (O-projection and down)
+    if (in.op == OP_OPROJ || in.op == OP_DOWN) {
+        const int tok = (in.op == OP_OPROJ && l == 0) ? current_token(p) : 0;
+        const uint32_t rtag = ep8 | (uint32_t)(in.op == OP_OPROJ ? 2 * l : 2 * l + 1);
+        for (int i = tid; i < n; i += kConsumerThreads) {
+            float v = 0.f;
+            if (in.op == OP_OPROJ && l == 0) {
+                if (CHK(p.embed + (size_t)tok * p.d + r0 + i, 2, 13))
+                    v = bf16f(__ldg(p.embed + (size_t)tok * p.d + r0 + i));
+            } else if (!bad && !ll_read1(p, p.xll + r0 + i, rtag, v)) {
+                bad = true;
+            }
+            if (CHKS(cx.resid + i, 4, 54)) cx.resid[i] = v;
+        }
+    }
+    // this lane's input slice
+    float xr[NX];
+    float *red = in.op == OP_DOWN ? cx.dred : cx.red;
+    const int sbase = ks * g.kslice;
+    {
+        // consecutive instructions of the same op and layer share their input
+        const int32_t key = (in.op << 16) | l;
+        const bool reuse = cx.misc->staged_key == key;
+        float ss = cx.misc->staged_ss;
+        if (!reuse && !stage_input(p, cx, bad ? nullptr : src, src_bf, tag, g.K, gain, ss)) bad = true;
+        bad = consumer_sync_any(bad);
+        if (tid == 0) {
+            cx.misc->staged_key = bad ? -1 : key;
+            cx.misc->staged_ss = ss;
+        }
+        const float rstd = gain ? 1.0f / sqrtf(ss / (float)g.K + p.eps) : 1.0f;
+        const uint16_t *gbuf = reinterpret_cast<const uint16_t *>(cx.xbuf + kMaxStaged);
+#pragma unroll
+        for (int c = 0; c < NX / 8; ++c) {
+            const int idx = sbase + (c * 32 + lane) * 8;
+            const float4 u = *reinterpret_cast<const float4 *>(cx.xbuf + idx);
+            const float4 v = *reinterpret_cast<const float4 *>(cx.xbuf + idx + 4);
+            float *x = xr + c * 8;
+            x[0] = u.x; x[1] = u.y; x[2] = u.z; x[3] = u.w;
+            x[4] = v.x; x[5] = v.y; x[6] = v.z; x[7] = v.w;
+            if (gain) {
+                const uint4 gb = *reinterpret_cast<const uint4 *>(gbuf + idx);
+                x[0] *= rstd * bf_lo(gb.x); x[1] *= rstd * bf_hi(gb.x);
+                x[2] *= rstd * bf_lo(gb.y); x[3] *= rstd * bf_hi(gb.y);
+                x[4] *= rstd * bf_lo(gb.z); x[5] *= rstd * bf_hi(gb.z);
+                x[6] *= rstd * bf_lo(gb.w); x[7] *= rstd * bf_hi(gb.w);
+            }
+        }
+    }
+    phase_stamp(p, cx, 0);
+    // Tiles. Warp (rg, ks) owns rows rg*M .. rg*M+M-1 of every tile (M = 64/NX
+    // for every geometry the host plans) and K-slice ks. Everything the loop
+    // needs is copied into registers first: values read through `p` or `g`
+    // live in shared memory and would be reloaded after every barrier op.
+    constexpr int M = 64 / NX;
+    const int sw = g.sw;
+    const int per = gu ? g.rt / 2 : g.rt;
+    const int nt = (n + per - 1) / per;
+    const int row_u4 = g.K / 8;  // 16-byte chunks per row
+    const bool tracing = p.trace != nullptr;
+    const uint4 *pages = reinterpret_cast<const uint4 *>(cx.pages);
+    const int woff = rg * M * row_u4 + sbase / 8 + lane;
+    const bool second = (lane & 16) != 0;  // lanes 16-31 hold the second row's sum
+    // row r of a tile is output row j*per + roff[r] (+ n for the up half of a gate/up tile)
+    int roff[M], obase[M];
+#pragma unroll
+    for (int q = 0; q < M; ++q) {
+        const int r = rg * M + q;
+        const bool up = gu && r >= per;
+        roff[q] = up ? r - per : r;
+        obase[q] = up ? n : 0;
+    }
+    int pg = (int)(t % kPages);
+    uint32_t par = (t / kPages) & 1u;
+    for (int j = 0; j < nt; ++j) {
+        if (!bad && !wait_tile(p, cx, pg, par, tracing)) bad = true;
+        bad = __any_sync(0xFFFFFFFFu, bad);  // warp-uniform from here on
+        bool released = false;
+        if (!bad) {
+            const uint4 *page = pages + pg * (kPageBytes / 16) + woff;
+#pragma unroll
+            for (int q = 0; q < M; q += 2) {
+                const int row0 = j * per + roff[q], row1 = j * per + roff[q + 1];
+                const bool v0 = row0 < n, v1 = row1 < n;
+                if (!v0 && !v1) continue;
+                const uint4 *wa = page + q * row_u4;
+                const uint4 *wb = v1 ? wa + row_u4 : wa;  // an invalid second row re-reads the first
+                float ra = 0.f, rb = 0.f;
+                if (CHKS(wa, 16, 44) && CHKS(wa + (NX / 8 - 1) * 32, 16, 45) && CHKS(wb, 16, 44) &&
+                    CHKS(wb + (NX / 8 - 1) * 32, 16, 45))
+                    dot_rows2<NX>(wa, wb, xr, ra, rb);
+                // with one row pair per warp the page is free once the weights are in registers
+                if (M == 2) {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&cx.empty[pg]);
+                    released = true;
+                }
+                const float sum = warp_sum2(ra, rb);
+                const bool vh = second ? v1 : v0;
+                const int oh = second ? obase[q + 1] + row1 : obase[q] + row0;
+                if ((lane & 15) == 0 && vh && CHKS(red + oh * sw + ks, 4, 46)) red[oh * sw + ks] = sum;
+            }
+        }
+        if (!released) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&cx.empty[pg]);
+        }
+        ++t;
+        if (++pg == kPages) {
+            pg = 0;
+            par ^= 1u;
+        }
+    }
+}
+
+__device__ void do_gemv(const Params &p, const Ctx &cx, const Instr &in, uint32_t &t, bool &bad) {
+    const Geo &g = geo_of(p, in.op);
+    const int tid = threadIdx.x;
+    const int l = in.layer;
+    switch (g.nx) {  // the host plans every operand with nx in {8, 16, 24, 32}
+        case 8: gemv_instr<8>(p, cx, in, g, t, bad); break;
+        case 16: gemv_instr<16>(p, cx, in, g, t, bad); break;
+        case 24: gemv_instr<24>(p, cx, in, g, t, bad); break;
+        default: gemv_instr<32>(p, cx, in, g, t, bad); break;
+    }
+    phase_stamp(p, cx, 1);
+    bad = consumer_sync_any(bad);
+    if (bad) return;
+    // ---- epilogue: combine K-slices, apply the op's output transform
+    const int n = in.a1, r0 = in.a0, sw = g.sw;
+    const uint32_t ep8 = cx.misc->ep8;
+    const float *red = in.op == OP_DOWN ? cx.dred : cx.red;
+    switch (in.op) {
+        case OP_QKV: {
+            uint2 *dst = p.qkvll + (size_t)l * (p.Hq + 2 * p.Hkv) * p.hd + r0;  // stacked q | k | v
+            for (int i = tid; i < n; i += kConsumerThreads) {
+                float v = 0.f;
+                for (int s = 0; s < sw; ++s) v += red[i * sw + s];
+                if (CHK(dst + i, 8, 12)) ll_store(dst + i, v, ep8);
+            }
+            break;
+        }
+        case OP_OPROJ:
+        case OP_DOWN: {
+            const uint32_t wtag = ep8 | (uint32_t)(in.op == OP_OPROJ ? 2 * l + 1 : 2 * l + 2);
+            for (int i = tid; i < n; i += kConsumerThreads) {
+                float v = 0.f;
+                for (int s = 0; s < sw; ++s) v += red[i * sw + s];
+                if (CHK(p.xll + r0 + i, 8, 15)) ll_store(p.xll + r0 + i, cx.resid[i] + v, wtag);
+            }
+            break;
+        }
+        case OP_GATEUP: {
+            uint2 *dst = p.hll + (size_t)l * p.F + r0;
+            for (int i = tid; i < n; i += kConsumerThreads) {
+                float gv = 0.f, uv = 0.f;
+                for (int s = 0; s < sw; ++s) {
+                    gv += red[i * sw + s];
+                    uv += red[(n + i) * sw + s];
+                }
+                if (CHK(dst + i, 8, 16)) ll_store(dst + i, gv / (1.0f + expf(-gv)) * uv, ep8);
+            }
+            break;
+        }
+        default: {  // OP_LMHEAD
+            unsigned long long best = 0ull;
+            for (int i = tid; i < n; i += kConsumerThreads) {
+                float v = 0.f;
+                for (int s = 0; s < sw; ++s) v += red[i * sw + s];
+                if (p.out_logits && CHK(p.out_logits + r0 + i, 4, 18)) p.out_logits[r0 + i] = v;
+                const unsigned long long k = argmax_key(v, (uint32_t)(r0 + i));
+                best = k > best ? k : best;
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const unsigned long long other = __shfl_xor_sync(0xFFFFFFFFu, best, o);
+                best = other > best ? other : best;
+            }
+            const int warp = tid >> 5;
+            if ((tid & 31) == 0) cx.misc->best8[warp] = best;
+            consumer_sync();
+            if (tid == 0) {
+                unsigned long long b = 0ull;
+                for (int w = 0; w < kConsumerWarps; ++w) b = cx.misc->best8[w] > b ? cx.misc->best8[w] : b;
+                if (CHK(p.lm_part + in.slot, 8, 19)) p.lm_part[in.slot] = b;
+                // the last LM-head instruction to arrive reduces all block maxima
+                const uint32_t old = CHK(p.ctr + p.cl.lm_arrive, 4, 31)
+                                         ? atom_acq_rel_add(p.ctr + p.cl.lm_arrive, 1u) : 0u;
+                const bool last = old == (uint32_t)p.n_lm - 1u;
+                if (last) __threadfence();
+                cx.misc->flag = last ? 1 : 0;
+            }
+            consumer_sync();
+            if (cx.misc->flag) {
+                // all consumer threads load the block maxima at once
+                unsigned long long g2 = 0ull;
+                for (int s = tid; s < p.n_lm; s += kConsumerThreads) {
+                    const unsigned long long v = CHK(p.lm_part + s, 8, 20) ? __ldcg(p.lm_part + s) : 0ull;
+                    g2 = v > g2 ? v : g2;
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    const unsigned long long other = __shfl_xor_sync(0xFFFFFFFFu, g2, o);
+                    g2 = other > g2 ? other : g2;
+                }
+                if ((tid & 31) == 0) cx.misc->best8[warp] = g2;
+                consumer_sync();
+                if (tid == 0) {
+                    unsigned long long b = 0ull;
+                    for (int w = 0; w < kConsumerWarps; ++w) b = cx.misc->best8[w] > b ? cx.misc->best8[w] : b;
+                    if (CHK(p.out_token, 4, 21))
+                        *p.out_token = (int32_t)(0xFFFFFFFFu - (uint32_t)(b & 0xFFFFFFFFull));
+                }
+            }
+            break;
+        }
+    }
+}
+
+template <int HD, int G>
+struct AttnWarpState {
+    // running max (log2 units) and sum of the head this lane scores
+    // (head dq % GP of the score layout), the same in every lane of that head
+    float m, l;
+    // lane (pv, dg) of the P.V layout: unnormalised output dims dg*8..dg*8+7
+    // of every head, summed over the positions pv, pv + PGV, ... it saw
+    float o[G][8];
+};
+
+// Lane layouts of one chunk of up to 32 positions:
+//  scores: lane = (position pl, dim group dq): DQ = HD/16 groups of 16 dims,
+//          PG = 32/DQ positions per pass, NPASS passes. A lane multiplies its
+//          16 dims for all heads, then a reduce-scatter over the dim groups
+//          leaves it the full score of head dq % GP (GP = G, or 4 for G = 3).
+//  P.V:    lane = (position group pv, dim group dg): DGV = HD/8 groups of 8 dims,
+//          PGV = 32/DGV groups; a lane walks positions pv, pv + PGV, ...
+template <int HD, int G>
+struct AttnLayout {
+    static constexpr int DQ = HD / 16, PG = 32 / DQ, NPASS = 32 / PG;
+    static constexpr int DGV = HD / 8, PGV = 32 / DGV;
+    static constexpr int GP = G == 3 ? 4 : G;
+};
+
+// One chunk of up to 32 positions for this warp. Kp/Vp point at the chunk's
+// first key/value row (bf16, HD each); npos valid positions; q holds the G
+// pre-scaled query heads [G][HD] (fp32, shared); pbuf is this warp's
+// [32][4] scratch for the softmax weights. Scores are in log2 units; the
+// warp's online-softmax state st is updated in place. Shared-memory reads
+// are conflict-free: each K or V row is read whole by consecutive lanes
+// (odd rows with their two 16-byte halves swapped), q and the weights by
+// groups of lanes at one address.
+template <int HD, int G>
+__device__ __forceinline__ void attn_chunk(AttnWarpState<HD, G> &st, const uint16_t *Kp,
+                                           const uint16_t *Vp, int npos, const float *q,
+                                           float *pbuf) {
+    using Lay = AttnLayout<HD, G>;
+    constexpr int DQ = Lay::DQ, PG = Lay::PG, NPASS = Lay::NPASS, DGV = Lay::DGV, PGV = Lay::PGV;
+    constexpr int GP = Lay::GP;
+    const int lane = threadIdx.x & 31;
+    const int pl = lane / DQ, dq = lane % DQ;
+    // ---- scores of head dq % GP at positions k*PG + pl
+    float s[NPASS];
+    {
+        float2 qr[GP][8];
+#pragma unroll
+        for (int g = 0; g < GP; ++g) {
+            const float4 *qg = reinterpret_cast<const float4 *>(q + (g < G ? g : 0) * HD + dq * 16);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const float4 v = g < G ? qg[c] : make_float4(0.f, 0.f, 0.f, 0.f);
+                qr[g][2 * c] = make_float2(v.x, v.y);
+                qr[g][2 * c + 1] = make_float2(v.z, v.w);
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < NPASS; ++k) {
+            const int pos = k * PG + pl;
+            const bool valid = pos < npos;
+            const int row = valid ? pos : 0;
+            // 32 bytes of this row: halves in an order that depends on the
+            // row's bank offset so that a pass touches every bank evenly
+            const bool swap = ((row + (dq * 32) / 128) & 1) != 0;
+            const uint4 *kr = reinterpret_cast<const uint4 *>(Kp + (size_t)row * HD + dq * 16);
+            uint4 w0 = kr[swap ? 1 : 0], w1 = kr[swap ? 0 : 1];
+            if (swap) {
+                const uint4 t = w0;
+                w0 = w1;
+                w1 = t;
+            }
+            const uint32_t u[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+            float v[GP];
+#pragma unroll
+            for (int g = 0; g < GP; ++g) {
+                float2 a = make_float2(0.f, 0.f), b = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int e = 0; e < 8; e += 2) {
+                    a = __ffma2_rn(make_float2(bf_lo(u[e]), bf_hi(u[e])), qr[g][e], a);
+                    b = __ffma2_rn(make_float2(bf_lo(u[e + 1]), bf_hi(u[e + 1])), qr[g][e + 1], b);
+                }
+                v[g] = (a.x + a.y) + (b.x + b.y);
+            }
+            // reduce-scatter over the low dim-group bits, then plain sums
+            float c;
+            if constexpr (GP == 4) {
+                const bool hi2 = (dq & 2) != 0, hi1 = (dq & 1) != 0;
+                float a0 = hi2 ? v[2] : v[0], a1 = hi2 ? v[3] : v[1];
+                const float b0 = hi2 ? v[0] : v[2], b1 = hi2 ? v[1] : v[3];
+                a0 += __shfl_xor_sync(0xFFFFFFFFu, b0, 2);
+                a1 += __shfl_xor_sync(0xFFFFFFFFu, b1, 2);
+                c = hi1 ? a1 : a0;
+                c += __shfl_xor_sync(0xFFFFFFFFu, hi1 ? a0 : a1, 1);
+#pragma unroll
+                for (int o = 4; o < DQ; o <<= 1) c += __shfl_xor_sync(0xFFFFFFFFu, c, o);
+            } else if constexpr (GP == 2) {
+                const bool hi1 = (dq & 1) != 0;
+                c = hi1 ? v[1] : v[0];
+                c += __shfl_xor_sync(0xFFFFFFFFu, hi1 ? v[0] : v[1], 1);
+#pragma unroll
+                for (int o = 2; o < DQ; o <<= 1) c += __shfl_xor_sync(0xFFFFFFFFu, c, o);
+            } else {
+                c = v[0];
+#pragma unroll
+                for (int o = 1; o < DQ; o <<= 1) c += __shfl_xor_sync(0xFFFFFFFFu, c, o);
+            }
+            s[k] = valid ? c : -INFINITY;
+        }
+    }
+    // ---- online softmax of this lane's head across the chunk; positions
+    // differ in the lane bits above the dim group
+    const int hg = dq % GP;
+    float mloc = s[0];
+#pragma unroll
+    for (int k = 1; k < NPASS; ++k) mloc = fmaxf(mloc, s[k]);
+#pragma unroll
+    for (int o = DQ; o < 32; o <<= 1) mloc = fmaxf(mloc, __shfl_xor_sync(0xFFFFFFFFu, mloc, o));
+    const float mnew = fmaxf(st.m, mloc);
+    const float corr = exp2f(st.m - mnew);
+    float ls = 0.f;
+#pragma unroll
+    for (int k = 0; k < NPASS; ++k) {
+        s[k] = exp2f(s[k] - mnew);  // exp2(-inf) = 0 for invalid positions
+        ls += s[k];
+    }
+#pragma unroll
+    for (int o = DQ; o < 32; o <<= 1) ls += __shfl_xor_sync(0xFFFFFFFFu, ls, o);
+    st.l = st.l * corr + ls;
+    st.m = mnew;
+    if (dq < GP && hg < G) {
+#pragma unroll
+        for (int k = 0; k < NPASS; ++k) pbuf[(k * PG + pl) * 4 + hg] = s[k];
+    }
+    // every lane rescales all heads: head g's factor from lane g (pl 0, dq g)
+    float cg[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) cg[g] = __shfl_sync(0xFFFFFFFFu, corr, g);
+    __syncwarp();
+    // ---- P.V
+    {
+        const int pv = lane / DGV, dg = lane % DGV;
+        float2 o2[G][4];
+#pragma unroll
+        for (int g = 0; g < G; ++g)
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                o2[g][e] = make_float2(st.o[g][2 * e] * cg[g], st.o[g][2 * e + 1] * cg[g]);
+#pragma unroll
+        for (int i = 0; i < 32 / PGV; ++i) {
+            const int pos = i * PGV + pv;
+            if (pos < npos) {
+                const float4 pp = *reinterpret_cast<const float4 *>(pbuf + pos * 4);
+                const uint4 w = *reinterpret_cast<const uint4 *>(Vp + (size_t)pos * HD + dg * 8);
+                const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+                const float pg[4] = {pp.x, pp.y, pp.z, pp.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 v = make_float2(bf_lo(u[e]), bf_hi(u[e]));
+#pragma unroll
+                    for (int g = 0; g < G; ++g) o2[g][e] = __ffma2_rn(v, make_float2(pg[g], pg[g]), o2[g][e]);
+                }
+            }
+        }
+#pragma unroll
+        for (int g = 0; g < G; ++g)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                st.o[g][2 * e] = o2[g][e].x;
+                st.o[g][2 * e + 1] = o2[g][e].y;
+            }
+    }
+    __syncwarp();
+}
+
+template <int HD, int G>
+__device__ void do_attn_hd(const Params &p, const Ctx &cx, const Instr &in, uint32_t &t, bool &bad) {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int l = in.layer, kvh = in.a0, split = in.a1;
+    const AttnRange r = attn_range(p, split);
+    const int seff = attn_seff(p);
+    if (!r.active) return;  // nothing cached for this split at this position
+    const uint32_t ep8 = cx.misc->ep8;
+    if (tid == 0) cx.misc->staged_key = -1;  // xbuf becomes attention scratch
+    const int qkv_stride = (p.Hq + 2 * p.Hkv) * HD;
+    const uint2 *qkv = p.qkvll + (size_t)l * qkv_stride;
+    // shared scratch: q [G][HD] | knew [HD] bf16 | vnew [HD] bf16 | warp states
+    // [8][G][HD+2]; the host checks G*HD + HD + 8*G*(HD+2) <= kXbufFloats.
+    float *qs = cx.xbuf;
+    uint16_t *knew = reinterpret_cast<uint16_t *>(cx.xbuf + G * HD);
+    uint16_t *vnew = knew + HD;
+    constexpr int WS = HD + 4;  // warp-state row: HD outputs, max, sum, pad (16-byte rows)
+    float *wst = cx.xbuf + G * HD + HD;
+    float *pbuf = cx.red + warp * (32 * kMaxG);
+
+    // q of the group's heads (rotated, pre-scaled by log2(e)/sqrt(hd)) and,
+    // for the split that owns the new position, its key and value: polled
+    // from the QKV instructions' tagged outputs.
+    {
+        const float qscale = 1.4426950408889634f / sqrtf((float)HD);
+        const float *rope = p.rope + (size_t)p.pos * HD;  // [HD/2][2]
+        for (int idx = tid; idx < G * (HD / 2); idx += kConsumerThreads) {
+            const int g = idx / (HD / 2), i = idx % (HD / 2);
+            const uint2 *qh = qkv + (size_t)(kvh * G + g) * HD;
+            const uint2 *srcs[2] = {qh + i, qh + i + HD / 2};
+            float ab[2];
+            if (bad || !ll_read_n<2>(p, srcs, ep8, ab) || !CHK(rope + 2 * i, 8, 28) ||
+                !CHKS(qs + g * HD + i + HD / 2, 4, 48)) {
+                bad = true;
+                continue;
+            }
+            const float a = ab[0], b = ab[1];
+            const float c = rope[2 * i], s = rope[2 * i + 1];
+            qs[g * HD + i] = (a * c - b * s) * qscale;
+            qs[g * HD + i + HD / 2] = (b * c + a * s) * qscale;
+        }
+        if (r.has_new) {
+            const uint2 *kh = qkv + (size_t)p.Hq * HD + (size_t)kvh * HD;
+            const uint2 *vh = qkv + (size_t)(p.Hq + p.Hkv) * HD + (size_t)kvh * HD;
+            const size_t cache_off = (((size_t)l * p.max_batch) * p.Hkv + kvh) * p.max_seq * HD +
+                                     (size_t)p.pos * HD;
+            for (int i = tid; i < HD / 2; i += kConsumerThreads) {
+                const uint2 *srcs[4] = {kh + i, kh + i + HD / 2, vh + i, vh + i + HD / 2};
+                float kv4[4];
+                if (bad || !ll_read_n<4>(p, srcs, ep8, kv4) || !CHK(p.kc + cache_off + i, 2, 24) || !CHK(p.kc + cache_off + i + HD / 2, 2, 24) ||
+                    !CHK(p.vc + cache_off + i, 2, 24) || !CHK(p.vc + cache_off + i + HD / 2, 2, 24) ||
+                    !CHK(rope + 2 * i, 8, 28) || !CHKS(vnew + i + HD / 2, 2, 49)) {
+                    bad = true;
+                    continue;
+                }
+                const float a = kv4[0], b = kv4[1];
+                const float c = rope[2 * i], s = rope[2 * i + 1];
+                const uint16_t k0 = f2bf(a * c - b * s), k1 = f2bf(b * c + a * s);
+                const uint16_t v0 = f2bf(kv4[2]), v1 = f2bf(kv4[3]);
+                knew[i] = k0;
+                knew[i + HD / 2] = k1;
+                vnew[i] = v0;
+                vnew[i + HD / 2] = v1;
+                p.kc[cache_off + i] = k0;
+                p.kc[cache_off + i + HD / 2] = k1;
+                p.vc[cache_off + i] = v0;
+                p.vc[cache_off + i + HD / 2] = v1;
+            }
+        }
+        bad = consumer_sync_any(bad);
+        phase_stamp(p, cx, 0);
+    }
+    // per-warp online softmax over the split's tiles
+    AttnWarpState<HD, G> st;
+    st.m = -INFINITY;
+    st.l = 0.f;
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) st.o[g][e] = 0.f;
+    // Tiles of ppt positions are split into chunks of 32 (one lane per
+    // position); tile j goes to warp group j % slots, chunk c of it to warp
+    // group_base + c, so the chunks of a short context run side by side.
+    constexpr int CPT = (kPageBytes / 2) / (HD * 2) / 32;  // chunks per tile
+    constexpr int SLOTS = kConsumerWarps / CPT;
+    // the new position needs only the polled q/k/v: the last warp does it
+    // while the cached tiles may still be landing
+    if (!bad && r.has_new && warp == kConsumerWarps - 1) attn_chunk<HD, G>(st, knew, vnew, 1, qs, pbuf);
+    const int nt = (r.t1 - r.t0 + p.ppt - 1) / p.ppt;
+    for (int j = 0; j < nt; ++j, ++t) {
+        const int pg = t % kPages;
+        if (!bad && !wait_tile(p, cx, pg, (t / kPages) & 1, p.trace != nullptr)) bad = true;
+        const int chunk = warp - (j % SLOTS) * CPT;
+        if (!bad && chunk >= 0 && chunk < CPT) {
+            const int ts = r.t0 + j * p.ppt;
+            int n = r.t1 - ts;
+            if (n > p.ppt) n = p.ppt;
+            int np = n - chunk * 32;
+            np = np > 32 ? 32 : np;
+            if (np > 0 && CHKS(cx.pages + (size_t)pg * kPageBytes + (size_t)(chunk * 32 + np) * HD * 2 - 2, 2, 50) &&
+                CHKS(pbuf + 32 * kMaxG - 1, 4, 51)) {
+                const uint16_t *Kp = reinterpret_cast<const uint16_t *>(cx.pages + (size_t)pg * kPageBytes) +
+                                     (size_t)chunk * 32 * HD;
+                const uint16_t *Vp = reinterpret_cast<const uint16_t *>(cx.pages + (size_t)pg * kPageBytes +
+                                                                          kPageBytes / 2) +
+                                     (size_t)chunk * 32 * HD;
+                attn_chunk<HD, G>(st, Kp, Vp, np, qs, pbuf);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&cx.empty[pg]);
+    }
+    bad = consumer_sync_any(bad);
+    phase_stamp(p, cx, 1);
+    if (bad) return;
+    // warp states -> shared: sum the P.V lanes' position groups, then the
+    // lanes of group 0 hold the warp's output dims dg*8 .. dg*8+7; lane g
+    // (position 0, dim group g of the score layout) holds head g's max and sum
+    {
+        constexpr int DGV = AttnLayout<HD, G>::DGV;
+        float *my = wst + (size_t)warp * G * WS;
+        if (!CHKS(my + G * WS - 1, 4, 52)) my = wst;
+#pragma unroll
+        for (int g = 0; g < G; ++g)
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+#pragma unroll
+                for (int o = DGV; o < 32; o <<= 1) st.o[g][e] += __shfl_xor_sync(0xFFFFFFFFu, st.o[g][e], o);
+        if (lane < DGV) {
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                float4 *dst = reinterpret_cast<float4 *>(my + g * WS + lane * 8);
+                dst[0] = make_float4(st.o[g][0], st.o[g][1], st.o[g][2], st.o[g][3]);
+                dst[1] = make_float4(st.o[g][4], st.o[g][5], st.o[g][6], st.o[g][7]);
+            }
+        }
+        if (lane < G) {
+            my[lane * WS + HD] = st.m;
+            my[lane * WS + HD + 1] = st.l;
+        }
+    }
+    consumer_sync();
+    uint2 *out = p.attll + (size_t)l * p.Hq * HD + (size_t)kvh * G * HD;
+    if (seff == 1) {
+        // The only active split holds the whole context: normalise and
+        // publish the attention output directly.
+        for (int idx = tid; idx < G * HD; idx += kConsumerThreads) {
+            const int g = idx / HD, e = idx % HD;
+            float M = -INFINITY;
+            for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, wst[(w * G + g) * WS + HD]);
+            float num = 0.f, den = 0.f;
+            for (int w = 0; w < kConsumerWarps; ++w) {
+                const float mw = wst[(w * G + g) * WS + HD];
+                if (mw == -INFINITY) continue;
+                const float wgt = exp2f(mw - M);
+                num += wst[(w * G + g) * WS + e] * wgt;
+                den += wst[(w * G + g) * WS + HD + 1] * wgt;
+            }
+            if (CHK(out + idx, 8, 27)) ll_store(out + idx, num / den, ep8);
+        }
+        return;
+    }
+    // Several splits: publish this split's partial (o unnormalised, m, l) ...
+    constexpr int PS = HD + 2;  // partial row in global memory: HD outputs, max, sum
+    uint2 *part = p.partll + ((size_t)l * p.Hq + (size_t)kvh * G) * p.S * PS;
+    for (int idx = tid; idx < G * PS; idx += kConsumerThreads) {
+        const int g = idx / PS, e = idx % PS;
+        float M = -INFINITY;
+        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, wst[(w * G + g) * WS + HD]);
+        float acc = 0.f;
+        if (e == HD) {
+            acc = M;
+        } else if (M != -INFINITY) {
+            for (int w = 0; w < kConsumerWarps; ++w) {
+                const float mw = wst[(w * G + g) * WS + HD];
+                if (mw != -INFINITY) acc += wst[(w * G + g) * WS + e] * exp2f(mw - M);
+            }
+        }
+        uint2 *dst = part + ((size_t)g * p.S + split) * PS + e;
+        if (CHK(dst, 8, 25)) ll_store(dst, acc, ep8);
+    }
+    // ... and the split that owns the new position merges all of them
+    // (log-sum-exp), polling the others' tagged partials with all loads of
+    // a poll in flight together.
+    if (!r.has_new) return;
+    for (int idx = tid; idx < G * HD && !bad; idx += kConsumerThreads) {
+        const int g = idx / HD, e = idx % HD;
+        const uint2 *sg = part + (size_t)g * p.S * PS;
+        float num = 0.f, den = 0.f, M = -INFINITY;
+        for (int s0 = 0; s0 < seff && !bad; s0 += kMergeBatch) {
+            const int ns = seff - s0 < kMergeBatch ? seff - s0 : kMergeBatch;
+            uint2 mv[kMergeBatch], lv[kMergeBatch], ov[kMergeBatch];
+            Spin sp;
+            while (true) {
+                bool ok = true;
+#pragma unroll
+                for (int k = 0; k < kMergeBatch; ++k) {
+                    if (k < ns) {
+                        const uint2 *ps = sg + (size_t)(s0 + k) * PS;
+                        mv[k] = ll_ld8(ps + HD);
+                        lv[k] = ll_ld8(ps + HD + 1);
+                        ov[k] = ll_ld8(ps + e);
+                    }
+                }
+#pragma unroll
+                for (int k = 0; k < kMergeBatch; ++k)
+                    if (k < ns) ok = ok && mv[k].y == ep8 && lv[k].y == ep8 && ov[k].y == ep8;
+                if (ok) break;
+                if (!sp.keep_going(p)) {
+                    bad = true;
+                    break;
+                }
+            }
+            if (bad) break;
+            // online combination across batches of splits
+#pragma unroll
+            for (int k = 0; k < kMergeBatch; ++k) {
+                if (k >= ns) continue;
+                const float m = __uint_as_float(mv[k].x);
+                if (m == -INFINITY) continue;
+                const float Mn = fmaxf(M, m);
+                const float a = exp2f(M - Mn), b = exp2f(m - Mn);
+                num = num * a + __uint_as_float(ov[k].x) * b;
+                den = den * a + __uint_as_float(lv[k].x) * b;
+                M = Mn;
+            }
+        }
+        if (!bad && CHK(out + idx, 8, 27)) ll_store(out + idx, num / den, ep8);
+    }
+    bad = consumer_sync_any(bad);
+}
+
+// ---------------------------------------------------------------------------
+// Consumer: interprets the queue.
+// ---------------------------------------------------------------------------
+template <int HD, int G>
+__device__ void consumer(const Params &p, const Ctx &cx, int qb, int qe, int q0) {
+    const int tid = threadIdx.x;
+    uint32_t t = 0;
+    bool bad = false;
+    long long *trace = p.trace ? p.trace + (size_t)blockIdx.x * p.trace_cap * kTraceWords : nullptr;
+    for (int i = qb; i < qe && !bad; ++i) {
+        const Instr in = load_instr(p, i);
+        if (i + 1 < qe) prefetch_instr(p, i + 1);
+        const uint64_t ts = trace ? gtimer() : 0;
+        if (trace && tid == 0) {
+            cx.misc->phase[0] = cx.misc->phase[1] = cx.misc->phase[2] = (long long)ts;
+            cx.misc->tile_wait = 0;
+        }
+        if (in.op == OP_ATTN) {
+            do_attn_hd<HD, G>(p, cx, in, t, bad);
+        } else {
+            do_gemv(p, cx, in, t, bad);
+        }
+        phase_stamp(p, cx, 2);
+        bad = consumer_sync_any(bad);
+        if (bad) break;
+        if (tid == 0 && trace && (i - q0) < p.trace_cap &&
+            CHK(trace + (size_t)(i - q0) * kTraceWords, 8 * kTraceWords, 34)) {
+            long long *rec = trace + (size_t)(i - q0) * kTraceWords;  // slot = place in the SM's queue
+            rec[0] = blockIdx.x;
+            rec[1] = in.op;
+            rec[2] = (long long)ts - cx.misc->tile_wait;  // start minus time spent waiting for tiles
+            rec[3] = (long long)ts;
+            rec[4] = cx.misc->phase[0];
+            rec[5] = cx.misc->phase[1];
+            rec[6] = cx.misc->phase[2];
+            rec[7] = (long long)gtimer();
+        }
+    }
+    if (bad && tid == 0) cx.misc->aborted = 1;
+}
+
+// The kernel is instantiated per head dimension and per group size G
+// (query heads per kv head) so that each instance holds only the attention
+// code its model runs: a smaller instruction footprint keeps the hot loops
+// in the instruction cache.
+template <int HD, int G>
+__global__ void __launch_bounds__(kThreads, 1) mk_megakernel(const Params prm) {
+    uint8_t *smem = mk_smem;
+    // Launch parameters are copied to shared memory once; every device
+    // function reads them from there (no generic pointer into param space).
+    Params *sp = reinterpret_cast<Params *>(smem + kSmemParams);
+    Ctx cx;
+    cx.pages = smem + kSmemPages;
+    cx.xbuf = reinterpret_cast<float *>(smem + kSmemXbuf);
+    cx.red = reinterpret_cast<float *>(smem + kSmemRed);
+    cx.resid = reinterpret_cast<float *>(smem + kSmemResid);
+    cx.dred = reinterpret_cast<float *>(smem + kSmemDred);
+    cx.full = reinterpret_cast<uint64_t *>(smem + kSmemBars);
+    cx.empty = cx.full + kPages;
+    cx.misc = reinterpret_cast<Misc *>(smem + kSmemMisc);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (tid == 0) {
+        *sp = prm;
+        for (int i = 0; i < kPages; ++i) {
+            mbar_init(&cx.full[i], 1);
+            mbar_init(&cx.empty[i], kConsumerWarps);
+        }
+        cx.misc->flag = 0;
+        cx.misc->aborted = 0;
+        cx.misc->n_issued = 0;
+        cx.misc->staged_key = -1;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    __syncthreads();
+    const Params &p = *sp;
+    if (tid == 0) {
+        uint32_t e = 1;
+        if (CHK(p.epoch, 4, 32)) e = *(volatile uint32_t *)p.epoch & 0xFFFFFFu;
+        cx.misc->ep8 = (e ? e : 1u) << 8;
+    }
+    __syncthreads();
+    const int *qrow = p.q_begin + (size_t)blockIdx.x * (p.n_stages + 1);
+    bool run = CHK(qrow + p.stage_lo, 4, 2) && CHK(qrow + p.stage_hi, 4, 2) &&
+               CHK(p.status, 4, 32) && CHK(p.abort_flag, 4, 32) && CHK(p.exit_ctr, 4, 32);
+    const int qb = run ? __ldg(qrow + p.stage_lo) : 0, qe = run ? __ldg(qrow + p.stage_hi) : 0;
+    const int q0 = run ? __ldg(qrow) : 0;  // the SM's first instruction (trace slots)
+    run = run && *(volatile int32_t *)p.status == DS_OK;
+    if (run) {
+        const int tok = current_token(p);
+        if (tok < 0 || tok >= p.V) {
+            if (tid == 0) {
+                atomicCAS(p.status, DS_OK, DS_BAD_TOKEN);
+                atomicExch(p.abort_flag, 1);
+            }
+            run = false;
+        }
+    }
+    if (run) {
+        if (warp == kConsumerWarps) {
+            if (lane == 0) producer(p, cx, qb, qe);
+        } else {
+            consumer<HD, G>(p, cx, qb, qe, q0);
+        }
+    }
+    __syncthreads();
+    // Drain: copies issued but never consumed (only after an abort) must land
+    // before the CTA's shared memory is released.
+    if (tid == 0 && run) {
+        const uint32_t ni = cx.misc->n_issued;
+        const uint32_t lo = ni > (uint32_t)kPages ? ni - kPages : 0u;
+        for (uint32_t t = lo; t < ni; ++t) {
+            const uint64_t t0 = gtimer();
+            while (!mbar_try_wait(&cx.full[t % kPages], (t / kPages) & 1)) {
+                if (gtimer() - t0 > 1000000000ull) break;
+            }
+        }
+    }
+    // End of step: the last CTA out resets the counters and advances the
+    // epoch that tags this step's activations.
+    if (p.reset_at_exit && tid == 0 && CHK(p.exit_ctr, 4, 32) &&
+        CHK(p.ctr + p.cl.total - 1, 4, 32) && CHK(p.epoch, 4, 32)) {
+        __threadfence();
+        const uint32_t old = atomicAdd(p.exit_ctr, 1u);
+        if (old == gridDim.x - 1) {
+            __threadfence();
+            for (int c = 0; c < p.cl.total; ++c) p.ctr[c] = 0u;
+            const uint32_t e = (cx.misc->ep8 >> 8) + 1u;
+            *(volatile uint32_t *)p.epoch = (e & 0xFFFFFFu) ? (e & 0xFFFFFFu) : 1u;
+            *p.abort_flag = 0;
+            *p.exit_ctr = 0u;
+            __threadfence();
+        }
+    }
+}
+
+}  // namespace
+}  // namespace mk
