@@ -78,6 +78,7 @@ def load(path: str | None = None):
     L.mk_decode_step_dev.argtypes = [_VP, _VP, _I32, _VP, _VP, _VP]
     L.mk_decode_step_host.argtypes = [_VP, _PI32, _I32, _VP, _PI32, _VP]
     L.mk_decode_step_unfused.argtypes = [_VP, _I32, _I32, _VP, _VP, _VP]
+    L.mk_decode_step_batch.argtypes = [_VP, _VP, _VP, _I32, _VP, _VP, _VP]
     L.mk_get_status.argtypes = [_VP]
     L.mk_set_wait_timeout.argtypes = [_VP, ctypes.c_uint64]
     L.mk_set_trace.argtypes = [_VP, _I32]
@@ -186,6 +187,14 @@ class Megakernel:
         check(load().mk_decode_step_dev(self.h, d_token.data_ptr(), int(pos),
                                         logits.data_ptr() if logits is not None else None,
                                         out_token.data_ptr(), _stream_ptr(stream)))
+
+    def step_batch(self, d_tokens, d_positions, out_tokens, logits=None, stream=None) -> None:
+        """d_tokens, d_positions, out_tokens: int32 CUDA tensors [B]; logits: float32 CUDA
+        tensor [B][vocab] or None. Sequence b uses batch slot b of the KV cache."""
+        check(load().mk_decode_step_batch(self.h, d_tokens.data_ptr(), d_positions.data_ptr(),
+                                          int(d_tokens.numel()),
+                                          logits.data_ptr() if logits is not None else None,
+                                          out_tokens.data_ptr(), _stream_ptr(stream)))
 
     def step_unfused(self, token: int, pos: int, out_token, logits=None, stream=None) -> None:
         check(load().mk_decode_step_unfused(self.h, int(token), int(pos),

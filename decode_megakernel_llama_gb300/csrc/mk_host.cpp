@@ -91,7 +91,7 @@ int check_config(const mk_config *c) {
     if (c->n_heads % c->n_kv_heads != 0)
         return fail(MK_ERR_INVALID_ARG, "n_heads must be a multiple of n_kv_heads");
     const int G = c->n_heads / c->n_kv_heads, hd = c->head_dim;
-    if (G > 4 || G * hd + hd + mk::kConsumerWarps * G * (hd + 4) > mk::kXbufFloats)
+    if (G > 4 || G * (hd / 16 * 20) + hd + mk::kConsumerWarps * G * (hd + 4) > mk::kXbufFloats)
         return fail(MK_ERR_UNSUPPORTED, "too many query heads per kv head for the attention scratch");
     const int qd = c->n_heads * hd;
     if (c->d_model % 256 || qd % 256 || c->ffn_dim % 256)
@@ -492,6 +492,10 @@ void fill_params(const Image &im, const mk_config *config, const mk_weights *w,
     if (const char *env = getenv("MK_MAX_INFLIGHT")) p.max_inflight = atoi(env);
     if (p.max_inflight < 1) p.max_inflight = 1;
     if (p.max_inflight > mk::kPages) p.max_inflight = mk::kPages;
+    p.poll_inflight = 1;  // while consumers poll, keep their loads from queuing behind tile data
+    if (const char *env = getenv("MK_POLL_INFLIGHT")) p.poll_inflight = atoi(env);
+    if (p.poll_inflight < 1) p.poll_inflight = 1;
+    if (p.poll_inflight > p.max_inflight) p.poll_inflight = p.max_inflight;
 }
 
 int upload_image(const Image &im, const mk_config *config, const mk_weights *w,
@@ -545,11 +549,13 @@ int upload_image(const Image &im, const mk_config *config, const mk_weights *w,
 
 int launch_step(const mk::Params &base, int n_sm, int n_stages, int32_t token,
                 const int32_t *d_token, int32_t position, float *out_logits, int32_t *out_token,
-                cudaStream_t stream, bool unfused) {
+                cudaStream_t stream, bool unfused, const int32_t *d_pos, int32_t bslot) {
     mk::Params p = base;
     p.token = token;
     p.d_token = d_token;
     p.pos = position;
+    p.d_pos = d_pos;
+    p.bslot = bslot;
     p.out_logits = out_logits;
     p.out_token = out_token;
     cudaError_t e;
@@ -596,10 +602,11 @@ struct mk_handle {
 namespace {
 
 int launch(mk_handle *h, int32_t token, const int32_t *d_token, int32_t position, float *out_logits,
-           int32_t *out_token, cudaStream_t stream, bool unfused) {
+           int32_t *out_token, cudaStream_t stream, bool unfused, const int32_t *d_pos = nullptr,
+           int32_t bslot = 0) {
     if (!h) return fail(MK_ERR_INVALID_ARG, "handle is NULL");
     if (!out_token) return fail(MK_ERR_INVALID_ARG, "out_token is NULL");
-    if (position < 0 || position >= h->cfg.max_seq)
+    if (!d_pos && (position < 0 || position >= h->cfg.max_seq))
         return fail(MK_ERR_INVALID_ARG, "position outside [0, max_seq)");
     if (!d_token && (token < 0 || token >= h->cfg.vocab))
         return fail(MK_ERR_INVALID_ARG, "token_id outside [0, vocab)");
@@ -610,7 +617,7 @@ int launch(mk_handle *h, int32_t token, const int32_t *d_token, int32_t position
     p.trace = h->trace_on ? h->d_trace : nullptr;
     p.trace_cap = h->trace_cap;
     return mkint::launch_step(p, h->im.n_sm, h->im.n_stages, token, d_token, position, out_logits,
-                              out_token, stream, unfused);
+                              out_token, stream, unfused, d_pos, bslot);
 }
 
 }  // namespace
@@ -693,6 +700,20 @@ int mk_decode_step_dev(mk_handle *h, const int32_t *d_token_id, int32_t position
     return launch(h, 0, d_token_id, position, out_logits, out_token, (cudaStream_t)stream, false);
 }
 
+int mk_decode_step_batch(mk_handle *h, const int32_t *d_tokens, const int32_t *d_positions, int32_t batch,
+                         float *out_logits, int32_t *out_tokens, void *stream) {
+    if (!h) return fail(MK_ERR_INVALID_ARG, "handle is NULL");
+    if (!d_tokens || !d_positions || !out_tokens)
+        return fail(MK_ERR_INVALID_ARG, "d_tokens, d_positions and out_tokens must not be NULL");
+    if (batch < 1 || batch > h->cfg.max_batch) return fail(MK_ERR_INVALID_ARG, "batch outside [1, max_batch]");
+    for (int32_t b = 0; b < batch; ++b) {
+        const int rc = launch(h, 0, d_tokens + b, 0, out_logits ? out_logits + (size_t)b * h->cfg.vocab : nullptr,
+                              out_tokens + b, (cudaStream_t)stream, false, d_positions + b, b);
+        if (rc) return rc;
+    }
+    return MK_OK;
+}
+
 int mk_decode_step_unfused(mk_handle *h, int32_t token_id, int32_t position, float *out_logits,
                            int32_t *out_token, void *stream) {
     return launch(h, token_id, nullptr, position, out_logits, out_token, (cudaStream_t)stream, true);
@@ -738,6 +759,7 @@ int mk_get_status(mk_handle *h) {
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return cuda_fail(e, "status reset");
     if (st == mk::DS_BAD_TOKEN) return fail(MK_ERR_INVALID_ARG, "device token outside [0, vocab)");
+    if (st == mk::DS_BAD_POS) return fail(MK_ERR_INVALID_ARG, "device position outside [0, max_seq)");
     return fail(MK_ERR_TIMEOUT, "an in-kernel dependency wait timed out");
 }
 

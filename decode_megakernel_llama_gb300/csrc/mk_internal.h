@@ -39,7 +39,7 @@ void fill_params(const Image &im, const mk_config *config, const mk_weights *w,
                  const mk_kv_cache *kv, char *base, mk::Params &p);
 int launch_step(const mk::Params &base, int n_sm, int n_stages, int32_t token,
                 const int32_t *d_token, int32_t position, float *out_logits, int32_t *out_token,
-                cudaStream_t stream, bool unfused);
+                cudaStream_t stream, bool unfused, const int32_t *d_pos = nullptr, int32_t bslot = 0);
 int set_error(int code, const char *msg);
 
 }  // namespace mkint

@@ -246,6 +246,7 @@ struct Misc {
     float red8[kConsumerWarps];
     unsigned long long best8[kConsumerWarps];
     volatile int32_t flag;      // broadcast slot
+    volatile int32_t polling;   // consumers are polling for an input (producer throttles)
     volatile int32_t aborted;   // this CTA gave up
     volatile uint32_t n_issued; // tiles issued by the producer
     uint32_t ep8;               // this step's epoch << 8
@@ -486,7 +487,7 @@ __device__ __forceinline__ TileCopy tile_copy(const Params &p, const Instr &in, 
         const int ts = r.t0 + j * p.ppt;
         int n = r.t1 - ts;
         if (n > p.ppt) n = p.ppt;
-        const size_t base = ((size_t)(in.layer * p.max_batch) * p.Hkv + in.a0) * p.max_seq * p.hd +
+        const size_t base = (((size_t)in.layer * p.max_batch + p.bslot) * p.Hkv + in.a0) * p.max_seq * p.hd +
                             (size_t)ts * p.hd;
         c.bytes0 = c.bytes1 = (uint32_t)n * p.hd * 2;
         c.src0 = p.kc + base;
@@ -584,8 +585,10 @@ __device__ void producer(const Params &p, const Ctx &cx, int qb, int qe) {
                 cx.misc->aborted = 1;
                 return;
             }
-            // at most `back` tiles in flight
-            if (t >= back && !wait_bar(p, &cx.full[(t - back) % kPages], ((t - back) / kPages) & 1)) {
+            // at most `back` tiles in flight (fewer while the consumers poll
+            // for an input, so that their loads do not queue behind tile data)
+            const uint32_t b = cx.misc->polling ? (uint32_t)p.poll_inflight : back;
+            if (t >= b && !wait_bar(p, &cx.full[(t - b) % kPages], ((t - b) / kPages) & 1)) {
                 cx.misc->aborted = 1;
                 return;
             }
@@ -683,6 +686,7 @@ __device__ bool stage_input(const Params &p, const Ctx &cx, const uint2 *src, co
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     uint16_t *gbuf = reinterpret_cast<uint16_t *>(cx.xbuf + kMaxStaged);
     bool ok = src != nullptr || src_bf != nullptr;
+    if (tid == 0 && src) cx.misc->polling = 1;
     float ss = 0.f;
     if (gain) {
         for (int i = tid * 8; i < K; i += kConsumerThreads * 8)
@@ -716,6 +720,7 @@ __device__ bool stage_input(const Params &p, const Ctx &cx, const uint2 *src, co
     ss = warp_sum(ss);
     if (lane == 0) cx.misc->red8[warp] = ss;
     ok = !consumer_sync_any(!ok);
+    if (tid == 0) cx.misc->polling = 0;
     float tot = 0.f;
 #pragma unroll
     for (int w = 0; w < kConsumerWarps; ++w) tot += cx.misc->red8[w];
@@ -995,11 +1000,15 @@ struct AttnLayout {
     static constexpr int DQ = HD / 16, PG = 32 / DQ, NPASS = 32 / PG;
     static constexpr int DGV = HD / 8, PGV = 32 / DGV;
     static constexpr int GP = G == 3 ? 4 : G;
+    // q in shared memory: head g, dim d at g*QSTR + (d/16)*20 + d%16; the
+    // 4-float pad puts the dim groups read together on different banks
+    static constexpr int QSTR = HD / 16 * 20;
+    static __device__ __forceinline__ int qidx(int g, int d) { return g * QSTR + (d >> 4) * 20 + (d & 15); }
 };
 
 // One chunk of up to 32 positions for this warp. Kp/Vp point at the chunk's
 // first key/value row (bf16, HD each); npos valid positions; q holds the G
-// pre-scaled query heads [G][HD] (fp32, shared); pbuf is this warp's
+// pre-scaled query heads (fp32, shared, AttnLayout::qidx); pbuf is this warp's
 // [32][4] scratch for the softmax weights. Scores are in log2 units; the
 // warp's online-softmax state st is updated in place. Shared-memory reads
 // are conflict-free: each K or V row is read whole by consecutive lanes
@@ -1020,7 +1029,7 @@ __device__ __forceinline__ void attn_chunk(AttnWarpState<HD, G> &st, const uint1
         float2 qr[GP][8];
 #pragma unroll
         for (int g = 0; g < GP; ++g) {
-            const float4 *qg = reinterpret_cast<const float4 *>(q + (g < G ? g : 0) * HD + dq * 16);
+            const float4 *qg = reinterpret_cast<const float4 *>(q + Lay::qidx(g < G ? g : 0, dq * 16));
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 const float4 v = g < G ? qg[c] : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -1157,13 +1166,14 @@ __device__ void do_attn_hd(const Params &p, const Ctx &cx, const Instr &in, uint
     if (tid == 0) cx.misc->staged_key = -1;  // xbuf becomes attention scratch
     const int qkv_stride = (p.Hq + 2 * p.Hkv) * HD;
     const uint2 *qkv = p.qkvll + (size_t)l * qkv_stride;
-    // shared scratch: q [G][HD] | knew [HD] bf16 | vnew [HD] bf16 | warp states
-    // [8][G][HD+2]; the host checks G*HD + HD + 8*G*(HD+2) <= kXbufFloats.
+    // shared scratch: q [G][QSTR] | knew [HD] bf16 | vnew [HD] bf16 | warp states
+    // [8][G][HD+4]; the host checks G*QSTR + HD + 8*G*(HD+4) <= kXbufFloats.
+    using Lay = AttnLayout<HD, G>;
     float *qs = cx.xbuf;
-    uint16_t *knew = reinterpret_cast<uint16_t *>(cx.xbuf + G * HD);
+    uint16_t *knew = reinterpret_cast<uint16_t *>(cx.xbuf + G * Lay::QSTR);
     uint16_t *vnew = knew + HD;
     constexpr int WS = HD + 4;  // warp-state row: HD outputs, max, sum, pad (16-byte rows)
-    float *wst = cx.xbuf + G * HD + HD;
+    float *wst = cx.xbuf + G * Lay::QSTR + HD;
     float *pbuf = cx.red + warp * (32 * kMaxG);
 
     // q of the group's heads (rotated, pre-scaled by log2(e)/sqrt(hd)) and,
@@ -1178,19 +1188,19 @@ __device__ void do_attn_hd(const Params &p, const Ctx &cx, const Instr &in, uint
             const uint2 *srcs[2] = {qh + i, qh + i + HD / 2};
             float ab[2];
             if (bad || !ll_read_n<2>(p, srcs, ep8, ab) || !CHK(rope + 2 * i, 8, 28) ||
-                !CHKS(qs + g * HD + i + HD / 2, 4, 48)) {
+                !CHKS(qs + Lay::qidx(g, i + HD / 2), 4, 48)) {
                 bad = true;
                 continue;
             }
             const float a = ab[0], b = ab[1];
             const float c = rope[2 * i], s = rope[2 * i + 1];
-            qs[g * HD + i] = (a * c - b * s) * qscale;
-            qs[g * HD + i + HD / 2] = (b * c + a * s) * qscale;
+            qs[Lay::qidx(g, i)] = (a * c - b * s) * qscale;
+            qs[Lay::qidx(g, i + HD / 2)] = (b * c + a * s) * qscale;
         }
         if (r.has_new) {
             const uint2 *kh = qkv + (size_t)p.Hq * HD + (size_t)kvh * HD;
             const uint2 *vh = qkv + (size_t)(p.Hq + p.Hkv) * HD + (size_t)kvh * HD;
-            const size_t cache_off = (((size_t)l * p.max_batch) * p.Hkv + kvh) * p.max_seq * HD +
+            const size_t cache_off = (((size_t)l * p.max_batch + p.bslot) * p.Hkv + kvh) * p.max_seq * HD +
                                      (size_t)p.pos * HD;
             for (int i = tid; i < HD / 2; i += kConsumerThreads) {
                 const uint2 *srcs[4] = {kh + i, kh + i + HD / 2, vh + i, vh + i + HD / 2};
@@ -1446,6 +1456,7 @@ __global__ void __launch_bounds__(kThreads, 1) mk_megakernel(const Params prm) {
             mbar_init(&cx.empty[i], kConsumerWarps);
         }
         cx.misc->flag = 0;
+        cx.misc->polling = 0;
         cx.misc->aborted = 0;
         cx.misc->n_issued = 0;
         cx.misc->staged_key = -1;
@@ -1455,6 +1466,8 @@ __global__ void __launch_bounds__(kThreads, 1) mk_megakernel(const Params prm) {
     __syncthreads();
     const Params &p = *sp;
     if (tid == 0) {
+        // a position held in device memory is read once, before anything uses it
+        if (p.d_pos) sp->pos = CHK(p.d_pos, 4, 33) ? *(volatile const int32_t *)p.d_pos : -1;
         uint32_t e = 1;
         if (CHK(p.epoch, 4, 32)) e = *(volatile uint32_t *)p.epoch & 0xFFFFFFu;
         cx.misc->ep8 = (e ? e : 1u) << 8;
@@ -1468,9 +1481,10 @@ __global__ void __launch_bounds__(kThreads, 1) mk_megakernel(const Params prm) {
     run = run && *(volatile int32_t *)p.status == DS_OK;
     if (run) {
         const int tok = current_token(p);
-        if (tok < 0 || tok >= p.V) {
+        const bool bad_tok = tok < 0 || tok >= p.V, bad_pos = p.pos < 0 || p.pos >= p.max_seq;
+        if (bad_tok || bad_pos) {
             if (tid == 0) {
-                atomicCAS(p.status, DS_OK, DS_BAD_TOKEN);
+                atomicCAS(p.status, DS_OK, bad_tok ? DS_BAD_TOKEN : DS_BAD_POS);
                 atomicExch(p.abort_flag, 1);
             }
             run = false;

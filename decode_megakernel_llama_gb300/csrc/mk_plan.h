@@ -129,6 +129,8 @@ struct Params {
     int32_t token;
     const int32_t *d_token; // if non-null, overrides token
     int32_t pos;
+    const int32_t *d_pos;   // if non-null, overrides pos (read once at the start of the step)
+    int32_t bslot;          // batch slot of the KV cache this step reads and appends to
     float *out_logits;      // nullable
     int32_t *out_token;
     unsigned long long timeout_ns;
@@ -136,6 +138,7 @@ struct Params {
     int32_t trace_cap;
     unsigned long long l2_lookahead;  // bytes per SM prefetched into L2 beyond the smem ring
     int32_t max_inflight;             // tiles per SM whose copies may be outstanding at once
+    int32_t poll_inflight;            // ... while the consumers poll for an instruction's input
     // address self-checks (only read by a build with MK_CHECKED defined)
     int32_t n_ranges;
     const unsigned long long *ranges;  // [n_ranges][2] valid [begin, end) byte ranges
@@ -144,6 +147,6 @@ struct Params {
 static_assert(sizeof(Params) <= kParamsSlot, "Params must fit its shared-memory slot");
 
 // Device status codes written to *status.
-enum DevStatus : int32_t { DS_OK = 0, DS_TIMEOUT = 1, DS_BAD_TOKEN = 2 };
+enum DevStatus : int32_t { DS_OK = 0, DS_TIMEOUT = 1, DS_BAD_TOKEN = 2, DS_BAD_POS = 3 };
 
 }  // namespace mk

@@ -28,7 +28,8 @@
  *   - Pointers handed to mk_create are borrowed: the caller owns them and
  *     must keep them alive and unmoved until mk_destroy. The library never
  *     writes the weights; of the KV cache it writes only row `position` of
- *     each layer (and batch slot 0) per step.
+ *     each layer of the stepping sequence's batch slot (slot 0 for the
+ *     single-sequence calls).
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream). Calls
  *     are asynchronous on it; a handle is not thread-safe and must not have
  *     two steps in flight on different streams at once.
@@ -62,7 +63,7 @@ typedef enum mk_status {
 typedef struct mk_config {
     int32_t n_layers, d_model, n_heads, n_kv_heads, head_dim, ffn_dim, vocab;
     int32_t max_seq;     /* positions in the KV cache per sequence */
-    int32_t max_batch;   /* sequences in the KV cache (batch slot 0 is used) */
+    int32_t max_batch;   /* sequences in the KV cache (slot 0 for the single-sequence calls) */
     int32_t attn_splits; /* KV splits per kv head for attention, 0 = automatic */
     float rms_eps, rope_theta;
 } mk_config;
@@ -118,6 +119,19 @@ int mk_decode_step_dev(mk_handle *h, const int32_t *d_token_id, int32_t position
  * stream. host buffers should be pinned for asynchronous copies. */
 int mk_decode_step_host(mk_handle *h, const int32_t *host_token, int32_t position,
                         float *host_logits, int32_t *host_out_token, void *stream);
+
+/* One decode step for each of `batch` sequences (1 <= batch <= max_batch):
+ * sequence b reads its token from d_tokens[b] and its position from
+ * d_positions[b] (device int32 arrays, read when its step runs, so both can
+ * be produced by the previous step on the device), attends over batch slot b
+ * of the KV cache, appends its key/value row at its position, and writes its
+ * greedy token to out_tokens[b] (device int32[batch]) and, if out_logits is
+ * not NULL, its logits to out_logits[b*vocab .. ] (device float[batch][vocab]).
+ * The sequences run one fused step after another on `stream` (one launch
+ * each, in batch order); a device token or position out of range is reported
+ * by mk_get_status (MK_ERR_INVALID_ARG) and that sequence's step does nothing. */
+int mk_decode_step_batch(mk_handle *h, const int32_t *d_tokens, const int32_t *d_positions, int32_t batch,
+                         float *out_logits, int32_t *out_tokens, void *stream);
 
 /* The same step as a chain of separate kernel launches, one per stage
  * (QKV, attention, O-projection, gate/up, down per layer; LM head), with the

@@ -1,0 +1,116 @@
+"""GPU parity of the batched entry point (mk_decode_step_batch): each
+sequence of the batch against its own oracle twin, teacher-forced, with
+device-resident tokens and positions and one KV-cache slot per sequence."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from decode_megakernel_llama_gb300 import _lib, synth
+from decode_megakernel_llama_gb300.build import build
+from decode_megakernel_llama_gb300.configs import LLAMA_1B, TINY
+
+from gpu_helpers import compare, oracle_config
+
+pytestmark = pytest.mark.gpu
+
+
+class BatchPair:
+    def __init__(self, shape, max_seq: int, batch: int):
+        build()
+        dev = torch.device("cuda:0")
+        self.shape, self.B = shape, batch
+        self.w = synth.make_weights(shape, dev, 0)
+        self.k, self.v = synth.kv_cache(shape, max_seq, batch, dev)
+        self.mk = _lib.Megakernel(shape, self.w, self.k, self.v)
+        hw = synth.host_weights(self.w)
+        self.orc = [oracle.OracleModel(oracle_config(shape), hw, max_seq) for _ in range(batch)]
+        self.tok_in = torch.zeros(batch, dtype=torch.int32, device=dev)
+        self.pos_in = torch.zeros(batch, dtype=torch.int32, device=dev)
+        self.tok_out = torch.zeros(batch, dtype=torch.int32, device=dev)
+        self.logits = torch.empty(batch, shape.vocab, dtype=torch.float32, device=dev)
+
+    def step(self, tokens, positions):
+        self.tok_in.copy_(torch.tensor(tokens, dtype=torch.int32))
+        self.pos_in.copy_(torch.tensor(positions, dtype=torch.int32))
+        self.mk.step_batch(self.tok_in, self.pos_in, self.tok_out, self.logits)
+        torch.cuda.synchronize()
+        assert self.mk.status() == 0, _lib.load().mk_last_error()
+        return self.logits.double().cpu().numpy(), self.tok_out.cpu().numpy().tolist()
+
+    def close(self):
+        self.mk.close()
+
+
+def run_lockstep(bp: BatchPair, prompts, n_decode: int, check_from: int = 0):
+    nxt = [None] * bp.B
+    n = len(prompts[0])
+    for i in range(n + n_decode):
+        toks = [int(prompts[b][i]) if i < n else nxt[b] for b in range(bp.B)]
+        gl, gt = bp.step(toks, [i] * bp.B)
+        for b in range(bp.B):
+            ol, ot = bp.orc[b].decode_step(toks[b], i)
+            if i >= check_from:
+                compare(gl[b], gt[b], ol, ot, f"seq {b} step {i}")
+            nxt[b] = ot
+
+
+def test_tiny_batch3_lockstep_teacher_forced(cuda_dev):
+    bp = BatchPair(TINY, 24, 3)
+    prompts = [synth.prompt_tokens(TINY.vocab, 6, seq=b) for b in range(3)]
+    run_lockstep(bp, prompts, 10)
+    bp.close()
+
+
+def test_tiny_batch_positions_differ_per_sequence(cuda_dev):
+    # sequence 0 runs two steps ahead through the single-sequence call (slot 0),
+    # then both advance together at different positions
+    bp = BatchPair(TINY, 24, 2)
+    torch_tok = torch.zeros(1, dtype=torch.int32, device="cuda:0")
+    lg = torch.empty(TINY.vocab, dtype=torch.float32, device="cuda:0")
+    for pos, tok in enumerate([17, 230]):
+        bp.mk.step(tok, pos, torch_tok, lg)
+        bp.orc[0].decode_step(tok, pos)
+    torch.cuda.synchronize()
+    toks = [[5, 6, 7], [900, 901, 902]]
+    for i in range(3):
+        gl, gt = bp.step([toks[0][i], toks[1][i]], [2 + i, i])
+        ol0, ot0 = bp.orc[0].decode_step(toks[0][i], 2 + i)
+        ol1, ot1 = bp.orc[1].decode_step(toks[1][i], i)
+        compare(gl[0], gt[0], ol0, ot0, f"seq 0 step {i}")
+        compare(gl[1], gt[1], ol1, ot1, f"seq 1 step {i}")
+    bp.close()
+
+
+def test_batch_slot0_equals_single_sequence_step(cuda_dev):
+    a = BatchPair(TINY, 16, 2)
+    b = BatchPair(TINY, 16, 2)
+    out = torch.zeros(1, dtype=torch.int32, device="cuda:0")
+    lg = torch.empty(TINY.vocab, dtype=torch.float32, device="cuda:0")
+    for pos, tok in enumerate([3, 1, 4, 1, 5]):
+        la, _ = a.step([tok, 9], [pos, pos])
+        b.mk.step(tok, pos, out, lg)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(la[0], lg.double().cpu().numpy())
+    a.close()
+    b.close()
+
+
+def test_device_position_out_of_range_sets_status(cuda_dev):
+    bp = BatchPair(TINY, 8, 2)
+    bp.tok_in.copy_(torch.tensor([1, 2], dtype=torch.int32))
+    bp.pos_in.copy_(torch.tensor([0, 8], dtype=torch.int32))  # 8 == max_seq
+    bp.mk.step_batch(bp.tok_in, bp.pos_in, bp.tok_out, bp.logits)
+    torch.cuda.synchronize()
+    assert bp.mk.status() == _lib.MK_ERR_INVALID_ARG
+    with pytest.raises(_lib.MKError):
+        bp.mk.step_batch(bp.tok_in[:0], bp.pos_in[:0], bp.tok_out, bp.logits)  # batch 0
+    bp.close()
+
+
+def test_llama1b_batch8_short_lockstep(cuda_dev):
+    # the batch-8 workload's shape, on short prompts so the oracle keeps up
+    bp = BatchPair(LLAMA_1B, 8, 8)
+    prompts = [synth.prompt_tokens(LLAMA_1B.vocab, 3, seq=b) for b in range(8)]
+    run_lockstep(bp, prompts, 1, check_from=2)
+    bp.close()
