@@ -74,7 +74,8 @@ def measured_peak():
 
 def kernel_sha() -> str:
     h = hashlib.sha256()
-    for f in ("mk_kernel.cu", "mk_plan.h", "mk_host.cpp"):
+    for f in ("mk_kernel.cuh", "mk_kernel_hd64.cu", "mk_kernel_hd128.cu", "mk_kernel.cu", "mk_plan.h",
+              "mk_host.cpp"):
         h.update(open(os.path.join(ROOT, "decode_megakernel_llama_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 
