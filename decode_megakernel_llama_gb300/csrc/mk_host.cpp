@@ -66,7 +66,24 @@ bool make_geo(int K, Geo &g, int max_nx = 32) {
     return true;
 }
 
+// Batched steps: tiles of rt rows x a K-chunk of KC = min(K, 2048) columns,
+// 8 rows and a 256-wide slice per warp (see mk_plan.h).
+bool make_geo_batch(int K, Geo &g) {
+    const int KC = std::min(K, 2048);
+    if (K <= 0 || K % KC != 0 || (KC != 256 && KC != 512 && KC != 1024 && KC != 2048)) return false;
+    g.K = K;
+    g.sw = KC / 256;
+    g.rw = mk::kConsumerWarps / g.sw;
+    g.m = 8;
+    g.rt = g.rw * g.m;
+    g.nx = 8;
+    g.kslice = 256;
+    g.pad = KC;
+    return g.rt * KC * 2 <= mk::kPageBytes;
+}
+
 struct Plan {
+    int nb = 1;  // sequences of one step
     int n_sm = 0, S = 1, ppt = 0, n_lm = 0, n_stages = 0;
     mk::CtrLayout cl{};
     Geo geo_qkv{}, geo_o{}, geo_gu{}, geo_down{}, geo_lm{};
@@ -138,7 +155,7 @@ std::vector<Chunk> split_rows(int N, double cost_per_row, std::vector<double> &l
     return out;
 }
 
-int build_plan(const mk_config *c, int n_sm, Plan &P) {
+int build_plan(const mk_config *c, int n_sm, Plan &P, int nb) {
     int rc = check_config(c);
     if (rc) return rc;
     if (n_sm < 1 || n_sm > 4096) return fail(MK_ERR_INVALID_ARG, "bad SM count");
@@ -147,9 +164,21 @@ int build_plan(const mk_config *c, int n_sm, Plan &P) {
     const int qd = Hq * hd, kvd = Hkv * hd;
     P = Plan();
     P.n_sm = n_sm;
-    if (!make_geo(d, P.geo_qkv) || !make_geo(qd, P.geo_o) || !make_geo(d, P.geo_gu) ||
-        !make_geo(F, P.geo_down) || !make_geo(d, P.geo_lm))
+    P.nb = nb;
+    if (nb > 1) {
+        // batched steps: hd 64 instances, normed inputs in one K-chunk
+        if (nb > mk::kMaxBatch || hd != 64 || d > 2048 || !make_geo_batch(d, P.geo_qkv) ||
+            !make_geo_batch(qd, P.geo_o) || !make_geo_batch(d, P.geo_gu) || !make_geo_batch(F, P.geo_down) ||
+            !make_geo_batch(d, P.geo_lm))
+            return fail(MK_ERR_UNSUPPORTED, "no batched tile geometry for this model");
+        // LM-head rows per SM beyond the shared accumulators run through a ring
+        // of 8 tiles, which needs tiles of at most 32 rows
+        if ((V + n_sm - 1) / n_sm * mk::kMaxBatch > mk::kRedCap && P.geo_lm.rt * 8 * mk::kMaxBatch > mk::kRedCap)
+            return fail(MK_ERR_UNSUPPORTED, "no batched LM-head geometry for this model");
+    } else if (!make_geo(d, P.geo_qkv) || !make_geo(qd, P.geo_o) || !make_geo(d, P.geo_gu) ||
+               !make_geo(F, P.geo_down) || !make_geo(d, P.geo_lm)) {
         return fail(MK_ERR_UNSUPPORTED, "no tile geometry for these input lengths");
+    }
     if (P.geo_gu.rt < 2 || P.geo_gu.rt % 2)
         return fail(MK_ERR_UNSUPPORTED, "gate/up tile needs an even row count");
     P.ppt = (mk::kPageBytes / 2) / (hd * 2);
@@ -183,17 +212,21 @@ int build_plan(const mk_config *c, int n_sm, Plan &P) {
         in.bytes_lo = (int32_t)(b & 0xFFFFFFFFll);
         in.bytes_hi = (int32_t)(b >> 32);
     };
-    const int cap_qkv = mk::kRedCap / P.geo_qkv.sw,
-              cap_o = std::min(mk::kRedCap / P.geo_o.sw, mk::kResidFloats),
-              cap_gu = mk::kRedCap / (2 * P.geo_gu.sw),
-              cap_down = std::min(mk::kDredFloats / P.geo_down.sw, mk::kResidFloats),
-              cap_lm = mk::kRedCap / P.geo_lm.sw;
+    // rows per instruction: what the per-row partials (batched: the shared
+    // accumulators and the residual rows of every sequence) can hold
+    const int cap_qkv = nb > 1 ? mk::kRedCap / mk::kMaxBatch : mk::kRedCap / P.geo_qkv.sw,
+              cap_o = nb > 1 ? std::min(mk::kRedCap / mk::kMaxBatch, mk::kResidFloats / nb)
+                             : std::min(mk::kRedCap / P.geo_o.sw, mk::kResidFloats),
+              cap_gu = nb > 1 ? mk::kRedCap / (2 * mk::kMaxBatch) : mk::kRedCap / (2 * P.geo_gu.sw),
+              cap_down = nb > 1 ? std::min(mk::kRedCap / mk::kMaxBatch, mk::kResidFloats / nb)
+                                : std::min(mk::kDredFloats / P.geo_down.sw, mk::kResidFloats),
+              cap_lm = nb > 1 ? 1 << 20 : mk::kRedCap / P.geo_lm.sw;
     // Short contexts: the attention of a layer runs on SMs that get no QKV
     // rows, so it starts as soon as q/k/v are published and its cached
     // keys/values are prefetched at the start of the layer. Long contexts
     // spread attention (and its KV streaming) over every SM instead.
     const double attn_cost = 2.0 * 2.0 * hd * std::ceil((double)c->max_seq / S) + 4096.0;
-    const bool dedicated_attn = Hkv * S * 4 <= n_sm;
+    const bool dedicated_attn = Hkv * S * nb * 4 <= n_sm;
     int prev_down = 0;
     for (int l = 0; l < L; ++l) {
         const int st = mk::kStagesPerLayer * l;
@@ -204,7 +237,7 @@ int build_plan(const mk_config *c, int n_sm, Plan &P) {
             std::vector<int> order(n_sm);
             std::iota(order.begin(), order.end(), 0);
             std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return load[a] < load[b]; });
-            for (int i = 0; i < Hkv * S; ++i) {
+            for (int i = 0; i < Hkv * S * nb; ++i) {
                 attn_sm.push_back(order[i]);
                 excluded[order[i]] = 1;
             }
@@ -242,15 +275,17 @@ int build_plan(const mk_config *c, int n_sm, Plan &P) {
             set_bytes(in, 2ll * in.a1 * d);
             P.q[ch.sm].push_back(in);
         }
-        // ---- attention: Hkv x S splits
+        // ---- attention: Hkv x S splits (x nb sequences; `mat` = sequence)
+        for (int b = 0; b < nb; ++b)
         for (int h = 0; h < Hkv; ++h)
             for (int s = 0; s < S; ++s) {
-                int sm = dedicated_attn ? attn_sm[h * S + s]
+                int sm = dedicated_attn ? attn_sm[(b * Hkv + h) * S + s]
                                         : (int)(std::min_element(load.begin(), load.end()) - load.begin());
                 load[sm] += attn_cost;
                 Instr in = mk_instr(mk::OP_ATTN, l, st + 1);
                 in.a0 = h;
                 in.a1 = s;
+                in.mat = b;
                 in.wait_ctr = cl.qkv_grp + l * Hkv + h;
                 in.wait_target = touch[h];
                 P.q[sm].push_back(in);
@@ -381,11 +416,11 @@ int check_device(int *dev, int *n_sm) {
     return MK_OK;
 }
 
-int make_image(const mk_config *config, const mk_weights *w, int n_sm, Image &im) {
+int make_image(const mk_config *config, const mk_weights *w, int n_sm, Image &im, int nb) {
     im = Image();
     im.impl = std::make_shared<ImageImpl>();
     Plan &P = im.impl->plan;
-    int rc = build_plan(config, n_sm, P);
+    int rc = build_plan(config, n_sm, P, nb);
     if (rc) return rc;
     const mk_config &c = *config;
     const int L = c.n_layers, d = c.d_model, Hq = c.n_heads, Hkv = c.n_kv_heads, hd = c.head_dim,
@@ -433,15 +468,15 @@ int make_image(const mk_config *config, const mk_weights *w, int n_sm, Image &im
     im.o_zero_end = b.off;
     im.o_layers = b.take(sizeof(mk::LayerW) * L);
     im.o_epoch = b.take(sizeof(uint32_t));
-    im.o_x = b.take(8 * (size_t)d);  // tagged words {value, tag}
-    im.o_qkv = b.take(8 * (size_t)L * (Hq + 2 * Hkv) * hd);
-    im.o_part = b.take(8 * (size_t)L * Hq * P.S * (hd + 2));
-    im.o_att = b.take(8 * (size_t)L * Hq * hd);
-    im.o_h = b.take(8 * (size_t)L * F);
-    im.o_lm = b.take(sizeof(unsigned long long) * P.n_lm);
-    im.o_tin = b.take(sizeof(int32_t));
-    im.o_tout = b.take(sizeof(int32_t));
-    im.o_logits = b.take(sizeof(float) * V);
+    im.o_x = b.take(8 * (size_t)nb * d);  // tagged words {value, tag}, one row per sequence
+    im.o_qkv = b.take(8 * (size_t)L * nb * (Hq + 2 * Hkv) * hd);
+    im.o_part = b.take(8 * (size_t)L * nb * Hq * P.S * (hd + 2));
+    im.o_att = b.take(8 * (size_t)L * nb * Hq * hd);
+    im.o_h = b.take(8 * (size_t)L * nb * F);
+    im.o_lm = b.take(sizeof(unsigned long long) * nb * P.n_lm);
+    im.o_tin = b.take(sizeof(int32_t) * nb);
+    im.o_tout = b.take(sizeof(int32_t) * nb);
+    im.o_logits = b.take(sizeof(float) * nb * V);
     im.o_rope = b.take(sizeof(float) * im.rope.size());
     im.o_instr = b.take(sizeof(Instr) * im.flat.size());
     im.o_qbeg = b.take(sizeof(int32_t) * im.qbeg.size());
@@ -460,6 +495,7 @@ void fill_params(const Image &im, const mk_config *config, const mk_weights *w,
     p.F = c.ffn_dim; p.V = c.vocab; p.max_seq = c.max_seq; p.max_batch = c.max_batch;
     p.S = P.S; p.G = c.n_heads / c.n_kv_heads; p.ppt = P.ppt; p.eps = c.rms_eps;
     p.n_lm = P.n_lm; p.n_stages = P.n_stages;
+    p.nb = P.nb;
     p.geo_qkv = P.geo_qkv; p.geo_o = P.geo_o; p.geo_gu = P.geo_gu; p.geo_down = P.geo_down;
     p.geo_lm = P.geo_lm;
     p.cl = P.cl;
@@ -486,13 +522,14 @@ void fill_params(const Image &im, const mk_config *config, const mk_weights *w,
     p.ranges = reinterpret_cast<const unsigned long long *>(base + im.o_ranges);
     p.dbg = reinterpret_cast<unsigned long long *>(base + im.o_dbg);
     p.timeout_ns = 2000000000ull;
-    p.l2_lookahead = 0;
-    if (const char *env = getenv("MK_L2_LOOKAHEAD_KB")) p.l2_lookahead = strtoull(env, nullptr, 10) << 10;
     p.max_inflight = 3;
     if (const char *env = getenv("MK_MAX_INFLIGHT")) p.max_inflight = atoi(env);
     if (p.max_inflight < 1) p.max_inflight = 1;
     if (p.max_inflight > mk::kPages) p.max_inflight = mk::kPages;
     p.poll_inflight = 1;  // while consumers poll, keep their loads from queuing behind tile data
+    p.l2_tiles = 0;
+    if (const char *env = getenv("MK_L2_TILES")) p.l2_tiles = atoi(env);
+    if (p.l2_tiles < 0) p.l2_tiles = 0;
     if (const char *env = getenv("MK_POLL_INFLIGHT")) p.poll_inflight = atoi(env);
     if (p.poll_inflight < 1) p.poll_inflight = 1;
     if (p.poll_inflight > p.max_inflight) p.poll_inflight = p.max_inflight;
@@ -597,6 +634,13 @@ struct mk_handle {
     long long *d_trace = nullptr;
     int trace_cap = 0;
     bool trace_on = false;
+    // batched steps of all max_batch sequences in one launch (max_batch > 1 and
+    // a model the batched instances support), with their own scratch
+    bool has_batch = false;
+    mkint::Image bim;
+    mk::Params bbase{};
+    void *bdev_mem = nullptr;
+    size_t bzero_bytes = 0;
 };
 
 namespace {
@@ -629,7 +673,7 @@ const char *mk_last_error(void) { return g_err.c_str(); }
 int mk_plan_inspect(const mk_config *config, int32_t n_sm, int32_t *out_instr, int32_t cap,
                     int32_t *out_queue_len, int32_t *out_n_counters) {
     Plan P;
-    int rc = build_plan(config, n_sm, P);
+    int rc = build_plan(config, n_sm, P, 1);
     if (rc) return rc;
     const size_t n = P.n_instr();
     if (out_queue_len)
@@ -675,6 +719,27 @@ int mk_create(const mk_config *config, const mk_weights *w, const mk_kv_cache *k
         return rc;
     }
     mkint::fill_params(h->im, config, w, kv, base, h->base);
+    if (config->max_batch > 1 && config->max_batch <= mk::kMaxBatch &&
+        mkint::make_image(config, w, n_sm, h->bim, config->max_batch) == MK_OK) {
+        e = cudaMalloc(&h->bdev_mem, h->bim.total);
+        if (e != cudaSuccess) {
+            cudaFree(h->dev_mem);
+            delete h;
+            return cuda_fail(e, "cudaMalloc(batched scratch)");
+        }
+        char *bb = static_cast<char *>(h->bdev_mem);
+        rc = mkint::upload_image(h->bim, config, w, kv, bb, nullptr);
+        if (rc) {
+            cudaFree(h->bdev_mem);
+            cudaFree(h->dev_mem);
+            delete h;
+            return rc;
+        }
+        mkint::fill_params(h->bim, config, w, kv, bb, h->bbase);
+        h->bzero_bytes = h->bim.o_zero_end - h->bim.o_ctr;
+        h->has_batch = true;
+    }
+    fail(MK_OK, "");  // a model without batched instances is not an error
     h->d_tok_in = reinterpret_cast<int32_t *>(base + h->im.o_tin);
     h->d_tok_out = reinterpret_cast<int32_t *>(base + h->im.o_tout);
     h->d_logits = reinterpret_cast<float *>(base + h->im.o_logits);
@@ -706,6 +771,15 @@ int mk_decode_step_batch(mk_handle *h, const int32_t *d_tokens, const int32_t *d
     if (!d_tokens || !d_positions || !out_tokens)
         return fail(MK_ERR_INVALID_ARG, "d_tokens, d_positions and out_tokens must not be NULL");
     if (batch < 1 || batch > h->cfg.max_batch) return fail(MK_ERR_INVALID_ARG, "batch outside [1, max_batch]");
+    if (h->has_batch && batch == h->cfg.max_batch) {
+        // all sequences in one launch: every weight tile read once for all of them
+        cudaError_t e = cudaSetDevice(h->device);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaSetDevice");
+        mk::Params p = h->bbase;
+        p.timeout_ns = h->timeout_ns;
+        return mkint::launch_step(p, h->bim.n_sm, h->bim.n_stages, 0, d_tokens, 0, out_logits, out_tokens,
+                                  (cudaStream_t)stream, false, d_positions, 0);
+    }
     for (int32_t b = 0; b < batch; ++b) {
         const int rc = launch(h, 0, d_tokens + b, 0, out_logits ? out_logits + (size_t)b * h->cfg.vocab : nullptr,
                               out_tokens + b, (cudaStream_t)stream, false, d_positions + b, b);
@@ -750,14 +824,17 @@ int mk_get_status(mk_handle *h) {
     cudaError_t e = cudaSetDevice(h->device);
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
-    int32_t st = 0;
+    int32_t st = 0, bst = 0;
     e = cudaMemcpy(&st, h->base.status, sizeof st, cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess && h->has_batch) e = cudaMemcpy(&bst, h->bbase.status, sizeof bst, cudaMemcpyDeviceToHost);
     if (e != cudaSuccess) return cuda_fail(e, "status read");
-    if (st == mk::DS_OK) return MK_OK;
+    if (st == mk::DS_OK && bst == mk::DS_OK) return MK_OK;
     // a failed step leaves counters mid-way: clear them with the status
     e = cudaMemset(h->base.ctr, 0, h->zero_bytes);
+    if (e == cudaSuccess && h->has_batch) e = cudaMemset(h->bbase.ctr, 0, h->bzero_bytes);
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return cuda_fail(e, "status reset");
+    if (st == mk::DS_OK) st = bst;
     if (st == mk::DS_BAD_TOKEN) return fail(MK_ERR_INVALID_ARG, "device token outside [0, vocab)");
     if (st == mk::DS_BAD_POS) return fail(MK_ERR_INVALID_ARG, "device position outside [0, max_seq)");
     return fail(MK_ERR_TIMEOUT, "an in-kernel dependency wait timed out");
@@ -838,6 +915,7 @@ void mk_destroy(mk_handle *h) {
     cudaDeviceSynchronize();
     if (h->d_trace) cudaFree(h->d_trace);
     if (h->dev_mem) cudaFree(h->dev_mem);
+    if (h->bdev_mem) cudaFree(h->bdev_mem);
     delete h;
 }
 

@@ -32,7 +32,7 @@ struct Image {
 
 int check_inputs(const mk_config *config, const mk_weights *w, const mk_kv_cache *kv);
 int check_device(int *dev, int *n_sm);
-int make_image(const mk_config *config, const mk_weights *w, int n_sm, Image &im);
+int make_image(const mk_config *config, const mk_weights *w, int n_sm, Image &im, int nb = 1);
 int upload_image(const Image &im, const mk_config *config, const mk_weights *w,
                  const mk_kv_cache *kv, char *base, cudaStream_t s);
 void fill_params(const Image &im, const mk_config *config, const mk_weights *w,

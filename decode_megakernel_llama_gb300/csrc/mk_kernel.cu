@@ -6,30 +6,35 @@
 #include "mk_plan.h"
 
 extern "C" const void *mk_kernel_fn_hd64(int G);
+extern "C" const void *mk_kernel_fn_hd64_batch(int G);
 extern "C" const void *mk_kernel_fn_hd128(int G);
 
 namespace {
-// instance for head dim hd (64 or 128) and G query heads per kv head (1..4)
-const void *kernel_for(int hd, int G) {
-    if (hd == 64) return mk_kernel_fn_hd64(G);
-    if (hd == 128) return mk_kernel_fn_hd128(G);
+// instance for head dim hd (64 or 128), G query heads per kv head (1..4) and
+// single-sequence or batched steps (batched: hd 64 only)
+const void *kernel_for(int hd, int G, bool batch = false) {
+    if (hd == 64) return batch ? mk_kernel_fn_hd64_batch(G) : mk_kernel_fn_hd64(G);
+    if (hd == 128 && !batch) return mk_kernel_fn_hd128(G);
     return nullptr;
 }
 }  // namespace
 
 extern "C" cudaError_t mk_kernel_configure(void) {
     for (int hd : {64, 128})
-        for (int G = 1; G <= 4; ++G) {
-            const cudaError_t e = cudaFuncSetAttribute(kernel_for(hd, G), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                       mk::kSmemBytes);
-            if (e != cudaSuccess) return e;
-        }
+        for (int G = 1; G <= 4; ++G)
+            for (bool batch : {false, true}) {
+                const void *fn = kernel_for(hd, G, batch);
+                if (!fn) continue;
+                const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                           mk::kSmemBytes);
+                if (e != cudaSuccess) return e;
+            }
     return cudaSuccess;
 }
 
 extern "C" cudaError_t mk_kernel_launch(const mk::Params *p, int n_sm, int cooperative,
                                         cudaStream_t stream) {
-    const void *fn = kernel_for(p->hd, p->G);
+    const void *fn = kernel_for(p->hd, p->G, p->nb > 1);
     if (!fn) return cudaErrorInvalidValue;
     void *args[] = {const_cast<mk::Params *>(p)};
     if (cooperative)

@@ -421,10 +421,16 @@ __device__ __forceinline__ const Geo &geo_of(const Params &p, int op) {
     }
 }
 
-__device__ __forceinline__ int current_token(const Params &p) {
-    if (p.d_token && !CHK(p.d_token, 4, 33)) return -1;
-    return p.d_token ? *(volatile const int32_t *)p.d_token : p.token;
+__device__ __forceinline__ int current_token(const Params &p, int b = 0) {
+    if (p.d_token && !CHK(p.d_token + b, 4, 33)) return -1;
+    return p.d_token ? *(volatile const int32_t *)(p.d_token + b) : p.token;
 }
+
+// Sequence of an instruction in a batched step (attention instructions carry
+// it in `mat`), its position and its KV-cache slot.
+__device__ __forceinline__ int seq_of(const Params &p, const Instr &in) { return p.nb > 1 ? in.mat : 0; }
+__device__ __forceinline__ int pos_of(const Params &p, int b) { return p.nb > 1 ? p.posb[b] : p.pos; }
+__device__ __forceinline__ int slot_of(const Params &p, int b) { return p.nb > 1 ? b : p.bslot; }
 
 // ---------------------------------------------------------------------------
 // Attention split bookkeeping (identical on producer and consumer side).
@@ -436,35 +442,36 @@ struct AttnRange {
     int active, t0, t1, has_new;
 };
 
-__device__ __forceinline__ int attn_seff(const Params &p) {
+__device__ __forceinline__ int attn_seff(const Params &p, int pos) {
     const int per = p.ppt * kMinSplitTiles;
-    int need = (p.pos + per - 1) / per;
+    int need = (pos + per - 1) / per;
     if (need < 1) need = 1;
     return need < p.S ? need : p.S;
 }
 
-__device__ __forceinline__ AttnRange attn_range(const Params &p, int split) {
+__device__ __forceinline__ AttnRange attn_range(const Params &p, int split, int pos) {
     AttnRange r;
-    const int seff = attn_seff(p);
+    const int seff = attn_seff(p, pos);
     r.active = split < seff;
-    const int chunk = (p.pos + seff - 1) / seff;
+    const int chunk = (pos + seff - 1) / seff;
     r.t0 = split * chunk;
-    if (r.t0 > p.pos) r.t0 = p.pos;
+    if (r.t0 > pos) r.t0 = pos;
     r.t1 = r.t0 + chunk;
-    if (r.t1 > p.pos) r.t1 = p.pos;
+    if (r.t1 > pos) r.t1 = pos;
     r.has_new = (split == seff - 1);
     return r;
 }
 
 __device__ __forceinline__ int num_tiles(const Params &p, const Instr &in) {
     if (in.op == OP_ATTN) {
-        const AttnRange r = attn_range(p, in.a1);
+        const AttnRange r = attn_range(p, in.a1, pos_of(p, seq_of(p, in)));
         if (!r.active) return 0;
         return (r.t1 - r.t0 + p.ppt - 1) / p.ppt;
     }
     const Geo &g = geo_of(p, in.op);
     const int per = (in.op == OP_GATEUP) ? g.rt / 2 : g.rt;
-    return (in.a1 + per - 1) / per;
+    const int nrb = (in.a1 + per - 1) / per;
+    return p.nb > 1 ? nrb * (g.K / g.pad) : nrb;  // batched: one tile per (K-chunk, row block)
 }
 
 // ---------------------------------------------------------------------------
@@ -483,11 +490,12 @@ __device__ __forceinline__ TileCopy tile_copy(const Params &p, const Instr &in, 
     c.bytes1 = 0;
     c.dst1 = 0;
     if (in.op == OP_ATTN) {
-        const AttnRange r = attn_range(p, in.a1);
+        const int b = seq_of(p, in);
+        const AttnRange r = attn_range(p, in.a1, pos_of(p, b));
         const int ts = r.t0 + j * p.ppt;
         int n = r.t1 - ts;
         if (n > p.ppt) n = p.ppt;
-        const size_t base = (((size_t)in.layer * p.max_batch + p.bslot) * p.Hkv + in.a0) * p.max_seq * p.hd +
+        const size_t base = (((size_t)in.layer * p.max_batch + slot_of(p, b)) * p.Hkv + in.a0) * p.max_seq * p.hd +
                             (size_t)ts * p.hd;
         c.bytes0 = c.bytes1 = (uint32_t)n * p.hd * 2;
         c.src0 = p.kc + base;
@@ -537,63 +545,138 @@ __device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
-// ---------------------------------------------------------------------------
-// Producer: walks the same queue as the consumers and issues every tile into
-// the page ring. Optionally a second cursor prefetches tiles up to
-// p.l2_lookahead bytes beyond the ring into L2.
-// ---------------------------------------------------------------------------
-struct PrefetchCursor {
-    int i, j, nt;
-    unsigned long long bytes;  // bytes of all tiles before (i, j)
+// Second walk over the queue, ahead of the ring: tiles the ring cannot hold
+// yet are pulled into L2 while the producer would otherwise wait for a free
+// page, so HBM keeps streaming through dependency waits and the tiles of the
+// next instructions later land from L2.
+struct L2Cursor {
+    int i, j, nt;  // instruction, tile within it, its tile count
+    uint32_t t;    // global tile index of (i, j)
 };
 
-__device__ void prefetch_until(const Params &p, PrefetchCursor &pc, int qe, unsigned long long limit,
-                               unsigned long long filled) {
-    while (pc.i < qe && pc.bytes < limit) {
-        if (pc.j >= pc.nt) {
-            ++pc.i;
-            pc.j = 0;
-            if (pc.i < qe) pc.nt = num_tiles(p, load_instr(p, pc.i));
-            continue;
-        }
-        const Instr in = load_instr(p, pc.i);
-        const TileCopy c = tile_copy(p, in, pc.j);
-        if (pc.bytes >= filled) {  // tiles already in the ring need no prefetch
-            if (CHK(c.src0, c.bytes0, 35)) prefetch_l2(c.src0, c.bytes0);
-            if (c.bytes1 && CHK(c.src1, c.bytes1, 36)) prefetch_l2(c.src1, c.bytes1);
-        }
-        pc.bytes += c.bytes0 + c.bytes1;
-        ++pc.j;
+__device__ __forceinline__ void l2_advance(const Params &p, L2Cursor &c, int qe) {
+    ++c.t;
+    if (++c.j < c.nt) return;
+    c.j = 0;
+    c.nt = 0;
+    while (++c.i < qe && (c.nt = num_tiles(p, load_instr(p, c.i))) == 0) {
     }
 }
 
+__device__ __forceinline__ void l2_prefetch_tile(const Params &p, const L2Cursor &c) {
+    const TileCopy tc = tile_copy(p, load_instr(p, c.i), c.j);
+    if (CHK(tc.src0, tc.bytes0, 35)) prefetch_l2(tc.src0, tc.bytes0);
+    if (tc.bytes1 && CHK(tc.src1, tc.bytes1, 36)) prefetch_l2(tc.src1, tc.bytes1);
+}
+
+// ---------------------------------------------------------------------------
+// Producer: walks the same queue as the consumers and issues every tile into
+// the page ring. Per instruction it resolves the tile sources once; per tile
+// it only advances pointers (GEMV tiles of one instruction are equally
+// strided rows of one or two matrices).
+// ---------------------------------------------------------------------------
 __device__ void producer(const Params &p, const Ctx &cx, int qb, int qe) {
     const uint64_t pol = policy_evict_first();
-    const unsigned long long la = p.l2_lookahead;
-    PrefetchCursor pc{qb, 0, qb < qe ? num_tiles(p, load_instr(p, qb)) : 0, 0ull};
-    unsigned long long filled = 0;  // bytes issued into the ring
     uint32_t t = 0;
-    const uint32_t back = (uint32_t)p.max_inflight;
+    int pg = 0;         // page of tile t
+    uint32_t use = 0;   // how many times page pg has been filled before (parity of its phase)
+    const uint32_t back = (uint32_t)p.max_inflight, pback = (uint32_t)p.poll_inflight;
+    const uint32_t la = p.nb > 1 ? 0u : (uint32_t)p.l2_tiles;  // tiles beyond the ring pulled into L2
+    L2Cursor lc{qb, 0, qb < qe ? num_tiles(p, load_instr(p, qb)) : 0, 0u};
+    if (lc.nt == 0 && qb < qe) {
+        lc.j = -1;
+        l2_advance(p, lc, qe);
+        lc.t = 0;
+    }
     for (int i = qb; i < qe; ++i) {
         const Instr in = load_instr(p, i);
         if (i + 1 < qe) prefetch_instr(p, i + 1);
         const int nt = num_tiles(p, in);
+        // batched steps: tile j = (K-chunk j / nrb, row block j % nrb)
+        const bool batched = p.nb > 1 && in.op != OP_ATTN;
+        int nrb = 1, nkc = 1, KC = 0, bper = 0;
+        const uint16_t *rowmat = nullptr;  // matrix of the per-row copies (K-chunked tiles)
+        if (batched) {
+            const Geo &g = geo_of(p, in.op);
+            KC = g.pad;
+            nkc = g.K / KC;
+            bper = in.op == OP_GATEUP ? g.rt / 2 : g.rt;
+            nrb = (in.a1 + bper - 1) / bper;
+            const LayerW *lw = p.layers + in.layer;
+            rowmat = in.op == OP_OPROJ ? lw->wo : (in.op == OP_DOWN ? lw->w_down : nullptr);
+        }
+        // GEMV ops other than the stacked QKV: tile j = tile 0 shifted by j*per rows
+        const bool strided = !batched && (in.op == OP_OPROJ || in.op == OP_GATEUP || in.op == OP_DOWN || in.op == OP_LMHEAD);
+        TileCopy c0{};
+        size_t row_bytes = 0;
+        int per = 0;
+        if (strided && nt > 0) {
+            c0 = tile_copy(p, in, 0);
+            const Geo &g = geo_of(p, in.op);
+            row_bytes = (size_t)g.K * 2;
+            per = in.op == OP_GATEUP ? g.rt / 2 : g.rt;
+        }
         for (int j = 0; j < nt; ++j, ++t) {
-            const int pg = t % kPages;
-            if (la) prefetch_until(p, pc, qe, filled + la, filled);
-            if (t >= kPages && !wait_bar(p, &cx.empty[pg], ((t / kPages) - 1) & 1)) {
-                cx.misc->aborted = 1;
-                return;
+            if (t >= kPages && !mbar_try_wait(&cx.empty[pg], (use - 1) & 1)) {
+                // the ring is full: use the wait to pull the next tiles into L2
+                while (lc.i < qe && lc.t < t) l2_advance(p, lc, qe);
+                while (lc.i < qe && lc.t < t + la && !mbar_try_wait(&cx.empty[pg], (use - 1) & 1)) {
+                    l2_prefetch_tile(p, lc);
+                    l2_advance(p, lc, qe);
+                }
+                if (!wait_bar(p, &cx.empty[pg], (use - 1) & 1)) {
+                    cx.misc->aborted = 1;
+                    return;
+                }
             }
-            // at most `back` tiles in flight (fewer while the consumers poll
-            // for an input, so that their loads do not queue behind tile data)
-            const uint32_t b = cx.misc->polling ? (uint32_t)p.poll_inflight : back;
-            if (t >= b && !wait_bar(p, &cx.full[(t - b) % kPages], ((t - b) / kPages) & 1)) {
-                cx.misc->aborted = 1;
-                return;
+            // at most `b` tiles in flight (fewer while the consumers poll for
+            // an input, so that their loads do not queue behind tile data)
+            const uint32_t b = cx.misc->polling ? pback : back;
+            if (t >= b) {
+                const uint32_t tb = t - b;
+                if (!wait_bar(p, &cx.full[tb % kPages], (tb / kPages) & 1)) {
+                    cx.misc->aborted = 1;
+                    return;
+                }
             }
             uint8_t *dst = cx.pages + (size_t)pg * kPageBytes;
-            const TileCopy c = tile_copy(p, in, j);
+            if (batched && nkc > 1) {
+                // one copy per row: the rows' segments [kc*KC, (kc+1)*KC) of a K-chunked tile
+                const int kc = j / nrb, rb = j % nrb;
+                int rows = in.a1 - rb * bper;
+                rows = rows < bper ? rows : bper;
+                const uint32_t rbytes = (uint32_t)KC * 2;
+                // row length K = KC * nkc elements
+                const uint16_t *src = rowmat + ((size_t)in.a0 + (size_t)rb * bper) * (size_t)(KC * nkc) +
+                                      (size_t)kc * KC;
+                const bool ok = rowmat && rows > 0 && CHK(src, rbytes, 3) &&
+                                CHK(src + (size_t)(rows - 1) * KC * nkc, rbytes, 3) &&
+                                CHKS(dst, rows * rbytes, 40);
+                mbar_expect_tx(&cx.full[pg], ok ? rows * rbytes : 0u);
+                if (ok)
+                    for (int r = 0; r < rows; ++r)
+                        bulk_g2s(dst + (size_t)r * rbytes, src + (size_t)r * KC * nkc, rbytes, &cx.full[pg], pol);
+                cx.misc->n_issued = t + 1;
+                if (++pg == kPages) {
+                    pg = 0;
+                    ++use;
+                }
+                continue;
+            }
+            TileCopy c;
+            if (batched) {
+                c = tile_copy(p, in, j % nrb);  // one K-chunk: whole rows, as in single-sequence steps
+            } else if (strided) {
+                const size_t off = (size_t)j * per * row_bytes;
+                const int rows = in.a1 - j * per < per ? in.a1 - j * per : per;
+                c.src0 = static_cast<const uint8_t *>(c0.src0) + off;
+                c.src1 = c0.bytes1 ? static_cast<const uint8_t *>(c0.src1) + off : nullptr;
+                c.bytes0 = (uint32_t)(rows * row_bytes);
+                c.bytes1 = c0.bytes1 ? c.bytes0 : 0u;
+                c.dst1 = c0.dst1;
+            } else {
+                c = tile_copy(p, in, j);
+            }
             const bool ok = CHK(c.src0, c.bytes0, 3) && (!c.bytes1 || CHK(c.src1, c.bytes1, 4)) &&
                             CHKS(dst, c.bytes0, 40) && (!c.bytes1 || CHKS(dst + c.dst1, c.bytes1, 41));
             mbar_expect_tx(&cx.full[pg], ok ? c.bytes0 + c.bytes1 : 0u);
@@ -601,8 +684,11 @@ __device__ void producer(const Params &p, const Ctx &cx, int qb, int qe) {
                 bulk_g2s(dst, c.src0, c.bytes0, &cx.full[pg], pol);
                 if (c.bytes1) bulk_g2s(dst + c.dst1, c.src1, c.bytes1, &cx.full[pg], pol);
             }
-            filled += c.bytes0 + c.bytes1;
             cx.misc->n_issued = t + 1;
+            if (++pg == kPages) {
+                pg = 0;
+                ++use;
+            }
         }
     }
 }
@@ -978,6 +1064,347 @@ __device__ void do_gemv(const Params &p, const Ctx &cx, const Instr &in, uint32_
     }
 }
 
+// ---------------------------------------------------------------------------
+// Batched GEMV (nb > 1 sequences in one step, every weight read once).
+// Tile = rt rows x a K-chunk of KC = g.pad columns; tiles run K-chunk by
+// K-chunk, row block by row block. Warp (rg, ks) owns 8 rows of every tile
+// (for gate/up: 4 gate rows and the matching 4 up rows) and the 256-wide
+// slice ks of the chunk; each lane keeps its 8 inputs of that slice for
+// every sequence in registers, so each weight feeds nb FMAs. A warp-wide
+// transpose reduction leaves each even lane one (row, sequence) sum, which
+// it adds into a shared accumulator; the last warp to finish a tile of the
+// last K-chunk (an arrival counter per tile) applies the op's transform and
+// publishes the tile's outputs, with no CTA-wide barrier per tile.
+// ---------------------------------------------------------------------------
+
+// Warp reduction of 8 values at once: afterwards lanes 4j .. 4j+3 hold the
+// sum over the warp of value j.
+__device__ __forceinline__ float reduce8(float (&v)[8]) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int h = 4, o = 16; h >= 1; h >>= 1, o >>= 1) {
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < h; ++i) {
+            const float send = up ? v[i] : v[i + h];
+            const float keep = up ? v[i + h] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, o);
+        }
+    }
+    float r = v[0] + __shfl_xor_sync(0xFFFFFFFFu, v[0], 2);
+    return r + __shfl_xor_sync(0xFFFFFFFFu, r, 1);
+}
+
+// Polls 8 tagged elements of each of nb sequences (sequence b at base +
+// b*stride, 16-byte aligned): first one word per sequence, then all words,
+// four sequences' loads in flight together. Returns false on abort/timeout.
+__device__ __forceinline__ bool ll_read_seqs(const Params &p, const uint2 *base, size_t stride, int nb,
+                                             uint32_t tag, float (&out)[kMaxBatch][8]) {
+#pragma unroll
+    for (int b = 0; b < kMaxBatch; ++b)
+        if (b < nb && !CHK(base + b * stride, 64, 38)) return false;
+    Spin sp;
+    while (true) {
+        bool ok = true;
+        uint2 v[kMaxBatch];
+#pragma unroll
+        for (int b = 0; b < kMaxBatch; ++b)
+            if (b < nb) v[b] = ll_ld8(base + b * stride + 7);
+#pragma unroll
+        for (int b = 0; b < kMaxBatch; ++b)
+            if (b < nb) ok = ok && v[b].y == tag;
+        if (ok) break;
+        if (!sp.keep_going(p)) return false;
+    }
+#pragma unroll
+    for (int h = 0; h < kMaxBatch; h += 2) {
+        while (true) {
+            uint4 v[2][4];
+            bool ok = true;
+#pragma unroll
+            for (int i = 0; i < 2; ++i)
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    if (h + i < nb) v[i][k] = ll_ld16(base + (h + i) * stride + 2 * k);
+#pragma unroll
+            for (int i = 0; i < 2; ++i)
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    if (h + i < nb) ok = ok && v[i][k].y == tag && v[i][k].w == tag;
+            if (ok) {
+#pragma unroll
+                for (int i = 0; i < 2; ++i)
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        out[h + i][2 * k] = h + i < nb ? __uint_as_float(v[i][k].x) : 0.f;
+                        out[h + i][2 * k + 1] = h + i < nb ? __uint_as_float(v[i][k].z) : 0.f;
+                    }
+                break;
+            }
+            if (!sp.keep_going(p)) return false;
+        }
+    }
+    return true;
+}
+
+__device__ bool gemv_batch(const Params &p, const Ctx &cx, const Instr &in, uint32_t &t, bool &bad) {
+    const Geo &g = geo_of(p, in.op);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int sw = g.sw, rg = warp / sw, ks = warp % sw;
+    const int K = g.K, KC = g.pad, nkc = K / KC, R = g.rt;
+    const int l = in.layer, n = in.a1, r0 = in.a0, op = in.op, nb = p.nb;
+    const bool gu = op == OP_GATEUP;
+    const int per = gu ? R / 2 : R;  // output rows per tile
+    const int nrb = (n + per - 1) / per;
+    const uint32_t ep8 = cx.misc->ep8;
+    const LayerW *lw = p.layers + l;
+    // inputs: tagged words of each sequence, or its bf16 embedding row (layer-0 QKV)
+    const uint2 *src = nullptr;
+    size_t sstride = 0;
+    uint32_t tag = ep8;
+    const uint16_t *gain = nullptr;
+    const bool emb = op == OP_QKV && l == 0;
+    switch (op) {
+        case OP_QKV:
+            gain = lw->attn_norm;
+            src = p.xll; sstride = p.d; tag = ep8 | (uint32_t)(2 * l);
+            break;
+        case OP_GATEUP: gain = lw->mlp_norm; src = p.xll; sstride = p.d; tag = ep8 | (uint32_t)(2 * l + 1); break;
+        case OP_LMHEAD: gain = p.final_norm; src = p.xll; sstride = p.d; tag = ep8 | (uint32_t)(2 * p.L); break;
+        case OP_OPROJ: src = p.attll + (size_t)l * nb * p.Hq * p.hd; sstride = (size_t)p.Hq * p.hd; break;
+        default: src = p.hll + (size_t)l * nb * p.F; sstride = p.F; break;  // OP_DOWN
+    }
+    // shared accumulators: per output row (and gate/up half) and sequence, for
+    // the whole instruction when they fit, else a ring of 8 tiles (LM head)
+    const int vals = gu ? 2 : 1;
+    const bool ring = n * vals * kMaxBatch > kRedCap;
+    float *acc = cx.red;
+    int *cnt = reinterpret_cast<int *>(cx.dred);  // arrivals per row block (or ring slot)
+    float *resid = cx.resid;                       // [nb][n] residual rows (O-proj, down)
+    {
+        const int na = ring ? 8 * R * kMaxBatch : n * vals * kMaxBatch;
+        for (int i = tid; i < na; i += kConsumerThreads)
+            if (CHKS(acc + i, 4, 55)) acc[i] = 0.f;
+        for (int i = tid; i < (ring ? 8 : nrb); i += kConsumerThreads)
+            if (CHKS(cnt + i, 4, 56)) cnt[i] = 0;
+    }
+    if (op == OP_OPROJ || op == OP_DOWN) {
+        const uint32_t rtag = ep8 | (uint32_t)(op == OP_OPROJ ? 2 * l : 2 * l + 1);
+        for (int i = tid; i < n * nb; i += kConsumerThreads) {
+            const int b = i / n, r = i % n;
+            float v = 0.f;
+            if (op == OP_OPROJ && l == 0) {
+                const int tok = current_token(p, b);
+                if (CHK(p.embed + (size_t)tok * p.d + r0 + r, 2, 13)) v = bf16f(__ldg(p.embed + (size_t)tok * p.d + r0 + r));
+            } else if (!bad && !ll_read1(p, p.xll + (size_t)b * p.d + r0 + r, rtag, v)) {
+                bad = true;
+            }
+            if (CHKS(resid + i, 4, 54)) resid[i] = v;
+        }
+    }
+    // inputs of K-chunk 0 (and the RMSNorm scale, whose ops have one chunk)
+    float xb[kMaxBatch][8];
+    auto load_inputs = [&](int kc) -> bool {
+        const int e0 = kc * KC + ks * 256 + lane * 8;
+        if (emb) {
+#pragma unroll
+            for (int b = 0; b < kMaxBatch; ++b) {
+                uint4 w = make_uint4(0u, 0u, 0u, 0u);
+                if (b < nb) {
+                    const uint16_t *row = p.embed + (size_t)current_token(p, b) * p.d + e0;
+                    if (CHK(row, 16, 9)) w = __ldg(reinterpret_cast<const uint4 *>(row));
+                }
+                xb[b][0] = bf_lo(w.x); xb[b][1] = bf_hi(w.x); xb[b][2] = bf_lo(w.y); xb[b][3] = bf_hi(w.y);
+                xb[b][4] = bf_lo(w.z); xb[b][5] = bf_hi(w.z); xb[b][6] = bf_lo(w.w); xb[b][7] = bf_hi(w.w);
+            }
+            return true;
+        }
+        return ll_read_seqs(p, src + e0, sstride, nb, tag, xb);
+    };
+    if (!bad && !load_inputs(0)) bad = true;
+    float *ssw = cx.xbuf;  // [8 warps][kMaxBatch] partial sums of squares
+    if (gain) {
+#pragma unroll
+        for (int b = 0; b < kMaxBatch; ++b) {
+            float s2 = 0.f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) s2 = fmaf(xb[b][e], xb[b][e], s2);
+            s2 = warp_sum(s2);
+            if (lane == 0 && CHKS(ssw + warp * kMaxBatch + b, 4, 57)) ssw[warp * kMaxBatch + b] = s2;
+        }
+    }
+    bad = consumer_sync_any(bad);
+    if (bad) return true;
+    if (gain) {
+        uint4 gw = make_uint4(0u, 0u, 0u, 0u);
+        const uint16_t *gp = gain + ks * 256 + lane * 8;
+        if (CHK(gp, 16, 11)) gw = __ldg(reinterpret_cast<const uint4 *>(gp));
+        const float gf[8] = {bf_lo(gw.x), bf_hi(gw.x), bf_lo(gw.y), bf_hi(gw.y),
+                             bf_lo(gw.z), bf_hi(gw.z), bf_lo(gw.w), bf_hi(gw.w)};
+#pragma unroll
+        for (int b = 0; b < kMaxBatch; ++b) {
+            float tot = 0.f;
+            for (int w = 0; w < sw; ++w) tot += ssw[w * kMaxBatch + b];  // the row group's distinct slices
+            const float rs = 1.0f / sqrtf(tot / (float)K + p.eps);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) xb[b][e] *= rs * gf[e];
+        }
+    }
+    phase_stamp(p, cx, 0);
+    // this warp's 8 rows of a tile: rows ra0 + q (for gate/up: 4 gate rows and
+    // the up rows of the same outputs, `per` rows further)
+    const int ra0 = gu ? rg * 4 : rg * 8;
+    const int row_u4 = KC / 8;
+    const uint4 *pages = reinterpret_cast<const uint4 *>(cx.pages);
+    const int woff = ks * 32 + lane;  // 16-byte chunk of this lane in a row of the tile
+    const bool tracing = p.trace != nullptr;
+    unsigned long long best = 0ull;  // LM head: this lane's best key of sequence lane & 7
+    int pg = (int)(t % kPages);
+    uint32_t par = (t / kPages) & 1u;
+    for (int kc = 0; kc < nkc; ++kc) {
+        if (kc > 0 && !bad && !load_inputs(kc)) bad = true;
+        const bool last_chunk = kc == nkc - 1;
+        for (int rb = 0; rb < nrb; ++rb) {
+            const int j = kc * nrb + rb;
+            if (!bad && !wait_tile(p, cx, pg, par, tracing)) bad = true;
+            bad = __any_sync(0xFFFFFFFFu, bad);
+            const int slot = ring ? (j & 7) : rb;
+            if (!bad) {
+                const uint4 *page = pages + pg * (kPageBytes / 16) + woff;
+#pragma unroll 1
+                for (int q = 0; q < 8; ++q) {
+                    const int trow = gu ? (q < 4 ? ra0 + q : per + ra0 + q - 4) : ra0 + q;  // tile row
+                    const uint4 w = page[trow * row_u4];
+                    if (q == 7) {  // the page is free once its weights are in registers
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&cx.empty[pg]);
+                    }
+                    float2 a2[kMaxBatch];
+#pragma unroll
+                    for (int b = 0; b < kMaxBatch; ++b) a2[b] = make_float2(0.f, 0.f);
+                    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const float2 f = make_float2(bf_lo(u[k]), bf_hi(u[k]));
+#pragma unroll
+                        for (int b = 0; b < kMaxBatch; ++b)
+                            a2[b] = __ffma2_rn(f, make_float2(xb[b][2 * k], xb[b][2 * k + 1]), a2[b]);
+                    }
+                    float v[8];
+#pragma unroll
+                    for (int b = 0; b < kMaxBatch; ++b) v[b] = a2[b].x + a2[b].y;
+                    const float sum = reduce8(v);
+                    const int bq = lane >> 2;
+                    int arow;  // accumulator row
+                    if (ring) arow = slot * R + trow;
+                    else if (gu) arow = (rb * per + (trow % per)) * 2 + (trow >= per ? 1 : 0);
+                    else arow = rb * per + trow;
+                    const int orow = rb * per + (gu ? trow % per : trow);
+                    if ((lane & 3) == 0 && bq < nb && orow < n && CHKS(acc + arow * kMaxBatch + bq, 4, 58))
+                        atomicAdd(acc + arow * kMaxBatch + bq, sum);
+                }
+            } else {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&cx.empty[pg]);
+            }
+            ++t;
+            if (++pg == kPages) {
+                pg = 0;
+                par ^= 1u;
+            }
+            if (!last_chunk) continue;
+            // the last warp to finish this tile publishes its rows
+            __threadfence_block();
+            __syncwarp();
+            int old = 0;
+            if (lane == 0 && CHKS(cnt + slot, 4, 59)) old = atomicAdd(cnt + slot, 1);
+            old = __shfl_sync(0xFFFFFFFFu, old, 0);
+            if (old != kConsumerWarps - 1 || bad) continue;
+            __threadfence_block();
+            for (int idx = lane; idx < per * kMaxBatch; idx += 32) {
+                const int i = idx / kMaxBatch, b = idx % kMaxBatch;  // b == lane & 7
+                const int o = rb * per + i;
+                const int arow = ring ? slot * R + i : (gu ? o * 2 : o);
+                const float v = acc[arow * kMaxBatch + b];
+                if (b < nb && o < n) {
+                    if (op == OP_QKV) {
+                        uint2 *dst = p.qkvll + ((size_t)l * nb + b) * (p.Hq + 2 * p.Hkv) * p.hd + r0 + o;
+                        if (CHK(dst, 8, 12)) ll_store(dst, v, ep8);
+                    } else if (op == OP_OPROJ || op == OP_DOWN) {
+                        const uint32_t wtag = ep8 | (uint32_t)(op == OP_OPROJ ? 2 * l + 1 : 2 * l + 2);
+                        uint2 *dst = p.xll + (size_t)b * p.d + r0 + o;
+                        if (CHK(dst, 8, 15)) ll_store(dst, resid[b * n + o] + v, wtag);
+                    } else if (gu) {
+                        const float up = acc[(arow + 1) * kMaxBatch + b];
+                        uint2 *dst = p.hll + ((size_t)l * nb + b) * p.F + r0 + o;
+                        if (CHK(dst, 8, 16)) ll_store(dst, v / (1.0f + expf(-v)) * up, ep8);
+                    } else {  // LM head
+                        float *lg = p.out_logits ? p.out_logits + (size_t)b * p.V + r0 + o : nullptr;
+                        if (lg && CHK(lg, 4, 18)) *lg = v;
+                        const unsigned long long key = argmax_key(v, (uint32_t)(r0 + o));
+                        best = key > best ? key : best;
+                    }
+                }
+                if (ring) acc[arow * kMaxBatch + b] = 0.f;
+            }
+            if (ring && lane == 0) cnt[slot] = 0;
+            __threadfence_block();
+        }
+    }
+    phase_stamp(p, cx, 1);
+    if (op != OP_LMHEAD) return false;
+    // ---- LM head: per-sequence block argmax, then the last block reduces them
+    bad = consumer_sync_any(bad);
+    if (bad) return true;
+#pragma unroll
+    for (int o = 8; o < 32; o <<= 1) {  // lanes with the same sequence (lane & 7)
+        const unsigned long long other = __shfl_xor_sync(0xFFFFFFFFu, best, o);
+        best = other > best ? other : best;
+    }
+    unsigned long long *bw = reinterpret_cast<unsigned long long *>(cx.xbuf);  // [8 warps][kMaxBatch]
+    if (lane < kMaxBatch) bw[warp * kMaxBatch + lane] = best;
+    consumer_sync();
+    if (tid < nb) {
+        unsigned long long bb = 0ull;
+        for (int w = 0; w < kConsumerWarps; ++w) bb = bw[w * kMaxBatch + tid] > bb ? bw[w * kMaxBatch + tid] : bb;
+        if (CHK(p.lm_part + (size_t)tid * p.n_lm + in.slot, 8, 19)) p.lm_part[(size_t)tid * p.n_lm + in.slot] = bb;
+    }
+    consumer_sync();
+    if (tid == 0) {
+        __threadfence();
+        const uint32_t old = CHK(p.ctr + p.cl.lm_arrive, 4, 31) ? atom_acq_rel_add(p.ctr + p.cl.lm_arrive, 1u) : 0u;
+        const bool last = old == (uint32_t)p.n_lm - 1u;
+        if (last) __threadfence();
+        cx.misc->flag = last ? 1 : 0;
+    }
+    consumer_sync();
+    if (cx.misc->flag) {
+        for (int b = 0; b < nb; ++b) {
+            unsigned long long g2 = 0ull;
+            for (int s2 = tid; s2 < p.n_lm; s2 += kConsumerThreads) {
+                const unsigned long long v = CHK(p.lm_part + (size_t)b * p.n_lm + s2, 8, 20)
+                                                 ? __ldcg(p.lm_part + (size_t)b * p.n_lm + s2) : 0ull;
+                g2 = v > g2 ? v : g2;
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const unsigned long long other = __shfl_xor_sync(0xFFFFFFFFu, g2, o);
+                g2 = other > g2 ? other : g2;
+            }
+            if (lane == 0) cx.misc->best8[warp] = g2;
+            consumer_sync();
+            if (tid == 0) {
+                unsigned long long bb = 0ull;
+                for (int w = 0; w < kConsumerWarps; ++w) bb = cx.misc->best8[w] > bb ? cx.misc->best8[w] : bb;
+                if (CHK(p.out_token + b, 4, 21))
+                    p.out_token[b] = (int32_t)(0xFFFFFFFFu - (uint32_t)(bb & 0xFFFFFFFFull));
+            }
+            consumer_sync();
+        }
+    }
+    return false;
+}
+
 template <int HD, int G>
 struct AttnWarpState {
     // running max (log2 units) and sum of the head this lane scores
@@ -1159,13 +1586,14 @@ template <int HD, int G>
 __device__ void do_attn_hd(const Params &p, const Ctx &cx, const Instr &in, uint32_t &t, bool &bad) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int l = in.layer, kvh = in.a0, split = in.a1;
-    const AttnRange r = attn_range(p, split);
-    const int seff = attn_seff(p);
+    const int b = seq_of(p, in), pos = pos_of(p, b);  // sequence of a batched step
+    const AttnRange r = attn_range(p, split, pos);
+    const int seff = attn_seff(p, pos);
     if (!r.active) return;  // nothing cached for this split at this position
     const uint32_t ep8 = cx.misc->ep8;
     if (tid == 0) cx.misc->staged_key = -1;  // xbuf becomes attention scratch
     const int qkv_stride = (p.Hq + 2 * p.Hkv) * HD;
-    const uint2 *qkv = p.qkvll + (size_t)l * qkv_stride;
+    const uint2 *qkv = p.qkvll + ((size_t)l * p.nb + b) * qkv_stride;
     // shared scratch: q [G][QSTR] | knew [HD] bf16 | vnew [HD] bf16 | warp states
     // [8][G][HD+4]; the host checks G*QSTR + HD + 8*G*(HD+4) <= kXbufFloats.
     using Lay = AttnLayout<HD, G>;
@@ -1181,7 +1609,7 @@ __device__ void do_attn_hd(const Params &p, const Ctx &cx, const Instr &in, uint
     // from the QKV instructions' tagged outputs.
     {
         const float qscale = 1.4426950408889634f / sqrtf((float)HD);
-        const float *rope = p.rope + (size_t)p.pos * HD;  // [HD/2][2]
+        const float *rope = p.rope + (size_t)pos * HD;  // [HD/2][2]
         for (int idx = tid; idx < G * (HD / 2); idx += kConsumerThreads) {
             const int g = idx / (HD / 2), i = idx % (HD / 2);
             const uint2 *qh = qkv + (size_t)(kvh * G + g) * HD;
@@ -1200,8 +1628,8 @@ __device__ void do_attn_hd(const Params &p, const Ctx &cx, const Instr &in, uint
         if (r.has_new) {
             const uint2 *kh = qkv + (size_t)p.Hq * HD + (size_t)kvh * HD;
             const uint2 *vh = qkv + (size_t)(p.Hq + p.Hkv) * HD + (size_t)kvh * HD;
-            const size_t cache_off = (((size_t)l * p.max_batch + p.bslot) * p.Hkv + kvh) * p.max_seq * HD +
-                                     (size_t)p.pos * HD;
+            const size_t cache_off = (((size_t)l * p.max_batch + slot_of(p, b)) * p.Hkv + kvh) * p.max_seq * HD +
+                                     (size_t)pos * HD;
             for (int i = tid; i < HD / 2; i += kConsumerThreads) {
                 const uint2 *srcs[4] = {kh + i, kh + i + HD / 2, vh + i, vh + i + HD / 2};
                 float kv4[4];
@@ -1298,7 +1726,7 @@ __device__ void do_attn_hd(const Params &p, const Ctx &cx, const Instr &in, uint
         }
     }
     consumer_sync();
-    uint2 *out = p.attll + (size_t)l * p.Hq * HD + (size_t)kvh * G * HD;
+    uint2 *out = p.attll + ((size_t)l * p.nb + b) * p.Hq * HD + (size_t)kvh * G * HD;
     if (seff == 1) {
         // The only active split holds the whole context: normalise and
         // publish the attention output directly.
@@ -1320,7 +1748,7 @@ __device__ void do_attn_hd(const Params &p, const Ctx &cx, const Instr &in, uint
     }
     // Several splits: publish this split's partial (o unnormalised, m, l) ...
     constexpr int PS = HD + 2;  // partial row in global memory: HD outputs, max, sum
-    uint2 *part = p.partll + ((size_t)l * p.Hq + (size_t)kvh * G) * p.S * PS;
+    uint2 *part = p.partll + (((size_t)l * p.nb + b) * p.Hq + (size_t)kvh * G) * p.S * PS;
     for (int idx = tid; idx < G * PS; idx += kConsumerThreads) {
         const int g = idx / PS, e = idx % PS;
         float M = -INFINITY;
@@ -1391,7 +1819,7 @@ __device__ void do_attn_hd(const Params &p, const Ctx &cx, const Instr &in, uint
 // ---------------------------------------------------------------------------
 // Consumer: interprets the queue.
 // ---------------------------------------------------------------------------
-template <int HD, int G>
+template <int HD, int G, bool BATCH>
 __device__ void consumer(const Params &p, const Ctx &cx, int qb, int qe, int q0) {
     const int tid = threadIdx.x;
     uint32_t t = 0;
@@ -1407,6 +1835,9 @@ __device__ void consumer(const Params &p, const Ctx &cx, int qb, int qe, int q0)
         }
         if (in.op == OP_ATTN) {
             do_attn_hd<HD, G>(p, cx, in, t, bad);
+        } else if constexpr (BATCH) {
+            gemv_batch(p, cx, in, t, bad);
+            if (tid == 0) cx.misc->staged_key = -1;
         } else {
             do_gemv(p, cx, in, t, bad);
         }
@@ -1432,8 +1863,9 @@ __device__ void consumer(const Params &p, const Ctx &cx, int qb, int qe, int q0)
 // The kernel is instantiated per head dimension and per group size G
 // (query heads per kv head) so that each instance holds only the attention
 // code its model runs: a smaller instruction footprint keeps the hot loops
-// in the instruction cache.
-template <int HD, int G>
+// in the instruction cache. BATCH instances run batched steps (nb > 1); the
+// single-sequence instances carry none of that code.
+template <int HD, int G, bool BATCH>
 __global__ void __launch_bounds__(kThreads, 1) mk_megakernel(const Params prm) {
     uint8_t *smem = mk_smem;
     // Launch parameters are copied to shared memory once; every device
@@ -1466,8 +1898,12 @@ __global__ void __launch_bounds__(kThreads, 1) mk_megakernel(const Params prm) {
     __syncthreads();
     const Params &p = *sp;
     if (tid == 0) {
-        // a position held in device memory is read once, before anything uses it
-        if (p.d_pos) sp->pos = CHK(p.d_pos, 4, 33) ? *(volatile const int32_t *)p.d_pos : -1;
+        // positions held in device memory are read once, before anything uses them
+        if (p.d_pos) {
+            for (int b = 0; b < p.nb && b < kMaxBatch; ++b)
+                sp->posb[b] = CHK(p.d_pos + b, 4, 33) ? *(volatile const int32_t *)(p.d_pos + b) : -1;
+            sp->pos = sp->posb[0];
+        }
         uint32_t e = 1;
         if (CHK(p.epoch, 4, 32)) e = *(volatile uint32_t *)p.epoch & 0xFFFFFFu;
         cx.misc->ep8 = (e ? e : 1u) << 8;
@@ -1480,8 +1916,12 @@ __global__ void __launch_bounds__(kThreads, 1) mk_megakernel(const Params prm) {
     const int q0 = run ? __ldg(qrow) : 0;  // the SM's first instruction (trace slots)
     run = run && *(volatile int32_t *)p.status == DS_OK;
     if (run) {
-        const int tok = current_token(p);
-        const bool bad_tok = tok < 0 || tok >= p.V, bad_pos = p.pos < 0 || p.pos >= p.max_seq;
+        bool bad_tok = false, bad_pos = false;
+        for (int b = 0; b < p.nb; ++b) {
+            const int tok = current_token(p, b), pos = pos_of(p, b);
+            bad_tok = bad_tok || tok < 0 || tok >= p.V;
+            bad_pos = bad_pos || pos < 0 || pos >= p.max_seq;
+        }
         if (bad_tok || bad_pos) {
             if (tid == 0) {
                 atomicCAS(p.status, DS_OK, bad_tok ? DS_BAD_TOKEN : DS_BAD_POS);
@@ -1494,7 +1934,7 @@ __global__ void __launch_bounds__(kThreads, 1) mk_megakernel(const Params prm) {
         if (warp == kConsumerWarps) {
             if (lane == 0) producer(p, cx, qb, qe);
         } else {
-            consumer<HD, G>(p, cx, qb, qe, q0);
+            consumer<HD, G, BATCH>(p, cx, qb, qe, q0);
         }
     }
     __syncthreads();

@@ -4,10 +4,10 @@
 
 extern "C" const void *mk_kernel_fn_hd128(int G) {
     switch (G) {
-        case 1: return (const void *)mk::mk_megakernel<128, 1>;
-        case 2: return (const void *)mk::mk_megakernel<128, 2>;
-        case 3: return (const void *)mk::mk_megakernel<128, 3>;
-        case 4: return (const void *)mk::mk_megakernel<128, 4>;
+        case 1: return (const void *)mk::mk_megakernel<128, 1, false>;
+        case 2: return (const void *)mk::mk_megakernel<128, 2, false>;
+        case 3: return (const void *)mk::mk_megakernel<128, 3, false>;
+        case 4: return (const void *)mk::mk_megakernel<128, 4, false>;
         default: return nullptr;
     }
 }

@@ -4,10 +4,21 @@
 
 extern "C" const void *mk_kernel_fn_hd64(int G) {
     switch (G) {
-        case 1: return (const void *)mk::mk_megakernel<64, 1>;
-        case 2: return (const void *)mk::mk_megakernel<64, 2>;
-        case 3: return (const void *)mk::mk_megakernel<64, 3>;
-        case 4: return (const void *)mk::mk_megakernel<64, 4>;
+        case 1: return (const void *)mk::mk_megakernel<64, 1, false>;
+        case 2: return (const void *)mk::mk_megakernel<64, 2, false>;
+        case 3: return (const void *)mk::mk_megakernel<64, 3, false>;
+        case 4: return (const void *)mk::mk_megakernel<64, 4, false>;
+        default: return nullptr;
+    }
+}
+
+// Batched-step instances (hd 64 only).
+extern "C" const void *mk_kernel_fn_hd64_batch(int G) {
+    switch (G) {
+        case 1: return (const void *)mk::mk_megakernel<64, 1, true>;
+        case 2: return (const void *)mk::mk_megakernel<64, 2, true>;
+        case 3: return (const void *)mk::mk_megakernel<64, 3, true>;
+        case 4: return (const void *)mk::mk_megakernel<64, 4, true>;
         default: return nullptr;
     }
 }

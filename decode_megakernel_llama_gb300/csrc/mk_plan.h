@@ -30,6 +30,7 @@ constexpr int kMaxStaged = 4096;                     // max normed input length 
 constexpr int kMaxStagedLong = 8192;                 // max un-normed input length (down projection)
 constexpr int kResidFloats = 256;                    // residual rows of one O-proj / down instruction
 constexpr int kDredFloats = 256;                     // per-row partials of one down instruction
+constexpr int kMaxBatch = 8;                         // sequences of one batched step
 constexpr int kMaxG = 8;                             // max query heads per kv head (1,2,3,4,6,8)
 constexpr int kTraceWords = 8;                       // int64 per trace record
 constexpr int kMinSplitTiles = 4;                    // an attention split gets >= 4 KV tiles
@@ -80,6 +81,9 @@ static_assert(sizeof(Instr) == 64, "Instr must be 64 bytes");
 // A warp owns rows of a tile (row group rg) and a K-slice (ks):
 //   sw = K-slices per row, rw = 8/sw row groups, m rows per warp per tile,
 //   rt = rw*m rows per tile, nx = floats of the input each lane keeps.
+// Batched steps: tiles hold rt rows x a K-chunk of pad (<= 2048) columns,
+// each warp a 256-wide slice of the chunk (nx = 8 per sequence) and m = 8
+// rows; the chunks of one row are separate tiles.
 struct Geo {
     int32_t K, sw, rw, m, rt, nx, kslice, pad;
 };
@@ -131,14 +135,18 @@ struct Params {
     int32_t pos;
     const int32_t *d_pos;   // if non-null, overrides pos (read once at the start of the step)
     int32_t bslot;          // batch slot of the KV cache this step reads and appends to
+    // batched step (nb > 1): d_token and d_pos hold nb entries; sequence b
+    // uses KV slot b and the b-th row of every activation buffer
+    int32_t nb;
+    int32_t posb[kMaxBatch];
     float *out_logits;      // nullable
     int32_t *out_token;
     unsigned long long timeout_ns;
     long long *trace;       // nullable: [n_sm][trace_cap][kTraceWords]
     int32_t trace_cap;
-    unsigned long long l2_lookahead;  // bytes per SM prefetched into L2 beyond the smem ring
     int32_t max_inflight;             // tiles per SM whose copies may be outstanding at once
     int32_t poll_inflight;            // ... while the consumers poll for an instruction's input
+    int32_t l2_tiles;                 // tiles beyond the smem ring the producer may pull into L2 while it waits
     // address self-checks (only read by a build with MK_CHECKED defined)
     int32_t n_ranges;
     const unsigned long long *ranges;  // [n_ranges][2] valid [begin, end) byte ranges

@@ -82,18 +82,24 @@ def test_tiny_batch_positions_differ_per_sequence(cuda_dev):
     bp.close()
 
 
-def test_batch_slot0_equals_single_sequence_step(cuda_dev):
+def test_batched_step_matches_single_sequence_steps(cuda_dev):
+    # the fused batched step (all sequences in one launch) against the same
+    # sequences stepped one by one through the single-sequence call
     a = BatchPair(TINY, 16, 2)
-    b = BatchPair(TINY, 16, 2)
+    singles = [BatchPair(TINY, 16, 1), BatchPair(TINY, 16, 1)]
     out = torch.zeros(1, dtype=torch.int32, device="cuda:0")
     lg = torch.empty(TINY.vocab, dtype=torch.float32, device="cuda:0")
-    for pos, tok in enumerate([3, 1, 4, 1, 5]):
-        la, _ = a.step([tok, 9], [pos, pos])
-        b.mk.step(tok, pos, out, lg)
-        torch.cuda.synchronize()
-        np.testing.assert_array_equal(la[0], lg.double().cpu().numpy())
+    for pos, toks in enumerate([(3, 9), (1, 2), (4, 7), (1, 1), (5, 0)]):
+        la, ta = a.step(list(toks), [pos, pos])
+        for b in range(2):
+            singles[b].mk.step(toks[b], pos, out, lg)
+            torch.cuda.synchronize()
+            ls = lg.double().cpu().numpy()
+            assert np.abs(la[b] - ls).max() <= 1e-3, (pos, b, np.abs(la[b] - ls).max())
+            assert ta[b] == int(out.item()) or np.sort(ls)[-1] - np.sort(ls)[-2] < 1e-3
     a.close()
-    b.close()
+    for s_ in singles:
+        s_.close()
 
 
 def test_device_position_out_of_range_sets_status(cuda_dev):
