@@ -206,6 +206,74 @@ def run_reference(args, ws, rank):
     print(json.dumps(line), flush=True)
 
 
+def run_batch(args, ws, rank, local):
+    """The batched workload (llama1b_b8): B sequences per step in one launch
+    (mk_decode_step_batch), their caches pre-filled with seeded keys/values up
+    to the prompt length (a stand-in for B prompts run in lockstep), then K
+    timed steps with tokens and positions chained on the device."""
+    import torch
+    from decode_megakernel_llama_gb300 import _lib, synth
+    from decode_megakernel_llama_gb300.build import build
+    from decode_megakernel_llama_gb300.configs import WORKLOADS
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    build()
+    wl = WORKLOADS[args.workload]
+    shape, B, P = wl.shape, wl.batch, wl.prompt_len
+    K, W = args.steps, args.warmup
+    max_seq = P + W + K + 1
+    w = synth.make_weights(shape, dev, 0)
+    kc, vc = synth.kv_cache(shape, max_seq, B, dev)
+    synth.prefill_cache(kc, vc, P)
+    mk = _lib.Megakernel(shape, w, kc, vc)
+    stream = torch.cuda.current_stream(dev)
+    toks = torch.stack([synth.prompt_tokens(shape.vocab, 1, seq=b) for b in range(B)]).view(B).to(dev)
+    pos = torch.full((B,), P, dtype=torch.int32, device=dev)
+    out = torch.zeros(B, dtype=torch.int32, device=dev)
+    one = torch.ones(B, dtype=torch.int32, device=dev)
+
+    def step():
+        mk.step_batch(toks, pos, out, None, stream)
+        toks.copy_(out)
+        pos.add_(one)
+
+    for _ in range(W):
+        step()
+    torch.cuda.synchronize()
+    if mk.status() != 0:
+        raise SystemExit("megakernel status error in the batched warm-up")
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        a.record(stream)
+        for _ in range(K):
+            step()
+        b.record(stream)
+        torch.cuda.synchronize()
+    if mk.status() != 0:
+        raise SystemExit("megakernel status error in the batched steps")
+    ms = a.elapsed_time(b) / K
+    kv = shape.kv_read_bytes(P + W + K // 2 + 1, B)
+    bytes_step = shape.step_weight_bytes() + kv
+    achieved = bytes_step / (ms * 1e-3) / 1e9
+    peak, peak_kind = measured_peak()
+    line = {
+        "metric": f"batch-{B} decode us/token ({shape.name} shape), one launch per step for all {B} sequences",
+        "value": 1e3 * ms / B, "unit": "us/token", "n_gpus": 1, "steps": K, "warmup": W,
+        "ms_per_step": ms, "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{wl.name}: {B} sequences, caches pre-filled to {P} positions, "
+                               f"timed positions {P + W}..{P + W + K - 1}"},
+        "tokens_per_s": B * 1e3 / ms,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_source": peak_kind, "bytes_per_launch": bytes_step,
+                     "traffic": None, "kernel": "mk_megakernel (batched)"},
+        "gpu_launches": K,
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    mk.close()
+
+
 def run_mk(args, ws, rank, local):
     import torch
     import torch.distributed as dist
@@ -416,8 +484,11 @@ def run_mk(args, ws, rank, local):
 def main():
     args = parse()
     ws, rank, local = dist_env()
+    from decode_megakernel_llama_gb300.configs import WORKLOADS
     if args.impl == "reference":
         run_reference(args, ws, rank)
+    elif WORKLOADS[args.workload].batch > 1:
+        run_batch(args, ws, rank, local)
     else:
         run_mk(args, ws, rank, local)
 
