@@ -1065,79 +1065,79 @@ __device__ void do_gemv(const Params &p, const Ctx &cx, const Instr &in, uint32_
 }
 
 // ---------------------------------------------------------------------------
-// Batched GEMV (nb > 1 sequences in one step, every weight read once).
+// Batched GEMV (nb > 1 sequences in one step, every weight read once): a
+// real contraction Y[nb, rows] = X[nb, K] W^T, on the tensor cores with
+// mma.sync m16n8k16 (bf16 in, fp32 accumulate). MMA rows 0-7 are the 8
+// sequences' inputs rounded to bf16 (hi), rows 8-15 the remainders (lo), so
+// hi + lo carries the fp32 input to within 2^-16; the 8 MMA columns are 8
+// weight rows of the tile.
 // Tile = rt rows x a K-chunk of KC = g.pad columns; tiles run K-chunk by
 // K-chunk, row block by row block. Warp (rg, ks) owns 8 rows of every tile
 // (for gate/up: 4 gate rows and the matching 4 up rows) and the 256-wide
-// slice ks of the chunk; each lane keeps its 8 inputs of that slice for
-// every sequence in registers, so each weight feeds nb FMAs. A warp-wide
-// transpose reduction leaves each even lane one (row, sequence) sum, which
-// it adds into a shared accumulator; the last warp to finish a tile of the
-// last K-chunk (an arrival counter per tile) applies the op's transform and
+// slice ks of the chunk: 16 MMAs per tile. The k order inside each 32-column
+// block is permuted identically for X and W so that every lane reads 16
+// contiguous bytes of a weight row. Lanes add their (sequence, row) sums
+// into a shared accumulator; the last warp to finish a tile of the last
+// K-chunk (an arrival counter per tile) applies the op's transform and
 // publishes the tile's outputs, with no CTA-wide barrier per tile.
 // ---------------------------------------------------------------------------
 
-// Warp reduction of 8 values at once: afterwards lanes 4j .. 4j+3 hold the
-// sum over the warp of value j.
-__device__ __forceinline__ float reduce8(float (&v)[8]) {
-    const int lane = threadIdx.x & 31;
-#pragma unroll
-    for (int h = 4, o = 16; h >= 1; h >>= 1, o >>= 1) {
-        const bool up = (lane & o) != 0;
-#pragma unroll
-        for (int i = 0; i < h; ++i) {
-            const float send = up ? v[i] : v[i + h];
-            const float keep = up ? v[i + h] : v[i];
-            v[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, o);
-        }
-    }
-    float r = v[0] + __shfl_xor_sync(0xFFFFFFFFu, v[0], 2);
-    return r + __shfl_xor_sync(0xFFFFFFFFu, r, 1);
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                               uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Polls 8 tagged elements of each of nb sequences (sequence b at base +
-// b*stride, 16-byte aligned): first one word per sequence, then all words,
-// four sequences' loads in flight together. Returns false on abort/timeout.
-__device__ __forceinline__ bool ll_read_seqs(const Params &p, const uint2 *base, size_t stride, int nb,
-                                             uint32_t tag, float (&out)[kMaxBatch][8]) {
+// Two fp32 values as (hi, lo) bf16 pairs: hi = bf16(v), lo = bf16(v - hi).
+__device__ __forceinline__ void split_pair(float v0, float v1, uint32_t &hi, uint32_t &lo) {
+    const uint16_t h0 = f2bf(v0), h1 = f2bf(v1);
+    const uint16_t l0 = f2bf(v0 - bf16f(h0)), l1 = f2bf(v1 - bf16f(h1));
+    hi = (uint32_t)h0 | ((uint32_t)h1 << 16);
+    lo = (uint32_t)l0 | ((uint32_t)l1 << 16);
+}
+
+// Polls n (<= 8) chunks of 8 tagged elements, chunk c at base + c*cstride
+// (16-byte aligned): one word per chunk first, then all words, two chunks'
+// loads in flight together. Returns false on abort/timeout.
+__device__ __forceinline__ bool ll_read_blocks(const Params &p, const uint2 *base, int cstride, uint32_t tag,
+                                               float (&out)[8][8]) {
 #pragma unroll
-    for (int b = 0; b < kMaxBatch; ++b)
-        if (b < nb && !CHK(base + b * stride, 64, 38)) return false;
+    for (int c = 0; c < 8; ++c)
+        if (!CHK(base + c * cstride, 64, 38)) return false;
     Spin sp;
     while (true) {
         bool ok = true;
-        uint2 v[kMaxBatch];
+        uint2 v[8];
 #pragma unroll
-        for (int b = 0; b < kMaxBatch; ++b)
-            if (b < nb) v[b] = ll_ld8(base + b * stride + 7);
+        for (int c = 0; c < 8; ++c) v[c] = ll_ld8(base + c * cstride + 7);
 #pragma unroll
-        for (int b = 0; b < kMaxBatch; ++b)
-            if (b < nb) ok = ok && v[b].y == tag;
+        for (int c = 0; c < 8; ++c) ok = ok && v[c].y == tag;
         if (ok) break;
         if (!sp.keep_going(p)) return false;
     }
 #pragma unroll
-    for (int h = 0; h < kMaxBatch; h += 2) {
+    for (int h = 0; h < 8; h += 2) {
         while (true) {
             uint4 v[2][4];
             bool ok = true;
 #pragma unroll
             for (int i = 0; i < 2; ++i)
 #pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    if (h + i < nb) v[i][k] = ll_ld16(base + (h + i) * stride + 2 * k);
+                for (int k = 0; k < 4; ++k) v[i][k] = ll_ld16(base + (h + i) * cstride + 2 * k);
 #pragma unroll
             for (int i = 0; i < 2; ++i)
 #pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    if (h + i < nb) ok = ok && v[i][k].y == tag && v[i][k].w == tag;
+                for (int k = 0; k < 4; ++k) ok = ok && v[i][k].y == tag && v[i][k].w == tag;
             if (ok) {
 #pragma unroll
                 for (int i = 0; i < 2; ++i)
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
-                        out[h + i][2 * k] = h + i < nb ? __uint_as_float(v[i][k].x) : 0.f;
-                        out[h + i][2 * k + 1] = h + i < nb ? __uint_as_float(v[i][k].z) : 0.f;
+                        out[h + i][2 * k] = __uint_as_float(v[i][k].x);
+                        out[h + i][2 * k + 1] = __uint_as_float(v[i][k].z);
                     }
                 break;
             }
@@ -1158,6 +1158,7 @@ __device__ bool gemv_batch(const Params &p, const Ctx &cx, const Instr &in, uint
     const int nrb = (n + per - 1) / per;
     const uint32_t ep8 = cx.misc->ep8;
     const LayerW *lw = p.layers + l;
+    const int gq = lane >> 2, tq = lane & 3;  // MMA fragment coordinates
     // inputs: tagged words of each sequence, or its bf16 embedding row (layer-0 QKV)
     const uint2 *src = nullptr;
     size_t sstride = 0;
@@ -1202,61 +1203,87 @@ __device__ bool gemv_batch(const Params &p, const Ctx &cx, const Instr &in, uint
             if (CHKS(resid + i, 4, 54)) resid[i] = v;
         }
     }
-    // inputs of K-chunk 0 (and the RMSNorm scale, whose ops have one chunk)
-    float xb[kMaxBatch][8];
+    // This lane's inputs: sequence gq, elements 32*blk + 8*tq .. +8 of the
+    // warp's slice (blk = 0..7), as (hi, lo) bf16 pairs: the A fragments of
+    // all 16 MMAs of a tile. Sequences >= nb are zero.
+    uint32_t xh[8][4], xl[8][4];
+    float ss = 0.f;  // this lane's part of its sequence's sum of squares
     auto load_inputs = [&](int kc) -> bool {
-        const int e0 = kc * KC + ks * 256 + lane * 8;
-        if (emb) {
+        float xv[8][8];
+        const int e0 = kc * KC + ks * 256 + 8 * tq;  // + 32 * blk
+        bool ok = true;
+        if (gq >= nb) {
 #pragma unroll
-            for (int b = 0; b < kMaxBatch; ++b) {
+            for (int c = 0; c < 8; ++c)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) xv[c][e] = 0.f;
+        } else if (emb) {
+            const uint16_t *row = p.embed + (size_t)current_token(p, gq) * p.d + e0;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
                 uint4 w = make_uint4(0u, 0u, 0u, 0u);
-                if (b < nb) {
-                    const uint16_t *row = p.embed + (size_t)current_token(p, b) * p.d + e0;
-                    if (CHK(row, 16, 9)) w = __ldg(reinterpret_cast<const uint4 *>(row));
-                }
-                xb[b][0] = bf_lo(w.x); xb[b][1] = bf_hi(w.x); xb[b][2] = bf_lo(w.y); xb[b][3] = bf_hi(w.y);
-                xb[b][4] = bf_lo(w.z); xb[b][5] = bf_hi(w.z); xb[b][6] = bf_lo(w.w); xb[b][7] = bf_hi(w.w);
+                if (CHK(row + 32 * c, 16, 9)) w = __ldg(reinterpret_cast<const uint4 *>(row + 32 * c));
+                xv[c][0] = bf_lo(w.x); xv[c][1] = bf_hi(w.x); xv[c][2] = bf_lo(w.y); xv[c][3] = bf_hi(w.y);
+                xv[c][4] = bf_lo(w.z); xv[c][5] = bf_hi(w.z); xv[c][6] = bf_lo(w.w); xv[c][7] = bf_hi(w.w);
             }
-            return true;
+        } else {
+            ok = ll_read_blocks(p, src + (size_t)gq * sstride + e0, 32, tag, xv);
         }
-        return ll_read_seqs(p, src + e0, sstride, nb, tag, xb);
+        if (gain) {  // one K-chunk: keep the raw values' squares, scale after the barrier
+            ss = 0.f;
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) ss = fmaf(xv[c][e], xv[c][e], ss);
+            const uint16_t *gp = gain + e0;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                uint4 gw = make_uint4(0u, 0u, 0u, 0u);
+                if (CHK(gp + 32 * c, 16, 11)) gw = __ldg(reinterpret_cast<const uint4 *>(gp + 32 * c));
+                xv[c][0] *= bf_lo(gw.x); xv[c][1] *= bf_hi(gw.x); xv[c][2] *= bf_lo(gw.y); xv[c][3] *= bf_hi(gw.y);
+                xv[c][4] *= bf_lo(gw.z); xv[c][5] *= bf_hi(gw.z); xv[c][6] *= bf_lo(gw.w); xv[c][7] *= bf_hi(gw.w);
+            }
+        }
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) split_pair(xv[c][2 * k], xv[c][2 * k + 1], xh[c][k], xl[c][k]);
+        return ok;
     };
     if (!bad && !load_inputs(0)) bad = true;
     float *ssw = cx.xbuf;  // [8 warps][kMaxBatch] partial sums of squares
     if (gain) {
-#pragma unroll
-        for (int b = 0; b < kMaxBatch; ++b) {
-            float s2 = 0.f;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) s2 = fmaf(xb[b][e], xb[b][e], s2);
-            s2 = warp_sum(s2);
-            if (lane == 0 && CHKS(ssw + warp * kMaxBatch + b, 4, 57)) ssw[warp * kMaxBatch + b] = s2;
-        }
+        // lanes 4g .. 4g+3 hold sequence g's slice
+        ss += __shfl_xor_sync(0xFFFFFFFFu, ss, 1);
+        ss += __shfl_xor_sync(0xFFFFFFFFu, ss, 2);
+        if (tq == 0 && CHKS(ssw + warp * kMaxBatch + gq, 4, 57)) ssw[warp * kMaxBatch + gq] = ss;
     }
     bad = consumer_sync_any(bad);
     if (bad) return true;
     if (gain) {
-        uint4 gw = make_uint4(0u, 0u, 0u, 0u);
-        const uint16_t *gp = gain + ks * 256 + lane * 8;
-        if (CHK(gp, 16, 11)) gw = __ldg(reinterpret_cast<const uint4 *>(gp));
-        const float gf[8] = {bf_lo(gw.x), bf_hi(gw.x), bf_lo(gw.y), bf_hi(gw.y),
-                             bf_lo(gw.z), bf_hi(gw.z), bf_lo(gw.w), bf_hi(gw.w)};
+        // RMSNorm: x * g / rms; the gain is already in, the 1/rms factor is
+        // applied to the hi/lo pairs exactly as a fp32 rescale of the inputs
+        float tot = 0.f;
+        for (int w = 0; w < sw; ++w) tot += ssw[w * kMaxBatch + gq];  // the row group's distinct slices
+        const float rs = 1.0f / sqrtf(tot / (float)K + p.eps);
 #pragma unroll
-        for (int b = 0; b < kMaxBatch; ++b) {
-            float tot = 0.f;
-            for (int w = 0; w < sw; ++w) tot += ssw[w * kMaxBatch + b];  // the row group's distinct slices
-            const float rs = 1.0f / sqrtf(tot / (float)K + p.eps);
+        for (int c = 0; c < 8; ++c)
 #pragma unroll
-            for (int e = 0; e < 8; ++e) xb[b][e] *= rs * gf[e];
-        }
+            for (int k = 0; k < 4; ++k) {
+                const float v0 = (bf16f((uint16_t)(xh[c][k] & 0xFFFFu)) + bf16f((uint16_t)(xl[c][k] & 0xFFFFu))) * rs;
+                const float v1 = (bf16f((uint16_t)(xh[c][k] >> 16)) + bf16f((uint16_t)(xl[c][k] >> 16))) * rs;
+                split_pair(v0, v1, xh[c][k], xl[c][k]);
+            }
     }
     phase_stamp(p, cx, 0);
-    // this warp's 8 rows of a tile: rows ra0 + q (for gate/up: 4 gate rows and
-    // the up rows of the same outputs, `per` rows further)
+    // this warp's 8 rows of a tile (MMA columns): rows ra0 + c, for gate/up
+    // columns 0-3 gate rows and 4-7 the up rows of the same outputs
     const int ra0 = gu ? rg * 4 : rg * 8;
+    const int mycol = gq;  // the weight row this lane loads: MMA column gq
+    const int wrow = gu ? (mycol < 4 ? ra0 + mycol : per + ra0 + mycol - 4) : ra0 + mycol;
     const int row_u4 = KC / 8;
     const uint4 *pages = reinterpret_cast<const uint4 *>(cx.pages);
-    const int woff = ks * 32 + lane;  // 16-byte chunk of this lane in a row of the tile
+    const int woff = wrow * row_u4 + ks * 32 + tq;  // + 4 * blk: 16 bytes at element 32*blk + 8*tq
     const bool tracing = p.trace != nullptr;
     unsigned long long best = 0ull;  // LM head: this lane's best key of sequence lane & 7
     int pg = (int)(t % kPages);
@@ -1271,37 +1298,30 @@ __device__ bool gemv_batch(const Params &p, const Ctx &cx, const Instr &in, uint
             const int slot = ring ? (j & 7) : rb;
             if (!bad) {
                 const uint4 *page = pages + pg * (kPageBytes / 16) + woff;
-#pragma unroll 1
-                for (int q = 0; q < 8; ++q) {
-                    const int trow = gu ? (q < 4 ? ra0 + q : per + ra0 + q - 4) : ra0 + q;  // tile row
-                    const uint4 w = page[trow * row_u4];
-                    if (q == 7) {  // the page is free once its weights are in registers
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(&cx.empty[pg]);
-                    }
-                    float2 a2[kMaxBatch];
+                uint4 w[8];
 #pragma unroll
-                    for (int b = 0; b < kMaxBatch; ++b) a2[b] = make_float2(0.f, 0.f);
-                    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+                for (int c = 0; c < 8; ++c) w[c] = page[4 * c];
+                __syncwarp();  // the page is free once its weights are in registers
+                if (lane == 0) mbar_arrive(&cx.empty[pg]);
+                float d[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const float2 f = make_float2(bf_lo(u[k]), bf_hi(u[k]));
+                for (int c = 0; c < 8; ++c) {
+                    mma_bf16_16816(d, xh[c][0], xl[c][0], xh[c][1], xl[c][1], w[c].x, w[c].y);
+                    mma_bf16_16816(d, xh[c][2], xl[c][2], xh[c][3], xl[c][3], w[c].z, w[c].w);
+                }
+                // d0/d1: sequence gq (hi) at columns 2tq, 2tq+1; d2/d3: its lo part
+                const float s0 = d[0] + d[2], s1 = d[1] + d[3];
 #pragma unroll
-                        for (int b = 0; b < kMaxBatch; ++b)
-                            a2[b] = __ffma2_rn(f, make_float2(xb[b][2 * k], xb[b][2 * k + 1]), a2[b]);
-                    }
-                    float v[8];
-#pragma unroll
-                    for (int b = 0; b < kMaxBatch; ++b) v[b] = a2[b].x + a2[b].y;
-                    const float sum = reduce8(v);
-                    const int bq = lane >> 2;
+                for (int h = 0; h < 2; ++h) {
+                    const int col = 2 * tq + h;
+                    const int trow = gu ? (col < 4 ? ra0 + col : per + ra0 + col - 4) : ra0 + col;  // tile row
                     int arow;  // accumulator row
                     if (ring) arow = slot * R + trow;
                     else if (gu) arow = (rb * per + (trow % per)) * 2 + (trow >= per ? 1 : 0);
                     else arow = rb * per + trow;
                     const int orow = rb * per + (gu ? trow % per : trow);
-                    if ((lane & 3) == 0 && bq < nb && orow < n && CHKS(acc + arow * kMaxBatch + bq, 4, 58))
-                        atomicAdd(acc + arow * kMaxBatch + bq, sum);
+                    if (gq < nb && orow < n && CHKS(acc + arow * kMaxBatch + gq, 4, 58))
+                        atomicAdd(acc + arow * kMaxBatch + gq, h ? s1 : s0);
                 }
             } else {
                 __syncwarp();
