@@ -270,6 +270,16 @@ def run_batch(args, ws, rank, local):
         "gpu_launches": K,
         "clocks": clk.summary(),
     }
+    if args.trace:
+        from decode_megakernel_llama_gb300 import trace as mktrace
+        mk.set_trace(True)
+        step()
+        torch.cuda.synchronize()
+        rec = mk.read_trace()
+        mk.set_trace(False)
+        with open(args.trace, "w") as f:
+            json.dump(mktrace.summarize(rec), f, indent=1)
+        mktrace.to_chrome(rec, os.path.splitext(args.trace)[0] + ".chrome.json")
     print(json.dumps(line), flush=True)
     mk.close()
 

@@ -113,11 +113,12 @@ def make_config(shape, max_seq: int, max_batch: int = 1, attn_splits: int = 0) -
                      int(attn_splits), float(shape.rms_eps), float(shape.rope_theta))
 
 
-def plan_inspect(shape, n_sm: int, max_seq: int, attn_splits: int = 0):
-    """Host-only plan: returns (instr int32 [n, 16] as list of lists, queue lengths, n_counters)."""
+def plan_inspect(shape, n_sm: int, max_seq: int, attn_splits: int = 0, max_batch: int = 1):
+    """Host-only plan: returns (instr int32 [n, 16] as list of lists, queue lengths, n_counters).
+    max_batch > 1 gives the fused batched step's plan where the model supports it."""
     import numpy as np
     L = load()
-    cfg = make_config(shape, max_seq, 1, attn_splits)
+    cfg = make_config(shape, max_seq, max_batch, attn_splits)
     qlen = (ctypes.c_int32 * n_sm)()
     nctr = ctypes.c_int32(0)
     n = check(L.mk_plan_inspect(ctypes.byref(cfg), n_sm, None, 0, qlen, ctypes.byref(nctr)))
@@ -220,9 +221,8 @@ class Megakernel:
 
     def read_trace(self):
         import numpy as np
-        n_sm, n_instr = ctypes.c_int32(), ctypes.c_int32()
-        check(load().mk_plan_size(self.h, ctypes.byref(n_sm), ctypes.byref(n_instr)))
-        buf = np.zeros((max(1, n_instr.value), 8), dtype=np.int64)
+        need = check(load().mk_read_trace(self.h, None, 0))
+        buf = np.zeros((max(1, need), 8), dtype=np.int64)
         n = check(load().mk_read_trace(self.h, buf.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
                                        buf.shape[0]))
         return buf[:n]

@@ -69,15 +69,16 @@ bool make_geo(int K, Geo &g, int max_nx = 32) {
 // Batched steps: tiles of rt rows x a K-chunk of KC = min(K, 2048) columns,
 // 8 rows and a 256-wide slice per warp (see mk_plan.h).
 bool make_geo_batch(int K, Geo &g) {
-    const int KC = std::min(K, 2048);
-    if (K <= 0 || K % KC != 0 || (KC != 256 && KC != 512 && KC != 1024 && KC != 2048)) return false;
+    // K-chunks of KC <= 1024 columns, 128 per warp; 16 rows per warp
+    const int KC = std::min(K, 1024);
+    if (K <= 0 || K % KC != 0 || (KC != 128 && KC != 256 && KC != 512 && KC != 1024)) return false;
     g.K = K;
-    g.sw = KC / 256;
+    g.sw = KC / 128;
     g.rw = mk::kConsumerWarps / g.sw;
-    g.m = 8;
+    g.m = 16;
     g.rt = g.rw * g.m;
-    g.nx = 8;
-    g.kslice = 256;
+    g.nx = 4;
+    g.kslice = 128;
     g.pad = KC;
     return g.rt * KC * 2 <= mk::kPageBytes;
 }
@@ -166,8 +167,8 @@ int build_plan(const mk_config *c, int n_sm, Plan &P, int nb) {
     P.n_sm = n_sm;
     P.nb = nb;
     if (nb > 1) {
-        // batched steps: hd 64 instances, normed inputs in one K-chunk
-        if (nb > mk::kMaxBatch || hd != 64 || d > 2048 || !make_geo_batch(d, P.geo_qkv) ||
+        // batched steps: hd 64 instances
+        if (nb > mk::kMaxBatch || hd != 64 || !make_geo_batch(d, P.geo_qkv) ||
             !make_geo_batch(qd, P.geo_o) || !make_geo_batch(d, P.geo_gu) || !make_geo_batch(F, P.geo_down) ||
             !make_geo_batch(d, P.geo_lm))
             return fail(MK_ERR_UNSUPPORTED, "no batched tile geometry for this model");
@@ -297,7 +298,7 @@ int build_plan(const mk_config *c, int n_sm, Plan &P, int nb) {
             in.a0 = ch.r0;
             in.a1 = ch.n;
             in.wait_ctr = cl.attn_done + l;
-            in.wait_target = Hkv;
+            in.wait_target = Hkv * nb;  // the last split of every (sequence, kv head)
             in.sig_ctr = cl.oproj_done + l;
             in.sig_n = 1;
             set_bytes(in, 2ll * ch.n * qd);
@@ -634,6 +635,7 @@ struct mk_handle {
     long long *d_trace = nullptr;
     int trace_cap = 0;
     bool trace_on = false;
+    bool trace_batch = false;  // the last traced launch ran the batched image
     // batched steps of all max_batch sequences in one launch (max_batch > 1 and
     // a model the batched instances support), with their own scratch
     bool has_batch = false;
@@ -660,6 +662,7 @@ int launch(mk_handle *h, int32_t token, const int32_t *d_token, int32_t position
     p.timeout_ns = h->timeout_ns;
     p.trace = h->trace_on ? h->d_trace : nullptr;
     p.trace_cap = h->trace_cap;
+    if (h->trace_on) h->trace_batch = false;
     return mkint::launch_step(p, h->im.n_sm, h->im.n_stages, token, d_token, position, out_logits,
                               out_token, stream, unfused, d_pos, bslot);
 }
@@ -673,7 +676,9 @@ const char *mk_last_error(void) { return g_err.c_str(); }
 int mk_plan_inspect(const mk_config *config, int32_t n_sm, int32_t *out_instr, int32_t cap,
                     int32_t *out_queue_len, int32_t *out_n_counters) {
     Plan P;
-    int rc = build_plan(config, n_sm, P, 1);
+    int rc = MK_ERR_UNSUPPORTED;
+    if (config && config->max_batch > 1) rc = build_plan(config, n_sm, P, config->max_batch);
+    if (rc) rc = build_plan(config, n_sm, P, 1);
     if (rc) return rc;
     const size_t n = P.n_instr();
     if (out_queue_len)
@@ -777,6 +782,9 @@ int mk_decode_step_batch(mk_handle *h, const int32_t *d_tokens, const int32_t *d
         if (e != cudaSuccess) return cuda_fail(e, "cudaSetDevice");
         mk::Params p = h->bbase;
         p.timeout_ns = h->timeout_ns;
+        p.trace = h->trace_on ? h->d_trace : nullptr;
+        p.trace_cap = h->trace_cap;
+        if (h->trace_on) h->trace_batch = true;
         return mkint::launch_step(p, h->bim.n_sm, h->bim.n_stages, 0, d_tokens, 0, out_logits, out_tokens,
                                   (cudaStream_t)stream, false, d_positions, 0);
     }
@@ -851,6 +859,8 @@ int mk_set_trace(mk_handle *h, int32_t enable) {
     if (enable && !h->d_trace) {
         int cap = 0;
         for (int q : h->im.qlen) cap = std::max(cap, q);
+        if (h->has_batch)
+            for (int q : h->bim.qlen) cap = std::max(cap, q);
         cap = std::max(cap, 1);
         cudaError_t e = cudaSetDevice(h->device);
         if (e == cudaSuccess)
@@ -868,17 +878,23 @@ int mk_set_trace(mk_handle *h, int32_t enable) {
 }
 
 int mk_read_trace(mk_handle *h, int64_t *host_out, int32_t cap) {
-    if (!h || !host_out || cap < 0) return fail(MK_ERR_INVALID_ARG, "bad arguments");
+    if (!h || cap < 0) return fail(MK_ERR_INVALID_ARG, "bad arguments");
     if (!h->d_trace) return 0;
-    std::vector<long long> buf(mk::kTraceWords * (size_t)h->trace_cap * h->im.n_sm);
+    const mkint::Image &im = h->trace_batch ? h->bim : h->im;
+    if (!host_out) {
+        int n = 0;
+        for (int s = 0; s < im.n_sm; ++s) n += std::min(im.qlen[s], h->trace_cap);
+        return n;
+    }
+    std::vector<long long> buf(mk::kTraceWords * (size_t)h->trace_cap * im.n_sm);
     cudaError_t e = cudaSetDevice(h->device);
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e == cudaSuccess)
         e = cudaMemcpy(buf.data(), h->d_trace, sizeof(long long) * buf.size(), cudaMemcpyDeviceToHost);
     if (e != cudaSuccess) return cuda_fail(e, "trace read");
     int n = 0;
-    for (int s = 0; s < h->im.n_sm; ++s)
-        for (int i = 0; i < h->im.qlen[s] && i < h->trace_cap; ++i) {
+    for (int s = 0; s < im.n_sm; ++s)
+        for (int i = 0; i < im.qlen[s] && i < h->trace_cap; ++i) {
             if (n >= cap) return n;
             std::memcpy(host_out + mk::kTraceWords * (size_t)n,
                         &buf[mk::kTraceWords * ((size_t)s * h->trace_cap + i)],

@@ -575,6 +575,44 @@ __device__ __forceinline__ void l2_prefetch_tile(const Params &p, const L2Cursor
 // it only advances pointers (GEMV tiles of one instruction are equally
 // strided rows of one or two matrices).
 // ---------------------------------------------------------------------------
+// Accumulators of a batched instruction: per output row (two per row for
+// gate/up) and sequence, for the whole instruction, or a ring of 8 tiles.
+__device__ __forceinline__ bool batch_ring(int n, int op) {
+    return n * (op == OP_GATEUP ? 2 : 1) * kMaxBatch > kRedCap;
+}
+
+// Tile j of a batched instruction: (K-chunk, row block), in groups of gsz
+// row blocks (all K-chunks of a group before the next group).
+struct BTile {
+    int kc, rb;
+};
+__device__ __forceinline__ BTile batch_tile(int j, int nrb, int nkc, int gsz) {
+    const int grp = j / (gsz * nkc);
+    const int q = j - grp * gsz * nkc;
+    const int left = nrb - grp * gsz;
+    const int gs = left < gsz ? left : gsz;
+    return {q / gs, grp * gsz + q % gs};
+}
+
+// Start of weight row `row` (stacked [Wq; Wk; Wv] rows for QKV; for gate/up
+// `up` selects the up matrix) of a batched GEMV instruction.
+__device__ __forceinline__ const uint16_t *batch_row(const Params &p, const Instr &in, size_t row, bool up) {
+    const LayerW *lw = p.layers + in.layer;
+    const size_t K = (size_t)geo_of(p, in.op).K;
+    switch (in.op) {
+        case OP_QKV: {
+            const size_t qd = (size_t)p.Hq * p.hd, kvd = (size_t)p.Hkv * p.hd;
+            if (row < qd) return lw->wq + row * K;
+            if (row < qd + kvd) return lw->wk + (row - qd) * K;
+            return lw->wv + (row - qd - kvd) * K;
+        }
+        case OP_GATEUP: return (up ? lw->w_up : lw->w_gate) + row * K;
+        case OP_OPROJ: return lw->wo + row * K;
+        case OP_DOWN: return lw->w_down + row * K;
+        default: return p.embed + row * K;
+    }
+}
+
 __device__ void producer(const Params &p, const Ctx &cx, int qb, int qe) {
     const uint64_t pol = policy_evict_first();
     uint32_t t = 0;
@@ -592,18 +630,16 @@ __device__ void producer(const Params &p, const Ctx &cx, int qb, int qe) {
         const Instr in = load_instr(p, i);
         if (i + 1 < qe) prefetch_instr(p, i + 1);
         const int nt = num_tiles(p, in);
-        // batched steps: tile j = (K-chunk j / nrb, row block j % nrb)
+        // batched steps: tile j = (K-chunk, row block) in the consumers' order
         const bool batched = p.nb > 1 && in.op != OP_ATTN;
-        int nrb = 1, nkc = 1, KC = 0, bper = 0;
-        const uint16_t *rowmat = nullptr;  // matrix of the per-row copies (K-chunked tiles)
+        int nrb = 1, nkc = 1, KC = 0, bper = 0, gsz = 1;
         if (batched) {
             const Geo &g = geo_of(p, in.op);
             KC = g.pad;
             nkc = g.K / KC;
             bper = in.op == OP_GATEUP ? g.rt / 2 : g.rt;
             nrb = (in.a1 + bper - 1) / bper;
-            const LayerW *lw = p.layers + in.layer;
-            rowmat = in.op == OP_OPROJ ? lw->wo : (in.op == OP_DOWN ? lw->w_down : nullptr);
+            gsz = batch_ring(in.a1, in.op) ? 8 : nrb;
         }
         // GEMV ops other than the stacked QKV: tile j = tile 0 shifted by j*per rows
         const bool strided = !batched && (in.op == OP_OPROJ || in.op == OP_GATEUP || in.op == OP_DOWN || in.op == OP_LMHEAD);
@@ -641,21 +677,44 @@ __device__ void producer(const Params &p, const Ctx &cx, int qb, int qe) {
             }
             uint8_t *dst = cx.pages + (size_t)pg * kPageBytes;
             if (batched && nkc > 1) {
-                // one copy per row: the rows' segments [kc*KC, (kc+1)*KC) of a K-chunked tile
-                const int kc = j / nrb, rb = j % nrb;
-                int rows = in.a1 - rb * bper;
+                // one copy per row: the rows' segments [kc*KC, (kc+1)*KC) of a
+                // K-chunked tile (gate/up: gate rows, then the up rows from
+                // bper rows into the page)
+                const BTile bt = batch_tile(j, nrb, nkc, gsz);
+                int rows = in.a1 - bt.rb * bper;
                 rows = rows < bper ? rows : bper;
                 const uint32_t rbytes = (uint32_t)KC * 2;
-                // row length K = KC * nkc elements
-                const uint16_t *src = rowmat + ((size_t)in.a0 + (size_t)rb * bper) * (size_t)(KC * nkc) +
-                                      (size_t)kc * KC;
-                const bool ok = rowmat && rows > 0 && CHK(src, rbytes, 3) &&
-                                CHK(src + (size_t)(rows - 1) * KC * nkc, rbytes, 3) &&
-                                CHKS(dst, rows * rbytes, 40);
-                mbar_expect_tx(&cx.full[pg], ok ? rows * rbytes : 0u);
+                const size_t rowlen = (size_t)KC * nkc, coff = (size_t)bt.kc * KC;
+                const int halves = in.op == OP_GATEUP ? 2 : 1;
+                const size_t row0 = (size_t)in.a0 + (size_t)bt.rb * bper;
+                // rows before a matrix boundary of the stacked QKV (the rest
+                // come from the next matrix)
+                int m = rows;
+                if (in.op == OP_QKV) {
+                    const size_t qd = (size_t)p.Hq * p.hd, kvd = (size_t)p.Hkv * p.hd;
+                    const size_t bound = row0 < qd ? qd : (row0 < qd + kvd ? qd + kvd : qd + 2 * kvd);
+                    if (row0 + (size_t)rows > bound) m = (int)(bound - row0);
+                }
+                bool ok = rows > 0 && CHKS(dst, (uint32_t)(bper * (halves - 1) + rows) * rbytes, 40);
+                const uint16_t *seg[2][2];  // [half][segment]: source of the segment's first row
+                for (int hf = 0; hf < halves && ok; ++hf) {
+                    seg[hf][0] = batch_row(p, in, row0, hf) + coff;
+                    seg[hf][1] = m < rows ? batch_row(p, in, row0 + m, hf) + coff : seg[hf][0];
+                    ok = CHK(seg[hf][0], rbytes, 3) && CHK(seg[hf][0] + (size_t)(m - 1) * rowlen, rbytes, 3) &&
+                         (m == rows || (CHK(seg[hf][1], rbytes, 3) &&
+                                        CHK(seg[hf][1] + (size_t)(rows - m - 1) * rowlen, rbytes, 3)));
+                }
+                mbar_expect_tx(&cx.full[pg], ok ? (uint32_t)(halves * rows) * rbytes : 0u);
                 if (ok)
-                    for (int r = 0; r < rows; ++r)
-                        bulk_g2s(dst + (size_t)r * rbytes, src + (size_t)r * KC * nkc, rbytes, &cx.full[pg], pol);
+                    for (int hf = 0; hf < halves; ++hf) {
+                        uint8_t *d0 = dst + (size_t)hf * bper * rbytes;
+                        const uint16_t *s0 = seg[hf][0];
+                        for (int r = 0; r < m; ++r, s0 += rowlen, d0 += rbytes)
+                            bulk_g2s(d0, s0, rbytes, &cx.full[pg], pol);
+                        s0 = seg[hf][1];
+                        for (int r = m; r < rows; ++r, s0 += rowlen, d0 += rbytes)
+                            bulk_g2s(d0, s0, rbytes, &cx.full[pg], pol);
+                    }
                 cx.misc->n_issued = t + 1;
                 if (++pg == kPages) {
                     pg = 0;
@@ -665,7 +724,7 @@ __device__ void producer(const Params &p, const Ctx &cx, int qb, int qe) {
             }
             TileCopy c;
             if (batched) {
-                c = tile_copy(p, in, j % nrb);  // one K-chunk: whole rows, as in single-sequence steps
+                c = tile_copy(p, in, batch_tile(j, nrb, 1, gsz).rb);  // one K-chunk: whole rows
             } else if (strided) {
                 const size_t off = (size_t)j * per * row_bytes;
                 const int rows = in.a1 - j * per < per ? in.a1 - j * per : per;
@@ -1069,17 +1128,25 @@ __device__ void do_gemv(const Params &p, const Ctx &cx, const Instr &in, uint32_
 // real contraction Y[nb, rows] = X[nb, K] W^T, on the tensor cores with
 // mma.sync m16n8k16 (bf16 in, fp32 accumulate). MMA rows 0-7 are the 8
 // sequences' inputs rounded to bf16 (hi), rows 8-15 the remainders (lo), so
-// hi + lo carries the fp32 input to within 2^-16; the 8 MMA columns are 8
-// weight rows of the tile.
-// Tile = rt rows x a K-chunk of KC = g.pad columns; tiles run K-chunk by
-// K-chunk, row block by row block. Warp (rg, ks) owns 8 rows of every tile
-// (for gate/up: 4 gate rows and the matching 4 up rows) and the 256-wide
-// slice ks of the chunk: 16 MMAs per tile. The k order inside each 32-column
-// block is permuted identically for X and W so that every lane reads 16
-// contiguous bytes of a weight row. Lanes add their (sequence, row) sums
-// into a shared accumulator; the last warp to finish a tile of the last
+// hi + lo carries the fp32 input to within 2^-16; the MMA columns are weight
+// rows.
+// Tile = rt rows x a K-chunk of KC = g.pad columns (32 KB). Warp (rg, ks)
+// owns 16 rows of every tile (two MMA column blocks; for gate/up 8 gate rows
+// and the matching 8 up rows) and the 128-wide slice ks of the chunk: 16
+// MMAs per tile, its inputs in 32 registers. The k order inside each
+// 32-column block is permuted identically for X and W so that every lane
+// reads 16 contiguous bytes of a weight row. Lanes add their (sequence, row)
+// sums into a shared accumulator; the last warp to finish a tile of the last
 // K-chunk (an arrival counter per tile) applies the op's transform and
-// publishes the tile's outputs, with no CTA-wide barrier per tile.
+// publishes the tile's outputs, with no CTA-wide barrier per tile. The
+// RMSNorm factor of a sequence is a scalar of the whole row, so it is
+// applied there too, from the sums of squares the warps gathered while
+// loading their slices.
+// Tile order: K-chunk by K-chunk over all row blocks when the instruction's
+// accumulators fit in shared memory; otherwise (LM head) groups of 8 row
+// blocks, all K-chunks of a group before the next, through a ring of 8
+// accumulator slots (a warp runs at most kPages tiles ahead of the slowest,
+// and a slot is reused 8 tiles later).
 // ---------------------------------------------------------------------------
 
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
@@ -1099,52 +1166,48 @@ __device__ __forceinline__ void split_pair(float v0, float v1, uint32_t &hi, uin
     lo = (uint32_t)l0 | ((uint32_t)l1 << 16);
 }
 
-// Polls n (<= 8) chunks of 8 tagged elements, chunk c at base + c*cstride
-// (16-byte aligned): one word per chunk first, then all words, two chunks'
-// loads in flight together. Returns false on abort/timeout.
-__device__ __forceinline__ bool ll_read_blocks(const Params &p, const uint2 *base, int cstride, uint32_t tag,
-                                               float (&out)[8][8]) {
+// Reads 4 chunks of 8 tagged elements, chunk c at base + 32*c (16-byte
+// aligned). All 16 loads go out together; if any element is not yet
+// published, one word per chunk is polled before all are read again.
+// Returns false on abort/timeout.
+__device__ __forceinline__ bool ll_read_blocks4(const Params &p, const uint2 *base, uint32_t tag,
+                                                float (&out)[4][8]) {
 #pragma unroll
-    for (int c = 0; c < 8; ++c)
-        if (!CHK(base + c * cstride, 64, 38)) return false;
+    for (int c = 0; c < 4; ++c)
+        if (!CHK(base + 32 * c, 64, 38)) return false;
     Spin sp;
     while (true) {
+        uint4 v[4][4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) v[c][k] = ll_ld16(base + 32 * c + 2 * k);
         bool ok = true;
-        uint2 v[8];
 #pragma unroll
-        for (int c = 0; c < 8; ++c) v[c] = ll_ld8(base + c * cstride + 7);
+        for (int c = 0; c < 4; ++c)
 #pragma unroll
-        for (int c = 0; c < 8; ++c) ok = ok && v[c].y == tag;
-        if (ok) break;
-        if (!sp.keep_going(p)) return false;
-    }
+            for (int k = 0; k < 4; ++k) ok = ok && v[c][k].y == tag && v[c][k].w == tag;
+        if (ok) {
 #pragma unroll
-    for (int h = 0; h < 8; h += 2) {
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    out[c][2 * k] = __uint_as_float(v[c][k].x);
+                    out[c][2 * k + 1] = __uint_as_float(v[c][k].z);
+                }
+            return true;
+        }
         while (true) {
-            uint4 v[2][4];
-            bool ok = true;
+            bool ready = true;
+            uint2 w[4];
 #pragma unroll
-            for (int i = 0; i < 2; ++i)
+            for (int c = 0; c < 4; ++c) w[c] = ll_ld8(base + 32 * c + 7);
 #pragma unroll
-                for (int k = 0; k < 4; ++k) v[i][k] = ll_ld16(base + (h + i) * cstride + 2 * k);
-#pragma unroll
-            for (int i = 0; i < 2; ++i)
-#pragma unroll
-                for (int k = 0; k < 4; ++k) ok = ok && v[i][k].y == tag && v[i][k].w == tag;
-            if (ok) {
-#pragma unroll
-                for (int i = 0; i < 2; ++i)
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        out[h + i][2 * k] = __uint_as_float(v[i][k].x);
-                        out[h + i][2 * k + 1] = __uint_as_float(v[i][k].z);
-                    }
-                break;
-            }
+            for (int c = 0; c < 4; ++c) ready = ready && w[c].y == tag;
             if (!sp.keep_going(p)) return false;
+            if (ready) break;
         }
     }
-    return true;
 }
 
 __device__ bool gemv_batch(const Params &p, const Ctx &cx, const Instr &in, uint32_t &t, bool &bad) {
@@ -1156,6 +1219,9 @@ __device__ bool gemv_batch(const Params &p, const Ctx &cx, const Instr &in, uint
     const bool gu = op == OP_GATEUP;
     const int per = gu ? R / 2 : R;  // output rows per tile
     const int nrb = (n + per - 1) / per;
+    const bool ring = batch_ring(n, op);
+    const int gsz = ring ? 8 : nrb;
+    const int nt = nrb * nkc;
     const uint32_t ep8 = cx.misc->ep8;
     const LayerW *lw = p.layers + l;
     const int gq = lane >> 2, tq = lane & 3;  // MMA fragment coordinates
@@ -1175,19 +1241,17 @@ __device__ bool gemv_batch(const Params &p, const Ctx &cx, const Instr &in, uint
         case OP_OPROJ: src = p.attll + (size_t)l * nb * p.Hq * p.hd; sstride = (size_t)p.Hq * p.hd; break;
         default: src = p.hll + (size_t)l * nb * p.F; sstride = p.F; break;  // OP_DOWN
     }
-    // shared accumulators: per output row (and gate/up half) and sequence, for
-    // the whole instruction when they fit, else a ring of 8 tiles (LM head)
-    const int vals = gu ? 2 : 1;
-    const bool ring = n * vals * kMaxBatch > kRedCap;
     float *acc = cx.red;
     int *cnt = reinterpret_cast<int *>(cx.dred);  // arrivals per row block (or ring slot)
     float *resid = cx.resid;                       // [nb][n] residual rows (O-proj, down)
+    float *ssum = cx.misc->red8;                   // [kMaxBatch] sums of squares of the inputs
     {
-        const int na = ring ? 8 * R * kMaxBatch : n * vals * kMaxBatch;
+        const int na = ring ? 8 * R * kMaxBatch : n * (gu ? 2 : 1) * kMaxBatch;
         for (int i = tid; i < na; i += kConsumerThreads)
             if (CHKS(acc + i, 4, 55)) acc[i] = 0.f;
         for (int i = tid; i < (ring ? 8 : nrb); i += kConsumerThreads)
             if (CHKS(cnt + i, 4, 56)) cnt[i] = 0;
+        if (tid < kMaxBatch) ssum[tid] = 0.f;
     }
     if (op == OP_OPROJ || op == OP_DOWN) {
         const uint32_t rtag = ep8 | (uint32_t)(op == OP_OPROJ ? 2 * l : 2 * l + 1);
@@ -1203,41 +1267,47 @@ __device__ bool gemv_batch(const Params &p, const Ctx &cx, const Instr &in, uint
             if (CHKS(resid + i, 4, 54)) resid[i] = v;
         }
     }
-    // This lane's inputs: sequence gq, elements 32*blk + 8*tq .. +8 of the
-    // warp's slice (blk = 0..7), as (hi, lo) bf16 pairs: the A fragments of
-    // all 16 MMAs of a tile. Sequences >= nb are zero.
-    uint32_t xh[8][4], xl[8][4];
-    float ss = 0.f;  // this lane's part of its sequence's sum of squares
-    auto load_inputs = [&](int kc) -> bool {
-        float xv[8][8];
-        const int e0 = kc * KC + ks * 256 + 8 * tq;  // + 32 * blk
+    bad = consumer_sync_any(bad);
+    if (bad) return true;
+    // This lane's inputs: sequence gq, elements 32*c + 8*tq .. +8 of the
+    // warp's slice (c = 0..3), times the norm gain, as (hi, lo) bf16 pairs:
+    // the A fragments of all 16 MMAs of a tile. Sequences >= nb are zero.
+    uint32_t xh[4][4], xl[4][4];
+    auto load_inputs = [&](int kc, bool first) -> bool {
+        float xv[4][8];
+        const int e0 = kc * KC + ks * 128 + 8 * tq;  // + 32 * c
         bool ok = true;
         if (gq >= nb) {
 #pragma unroll
-            for (int c = 0; c < 8; ++c)
+            for (int c = 0; c < 4; ++c)
 #pragma unroll
                 for (int e = 0; e < 8; ++e) xv[c][e] = 0.f;
         } else if (emb) {
             const uint16_t *row = p.embed + (size_t)current_token(p, gq) * p.d + e0;
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
+            for (int c = 0; c < 4; ++c) {
                 uint4 w = make_uint4(0u, 0u, 0u, 0u);
                 if (CHK(row + 32 * c, 16, 9)) w = __ldg(reinterpret_cast<const uint4 *>(row + 32 * c));
                 xv[c][0] = bf_lo(w.x); xv[c][1] = bf_hi(w.x); xv[c][2] = bf_lo(w.y); xv[c][3] = bf_hi(w.y);
                 xv[c][4] = bf_lo(w.z); xv[c][5] = bf_hi(w.z); xv[c][6] = bf_lo(w.w); xv[c][7] = bf_hi(w.w);
             }
         } else {
-            ok = ll_read_blocks(p, src + (size_t)gq * sstride + e0, 32, tag, xv);
+            ok = ll_read_blocks4(p, src + (size_t)gq * sstride + e0, tag, xv);
         }
-        if (gain) {  // one K-chunk: keep the raw values' squares, scale after the barrier
-            ss = 0.f;
+        if (gain) {
+            if (first && rg == 0) {  // each chunk's squares once (row group 0); lanes 4g .. 4g+3 hold sequence g
+                float ss = 0.f;
 #pragma unroll
-            for (int c = 0; c < 8; ++c)
+                for (int c = 0; c < 4; ++c)
 #pragma unroll
-                for (int e = 0; e < 8; ++e) ss = fmaf(xv[c][e], xv[c][e], ss);
+                    for (int e = 0; e < 8; ++e) ss = fmaf(xv[c][e], xv[c][e], ss);
+                ss += __shfl_xor_sync(0xFFFFFFFFu, ss, 1);
+                ss += __shfl_xor_sync(0xFFFFFFFFu, ss, 2);
+                if (tq == 0 && gq < nb) atomicAdd(ssum + gq, ss);
+            }
             const uint16_t *gp = gain + e0;
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
+            for (int c = 0; c < 4; ++c) {
                 uint4 gw = make_uint4(0u, 0u, 0u, 0u);
                 if (CHK(gp + 32 * c, 16, 11)) gw = __ldg(reinterpret_cast<const uint4 *>(gp + 32 * c));
                 xv[c][0] *= bf_lo(gw.x); xv[c][1] *= bf_hi(gw.x); xv[c][2] *= bf_lo(gw.y); xv[c][3] *= bf_hi(gw.y);
@@ -1245,131 +1315,124 @@ __device__ bool gemv_batch(const Params &p, const Ctx &cx, const Instr &in, uint
             }
         }
 #pragma unroll
-        for (int c = 0; c < 8; ++c)
+        for (int c = 0; c < 4; ++c)
 #pragma unroll
             for (int k = 0; k < 4; ++k) split_pair(xv[c][2 * k], xv[c][2 * k + 1], xh[c][k], xl[c][k]);
         return ok;
     };
-    if (!bad && !load_inputs(0)) bad = true;
-    float *ssw = cx.xbuf;  // [8 warps][kMaxBatch] partial sums of squares
-    if (gain) {
-        // lanes 4g .. 4g+3 hold sequence g's slice
-        ss += __shfl_xor_sync(0xFFFFFFFFu, ss, 1);
-        ss += __shfl_xor_sync(0xFFFFFFFFu, ss, 2);
-        if (tq == 0 && CHKS(ssw + warp * kMaxBatch + gq, 4, 57)) ssw[warp * kMaxBatch + gq] = ss;
-    }
-    bad = consumer_sync_any(bad);
-    if (bad) return true;
-    if (gain) {
-        // RMSNorm: x * g / rms; the gain is already in, the 1/rms factor is
-        // applied to the hi/lo pairs exactly as a fp32 rescale of the inputs
-        float tot = 0.f;
-        for (int w = 0; w < sw; ++w) tot += ssw[w * kMaxBatch + gq];  // the row group's distinct slices
-        const float rs = 1.0f / sqrtf(tot / (float)K + p.eps);
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const float v0 = (bf16f((uint16_t)(xh[c][k] & 0xFFFFu)) + bf16f((uint16_t)(xl[c][k] & 0xFFFFu))) * rs;
-                const float v1 = (bf16f((uint16_t)(xh[c][k] >> 16)) + bf16f((uint16_t)(xl[c][k] >> 16))) * rs;
-                split_pair(v0, v1, xh[c][k], xl[c][k]);
-            }
-    }
     phase_stamp(p, cx, 0);
-    // this warp's 8 rows of a tile (MMA columns): rows ra0 + c, for gate/up
-    // columns 0-3 gate rows and 4-7 the up rows of the same outputs
-    const int ra0 = gu ? rg * 4 : rg * 8;
-    const int mycol = gq;  // the weight row this lane loads: MMA column gq
-    const int wrow = gu ? (mycol < 4 ? ra0 + mycol : per + ra0 + mycol - 4) : ra0 + mycol;
+    // this warp's 16 rows of a tile: MMA column block 0 and 1, column gq of
+    // each is the weight row this lane loads; for gate/up block 0 holds gate
+    // rows and block 1 the up rows of the same outputs
+    const int ra0 = gu ? rg * 8 : rg * 16;
+    const int trow0 = ra0 + gq, trow1 = gu ? per + ra0 + gq : ra0 + 8 + gq;
     const int row_u4 = KC / 8;
     const uint4 *pages = reinterpret_cast<const uint4 *>(cx.pages);
-    const int woff = wrow * row_u4 + ks * 32 + tq;  // + 4 * blk: 16 bytes at element 32*blk + 8*tq
+    const int woff0 = trow0 * row_u4 + ks * 16 + tq, woff1 = trow1 * row_u4 + ks * 16 + tq;  // + 4 * c
     const bool tracing = p.trace != nullptr;
     unsigned long long best = 0ull;  // LM head: this lane's best key of sequence lane & 7
     int pg = (int)(t % kPages);
     uint32_t par = (t / kPages) & 1u;
-    for (int kc = 0; kc < nkc; ++kc) {
-        if (kc > 0 && !bad && !load_inputs(kc)) bad = true;
-        const bool last_chunk = kc == nkc - 1;
-        for (int rb = 0; rb < nrb; ++rb) {
-            const int j = kc * nrb + rb;
-            if (!bad && !wait_tile(p, cx, pg, par, tracing)) bad = true;
-            bad = __any_sync(0xFFFFFFFFu, bad);
-            const int slot = ring ? (j & 7) : rb;
-            if (!bad) {
-                const uint4 *page = pages + pg * (kPageBytes / 16) + woff;
-                uint4 w[8];
-#pragma unroll
-                for (int c = 0; c < 8; ++c) w[c] = page[4 * c];
-                __syncwarp();  // the page is free once its weights are in registers
-                if (lane == 0) mbar_arrive(&cx.empty[pg]);
-                float d[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    mma_bf16_16816(d, xh[c][0], xl[c][0], xh[c][1], xl[c][1], w[c].x, w[c].y);
-                    mma_bf16_16816(d, xh[c][2], xl[c][2], xh[c][3], xl[c][3], w[c].z, w[c].w);
-                }
-                // d0/d1: sequence gq (hi) at columns 2tq, 2tq+1; d2/d3: its lo part
-                const float s0 = d[0] + d[2], s1 = d[1] + d[3];
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int col = 2 * tq + h;
-                    const int trow = gu ? (col < 4 ? ra0 + col : per + ra0 + col - 4) : ra0 + col;  // tile row
-                    int arow;  // accumulator row
-                    if (ring) arow = slot * R + trow;
-                    else if (gu) arow = (rb * per + (trow % per)) * 2 + (trow >= per ? 1 : 0);
-                    else arow = rb * per + trow;
-                    const int orow = rb * per + (gu ? trow % per : trow);
-                    if (gq < nb && orow < n && CHKS(acc + arow * kMaxBatch + gq, 4, 58))
-                        atomicAdd(acc + arow * kMaxBatch + gq, h ? s1 : s0);
-                }
-            } else {
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&cx.empty[pg]);
-            }
-            ++t;
-            if (++pg == kPages) {
-                pg = 0;
-                par ^= 1u;
-            }
-            if (!last_chunk) continue;
-            // the last warp to finish this tile publishes its rows
-            __threadfence_block();
-            __syncwarp();
-            int old = 0;
-            if (lane == 0 && CHKS(cnt + slot, 4, 59)) old = atomicAdd(cnt + slot, 1);
-            old = __shfl_sync(0xFFFFFFFFu, old, 0);
-            if (old != kConsumerWarps - 1 || bad) continue;
-            __threadfence_block();
-            for (int idx = lane; idx < per * kMaxBatch; idx += 32) {
-                const int i = idx / kMaxBatch, b = idx % kMaxBatch;  // b == lane & 7
-                const int o = rb * per + i;
-                const int arow = ring ? slot * R + i : (gu ? o * 2 : o);
-                const float v = acc[arow * kMaxBatch + b];
-                if (b < nb && o < n) {
-                    if (op == OP_QKV) {
-                        uint2 *dst = p.qkvll + ((size_t)l * nb + b) * (p.Hq + 2 * p.Hkv) * p.hd + r0 + o;
-                        if (CHK(dst, 8, 12)) ll_store(dst, v, ep8);
-                    } else if (op == OP_OPROJ || op == OP_DOWN) {
-                        const uint32_t wtag = ep8 | (uint32_t)(op == OP_OPROJ ? 2 * l + 1 : 2 * l + 2);
-                        uint2 *dst = p.xll + (size_t)b * p.d + r0 + o;
-                        if (CHK(dst, 8, 15)) ll_store(dst, resid[b * n + o] + v, wtag);
-                    } else if (gu) {
-                        const float up = acc[(arow + 1) * kMaxBatch + b];
-                        uint2 *dst = p.hll + ((size_t)l * nb + b) * p.F + r0 + o;
-                        if (CHK(dst, 8, 16)) ll_store(dst, v / (1.0f + expf(-v)) * up, ep8);
-                    } else {  // LM head
-                        float *lg = p.out_logits ? p.out_logits + (size_t)b * p.V + r0 + o : nullptr;
-                        if (lg && CHK(lg, 4, 18)) *lg = v;
-                        const unsigned long long key = argmax_key(v, (uint32_t)(r0 + o));
-                        best = key > best ? key : best;
-                    }
-                }
-                if (ring) acc[arow * kMaxBatch + b] = 0.f;
-            }
-            if (ring && lane == 0) cnt[slot] = 0;
-            __threadfence_block();
+    int cur = -1;  // (group, K-chunk) whose inputs the registers hold
+    for (int j = 0; j < nt; ++j) {
+        const BTile bt = batch_tile(j, nrb, nkc, gsz);
+        const int rb = bt.rb, grp = rb / gsz;
+        const int key = grp * nkc + bt.kc;
+        if (key != cur) {
+            if (!bad && !load_inputs(bt.kc, grp == 0)) bad = true;
+            cur = key;
         }
+        const bool last_chunk = bt.kc == nkc - 1;
+        if (!bad && !wait_tile(p, cx, pg, par, tracing)) bad = true;
+        bad = __any_sync(0xFFFFFFFFu, bad);
+        const int slot = ring ? (rb & 7) : rb;
+        if (!bad) {
+            const uint4 *page = pages + pg * (kPageBytes / 16);
+            uint4 w0[4], w1[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                w0[c] = page[woff0 + 4 * c];
+                w1[c] = page[woff1 + 4 * c];
+            }
+            __syncwarp();  // the page is free once its weights are in registers
+            if (lane == 0) mbar_arrive(&cx.empty[pg]);
+            float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                mma_bf16_16816(d0, xh[c][0], xl[c][0], xh[c][1], xl[c][1], w0[c].x, w0[c].y);
+                mma_bf16_16816(d1, xh[c][0], xl[c][0], xh[c][1], xl[c][1], w1[c].x, w1[c].y);
+                mma_bf16_16816(d0, xh[c][2], xl[c][2], xh[c][3], xl[c][3], w0[c].z, w0[c].w);
+                mma_bf16_16816(d1, xh[c][2], xl[c][2], xh[c][3], xl[c][3], w1[c].z, w1[c].w);
+            }
+            // d[0], d[1]: sequence gq (hi) at columns 2tq, 2tq+1; d[2], d[3] its lo part
+            if (gq < nb) {
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    const int blk = h >> 1, col = 2 * tq + (h & 1);
+                    const float v = blk ? d1[h & 1] + d1[2 + (h & 1)] : d0[h & 1] + d0[2 + (h & 1)];
+                    int o, arow;  // output row within the tile, accumulator row
+                    if (gu) {
+                        o = ra0 + col;
+                        arow = ((ring ? slot : rb) * per + o) * 2 + blk;
+                    } else {
+                        o = ra0 + 8 * blk + col;
+                        arow = (ring ? slot * R : rb * per) + o;
+                    }
+                    if (rb * per + o < n && CHKS(acc + arow * kMaxBatch + gq, 4, 58))
+                        atomicAdd(acc + arow * kMaxBatch + gq, v);
+                }
+            }
+        } else {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&cx.empty[pg]);
+        }
+        ++t;
+        if (++pg == kPages) {
+            pg = 0;
+            par ^= 1u;
+        }
+        if (!last_chunk) continue;
+        // the last warp to finish this tile publishes its rows
+        __threadfence_block();
+        __syncwarp();
+        int old = 0;
+        if (lane == 0 && CHKS(cnt + slot, 4, 59)) old = atomicAdd(cnt + slot, 1);
+        old = __shfl_sync(0xFFFFFFFFu, old, 0);
+        if (old != kConsumerWarps - 1 || bad) continue;
+        __threadfence_block();
+        const int b = lane & 7;  // the sequence of every element this lane finalizes
+        const float rs = gain && b < nb ? 1.0f / sqrtf(ssum[b] / (float)K + p.eps) : 1.0f;
+        for (int idx = lane; idx < per * kMaxBatch; idx += 32) {
+            const int i = idx / kMaxBatch;
+            const int o = rb * per + i;
+            const int arow = gu ? ((ring ? slot : rb) * per + i) * 2 : (ring ? slot * R : rb * per) + i;
+            if (b < nb && o < n) {
+                const float v = acc[arow * kMaxBatch + b] * rs;
+                if (op == OP_QKV) {
+                    uint2 *dst = p.qkvll + ((size_t)l * nb + b) * (p.Hq + 2 * p.Hkv) * p.hd + r0 + o;
+                    if (CHK(dst, 8, 12)) ll_store(dst, v, ep8);
+                } else if (op == OP_OPROJ || op == OP_DOWN) {
+                    const uint32_t wtag = ep8 | (uint32_t)(op == OP_OPROJ ? 2 * l + 1 : 2 * l + 2);
+                    uint2 *dst = p.xll + (size_t)b * p.d + r0 + o;
+                    if (CHK(dst, 8, 15)) ll_store(dst, resid[b * n + o] + v, wtag);
+                } else if (gu) {
+                    const float up = acc[(arow + 1) * kMaxBatch + b] * rs;
+                    uint2 *dst = p.hll + ((size_t)l * nb + b) * p.F + r0 + o;
+                    if (CHK(dst, 8, 16)) ll_store(dst, v / (1.0f + expf(-v)) * up, ep8);
+                } else {  // LM head
+                    float *lg = p.out_logits ? p.out_logits + (size_t)b * p.V + r0 + o : nullptr;
+                    if (lg && CHK(lg, 4, 18)) *lg = v;
+                    const unsigned long long key2 = argmax_key(v, (uint32_t)(r0 + o));
+                    best = key2 > best ? key2 : best;
+                }
+            }
+            if (ring) {
+                acc[arow * kMaxBatch + b] = 0.f;
+                if (gu) acc[(arow + 1) * kMaxBatch + b] = 0.f;
+            }
+        }
+        if (ring && lane == 0) cnt[slot] = 0;
+        __threadfence_block();
     }
     phase_stamp(p, cx, 1);
     if (op != OP_LMHEAD) return false;

@@ -81,9 +81,9 @@ static_assert(sizeof(Instr) == 64, "Instr must be 64 bytes");
 // A warp owns rows of a tile (row group rg) and a K-slice (ks):
 //   sw = K-slices per row, rw = 8/sw row groups, m rows per warp per tile,
 //   rt = rw*m rows per tile, nx = floats of the input each lane keeps.
-// Batched steps: tiles hold rt rows x a K-chunk of pad (<= 2048) columns,
-// each warp a 256-wide slice of the chunk (nx = 8 per sequence) and m = 8
-// rows; the chunks of one row are separate tiles.
+// Batched steps: tiles hold rt rows x a K-chunk of pad (<= 1024) columns,
+// each warp a 128-wide slice of the chunk (kslice) and m = 16 rows; the
+// chunks of one row are separate tiles.
 struct Geo {
     int32_t K, sw, rw, m, rt, nx, kslice, pad;
 };

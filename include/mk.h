@@ -189,7 +189,11 @@ int mk_set_trace(mk_handle *h, int32_t enable);
  * the instruction spent waiting for its weight / KV tiles to land. Phases of
  * a GEMV instruction: input polled (and normalised), tiles done, epilogue
  * written; of an attention instruction: q/k/v polled, tiles done, output
- * written. Returns the number of records (or a negative status). cap = records. */
+ * written. The last traced step is a single-sequence or a fused batched
+ * step (mk_decode_step_batch), whichever ran last with tracing on. Returns
+ * the number of records copied (or a negative status); cap = records that
+ * fit in host_out. With host_out NULL, returns the number of records the
+ * last traced step holds and copies nothing. */
 int mk_read_trace(mk_handle *h, int64_t *host_out, int32_t cap);
 
 /* Diagnostics of a library built with MK_CHECKED (every device-side global
@@ -205,7 +209,10 @@ int mk_debug_read(mk_handle *h, uint64_t *host_out4);
 int mk_plan_size(const mk_handle *h, int32_t *n_sm, int32_t *n_instr);
 
 /* Host-only, no device needed: plans the queues for `config` on `n_sm` SMs
- * and writes them out for inspection. out_instr receives n_instr records of
+ * and writes them out for inspection. With config->max_batch > 1 and a model
+ * the fused batched step supports, this is the batched step's plan (ATTN
+ * records then carry the sequence index in mat), else the single-sequence
+ * plan. out_instr receives n_instr records of
  * MK_INSTR_WORDS int32 (queue order, SM after SM), out_queue_len[n_sm] the
  * queue lengths, *out_n_counters the number of dependency counters.
  * Returns the number of instructions, or a negative status if cap is too

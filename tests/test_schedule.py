@@ -253,3 +253,130 @@ def test_attention_splits_cover_every_cached_position():
                 t = attn_tiles(pos, S, 128, s)
                 got += [p for ts, n in t for p in range(ts, ts + n)]
             assert got == list(range(pos)), (pos, S)
+
+
+# ---- the fused batched step's plan (max_batch > 1) ----
+
+BATCH_CASES = [(TINY, 152, 40, 3), (TINY, 16, 24, 2), (LLAMA_1B, 152, 1024, 8), (LLAMA_1B, 148, 600, 4)]
+
+
+def simulate_batch(instr, queues, nctr, shape, nb, seed):
+    """As simulate(), with one merge per (sequence, layer, kv head)."""
+    rng = random.Random(seed)
+    ctr = [0] * nctr
+    L, Hkv = shape.n_layers, shape.n_kv_heads
+    S = sum(1 for r in instr if r[F_OP] == OP_ATTN and r[F_LAYER] == 0 and r[F_A0] == 0 and r[F_MAT] == 0)
+    attn_done0 = 2 * L * Hkv
+    merged = defaultdict(int)
+    ptr = [0] * len(queues)
+    remaining = sum(len(q) for q in queues)
+    while remaining:
+        ready = [s for s, q in enumerate(queues) if ptr[s] < len(q)
+                 and (q[ptr[s]][F_WAIT] < 0 or ctr[int(q[ptr[s]][F_WAIT])] >= int(q[ptr[s]][F_TGT]))]
+        if not ready:
+            return False
+        s = rng.choice(ready)
+        r = queues[s][ptr[s]]
+        ptr[s] += 1
+        remaining -= 1
+        for c in range(int(r[F_SIG]), int(r[F_SIG]) + int(r[F_SIGN])):
+            ctr[c] += 1
+        if r[F_OP] == OP_ATTN:
+            key = (int(r[F_MAT]), int(r[F_LAYER]), int(r[F_A0]))
+            merged[key] += 1
+            if merged[key] == S:
+                ctr[attn_done0 + int(r[F_LAYER])] += 1
+    return True
+
+
+@pytest.mark.parametrize("shape,n_sm,max_seq,nb", BATCH_CASES)
+def test_batched_plan_covers_every_row_and_sequence(shape, n_sm, max_seq, nb):
+    instr, qlen, nctr = _lib.plan_inspect(shape, n_sm, max_seq, max_batch=nb)
+    hd, d, F = shape.head_dim, shape.d_model, shape.ffn_dim
+    stacked = (shape.n_heads + 2 * shape.n_kv_heads) * hd
+    by = defaultdict(list)
+    for r in instr:
+        op, l = int(r[F_OP]), int(r[F_LAYER])
+        if op == OP_ATTN:
+            by[(op, l, int(r[F_A0]), int(r[F_MAT]))].append((int(r[F_A1]), 1))
+        else:
+            assert int(r[F_MAT]) == 0
+            by[(op, l)].append((int(r[F_A0]), int(r[F_A1])))
+    S = len(by[(OP_ATTN, 0, 0, 0)])
+    assert S >= 1
+    assert not any(k[0] == OP_ATTN and k[3] >= nb for k in by)
+    for l in range(shape.n_layers):
+        cover(by[(OP_QKV, l)], stacked)
+        for b in range(nb):
+            for h in range(shape.n_kv_heads):
+                cover(by[(OP_ATTN, l, h, b)], S)
+        cover(by[(OP_OPROJ, l)], d)
+        cover(by[(OP_GATEUP, l)], F)
+        cover(by[(OP_DOWN, l)], d)
+    cover(by[(OP_LMHEAD, 0)], shape.vocab)
+    # shared-memory capacities of the batched GEMV: accumulators for all 8
+    # sequence lanes of every output row (two per row for gate/up), and the
+    # residual rows of every sequence for O-proj and down
+    for r in instr:
+        op, n = int(r[F_OP]), int(r[F_A1])
+        if op in (OP_QKV, OP_OPROJ, OP_DOWN):
+            assert n * 8 <= REDCAP
+        if op == OP_GATEUP:
+            assert 2 * n * 8 <= REDCAP
+        if op in (OP_OPROJ, OP_DOWN):
+            assert n * nb <= RESID
+    queues, k = [], 0
+    for q in qlen:
+        queues.append(instr[k:k + q])
+        k += q
+    for seed in range(2):
+        assert simulate_batch(instr, queues, nctr, shape, nb, seed)
+
+
+def batch_geo(K):
+    KC = min(K, 1024)
+    sw = KC // 128
+    return dict(K=K, KC=KC, sw=sw, rt=(WARPS // sw) * 16)
+
+
+@pytest.mark.parametrize("shape,n_sm,max_seq,nb", BATCH_CASES)
+def test_batched_tile_copies_stay_in_bounds(shape, n_sm, max_seq, nb):
+    # tile = rt rows x a K-chunk of KC columns; a K-chunked tile is copied
+    # row by row (KC*2 bytes each, 16-byte aligned); every warp's 16 rows and
+    # 128-wide slice lie inside the tile
+    instr, _, _ = _lib.plan_inspect(shape, n_sm, max_seq, max_batch=nb)
+    d, F, hd = shape.d_model, shape.ffn_dim, shape.head_dim
+    qd, kvd = shape.n_heads * hd, shape.n_kv_heads * hd
+    G = {OP_QKV: batch_geo(d), OP_OPROJ: batch_geo(qd), OP_GATEUP: batch_geo(d), OP_DOWN: batch_geo(F),
+         OP_LMHEAD: batch_geo(d)}
+    mat_rows = {OP_QKV: qd + 2 * kvd, OP_OPROJ: d, OP_GATEUP: F, OP_DOWN: d, OP_LMHEAD: shape.vocab}
+    for r in instr:
+        op = int(r[F_OP])
+        if op == OP_ATTN:
+            continue
+        g = G[op]
+        assert g["K"] % g["KC"] == 0 and g["rt"] * g["KC"] * 2 <= PAGE and (g["KC"] * 2) % 16 == 0
+        per = g["rt"] // 2 if op == OP_GATEUP else g["rt"]
+        n, a0 = int(r[F_A1]), int(r[F_A0])
+        for j in range(-(-n // per)):
+            rows = min(per, n - j * per)
+            assert rows > 0 and a0 + j * per + rows <= mat_rows[op]
+        # warp (rg, ks): rows rg*16 .. +16 (gate/up: rg*8 .. +8 of each half), columns ks*128 .. +128
+        for w in range(WARPS):
+            rg, ks = w // g["sw"], w % g["sw"]
+            assert (ks + 1) * 128 <= g["KC"]
+            if op == OP_GATEUP:
+                assert per + rg * 8 + 8 <= g["rt"]
+            else:
+                assert rg * 16 + 16 <= g["rt"]
+
+
+def test_batched_plan_falls_back_where_unsupported():
+    # head_dim 128 has no batched kernel instance, and TINY on 5 SMs would
+    # need more LM-head rows per SM than the shared accumulators hold: both
+    # give the single-sequence plan (no attention for sequences > 0)
+    for shape, n_sm in ((LLAMA_3B, 152), (TINY, 5)):
+        instr, _, _ = _lib.plan_inspect(shape, n_sm, 64, max_batch=2)
+        assert not any(int(r[F_MAT]) > 0 for r in instr if r[F_OP] == OP_ATTN)
+        single, _, _ = _lib.plan_inspect(shape, n_sm, 64)
+        assert np.array_equal(instr, single)
