@@ -469,11 +469,14 @@ int make_image(const mk_config *config, const mk_weights *w, int n_sm, Image &im
     im.o_zero_end = b.off;
     im.o_layers = b.take(sizeof(mk::LayerW) * L);
     im.o_epoch = b.take(sizeof(uint32_t));
-    im.o_x = b.take(8 * (size_t)nb * d);  // tagged words {value, tag}, one row per sequence
+    // tagged words {value, tag}; x, the attention output and h hold one row
+    // per sequence, or (batched steps) all kMaxBatch sequence slots interleaved
+    const size_t nbv = nb > 1 ? (size_t)mk::kMaxBatch : 1;
+    im.o_x = b.take(8 * nbv * d);
     im.o_qkv = b.take(8 * (size_t)L * nb * (Hq + 2 * Hkv) * hd);
     im.o_part = b.take(8 * (size_t)L * nb * Hq * P.S * (hd + 2));
-    im.o_att = b.take(8 * (size_t)L * nb * Hq * hd);
-    im.o_h = b.take(8 * (size_t)L * nb * F);
+    im.o_att = b.take(8 * (size_t)L * nbv * Hq * hd);
+    im.o_h = b.take(8 * (size_t)L * nbv * F);
     im.o_lm = b.take(sizeof(unsigned long long) * nb * P.n_lm);
     im.o_tin = b.take(sizeof(int32_t) * nb);
     im.o_tout = b.take(sizeof(int32_t) * nb);

@@ -239,6 +239,16 @@ __device__ __forceinline__ uint2 ll_ld8(const uint2 *src) {  // one tagged eleme
     return make_uint2((uint32_t)a, (uint32_t)(a >> 32));
 }
 
+// Batched steps keep x, the attention output and h of all kMaxBatch
+// sequence slots interleaved so that the batched GEMV's input reads are
+// coalesced: element e of sequence b sits in group (e/32)*4 + (e/2)%4 of 64
+// words, at b*8 + ((e/8)%4)*2 + e%2. The 32 lanes (b, t) of a warp that read
+// elements 8t + 2k, +1 of a 32-element block of every sequence then read one
+// contiguous 512-byte span.
+__device__ __forceinline__ size_t bofs(int b, int e) {
+    return (size_t)(((e >> 5) * 4 + ((e >> 1) & 3)) * 64 + b * 8 + ((e >> 3) & 3) * 2 + (e & 1));
+}
+
 // ---------------------------------------------------------------------------
 // Shared state
 // ---------------------------------------------------------------------------
@@ -1166,22 +1176,24 @@ __device__ __forceinline__ void split_pair(float v0, float v1, uint32_t &hi, uin
     lo = (uint32_t)l0 | ((uint32_t)l1 << 16);
 }
 
-// Reads 4 chunks of 8 tagged elements, chunk c at base + 32*c (16-byte
-// aligned). All 16 loads go out together; if any element is not yet
-// published, one word per chunk is polled before all are read again.
+// Reads elements 32*c + 2*k, +1 (c, k = 0..3) after element e0 = 8t of a
+// 32-element block of one sequence from an interleaved batched buffer: q =
+// buffer + bofs(b, e0), the pair (c, k) at q + 256*c + 64*k. All 16 loads go
+// out together; if any element is not yet published, one word per block is
+// polled before all are read again. out[c][2k + j] = element e0 + 32c + 2k + j.
 // Returns false on abort/timeout.
-__device__ __forceinline__ bool ll_read_blocks4(const Params &p, const uint2 *base, uint32_t tag,
+__device__ __forceinline__ bool ll_read_blocks4(const Params &p, const uint2 *q, uint32_t tag,
                                                 float (&out)[4][8]) {
 #pragma unroll
     for (int c = 0; c < 4; ++c)
-        if (!CHK(base + 32 * c, 64, 38)) return false;
+        if (!CHK(q + 256 * c, 8 * 194, 38)) return false;
     Spin sp;
     while (true) {
         uint4 v[4][4];
 #pragma unroll
         for (int c = 0; c < 4; ++c)
 #pragma unroll
-            for (int k = 0; k < 4; ++k) v[c][k] = ll_ld16(base + 32 * c + 2 * k);
+            for (int k = 0; k < 4; ++k) v[c][k] = ll_ld16(q + 256 * c + 64 * k);
         bool ok = true;
 #pragma unroll
         for (int c = 0; c < 4; ++c)
@@ -1201,7 +1213,7 @@ __device__ __forceinline__ bool ll_read_blocks4(const Params &p, const uint2 *ba
             bool ready = true;
             uint2 w[4];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) w[c] = ll_ld8(base + 32 * c + 7);
+            for (int c = 0; c < 4; ++c) w[c] = ll_ld8(q + 256 * c + 193);
 #pragma unroll
             for (int c = 0; c < 4; ++c) ready = ready && w[c].y == tag;
             if (!sp.keep_going(p)) return false;
@@ -1226,20 +1238,16 @@ __device__ bool gemv_batch(const Params &p, const Ctx &cx, const Instr &in, uint
     const LayerW *lw = p.layers + l;
     const int gq = lane >> 2, tq = lane & 3;  // MMA fragment coordinates
     // inputs: tagged words of each sequence, or its bf16 embedding row (layer-0 QKV)
-    const uint2 *src = nullptr;
-    size_t sstride = 0;
+    const uint2 *src = nullptr;  // interleaved batched buffer (bofs)
     uint32_t tag = ep8;
     const uint16_t *gain = nullptr;
     const bool emb = op == OP_QKV && l == 0;
     switch (op) {
-        case OP_QKV:
-            gain = lw->attn_norm;
-            src = p.xll; sstride = p.d; tag = ep8 | (uint32_t)(2 * l);
-            break;
-        case OP_GATEUP: gain = lw->mlp_norm; src = p.xll; sstride = p.d; tag = ep8 | (uint32_t)(2 * l + 1); break;
-        case OP_LMHEAD: gain = p.final_norm; src = p.xll; sstride = p.d; tag = ep8 | (uint32_t)(2 * p.L); break;
-        case OP_OPROJ: src = p.attll + (size_t)l * nb * p.Hq * p.hd; sstride = (size_t)p.Hq * p.hd; break;
-        default: src = p.hll + (size_t)l * nb * p.F; sstride = p.F; break;  // OP_DOWN
+        case OP_QKV: gain = lw->attn_norm; src = p.xll; tag = ep8 | (uint32_t)(2 * l); break;
+        case OP_GATEUP: gain = lw->mlp_norm; src = p.xll; tag = ep8 | (uint32_t)(2 * l + 1); break;
+        case OP_LMHEAD: gain = p.final_norm; src = p.xll; tag = ep8 | (uint32_t)(2 * p.L); break;
+        case OP_OPROJ: src = p.attll + (size_t)l * kMaxBatch * p.Hq * p.hd; break;
+        default: src = p.hll + (size_t)l * kMaxBatch * p.F; break;  // OP_DOWN
     }
     float *acc = cx.red;
     int *cnt = reinterpret_cast<int *>(cx.dred);  // arrivals per row block (or ring slot)
@@ -1261,7 +1269,7 @@ __device__ bool gemv_batch(const Params &p, const Ctx &cx, const Instr &in, uint
             if (op == OP_OPROJ && l == 0) {
                 const int tok = current_token(p, b);
                 if (CHK(p.embed + (size_t)tok * p.d + r0 + r, 2, 13)) v = bf16f(__ldg(p.embed + (size_t)tok * p.d + r0 + r));
-            } else if (!bad && !ll_read1(p, p.xll + (size_t)b * p.d + r0 + r, rtag, v)) {
+            } else if (!bad && !ll_read1(p, p.xll + bofs(b, r0 + r), rtag, v)) {
                 bad = true;
             }
             if (CHKS(resid + i, 4, 54)) resid[i] = v;
@@ -1292,7 +1300,7 @@ __device__ bool gemv_batch(const Params &p, const Ctx &cx, const Instr &in, uint
                 xv[c][4] = bf_lo(w.z); xv[c][5] = bf_hi(w.z); xv[c][6] = bf_lo(w.w); xv[c][7] = bf_hi(w.w);
             }
         } else {
-            ok = ll_read_blocks4(p, src + (size_t)gq * sstride + e0, tag, xv);
+            ok = ll_read_blocks4(p, src + bofs(gq, e0), tag, xv);
         }
         if (gain) {
             if (first && rg == 0) {  // each chunk's squares once (row group 0); lanes 4g .. 4g+3 hold sequence g
@@ -1413,11 +1421,11 @@ __device__ bool gemv_batch(const Params &p, const Ctx &cx, const Instr &in, uint
                     if (CHK(dst, 8, 12)) ll_store(dst, v, ep8);
                 } else if (op == OP_OPROJ || op == OP_DOWN) {
                     const uint32_t wtag = ep8 | (uint32_t)(op == OP_OPROJ ? 2 * l + 1 : 2 * l + 2);
-                    uint2 *dst = p.xll + (size_t)b * p.d + r0 + o;
+                    uint2 *dst = p.xll + bofs(b, r0 + o);
                     if (CHK(dst, 8, 15)) ll_store(dst, resid[b * n + o] + v, wtag);
                 } else if (gu) {
                     const float up = acc[(arow + 1) * kMaxBatch + b] * rs;
-                    uint2 *dst = p.hll + ((size_t)l * nb + b) * p.F + r0 + o;
+                    uint2 *dst = p.hll + (size_t)l * kMaxBatch * p.F + bofs(b, r0 + o);
                     if (CHK(dst, 8, 16)) ll_store(dst, v / (1.0f + expf(-v)) * up, ep8);
                 } else {  // LM head
                     float *lg = p.out_logits ? p.out_logits + (size_t)b * p.V + r0 + o : nullptr;
@@ -1809,7 +1817,12 @@ __device__ void do_attn_hd(const Params &p, const Ctx &cx, const Instr &in, uint
         }
     }
     consumer_sync();
-    uint2 *out = p.attll + ((size_t)l * p.nb + b) * p.Hq * HD + (size_t)kvh * G * HD;
+    // output word of element idx of this kv group's heads (batched steps: interleaved)
+    auto out_at = [&](int idx) -> uint2 * {
+        const int e = kvh * G * HD + idx;
+        return p.nb > 1 ? p.attll + (size_t)l * kMaxBatch * p.Hq * HD + bofs(b, e)
+                        : p.attll + (size_t)l * p.Hq * HD + e;
+    };
     if (seff == 1) {
         // The only active split holds the whole context: normalise and
         // publish the attention output directly.
@@ -1825,7 +1838,7 @@ __device__ void do_attn_hd(const Params &p, const Ctx &cx, const Instr &in, uint
                 num += wst[(w * G + g) * WS + e] * wgt;
                 den += wst[(w * G + g) * WS + HD + 1] * wgt;
             }
-            if (CHK(out + idx, 8, 27)) ll_store(out + idx, num / den, ep8);
+            if (CHK(out_at(idx), 8, 27)) ll_store(out_at(idx), num / den, ep8);
         }
         return;
     }
@@ -1894,7 +1907,7 @@ __device__ void do_attn_hd(const Params &p, const Ctx &cx, const Instr &in, uint
                 M = Mn;
             }
         }
-        if (!bad && CHK(out + idx, 8, 27)) ll_store(out + idx, num / den, ep8);
+        if (!bad && CHK(out_at(idx), 8, 27)) ll_store(out_at(idx), num / den, ep8);
     }
     bad = consumer_sync_any(bad);
 }
