@@ -173,8 +173,8 @@ int build_plan(const mk_config *c, int n_sm, Plan &P, int nb) {
             !make_geo_batch(d, P.geo_lm))
             return fail(MK_ERR_UNSUPPORTED, "no batched tile geometry for this model");
         // LM-head rows per SM beyond the shared accumulators run through a ring
-        // of 8 tiles, which needs tiles of at most 32 rows
-        if ((V + n_sm - 1) / n_sm * mk::kMaxBatch > mk::kRedCap && P.geo_lm.rt * 8 * mk::kMaxBatch > mk::kRedCap)
+        // of 8 tiles, which must fit them
+        if ((V + n_sm - 1) / n_sm * mk::kMaxBatch > mk::kBatchAcc && P.geo_lm.rt * 8 * mk::kMaxBatch > mk::kBatchAcc)
             return fail(MK_ERR_UNSUPPORTED, "no batched LM-head geometry for this model");
     } else if (!make_geo(d, P.geo_qkv) || !make_geo(qd, P.geo_o) || !make_geo(d, P.geo_gu) ||
                !make_geo(F, P.geo_down) || !make_geo(d, P.geo_lm)) {

@@ -585,10 +585,11 @@ __device__ __forceinline__ void l2_prefetch_tile(const Params &p, const L2Cursor
 // it only advances pointers (GEMV tiles of one instruction are equally
 // strided rows of one or two matrices).
 // ---------------------------------------------------------------------------
-// Accumulators of a batched instruction: per output row (two per row for
-// gate/up) and sequence, for the whole instruction, or a ring of 8 tiles.
+// Accumulators of a batched instruction (kBatchAcc floats): per output row
+// (two per row for gate/up) and sequence, for the whole instruction, or a
+// ring of 8 tiles.
 __device__ __forceinline__ bool batch_ring(int n, int op) {
-    return n * (op == OP_GATEUP ? 2 : 1) * kMaxBatch > kRedCap;
+    return n * (op == OP_GATEUP ? 2 : 1) * kMaxBatch > kBatchAcc;
 }
 
 // Tile j of a batched instruction: (K-chunk, row block), in groups of gsz
@@ -1249,16 +1250,15 @@ __device__ bool gemv_batch(const Params &p, const Ctx &cx, const Instr &in, uint
         case OP_OPROJ: src = p.attll + (size_t)l * kMaxBatch * p.Hq * p.hd; break;
         default: src = p.hll + (size_t)l * kMaxBatch * p.F; break;  // OP_DOWN
     }
-    float *acc = cx.red;
-    int *cnt = reinterpret_cast<int *>(cx.dred);  // arrivals per row block (or ring slot)
+    float *acc = cx.xbuf;                          // kBatchAcc floats: xbuf and red
+    int *cnt = reinterpret_cast<int *>(cx.dred);  // ring: arrivals per slot
     float *resid = cx.resid;                       // [nb][n] residual rows (O-proj, down)
     float *ssum = cx.misc->red8;                   // [kMaxBatch] sums of squares of the inputs
     {
         const int na = ring ? 8 * R * kMaxBatch : n * (gu ? 2 : 1) * kMaxBatch;
         for (int i = tid; i < na; i += kConsumerThreads)
             if (CHKS(acc + i, 4, 55)) acc[i] = 0.f;
-        for (int i = tid; i < (ring ? 8 : nrb); i += kConsumerThreads)
-            if (CHKS(cnt + i, 4, 56)) cnt[i] = 0;
+        if (ring && tid < 8 && CHKS(cnt + tid, 4, 56)) cnt[tid] = 0;
         if (tid < kMaxBatch) ssum[tid] = 0.f;
     }
     if (op == OP_OPROJ || op == OP_DOWN) {
@@ -1339,6 +1339,28 @@ __device__ bool gemv_batch(const Params &p, const Ctx &cx, const Instr &in, uint
     const int woff0 = trow0 * row_u4 + ks * 16 + tq, woff1 = trow1 * row_u4 + ks * 16 + tq;  // + 4 * c
     const bool tracing = p.trace != nullptr;
     unsigned long long best = 0ull;  // LM head: this lane's best key of sequence lane & 7
+    // Applies the op's transform to output row o (of the instruction) of
+    // sequence b, accumulator row arow, and publishes it.
+    auto publish = [&](int o, int b, int arow, float rs) {
+        const float v = acc[arow * kMaxBatch + b] * rs;
+        if (op == OP_QKV) {
+            uint2 *dst = p.qkvll + ((size_t)l * nb + b) * (p.Hq + 2 * p.Hkv) * p.hd + r0 + o;
+            if (CHK(dst, 8, 12)) ll_store(dst, v, ep8);
+        } else if (op == OP_OPROJ || op == OP_DOWN) {
+            const uint32_t wtag = ep8 | (uint32_t)(op == OP_OPROJ ? 2 * l + 1 : 2 * l + 2);
+            uint2 *dst = p.xll + bofs(b, r0 + o);
+            if (CHK(dst, 8, 15)) ll_store(dst, resid[b * n + o] + v, wtag);
+        } else if (gu) {
+            const float up = acc[(arow + 1) * kMaxBatch + b] * rs;
+            uint2 *dst = p.hll + (size_t)l * kMaxBatch * p.F + bofs(b, r0 + o);
+            if (CHK(dst, 8, 16)) ll_store(dst, v / (1.0f + expf(-v)) * up, ep8);
+        } else {  // LM head
+            float *lg = p.out_logits ? p.out_logits + (size_t)b * p.V + r0 + o : nullptr;
+            if (lg && CHK(lg, 4, 18)) *lg = v;
+            const unsigned long long key = argmax_key(v, (uint32_t)(r0 + o));
+            best = key > best ? key : best;
+        }
+    };
     int pg = (int)(t % kPages);
     uint32_t par = (t / kPages) & 1u;
     int cur = -1;  // (group, K-chunk) whose inputs the registers hold
@@ -1399,8 +1421,9 @@ __device__ bool gemv_batch(const Params &p, const Ctx &cx, const Instr &in, uint
             pg = 0;
             par ^= 1u;
         }
-        if (!last_chunk) continue;
-        // the last warp to finish this tile publishes its rows
+        if (!ring || !last_chunk) continue;
+        // ring: the last warp to finish a tile of the last K-chunk publishes
+        // its rows and frees the slot
         __threadfence_block();
         __syncwarp();
         int old = 0;
@@ -1408,39 +1431,28 @@ __device__ bool gemv_batch(const Params &p, const Ctx &cx, const Instr &in, uint
         old = __shfl_sync(0xFFFFFFFFu, old, 0);
         if (old != kConsumerWarps - 1 || bad) continue;
         __threadfence_block();
-        const int b = lane & 7;  // the sequence of every element this lane finalizes
-        const float rs = gain && b < nb ? 1.0f / sqrtf(ssum[b] / (float)K + p.eps) : 1.0f;
-        for (int idx = lane; idx < per * kMaxBatch; idx += 32) {
-            const int i = idx / kMaxBatch;
-            const int o = rb * per + i;
-            const int arow = gu ? ((ring ? slot : rb) * per + i) * 2 : (ring ? slot * R : rb * per) + i;
-            if (b < nb && o < n) {
-                const float v = acc[arow * kMaxBatch + b] * rs;
-                if (op == OP_QKV) {
-                    uint2 *dst = p.qkvll + ((size_t)l * nb + b) * (p.Hq + 2 * p.Hkv) * p.hd + r0 + o;
-                    if (CHK(dst, 8, 12)) ll_store(dst, v, ep8);
-                } else if (op == OP_OPROJ || op == OP_DOWN) {
-                    const uint32_t wtag = ep8 | (uint32_t)(op == OP_OPROJ ? 2 * l + 1 : 2 * l + 2);
-                    uint2 *dst = p.xll + bofs(b, r0 + o);
-                    if (CHK(dst, 8, 15)) ll_store(dst, resid[b * n + o] + v, wtag);
-                } else if (gu) {
-                    const float up = acc[(arow + 1) * kMaxBatch + b] * rs;
-                    uint2 *dst = p.hll + (size_t)l * kMaxBatch * p.F + bofs(b, r0 + o);
-                    if (CHK(dst, 8, 16)) ll_store(dst, v / (1.0f + expf(-v)) * up, ep8);
-                } else {  // LM head
-                    float *lg = p.out_logits ? p.out_logits + (size_t)b * p.V + r0 + o : nullptr;
-                    if (lg && CHK(lg, 4, 18)) *lg = v;
-                    const unsigned long long key2 = argmax_key(v, (uint32_t)(r0 + o));
-                    best = key2 > best ? key2 : best;
-                }
-            }
-            if (ring) {
+        {
+            const int b = lane & 7;  // the sequence of every element this lane publishes
+            const float rs = gain && b < nb ? 1.0f / sqrtf(ssum[b] / (float)K + p.eps) : 1.0f;
+            for (int idx = lane; idx < per * kMaxBatch; idx += 32) {
+                const int i = idx / kMaxBatch;
+                const int arow = gu ? (slot * per + i) * 2 : slot * R + i;
+                if (b < nb && rb * per + i < n) publish(rb * per + i, b, arow, rs);
                 acc[arow * kMaxBatch + b] = 0.f;
                 if (gu) acc[(arow + 1) * kMaxBatch + b] = 0.f;
             }
         }
-        if (ring && lane == 0) cnt[slot] = 0;
+        if (lane == 0) cnt[slot] = 0;
         __threadfence_block();
+    }
+    if (!ring) {
+        // all tiles accumulated: every thread publishes rows of one sequence
+        bad = consumer_sync_any(bad);
+        if (bad) return true;
+        const int b = tid & 7;
+        const float rs = gain && b < nb ? 1.0f / sqrtf(ssum[b] / (float)K + p.eps) : 1.0f;
+        if (b < nb)
+            for (int i = tid >> 3; i < n; i += kConsumerThreads / kMaxBatch) publish(i, b, gu ? 2 * i : i, rs);
     }
     phase_stamp(p, cx, 1);
     if (op != OP_LMHEAD) return false;

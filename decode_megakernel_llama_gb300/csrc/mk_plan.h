@@ -25,6 +25,7 @@ constexpr int kThreads = kConsumerThreads + 32;      // + one producer (TMA) war
 constexpr int kPageBytes = 32768;                    // one shared-memory page
 constexpr int kPages = 6;                            // pages in the ring
 constexpr int kRedCap = 2048;                        // floats of per-row partials
+constexpr int kBatchAcc = 8192;                      // floats of the batched GEMV's accumulators (xbuf + red)
 constexpr int kXbufFloats = 6144;                    // staged input (4096 fp32 + 4096 bf16 gains) / attention scratch
 constexpr int kMaxStaged = 4096;                     // max normed input length staged with its gains
 constexpr int kMaxStagedLong = 8192;                 // max un-normed input length (down projection)
@@ -49,6 +50,7 @@ constexpr int kSmemMisc = kSmemBars + 2 * kPages * 8;
 constexpr int kSmemParams = kSmemMisc + 256;      // shared copy of the launch parameters
 constexpr int kParamsSlot = 640;
 constexpr int kSmemBytes = kSmemParams + kParamsSlot;
+static_assert(kSmemXbuf + kBatchAcc * 4 <= kSmemResid, "batched accumulators overlap the residual rows");
 static_assert(kSmemBytes <= 232448, "shared memory of one CTA exceeds 227 KB");
 
 // ---- opcodes ------------------------------------------------------------

@@ -8,7 +8,7 @@ import torch
 import oracle
 from decode_megakernel_llama_gb300 import _lib, synth
 from decode_megakernel_llama_gb300.build import build
-from decode_megakernel_llama_gb300.configs import LLAMA_1B, TINY
+from decode_megakernel_llama_gb300.configs import LLAMA_1B, TINY, ModelShape
 
 from gpu_helpers import compare, oracle_config
 
@@ -119,4 +119,14 @@ def test_llama1b_batch8_short_lockstep(cuda_dev):
     bp = BatchPair(LLAMA_1B, 8, 8)
     prompts = [synth.prompt_tokens(LLAMA_1B.vocab, 3, seq=b) for b in range(8)]
     run_lockstep(bp, prompts, 1, check_from=2)
+    bp.close()
+
+
+def test_wide_vocab_batch2_lm_head_ring(cuda_dev):
+    # more LM-head rows per SM than the shared accumulators hold for all
+    # sequences: the LM head runs through its ring of accumulator slots
+    wide = ModelShape("wide-vocab", 2, 256, 4, 2, 64, 1024, 160000, 1e-5, 1e4)
+    bp = BatchPair(wide, 8, 2)
+    prompts = [synth.prompt_tokens(wide.vocab, 3, seq=b) for b in range(2)]
+    run_lockstep(bp, prompts, 2)
     bp.close()
