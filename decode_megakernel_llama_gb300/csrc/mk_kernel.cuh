@@ -239,14 +239,31 @@ __device__ __forceinline__ uint2 ll_ld8(const uint2 *src) {  // one tagged eleme
     return make_uint2((uint32_t)a, (uint32_t)(a >> 32));
 }
 
-// Batched steps keep x, the attention output and h of all kMaxBatch
-// sequence slots interleaved so that the batched GEMV's input reads are
-// coalesced: element e of sequence b sits in group (e/32)*4 + (e/2)%4 of 64
-// words, at b*8 + ((e/8)%4)*2 + e%2. The 32 lanes (b, t) of a warp that read
-// elements 8t + 2k, +1 of a 32-element block of every sequence then read one
-// contiguous 512-byte span.
+// Batched steps keep x, the attention output and h as plain fp32 with the
+// kMaxBatch sequence slots interleaved, so that the batched GEMV's input
+// reads are coalesced: element e of sequence b sits in group (e/32)*2 +
+// (e/4)%2 of 128 floats, at b*16 + ((e/8)%4)*4 + e%4. The 32 lanes (b, t) of
+// a warp that read elements 8t .. 8t+3 (or 8t+4 .. 8t+7) of a 32-element
+// block of every sequence then read one contiguous 512-byte span. These
+// buffers are published by completion counters (release by the producing
+// instruction, acquire before the consuming one), not by tags.
 __device__ __forceinline__ size_t bofs(int b, int e) {
-    return (size_t)(((e >> 5) * 4 + ((e >> 1) & 3)) * 64 + b * 8 + ((e >> 3) & 3) * 2 + (e & 1));
+    return (size_t)(((e >> 5) * 2 + ((e >> 2) & 1)) * 128 + b * 16 + ((e >> 3) & 3) * 4 + (e & 3));
+}
+
+__device__ __forceinline__ float4 ld_relaxed_f4(const float *src) {
+    float4 v;
+    asm volatile("ld.relaxed.gpu.global.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "l"(src)
+                 : "memory");
+    return v;
+}
+
+__device__ __forceinline__ float ld_relaxed_f(const float *src) {
+    float v;
+    asm volatile("ld.relaxed.gpu.global.f32 %0, [%1];" : "=f"(v) : "l"(src) : "memory");
+    return v;
 }
 
 // ---------------------------------------------------------------------------
@@ -1177,50 +1194,42 @@ __device__ __forceinline__ void split_pair(float v0, float v1, uint32_t &hi, uin
     lo = (uint32_t)l0 | ((uint32_t)l1 << 16);
 }
 
-// Reads elements 32*c + 2*k, +1 (c, k = 0..3) after element e0 = 8t of a
-// 32-element block of one sequence from an interleaved batched buffer: q =
-// buffer + bofs(b, e0), the pair (c, k) at q + 256*c + 64*k. All 16 loads go
-// out together; if any element is not yet published, one word per block is
-// polled before all are read again. out[c][2k + j] = element e0 + 32c + 2k + j.
-// Returns false on abort/timeout.
-__device__ __forceinline__ bool ll_read_blocks4(const Params &p, const uint2 *q, uint32_t tag,
-                                                float (&out)[4][8]) {
+// Reads elements e0 + 32*c + j (c = 0..3, j = 0..7) of one sequence from an
+// interleaved batched buffer, e0 = 8t: q = buffer + bofs(b, e0), the four
+// elements from 32*c + 4*h at q + 256*c + 128*h. All 8 loads go out together.
+__device__ __forceinline__ void ld_blocks4(const float *q, float (&out)[4][8]) {
+    float4 v[4][2];
 #pragma unroll
     for (int c = 0; c < 4; ++c)
-        if (!CHK(q + 256 * c, 8 * 194, 38)) return false;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) v[c][h] = ld_relaxed_f4(q + 256 * c + 128 * h);
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            out[c][4 * h] = v[c][h].x;
+            out[c][4 * h + 1] = v[c][h].y;
+            out[c][4 * h + 2] = v[c][h].z;
+            out[c][4 * h + 3] = v[c][h].w;
+        }
+}
+
+// Completion counters of the batched steps: an instruction that waits on
+// one spins (thread 0, acquire) until it reaches its target, then the
+// consumers' barrier orders everyone's reads after it; a producing
+// instruction releases its counters after a barrier over its writers.
+__device__ __forceinline__ bool ctr_wait(const Params &p, int idx, uint32_t target) {
+    if (idx < 0 || !CHK(p.ctr + idx, 4, 60)) return true;
     Spin sp;
-    while (true) {
-        uint4 v[4][4];
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-            for (int k = 0; k < 4; ++k) v[c][k] = ll_ld16(q + 256 * c + 64 * k);
-        bool ok = true;
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-            for (int k = 0; k < 4; ++k) ok = ok && v[c][k].y == tag && v[c][k].w == tag;
-        if (ok) {
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    out[c][2 * k] = __uint_as_float(v[c][k].x);
-                    out[c][2 * k + 1] = __uint_as_float(v[c][k].z);
-                }
-            return true;
-        }
-        while (true) {
-            bool ready = true;
-            uint2 w[4];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) w[c] = ll_ld8(q + 256 * c + 193);
-#pragma unroll
-            for (int c = 0; c < 4; ++c) ready = ready && w[c].y == tag;
-            if (!sp.keep_going(p)) return false;
-            if (ready) break;
-        }
-    }
+    while (ld_acquire(p.ctr + idx) < target)
+        if (!sp.keep_going(p)) return false;
+    return true;
+}
+
+__device__ __forceinline__ void ctr_signal(const Params &p, int idx, int n) {
+    __threadfence();
+    for (int k = 0; k < n; ++k)
+        if (CHK(p.ctr + idx + k, 4, 61)) red_release_add(p.ctr + idx + k, 1u);
 }
 
 __device__ bool gemv_batch(const Params &p, const Ctx &cx, const Instr &in, uint32_t &t, bool &bad) {
@@ -1239,16 +1248,18 @@ __device__ bool gemv_batch(const Params &p, const Ctx &cx, const Instr &in, uint
     const LayerW *lw = p.layers + l;
     const int gq = lane >> 2, tq = lane & 3;  // MMA fragment coordinates
     // inputs: tagged words of each sequence, or its bf16 embedding row (layer-0 QKV)
-    const uint2 *src = nullptr;  // interleaved batched buffer (bofs)
-    uint32_t tag = ep8;
+    // inputs: interleaved fp32 buffers (bofs), or the bf16 embedding rows (layer-0 QKV)
+    float *const xf = reinterpret_cast<float *>(p.xll);
+    float *const hf = reinterpret_cast<float *>(p.hll) + (size_t)l * kMaxBatch * p.F;
+    const float *src = nullptr;
     const uint16_t *gain = nullptr;
     const bool emb = op == OP_QKV && l == 0;
     switch (op) {
-        case OP_QKV: gain = lw->attn_norm; src = p.xll; tag = ep8 | (uint32_t)(2 * l); break;
-        case OP_GATEUP: gain = lw->mlp_norm; src = p.xll; tag = ep8 | (uint32_t)(2 * l + 1); break;
-        case OP_LMHEAD: gain = p.final_norm; src = p.xll; tag = ep8 | (uint32_t)(2 * p.L); break;
-        case OP_OPROJ: src = p.attll + (size_t)l * kMaxBatch * p.Hq * p.hd; break;
-        default: src = p.hll + (size_t)l * kMaxBatch * p.F; break;  // OP_DOWN
+        case OP_QKV: gain = lw->attn_norm; src = xf; break;
+        case OP_GATEUP: gain = lw->mlp_norm; src = xf; break;
+        case OP_LMHEAD: gain = p.final_norm; src = xf; break;
+        case OP_OPROJ: src = reinterpret_cast<const float *>(p.attll) + (size_t)l * kMaxBatch * p.Hq * p.hd; break;
+        default: src = hf; break;  // OP_DOWN
     }
     float *acc = cx.xbuf;                          // kBatchAcc floats: xbuf and red
     int *cnt = reinterpret_cast<int *>(cx.dred);  // ring: arrivals per slot
@@ -1261,22 +1272,23 @@ __device__ bool gemv_batch(const Params &p, const Ctx &cx, const Instr &in, uint
         if (ring && tid < 8 && CHKS(cnt + tid, 4, 56)) cnt[tid] = 0;
         if (tid < kMaxBatch) ssum[tid] = 0.f;
     }
-    if (op == OP_OPROJ || op == OP_DOWN) {
-        const uint32_t rtag = ep8 | (uint32_t)(op == OP_OPROJ ? 2 * l : 2 * l + 1);
+    // this instruction's inputs are complete once its wait counter is
+    if (tid == 0 && !bad && !ctr_wait(p, in.wait_ctr, (uint32_t)in.wait_target)) bad = true;
+    bad = consumer_sync_any(bad);
+    if (bad) return true;
+    if (op == OP_OPROJ || op == OP_DOWN) {  // residual rows of every sequence
         for (int i = tid; i < n * nb; i += kConsumerThreads) {
             const int b = i / n, r = i % n;
-            float v = 0.f;
+            float v;
             if (op == OP_OPROJ && l == 0) {
                 const int tok = current_token(p, b);
-                if (CHK(p.embed + (size_t)tok * p.d + r0 + r, 2, 13)) v = bf16f(__ldg(p.embed + (size_t)tok * p.d + r0 + r));
-            } else if (!bad && !ll_read1(p, p.xll + bofs(b, r0 + r), rtag, v)) {
-                bad = true;
+                v = CHK(p.embed + (size_t)tok * p.d + r0 + r, 2, 13) ? bf16f(__ldg(p.embed + (size_t)tok * p.d + r0 + r)) : 0.f;
+            } else {
+                v = CHK(xf + bofs(b, r0 + r), 4, 14) ? ld_relaxed_f(xf + bofs(b, r0 + r)) : 0.f;
             }
             if (CHKS(resid + i, 4, 54)) resid[i] = v;
         }
     }
-    bad = consumer_sync_any(bad);
-    if (bad) return true;
     // This lane's inputs: sequence gq, elements 32*c + 8*tq .. +8 of the
     // warp's slice (c = 0..3), times the norm gain, as (hi, lo) bf16 pairs:
     // the A fragments of all 16 MMAs of a tile. Sequences >= nb are zero.
@@ -1299,8 +1311,10 @@ __device__ bool gemv_batch(const Params &p, const Ctx &cx, const Instr &in, uint
                 xv[c][0] = bf_lo(w.x); xv[c][1] = bf_hi(w.x); xv[c][2] = bf_lo(w.y); xv[c][3] = bf_hi(w.y);
                 xv[c][4] = bf_lo(w.z); xv[c][5] = bf_hi(w.z); xv[c][6] = bf_lo(w.w); xv[c][7] = bf_hi(w.w);
             }
+        } else if (CHK(src + bofs(gq, e0), 16, 38) && CHK(src + bofs(gq, e0) + 896, 16, 38)) {
+            ld_blocks4(src + bofs(gq, e0), xv);
         } else {
-            ok = ll_read_blocks4(p, src + bofs(gq, e0), tag, xv);
+            ok = false;
         }
         if (gain) {
             if (first && rg == 0) {  // each chunk's squares once (row group 0); lanes 4g .. 4g+3 hold sequence g
@@ -1347,13 +1361,12 @@ __device__ bool gemv_batch(const Params &p, const Ctx &cx, const Instr &in, uint
             uint2 *dst = p.qkvll + ((size_t)l * nb + b) * (p.Hq + 2 * p.Hkv) * p.hd + r0 + o;
             if (CHK(dst, 8, 12)) ll_store(dst, v, ep8);
         } else if (op == OP_OPROJ || op == OP_DOWN) {
-            const uint32_t wtag = ep8 | (uint32_t)(op == OP_OPROJ ? 2 * l + 1 : 2 * l + 2);
-            uint2 *dst = p.xll + bofs(b, r0 + o);
-            if (CHK(dst, 8, 15)) ll_store(dst, resid[b * n + o] + v, wtag);
+            float *dst = xf + bofs(b, r0 + o);
+            if (CHK(dst, 4, 15)) *dst = resid[b * n + o] + v;
         } else if (gu) {
             const float up = acc[(arow + 1) * kMaxBatch + b] * rs;
-            uint2 *dst = p.hll + (size_t)l * kMaxBatch * p.F + bofs(b, r0 + o);
-            if (CHK(dst, 8, 16)) ll_store(dst, v / (1.0f + expf(-v)) * up, ep8);
+            float *dst = hf + bofs(b, r0 + o);
+            if (CHK(dst, 4, 16)) *dst = v / (1.0f + expf(-v)) * up;
         } else {  // LM head
             float *lg = p.out_logits ? p.out_logits + (size_t)b * p.V + r0 + o : nullptr;
             if (lg && CHK(lg, 4, 18)) *lg = v;
@@ -1453,6 +1466,14 @@ __device__ bool gemv_batch(const Params &p, const Ctx &cx, const Instr &in, uint
         const float rs = gain && b < nb ? 1.0f / sqrtf(ssum[b] / (float)K + p.eps) : 1.0f;
         if (b < nb)
             for (int i = tid >> 3; i < n; i += kConsumerThreads / kMaxBatch) publish(i, b, gu ? 2 * i : i, rs);
+    }
+    // O-proj, gate/up and down release their completion counters (the
+    // attention of QKV's outputs and the LM head's argmax use their own
+    // protocols)
+    if (op == OP_OPROJ || op == OP_GATEUP || op == OP_DOWN) {
+        bad = consumer_sync_any(bad);
+        if (bad) return true;
+        if (tid == 0) ctr_signal(p, in.sig_ctr, in.sig_n);
     }
     phase_stamp(p, cx, 1);
     if (op != OP_LMHEAD) return false;
@@ -1830,10 +1851,16 @@ __device__ void do_attn_hd(const Params &p, const Ctx &cx, const Instr &in, uint
     }
     consumer_sync();
     // output word of element idx of this kv group's heads (batched steps: interleaved)
-    auto out_at = [&](int idx) -> uint2 * {
-        const int e = kvh * G * HD + idx;
-        return p.nb > 1 ? p.attll + (size_t)l * kMaxBatch * p.Hq * HD + bofs(b, e)
-                        : p.attll + (size_t)l * p.Hq * HD + e;
+    // (batched steps: plain fp32, interleaved, released by the attn_done counter)
+    uint2 *const out = p.attll + (size_t)l * p.Hq * HD + (size_t)kvh * G * HD;
+    float *const outf = reinterpret_cast<float *>(p.attll) + (size_t)l * kMaxBatch * p.Hq * HD;
+    auto put = [&](int idx, float v) {
+        if (p.nb > 1) {
+            float *dst = outf + bofs(b, kvh * G * HD + idx);
+            if (CHK(dst, 4, 27)) *dst = v;
+        } else if (CHK(out + idx, 8, 27)) {
+            ll_store(out + idx, v, ep8);
+        }
     };
     if (seff == 1) {
         // The only active split holds the whole context: normalise and
@@ -1850,7 +1877,11 @@ __device__ void do_attn_hd(const Params &p, const Ctx &cx, const Instr &in, uint
                 num += wst[(w * G + g) * WS + e] * wgt;
                 den += wst[(w * G + g) * WS + HD + 1] * wgt;
             }
-            if (CHK(out_at(idx), 8, 27)) ll_store(out_at(idx), num / den, ep8);
+            put(idx, num / den);
+        }
+        if (p.nb > 1) {  // batched steps: release this (sequence, kv head)'s output
+            consumer_sync();
+            if (tid == 0) ctr_signal(p, p.cl.attn_done + l, 1);
         }
         return;
     }
@@ -1919,9 +1950,10 @@ __device__ void do_attn_hd(const Params &p, const Ctx &cx, const Instr &in, uint
                 M = Mn;
             }
         }
-        if (!bad && CHK(out_at(idx), 8, 27)) ll_store(out_at(idx), num / den, ep8);
+        if (!bad) put(idx, num / den);
     }
     bad = consumer_sync_any(bad);
+    if (p.nb > 1 && !bad && tid == 0) ctr_signal(p, p.cl.attn_done + l, 1);
 }
 
 // ---------------------------------------------------------------------------
