@@ -25,6 +25,7 @@ extern "C" cudaError_t mk_kernel_configure(void);
 extern "C" cudaError_t mk_kernel_launch(const mk::Params *p, int n_sm, int cooperative,
                                         cudaStream_t stream);
 extern "C" cudaError_t mk_kernel_occupancy(int *blocks_per_sm);
+extern "C" cudaError_t mk_convert_bf16_f16(const void *src, void *dst, size_t n, cudaStream_t stream);
 
 namespace {
 
@@ -484,7 +485,7 @@ int make_image(const mk_config *config, const mk_weights *w, int n_sm, Image &im
     im.o_rope = b.take(sizeof(float) * im.rope.size());
     im.o_instr = b.take(sizeof(Instr) * im.flat.size());
     im.o_qbeg = b.take(sizeof(int32_t) * im.qbeg.size());
-    im.n_ranges = 5 + 9 * L;
+    im.n_ranges = 6 + 9 * L;
     im.o_ranges = b.take(sizeof(unsigned long long) * 2 * im.n_ranges);
     im.total = b.off;
     return MK_OK;
@@ -505,6 +506,7 @@ void fill_params(const Image &im, const mk_config *config, const mk_weights *w,
     p.cl = P.cl;
     p.embed = (const uint16_t *)w->embed;
     p.final_norm = (const uint16_t *)w->final_norm;
+    p.lm_w = p.embed;
     p.layers = reinterpret_cast<const mk::LayerW *>(base + im.o_layers);
     p.kc = (uint16_t *)kv->k;
     p.vc = (uint16_t *)kv->v;
@@ -540,7 +542,7 @@ void fill_params(const Image &im, const mk_config *config, const mk_weights *w,
 }
 
 int upload_image(const Image &im, const mk_config *config, const mk_weights *w,
-                 const mk_kv_cache *kv, char *base, cudaStream_t s) {
+                 const mk_kv_cache *kv, char *base, cudaStream_t s, const void *lm_w) {
     const mk_config &c = *config;
     const int L = c.n_layers, d = c.d_model, Hq = c.n_heads, Hkv = c.n_kv_heads, hd = c.head_dim,
               F = c.ffn_dim, V = c.vocab;
@@ -556,6 +558,7 @@ int upload_image(const Image &im, const mk_config *config, const mk_weights *w,
     add_range(kv->v, kv_bytes);
     add_range(w->embed, (size_t)V * d * 2);
     add_range(w->final_norm, (size_t)d * 2);
+    add_range(lm_w, lm_w ? (size_t)V * d * 2 : 0);  // (an empty range when absent)
     const int qd = Hq * hd, kvd = Hkv * hd;
     for (int l = 0; l < L; ++l) {
         const mk_layer_weights &lw = w->layers[l];
@@ -645,6 +648,7 @@ struct mk_handle {
     mkint::Image bim;
     mk::Params bbase{};
     void *bdev_mem = nullptr;
+    void *w16 = nullptr;  // fp16 copies of the GEMV weights and the LM head (batched steps)
     size_t bzero_bytes = 0;
 };
 
@@ -729,23 +733,69 @@ int mk_create(const mk_config *config, const mk_weights *w, const mk_kv_cache *k
     mkint::fill_params(h->im, config, w, kv, base, h->base);
     if (config->max_batch > 1 && config->max_batch <= mk::kMaxBatch &&
         mkint::make_image(config, w, n_sm, h->bim, config->max_batch) == MK_OK) {
-        e = cudaMalloc(&h->bdev_mem, h->bim.total);
+        // the batched step runs its GEMVs on fp16 copies of the weights
+        const mk_config &c = *config;
+        const size_t d = c.d_model, qd = (size_t)c.n_heads * c.head_dim, kvd = (size_t)c.n_kv_heads * c.head_dim,
+                     F = c.ffn_dim;
+        const size_t per_layer = qd * d + 2 * kvd * d + d * qd + 2 * F * d + d * F;
+        const size_t n16 = per_layer * c.n_layers + (size_t)c.vocab * d;
+        std::vector<mk_layer_weights> lw16(c.n_layers);
+        mk_weights w16 = *w;
+        uint16_t *lm16 = nullptr;
+        e = cudaMalloc(&h->w16, n16 * 2);
+        if (e == cudaSuccess) {
+            uint16_t *dst = static_cast<uint16_t *>(h->w16);
+            auto copy = [&](const void *src, size_t n) -> const void * {
+                uint16_t *at = dst;
+                if (e == cudaSuccess) e = mk_convert_bf16_f16(src, at, n, nullptr);
+                dst += n;
+                return at;
+            };
+            for (int l = 0; l < c.n_layers; ++l) {
+                const mk_layer_weights &a = w->layers[l];
+                mk_layer_weights &b = lw16[l];
+                b = a;
+                b.wq = copy(a.wq, qd * d);
+                b.wk = copy(a.wk, kvd * d);
+                b.wv = copy(a.wv, kvd * d);
+                b.wo = copy(a.wo, d * qd);
+                b.w_gate = copy(a.w_gate, F * d);
+                b.w_up = copy(a.w_up, F * d);
+                b.w_down = copy(a.w_down, d * F);
+            }
+            lm16 = const_cast<uint16_t *>(static_cast<const uint16_t *>(copy(w->embed, (size_t)c.vocab * d)));
+            if (e == cudaSuccess) e = cudaDeviceSynchronize();
+            w16.layers = lw16.data();
+            // the image's layer table points at the copies
+            for (int l = 0; l < c.n_layers; ++l) {
+                const mk_layer_weights &b = lw16[l];
+                h->bim.lws[l] = {(const uint16_t *)b.attn_norm, (const uint16_t *)b.wq, (const uint16_t *)b.wk,
+                                 (const uint16_t *)b.wv, (const uint16_t *)b.wo, (const uint16_t *)b.mlp_norm,
+                                 (const uint16_t *)b.w_gate, (const uint16_t *)b.w_up, (const uint16_t *)b.w_down};
+            }
+        }
+        if (e == cudaSuccess) e = cudaMalloc(&h->bdev_mem, h->bim.total);
         if (e != cudaSuccess) {
-            cudaFree(h->dev_mem);
-            delete h;
-            return cuda_fail(e, "cudaMalloc(batched scratch)");
+            // no room for the batched step: batches run sequence by sequence
+            cudaGetLastError();
+            if (h->w16) cudaFree(h->w16);
+            h->w16 = nullptr;
+            h->bdev_mem = nullptr;
+        } else {
+            char *bb = static_cast<char *>(h->bdev_mem);
+            rc = mkint::upload_image(h->bim, config, &w16, kv, bb, nullptr, lm16);
+            if (rc) {
+                cudaFree(h->bdev_mem);
+                cudaFree(h->w16);
+                cudaFree(h->dev_mem);
+                delete h;
+                return rc;
+            }
+            mkint::fill_params(h->bim, config, &w16, kv, bb, h->bbase);
+            h->bbase.lm_w = lm16;
+            h->bzero_bytes = h->bim.o_zero_end - h->bim.o_ctr;
+            h->has_batch = true;
         }
-        char *bb = static_cast<char *>(h->bdev_mem);
-        rc = mkint::upload_image(h->bim, config, w, kv, bb, nullptr);
-        if (rc) {
-            cudaFree(h->bdev_mem);
-            cudaFree(h->dev_mem);
-            delete h;
-            return rc;
-        }
-        mkint::fill_params(h->bim, config, w, kv, bb, h->bbase);
-        h->bzero_bytes = h->bim.o_zero_end - h->bim.o_ctr;
-        h->has_batch = true;
     }
     fail(MK_OK, "");  // a model without batched instances is not an error
     h->d_tok_in = reinterpret_cast<int32_t *>(base + h->im.o_tin);
@@ -935,6 +985,7 @@ void mk_destroy(mk_handle *h) {
     if (h->d_trace) cudaFree(h->d_trace);
     if (h->dev_mem) cudaFree(h->dev_mem);
     if (h->bdev_mem) cudaFree(h->bdev_mem);
+    if (h->w16) cudaFree(h->w16);
     delete h;
 }
 

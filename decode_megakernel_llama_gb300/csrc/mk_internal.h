@@ -33,8 +33,10 @@ struct Image {
 int check_inputs(const mk_config *config, const mk_weights *w, const mk_kv_cache *kv);
 int check_device(int *dev, int *n_sm);
 int make_image(const mk_config *config, const mk_weights *w, int n_sm, Image &im, int nb = 1);
+// lm_w: a separate copy of the LM-head weights to register for the
+// address self-checks (batched steps), or NULL
 int upload_image(const Image &im, const mk_config *config, const mk_weights *w,
-                 const mk_kv_cache *kv, char *base, cudaStream_t s);
+                 const mk_kv_cache *kv, char *base, cudaStream_t s, const void *lm_w = nullptr);
 void fill_params(const Image &im, const mk_config *config, const mk_weights *w,
                  const mk_kv_cache *kv, char *base, mk::Params &p);
 int launch_step(const mk::Params &base, int n_sm, int n_stages, int32_t token,

@@ -1,6 +1,7 @@
 // mk_kernel.cu — host-side launch helpers of the megakernel (called from
 // mk_host.cpp): picks the instance for the model's head dimension and group
 // size and launches it.
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "mk_plan.h"
@@ -46,4 +47,19 @@ extern "C" cudaError_t mk_kernel_occupancy(int *blocks_per_sm) {
     // every instance has the same block size and shared memory
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, kernel_for(64, 4), mk::kThreads,
                                                          mk::kSmemBytes);
+}
+
+namespace {
+// bf16 -> fp16, round to nearest (exact for magnitudes in fp16's normal range)
+__global__ void bf16_to_f16(const uint16_t *__restrict__ src, uint16_t *__restrict__ dst, size_t n) {
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
+        dst[i] = __half_as_ushort(__float2half_rn(__uint_as_float((uint32_t)src[i] << 16)));
+}
+}  // namespace
+
+// fp16 copy of n bf16 values (device pointers), on `stream`.
+extern "C" cudaError_t mk_convert_bf16_f16(const void *src, void *dst, size_t n, cudaStream_t stream) {
+    if (n == 0) return cudaSuccess;
+    bf16_to_f16<<<1024, 256, 0, stream>>>(static_cast<const uint16_t *>(src), static_cast<uint16_t *>(dst), n);
+    return cudaGetLastError();
 }

@@ -29,6 +29,7 @@
 // in the status word, raises the abort flag that all CTAs poll, waits for
 // its own copies in flight and returns. Nothing traps. Counters remain only
 // for the LM head's global argmax and for the end of the step.
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -563,7 +564,7 @@ __device__ __forceinline__ TileCopy tile_copy(const Params &p, const Instr &in, 
         }
         case OP_OPROJ: c.src0 = lw->wo + row0 * g.K; break;
         case OP_DOWN: c.src0 = lw->w_down + row0 * g.K; break;
-        default: c.src0 = p.embed + row0 * g.K; break;
+        default: c.src0 = p.lm_w + row0 * g.K; break;
     }
     return c;
 }
@@ -637,7 +638,7 @@ __device__ __forceinline__ const uint16_t *batch_row(const Params &p, const Inst
         case OP_GATEUP: return (up ? lw->w_up : lw->w_gate) + row * K;
         case OP_OPROJ: return lw->wo + row * K;
         case OP_DOWN: return lw->w_down + row * K;
-        default: return p.embed + row * K;
+        default: return p.lm_w + row * K;
     }
 }
 
@@ -1153,15 +1154,15 @@ __device__ void do_gemv(const Params &p, const Ctx &cx, const Instr &in, uint32_
 
 // ---------------------------------------------------------------------------
 // Batched GEMV (nb > 1 sequences in one step, every weight read once): a
-// real contraction Y[nb, rows] = X[nb, K] W^T, on the tensor cores with
-// mma.sync m16n8k16 (bf16 in, fp32 accumulate). MMA rows 0-7 are the 8
-// sequences' inputs rounded to bf16 (hi), rows 8-15 the remainders (lo), so
-// hi + lo carries the fp32 input to within 2^-16; the MMA columns are weight
-// rows.
+// real contraction Y[rows, nb] = W X^T, on the tensor cores with mma.sync
+// m16n8k16 (fp16 in, fp32 accumulate): A = 16 weight rows from the handle's
+// fp16 copy of the bf16 weights (exact in fp16's normal range), B = the 8
+// sequences' inputs rounded to fp16 (relative error <= 2^-11), D in
+// registers.
 // Tile = rt rows x a K-chunk of KC = g.pad columns (32 KB). Warp (rg, ks)
-// owns 16 rows of every tile (two MMA column blocks; for gate/up 8 gate rows
-// and the matching 8 up rows) and the 128-wide slice ks of the chunk: 16
-// MMAs per tile, its inputs in 32 registers. The k order inside each
+// owns 16 rows of every tile (the MMA's A rows; for gate/up 8 gate rows and
+// the matching 8 up rows) and the 128-wide slice ks of the chunk: 8 MMAs per
+// tile, its inputs in 16 registers. The k order inside each
 // 32-column block is permuted identically for X and W so that every lane
 // reads 16 contiguous bytes of a weight row. Lanes add their (sequence, row)
 // sums into a shared accumulator; the last warp to finish a tile of the last
@@ -1177,22 +1178,16 @@ __device__ void do_gemv(const Params &p, const Ctx &cx, const Instr &in, uint32_
 // and a slot is reused 8 tiles later).
 // ---------------------------------------------------------------------------
 
-__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                               uint32_t a3, uint32_t b0, uint32_t b1) {
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                              uint32_t a3, uint32_t b0, uint32_t b1) {
     asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
         "{%0,%1,%2,%3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Two fp32 values as (hi, lo) bf16 pairs: hi = bf16(v), lo = bf16(v - hi).
-__device__ __forceinline__ void split_pair(float v0, float v1, uint32_t &hi, uint32_t &lo) {
-    const uint16_t h0 = f2bf(v0), h1 = f2bf(v1);
-    const uint16_t l0 = f2bf(v0 - bf16f(h0)), l1 = f2bf(v1 - bf16f(h1));
-    hi = (uint32_t)h0 | ((uint32_t)h1 << 16);
-    lo = (uint32_t)l0 | ((uint32_t)l1 << 16);
-}
+__device__ __forceinline__ uint32_t f2h(float f) { return (uint32_t)__half_as_ushort(__float2half_rn(f)); }
 
 // Reads elements e0 + 32*c + j (c = 0..3, j = 0..7) of one sequence from an
 // interleaved batched buffer, e0 = 8t: q = buffer + bofs(b, e0), the four
@@ -1247,7 +1242,6 @@ __device__ bool gemv_batch(const Params &p, const Ctx &cx, const Instr &in, uint
     const uint32_t ep8 = cx.misc->ep8;
     const LayerW *lw = p.layers + l;
     const int gq = lane >> 2, tq = lane & 3;  // MMA fragment coordinates
-    // inputs: tagged words of each sequence, or its bf16 embedding row (layer-0 QKV)
     // inputs: interleaved fp32 buffers (bofs), or the bf16 embedding rows (layer-0 QKV)
     float *const xf = reinterpret_cast<float *>(p.xll);
     float *const hf = reinterpret_cast<float *>(p.hll) + (size_t)l * kMaxBatch * p.F;
@@ -1290,9 +1284,9 @@ __device__ bool gemv_batch(const Params &p, const Ctx &cx, const Instr &in, uint
         }
     }
     // This lane's inputs: sequence gq, elements 32*c + 8*tq .. +8 of the
-    // warp's slice (c = 0..3), times the norm gain, as (hi, lo) bf16 pairs:
-    // the A fragments of all 16 MMAs of a tile. Sequences >= nb are zero.
-    uint32_t xh[4][4], xl[4][4];
+    // warp's slice (c = 0..3), times the norm gain, as fp16 pairs: the B
+    // fragments of all 8 MMAs of a tile. Sequences >= nb are zero.
+    uint32_t xb[4][4];
     auto load_inputs = [&](int kc, bool first) -> bool {
         float xv[4][8];
         const int e0 = kc * KC + ks * 128 + 8 * tq;  // + 32 * c
@@ -1339,13 +1333,14 @@ __device__ bool gemv_batch(const Params &p, const Ctx &cx, const Instr &in, uint
 #pragma unroll
         for (int c = 0; c < 4; ++c)
 #pragma unroll
-            for (int k = 0; k < 4; ++k) split_pair(xv[c][2 * k], xv[c][2 * k + 1], xh[c][k], xl[c][k]);
+            for (int k = 0; k < 4; ++k)
+                xb[c][k] = f2h(xv[c][2 * k]) | (f2h(xv[c][2 * k + 1]) << 16);
         return ok;
     };
     phase_stamp(p, cx, 0);
-    // this warp's 16 rows of a tile: MMA column block 0 and 1, column gq of
-    // each is the weight row this lane loads; for gate/up block 0 holds gate
-    // rows and block 1 the up rows of the same outputs
+    // this warp's 16 rows of a tile: this lane loads the A rows gq (trow0)
+    // and gq + 8 (trow1); for gate/up they are the gate row and the up row
+    // of the same output
     const int ra0 = gu ? rg * 8 : rg * 16;
     const int trow0 = ra0 + gq, trow1 = gu ? per + ra0 + gq : ra0 + 8 + gq;
     const int row_u4 = KC / 8;
@@ -1399,31 +1394,27 @@ __device__ bool gemv_batch(const Params &p, const Ctx &cx, const Instr &in, uint
             }
             __syncwarp();  // the page is free once its weights are in registers
             if (lane == 0) mbar_arrive(&cx.empty[pg]);
-            float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+            // A = 16 weight rows (this lane: rows gq and gq + 8), B = the 8
+            // sequences' inputs; D rows gq / gq + 8, columns (sequences) 2tq, 2tq+1
+            float d[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
-                mma_bf16_16816(d0, xh[c][0], xl[c][0], xh[c][1], xl[c][1], w0[c].x, w0[c].y);
-                mma_bf16_16816(d1, xh[c][0], xl[c][0], xh[c][1], xl[c][1], w1[c].x, w1[c].y);
-                mma_bf16_16816(d0, xh[c][2], xl[c][2], xh[c][3], xl[c][3], w0[c].z, w0[c].w);
-                mma_bf16_16816(d1, xh[c][2], xl[c][2], xh[c][3], xl[c][3], w1[c].z, w1[c].w);
+                mma_f16_16816(d, w0[c].x, w1[c].x, w0[c].y, w1[c].y, xb[c][0], xb[c][1]);
+                mma_f16_16816(d, w0[c].z, w1[c].z, w0[c].w, w1[c].w, xb[c][2], xb[c][3]);
             }
-            // d[0], d[1]: sequence gq (hi) at columns 2tq, 2tq+1; d[2], d[3] its lo part
-            if (gq < nb) {
 #pragma unroll
-                for (int h = 0; h < 4; ++h) {
-                    const int blk = h >> 1, col = 2 * tq + (h & 1);
-                    const float v = blk ? d1[h & 1] + d1[2 + (h & 1)] : d0[h & 1] + d0[2 + (h & 1)];
-                    int o, arow;  // output row within the tile, accumulator row
-                    if (gu) {
-                        o = ra0 + col;
-                        arow = ((ring ? slot : rb) * per + o) * 2 + blk;
-                    } else {
-                        o = ra0 + 8 * blk + col;
-                        arow = (ring ? slot * R : rb * per) + o;
-                    }
-                    if (rb * per + o < n && CHKS(acc + arow * kMaxBatch + gq, 4, 58))
-                        atomicAdd(acc + arow * kMaxBatch + gq, v);
+            for (int h = 0; h < 4; ++h) {
+                const int blk = h >> 1, b = 2 * tq + (h & 1);  // weight row block (gq / gq + 8), sequence
+                int o, arow;  // output row within the tile, accumulator row
+                if (gu) {
+                    o = ra0 + gq;
+                    arow = ((ring ? slot : rb) * per + o) * 2 + blk;
+                } else {
+                    o = ra0 + 8 * blk + gq;
+                    arow = (ring ? slot * R : rb * per) + o;
                 }
+                if (b < nb && rb * per + o < n && CHKS(acc + arow * kMaxBatch + b, 4, 58))
+                    atomicAdd(acc + arow * kMaxBatch + b, d[h]);
             }
         } else {
             __syncwarp();

@@ -113,6 +113,7 @@ struct Params {
     CtrLayout cl;
     // weights (borrowed)
     const uint16_t *embed, *final_norm;
+    const uint16_t *lm_w;  // LM-head weight rows: the tied embedding (batched steps: its fp16 copy)
     const LayerW *layers;   // device array [L]
     uint16_t *kc, *vc;      // KV caches
     // scratch (library-owned); activations are tagged words {value, tag}

@@ -10,7 +10,7 @@ from decode_megakernel_llama_gb300 import _lib, synth
 from decode_megakernel_llama_gb300.build import build
 from decode_megakernel_llama_gb300.configs import LLAMA_1B, TINY, ModelShape
 
-from gpu_helpers import compare, oracle_config
+from gpu_helpers import MARGIN, MAX_ABS, compare, oracle_config
 
 pytestmark = pytest.mark.gpu
 
@@ -84,7 +84,10 @@ def test_tiny_batch_positions_differ_per_sequence(cuda_dev):
 
 def test_batched_step_matches_single_sequence_steps(cuda_dev):
     # the fused batched step (all sequences in one launch) against the same
-    # sequences stepped one by one through the single-sequence call
+    # sequences stepped one by one through the single-sequence call: the
+    # fused step feeds its GEMVs bf16 inputs, the single-sequence step fp32,
+    # so they agree to the parity tolerance, with the same greedy token
+    # wherever the top two logits are clearly apart
     a = BatchPair(TINY, 16, 2)
     singles = [BatchPair(TINY, 16, 1), BatchPair(TINY, 16, 1)]
     out = torch.zeros(1, dtype=torch.int32, device="cuda:0")
@@ -95,8 +98,8 @@ def test_batched_step_matches_single_sequence_steps(cuda_dev):
             singles[b].mk.step(toks[b], pos, out, lg)
             torch.cuda.synchronize()
             ls = lg.double().cpu().numpy()
-            assert np.abs(la[b] - ls).max() <= 1e-3, (pos, b, np.abs(la[b] - ls).max())
-            assert ta[b] == int(out.item()) or np.sort(ls)[-1] - np.sort(ls)[-2] < 1e-3
+            assert np.abs(la[b] - ls).max() <= MAX_ABS, (pos, b, np.abs(la[b] - ls).max())
+            assert ta[b] == int(out.item()) or np.sort(ls)[-1] - np.sort(ls)[-2] < MARGIN
     a.close()
     for s_ in singles:
         s_.close()
