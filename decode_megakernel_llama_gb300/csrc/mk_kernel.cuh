@@ -356,42 +356,6 @@ __device__ __forceinline__ bool ll_read_n(const Params &p, const uint2 *const *s
     }
 }
 
-// Waits for NC chunks of 8 tagged elements, chunk c at base + c*stride
-// (16-byte aligned), all loads of a poll in flight together. While the
-// producers are still running it polls a single word (the thread's last
-// element) so that waiting CTAs put one 8-byte load per thread and round on
-// L2 instead of their whole slice.
-template <int NC>
-__device__ __forceinline__ bool ll_read_chunks(const Params &p, const uint2 *base, int stride,
-                                               uint32_t tag, float *out) {
-#pragma unroll
-    for (int c = 0; c < NC; ++c)
-        if (!CHK(base + (size_t)c * stride, 64, 38)) return false;
-    Spin sp;
-    const uint2 *sentinel = base + (size_t)(NC - 1) * stride + 7;
-    while (ll_ld8(sentinel).y != tag)
-        if (!sp.keep_going(p)) return false;
-    while (true) {
-        uint4 v[NC * 4];
-#pragma unroll
-        for (int c = 0; c < NC; ++c)
-#pragma unroll
-            for (int k = 0; k < 4; ++k) v[c * 4 + k] = ll_ld16(base + (size_t)c * stride + 2 * k);
-        bool ok = true;
-#pragma unroll
-        for (int k = 0; k < NC * 4; ++k) ok = ok && v[k].y == tag && v[k].w == tag;
-        if (ok) {
-#pragma unroll
-            for (int k = 0; k < NC * 4; ++k) {
-                out[2 * k] = __uint_as_float(v[k].x);
-                out[2 * k + 1] = __uint_as_float(v[k].z);
-            }
-            return true;
-        }
-        if (!sp.keep_going(p)) return false;
-    }
-}
-
 // Bounded wait on an mbarrier phase.
 __device__ bool wait_bar(const Params &p, uint64_t *bar, uint32_t parity) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -785,26 +749,48 @@ __device__ void producer(const Params &p, const Ctx &cx, int qb, int qe) {
 // GEMV instructions
 // ---------------------------------------------------------------------------
 
-// Polls this thread's nc chunks of 8 tagged elements (chunk c at element
-// (c*256 + tid)*8 of src) with all loads of a poll in flight together, then
-// stores them to xbuf. Returns false on abort/timeout.
-template <int NC>
-__device__ __forceinline__ bool stage_chunks(const Params &p, const Ctx &cx, const uint2 *src,
-                                             uint32_t tag, float &ss) {
-    const int i0 = threadIdx.x * 8;
-    float v[NC * 8];
-    if (!ll_read_chunks<NC>(p, src + i0, kConsumerThreads * 8, tag, v)) return false;
+// Stages the thread's pairs of a tagged vector of K elements: pair u is
+// elements 512*u + 2*tid, +1 (u < NU, those below K), so the threads of a
+// warp read one contiguous 256-byte span per load. While the producers are
+// still running it polls a single word (the thread's last element), so that
+// waiting CTAs put one 8-byte load per thread and round on L2; then all
+// loads of a poll go out together. Returns false on abort/timeout.
+template <int NU>
+__device__ __forceinline__ bool stage_units(const Params &p, const Ctx &cx, const uint2 *src, int K,
+                                            uint32_t tag, float &ss) {
+    const int t2 = threadIdx.x * 2;
+    int last = -1;
 #pragma unroll
-    for (int c = 0; c < NC; ++c) {
-        float *dst = cx.xbuf + i0 + c * kConsumerThreads * 8;
-        if (!CHKS(dst, 32, 47)) return false;
-        *reinterpret_cast<float4 *>(dst) = make_float4(v[c * 8], v[c * 8 + 1], v[c * 8 + 2], v[c * 8 + 3]);
-        *reinterpret_cast<float4 *>(dst + 4) =
-            make_float4(v[c * 8 + 4], v[c * 8 + 5], v[c * 8 + 6], v[c * 8 + 7]);
+    for (int u = 0; u < NU; ++u)
+        if (512 * u + t2 < K) last = u;
+    if (last < 0) return true;
+    if (!CHK(src + t2, 16, 38) || !CHK(src + 512 * last + t2, 16, 38)) return false;
+    Spin sp;
+    const uint2 *sentinel = src + 512 * last + t2 + 1;
+    while (ll_ld8(sentinel).y != tag)
+        if (!sp.keep_going(p)) return false;
+    while (true) {
+        uint4 v[NU];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) ss = fmaf(v[c * 8 + e], v[c * 8 + e], ss);
+        for (int u = 0; u < NU; ++u)
+            v[u] = u <= last ? ll_ld16(src + 512 * u + t2) : make_uint4(0u, tag, 0u, tag);
+        bool ok = true;
+#pragma unroll
+        for (int u = 0; u < NU; ++u) ok = ok && v[u].y == tag && v[u].w == tag;
+        if (ok) {
+#pragma unroll
+            for (int u = 0; u < NU; ++u) {
+                if (u > last) continue;
+                const float a = __uint_as_float(v[u].x), b = __uint_as_float(v[u].z);
+                float *dst = cx.xbuf + 512 * u + t2;
+                if (!CHKS(dst, 8, 47)) return false;
+                *reinterpret_cast<float2 *>(dst) = make_float2(a, b);
+                ss = fmaf(a, a, fmaf(b, b, ss));
+            }
+            return true;
+        }
+        if (!sp.keep_going(p)) return false;
     }
-    return true;
 }
 
 // Two rows at once: both rows' weights are loaded before any FMA so the two
@@ -881,15 +867,13 @@ __device__ bool stage_input(const Params &p, const Ctx &cx, const uint2 *src, co
             for (int e = 0; e < 8; ++e) ss = fmaf(v[e], v[e], ss);
         }
     } else if (ok) {
-        // chunks of this thread that lie inside the vector
-        const int nc = (K - tid * 8 + kConsumerThreads * 8 - 1) / (kConsumerThreads * 8);
-        switch (nc) {
-            case 0: break;
-            case 1: ok = stage_chunks<1>(p, cx, src, tag, ss); break;
-            case 2: ok = stage_chunks<2>(p, cx, src, tag, ss); break;
-            case 3: ok = stage_chunks<3>(p, cx, src, tag, ss); break;
-            default: ok = stage_chunks<4>(p, cx, src, tag, ss); break;
-        }
+        // pairs of 512-element units (K <= 8192)
+        const int nu = (K + 511) / 512;
+        if (nu <= 1) ok = stage_units<1>(p, cx, src, K, tag, ss);
+        else if (nu <= 2) ok = stage_units<2>(p, cx, src, K, tag, ss);
+        else if (nu <= 4) ok = stage_units<4>(p, cx, src, K, tag, ss);
+        else if (nu <= 8) ok = stage_units<8>(p, cx, src, K, tag, ss);
+        else ok = stage_units<16>(p, cx, src, K, tag, ss);
     }
     ss = warp_sum(ss);
     if (lane == 0) cx.misc->red8[warp] = ss;
