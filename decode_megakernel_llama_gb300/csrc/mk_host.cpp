@@ -532,7 +532,7 @@ void fill_params(const Image &im, const mk_config *config, const mk_weights *w,
     if (const char *env = getenv("MK_MAX_INFLIGHT")) p.max_inflight = atoi(env);
     if (p.max_inflight < 1) p.max_inflight = 1;
     if (p.max_inflight > mk::kPages) p.max_inflight = mk::kPages;
-    p.poll_inflight = 1;  // while consumers poll, keep their loads from queuing behind tile data
+    p.poll_inflight = 2;  // while consumers poll, fewer tiles in flight so their loads do not queue behind tile data
     p.l2_tiles = 0;
     if (const char *env = getenv("MK_L2_TILES")) p.l2_tiles = atoi(env);
     if (p.l2_tiles < 0) p.l2_tiles = 0;
