@@ -20,8 +20,9 @@
 //     paging paragraph);
 //   * bf16 weights, fp32 accumulation (latency paragraph).
 //
-// CTA layout: warps 0..7 are consumers (GEMV / attention math), warp 8 lane 0
-// is the producer that issues bulk copies. Page p has a "full" mbarrier
+// CTA layout: warps 0..7 are consumers (GEMV / attention math), warp 8 is
+// the producer: its lane 0 waits for pages and arms their barriers, its
+// lanes issue the bulk copies. Page p has a "full" mbarrier
 // (producer -> consumers, completed by the copy's transaction bytes) and an
 // "empty" mbarrier (8 consumer warps -> producer).
 //
@@ -606,7 +607,10 @@ __device__ __forceinline__ const uint16_t *batch_row(const Params &p, const Inst
     }
 }
 
+// Runs on all 32 lanes of the producer warp: lane 0 waits for free pages
+// and arms each page's barrier, the lanes share a tile's copies.
 __device__ void producer(const Params &p, const Ctx &cx, int qb, int qe) {
+    const int lane = threadIdx.x & 31;
     const uint64_t pol = policy_evict_first();
     uint32_t t = 0;
     int pg = 0;         // page of tile t
@@ -646,28 +650,27 @@ __device__ void producer(const Params &p, const Ctx &cx, int qb, int qe) {
             per = in.op == OP_GATEUP ? g.rt / 2 : g.rt;
         }
         for (int j = 0; j < nt; ++j, ++t) {
-            if (t >= kPages && !mbar_try_wait(&cx.empty[pg], (use - 1) & 1)) {
-                // the ring is full: use the wait to pull the next tiles into L2
-                while (lc.i < qe && lc.t < t) l2_advance(p, lc, qe);
-                while (lc.i < qe && lc.t < t + la && !mbar_try_wait(&cx.empty[pg], (use - 1) & 1)) {
-                    l2_prefetch_tile(p, lc);
-                    l2_advance(p, lc, qe);
+            int fail = 0;
+            if (lane == 0) {
+                if (t >= kPages && !mbar_try_wait(&cx.empty[pg], (use - 1) & 1)) {
+                    // the ring is full: use the wait to pull the next tiles into L2
+                    while (lc.i < qe && lc.t < t) l2_advance(p, lc, qe);
+                    while (lc.i < qe && lc.t < t + la && !mbar_try_wait(&cx.empty[pg], (use - 1) & 1)) {
+                        l2_prefetch_tile(p, lc);
+                        l2_advance(p, lc, qe);
+                    }
+                    if (!wait_bar(p, &cx.empty[pg], (use - 1) & 1)) fail = 1;
                 }
-                if (!wait_bar(p, &cx.empty[pg], (use - 1) & 1)) {
-                    cx.misc->aborted = 1;
-                    return;
+                // at most `b` tiles in flight (fewer while the consumers poll for
+                // an input, so that their loads do not queue behind tile data)
+                const uint32_t b = cx.misc->polling ? pback : back;
+                if (!fail && t >= b) {
+                    const uint32_t tb = t - b;
+                    if (!wait_bar(p, &cx.full[tb % kPages], (tb / kPages) & 1)) fail = 1;
                 }
+                if (fail) cx.misc->aborted = 1;
             }
-            // at most `b` tiles in flight (fewer while the consumers poll for
-            // an input, so that their loads do not queue behind tile data)
-            const uint32_t b = cx.misc->polling ? pback : back;
-            if (t >= b) {
-                const uint32_t tb = t - b;
-                if (!wait_bar(p, &cx.full[tb % kPages], (tb / kPages) & 1)) {
-                    cx.misc->aborted = 1;
-                    return;
-                }
-            }
+            if (__shfl_sync(0xFFFFFFFFu, fail, 0)) return;
             uint8_t *dst = cx.pages + (size_t)pg * kPageBytes;
             if (batched && nkc > 1) {
                 // one copy per row: the rows' segments [kc*KC, (kc+1)*KC) of a
@@ -689,26 +692,24 @@ __device__ void producer(const Params &p, const Ctx &cx, int qb, int qe) {
                     if (row0 + (size_t)rows > bound) m = (int)(bound - row0);
                 }
                 bool ok = rows > 0 && CHKS(dst, (uint32_t)(bper * (halves - 1) + rows) * rbytes, 40);
-                const uint16_t *seg[2][2];  // [half][segment]: source of the segment's first row
-                for (int hf = 0; hf < halves && ok; ++hf) {
-                    seg[hf][0] = batch_row(p, in, row0, hf) + coff;
-                    seg[hf][1] = m < rows ? batch_row(p, in, row0 + m, hf) + coff : seg[hf][0];
-                    ok = CHK(seg[hf][0], rbytes, 3) && CHK(seg[hf][0] + (size_t)(m - 1) * rowlen, rbytes, 3) &&
-                         (m == rows || (CHK(seg[hf][1], rbytes, 3) &&
-                                        CHK(seg[hf][1] + (size_t)(rows - m - 1) * rowlen, rbytes, 3)));
-                }
-                mbar_expect_tx(&cx.full[pg], ok ? (uint32_t)(halves * rows) * rbytes : 0u);
+                // sources of the first row of each segment: (half 0 | 1) x (before | after the boundary)
+                const uint16_t *s00 = batch_row(p, in, row0, false) + coff;
+                const uint16_t *s01 = m < rows ? batch_row(p, in, row0 + m, false) + coff : s00;
+                const uint16_t *s10 = halves > 1 ? batch_row(p, in, row0, true) + coff : s00;
+                const uint16_t *s11 = s10;
+                ok = ok && CHK(s00, rbytes, 3) && CHK(s00 + (size_t)(m - 1) * rowlen, rbytes, 3) &&
+                     (m == rows || (CHK(s01, rbytes, 3) && CHK(s01 + (size_t)(rows - m - 1) * rowlen, rbytes, 3))) &&
+                     (halves == 1 || (CHK(s10, rbytes, 3) && CHK(s10 + (size_t)(rows - 1) * rowlen, rbytes, 3)));
+                if (lane == 0) mbar_expect_tx(&cx.full[pg], ok ? (uint32_t)(halves * rows) * rbytes : 0u);
+                __syncwarp();  // the barrier expects the bytes before any copy lands
                 if (ok)
-                    for (int hf = 0; hf < halves; ++hf) {
-                        uint8_t *d0 = dst + (size_t)hf * bper * rbytes;
-                        const uint16_t *s0 = seg[hf][0];
-                        for (int r = 0; r < m; ++r, s0 += rowlen, d0 += rbytes)
-                            bulk_g2s(d0, s0, rbytes, &cx.full[pg], pol);
-                        s0 = seg[hf][1];
-                        for (int r = m; r < rows; ++r, s0 += rowlen, d0 += rbytes)
-                            bulk_g2s(d0, s0, rbytes, &cx.full[pg], pol);
+                    for (int idx = lane; idx < halves * rows; idx += 32) {
+                        const int hf = idx / rows, r = idx % rows;
+                        const uint16_t *src = r < m ? (hf ? s10 : s00) + (size_t)r * rowlen
+                                                    : (hf ? s11 : s01) + (size_t)(r - m) * rowlen;
+                        bulk_g2s(dst + (size_t)(hf * bper + r) * rbytes, src, rbytes, &cx.full[pg], pol);
                     }
-                cx.misc->n_issued = t + 1;
+                if (lane == 0) cx.misc->n_issued = t + 1;
                 if (++pg == kPages) {
                     pg = 0;
                     ++use;
@@ -731,12 +732,14 @@ __device__ void producer(const Params &p, const Ctx &cx, int qb, int qe) {
             }
             const bool ok = CHK(c.src0, c.bytes0, 3) && (!c.bytes1 || CHK(c.src1, c.bytes1, 4)) &&
                             CHKS(dst, c.bytes0, 40) && (!c.bytes1 || CHKS(dst + c.dst1, c.bytes1, 41));
-            mbar_expect_tx(&cx.full[pg], ok ? c.bytes0 + c.bytes1 : 0u);
-            if (ok) {
-                bulk_g2s(dst, c.src0, c.bytes0, &cx.full[pg], pol);
-                if (c.bytes1) bulk_g2s(dst + c.dst1, c.src1, c.bytes1, &cx.full[pg], pol);
+            if (lane == 0) {
+                mbar_expect_tx(&cx.full[pg], ok ? c.bytes0 + c.bytes1 : 0u);
+                if (ok) {
+                    bulk_g2s(dst, c.src0, c.bytes0, &cx.full[pg], pol);
+                    if (c.bytes1) bulk_g2s(dst + c.dst1, c.src1, c.bytes1, &cx.full[pg], pol);
+                }
+                cx.misc->n_issued = t + 1;
             }
-            cx.misc->n_issued = t + 1;
             if (++pg == kPages) {
                 pg = 0;
                 ++use;
@@ -2047,7 +2050,7 @@ __global__ void __launch_bounds__(kThreads, 1) mk_megakernel(const Params prm) {
     }
     if (run) {
         if (warp == kConsumerWarps) {
-            if (lane == 0) producer(p, cx, qb, qe);
+            producer(p, cx, qb, qe);
         } else {
             consumer<HD, G, BATCH>(p, cx, qb, qe, q0);
         }
