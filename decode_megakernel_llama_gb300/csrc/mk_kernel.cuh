@@ -918,21 +918,15 @@ __device__ void gemv_instr(const Params &p, const Ctx &cx, const Instr &in, cons
         case OP_OPROJ: src = p.attll + (size_t)l * p.Hq * p.hd; break;
         default: src = p.hll + (size_t)l * p.F; break;  // OP_DOWN
     }
-    // residual rows of this instruction (O-projection and down)
-    if (in.op == OP_OPROJ || in.op == OP_DOWN) {
-        const int tok = (in.op == OP_OPROJ && l == 0) ? current_token(p) : 0;
-        const uint32_t rtag = ep8 | (uint32_t)(in.op == OP_OPROJ ? 2 * l : 2 * l + 1);
-        for (int i = tid; i < n; i += kConsumerThreads) {
-            float v = 0.f;
-            if (in.op == OP_OPROJ && l == 0) {
-                if (CHK(p.embed + (size_t)tok * p.d + r0 + i, 2, 13))
-                    v = bf16f(__ldg(p.embed + (size_t)tok * p.d + r0 + i));
-            } else if (!bad && !ll_read1(p, p.xll + r0 + i, rtag, v)) {
-                bad = true;
-            }
-            if (CHKS(cx.resid + i, 4, 54)) cx.resid[i] = v;
-        }
-    }
+    // residual rows of this instruction (O-projection and down; at most one
+    // per thread): the load is issued now and checked after the input is
+    // staged, so its round trip overlaps the input poll
+    const bool has_resid = in.op == OP_OPROJ || in.op == OP_DOWN;
+    const uint32_t rtag = ep8 | (uint32_t)(in.op == OP_OPROJ ? 2 * l : 2 * l + 1);
+    const bool resid_x = has_resid && !(in.op == OP_OPROJ && l == 0) && tid < n &&
+                         CHK(p.xll + r0 + tid, 8, 13);
+    uint2 rword = make_uint2(0u, 0u);
+    if (resid_x) rword = ll_ld8(p.xll + r0 + tid);
     // this lane's input slice
     float xr[NX];
     float *red = in.op == OP_DOWN ? cx.dred : cx.red;
@@ -943,6 +937,21 @@ __device__ void gemv_instr(const Params &p, const Ctx &cx, const Instr &in, cons
         const bool reuse = cx.misc->staged_key == key;
         float ss = cx.misc->staged_ss;
         if (!reuse && !stage_input(p, cx, bad ? nullptr : src, src_bf, tag, g.K, gain, ss)) bad = true;
+        if (has_resid) {
+            const int tok = (in.op == OP_OPROJ && l == 0) ? current_token(p) : 0;
+            for (int i = tid; i < n; i += kConsumerThreads) {
+                float v = 0.f;
+                if (in.op == OP_OPROJ && l == 0) {
+                    if (CHK(p.embed + (size_t)tok * p.d + r0 + i, 2, 13))
+                        v = bf16f(__ldg(p.embed + (size_t)tok * p.d + r0 + i));
+                } else if (i == tid && resid_x && rword.y == rtag) {
+                    v = __uint_as_float(rword.x);
+                } else if (!bad && !ll_read1(p, p.xll + r0 + i, rtag, v)) {
+                    bad = true;
+                }
+                if (CHKS(cx.resid + i, 4, 54)) cx.resid[i] = v;
+            }
+        }
         bad = consumer_sync_any(bad);
         if (tid == 0) {
             cx.misc->staged_key = bad ? -1 : key;
