@@ -391,6 +391,17 @@ def run_mk(args, ws, rank, local):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         e2e_val = 1e6 * float(t.item()) / (K * ws)
 
+    # ---- the same decode loop with the sampling epilogue on (temperature 0.8)
+    mk.set_sampling(0.8, 1234)
+    for s in range(W):
+        mk.step_dev(tok, P + s, tok, None, stream)
+    sampled_us = 1e3 * timed_decode() / K
+    mk.set_sampling(0.0)
+    if mk.status() != 0:
+        raise SystemExit("megakernel status error with sampling")
+    sampling_line = {"us_per_token": sampled_us, "temperature": 0.8,
+                     "note": "Gumbel-max draw from softmax(logits/T), Philox4x32-10 noise per vocabulary entry"}
+
     # ---- comparators: the same kernels as an unfused chain (and as a graph)
     comp = None
     if not args.no_comparators:
@@ -485,6 +496,7 @@ def run_mk(args, ws, rank, local):
             "gpu_launches": K,
             "clocks": clk.summary(),
             "comparators": comp,
+            "sampling": sampling_line,
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)

@@ -82,6 +82,7 @@ def load(path: str | None = None):
     L.mk_get_status.argtypes = [_VP]
     L.mk_set_wait_timeout.argtypes = [_VP, ctypes.c_uint64]
     L.mk_set_trace.argtypes = [_VP, _I32]
+    L.mk_set_sampling.argtypes = [_VP, ctypes.c_float, ctypes.c_uint64]
     L.mk_read_trace.argtypes = [_VP, ctypes.POINTER(ctypes.c_int64), _I32]
     L.mk_plan_size.argtypes = [_VP, _PI32, _PI32]
     L.mk_plan_inspect.argtypes = [ctypes.POINTER(mk_config), _I32, _PI32, _I32, _PI32, _PI32]
@@ -215,6 +216,11 @@ class Megakernel:
 
     def set_wait_timeout(self, ns: int) -> None:
         check(load().mk_set_wait_timeout(self.h, int(ns)))
+
+    def set_sampling(self, temperature: float, seed: int = 0) -> None:
+        """temperature > 0: tokens are drawn from softmax(logits / temperature)
+        (Gumbel-max with Philox noise keyed by seed); <= 0: greedy."""
+        check(load().mk_set_sampling(self.h, float(temperature), int(seed) & ((1 << 64) - 1)))
 
     def set_trace(self, on: bool) -> None:
         check(load().mk_set_trace(self.h, 1 if on else 0))

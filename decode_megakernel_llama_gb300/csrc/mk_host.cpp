@@ -642,6 +642,8 @@ struct mk_handle {
     int trace_cap = 0;
     bool trace_on = false;
     bool trace_batch = false;  // the last traced launch ran the batched image
+    float inv_temp = 0.f;      // sampling (mk_set_sampling); 0: greedy
+    uint64_t seed = 0;
     // batched steps of all max_batch sequences in one launch (max_batch > 1 and
     // a model the batched instances support), with their own scratch
     bool has_batch = false;
@@ -669,6 +671,9 @@ int launch(mk_handle *h, int32_t token, const int32_t *d_token, int32_t position
     p.timeout_ns = h->timeout_ns;
     p.trace = h->trace_on ? h->d_trace : nullptr;
     p.trace_cap = h->trace_cap;
+    p.inv_temp = h->inv_temp;
+    p.seed_lo = (uint32_t)(h->seed & 0xFFFFFFFFu);
+    p.seed_hi = (uint32_t)(h->seed >> 32);
     if (h->trace_on) h->trace_batch = false;
     return mkint::launch_step(p, h->im.n_sm, h->im.n_stages, token, d_token, position, out_logits,
                               out_token, stream, unfused, d_pos, bslot);
@@ -837,6 +842,9 @@ int mk_decode_step_batch(mk_handle *h, const int32_t *d_tokens, const int32_t *d
         p.timeout_ns = h->timeout_ns;
         p.trace = h->trace_on ? h->d_trace : nullptr;
         p.trace_cap = h->trace_cap;
+        p.inv_temp = h->inv_temp;
+        p.seed_lo = (uint32_t)(h->seed & 0xFFFFFFFFu);
+        p.seed_hi = (uint32_t)(h->seed >> 32);
         if (h->trace_on) h->trace_batch = true;
         return mkint::launch_step(p, h->bim.n_sm, h->bim.n_stages, 0, d_tokens, 0, out_logits, out_tokens,
                                   (cudaStream_t)stream, false, d_positions, 0);
@@ -904,6 +912,16 @@ int mk_get_status(mk_handle *h) {
 int mk_set_wait_timeout(mk_handle *h, uint64_t timeout_ns) {
     if (!h || timeout_ns == 0) return fail(MK_ERR_INVALID_ARG, "bad handle or zero timeout");
     h->timeout_ns = timeout_ns;
+    return MK_OK;
+}
+
+int mk_set_sampling(mk_handle *h, float temperature, uint64_t seed) {
+    if (!h) return fail(MK_ERR_INVALID_ARG, "handle is NULL");
+    if (!(temperature == temperature) || temperature > 1e30f || temperature < -1e30f)
+        return fail(MK_ERR_INVALID_ARG, "temperature is not finite");
+    if (temperature > 0.f && 1.0f / temperature > 1e30f) return fail(MK_ERR_INVALID_ARG, "temperature too small");
+    h->inv_temp = temperature > 0.f ? 1.0f / temperature : 0.f;
+    h->seed = seed;
     return MK_OK;
 }
 

@@ -205,6 +205,36 @@ __device__ __noinline__ bool chk_shared(const Params &p, const void *ptr, size_t
 #endif
 
 // Orderable key for the argmax: larger value wins, then lower index.
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw: "Parallel random numbers: as
+// easy as 1, 2, 3", SC'11): word 0 of the output block for counter (c0..c3)
+// and key (k0, k1). Ten rounds of two 32x32->64 multiplies by M0, M1 with
+// the key bumped by the Weyl constants W0, W1 after every round.
+__device__ __forceinline__ uint32_t philox_w0(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3, uint32_t k0,
+                                              uint32_t k1) {
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        const uint32_t lo0 = 0xD2511F53u * c0, hi0 = __umulhi(0xD2511F53u, c0);
+        const uint32_t lo1 = 0xCD9E8D57u * c2, hi1 = __umulhi(0xCD9E8D57u, c2);
+        c0 = hi1 ^ c1 ^ k0;
+        c1 = lo1;
+        c2 = hi0 ^ c3 ^ k1;
+        c3 = lo0;
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+    }
+    return c0;
+}
+
+// Gumbel noise of vocabulary entry i for the sequence on KV slot `slot` at
+// position `pos`: u = (top 24 bits of Philox(i, pos, slot, 0; seed) + 1/2) / 2^24,
+// an open interval (0, 1); g = -log(-log(u)). argmax_i(z_i + g_i) is a draw
+// from softmax(z).
+__device__ __forceinline__ float gumbel_noise(uint32_t i, int pos, int slot, uint32_t seed_lo, uint32_t seed_hi) {
+    const uint32_t x = philox_w0(i, (uint32_t)pos, (uint32_t)slot, 0u, seed_lo, seed_hi);
+    const float u = ((float)(x >> 8) + 0.5f) * (1.0f / 16777216.0f);
+    return -logf(-logf(u));
+}
+
 __device__ __forceinline__ unsigned long long argmax_key(float v, uint32_t idx) {
     uint32_t u = __float_as_uint(v);
     u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
@@ -1097,7 +1127,10 @@ __device__ void do_gemv(const Params &p, const Ctx &cx, const Instr &in, uint32_
                 float v = 0.f;
                 for (int s = 0; s < sw; ++s) v += red[i * sw + s];
                 if (p.out_logits && CHK(p.out_logits + r0 + i, 4, 18)) p.out_logits[r0 + i] = v;
-                const unsigned long long k = argmax_key(v, (uint32_t)(r0 + i));
+                const float z = p.inv_temp > 0.f
+                                    ? v * p.inv_temp + gumbel_noise((uint32_t)(r0 + i), p.pos, p.bslot, p.seed_lo, p.seed_hi)
+                                    : v;
+                const unsigned long long k = argmax_key(z, (uint32_t)(r0 + i));
                 best = k > best ? k : best;
             }
 #pragma unroll
@@ -1359,7 +1392,10 @@ __device__ bool gemv_batch(const Params &p, const Ctx &cx, const Instr &in, uint
         } else {  // LM head
             float *lg = p.out_logits ? p.out_logits + (size_t)b * p.V + r0 + o : nullptr;
             if (lg && CHK(lg, 4, 18)) *lg = v;
-            const unsigned long long key = argmax_key(v, (uint32_t)(r0 + o));
+            const float z = p.inv_temp > 0.f ? v * p.inv_temp + gumbel_noise((uint32_t)(r0 + o), pos_of(p, b), slot_of(p, b),
+                                                                            p.seed_lo, p.seed_hi)
+                                             : v;
+            const unsigned long long key = argmax_key(z, (uint32_t)(r0 + o));
             best = key > best ? key : best;
         }
     };

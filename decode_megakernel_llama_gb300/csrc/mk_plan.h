@@ -144,6 +144,10 @@ struct Params {
     int32_t posb[kMaxBatch];
     float *out_logits;      // nullable
     int32_t *out_token;
+    // sampling (inv_temp > 0): the token is argmax_i(logit_i * inv_temp + g_i)
+    // with Gumbel noise g_i from Philox4x32-10 keyed by the seed; 0: greedy
+    float inv_temp;
+    uint32_t seed_lo, seed_hi;
     unsigned long long timeout_ns;
     long long *trace;       // nullable: [n_sm][trace_cap][kTraceWords]
     int32_t trace_cap;

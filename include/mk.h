@@ -178,6 +178,17 @@ int mk_get_status(mk_handle *h);
  * (default 2e9). Host-only setting, takes effect on the next step. */
 int mk_set_wait_timeout(mk_handle *h, uint64_t timeout_ns);
 
+/* Sampling instead of greedy decoding for the following steps (all entry
+ * points of this handle). temperature > 0: the returned token is a draw from
+ * softmax(logits / temperature), taken as argmax_i(logit_i / temperature +
+ * g_i) with Gumbel noise g_i = -log(-log(u_i)), u_i = (top 24 bits of word 0
+ * of Philox4x32-10(counter {i, position, kv slot, 0}, key {seed low 32 bits,
+ * seed high 32 bits}) + 1/2) / 2^24 — a counter-based draw, so a step is
+ * reproducible from (seed, position, slot). temperature <= 0: greedy (the
+ * default). out_logits stay the unscaled logits. Host-only setting;
+ * MK_ERR_INVALID_ARG for a non-finite or vanishing temperature. */
+int mk_set_sampling(mk_handle *h, float temperature, uint64_t seed);
+
 /* Optional per-instruction timing: when `enable` is non-zero, every step
  * records %globaltimer stamps per instruction into a device buffer that
  * mk_read_trace copies out (see mk_read_trace). */

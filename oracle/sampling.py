@@ -1,0 +1,76 @@
+"""Sampling step of the oracle: a draw from softmax(logits / T) by the
+Gumbel-max rule with counter-based noise.
+
+TEST INFRASTRUCTURE ONLY, like the rest of this package: the test suite is
+its only user. It shares no code with the CUDA library; the library's
+sampling epilogue is a separate implementation of the same two published
+definitions.
+
+* Philox4x32-10 (J. Salmon, M. Moraes, R. Dror, D. Shaw, "Parallel random
+  numbers: as easy as 1, 2, 3", SC'11, section 3): a 128-bit counter and a
+  64-bit key; each of ten rounds multiplies counter words 0 and 2 by the
+  constants M0 = 0xD2511F53 and M1 = 0xCD9E8D57 into 64-bit products and
+  recombines the halves with words 1 and 3 and the key, which is then
+  bumped by the Weyl constants W0 = 0x9E3779B9 and W1 = 0xBB67AE85.
+* The Gumbel-max rule (E. J. Gumbel, 1954; used for sampling by Maddison,
+  Tarlow, Minka, "A* sampling", NIPS 2014): with g_i = -log(-log(u_i)) for
+  independent uniforms u_i, argmax_i(z_i + g_i) is distributed as
+  softmax(z).
+
+The noise of vocabulary entry i for the sequence on KV slot s at position
+pos is u_i = (top 24 bits of output word 0 of Philox(counter (i, pos, s, 0),
+key (seed mod 2^32, seed div 2^32)) + 1/2) / 2^24, and the sampled token is
+argmax_i(logit_i / T + g_i), lowest index on ties. The Philox pins are
+properties (bijectivity for a fixed key, key sensitivity, uniformity); the
+sampler's are a T -> 0 limit (greedy) and the softmax law of the draws.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+M0, M1 = 0xD2511F53, 0xCD9E8D57
+W0, W1 = 0x9E3779B9, 0xBB67AE85
+_MASK = 0xFFFFFFFF
+
+
+def philox4x32_10(c0, c1, c2, c3, k0: int, k1: int) -> tuple:
+    """All four output words of Philox4x32-10, elementwise over counter
+    arrays (any integer arrays of one shape, values < 2^32)."""
+    c = [np.asarray(x, dtype=np.uint64) & _MASK for x in (c0, c1, c2, c3)]
+    k0, k1 = np.uint64(k0 & _MASK), np.uint64(k1 & _MASK)
+    for _ in range(10):
+        p0 = c[0] * np.uint64(M0)           # exact: both factors < 2^32
+        p1 = c[2] * np.uint64(M1)
+        hi0, lo0 = p0 >> np.uint64(32), p0 & np.uint64(_MASK)
+        hi1, lo1 = p1 >> np.uint64(32), p1 & np.uint64(_MASK)
+        c = [hi1 ^ c[1] ^ k0, lo1, hi0 ^ c[3] ^ k1, lo0]
+        k0 = (k0 + np.uint64(W0)) & np.uint64(_MASK)
+        k1 = (k1 + np.uint64(W1)) & np.uint64(_MASK)
+    return tuple(x.astype(np.uint32) for x in c)
+
+
+def uniforms(n: int, position: int, slot: int, seed: int) -> np.ndarray:
+    """u_i in the open interval (0, 1), i = 0..n-1, as float64."""
+    i = np.arange(n, dtype=np.uint64)
+    w0 = philox4x32_10(i, np.full(n, position), np.full(n, slot), np.zeros(n), seed & _MASK,
+                       (seed >> 32) & _MASK)[0]
+    return ((w0 >> np.uint32(8)).astype(np.float64) + 0.5) / 16777216.0
+
+
+def gumbel(n: int, position: int, slot: int, seed: int) -> np.ndarray:
+    u = uniforms(n, position, slot, seed)
+    return -np.log(-np.log(u))
+
+
+def sample_scores(logits: np.ndarray, temperature: float, position: int, slot: int, seed: int) -> np.ndarray:
+    """z_i = logit_i / T + g_i (float64): the token is their argmax."""
+    logits = np.asarray(logits, dtype=np.float64)
+    return logits / temperature + gumbel(logits.shape[0], position, slot, seed)
+
+
+def sample_token(logits: np.ndarray, temperature: float, position: int, slot: int, seed: int) -> int:
+    """Greedy for temperature <= 0, else the Gumbel-max draw (lowest index on
+    ties: np.argmax returns the first maximum)."""
+    if temperature <= 0:
+        return int(np.argmax(np.asarray(logits, dtype=np.float64)))
+    return int(np.argmax(sample_scores(logits, temperature, position, slot, seed)))

@@ -1,0 +1,107 @@
+"""GPU parity of the sampling epilogue (mk_set_sampling): the sampled token of
+every step against the oracle's Gumbel-max draw on its own fp64 logits with
+the same (seed, position, slot) noise, teacher-forced. The token must match
+wherever the oracle's top two scores z_i = logit_i / T + g_i are more than
+SCORE_MARGIN apart (the logits may differ by the parity tolerance, scaled
+by 1/T), and must always be the argmax of the GPU's own logits plus the
+oracle's noise."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import sampling
+from decode_megakernel_llama_gb300 import _lib, synth
+from decode_megakernel_llama_gb300.build import build
+from decode_megakernel_llama_gb300.configs import LLAMA_1B, TINY
+
+from gpu_helpers import MAX_ABS, Pair, compare, oracle_config
+
+pytestmark = pytest.mark.gpu
+
+SEED = 0x5EED_0123_4567_89AB
+
+
+def check_sampled(gpu_logits, gpu_tok, orc_logits, T, pos, slot, where):
+    z = sampling.sample_scores(orc_logits, T, pos, slot, SEED)
+    top2 = np.sort(z)[-2:]
+    margin = 2 * MAX_ABS / T + 1e-3
+    if top2[1] - top2[0] > margin:
+        assert gpu_tok == int(np.argmax(z)), f"{where}: sampled {gpu_tok} != oracle {int(np.argmax(z))}"
+    # the GPU's token is the Gumbel-max of its own logits up to fp32 rounding
+    zg = sampling.sample_scores(gpu_logits, T, pos, slot, SEED)
+    assert zg[gpu_tok] >= zg.max() - 1e-3 * max(1.0, abs(zg.max())), where
+    return int(np.argmax(z))
+
+
+@pytest.mark.parametrize("T", [0.7, 1.5])
+def test_tiny_sampled_decode_matches_oracle(cuda_dev, T):
+    pair = Pair(TINY, 40)
+    pair.mk.set_sampling(T, SEED)
+    prompt = [int(t) for t in synth.prompt_tokens(TINY.vocab, 6)]
+    tok, differs = prompt[0], 0
+    for pos in range(20):
+        gl, gt = pair.gpu_step(tok, pos)
+        ol, ot_greedy = pair.orc.decode_step(tok, pos)
+        compare(gl, int(np.argmax(gl)), ol, ot_greedy, f"T {T} pos {pos}")  # logits parity as usual
+        ot = check_sampled(gl, gt, ol, T, pos, 0, f"T {T} pos {pos}")
+        differs += ot != ot_greedy
+        tok = prompt[pos + 1] if pos + 1 < len(prompt) else ot
+    assert differs > 0  # the draws are not the greedy tokens
+    # back to greedy
+    pair.mk.set_sampling(0.0)
+    gl, gt = pair.gpu_step(tok, 20)
+    assert gt == int(np.argmax(gl))
+    pair.close()
+
+
+def test_sampling_rejects_non_finite_temperature(cuda_dev):
+    pair = Pair(TINY, 8)
+    with pytest.raises(_lib.MKError):
+        pair.mk.set_sampling(float("nan"))
+    with pytest.raises(_lib.MKError):
+        pair.mk.set_sampling(float("inf"))
+    pair.close()
+
+
+def test_llama1b_sampled_steps(cuda_dev):
+    pair = Pair(LLAMA_1B, 8)
+    pair.mk.set_sampling(0.8, SEED)
+    prompt = [int(t) for t in synth.prompt_tokens(LLAMA_1B.vocab, 3)]
+    tok = prompt[0]
+    for pos in range(4):
+        gl, gt = pair.gpu_step(tok, pos)
+        ol, _ = pair.orc.decode_step(tok, pos)
+        ot = check_sampled(gl, gt, ol, 0.8, pos, 0, f"pos {pos}")
+        tok = prompt[pos + 1] if pos + 1 < len(prompt) else ot
+    pair.close()
+
+
+def test_tiny_batched_sampling_uses_each_sequence_slot(cuda_dev):
+    # the fused batched step draws sequence b's noise on slot b
+    build()
+    dev = torch.device("cuda:0")
+    B, T = 3, 0.9
+    w = synth.make_weights(TINY, dev, 0)
+    k, v = synth.kv_cache(TINY, 16, B, dev)
+    mk = _lib.Megakernel(TINY, w, k, v)
+    mk.set_sampling(T, SEED)
+    hw = synth.host_weights(w)
+    orcs = [oracle.OracleModel(oracle_config(TINY), hw, 16) for _ in range(B)]
+    toks = torch.tensor([5, 5, 5], dtype=torch.int32, device=dev)  # same token: only the slot differs
+    pos = torch.zeros(B, dtype=torch.int32, device=dev)
+    out = torch.zeros(B, dtype=torch.int32, device=dev)
+    logits = torch.empty(B, TINY.vocab, dtype=torch.float32, device=dev)
+    cur = [5, 5, 5]
+    for step in range(6):
+        toks.copy_(torch.tensor(cur, dtype=torch.int32))
+        pos.fill_(step)
+        mk.step_batch(toks, pos, out, logits)
+        torch.cuda.synchronize()
+        assert mk.status() == 0
+        gl = logits.double().cpu().numpy()
+        gt = out.cpu().numpy().tolist()
+        for b in range(B):
+            ol, _ = orcs[b].decode_step(cur[b], step)
+            cur[b] = check_sampled(gl[b], gt[b], ol, T, step, b, f"seq {b} step {step}")
+    mk.close()

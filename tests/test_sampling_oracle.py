@@ -1,0 +1,92 @@
+"""Pins of the oracle's sampling step (oracle/sampling.py) by properties:
+Philox4x32-10 is a bijection of the counter for a fixed key with avalanche in
+key and counter and uniform output; the Gumbel-max draw follows
+softmax(logits / T) and tends to the greedy token as T -> 0. The exact bit
+stream has no printed value to pin it to."""
+import numpy as np
+import pytest
+
+from oracle import sampling
+
+
+def test_philox_is_a_bijection_of_the_counter():
+    n = 1 << 16
+    c0 = np.arange(n)
+    out = sampling.philox4x32_10(c0, np.full(n, 7), np.full(n, 123456), np.full(n, 3), 0xDEADBEEF, 0x01234567)
+    assert len(np.unique(np.stack(out, axis=1), axis=0)) == n
+
+
+def _popcount(x: np.ndarray) -> np.ndarray:
+    x = x.astype(np.uint64)
+    c = np.zeros_like(x)
+    for _ in range(32):
+        c += x & np.uint64(1)
+        x >>= np.uint64(1)
+    return c
+
+
+@pytest.mark.parametrize("which", ["key", "counter"])
+def test_philox_flipping_one_input_bit_flips_half_the_output_bits(which):
+    rng = np.random.default_rng(5)
+    n = 4096
+    c = [rng.integers(0, 1 << 32, n, dtype=np.uint64) for _ in range(4)]
+    k0, k1 = 0x9A3B5C7D, 0x11223344
+    a = sampling.philox4x32_10(*c, k0, k1)
+    if which == "key":
+        b = sampling.philox4x32_10(*c, k0 ^ (1 << 13), k1)
+    else:
+        c2 = list(c)
+        c2[1] = c2[1] ^ np.uint64(1 << 20)
+        b = sampling.philox4x32_10(*c2, k0, k1)
+    flips = sum(_popcount(x ^ y) for x, y in zip(a, b))
+    assert abs(float(flips.mean()) - 64.0) < 1.0, flips.mean()
+
+
+def test_uniforms_are_uniform_in_the_open_interval():
+    u = sampling.uniforms(1 << 16, position=17, slot=2, seed=99)
+    assert u.min() > 0.0 and u.max() < 1.0
+    assert abs(u.mean() - 0.5) < 0.005
+    counts, _ = np.histogram(u, bins=64, range=(0.0, 1.0))
+    expected = len(u) / 64
+    chi2 = float(((counts - expected) ** 2 / expected).sum())
+    assert chi2 < 120.0, chi2  # 63 degrees of freedom: p < 1e-5 above ~115
+
+
+def test_noise_depends_on_position_slot_and_seed():
+    base = sampling.gumbel(64, 5, 0, 1)
+    assert not np.allclose(base, sampling.gumbel(64, 6, 0, 1))
+    assert not np.allclose(base, sampling.gumbel(64, 5, 1, 1))
+    assert not np.allclose(base, sampling.gumbel(64, 5, 0, 2))
+    assert not np.allclose(base, sampling.gumbel(64, 5, 0, 1 + (1 << 32)))
+    np.testing.assert_array_equal(base, sampling.gumbel(64, 5, 0, 1))
+
+
+@pytest.mark.parametrize("temperature", [1.0, 0.5, 2.0])
+def test_gumbel_max_draws_follow_the_softmax(temperature):
+    logits = np.array([0.0, 1.0, 2.0, -1.0, 0.5])
+    n = 20000
+    counts = np.zeros(len(logits))
+    for pos in range(n):  # independent noise per position
+        counts[sampling.sample_token(logits, temperature, pos, 3, 2024)] += 1
+    z = logits / temperature
+    p = np.exp(z - z.max())
+    p /= p.sum()
+    expected = n * p
+    chi2 = float(((counts - expected) ** 2 / expected).sum())
+    assert chi2 < 25.0, (chi2, counts, expected)  # 4 degrees of freedom: p < 1e-4 above ~23.5
+
+
+def test_small_temperature_is_greedy_and_nonpositive_is_greedy():
+    rng = np.random.default_rng(11)
+    for pos in range(50):
+        logits = rng.normal(size=300)
+        top = int(np.argmax(logits))
+        assert sampling.sample_token(logits, 0.0, pos, 0, 7) == top
+        assert sampling.sample_token(logits, -1.0, pos, 0, 7) == top
+        gap = np.sort(logits)[-1] - np.sort(logits)[-2]
+        if gap > 1e-3:
+            assert sampling.sample_token(logits, 1e-5, pos, 0, 7) == top
+
+
+def test_greedy_ties_go_to_the_lowest_index():
+    assert sampling.sample_token(np.array([1.0, 3.0, 3.0, 1.0]), 0.0, 0, 0, 0) == 1
