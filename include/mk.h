@@ -95,7 +95,11 @@ typedef struct mk_handle mk_handle;
 /* Plans the per-SM instruction queues for this model on the current device
  * (host scheduler), allocates the library's scratch (activations, attention
  * partials, dependency counters, queues, RoPE table) and uploads them.
- * Synchronous. On success *out receives the handle. */
+ * With max_batch > 1 and head_dim 64 it also plans the fused batched step
+ * and keeps, for it, an fp16 copy of every GEMV weight and of the LM head
+ * (2 bytes per weight, owned by the handle); if that does not fit, batches
+ * run sequence by sequence instead. Synchronous. On success *out receives
+ * the handle. */
 int mk_create(const mk_config *config, const mk_weights *weights, const mk_kv_cache *kv,
               mk_handle **out);
 
@@ -125,11 +129,17 @@ int mk_decode_step_host(mk_handle *h, const int32_t *host_token, int32_t positio
  * d_positions[b] (device int32 arrays, read when its step runs, so both can
  * be produced by the previous step on the device), attends over batch slot b
  * of the KV cache, appends its key/value row at its position, and writes its
- * greedy token to out_tokens[b] (device int32[batch]) and, if out_logits is
- * not NULL, its logits to out_logits[b*vocab .. ] (device float[batch][vocab]).
- * The sequences run one fused step after another on `stream` (one launch
- * each, in batch order); a device token or position out of range is reported
- * by mk_get_status (MK_ERR_INVALID_ARG) and that sequence's step does nothing. */
+ * greedy (or sampled, see mk_set_sampling) token to out_tokens[b] (device
+ * int32[batch]) and, if out_logits is not NULL, its logits to
+ * out_logits[b*vocab .. ] (device float[batch][vocab]).
+ * With batch == max_batch and the fused batched step planned (see
+ * mk_create), all sequences run in ONE launch that reads every weight tile
+ * once for all of them; its GEMVs take fp16 inputs, so its logits agree with
+ * the single-sequence step to the parity tolerance, not bit for bit.
+ * Otherwise the sequences run one fused step after another on `stream` (one
+ * launch each, in batch order). A device token or position out of range is
+ * reported by mk_get_status (MK_ERR_INVALID_ARG) and the step does nothing
+ * for that sequence (the fused launch: for the whole batch). */
 int mk_decode_step_batch(mk_handle *h, const int32_t *d_tokens, const int32_t *d_positions, int32_t batch,
                          float *out_logits, int32_t *out_tokens, void *stream);
 
