@@ -59,6 +59,18 @@ def algorithmic_bytes(shape, pos: int) -> int:
     return shape.step_weight_bytes() + shape.kv_read_bytes(pos + 1)
 
 
+def shape_desc(shape) -> str:
+    return (f"{shape.name} shape ({shape.n_layers} layers, d {shape.d_model}, {shape.n_heads} q / "
+            f"{shape.n_kv_heads} kv heads x {shape.head_dim}, SwiGLU {shape.ffn_dim}, vocab {shape.vocab} tied)")
+
+
+def l2_note(shape) -> str:
+    gb = shape.step_weight_bytes() / 1e9
+    if shape.step_weight_bytes() > 129e6:
+        return f"inputs larger than L2: {gb:.2f} GB of weights streamed every step"
+    return f"weights ({shape.step_weight_bytes() / 1e6:.1f} MB) fit in the 129 MB L2: a latency test, not a bandwidth one"
+
+
 def measured_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -197,7 +209,7 @@ def run_reference(args, ws, rank):
         "value": us, "unit": "us/token", "n_gpus": ws, "steps": K,
         "warmup": W, "ms_per_step": us / 1e3, "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"{wl.name}: Llama-1B shape, batch 1, greedy decode steps at "
+        "config": {"workload": f"{wl.name}: {shape_desc(shape)}, batch 1, greedy decode steps at "
                                f"positions {W}..{W + K - 1} (fp64 CPU oracle)"},
         "cpu_baseline": {"value": us, "unit": "us/token", "cores": thr, "kind": "oracle",
                          "sample": f"{K} timed oracle decode steps after {W} warm-up steps"},
@@ -307,11 +319,14 @@ def run_mk(args, ws, rank, local):
     shape = wl.shape
     K, W = args.steps, args.warmup
     P = wl.prompt_len
+    P0 = wl.prefill + P  # first decode position after the (pre-filled) context and the prompt
     if W < 3:
         raise SystemExit("--warmup must be >= 3")
-    max_seq = P + max(K, wl.decode_steps)
+    max_seq = P0 + max(K, wl.decode_steps)
     w = synth.make_weights(shape, dev, 0)
     kc, vc = synth.kv_cache(shape, max_seq, 1, dev)
+    if wl.prefill:
+        synth.prefill_cache(kc, vc, wl.prefill)
     mk = _lib.Megakernel(shape, w, kc, vc)
     prompt = synth.prompt_tokens(shape.vocab, P)
     stream = torch.cuda.current_stream(dev)
@@ -320,7 +335,7 @@ def run_mk(args, ws, rank, local):
 
     def run_prompt(step_fn):
         for i in range(P):
-            step_fn(int(prompt[i]), i)
+            step_fn(int(prompt[i]), wl.prefill + i)
 
     if args.profile:
         for s in range(W + K):
@@ -346,7 +361,7 @@ def run_mk(args, ws, rank, local):
         torch.cuda.synchronize()
         start.record(stream)
         for s in range(K):
-            mk.step_dev(tok, P + s, tok, None, stream)
+            mk.step_dev(tok, P0 + s, tok, None, stream)
         end.record(stream)
         torch.cuda.synchronize()
         return start.elapsed_time(end)  # ms
@@ -355,11 +370,11 @@ def run_mk(args, ws, rank, local):
         t_end = time.time() + 1.0
         while time.time() < t_end:      # load the GPU before the timed region
             for s in range(W):
-                mk.step_dev(tok, P + s, tok, None, stream)
+                mk.step_dev(tok, P0 + s, tok, None, stream)
             torch.cuda.synchronize()
         # W warm-up steps on the exact positions, then the timed K
         for s in range(W):
-            mk.step_dev(tok, P + s, tok, None, stream)
+            mk.step_dev(tok, P0 + s, tok, None, stream)
         ms = timed_decode()
     if mk.status() != 0:
         raise SystemExit("megakernel status error during timing")
@@ -376,13 +391,13 @@ def run_mk(args, ws, rank, local):
     h_out = torch.zeros(1, dtype=torch.int32).pin_memory()
     h_in[0] = int(prompt[-1])
     for s in range(W):
-        mk.step_host(h_in, P + s, h_out, None, stream)
+        mk.step_host(h_in, P0 + s, h_out, None, stream)
         h_in[0] = int(h_out[0])
     if ws > 1:
         dist.barrier()
     t0 = time.perf_counter()
     for s in range(K):
-        mk.step_host(h_in, P + s, h_out, None, stream)
+        mk.step_host(h_in, P0 + s, h_out, None, stream)
         h_in[0] = int(h_out[0])
     e2e_s = time.perf_counter() - t0
     e2e_val = 1e6 * e2e_s / K
@@ -394,7 +409,7 @@ def run_mk(args, ws, rank, local):
     # ---- the same decode loop with the sampling epilogue on (temperature 0.8)
     mk.set_sampling(0.8, 1234)
     for s in range(W):
-        mk.step_dev(tok, P + s, tok, None, stream)
+        mk.step_dev(tok, P0 + s, tok, None, stream)
     sampled_us = 1e3 * timed_decode() / K
     mk.set_sampling(0.0)
     if mk.status() != 0:
@@ -407,12 +422,12 @@ def run_mk(args, ws, rank, local):
     if not args.no_comparators:
         torch.cuda.synchronize()
         for s in range(W):
-            mk.step_unfused(int(prompt[-1]), P + s, tok, None, stream)
+            mk.step_unfused(int(prompt[-1]), P0 + s, tok, None, stream)
         torch.cuda.synchronize()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         for s in range(K):
-            mk.step_unfused(int(prompt[-1]), P + s, tok, None, stream)
+            mk.step_unfused(int(prompt[-1]), P0 + s, tok, None, stream)
         b.record(stream)
         torch.cuda.synchronize()
         unfused_us = 1e3 * a.elapsed_time(b) / K
@@ -422,10 +437,10 @@ def run_mk(args, ws, rank, local):
             cs = torch.cuda.Stream(dev)
             cs.wait_stream(stream)
             with torch.cuda.stream(cs):
-                mk.step_unfused(int(prompt[-1]), P, tok, None, cs)  # warm the capture stream
+                mk.step_unfused(int(prompt[-1]), P0, tok, None, cs)  # warm the capture stream
             torch.cuda.synchronize()
             with torch.cuda.graph(g, stream=cs):
-                mk.step_unfused(int(prompt[-1]), P, tok, None, cs)
+                mk.step_unfused(int(prompt[-1]), P0, tok, None, cs)
             for _ in range(W):
                 g.replay()
             torch.cuda.synchronize()
@@ -448,7 +463,7 @@ def run_mk(args, ws, rank, local):
     if args.trace:
         from decode_megakernel_llama_gb300 import trace as mktrace
         mk.set_trace(True)
-        mk.step_dev(tok, P + K // 2, tok, None, stream)  # a position in the middle of the timed range
+        mk.step_dev(tok, P0 + K // 2, tok, None, stream)  # a position in the middle of the timed range
         torch.cuda.synchronize()
         rec = mk.read_trace()
         mk.set_trace(False)
@@ -458,7 +473,7 @@ def run_mk(args, ws, rank, local):
         mktrace.to_chrome(rec, os.path.splitext(args.trace)[0] + ".chrome.json")
 
     # ---- roofline of the megakernel (the only kernel)
-    mean_bytes = sum(algorithmic_bytes(shape, P + s) for s in range(K)) / K
+    mean_bytes = sum(algorithmic_bytes(shape, P0 + s) for s in range(K)) / K
     achieved = mean_bytes / (us_per_tok_launch * 1e-6) / 1e9
     peak, peak_kind = measured_peak()
     roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
@@ -483,10 +498,10 @@ def run_mk(args, ws, rank, local):
             "value": value, "unit": "us/token", "n_gpus": ws, "steps": K, "warmup": W,
             "ms_per_step": t_max / K, "higher_is_better": False, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": f"{wl.name}: Llama-1B shape (16 layers, d 2048, 32 q / 8 kv heads "
-                                   f"x 64, SwiGLU 8192, vocab 128256 tied), batch 1, {P}-token prompt, "
-                                   f"timed decode positions {P}..{P + K - 1}",
-                       "l2": "inputs larger than L2: 2.47 GB of weights streamed every step",
+            "config": {"workload": f"{wl.name}: {shape_desc(shape)}, batch 1, "
+                                   + (f"KV cache pre-filled to {wl.prefill} positions, " if wl.prefill else "")
+                                   + f"{wl.prompt_len}-token prompt, timed decode positions {P0}..{P0 + K - 1}",
+                       "l2": l2_note(shape),
                        "parallelism": f"replicas x{ws}"},
             "tokens_per_s": 1e6 / value,
             "achieved_hbm_gbs": achieved,
