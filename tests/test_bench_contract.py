@@ -1,0 +1,53 @@
+"""Host-side checks of the benchmark: the roofline's algorithmic bytes equal
+the bytes of the tensors a step reads (counted from the generated weights,
+not from the formula), and the reference arm prints one JSON line with the
+contract's keys. CPU only."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+from decode_megakernel_llama_gb300 import synth  # noqa: E402
+from decode_megakernel_llama_gb300.configs import LLAMA_1B, TINY, ModelShape  # noqa: E402
+
+
+@pytest.mark.parametrize("shape", [TINY, ModelShape("odd", 3, 768, 12, 4, 64, 3072, 1000, 1e-5, 1e4)])
+def test_algorithmic_bytes_match_the_generated_tensors(shape):
+    w = synth.make_weights(shape, "cpu", 0)
+    tensors = [w["embed"], w["final_norm"]] + [t for lw in w["layers"] for t in lw.values()]
+    weight_bytes = sum(t.numel() * t.element_size() for t in tensors)
+    row = shape.d_model * 2  # the embedding row gathered for the token, besides the LM head's full read
+    for pos in (0, 5, 37):
+        kv = 2 * shape.n_layers * shape.n_kv_heads * (pos + 1) * shape.head_dim * 2  # K and V, bf16
+        assert bench.algorithmic_bytes(shape, pos) == weight_bytes + row + kv
+
+
+def test_llama1b_bytes_per_step():
+    # 1.2358 G bf16 weights (embedding counted for the LM head and once more
+    # for the gathered row) + 32 KB of keys/values per attended position
+    assert bench.algorithmic_bytes(LLAMA_1B, 0) == 2_471_632_896 + 32_768
+
+
+def test_reference_arm_prints_the_contract_line():
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload",
+                          "tiny", "--steps", "2", "--warmup", "1"], capture_output=True, text=True, timeout=600,
+                         cwd=ROOT)
+    assert out.returncode == 0, out.stderr[-2000:]
+    line = json.loads(out.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference"
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config"):
+        assert key in line, key
+    assert line["steps"] == 2 and line["warmup"] == 1 and line["higher_is_better"] is False
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == line["value"] and cb["sample"]
+    e2e = line["e2e"]
+    assert e2e["value"] == line["value"] and e2e["unit"] == line["unit"]
+    assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
+    assert "tiny shape" in line["config"]["workload"]
