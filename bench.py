@@ -54,6 +54,22 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(x: float, ws: int, device) -> float:
+    """The largest x over the ranks (the slowest replica sets the job's time)."""
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_us_per_token(t_max_s: float, k: int, ws: int) -> float:
+    """Whole-job time per token: ws replicas each decode k tokens in t_max_s."""
+    return 1e6 * t_max_s / (k * ws)
+
+
 def algorithmic_bytes(shape, pos: int) -> int:
     """Weights read by one step + keys/values attended over (positions 0..pos)."""
     return shape.step_weight_bytes() + shape.kv_read_bytes(pos + 1)
@@ -378,13 +394,9 @@ def run_mk(args, ws, rank, local):
         ms = timed_decode()
     if mk.status() != 0:
         raise SystemExit("megakernel status error during timing")
-    t_max = ms
-    if ws > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        t_max = float(t.item())
+    t_max = max_over_ranks(ms, ws, dev)
     us_per_tok_launch = 1e3 * ms / K                  # this rank's per-launch average
-    value = 1e3 * t_max / (K * ws)                     # aggregate us per token
+    value = aggregate_us_per_token(t_max * 1e-3, K, ws)  # aggregate us per token
 
     # ---- end to end: the public call with host buffers (token H2D, token D2H)
     h_in = torch.zeros(1, dtype=torch.int32).pin_memory()
@@ -400,11 +412,7 @@ def run_mk(args, ws, rank, local):
         mk.step_host(h_in, P0 + s, h_out, None, stream)
         h_in[0] = int(h_out[0])
     e2e_s = time.perf_counter() - t0
-    e2e_val = 1e6 * e2e_s / K
-    if ws > 1:
-        t = torch.tensor([e2e_s], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_val = 1e6 * float(t.item()) / (K * ws)
+    e2e_val = aggregate_us_per_token(max_over_ranks(e2e_s, ws, dev), K, ws)
 
     # ---- the same decode loop with the sampling epilogue on (temperature 0.8)
     mk.set_sampling(0.8, 1234)
