@@ -192,7 +192,9 @@ class Megakernel:
 
     def step_batch(self, d_tokens, d_positions, out_tokens, logits=None, stream=None) -> None:
         """d_tokens, d_positions, out_tokens: int32 CUDA tensors [B]; logits: float32 CUDA
-        tensor [B][vocab] or None. Sequence b uses batch slot b of the KV cache."""
+        tensor [B][vocab] or None. Sequence b uses batch slot b of the KV cache. With
+        B == max_batch (head dim 64) all sequences run in one fused launch that reads
+        every weight tile once (fp16 GEMV inputs); otherwise one launch per sequence."""
         check(load().mk_decode_step_batch(self.h, d_tokens.data_ptr(), d_positions.data_ptr(),
                                           int(d_tokens.numel()),
                                           logits.data_ptr() if logits is not None else None,
