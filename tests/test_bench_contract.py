@@ -51,3 +51,16 @@ def test_reference_arm_prints_the_contract_line():
     assert e2e["value"] == line["value"] and e2e["unit"] == line["unit"]
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
     assert "tiny shape" in line["config"]["workload"]
+
+
+def test_kernel_hash_covers_every_source_of_the_megakernel():
+    # the committed DRAM-traffic record is matched to the kernel by this hash,
+    # so every file that shapes the megakernel's code or plan must be in it
+    # (the allocation-free entry point's unit only moves its scratch)
+    from decode_megakernel_llama_gb300 import build as mkbuild
+    import inspect
+    src = inspect.getsource(bench.kernel_sha)
+    for f in mkbuild.DEPS:
+        if f in ("mk_noalloc.cu", "mk_internal.h"):
+            continue
+        assert f'"{f}"' in src, f
