@@ -38,8 +38,8 @@ def parse():
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--no-comparators", action="store_true",
                     help="skip the unfused-chain timings")
-    ap.add_argument("--cpu-seconds", type=float, default=12.0,
-                    help="budget of the oracle CPU-baseline sample")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="budget of each timed oracle CPU-baseline sample (all cores, one thread); 0 skips it")
     ap.add_argument("--profile", action="store_true",
                     help="only W warm-up and K decode steps (for ncu captures); prints one line")
     ap.add_argument("--trace", default=None,
@@ -172,31 +172,83 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def oracle_sample(shape, host_w, budget_s: float, threads: int | None = None):
-    """Times the oracle's decode step on a bounded sample; returns (us_per_token, n, threads)."""
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else platform)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def host_cores() -> int:
+    """Cores this process may run on (affinity), else the machine's count."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def oracle_model(shape, host_w, max_seq: int):
     import oracle
-    from decode_megakernel_llama_gb300 import synth
-    if threads:
-        oracle.set_threads(threads)
     cfg = oracle.OracleConfig(shape.n_layers, shape.d_model, shape.n_heads, shape.n_kv_heads,
                               shape.head_dim, shape.ffn_dim, shape.vocab, shape.rms_eps,
                               shape.rope_theta)
-    m = oracle.OracleModel(cfg, host_w, 64)
-    prompt = [int(t) for t in synth.prompt_tokens(shape.vocab, 64)]
-    n, t_total = 0, 0.0
-    while n < 64:
-        t0 = time.perf_counter()
-        m.decode_step(prompt[n], n)
-        t_total += time.perf_counter() - t0
-        n += 1
-        if t_total >= budget_s:
-            break
-    return 1e6 * t_total / n, n, oracle.get_threads()
+    return oracle.OracleModel(cfg, host_w, max_seq)
+
+
+def oracle_baseline(shape, host_w, prompt, P0: int, K: int, budget_all: float, budget_one: float):
+    """The oracle as it stands on the host cores, on the bench's own positions:
+    the prompt (positions 0..P0-1) untimed with all cores, then up to K decode
+    steps at positions P0.. timed with all cores (at most budget_all seconds),
+    then again from P0 with one thread (at most budget_one seconds)."""
+    import oracle
+    oracle.build()
+    cores = host_cores()
+    oracle.set_threads(cores)
+    m = oracle_model(shape, host_w, P0 + K)
+    tok = 0
+    for i in range(P0):
+        _, tok = m.decode_step(int(prompt[i]), i)
+
+    def timed(budget):
+        t, n, cur = 0.0, 0, tok
+        while n < K:
+            t0 = time.perf_counter()
+            _, cur = m.decode_step(cur, P0 + n)
+            t += time.perf_counter() - t0
+            n += 1
+            if t >= budget:
+                break
+        return 1e6 * t / n, n
+
+    us_all, n_all = timed(budget_all)
+    threads_all = oracle.get_threads()
+    oracle.set_threads(1)
+    us_one, n_one = timed(budget_one)
+    oracle.set_threads(cores)
+    return {"value": us_all, "unit": "us/token", "cores": threads_all, "kind": "oracle",
+            "sample": f"{n_all} fp64 oracle decode steps at positions {P0}..{P0 + n_all - 1} of the same "
+                      f"model after its {P0}-token prompt, {threads_all} OpenMP threads",
+            "single_thread": {"value": us_one, "unit": "us/token", "cores": 1,
+                              "sample": f"{n_one} steps at positions {P0}..{P0 + n_one - 1}, 1 thread"},
+            "cpu_model": cpu_model(), "affinity_cores": cores}
 
 
 def run_reference(args, ws, rank):
-    """The oracle as it stands, on the host cores: W untimed then K timed
-    decode steps (one token each) of the same workload shape."""
+    """The oracle as it stands, on the host cores, on the GPU arm's workload:
+    the prompt untimed, W warm-up steps, then K timed decode steps at the
+    same positions the GPU arm times (P0..P0+K-1)."""
     if rank != 0:
         return
     import oracle
@@ -206,18 +258,23 @@ def run_reference(args, ws, rank):
     wl = WORKLOADS[args.workload]
     shape = wl.shape
     K, W = args.steps, args.warmup
+    if wl.batch > 1 or wl.prefill:
+        raise SystemExit("--impl reference times the batch-1 workloads without pre-filled caches")
+    P0 = wl.prompt_len
     host_w = synth.host_weights(synth.make_weights(shape, "cpu", 0))
-    oracle.set_threads(os.cpu_count() or 1)
-    cfg = oracle.OracleConfig(shape.n_layers, shape.d_model, shape.n_heads, shape.n_kv_heads,
-                              shape.head_dim, shape.ffn_dim, shape.vocab, shape.rms_eps,
-                              shape.rope_theta)
-    m = oracle.OracleModel(cfg, host_w, K + W)
-    tok = int(synth.prompt_tokens(shape.vocab, 1)[0])
-    for pos in range(W):
-        _, tok = m.decode_step(tok, pos)
+    cores = host_cores()
+    oracle.set_threads(cores)
+    m = oracle_model(shape, host_w, P0 + max(K, W))
+    prompt = synth.prompt_tokens(shape.vocab, P0)
+    tok = 0
+    for i in range(P0):
+        _, tok = m.decode_step(int(prompt[i]), i)
+    tok = int(prompt[-1])
+    for s in range(W):
+        _, tok = m.decode_step(tok, P0 + s)
     t0 = time.perf_counter()
-    for pos in range(W, W + K):
-        _, tok = m.decode_step(tok, pos)
+    for s in range(K):
+        _, tok = m.decode_step(tok, P0 + s)
     us = 1e6 * (time.perf_counter() - t0) / K
     thr = oracle.get_threads()
     line = {
@@ -225,10 +282,12 @@ def run_reference(args, ws, rank):
         "value": us, "unit": "us/token", "n_gpus": ws, "steps": K,
         "warmup": W, "ms_per_step": us / 1e3, "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"{wl.name}: {shape_desc(shape)}, batch 1, greedy decode steps at "
-                               f"positions {W}..{W + K - 1} (fp64 CPU oracle)"},
+        "config": {"workload": f"{wl.name}: {shape_desc(shape)}, batch 1, {P0}-token prompt, "
+                               f"timed decode positions {P0}..{P0 + K - 1} (fp64 CPU oracle)"},
         "cpu_baseline": {"value": us, "unit": "us/token", "cores": thr, "kind": "oracle",
-                         "sample": f"{K} timed oracle decode steps after {W} warm-up steps"},
+                         "sample": f"the {P0}-token prompt untimed, {W} warm-up steps, then {K} timed "
+                                   f"decode steps at positions {P0}..{P0 + K - 1}",
+                         "cpu_model": cpu_model(), "affinity_cores": cores},
         "e2e": {"value": us, "unit": "us/token", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -491,14 +550,9 @@ def run_mk(args, ws, rank, local):
 
     # ---- oracle on the host cores (rank 0 at N=1 only)
     cpu = None
-    if rank == 0 and ws == 1:
-        import oracle
-        oracle.build()
-        host_w = synth.host_weights(w)
-        us, n, thr = oracle_sample(shape, host_w, args.cpu_seconds, os.cpu_count())
-        cpu = {"value": us, "unit": "us/token", "cores": thr, "kind": "oracle",
-               "sample": f"{n} oracle decode steps (positions 0..{n - 1}) of the same model, "
-                         f"{thr} OpenMP threads"}
+    if rank == 0 and ws == 1 and args.cpu_seconds > 0 and not wl.prefill:
+        cpu = oracle_baseline(shape, synth.host_weights(w), prompt, P0, K, args.cpu_seconds,
+                              args.cpu_seconds)
 
     if rank == 0:
         line = {

@@ -89,6 +89,7 @@ def load(path: str | None = None):
     L.mk_debug_read.argtypes = [_VP, ctypes.POINTER(ctypes.c_uint64)]
     L.mk_decode_step_noalloc.argtypes = [ctypes.POINTER(mk_config), ctypes.POINTER(mk_weights),
                                          ctypes.POINTER(mk_kv_cache), _I32, _I32, _VP, _VP, _VP]
+    L.mk_sampling_noise.argtypes = [_I32, _I32, _I32, ctypes.c_uint64, _VP, _VP, _VP, _VP]
     L.mk_destroy.argtypes = [_VP]
     L.mk_destroy.restype = None
     _lib = L
@@ -157,6 +158,16 @@ def decode_step_noalloc(shape, weights: dict, k_cache, v_cache, token: int, pos:
                                         int(token), int(pos),
                                         logits.data_ptr() if logits is not None else None,
                                         out_token.data_ptr(), _stream_ptr(stream)))
+
+
+def sampling_noise(n: int, position: int, slot: int, seed: int, out_words=None, out_noise=None,
+                   words=None, stream=None) -> None:
+    """mk_sampling_noise: the sampling epilogue's Philox words and Gumbel noise for
+    vocabulary entries 0..n-1 (int32/uint32 and float32 CUDA tensors [n]); with
+    `words` given, the noise of those words instead."""
+    ptr = lambda t: t.data_ptr() if t is not None else None
+    check(load().mk_sampling_noise(int(n), int(position), int(slot), int(seed) & ((1 << 64) - 1),
+                                   ptr(words), ptr(out_words), ptr(out_noise), _stream_ptr(stream)))
 
 
 class Megakernel:

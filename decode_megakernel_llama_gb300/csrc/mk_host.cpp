@@ -26,6 +26,8 @@ extern "C" cudaError_t mk_kernel_launch(const mk::Params *p, int n_sm, int coope
                                         cudaStream_t stream);
 extern "C" cudaError_t mk_kernel_occupancy(int *blocks_per_sm);
 extern "C" cudaError_t mk_convert_bf16_f16(const void *src, void *dst, size_t n, cudaStream_t stream);
+extern "C" cudaError_t mk_noise_launch(int n, int pos, int slot, uint64_t seed, const uint32_t *words,
+                                       uint32_t *out_words, float *out_noise, cudaStream_t stream);
 
 namespace {
 
@@ -922,6 +924,16 @@ int mk_set_sampling(mk_handle *h, float temperature, uint64_t seed) {
     if (temperature > 0.f && 1.0f / temperature > 1e30f) return fail(MK_ERR_INVALID_ARG, "temperature too small");
     h->inv_temp = temperature > 0.f ? 1.0f / temperature : 0.f;
     h->seed = seed;
+    return MK_OK;
+}
+
+int mk_sampling_noise(int32_t n, int32_t position, int32_t slot, uint64_t seed, const uint32_t *d_words,
+                      uint32_t *d_out_words, float *d_out_noise, void *stream) {
+    if (n < 0) return fail(MK_ERR_INVALID_ARG, "n must be >= 0");
+    if (!d_out_words && !d_out_noise) return fail(MK_ERR_INVALID_ARG, "no output buffer");
+    const cudaError_t e = mk_noise_launch(n, position, slot, seed, d_words, d_out_words, d_out_noise,
+                                          (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "noise kernel launch");
     return MK_OK;
 }
 

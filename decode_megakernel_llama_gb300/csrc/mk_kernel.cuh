@@ -204,7 +204,6 @@ __device__ __noinline__ bool chk_shared(const Params &p, const void *ptr, size_t
 #define CHKS(ptr, bytes, site) true
 #endif
 
-// Orderable key for the argmax: larger value wins, then lower index.
 // Philox4x32-10 (Salmon, Moraes, Dror, Shaw: "Parallel random numbers: as
 // easy as 1, 2, 3", SC'11): word 0 of the output block for counter (c0..c3)
 // and key (k0, k1). Ten rounds of two 32x32->64 multiplies by M0, M1 with
@@ -225,16 +224,23 @@ __device__ __forceinline__ uint32_t philox_w0(uint32_t c0, uint32_t c1, uint32_t
     return c0;
 }
 
-// Gumbel noise of vocabulary entry i for the sequence on KV slot `slot` at
-// position `pos`: u = (top 24 bits of Philox(i, pos, slot, 0; seed) + 1/2) / 2^24,
-// an open interval (0, 1); g = -log(-log(u)). argmax_i(z_i + g_i) is a draw
-// from softmax(z).
-__device__ __forceinline__ float gumbel_noise(uint32_t i, int pos, int slot, uint32_t seed_lo, uint32_t seed_hi) {
-    const uint32_t x = philox_w0(i, (uint32_t)pos, (uint32_t)slot, 0u, seed_lo, seed_hi);
-    const float u = ((float)(x >> 8) + 0.5f) * (1.0f / 16777216.0f);
+// Uniform in the open interval (0, 1) from one 32-bit word: the top 23 bits
+// plus 1/2, over 2^23. Every step is exact in fp32 (the largest value is
+// 1 - 2^-24), so -log(u) is never 0 and the noise below stays finite for
+// every word, the all-ones word included.
+__device__ __forceinline__ float gumbel_from_word(uint32_t x) {
+    const float u = ((float)(x >> 9) + 0.5f) * (1.0f / 8388608.0f);
     return -logf(-logf(u));
 }
 
+// Gumbel noise of vocabulary entry i for the sequence on KV slot `slot` at
+// position `pos`: g = -log(-log(u)), u from word 0 of Philox(i, pos, slot, 0;
+// seed). argmax_i(z_i + g_i) is a draw from softmax(z).
+__device__ __forceinline__ float gumbel_noise(uint32_t i, int pos, int slot, uint32_t seed_lo, uint32_t seed_hi) {
+    return gumbel_from_word(philox_w0(i, (uint32_t)pos, (uint32_t)slot, 0u, seed_lo, seed_hi));
+}
+
+// Orderable key for the argmax: larger value wins, then lower index.
 __device__ __forceinline__ unsigned long long argmax_key(float v, uint32_t idx) {
     uint32_t u = __float_as_uint(v);
     u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);

@@ -99,7 +99,12 @@ typedef struct mk_handle mk_handle;
  * and keeps, for it, an fp16 copy of every GEMV weight and of the LM head
  * (2 bytes per weight, owned by the handle); if that does not fit, batches
  * run sequence by sequence instead. Synchronous. On success *out receives
- * the handle. */
+ * the handle.
+ * Source: the article "Revolution der KI-Beschleunigung: Wie ein Low-Latency
+ * Megakernel den Llama-1B Turbo zündet" (dasgeld.co), paragraph on the
+ * internal infrastructure: a GPU interpreter runs
+ * instruction sequences that are planned once on the host, one per SM, and
+ * reused for many forward passes without recompiling. */
 int mk_create(const mk_config *config, const mk_weights *weights, const mk_kv_cache *kv,
               mk_handle **out);
 
@@ -107,20 +112,27 @@ int mk_create(const mk_config *config, const mk_weights *weights, const mk_kv_ca
  * the new key/value row at `position`, attends over 0..position, and writes
  * the greedy next token to out_token (device int32[1]) and, if out_logits is
  * not NULL, the fp32 logits to out_logits (device float[vocab]).
- * Exactly one kernel launch. */
+ * Exactly one kernel launch.
+ * Source: the same article, megakernel paragraphs (every step of the forward
+ * pass fused into one kernel, no launch or teardown between steps) and
+ * latency paragraph (one single-sequence forward pass in bf16). */
 int mk_decode_step(mk_handle *h, int32_t token_id, int32_t position, float *out_logits,
                    int32_t *out_token, void *stream);
 
 /* Same, with the token read from device memory (d_token_id, int32[1]) when
  * the step runs, so generation can chain out_token -> next step without a
- * host round trip. d_token_id may equal out_token. */
+ * host round trip. d_token_id may equal out_token.
+ * Source: as mk_decode_step (megakernel and latency paragraphs of the
+ * article); chaining the token on the device is this library's addition. */
 int mk_decode_step_dev(mk_handle *h, const int32_t *d_token_id, int32_t position,
                        float *out_logits, int32_t *out_token, void *stream);
 
 /* Same step through HOST buffers, for callers without device memory of their
  * own: copies *host_token to the device, runs the step, copies the greedy
  * token (and the logits if host_logits is not NULL) back, and waits for the
- * stream. host buffers should be pinned for asynchronous copies. */
+ * stream. host buffers should be pinned for asynchronous copies.
+ * Source: as mk_decode_step; the host-buffer form is this library's
+ * addition (the pages describe the device step only). */
 int mk_decode_step_host(mk_handle *h, const int32_t *host_token, int32_t position,
                         float *host_logits, int32_t *host_out_token, void *stream);
 
@@ -139,14 +151,21 @@ int mk_decode_step_host(mk_handle *h, const int32_t *host_token, int32_t positio
  * Otherwise the sequences run one fused step after another on `stream` (one
  * launch each, in batch order). A device token or position out of range is
  * reported by mk_get_status (MK_ERR_INVALID_ARG) and the step does nothing
- * for that sequence (the fused launch: for the whole batch). */
+ * for that sequence (the fused launch: for the whole batch).
+ * Source: the article's internal-infrastructure paragraph (the same planned
+ * sequences serve batch processing) and its megakernel paragraph on small
+ * batch sizes and single sequences. */
 int mk_decode_step_batch(mk_handle *h, const int32_t *d_tokens, const int32_t *d_positions, int32_t batch,
                          float *out_logits, int32_t *out_tokens, void *stream);
 
 /* The same step as a chain of separate kernel launches, one per stage
  * (QKV, attention, O-projection, gate/up, down per layer; LM head), with the
  * stream order between launches instead of in-kernel waits. Same results
- * bit for bit; exists to measure what fusing into one launch saves. */
+ * bit for bit; exists to measure what fusing into one launch saves.
+ * Source: the article's paragraphs on kernel launches and pipeline bubbles
+ * (the many-small-kernels baseline the megakernel replaces); the glossary
+ * entry "Megakernel" (synthszr.com), section on why the pauses between
+ * compute steps are expensive. */
 int mk_decode_step_unfused(mk_handle *h, int32_t token_id, int32_t position,
                            float *out_logits, int32_t *out_token, void *stream);
 
@@ -181,27 +200,55 @@ int mk_decode_step_noalloc(const mk_config *config, const mk_weights *weights,
 /* Device-side status of the last steps. Synchronises the handle's device,
  * returns MK_OK or MK_ERR_TIMEOUT (a bounded in-kernel wait expired; the step
  * that hit it produced undefined outputs) and resets it. After a timeout the
- * kernels refuse to run until this is called. */
+ * kernels refuse to run until this is called.
+ * Source: the article's synchronisation paragraph (dependencies resolved by
+ * counters in global memory inside the kernel); the pages say nothing about
+ * failures, so a bounded wait and this status word are the library's own
+ * failure mode for those in-kernel waits. */
 int mk_get_status(mk_handle *h);
 
 /* Bounded-wait limit for in-kernel dependency waits, in nanoseconds
- * (default 2e9). Host-only setting, takes effect on the next step. */
+ * (default 2e9). Host-only setting, takes effect on the next step.
+ * Source: as mk_get_status (the synchronisation paragraph's in-kernel
+ * waits); the limit itself is this library's convention. */
 int mk_set_wait_timeout(mk_handle *h, uint64_t timeout_ns);
 
 /* Sampling instead of greedy decoding for the following steps (all entry
  * points of this handle). temperature > 0: the returned token is a draw from
  * softmax(logits / temperature), taken as argmax_i(logit_i / temperature +
- * g_i) with Gumbel noise g_i = -log(-log(u_i)), u_i = (top 24 bits of word 0
+ * g_i) with Gumbel noise g_i = -log(-log(u_i)), u_i = (top 23 bits of word 0
  * of Philox4x32-10(counter {i, position, kv slot, 0}, key {seed low 32 bits,
- * seed high 32 bits}) + 1/2) / 2^24 — a counter-based draw, so a step is
- * reproducible from (seed, position, slot). temperature <= 0: greedy (the
- * default). out_logits stay the unscaled logits. Host-only setting;
- * MK_ERR_INVALID_ARG for a non-finite or vanishing temperature. */
+ * seed high 32 bits}) + 1/2) / 2^23, which lies strictly inside (0, 1) for
+ * every word — a counter-based draw, so a step is reproducible from (seed,
+ * position, slot). temperature <= 0: greedy (the default). out_logits stay
+ * the unscaled logits. Host-only setting; MK_ERR_INVALID_ARG for a
+ * non-finite or vanishing temperature.
+ * Source: the glossary entry "Megakernel" (synthszr.com), section on
+ * megakernels in chatbots (token-by-token generation); the pages define no
+ * sampler, so the draw follows two published definitions: the Gumbel-max
+ * rule (Gumbel 1954) and Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11). */
 int mk_set_sampling(mk_handle *h, float temperature, uint64_t seed);
+
+/* The sampling epilogue's random numbers on their own (no handle, no model):
+ * for i = 0..n-1, word x_i = word 0 of Philox4x32-10(counter {i, position,
+ * slot, 0}, key {seed low, seed high}) and noise g_i = -log(-log(u(x_i))),
+ * with u as in mk_set_sampling, computed by the same device functions the
+ * LM-head epilogue uses. If d_words (device uint32[n]) is not NULL, the
+ * noise is computed from those words instead of Philox (to check chosen
+ * words such as the all-ones word). Writes d_out_words (device uint32[n])
+ * and d_out_noise (device float[n]) when not NULL; at least one must be
+ * given. Asynchronous on `stream`; MK_ERR_INVALID_ARG for n < 0.
+ * Source: as mk_set_sampling; a diagnostic of this library. */
+int mk_sampling_noise(int32_t n, int32_t position, int32_t slot, uint64_t seed, const uint32_t *d_words,
+                      uint32_t *d_out_words, float *d_out_noise, void *stream);
+
 
 /* Optional per-instruction timing: when `enable` is non-zero, every step
  * records %globaltimer stamps per instruction into a device buffer that
- * mk_read_trace copies out (see mk_read_trace). */
+ * mk_read_trace copies out (see mk_read_trace).
+ * Source: the article's closing paragraph (synchronisation overhead and
+ * activation loading as the open costs): the trace measures exactly those
+ * waits per instruction. */
 int mk_set_trace(mk_handle *h, int32_t enable);
 
 /* Copies the trace of the last traced step to host_out: records of 8 int64
@@ -214,7 +261,8 @@ int mk_set_trace(mk_handle *h, int32_t enable);
  * step (mk_decode_step_batch), whichever ran last with tracing on. Returns
  * the number of records copied (or a negative status); cap = records that
  * fit in host_out. With host_out NULL, returns the number of records the
- * last traced step holds and copies nothing. */
+ * last traced step holds and copies nothing.
+ * Source: as mk_set_trace. */
 int mk_read_trace(mk_handle *h, int64_t *host_out, int32_t cap);
 
 /* Diagnostics of a library built with MK_CHECKED (every device-side global
@@ -222,11 +270,14 @@ int mk_read_trace(mk_handle *h, int64_t *host_out, int32_t cap);
  * first violation is recorded and the access skipped). Copies the record
  * {site, address, bytes, (block << 32) | thread} to host_out4 (site 0 = none)
  * after synchronising the device. Returns 1 for a checked build, 0 for a
- * normal build (whose record is always zero), or a negative status. */
+ * normal build (whose record is always zero), or a negative status.
+ * Source: none on the pages; a diagnostic of this library. */
 int mk_debug_read(mk_handle *h, uint64_t *host_out4);
 
 /* Number of streaming multiprocessors (persistent CTAs) the plan uses and
- * the number of instructions in the plan. */
+ * the number of instructions in the plan.
+ * Source: the article's internal-infrastructure paragraph (one instruction
+ * sequence per SM). */
 int mk_plan_size(const mk_handle *h, int32_t *n_sm, int32_t *n_instr);
 
 /* Host-only, no device needed: plans the queues for `config` on `n_sm` SMs
@@ -244,15 +295,22 @@ int mk_plan_size(const mk_handle *h, int32_t *n_sm, int32_t *n_instr);
  * a0/a1 = first row / row count (QKV rows of the stacked [Wq; Wk; Wv],
  * mat = 0); for ATTN a0 = kv head, a1 = split index. The wait/signal fields
  * describe the dependency DAG as counts (wait_ctr < 0: no wait); the kernel
- * itself waits on the tagged activation words those producers write.    */
+ * itself waits on the tagged activation words those producers write.
+ * Source: the article's internal-infrastructure paragraph (sequences planned
+ * on the host, one per SM) and synchronisation paragraph (counters that
+ * tell an instruction when its inputs are ready). */
 #define MK_INSTR_WORDS 16
 int mk_plan_inspect(const mk_config *config, int32_t n_sm, int32_t *out_instr, int32_t cap,
                     int32_t *out_queue_len, int32_t *out_n_counters);
 
-/* NULL-safe; waits for the device, then frees everything mk_create allocated. */
+/* NULL-safe; waits for the device, then frees everything mk_create allocated.
+ * Source: none; the pages are silent on resource lifetime, and this is the
+ * boundary's own convention (the counterpart of mk_create). */
 void mk_destroy(mk_handle *h);
 
-/* Thread-local text of the last error ("" if none). */
+/* Thread-local text of the last error ("" if none).
+ * Source: none; the pages are silent on error reporting, and this is the
+ * boundary's own convention. */
 const char *mk_last_error(void);
 
 #ifdef __cplusplus

@@ -18,11 +18,14 @@ definitions.
   softmax(z).
 
 The noise of vocabulary entry i for the sequence on KV slot s at position
-pos is u_i = (top 24 bits of output word 0 of Philox(counter (i, pos, s, 0),
-key (seed mod 2^32, seed div 2^32)) + 1/2) / 2^24, and the sampled token is
-argmax_i(logit_i / T + g_i), lowest index on ties. The Philox pins are
-properties (bijectivity for a fixed key, key sensitivity, uniformity); the
-sampler's are a T -> 0 limit (greedy) and the softmax law of the draws.
+pos is u_i = (top 23 bits of output word 0 of Philox(counter (i, pos, s, 0),
+key (seed mod 2^32, seed div 2^32)) + 1/2) / 2^23, which lies strictly
+inside (0, 1) for every word (at most 1 - 2^-24), and the sampled token is
+argmax_i(logit_i / T + g_i), lowest index on ties. Philox is pinned to the
+known-answer vectors published with the Random123 library (the SC'11
+authors' distribution) and by properties (bijectivity for a fixed key, key
+sensitivity, uniformity); the sampler by a T -> 0 limit (greedy) and the
+softmax law of the draws.
 """
 from __future__ import annotations
 
@@ -49,17 +52,30 @@ def philox4x32_10(c0, c1, c2, c3, k0: int, k1: int) -> tuple:
     return tuple(x.astype(np.uint32) for x in c)
 
 
+def words(n: int, position: int, slot: int, seed: int) -> np.ndarray:
+    """Output word 0 of Philox for counters (i, position, slot, 0), i = 0..n-1."""
+    i = np.arange(n, dtype=np.uint64)
+    return philox4x32_10(i, np.full(n, position), np.full(n, slot), np.zeros(n), seed & _MASK,
+                         (seed >> 32) & _MASK)[0]
+
+
+def uniform_from_word(w) -> np.ndarray:
+    """(top 23 bits of w + 1/2) / 2^23 as float64: in [2^-24, 1 - 2^-24]."""
+    w = np.asarray(w, dtype=np.uint32)
+    return ((w >> np.uint32(9)).astype(np.float64) + 0.5) / 8388608.0
+
+
+def gumbel_from_word(w) -> np.ndarray:
+    return -np.log(-np.log(uniform_from_word(w)))
+
+
 def uniforms(n: int, position: int, slot: int, seed: int) -> np.ndarray:
     """u_i in the open interval (0, 1), i = 0..n-1, as float64."""
-    i = np.arange(n, dtype=np.uint64)
-    w0 = philox4x32_10(i, np.full(n, position), np.full(n, slot), np.zeros(n), seed & _MASK,
-                       (seed >> 32) & _MASK)[0]
-    return ((w0 >> np.uint32(8)).astype(np.float64) + 0.5) / 16777216.0
+    return uniform_from_word(words(n, position, slot, seed))
 
 
 def gumbel(n: int, position: int, slot: int, seed: int) -> np.ndarray:
-    u = uniforms(n, position, slot, seed)
-    return -np.log(-np.log(u))
+    return gumbel_from_word(words(n, position, slot, seed))
 
 
 def sample_scores(logits: np.ndarray, temperature: float, position: int, slot: int, seed: int) -> np.ndarray:

@@ -1,6 +1,8 @@
 """GPU parity of the batched entry point (mk_decode_step_batch): each
 sequence of the batch against its own oracle twin, teacher-forced, with
 device-resident tokens and positions and one KV-cache slot per sequence."""
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -8,7 +10,7 @@ import torch
 import oracle
 from decode_megakernel_llama_gb300 import _lib, synth
 from decode_megakernel_llama_gb300.build import build
-from decode_megakernel_llama_gb300.configs import LLAMA_1B, TINY, ModelShape
+from decode_megakernel_llama_gb300.configs import LLAMA_1B, TINY, WORKLOADS, ModelShape
 
 from gpu_helpers import MARGIN, MAX_ABS, compare, oracle_config
 
@@ -16,15 +18,27 @@ pytestmark = pytest.mark.gpu
 
 
 class BatchPair:
-    def __init__(self, shape, max_seq: int, batch: int):
+    """The batched entry point on cuda:0 and one oracle per sequence. With
+    `prefill`, cache positions [0, prefill) of every slot hold seeded
+    bf16(N(0,1)) keys and values (the stand-in for prompts run in lockstep),
+    copied byte for byte into each sequence's oracle cache."""
+
+    def __init__(self, shape, max_seq: int, batch: int, prefill: int = 0, attn_splits: int = 0):
         build()
+        oracle.set_threads(os.cpu_count() or 1)
         dev = torch.device("cuda:0")
         self.shape, self.B = shape, batch
         self.w = synth.make_weights(shape, dev, 0)
         self.k, self.v = synth.kv_cache(shape, max_seq, batch, dev)
-        self.mk = _lib.Megakernel(shape, self.w, self.k, self.v)
+        if prefill:
+            synth.prefill_cache(self.k, self.v, prefill)
+        self.mk = _lib.Megakernel(shape, self.w, self.k, self.v, attn_splits=attn_splits)
         hw = synth.host_weights(self.w)
         self.orc = [oracle.OracleModel(oracle_config(shape), hw, max_seq) for _ in range(batch)]
+        if prefill:
+            for b in range(batch):
+                self.orc[b].k_cache[:] = synth.bf16_bits(self.k[:, b])
+                self.orc[b].v_cache[:] = synth.bf16_bits(self.v[:, b])
         self.tok_in = torch.zeros(batch, dtype=torch.int32, device=dev)
         self.pos_in = torch.zeros(batch, dtype=torch.int32, device=dev)
         self.tok_out = torch.zeros(batch, dtype=torch.int32, device=dev)
@@ -42,17 +56,22 @@ class BatchPair:
         self.mk.close()
 
 
-def run_lockstep(bp: BatchPair, prompts, n_decode: int, check_from: int = 0):
+def run_lockstep(bp: BatchPair, prompts, n_decode: int, check_from: int = 0, start_pos: int = 0):
+    """Teacher-forced lockstep: every sequence gets its prompt, then its own
+    oracle's greedy tokens; all sequences sit at the same position."""
     nxt = [None] * bp.B
     n = len(prompts[0])
+    worst = 0.0
     for i in range(n + n_decode):
         toks = [int(prompts[b][i]) if i < n else nxt[b] for b in range(bp.B)]
-        gl, gt = bp.step(toks, [i] * bp.B)
+        pos = start_pos + i
+        gl, gt = bp.step(toks, [pos] * bp.B)
         for b in range(bp.B):
-            ol, ot = bp.orc[b].decode_step(toks[b], i)
+            ol, ot = bp.orc[b].decode_step(toks[b], pos)
             if i >= check_from:
-                compare(gl[b], gt[b], ol, ot, f"seq {b} step {i}")
+                worst = max(worst, compare(gl[b], gt[b], ol, ot, f"seq {b} step {i} pos {pos}")[0])
             nxt[b] = ot
+    return worst
 
 
 def test_tiny_batch3_lockstep_teacher_forced(cuda_dev):
@@ -85,9 +104,10 @@ def test_tiny_batch_positions_differ_per_sequence(cuda_dev):
 def test_batched_step_matches_single_sequence_steps(cuda_dev):
     # the fused batched step (all sequences in one launch) against the same
     # sequences stepped one by one through the single-sequence call: the
-    # fused step feeds its GEMVs bf16 inputs, the single-sequence step fp32,
-    # so they agree to the parity tolerance, with the same greedy token
-    # wherever the top two logits are clearly apart
+    # fused step rounds its GEMV inputs for the tensor cores, the
+    # single-sequence step keeps them in fp32, so they agree to the parity
+    # tolerance, with the same greedy token wherever the top two logits are
+    # clearly apart
     a = BatchPair(TINY, 16, 2)
     singles = [BatchPair(TINY, 16, 1), BatchPair(TINY, 16, 1)]
     out = torch.zeros(1, dtype=torch.int32, device="cuda:0")
@@ -132,4 +152,32 @@ def test_wide_vocab_batch2_lm_head_ring(cuda_dev):
     bp = BatchPair(wide, 8, 2)
     prompts = [synth.prompt_tokens(wide.vocab, 3, seq=b) for b in range(2)]
     run_lockstep(bp, prompts, 2)
+    bp.close()
+
+
+def test_llama1b_batch8_workload_at_its_512_context(cuda_dev):
+    # The batch-8 workload as benchmarked: 8 sequences whose caches hold 512
+    # seeded positions, then all 64 decode steps in lockstep (positions
+    # 512..575). From position 513 on every (sequence, kv head) runs two KV
+    # splits of two or more 128-position tiles and merges them across SMs.
+    wl = WORKLOADS["llama1b_b8"]
+    P = wl.prompt_len
+    bp = BatchPair(LLAMA_1B, P + wl.decode_steps + 1, wl.batch, prefill=P)
+    instr, _, _ = _lib.plan_inspect(LLAMA_1B, 152, P + wl.decode_steps + 1, max_batch=wl.batch)
+    attn = instr[instr[:, 0] == 2]
+    assert attn[:, 3].max() == 1  # split index 1 exists: two splits per (sequence, kv head)
+    first = [[int(synth.prompt_tokens(LLAMA_1B.vocab, 1, seq=b)[0])] for b in range(wl.batch)]
+    worst = run_lockstep(bp, first, wl.decode_steps - 1, start_pos=P)
+    assert worst <= MAX_ABS
+    bp.close()
+
+
+def test_tiny_batch4_three_splits_and_a_ragged_tile(cuda_dev):
+    # 1100 cached positions: three KV splits of 367 positions each (tiles of
+    # 128, 128 and a ragged 111) per (sequence, kv head), merged across SMs
+    bp = BatchPair(TINY, 1200, 4, prefill=1100)
+    instr, _, _ = _lib.plan_inspect(TINY, 152, 1200, max_batch=4)
+    assert instr[instr[:, 0] == 2][:, 3].max() == 2
+    prompts = [synth.prompt_tokens(TINY.vocab, 2, seq=b) for b in range(4)]
+    run_lockstep(bp, prompts, 4, start_pos=1100)
     bp.close()

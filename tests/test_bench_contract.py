@@ -51,6 +51,18 @@ def test_reference_arm_prints_the_contract_line():
     assert e2e["value"] == line["value"] and e2e["unit"] == line["unit"]
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
     assert "tiny shape" in line["config"]["workload"]
+    # the same positions the GPU arm times: after the 8-token prompt
+    assert "timed decode positions 8..9" in line["config"]["workload"]
+    assert cb["cpu_model"] and cb["affinity_cores"] >= 1
+
+
+def test_cpu_baseline_reports_all_cores_and_one_thread():
+    w = synth.host_weights(synth.make_weights(TINY, "cpu", 0))
+    prompt = synth.prompt_tokens(TINY.vocab, 8)
+    cb = bench.oracle_baseline(TINY, w, prompt, 8, 3, 0.5, 0.5)
+    assert cb["kind"] == "oracle" and cb["value"] > 0 and cb["cores"] >= 1
+    assert cb["single_thread"]["cores"] == 1 and cb["single_thread"]["value"] > 0
+    assert "positions 8.." in cb["sample"] and cb["cpu_model"]
 
 
 def test_kernel_hash_covers_every_source_of_the_megakernel():

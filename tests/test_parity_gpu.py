@@ -83,28 +83,35 @@ def test_vocab_not_a_multiple_of_the_tile(cuda_dev):
 
 
 def test_llama1b_teacher_forced(cuda_dev):
+    # the whole workload: 128 prompt tokens and all 128 greedy decode steps
     wl = WORKLOADS["llama1b"]
     p = Pair(LLAMA_1B, wl.max_seq)
     prompt = synth.prompt_tokens(LLAMA_1B.vocab, wl.prompt_len)
-    stats = teacher_forced(p, prompt, 16, check_every=8)
+    stats = teacher_forced(p, prompt, wl.decode_steps, check_every=8)
     p.close()
+    assert len(stats) >= (wl.prompt_len + wl.decode_steps) // 8
     assert max(s[0] for s in stats) <= 5e-2
 
 
 def test_llama1b_long_context_prefilled_8192(cuda_dev):
+    # the whole workload: 8192 cached positions, then 64 decode steps
     wl = WORKLOADS["llama1b_ctx8192"]
     p = Pair(LLAMA_1B, wl.max_seq, prefill=wl.prefill)
-    prompt = synth.prompt_tokens(LLAMA_1B.vocab, 1)
-    teacher_forced(p, prompt, 7, start_pos=wl.prefill)
+    prompt = synth.prompt_tokens(LLAMA_1B.vocab, wl.prompt_len)
+    stats = teacher_forced(p, prompt, wl.decode_steps, start_pos=wl.prefill)
     p.close()
+    assert len(stats) == wl.prompt_len + wl.decode_steps
 
 
 def test_llama3b_teacher_forced(cuda_dev):
+    # the whole workload: 256 prompt tokens and all 128 greedy decode steps
+    # (head dim 128, three query heads per kv head)
     wl = WORKLOADS["llama3b"]
     p = Pair(LLAMA_3B, wl.max_seq)
-    prompt = synth.prompt_tokens(LLAMA_3B.vocab, 24)
-    teacher_forced(p, prompt, 8, check_every=4)
+    prompt = synth.prompt_tokens(LLAMA_3B.vocab, wl.prompt_len)
+    stats = teacher_forced(p, prompt, wl.decode_steps, check_every=16)
     p.close()
+    assert len(stats) >= (wl.prompt_len + wl.decode_steps) // 16
 
 
 def test_device_token_chaining_matches_host_token(tiny):

@@ -55,6 +55,32 @@ def test_tiny_sampled_decode_matches_oracle(cuda_dev, T):
     pair.close()
 
 
+@pytest.mark.parametrize("pos,slot,seed", [(0, 0, 0), (129, 3, SEED), (8191, 7, (1 << 64) - 1)])
+def test_kernel_philox_words_and_noise_match_the_oracle(cuda_dev, pos, slot, seed):
+    # the epilogue's random stream, bit for bit, and its noise to fp32 rounding
+    build()
+    n = 4096
+    words = torch.empty(n, dtype=torch.int32, device=cuda_dev)
+    noise = torch.empty(n, dtype=torch.float32, device=cuda_dev)
+    _lib.sampling_noise(n, pos, slot, seed, out_words=words, out_noise=noise)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(words.cpu().numpy().view(np.uint32), sampling.words(n, pos, slot, seed))
+    np.testing.assert_allclose(noise.double().cpu().numpy(), sampling.gumbel(n, pos, slot, seed),
+                               rtol=1e-5, atol=1e-5)
+
+
+def test_kernel_noise_is_finite_at_the_boundary_words(cuda_dev):
+    build()
+    w = np.array([0x00000000, 0x000001FF, 0xFFFFFE00, 0xFFFFFFFF], dtype=np.uint32)
+    words = torch.from_numpy(w.view(np.int32).copy()).to(cuda_dev)
+    noise = torch.empty(4, dtype=torch.float32, device=cuda_dev)
+    _lib.sampling_noise(4, 0, 0, 0, out_noise=noise, words=words)
+    torch.cuda.synchronize()
+    g = noise.double().cpu().numpy()
+    assert np.isfinite(g).all(), g
+    np.testing.assert_allclose(g, sampling.gumbel_from_word(w), rtol=1e-5, atol=1e-5)
+
+
 def test_sampling_rejects_non_finite_temperature(cuda_dev):
     pair = Pair(TINY, 8)
     with pytest.raises(_lib.MKError):

@@ -1,12 +1,50 @@
-"""Pins of the oracle's sampling step (oracle/sampling.py) by properties:
-Philox4x32-10 is a bijection of the counter for a fixed key with avalanche in
-key and counter and uniform output; the Gumbel-max draw follows
-softmax(logits / T) and tends to the greedy token as T -> 0. The exact bit
-stream has no printed value to pin it to."""
+"""Pins of the oracle's sampling step (oracle/sampling.py): Philox4x32-10
+against the known-answer vectors published with the Random123 library
+(tests/golden/philox4x32_10_kat.txt), and by properties (a bijection of the
+counter for a fixed key, avalanche in key and counter, uniform output); the
+word-to-uniform map stays strictly inside (0, 1) at both boundary words; the
+Gumbel-max draw follows softmax(logits / T) and tends to the greedy token as
+T -> 0."""
+import os
+
 import numpy as np
 import pytest
 
 from oracle import sampling
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "philox4x32_10_kat.txt")
+
+
+def kat_vectors():
+    rows = []
+    for line in open(GOLDEN):
+        line = line.split("#")[0].split()
+        if line:
+            rows.append([int(x, 16) for x in line])
+    return rows
+
+
+def test_philox_matches_the_published_known_answer_vectors():
+    rows = kat_vectors()
+    assert len(rows) == 3
+    for r in rows:
+        ctr, key, want = r[:4], r[4:6], r[6:10]
+        got = sampling.philox4x32_10(*[np.array([c], dtype=np.uint64) for c in ctr], key[0], key[1])
+        assert [int(g[0]) for g in got] == want, [hex(int(g[0])) for g in got]
+
+
+def test_word_to_uniform_stays_inside_the_open_interval_at_the_boundaries():
+    # the all-ones word was the failure case of a 24-bit mantissa recipe
+    # ((2^24 - 1) + 1/2 rounds to 2^24 in fp32): 23 bits keep every step exact
+    u = sampling.uniform_from_word(np.array([0x00000000, 0x000001FF, 0xFFFFFE00, 0xFFFFFFFF], dtype=np.uint32))
+    assert u[0] == 2.0 ** -24 and u[1] == 2.0 ** -24
+    assert u[2] == 1.0 - 2.0 ** -24 and u[3] == 1.0 - 2.0 ** -24
+    # the same values in fp32 arithmetic are exact, so a float kernel gets them too
+    top = np.float32(0xFFFFFFFF >> 9) + np.float32(0.5)
+    assert float(top * np.float32(1.0 / 8388608.0)) == 1.0 - 2.0 ** -24
+    g = sampling.gumbel_from_word(np.array([0, 0xFFFFFFFF], dtype=np.uint32))
+    assert np.isfinite(g).all()
+    assert g[0] < -2.8 and g[1] > 16.0  # -log(-log(2^-24)) and -log(2^-24 + ...)
 
 
 def test_philox_is_a_bijection_of_the_counter():

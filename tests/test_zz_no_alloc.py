@@ -34,14 +34,20 @@ def test_noalloc_step_matches_handle_step_twice(cuda_dev, shape, max_seq):
     t1 = torch.zeros(1, dtype=torch.int32, device=dev)
     t2 = torch.zeros(1, dtype=torch.int32, device=dev)
     tok = int(synth.prompt_tokens(shape.vocab, 1)[0])
+    free_delta = None
     for pos in range(2):   # two calls in a row reuse the resident plan
         mk.step(tok, pos, t1, l1)
+        torch.cuda.synchronize()
+        free0 = torch.cuda.mem_get_info()[0]
         _lib.decode_step_noalloc(shape, w, k2, v2, tok, pos, t2, l2)
         torch.cuda.synchronize()
+        if pos == 1:  # after the warm-up call (module load, plan upload) nothing is allocated
+            free_delta = free0 - torch.cuda.mem_get_info()[0]
         assert mk.status() == 0
         _close(l1, l2)
         assert int(t1.item()) == int(t2.item())
         tok = int(t1.item())
+    assert free_delta == 0, f"the allocation-free call changed free device memory by {free_delta} bytes"
     torch.testing.assert_close(k1, k2, rtol=0, atol=0)
     mk.close()
 
@@ -53,7 +59,7 @@ def test_noalloc_rejects_oversized_model(cuda_dev):
     w = synth.make_weights(big, dev, 0)
     k, v = synth.kv_cache(big, 1, 1, dev)
     out = torch.zeros(1, dtype=torch.int32, device=dev)
-    # a cache of 32768 positions needs a RoPE table and partials beyond 16 MiB
+    # a cache of 65536 positions needs a RoPE table beyond the 16 MiB array
     kbig = torch.empty((big.n_layers, 1, big.n_kv_heads, 65536, big.head_dim),
                        dtype=torch.bfloat16, device=dev)
     with pytest.raises(_lib.MKError) as e:
