@@ -89,6 +89,7 @@ def load(path: str | None = None):
     L.mk_debug_read.argtypes = [_VP, ctypes.POINTER(ctypes.c_uint64)]
     L.mk_decode_step_noalloc.argtypes = [ctypes.POINTER(mk_config), ctypes.POINTER(mk_weights),
                                          ctypes.POINTER(mk_kv_cache), _I32, _I32, _VP, _VP, _VP]
+    L.mk_set_sampling_filter.argtypes = [_VP, _I32, ctypes.c_float]
     L.mk_sampling_noise.argtypes = [_I32, _I32, _I32, ctypes.c_uint64, _VP, _VP, _VP, _VP]
     L.mk_destroy.argtypes = [_VP]
     L.mk_destroy.restype = None
@@ -234,6 +235,11 @@ class Megakernel:
         """temperature > 0: tokens are drawn from softmax(logits / temperature)
         (Gumbel-max with Philox noise keyed by seed); <= 0: greedy."""
         check(load().mk_set_sampling(self.h, float(temperature), int(seed) & ((1 << 64) - 1)))
+
+    def set_sampling_filter(self, top_k: int = 0, top_p: float = 1.0) -> None:
+        """Top-k / top-p filtering of the sampled draw (mk_set_sampling_filter);
+        top_k = 0 and top_p = 1 switch it off."""
+        check(load().mk_set_sampling_filter(self.h, int(top_k), float(top_p)))
 
     def set_trace(self, on: bool) -> None:
         check(load().mk_set_trace(self.h, 1 if on else 0))

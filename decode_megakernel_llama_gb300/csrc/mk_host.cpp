@@ -179,9 +179,14 @@ int build_plan(const mk_config *c, int n_sm, Plan &P, int nb) {
         // of 8 tiles, which must fit them
         if ((V + n_sm - 1) / n_sm * mk::kMaxBatch > mk::kBatchAcc && P.geo_lm.rt * 8 * mk::kMaxBatch > mk::kBatchAcc)
             return fail(MK_ERR_UNSUPPORTED, "no batched LM-head geometry for this model");
-    } else if (!make_geo(d, P.geo_qkv) || !make_geo(qd, P.geo_o) || !make_geo(d, P.geo_gu) ||
-               !make_geo(F, P.geo_down) || !make_geo(d, P.geo_lm)) {
-        return fail(MK_ERR_UNSUPPORTED, "no tile geometry for these input lengths");
+    } else {
+        // input floats per lane: 32 gives the fewest K-slices per row
+        int mnx = 32;
+        if (const char *env = getenv("MK_MAX_NX")) mnx = std::max(8, std::min(32, atoi(env)));
+        auto geo = [&](int K, Geo &g) { return make_geo(K, g, mnx) || make_geo(K, g, 32); };
+        if (!geo(d, P.geo_qkv) || !geo(qd, P.geo_o) || !geo(d, P.geo_gu) || !geo(F, P.geo_down) ||
+            !geo(d, P.geo_lm))
+            return fail(MK_ERR_UNSUPPORTED, "no tile geometry for these input lengths");
     }
     if (P.geo_gu.rt < 2 || P.geo_gu.rt % 2)
         return fail(MK_ERR_UNSUPPORTED, "gate/up tile needs an even row count");
@@ -481,6 +486,7 @@ int make_image(const mk_config *config, const mk_weights *w, int n_sm, Image &im
     im.o_att = b.take(8 * (size_t)L * nbv * Hq * hd);
     im.o_h = b.take(8 * (size_t)L * nbv * F);
     im.o_lm = b.take(sizeof(unsigned long long) * nb * P.n_lm);
+    im.o_cand = b.take(sizeof(unsigned long long) * mk::kMaxTopK * P.n_lm);
     im.o_tin = b.take(sizeof(int32_t) * nb);
     im.o_tout = b.take(sizeof(int32_t) * nb);
     im.o_logits = b.take(sizeof(float) * nb * V);
@@ -519,6 +525,9 @@ void fill_params(const Image &im, const mk_config *config, const mk_weights *w,
     p.hll = reinterpret_cast<uint2 *>(base + im.o_h);
     p.epoch = reinterpret_cast<uint32_t *>(base + im.o_epoch);
     p.lm_part = reinterpret_cast<unsigned long long *>(base + im.o_lm);
+    p.lm_cand = reinterpret_cast<unsigned long long *>(base + im.o_cand);
+    p.top_k = 0;
+    p.top_p = 1.f;
     p.ctr = reinterpret_cast<uint32_t *>(base + im.o_ctr);
     p.exit_ctr = reinterpret_cast<uint32_t *>(base + im.o_exit);
     p.status = reinterpret_cast<int32_t *>(base + im.o_status);
@@ -646,6 +655,8 @@ struct mk_handle {
     bool trace_batch = false;  // the last traced launch ran the batched image
     float inv_temp = 0.f;      // sampling (mk_set_sampling); 0: greedy
     uint64_t seed = 0;
+    int32_t top_k = 0;         // filtered draw (mk_set_sampling_filter); 0: off
+    float top_p = 1.f;
     // batched steps of all max_batch sequences in one launch (max_batch > 1 and
     // a model the batched instances support), with their own scratch
     bool has_batch = false;
@@ -676,6 +687,9 @@ int launch(mk_handle *h, int32_t token, const int32_t *d_token, int32_t position
     p.inv_temp = h->inv_temp;
     p.seed_lo = (uint32_t)(h->seed & 0xFFFFFFFFu);
     p.seed_hi = (uint32_t)(h->seed >> 32);
+    // a filter set with only top_p takes the nucleus among the kMaxTopK best
+    p.top_k = h->inv_temp > 0.f && (h->top_k > 0 || h->top_p < 1.f) ? (h->top_k > 0 ? h->top_k : mk::kMaxTopK) : 0;
+    p.top_p = h->top_p;
     if (h->trace_on) h->trace_batch = false;
     return mkint::launch_step(p, h->im.n_sm, h->im.n_stages, token, d_token, position, out_logits,
                               out_token, stream, unfused, d_pos, bslot);
@@ -836,7 +850,8 @@ int mk_decode_step_batch(mk_handle *h, const int32_t *d_tokens, const int32_t *d
     if (!d_tokens || !d_positions || !out_tokens)
         return fail(MK_ERR_INVALID_ARG, "d_tokens, d_positions and out_tokens must not be NULL");
     if (batch < 1 || batch > h->cfg.max_batch) return fail(MK_ERR_INVALID_ARG, "batch outside [1, max_batch]");
-    if (h->has_batch && batch == h->cfg.max_batch) {
+    const bool filtered = h->inv_temp > 0.f && (h->top_k > 0 || h->top_p < 1.f);
+    if (h->has_batch && batch == h->cfg.max_batch && !filtered) {
         // all sequences in one launch: every weight tile read once for all of them
         cudaError_t e = cudaSetDevice(h->device);
         if (e != cudaSuccess) return cuda_fail(e, "cudaSetDevice");
@@ -924,6 +939,19 @@ int mk_set_sampling(mk_handle *h, float temperature, uint64_t seed) {
     if (temperature > 0.f && 1.0f / temperature > 1e30f) return fail(MK_ERR_INVALID_ARG, "temperature too small");
     h->inv_temp = temperature > 0.f ? 1.0f / temperature : 0.f;
     h->seed = seed;
+    return MK_OK;
+}
+
+int mk_set_sampling_filter(mk_handle *h, int32_t top_k, float top_p) {
+    if (!h) return fail(MK_ERR_INVALID_ARG, "handle is NULL");
+    if (top_k < 0 || top_k > mk::kMaxTopK) return fail(MK_ERR_INVALID_ARG, "top_k outside [0, 64]");
+    if (!(top_p > 0.f && top_p <= 1.f)) return fail(MK_ERR_INVALID_ARG, "top_p outside (0, 1]");
+    // the last LM-head block gathers and sorts up to n_lm * kMaxTopK keys in
+    // its page ring, padded to a power of two: at most 16384 keys (128 KB)
+    if ((top_k > 0 || top_p < 1.f) && h->base.n_lm * mk::kMaxTopK > 16384)
+        return fail(MK_ERR_UNSUPPORTED, "too many LM-head blocks for the filtered draw");
+    h->top_k = top_k;
+    h->top_p = top_p;
     return MK_OK;
 }
 

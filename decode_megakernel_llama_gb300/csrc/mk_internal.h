@@ -22,7 +22,7 @@ struct Image {
     // byte offsets into the scratch region; [o_ctr, o_zero_end) starts at zero
     size_t o_ctr = 0, o_exit = 0, o_status = 0, o_abort = 0, o_dbg = 0, o_zero_end = 0;
     size_t o_epoch = 0, o_layers = 0, o_x = 0, o_qkv = 0, o_part = 0, o_att = 0, o_h = 0, o_lm = 0;
-    size_t o_tin = 0, o_tout = 0, o_logits = 0, o_rope = 0, o_instr = 0, o_qbeg = 0, o_ranges = 0;
+    size_t o_cand = 0, o_tin = 0, o_tout = 0, o_logits = 0, o_rope = 0, o_instr = 0, o_qbeg = 0, o_ranges = 0;
     std::vector<mk::Instr> flat;
     std::vector<int32_t> qbeg;
     std::vector<float> rope;

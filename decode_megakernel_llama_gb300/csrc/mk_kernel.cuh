@@ -317,6 +317,7 @@ struct Misc {
     uint32_t ep8;               // this step's epoch << 8
     int32_t staged_key;         // (op << 16 | layer) whose input xbuf holds, -1 none
     float staged_ss;            // its sum of squares
+    int32_t gcount;             // filtered draw: candidates gathered
     long long phase[3];         // trace: intra-instruction phase stamps
     long long tile_wait;        // trace: ns thread 0 spent waiting for tiles to land
 };
@@ -1078,6 +1079,158 @@ __device__ void gemv_instr(const Params &p, const Ctx &cx, const Instr &in, cons
     }
 }
 
+// ---------------------------------------------------------------------------
+// Filtered draw (top-k / top-p) in the LM-head epilogue.
+// ---------------------------------------------------------------------------
+// The logit and the vocabulary index held in an argmax key.
+__device__ __forceinline__ float key_value(unsigned long long k) {
+    uint32_t u = (uint32_t)(k >> 32);
+    u = (u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u;
+    return __uint_as_float(u);
+}
+__device__ __forceinline__ uint32_t key_index(unsigned long long k) { return 0xFFFFFFFFu - (uint32_t)k; }
+
+__device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const unsigned long long w = __shfl_xor_sync(0xFFFFFFFFu, v, o);
+        v = w > v ? w : v;
+    }
+    return v;
+}
+
+// Sorts keys[0, np) of shared memory into descending order (np a power of
+// two) with a bitonic network run by all consumer threads; ends with a
+// consumer barrier.
+__device__ void bitonic_desc(unsigned long long *keys, int np) {
+    const int tid = threadIdx.x;
+    for (int k = 2; k <= np; k <<= 1)
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            for (int i = tid; i < np; i += kConsumerThreads) {
+                const int l = i ^ j;
+                if (l > i) {
+                    const unsigned long long a = keys[i], b = keys[l];
+                    if ((i & k) == 0 ? a < b : a > b) {
+                        keys[i] = b;
+                        keys[l] = a;
+                    }
+                }
+            }
+            consumer_sync();
+        }
+}
+
+// LM-head epilogue of a filtered draw. Every LM-head instruction sorts the
+// keys (logit, then lowest index) of its rows and publishes its top_k best;
+// the last instruction to arrive gathers the keys no smaller than the
+// largest k-th key of any block (only those can be among the global top_k),
+// sorts them, and with warp 0 cuts the nucleus (the shortest prefix of the
+// top_k whose softmax mass at the temperature reaches top_p) and takes the
+// Gumbel-max among the kept candidates.
+__device__ void lm_filtered(const Params &p, const Ctx &cx, const Instr &in, const float *red, int sw) {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int n = in.a1, r0 = in.a0, K = p.top_k;
+    unsigned long long *keys = reinterpret_cast<unsigned long long *>(cx.xbuf);  // n <= 1024 keys (8 KB)
+    if (tid == 0) cx.misc->staged_key = -1;  // xbuf stops holding the staged input
+    int np = 2;
+    while (np < n || np < K) np <<= 1;
+    for (int i = tid; i < np; i += kConsumerThreads) {
+        unsigned long long k = 0ull;  // no real key is 0
+        if (i < n) {
+            float v = 0.f;
+            for (int s = 0; s < sw; ++s) v += red[i * sw + s];
+            if (p.out_logits && CHK(p.out_logits + r0 + i, 4, 18)) p.out_logits[r0 + i] = v;
+            k = argmax_key(v, (uint32_t)(r0 + i));
+        }
+        if (CHKS(keys + i, 8, 62)) keys[i] = k;
+    }
+    consumer_sync();
+    bitonic_desc(keys, np);
+    unsigned long long *mine = p.lm_cand + (size_t)in.slot * kMaxTopK;
+    for (int j = tid; j < K; j += kConsumerThreads)
+        if (CHK(mine + j, 8, 63)) mine[j] = keys[j];
+    consumer_sync();
+    if (tid == 0) {
+        __threadfence();
+        const uint32_t old = CHK(p.ctr + p.cl.lm_arrive, 4, 31) ? atom_acq_rel_add(p.ctr + p.cl.lm_arrive, 1u) : 0u;
+        const bool last = old == (uint32_t)p.n_lm - 1u;
+        if (last) __threadfence();
+        cx.misc->flag = last ? 1 : 0;
+        cx.misc->gcount = 0;
+    }
+    consumer_sync();
+    if (!cx.misc->flag) return;
+    // tau = the largest k-th key of any block
+    unsigned long long tau = 0ull;
+    for (int s = tid; s < p.n_lm; s += kConsumerThreads) {
+        const unsigned long long *q = p.lm_cand + (size_t)s * kMaxTopK + (K - 1);
+        const unsigned long long v = CHK(q, 8, 64) ? __ldcg(q) : 0ull;
+        tau = v > tau ? v : tau;
+    }
+    tau = warp_max_u64(tau);
+    if (lane == 0) cx.misc->best8[warp] = tau;
+    consumer_sync();
+    tau = 0ull;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) tau = cx.misc->best8[w] > tau ? cx.misc->best8[w] : tau;
+    // gather every key >= tau into the (now idle) page ring and sort them
+    unsigned long long *g = reinterpret_cast<unsigned long long *>(cx.pages);
+    const int total = p.n_lm * K;
+    for (int e = tid; e < total; e += kConsumerThreads) {
+        const unsigned long long *q = p.lm_cand + (size_t)(e / K) * kMaxTopK + e % K;
+        const unsigned long long v = CHK(q, 8, 64) ? __ldcg(q) : 0ull;
+        if (v != 0ull && v >= tau) {
+            const int at = atomicAdd(&cx.misc->gcount, 1);
+            if (CHKS(g + at, 8, 65)) g[at] = v;
+        }
+    }
+    consumer_sync();
+    const int ng = cx.misc->gcount;
+    int np2 = 2;
+    while (np2 < ng || np2 < K) np2 <<= 1;
+    for (int i = ng + tid; i < np2; i += kConsumerThreads)
+        if (CHKS(g + i, 8, 65)) g[i] = 0ull;
+    consumer_sync();
+    bitonic_desc(g, np2);
+    if (warp != 0) return;
+    // warp 0: candidate j = lane and j = lane + 32 (K <= 64), in key order
+    const int nc = ng < K ? ng : K;
+    const float zmax = key_value(g[0]);
+    const bool h0 = lane < nc, h1 = lane + 32 < nc;
+    const float z0 = h0 ? key_value(g[lane]) : 0.f, z1 = h1 ? key_value(g[lane + 32]) : 0.f;
+    const float e0 = h0 ? expf((z0 - zmax) * p.inv_temp) : 0.f, e1 = h1 ? expf((z1 - zmax) * p.inv_temp) : 0.f;
+    float c0 = e0, c1 = e1;  // inclusive prefix sums in candidate order
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float a = __shfl_up_sync(0xFFFFFFFFu, c0, o), b = __shfl_up_sync(0xFFFFFFFFu, c1, o);
+        if (lane >= o) {
+            c0 += a;
+            c1 += b;
+        }
+    }
+    c1 += __shfl_sync(0xFFFFFFFFu, c0, 31);
+    const float need = p.top_p * __shfl_sync(0xFFFFFFFFu, c1, 31);
+    int nkeep = nc;
+    if (p.top_p < 1.f) {
+        const uint32_t b0 = __ballot_sync(0xFFFFFFFFu, h0 && c0 >= need);
+        const uint32_t b1 = __ballot_sync(0xFFFFFFFFu, h1 && c1 >= need);
+        nkeep = b0 ? __ffs(b0) : (b1 ? 32 + __ffs(b1) : nc);
+    }
+    unsigned long long best = 0ull;
+    if (lane < nkeep) {
+        const uint32_t i = key_index(g[lane]);
+        best = argmax_key(z0 * p.inv_temp + gumbel_noise(i, p.pos, p.bslot, p.seed_lo, p.seed_hi), i);
+    }
+    if (lane + 32 < nkeep) {
+        const uint32_t i = key_index(g[lane + 32]);
+        const unsigned long long k1 =
+            argmax_key(z1 * p.inv_temp + gumbel_noise(i, p.pos, p.bslot, p.seed_lo, p.seed_hi), i);
+        best = k1 > best ? k1 : best;
+    }
+    best = warp_max_u64(best);
+    if (lane == 0 && CHK(p.out_token, 4, 21)) *p.out_token = (int32_t)key_index(best);
+}
+
 __device__ void do_gemv(const Params &p, const Ctx &cx, const Instr &in, uint32_t &t, bool &bad) {
     const Geo &g = geo_of(p, in.op);
     const int tid = threadIdx.x;
@@ -1128,6 +1281,10 @@ __device__ void do_gemv(const Params &p, const Ctx &cx, const Instr &in, uint32_
             break;
         }
         default: {  // OP_LMHEAD
+            if (p.top_k > 0 && p.inv_temp > 0.f) {
+                lm_filtered(p, cx, in, red, sw);
+                break;
+            }
             unsigned long long best = 0ull;
             for (int i = tid; i < n; i += kConsumerThreads) {
                 float v = 0.f;

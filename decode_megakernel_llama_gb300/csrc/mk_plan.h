@@ -36,6 +36,7 @@ constexpr int kMaxG = 8;                             // max query heads per kv h
 constexpr int kTraceWords = 8;                       // int64 per trace record
 constexpr int kMinSplitTiles = 4;                    // an attention split gets >= 4 KV tiles
 constexpr int kMergeBatch = 1;                       // splits read together by the merge
+constexpr int kMaxTopK = 64;                         // candidates kept per LM-head block (top-k / top-p)
 
 constexpr int kSmemPages = 0;
 constexpr int kSmemXbuf = kSmemPages + kPages * kPageBytes;
@@ -52,6 +53,7 @@ constexpr int kParamsSlot = 640;
 constexpr int kSmemBytes = kSmemParams + kParamsSlot;
 static_assert(kSmemXbuf + kBatchAcc * 4 <= kSmemResid, "batched accumulators overlap the residual rows");
 static_assert(kSmemBytes <= 232448, "shared memory of one CTA exceeds 227 KB");
+static_assert(16384 * 8 <= kPages * kPageBytes, "the filtered draw sorts up to 16384 keys in the page ring");
 
 // ---- opcodes ------------------------------------------------------------
 enum Op : int32_t {
@@ -148,6 +150,12 @@ struct Params {
     // with Gumbel noise g_i from Philox4x32-10 keyed by the seed; 0: greedy
     float inv_temp;
     uint32_t seed_lo, seed_hi;
+    // top-k / top-p filtering of the draw (inv_temp > 0 and top_k > 0): the
+    // top_k best logits, then the shortest prefix of them whose softmax mass
+    // reaches top_p; lm_cand holds each LM-head block's kMaxTopK best keys
+    int32_t top_k;
+    float top_p;
+    unsigned long long *lm_cand;  // [n_lm][kMaxTopK]
     unsigned long long timeout_ns;
     long long *trace;       // nullable: [n_sm][trace_cap][kTraceWords]
     int32_t trace_cap;

@@ -229,6 +229,28 @@ int mk_set_wait_timeout(mk_handle *h, uint64_t timeout_ns);
  * rule (Gumbel 1954) and Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11). */
 int mk_set_sampling(mk_handle *h, float temperature, uint64_t seed);
 
+/* Top-k / top-p filtering of the sampled draw for the following steps (all
+ * entry points of this handle; it applies while mk_set_sampling's
+ * temperature is > 0). The draw then chooses among a kept set only:
+ *   1. candidates: the top_k largest logits (ties: the lower vocabulary
+ *      index first); with top_k = 0 and top_p < 1, the MK_MAX_TOP_K largest;
+ *   2. within them, e_j = exp((logit_j - max logit) / temperature); the kept
+ *      set is the shortest prefix of the candidates whose sum of e_j reaches
+ *      top_p times the candidates' total (at least one candidate);
+ *   3. the token is argmax over the kept set of logit / temperature + g,
+ *      with the Gumbel noise g of mk_set_sampling.
+ * top_k = 0 and top_p = 1 (the default) switch filtering off. The sums run
+ * in fp32. With a filter on, mk_decode_step_batch steps its sequences one
+ * launch each. MK_ERR_INVALID_ARG for top_k outside [0, MK_MAX_TOP_K] or
+ * top_p outside (0, 1]; MK_ERR_UNSUPPORTED if the model's LM head has more
+ * than 256 blocks. Host-only setting, takes effect on the next step.
+ * Source: the glossary entry "Megakernel" (synthszr.com), section on
+ * megakernels in chatbots; the pages define no sampler, so the filter
+ * follows the nucleus sampling of Holtzman, Buys, Du, Forbes, Choi (ICLR
+ * 2020) with the customary top-k restriction before it. */
+#define MK_MAX_TOP_K 64
+int mk_set_sampling_filter(mk_handle *h, int32_t top_k, float top_p);
+
 /* The sampling epilogue's random numbers on their own (no handle, no model):
  * for i = 0..n-1, word x_i = word 0 of Philox4x32-10(counter {i, position,
  * slot, 0}, key {seed low, seed high}) and noise g_i = -log(-log(u(x_i))),

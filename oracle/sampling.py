@@ -90,3 +90,61 @@ def sample_token(logits: np.ndarray, temperature: float, position: int, slot: in
     if temperature <= 0:
         return int(np.argmax(np.asarray(logits, dtype=np.float64)))
     return int(np.argmax(sample_scores(logits, temperature, position, slot, seed)))
+
+
+# ---- top-k / top-p filtering ------------------------------------------------
+#
+# The filtered draw (the nucleus sampling of Holtzman, Buys, Du, Forbes,
+# Choi, "The Curious Case of Neural Text Degeneration", ICLR 2020, with the
+# usual top-k restriction before it):
+#   1. candidates: the k largest logits, ordered by value descending and,
+#      among equal values, by index ascending; k = top_k, or MAX_TOP_K when
+#      only top_p is set (the nucleus is taken among the MAX_TOP_K most likely
+#      tokens);
+#   2. within the candidates, e_j = exp((z_j - z_max) / T) and S = sum of e_j;
+#      keep the shortest prefix whose sum reaches top_p * S (at least one);
+#   3. draw argmax_j(z_j / T + g_j) over the kept prefix, g_j the Gumbel noise
+#      of vocabulary entry j as above (lowest index on ties).
+# top_k = 0 and top_p = 1 is the unfiltered temperature draw.
+
+MAX_TOP_K = 64
+
+
+def candidates(logits: np.ndarray, k: int) -> np.ndarray:
+    """Indices of the k largest logits, by value descending then index ascending."""
+    z = np.asarray(logits, dtype=np.float64)
+    order = np.lexsort((np.arange(z.shape[0]), -z))  # last key is primary: -z, then index
+    return order[:min(k, z.shape[0])]
+
+
+def kept_set(logits: np.ndarray, temperature: float, top_k: int, top_p: float) -> np.ndarray:
+    """The candidates a filtered draw chooses among, in candidate order."""
+    z = np.asarray(logits, dtype=np.float64)
+    if top_k <= 0 and top_p >= 1.0:
+        return candidates(z, z.shape[0])
+    k = top_k if top_k > 0 else MAX_TOP_K
+    c = candidates(z, k)
+    if top_p >= 1.0:
+        return c
+    e = np.exp((z[c] - z[c[0]]) / temperature)
+    need = top_p * e.sum()
+    acc, n = 0.0, 0
+    while n < len(c):
+        acc += e[n]
+        n += 1
+        if acc >= need:
+            break
+    return c[:n]
+
+
+def sample_token_filtered(logits: np.ndarray, temperature: float, position: int, slot: int, seed: int,
+                          top_k: int = 0, top_p: float = 1.0) -> int:
+    """The filtered draw; greedy for temperature <= 0."""
+    z = np.asarray(logits, dtype=np.float64)
+    if temperature <= 0:
+        return int(np.argmax(z))
+    keep = kept_set(z, temperature, top_k, top_p)
+    g = gumbel_from_word(words(z.shape[0], position, slot, seed))
+    s = z[keep] / temperature + g[keep]
+    best = np.flatnonzero(s == s.max())
+    return int(keep[best].min())

@@ -131,3 +131,96 @@ def test_tiny_batched_sampling_uses_each_sequence_slot(cuda_dev):
             ol, _ = orcs[b].decode_step(cur[b], step)
             cur[b] = check_sampled(gl[b], gt[b], ol, T, step, b, f"seq {b} step {step}")
     mk.close()
+
+
+def check_filtered(gpu_logits, gpu_tok, T, top_k, top_p, pos, slot, where):
+    """The GPU's filtered draw against the oracle's on the GPU's own logits.
+    The kept set is computed in fp64 here and in fp32 on the GPU, so a
+    nucleus whose cut falls within 1e-4 of top_p may differ by its last
+    member; the draw must then come from the larger set. Elsewhere the token
+    must be the oracle's, unless the two best noisy scores are within fp32
+    rounding of each other."""
+    hi = sampling.kept_set(gpu_logits, T, top_k, min(1.0, top_p + 1e-4))
+    lo = sampling.kept_set(gpu_logits, T, top_k, max(1e-6, top_p - 1e-4))
+    assert gpu_tok in set(hi.tolist()), f"{where}: token {gpu_tok} outside the kept set"
+    if len(hi) == len(lo):
+        want = sampling.sample_token_filtered(gpu_logits, T, pos, slot, SEED, top_k, top_p)
+        s = gpu_logits[hi] / T + sampling.gumbel(gpu_logits.shape[0], pos, slot, SEED)[hi]
+        top2 = np.sort(s)[-2:] if len(s) > 1 else np.array([-np.inf, s[0]])
+        if top2[1] - top2[0] > 1e-4 * max(1.0, abs(top2[1])):
+            assert gpu_tok == want, f"{where}: filtered draw {gpu_tok} != oracle {want}"
+    return len(hi)
+
+
+@pytest.mark.parametrize("top_k,top_p", [(1, 1.0), (5, 1.0), (64, 1.0), (0, 0.5), (40, 0.9), (0, 0.05)])
+def test_tiny_filtered_draws_match_the_oracle(cuda_dev, top_k, top_p):
+    T = 0.9
+    pair = Pair(TINY, 40)
+    pair.mk.set_sampling(T, SEED)
+    pair.mk.set_sampling_filter(top_k, top_p)
+    prompt = [int(t) for t in synth.prompt_tokens(TINY.vocab, 4)]
+    tok, sizes = prompt[0], []
+    for pos in range(16):
+        gl, gt = pair.gpu_step(tok, pos)
+        ol, ot_greedy = pair.orc.decode_step(tok, pos)
+        compare(gl, int(np.argmax(gl)), ol, ot_greedy, f"pos {pos}")  # logits parity as usual
+        sizes.append(check_filtered(gl, gt, T, top_k, top_p, pos, 0, f"k {top_k} p {top_p} pos {pos}"))
+        if top_k == 1:
+            assert gt == int(np.argmax(gl))
+        tok = prompt[pos + 1] if pos + 1 < len(prompt) else gt
+    if top_k > 0 and top_p >= 1.0:
+        assert set(sizes) == {top_k}
+    pair.mk.set_sampling_filter(0, 1.0)  # filter off again: the plain draw
+    gl, gt = pair.gpu_step(tok, 16)
+    check_sampled(gl, gt, pair.orc.decode_step(tok, 16)[0], T, 16, 0, "unfiltered")
+    pair.close()
+
+
+def test_llama1b_filtered_draws_match_the_oracle(cuda_dev):
+    # 152 LM-head blocks of 844 rows each: the candidate merge at full size
+    T = 0.7
+    pair = Pair(LLAMA_1B, 8)
+    pair.mk.set_sampling(T, SEED)
+    prompt = [int(t) for t in synth.prompt_tokens(LLAMA_1B.vocab, 3)]
+    tok = prompt[0]
+    for pos, (k, p) in enumerate([(50, 0.9), (0, 0.3), (8, 1.0), (64, 0.99)]):
+        pair.mk.set_sampling_filter(k, p)
+        gl, gt = pair.gpu_step(tok, pos)
+        check_filtered(gl, gt, T, k, p, pos, 0, f"k {k} p {p} pos {pos}")
+        tok = prompt[pos + 1] if pos + 1 < len(prompt) else gt
+    pair.close()
+
+
+def test_filtered_batch_steps_run_per_sequence(cuda_dev):
+    build()
+    dev = torch.device("cuda:0")
+    B, T = 3, 0.8
+    w = synth.make_weights(TINY, dev, 0)
+    k, v = synth.kv_cache(TINY, 16, B, dev)
+    mk = _lib.Megakernel(TINY, w, k, v)
+    mk.set_sampling(T, SEED)
+    mk.set_sampling_filter(10, 0.8)
+    toks = torch.tensor([5, 6, 7], dtype=torch.int32, device=dev)
+    pos = torch.zeros(B, dtype=torch.int32, device=dev)
+    out = torch.zeros(B, dtype=torch.int32, device=dev)
+    logits = torch.empty(B, TINY.vocab, dtype=torch.float32, device=dev)
+    for step in range(4):
+        pos.fill_(step)
+        mk.step_batch(toks, pos, out, logits)
+        torch.cuda.synchronize()
+        assert mk.status() == 0
+        gl = logits.double().cpu().numpy()
+        gt = out.cpu().numpy().tolist()
+        for b in range(B):
+            check_filtered(gl[b], gt[b], T, 10, 0.8, step, b, f"seq {b} step {step}")
+        toks.copy_(out)
+    mk.close()
+
+
+def test_filter_arguments_are_checked(cuda_dev):
+    pair = Pair(TINY, 8)
+    for k, p in [(-1, 1.0), (65, 1.0), (5, 0.0), (5, 1.5), (5, float("nan"))]:
+        with pytest.raises(_lib.MKError) as e:
+            pair.mk.set_sampling_filter(k, p)
+        assert e.value.code == _lib.MK_ERR_INVALID_ARG
+    pair.close()

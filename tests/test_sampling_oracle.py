@@ -128,3 +128,76 @@ def test_small_temperature_is_greedy_and_nonpositive_is_greedy():
 
 def test_greedy_ties_go_to_the_lowest_index():
     assert sampling.sample_token(np.array([1.0, 3.0, 3.0, 1.0]), 0.0, 0, 0, 0) == 1
+
+
+# ---- top-k / top-p (oracle/sampling.py: candidates, kept_set, sample_token_filtered)
+
+def test_top_k_1_is_greedy_at_any_temperature():
+    rng = np.random.default_rng(21)
+    for pos in range(40):
+        z = rng.normal(size=500)
+        z[rng.integers(0, 500)] = z.max()  # a tie at the top: the lower index wins
+        top = int(np.argmax(z))
+        for T in (0.3, 1.0, 4.0):
+            assert sampling.sample_token_filtered(z, T, pos, 1, 99, top_k=1) == top
+
+
+def test_no_filter_and_a_full_top_k_equal_the_plain_draw():
+    rng = np.random.default_rng(22)
+    for pos in range(40):
+        z = rng.normal(size=64) * 3
+        plain = sampling.sample_token(z, 0.9, pos, 2, 5)
+        assert sampling.sample_token_filtered(z, 0.9, pos, 2, 5) == plain
+        assert sampling.sample_token_filtered(z, 0.9, pos, 2, 5, top_k=64) == plain
+        assert sampling.sample_token_filtered(z, 0.9, pos, 2, 5, top_k=64, top_p=1.0) == plain
+
+
+def test_candidates_break_ties_by_the_lower_index():
+    z = np.array([1.0, 5.0, 3.0, 5.0, 3.0, 3.0, 0.0])
+    assert sampling.candidates(z, 4).tolist() == [1, 3, 2, 4]
+    assert sampling.kept_set(z, 1.0, 3, 1.0).tolist() == [1, 3, 2]
+
+
+@pytest.mark.parametrize("p", [0.05, 0.3, 0.5, 0.9, 0.999])
+def test_nucleus_is_the_smallest_set_reaching_the_mass(p):
+    # brute force over every subset of a small vocabulary: the kept set has
+    # the fewest members of any subset whose mass reaches p (a prefix of the
+    # sorted order attains that minimum), and it is a prefix of the order
+    import itertools
+    rng = np.random.default_rng(int(p * 1000))
+    for _ in range(20):
+        z = rng.normal(size=8) * 2
+        T = float(rng.uniform(0.5, 2.0))
+        e = np.exp((z - z.max()) / T)
+        prob = e / e.sum()
+        keep = sampling.kept_set(z, T, 0, p)
+        best = min(len(s) for r in range(1, 9) for s in itertools.combinations(range(8), r)
+                   if prob[list(s)].sum() >= p - 1e-12)
+        assert len(keep) == best
+        assert prob[keep].sum() >= p - 1e-12
+        assert prob[keep[:-1]].sum() < p  # minimal: without its last member it falls short
+        assert keep.tolist() == sampling.candidates(z, len(keep)).tolist()
+
+
+def test_top_p_acts_within_the_capped_candidates():
+    # 1000 equal logits: the nucleus of mass 0.9 would need 900 tokens, the
+    # cap keeps it to the MAX_TOP_K lowest indices
+    z = np.zeros(1000)
+    keep = sampling.kept_set(z, 1.0, 0, 0.9)
+    assert keep.tolist() == list(range(int(np.ceil(0.9 * sampling.MAX_TOP_K))))
+
+
+@pytest.mark.parametrize("top_k,top_p", [(3, 1.0), (0, 0.6), (4, 0.8)])
+def test_filtered_draws_follow_the_renormalised_softmax(top_k, top_p):
+    z = np.array([0.0, 1.0, 2.0, -1.0, 0.5, 1.5])
+    T = 0.8
+    keep = sampling.kept_set(z, T, top_k, top_p)
+    n = 20000
+    counts = np.zeros(len(z))
+    for pos in range(n):
+        counts[sampling.sample_token_filtered(z, T, pos, 0, 77, top_k, top_p)] += 1
+    assert counts[np.setdiff1d(np.arange(len(z)), keep)].sum() == 0
+    e = np.exp(z[keep] / T)
+    expected = n * e / e.sum()
+    chi2 = float(((counts[keep] - expected) ** 2 / expected).sum())
+    assert chi2 < 25.0, (chi2, counts, expected)  # <= 5 degrees of freedom: p < 1e-4 above ~20.5
