@@ -88,3 +88,44 @@ def host_weights(w: dict) -> dict:
         "final_norm": bf16_bits(w["final_norm"]),
         "layers": [{k: bf16_bits(v) for k, v in lw.items()} for lw in w["layers"]],
     }
+
+
+W2_MATS = ("wq", "wk", "wv", "wo", "w_gate", "w_up", "w_down")
+W2_BETAS = ("beta_q", "beta_k", "beta_v", "beta_o", "beta_gate", "beta_up", "beta_down")
+
+
+def make_ternary_weights(s: ModelShape, device="cpu", seed: int = 0) -> dict:
+    """A ternary-weight model of shape `s` (the W2A8 variant): embedding and
+    norm gains drawn as in make_weights (bf16), every projection matrix a
+    uniform draw from {-1, 0, +1} (int8) with one scale per matrix drawn
+    uniformly from [0.02, 0.03] and rounded to a bf16 value (so beta * Wq is
+    exact in bf16), which gives the matrices about the spread of the bf16
+    model's N(0, 0.02) weights. Recipe order: embed, then per layer
+    attn_norm, the seven matrices and their scales in W2_MATS order,
+    mlp_norm; then final_norm."""
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    shapes = layer_shapes(s)
+    w = {"embed": _normal((s.vocab, s.d_model), 0.02, 0.0, gen, device), "layers": []}
+    for _ in range(s.n_layers):
+        lw = {"attn_norm": _normal(shapes["attn_norm"], 0.05, 1.0, gen, device)}
+        for m, b in zip(W2_MATS, W2_BETAS):
+            lw[m] = (torch.randint(0, 3, shapes[m], generator=gen, device=device, dtype=torch.int32) - 1).to(torch.int8)
+            u = torch.rand((1,), generator=gen, device=device, dtype=torch.float32)
+            lw[b] = float((0.02 + 0.01 * u).to(torch.bfloat16).float().item())
+        lw["mlp_norm"] = _normal(shapes["mlp_norm"], 0.05, 1.0, gen, device)
+        w["layers"].append(lw)
+    w["final_norm"] = _normal((s.d_model,), 0.05, 1.0, gen, device)
+    return w
+
+
+def host_ternary_weights(w: dict) -> dict:
+    """The ternary model on the host: bf16 bits, int8 codes, float scales."""
+    out = {"embed": bf16_bits(w["embed"]), "final_norm": bf16_bits(w["final_norm"]), "layers": []}
+    for lw in w["layers"]:
+        h = {k: bf16_bits(lw[k]) for k in ("attn_norm", "mlp_norm")}
+        for m, b in zip(W2_MATS, W2_BETAS):
+            h[m] = lw[m].detach().contiguous().cpu().numpy()
+            h[b] = lw[b]
+        out["layers"].append(h)
+    return out

@@ -66,6 +66,20 @@ class _Weights(ctypes.Structure):
     _fields_ = [("embed", _P16), ("final_norm", _P16), ("layers", ctypes.POINTER(_Layer))]
 
 
+_P8 = ctypes.POINTER(ctypes.c_int8)
+
+
+class _LayerW2(ctypes.Structure):
+    _fields_ = ([("attn_norm", _P16), ("mlp_norm", _P16)]
+                + [(n, _P8) for n in ("wq", "wk", "wv", "wo", "w_gate", "w_up", "w_down")]
+                + [(n, ctypes.c_float) for n in ("beta_q", "beta_k", "beta_v", "beta_o", "beta_gate",
+                                                 "beta_up", "beta_down")])
+
+
+class _WeightsW2(ctypes.Structure):
+    _fields_ = [("embed", _P16), ("final_norm", _P16), ("layers", ctypes.POINTER(_LayerW2))]
+
+
 class _KV(ctypes.Structure):
     _fields_ = [("k", _P16), ("v", _P16), ("layer_stride", ctypes.c_int64),
                 ("max_seq", ctypes.c_int32)]
@@ -96,6 +110,13 @@ def lib():
         L.orc_full_forward.argtypes = [ctypes.POINTER(_Config), ctypes.POINTER(_Weights),
                                        ctypes.POINTER(ctypes.c_int), ctypes.c_int, _PD]
         L.orc_full_forward.restype = ctypes.c_int
+        L.orc_w2a8_quantize.argtypes = [_PD, ctypes.c_int, ctypes.POINTER(ctypes.c_int8)]
+        L.orc_w2a8_quantize.restype = ctypes.c_float
+        L.orc_matvec_w2a8.argtypes = [ctypes.POINTER(ctypes.c_int8), ctypes.c_float, ctypes.c_int64,
+                                      ctypes.c_int64, _PD, _PD]
+        L.orc_decode_step_w2a8.argtypes = [ctypes.POINTER(_Config), ctypes.POINTER(_WeightsW2),
+                                           ctypes.POINTER(_KV), ctypes.c_int, ctypes.c_int, _PD]
+        L.orc_decode_step_w2a8.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -269,3 +290,80 @@ class OracleModel:
         if tok < 0:
             raise ValueError("orc_full_forward rejected its arguments")
         return logits, int(tok)
+
+
+# ---- W2A8 projections (ternary weights, 8-bit activations) -------------------
+
+W2_MATS = ("wq", "wk", "wv", "wo", "w_gate", "w_up", "w_down")
+W2_BETAS = ("beta_q", "beta_k", "beta_v", "beta_o", "beta_gate", "beta_up", "beta_down")
+
+
+def _i8(a: np.ndarray) -> np.ndarray:
+    a = np.ascontiguousarray(a)
+    if a.dtype != np.int8:
+        raise TypeError(f"expected int8 ternary codes, got {a.dtype}")
+    return a
+
+
+def w2a8_quantize(x) -> tuple[np.ndarray, float]:
+    """Per-token absmax 8-bit codes of x and the scale s (fp32 arithmetic)."""
+    x = _f64(x)
+    q = np.empty(x.size, dtype=np.int8)
+    s = lib().orc_w2a8_quantize(_pd(x), x.size, q.ctypes.data_as(_P8))
+    return q, float(s)
+
+
+def matvec_w2a8(Wq: np.ndarray, beta: float, x) -> np.ndarray:
+    """y = beta / s * Wq x_q (Wq int8 ternary [rows][cols])."""
+    Wq = _i8(Wq)
+    x = _f64(x)
+    rows, cols = Wq.shape
+    y = np.empty(rows, dtype=np.float64)
+    lib().orc_matvec_w2a8(Wq.ctypes.data_as(_P8), float(beta), rows, cols, _pd(x), _pd(y))
+    return y
+
+
+class OracleModelW2A8(OracleModel):
+    """OracleModel whose projections are W2A8. `weights`: "embed" and
+    "final_norm" bf16 bits; "layers" dicts with bf16 "attn_norm",
+    "mlp_norm", int8 ternary matrices W2_MATS and float scales W2_BETAS."""
+
+    def __init__(self, cfg: OracleConfig, weights: dict, max_seq: int):
+        self.cfg = cfg
+        self.max_seq = int(max_seq)
+        self._keep = []
+        self._ww = _WeightsW2()
+        emb, fn = _u16(weights["embed"]), _u16(weights["final_norm"])
+        self._keep += [emb, fn]
+        self._ww.embed, self._ww.final_norm = _p16(emb), _p16(fn)
+        layers = (_LayerW2 * cfg.n_layers)()
+        for i, lw in enumerate(weights["layers"]):
+            for k in ("attn_norm", "mlp_norm"):
+                a = _u16(lw[k])
+                self._keep.append(a)
+                setattr(layers[i], k, _p16(a))
+            for k in W2_MATS:
+                a = _i8(lw[k])
+                self._keep.append(a)
+                setattr(layers[i], k, a.ctypes.data_as(_P8))
+            for k in W2_BETAS:
+                setattr(layers[i], k, float(lw[k]))
+        self._layers = layers
+        self._ww.layers = ctypes.cast(layers, ctypes.POINTER(_LayerW2))
+        self._c = _Config(cfg.n_layers, cfg.d_model, cfg.n_heads, cfg.n_kv_heads, cfg.head_dim,
+                          cfg.ffn_dim, cfg.vocab, cfg.rms_eps, cfg.rope_theta)
+        shape = (cfg.n_layers, cfg.n_kv_heads, self.max_seq, cfg.head_dim)
+        self.k_cache = np.zeros(shape, dtype=np.uint16)
+        self.v_cache = np.zeros(shape, dtype=np.uint16)
+
+    def decode_step(self, token: int, pos: int):
+        logits = np.empty(self.cfg.vocab, dtype=np.float64)
+        kv = self._kv()
+        tok = lib().orc_decode_step_w2a8(ctypes.byref(self._c), ctypes.byref(self._ww), ctypes.byref(kv),
+                                         int(token), int(pos), _pd(logits))
+        if tok < 0:
+            raise ValueError("orc_decode_step_w2a8 rejected its arguments")
+        return logits, int(tok)
+
+    def full_forward(self, tokens):
+        raise NotImplementedError("the W2A8 oracle steps incrementally only")

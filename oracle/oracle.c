@@ -286,3 +286,89 @@ int orc_full_forward(const orc_config *c, const orc_weights *w, const int *token
     free(o); free(t);
     return tok;
 }
+
+/* ---- W2A8 projections (see oracle.h) ----------------------------------- */
+
+float orc_w2a8_quantize(const double *x, int n, int8_t *codes) {
+    float amax = 0.0f;
+    for (int i = 0; i < n; ++i) {
+        const float a = fabsf((float)x[i]);
+        if (a > amax) amax = a;
+    }
+    const float s = 127.0f / (amax > 1e-5f ? amax : 1e-5f);
+    for (int i = 0; i < n; ++i) {
+        const float v = rintf((float)x[i] * s);
+        codes[i] = (int8_t)(v < -128.0f ? -128.0f : (v > 127.0f ? 127.0f : v));
+    }
+    return s;
+}
+
+void orc_matvec_w2a8(const int8_t *Wq, float beta, int64_t rows, int64_t cols, const double *x, double *y) {
+    int8_t *q = (int8_t *)malloc((size_t)cols);
+    const float s = orc_w2a8_quantize(x, (int)cols, q);
+    const double f = (double)beta / (double)s;
+#pragma omp parallel for schedule(static) num_threads(orc_get_threads())
+    for (int64_t r = 0; r < rows; ++r) {
+        int64_t acc = 0;
+        for (int64_t c = 0; c < cols; ++c) acc += (int64_t)Wq[r * cols + c] * (int64_t)q[c];
+        y[r] = f * (double)acc;
+    }
+    free(q);
+}
+
+int orc_decode_step_w2a8(const orc_config *c, const orc_weights_w2 *w, const orc_kv *kv, int token,
+                         int pos, double *logits) {
+    if (!valid_config(c) || !w || !kv || !logits) return -1;
+    if (token < 0 || token >= c->vocab || pos < 0 || pos >= kv->max_seq) return -1;
+    const int d = c->d_model, H = c->n_heads, Hkv = c->n_kv_heads, hd = c->head_dim;
+    const int F = c->ffn_dim, G = H / Hkv, S = kv->max_seq;
+
+    double *x = (double *)malloc(sizeof(double) * (size_t)d);
+    double *xh = (double *)malloc(sizeof(double) * (size_t)d);
+    double *q = (double *)malloc(sizeof(double) * (size_t)H * hd);
+    double *k = (double *)malloc(sizeof(double) * (size_t)Hkv * hd);
+    double *v = (double *)malloc(sizeof(double) * (size_t)Hkv * hd);
+    double *o = (double *)malloc(sizeof(double) * (size_t)H * hd);
+    double *t = (double *)malloc(sizeof(double) * (size_t)d);
+    double *gt = (double *)malloc(sizeof(double) * (size_t)F);
+    double *up = (double *)malloc(sizeof(double) * (size_t)F);
+
+    for (int i = 0; i < d; ++i) x[i] = orc_bf16_to_f64(w->embed[(int64_t)token * d + i]);
+
+    for (int l = 0; l < c->n_layers; ++l) {
+        const orc_layer_w2 *L = &w->layers[l];
+        uint16_t *Kl = kv->k + (int64_t)l * kv->layer_stride;
+        uint16_t *Vl = kv->v + (int64_t)l * kv->layer_stride;
+
+        orc_rmsnorm(x, L->attn_norm, d, c->rms_eps, xh);
+        orc_matvec_w2a8(L->wq, L->beta_q, (int64_t)H * hd, d, xh, q);
+        orc_matvec_w2a8(L->wk, L->beta_k, (int64_t)Hkv * hd, d, xh, k);
+        orc_matvec_w2a8(L->wv, L->beta_v, (int64_t)Hkv * hd, d, xh, v);
+        for (int h = 0; h < H; ++h) orc_rope(q + (int64_t)h * hd, hd, pos, c->rope_theta);
+        for (int h = 0; h < Hkv; ++h) orc_rope(k + (int64_t)h * hd, hd, pos, c->rope_theta);
+        for (int h = 0; h < Hkv; ++h)
+            for (int i = 0; i < hd; ++i) {
+                int64_t off = ((int64_t)h * S + pos) * hd + i;
+                Kl[off] = orc_f64_to_bf16(k[(int64_t)h * hd + i]);
+                Vl[off] = orc_f64_to_bf16(v[(int64_t)h * hd + i]);
+            }
+        for (int h = 0; h < H; ++h) {
+            int kvh = h / G;
+            orc_attend(q + (int64_t)h * hd, Kl + (int64_t)kvh * S * hd, Vl + (int64_t)kvh * S * hd,
+                       pos + 1, hd, o + (int64_t)h * hd);
+        }
+        orc_matvec_w2a8(L->wo, L->beta_o, d, (int64_t)H * hd, o, t);
+        for (int i = 0; i < d; ++i) x[i] += t[i];
+
+        orc_rmsnorm(x, L->mlp_norm, d, c->rms_eps, xh);
+        orc_matvec_w2a8(L->w_gate, L->beta_gate, F, d, xh, gt);
+        orc_matvec_w2a8(L->w_up, L->beta_up, F, d, xh, up);
+        for (int i = 0; i < F; ++i) gt[i] = orc_silu(gt[i]) * up[i];
+        orc_matvec_w2a8(L->w_down, L->beta_down, d, F, gt, t);
+        for (int i = 0; i < d; ++i) x[i] += t[i];
+    }
+    const orc_weights head = {w->embed, w->final_norm, NULL};  /* the LM head stays bf16 */
+    int tok = lm_head(c, &head, x, logits);
+    free(x); free(xh); free(q); free(k); free(v); free(o); free(t); free(gt); free(up);
+    return tok;
+}

@@ -113,6 +113,47 @@ int orc_decode_step(const orc_config *cfg, const orc_weights *w, const orc_kv *k
 int orc_full_forward(const orc_config *cfg, const orc_weights *w, const int *tokens, int n,
                      double *logits);
 
+/* ---- W2A8 projections -------------------------------------------------
+ * Ternary weights and 8-bit activations, as the page "BitNet 1.58bit GPU
+ * Inference Kernel: Revolutionäre Effizienz für KI-Modelle mit
+ * W2A8-Quantisierung" (dasgeld.co) describes its GEMV: 2-bit weights, 8-bit
+ * activations, an integer dot product (dp4a). The page gives no formulas;
+ * the plainest reading is BitNet b1.58's (Ma et al., 2024): a weight matrix
+ * is beta * Wq with Wq in {-1, 0, +1} and one fp32 scale beta per matrix; an
+ * input vector x is quantised per token by its absolute maximum,
+ *     s = 127 / max(max_i |x_i|, 1e-5),   x_q[i] = clamp(rint(x_i * s), -128, 127),
+ * in fp32 arithmetic (x first rounded to fp32: the decision is taken in the
+ * kernel's precision), and
+ *     y[r] = (beta / s) * sum_c Wq[r][c] * x_q[c]   (exact integer sum).  */
+
+/* Activation codes of x[n]; returns the scale s. */
+float orc_w2a8_quantize(const double *x, int n, int8_t *codes);
+
+/* y[r] = beta / s * sum_c Wq[r][c] x_q[c] for Wq int8 row-major [rows][cols]. */
+void orc_matvec_w2a8(const int8_t *Wq, float beta, int64_t rows, int64_t cols, const double *x, double *y);
+
+/* A layer whose seven projections are W2A8 (norm gains stay bf16). */
+typedef struct {
+    const uint16_t *attn_norm, *mlp_norm;
+    const int8_t *wq, *wk, *wv, *wo, *w_gate, *w_up, *w_down;
+    float beta_q, beta_k, beta_v, beta_o, beta_gate, beta_up, beta_down;
+} orc_layer_w2;
+
+/* embed (bf16, also the tied LM head, which stays bf16) and final_norm as in
+ * orc_weights; layers: [n_layers] W2A8 layers. */
+typedef struct {
+    const uint16_t *embed;
+    const uint16_t *final_norm;
+    const orc_layer_w2 *layers;
+} orc_weights_w2;
+
+/* orc_decode_step with every projection of every layer W2A8: the same step
+ * with orc_matvec_w2a8 in place of orc_matvec for Wq, Wk, Wv, Wo, Wg, Wu,
+ * Wd (each quantising its own input vector). Returns the greedy token, -1 on
+ * bad arguments. */
+int orc_decode_step_w2a8(const orc_config *cfg, const orc_weights_w2 *w, const orc_kv *kv, int token,
+                         int pos, double *logits);
+
 #ifdef __cplusplus
 }
 #endif
