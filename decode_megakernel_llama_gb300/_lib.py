@@ -91,6 +91,9 @@ def load(path: str | None = None):
                                          ctypes.POINTER(mk_kv_cache), _I32, _I32, _VP, _VP, _VP]
     L.mk_set_sampling_filter.argtypes = [_VP, _I32, ctypes.c_float]
     L.mk_sampling_noise.argtypes = [_I32, _I32, _I32, ctypes.c_uint64, _VP, _VP, _VP, _VP]
+    L.mk_w2_pack.argtypes = [_VP, ctypes.c_int64, ctypes.c_int64, _VP]
+    L.mk_w2_unpack.argtypes = [_VP, ctypes.c_int64, ctypes.c_int64, _VP]
+    L.mk_w2a8_gemv.argtypes = [_VP, ctypes.c_float, _I32, _I32, _VP, _VP, _VP]
     L.mk_destroy.argtypes = [_VP]
     L.mk_destroy.restype = None
     _lib = L
@@ -169,6 +172,34 @@ def sampling_noise(n: int, position: int, slot: int, seed: int, out_words=None, 
     ptr = lambda t: t.data_ptr() if t is not None else None
     check(load().mk_sampling_noise(int(n), int(position), int(slot), int(seed) & ((1 << 64) - 1),
                                    ptr(words), ptr(out_words), ptr(out_noise), _stream_ptr(stream)))
+
+
+def w2_pack(q):
+    """Host: ternary int8 codes [rows][cols] (numpy) -> packed uint32 [rows][cols / 16]
+    in the library's W2 layout (mk_w2_pack)."""
+    import numpy as np
+    q = np.ascontiguousarray(q, dtype=np.int8)
+    rows, cols = q.shape
+    out = np.empty((rows, cols // 16), dtype=np.uint32)
+    check(load().mk_w2_pack(q.ctypes.data, rows, cols, out.ctypes.data))
+    return out
+
+
+def w2_unpack(packed, cols: int):
+    """Host: the inverse of w2_pack (mk_w2_unpack)."""
+    import numpy as np
+    packed = np.ascontiguousarray(packed, dtype=np.uint32)
+    rows = packed.shape[0]
+    out = np.empty((rows, cols), dtype=np.int8)
+    check(load().mk_w2_unpack(packed.ctypes.data, rows, cols, out.ctypes.data))
+    return out
+
+
+def w2a8_gemv(packed, beta: float, rows: int, cols: int, x, y, stream=None) -> None:
+    """mk_w2a8_gemv on CUDA tensors: packed (uint32/int32 [rows][cols/16]),
+    x float32 [cols], y float32 [rows]."""
+    check(load().mk_w2a8_gemv(packed.data_ptr(), float(beta), int(rows), int(cols), x.data_ptr(),
+                              y.data_ptr(), _stream_ptr(stream)))
 
 
 class Megakernel:

@@ -265,6 +265,37 @@ int mk_sampling_noise(int32_t n, int32_t position, int32_t slot, uint64_t seed, 
                       uint32_t *d_out_words, float *d_out_noise, void *stream);
 
 
+/* ---- W2A8 GEMV: ternary weights, 8-bit activations ----------------------
+ * The GEMV of the page "BitNet 1.58bit GPU Inference Kernel: Revolutionäre
+ * Effizienz für KI-Modelle mit W2A8-Quantisierung" (dasgeld.co): 2-bit
+ * weights and 8-bit activations, sixteen 2-bit values interleaved in each
+ * 32-bit word, int8 dot products with dp4a. A weight matrix is
+ * beta * Wq with Wq in {-1, 0, +1} [rows][cols] and one fp32 scale beta; the
+ * input x is quantised per token, s = 127 / max(max|x|, 1e-5),
+ * x_q = clamp(rint(x * s), -128, 127) in fp32, and
+ * y[r] = beta / s * sum_c Wq[r][c] x_q[c] (exact integer sum, one fp32 scale).
+ *
+ * Packed layout (MK_W2 layout): row-major, cols / 16 uint32 words per row;
+ * word w holds elements 16w .. 16w+15, element 16w + 4j + i (i, j in 0..3)
+ * in bits [8i + 2j, 8i + 2j + 2) as the code Wq + 1 (code 3 is invalid). */
+
+/* Host: packs q (int8 in {-1, 0, 1}, row-major [rows][cols], cols a multiple
+ * of 16) into out (host uint32 [rows][cols / 16]). MK_ERR_INVALID_ARG for a
+ * NULL pointer, cols % 16 != 0 or a value outside {-1, 0, 1}. */
+int mk_w2_pack(const int8_t *q, int64_t rows, int64_t cols, uint32_t *out);
+
+/* Host: the inverse of mk_w2_pack; MK_ERR_INVALID_ARG on an invalid code. */
+int mk_w2_unpack(const uint32_t *packed, int64_t rows, int64_t cols, int8_t *q);
+
+/* y = W2A8(packed, beta) x on the device: d_packed [rows][cols / 16] uint32
+ * (16-byte aligned), d_x float[cols] (16-byte aligned), d_y float[rows];
+ * cols one of 2048, 4096, 6144, 8192. One kernel launch on `stream`
+ * (asynchronous); MK_ERR_INVALID_ARG for a bad pointer or size.
+ * Source: the BitNet page above (its GEMV kernel, interleaved 2-bit packing,
+ * dp4a); the quantisers follow BitNet b1.58 (Ma et al., 2024). */
+int mk_w2a8_gemv(const uint32_t *d_packed, float beta, int32_t rows, int32_t cols, const float *d_x,
+                 float *d_y, void *stream);
+
 /* Optional per-instruction timing: when `enable` is non-zero, every step
  * records %globaltimer stamps per instruction into a device buffer that
  * mk_read_trace copies out (see mk_read_trace).

@@ -62,3 +62,22 @@ def test_plan_inspect_cap_too_small(lib):
     buf = (ctypes.c_int32 * 16)()
     n = ctypes.c_int32()
     assert lib.mk_plan_inspect(ctypes.byref(cfg), 4, buf, 1, qlen, ctypes.byref(n)) == _lib.MK_ERR_INVALID_ARG
+
+
+def test_w2_packing_layout_and_round_trip():
+    # element 16w + 4j + i sits in bits [8i + 2j, 8i + 2j + 2) of word w as q + 1
+    import numpy as np
+    q = np.zeros((2, 32), dtype=np.int8)
+    q[0, 5] = 1     # w 0, j 1, i 1 -> bits 10..11 = 2
+    q[1, 16 + 14] = -1  # w 1, j 3, i 2 -> bits 22..23 = 0
+    p = _lib.w2_pack(q)
+    assert p[0, 0] == (0x55555555 & ~(3 << 10)) | (2 << 10)
+    assert p[0, 1] == 0x55555555
+    assert p[1, 1] == 0x55555555 & ~(3 << 22)
+    rng = np.random.default_rng(0)
+    r = (rng.integers(0, 3, (7, 2048)) - 1).astype(np.int8)
+    assert (_lib.w2_unpack(_lib.w2_pack(r), 2048) == r).all()
+    bad = r.copy()
+    bad[3, 100] = 2
+    with pytest.raises(_lib.MKError):
+        _lib.w2_pack(bad)
