@@ -94,6 +94,8 @@ def load(path: str | None = None):
     L.mk_w2_pack.argtypes = [_VP, ctypes.c_int64, ctypes.c_int64, _VP]
     L.mk_w2_unpack.argtypes = [_VP, ctypes.c_int64, ctypes.c_int64, _VP]
     L.mk_w2a8_gemv.argtypes = [_VP, ctypes.c_float, _I32, _I32, _VP, _VP, _VP]
+    L.mk_prefill.argtypes = [_VP, _VP, _I32, _I32, _VP, _VP, _VP]
+    L.mk_tc_gemm.argtypes = [_VP, _I32, _I32, _VP, _VP, _I32, _VP, _VP, _VP]
     L.mk_destroy.argtypes = [_VP]
     L.mk_destroy.restype = None
     _lib = L
@@ -202,6 +204,17 @@ def w2a8_gemv(packed, beta: float, rows: int, cols: int, x, y, stream=None) -> N
                               y.data_ptr(), _stream_ptr(stream)))
 
 
+def tc_gemm(w, bhi, blo, y, r=None, stream=None) -> None:
+    """mk_tc_gemm on CUDA tensors: w bf16 [M][K], bhi / blo bf16 [N][K], y (and r)
+    float32 [N][M]; y = W (bhi + blo)^T (+ r)."""
+    M, K = w.shape
+    N = bhi.shape[0]
+    rc = load().mk_tc_gemm(w.data_ptr(), int(M), int(K), bhi.data_ptr(), blo.data_ptr(), int(N), y.data_ptr(),
+                           r.data_ptr() if r is not None else None, _stream_ptr(stream))
+    if rc != 0:
+        raise MKError(rc, f"mk_tc_gemm returned {rc}")
+
+
 class Megakernel:
     """One model bound to the decode megakernel (owns an mk_handle).
 
@@ -242,6 +255,13 @@ class Megakernel:
                                           int(d_tokens.numel()),
                                           logits.data_ptr() if logits is not None else None,
                                           out_tokens.data_ptr(), _stream_ptr(stream)))
+
+    def prefill(self, d_tokens, start_pos: int, out_token, logits=None, stream=None) -> None:
+        """mk_prefill: d_tokens int32 CUDA tensor [n] at positions start_pos ..;
+        out_token int32 CUDA tensor [1]; logits float32 CUDA tensor [vocab] or None."""
+        check(load().mk_prefill(self.h, d_tokens.data_ptr(), int(d_tokens.numel()), int(start_pos),
+                                logits.data_ptr() if logits is not None else None, out_token.data_ptr(),
+                                _stream_ptr(stream)))
 
     def step_unfused(self, token: int, pos: int, out_token, logits=None, stream=None) -> None:
         check(load().mk_decode_step_unfused(self.h, int(token), int(pos),

@@ -11,8 +11,9 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libmk.so")
 LIB_CHECKED = os.path.join(BUILD, "libmk_checked.so")
-SOURCES = ["mk_kernel_hd64.cu", "mk_kernel_hd128.cu", "mk_kernel.cu", "mk_host.cpp", "mk_noalloc.cu", "mk_w2a8.cu"]
-DEPS = SOURCES + ["mk_kernel.cuh", "mk_plan.h", "mk_internal.h"]
+SOURCES = ["mk_kernel_hd64.cu", "mk_kernel_hd128.cu", "mk_kernel.cu", "mk_host.cpp", "mk_noalloc.cu", "mk_w2a8.cu",
+           "mk_prefill.cu"]
+DEPS = SOURCES + ["mk_kernel.cuh", "mk_plan.h", "mk_internal.h", "mk_prefill.h"]
 
 
 def nvcc() -> str:

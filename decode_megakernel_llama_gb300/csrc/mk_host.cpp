@@ -20,6 +20,7 @@
 
 #include "../../include/mk.h"
 #include "mk_plan.h"
+#include "mk_prefill.h"
 
 extern "C" cudaError_t mk_kernel_configure(void);
 extern "C" cudaError_t mk_kernel_launch(const mk::Params *p, int n_sm, int cooperative,
@@ -665,6 +666,12 @@ struct mk_handle {
     void *bdev_mem = nullptr;
     void *w16 = nullptr;  // fp16 copies of the GEMV weights and the LM head (batched steps)
     size_t bzero_bytes = 0;
+    // multi-token prefill (mk_prefill): tensor maps of the weights, made on
+    // the first call, and scratch for the largest prompt so far
+    bool pf_ready = false;
+    mkpf::Model pf_model;
+    mkpf::Scratch pf;
+    void *pf_mem = nullptr;
 };
 
 namespace {
@@ -910,10 +917,17 @@ int mk_get_status(mk_handle *h) {
     cudaError_t e = cudaSetDevice(h->device);
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
-    int32_t st = 0, bst = 0;
+    int32_t st = 0, bst = 0, pst = 0;
     e = cudaMemcpy(&st, h->base.status, sizeof st, cudaMemcpyDeviceToHost);
     if (e == cudaSuccess && h->has_batch) e = cudaMemcpy(&bst, h->bbase.status, sizeof bst, cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess && h->pf.err) e = cudaMemcpy(&pst, h->pf.err, sizeof pst, cudaMemcpyDeviceToHost);
     if (e != cudaSuccess) return cuda_fail(e, "status read");
+    if (pst != 0) {
+        e = cudaMemset(h->pf.err, 0, sizeof(int));
+        if (e != cudaSuccess) return cuda_fail(e, "status reset");
+        if (pst == 2) return fail(MK_ERR_INVALID_ARG, "prompt token outside [0, vocab)");
+        return fail(MK_ERR_TIMEOUT, "a bounded wait of the prefill expired");
+    }
     if (st == mk::DS_OK && bst == mk::DS_OK) return MK_OK;
     // a failed step leaves counters mid-way: clear them with the status
     e = cudaMemset(h->base.ctr, 0, h->zero_bytes);
@@ -924,6 +938,82 @@ int mk_get_status(mk_handle *h) {
     if (st == mk::DS_BAD_TOKEN) return fail(MK_ERR_INVALID_ARG, "device token outside [0, vocab)");
     if (st == mk::DS_BAD_POS) return fail(MK_ERR_INVALID_ARG, "device position outside [0, max_seq)");
     return fail(MK_ERR_TIMEOUT, "an in-kernel dependency wait timed out");
+}
+
+int mk_prefill(mk_handle *h, const int32_t *d_tokens, int32_t n, int32_t start_pos, float *out_logits,
+               int32_t *out_token, void *stream) {
+    if (!h || !d_tokens || !out_token) return fail(MK_ERR_INVALID_ARG, "handle, d_tokens or out_token is NULL");
+    if (n < 1 || start_pos < 0 || (int64_t)start_pos + n > h->cfg.max_seq)
+        return fail(MK_ERR_INVALID_ARG, "prompt positions outside [0, max_seq)");
+    cudaError_t e = cudaSetDevice(h->device);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaSetDevice");
+    const mk_config &c = h->cfg;
+    const int d = c.d_model, hd = c.head_dim, qd = c.n_heads * hd, kvd = c.n_kv_heads * hd, F = c.ffn_dim;
+    if (!h->pf_ready) {
+        mkpf::Model &m = h->pf_model;
+        m.L = c.n_layers; m.d = d; m.Hq = c.n_heads; m.Hkv = c.n_kv_heads; m.hd = hd; m.F = F; m.V = c.vocab;
+        m.max_seq = c.max_seq; m.n_sm = h->im.n_sm; m.eps = c.rms_eps;
+        m.embed = h->base.embed;
+        m.final_norm = h->base.final_norm;
+        m.rope = h->base.rope;
+        m.kc = h->base.kc;
+        m.vc = h->base.vc;
+        m.kv_layer_stride = (size_t)c.max_batch * c.n_kv_heads * c.max_seq * hd;
+        m.maps.resize(c.n_layers);
+        m.attn_norm.resize(c.n_layers);
+        m.mlp_norm.resize(c.n_layers);
+        for (int l = 0; l < c.n_layers; ++l) {
+            const mk::LayerW &lw = h->im.lws[l];
+            mkpf::LayerMaps &lm = m.maps[l];
+            m.attn_norm[l] = lw.attn_norm;
+            m.mlp_norm[l] = lw.mlp_norm;
+            if (!mkpf::encode_weight_map(&lm.wq, lw.wq, qd, d) || !mkpf::encode_weight_map(&lm.wk, lw.wk, kvd, d) ||
+                !mkpf::encode_weight_map(&lm.wv, lw.wv, kvd, d) || !mkpf::encode_weight_map(&lm.wo, lw.wo, d, qd) ||
+                !mkpf::encode_weight_map(&lm.wg, lw.w_gate, F, d) || !mkpf::encode_weight_map(&lm.wu, lw.w_up, F, d) ||
+                !mkpf::encode_weight_map(&lm.wd, lw.w_down, d, F))
+                return fail(MK_ERR_UNSUPPORTED, "could not encode the weights' tensor maps");
+        }
+        h->pf_ready = true;
+    }
+    if (h->pf.cap < n) {
+        // scratch for n tokens: residual, q|k|v, attention output, gate, up
+        // (fp32) and the hi/lo bf16 operand of the next contraction
+        const size_t kmax = std::max(std::max(d, qd), F), qkv = qd + 2 * kvd;
+        const size_t bytes = 4 * (size_t)n * (d + qkv + qd + 2 * (size_t)F) + 2 * 2 * (size_t)n * kmax +
+                             8 * (size_t)2 * h->im.n_sm + 4 * 256;
+        int32_t err_keep = 0;
+        if (h->pf.err) cudaMemcpy(&err_keep, h->pf.err, sizeof err_keep, cudaMemcpyDeviceToHost);
+        void *mem = nullptr;
+        e = cudaMalloc(&mem, bytes);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(prefill scratch)");
+        if (h->pf_mem) {
+            cudaDeviceSynchronize();
+            cudaFree(h->pf_mem);
+        }
+        h->pf_mem = mem;
+        char *b = static_cast<char *>(mem);
+        auto take = [&](size_t nbytes) {
+            char *at = b;
+            b += (nbytes + 255) & ~size_t(255);
+            return at;
+        };
+        mkpf::Scratch &sc = h->pf;
+        sc.cap = n;
+        sc.X = reinterpret_cast<float *>(take(4 * (size_t)n * d));
+        sc.QKV = reinterpret_cast<float *>(take(4 * (size_t)n * qkv));
+        sc.ATT = reinterpret_cast<float *>(take(4 * (size_t)n * qd));
+        sc.G = reinterpret_cast<float *>(take(4 * (size_t)n * F));
+        sc.U = reinterpret_cast<float *>(take(4 * (size_t)n * F));
+        sc.Ahi = reinterpret_cast<uint16_t *>(take(2 * (size_t)n * kmax));
+        sc.Alo = reinterpret_cast<uint16_t *>(take(2 * (size_t)n * kmax));
+        sc.keys = reinterpret_cast<unsigned long long *>(take(8 * (size_t)2 * h->im.n_sm));
+        sc.err = reinterpret_cast<int *>(take(4));
+        e = cudaMemcpy(sc.err, &err_keep, sizeof err_keep, cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) return cuda_fail(e, "prefill status");
+    }
+    e = mkpf::run(h->pf_model, h->pf, d_tokens, n, start_pos, out_logits, out_token, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+    return MK_OK;
 }
 
 int mk_set_wait_timeout(mk_handle *h, uint64_t timeout_ns) {
@@ -1044,6 +1134,7 @@ void mk_destroy(mk_handle *h) {
     if (h->dev_mem) cudaFree(h->dev_mem);
     if (h->bdev_mem) cudaFree(h->bdev_mem);
     if (h->w16) cudaFree(h->w16);
+    if (h->pf_mem) cudaFree(h->pf_mem);
     delete h;
 }
 

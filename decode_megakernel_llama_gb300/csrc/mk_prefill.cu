@@ -1,0 +1,642 @@
+// mk_prefill.cu — multi-token prefill: the prompt's projections as tensor-core
+// contractions (tcgen05), causal attention over the prompt, and the KV-cache
+// rows of every prompt position, in a handful of launches per layer.
+//
+// The megakernel article ("Revolution der KI-Beschleunigung: Wie ein
+// Low-Latency Megakernel den Llama-1B Turbo zündet", dasgeld.co, paragraph on
+// the internal infrastructure) plans the forward pass once and reuses it for
+// batch processing; a prompt of n tokens is such a batch. Its projections are
+// real dense contractions Y[n][out] = X[n][in] W[out][in]^T, so they run on
+// the 5th-generation tensor cores:
+//   * the weights are the MMA's A operand (M = 128 output features per CTA),
+//     the prompt's activations the B operand (N = 32 .. 128 tokens per CTA);
+//   * both arrive by TMA (cp.async.bulk.tensor) as 128-byte-swizzled K-major
+//     tiles of 64 elements into a 4-stage shared-memory ring with full/empty
+//     mbarriers;
+//   * one thread issues tcgen05.mma (kind::f16, bf16 x bf16 -> fp32) into an
+//     accumulator in tensor memory; tcgen05.commit frees a stage when its
+//     MMAs are done;
+//   * the epilogue reads the accumulator with tcgen05.ld and writes fp32
+//     (adding the residual where the layer has one).
+// The activations enter as two bf16 terms, hi = bf16(x) and lo = bf16(x -
+// hi), both multiplied by the same weight tile (twice the MMAs): x is then
+// carried to about 16 significant bits, so the prefill meets the decode
+// step's parity bar while the weights stay in their stored bf16.
+//
+// Every wait is bounded (%globaltimer, 2 s); on expiry the kernel records an
+// error in a status word, still drains its copies and frees its tensor
+// memory, and returns.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "mk_prefill.h"
+
+namespace mkpf {
+namespace {
+
+constexpr int kThreads = 128;  // 4 warps: TMA issuer, MMA issuer, and all four for the epilogue
+constexpr int kStages = 4;
+constexpr int kATileBytes = 128 * 128;  // 128 rows x 64 bf16
+constexpr uint64_t kWaitNs = 2000000000ull;
+
+__device__ __forceinline__ uint32_t saddr(const void *p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
+
+__device__ __forceinline__ uint64_t gtimer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(saddr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(saddr(bar)), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(saddr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait on an mbarrier phase; false (and the error word set) on expiry
+// or when another thread of the grid already gave up.
+__device__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *err) {
+    uint64_t t0 = 0;
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try(bar, parity)) return true;
+        if ((it & 63u) == 0) {
+            if (*(volatile int *)err) return false;
+            const uint64_t now = gtimer();
+            if (t0 == 0) {
+                t0 = now;
+            } else if (now - t0 > kWaitNs) {
+                atomicExch(err, 1);
+                return false;
+            }
+        }
+    }
+}
+
+// TMA: one box of a 2-D tensor map into shared memory, completing bytes on bar.
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            saddr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(saddr(bar))
+        : "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major bf16 tile in the 128-byte
+// swizzle layout that TMA writes: rows of 128 bytes (64 elements), atoms of 8
+// rows every 1024 bytes along M (or N). Fields: start address >> 4 (bits
+// 0-13), leading byte offset >> 4 (16-29; unused by this layout), stride
+// byte offset >> 4 (32-45), the fixed 0b001 (46-48), base offset 0 (the
+// tiles are 1024-byte aligned), swizzle mode 2 = 128 bytes (61-63). The k-th
+// 16-element slice of a row starts 32 bytes further.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t smem_byte_addr) {
+    uint64_t d = (uint64_t)((smem_byte_addr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)1 << 16;
+    d |= (uint64_t)(1024 >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+// Instruction descriptor of tcgen05.mma kind::f16: D fp32 (bits 4-5 = 1),
+// A and B bf16 (7-9 = 1, 10-12 = 1), both K-major (15, 16 = 0), N >> 3
+// (17-22), M >> 4 (24-28).
+template <int BN>
+__device__ __forceinline__ constexpr uint32_t idesc_bf16_f32() {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrives on bar once every MMA this thread issued before has completed.
+__device__ __forceinline__ void umma_commit(uint64_t *bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(saddr(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// 16 consecutive fp32 columns of this thread's tensor-memory lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15}, [%16];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+          "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Y[n][m] (+)= sum_k W[m][k] (Bhi[n][k] + Blo[n][k]) for m < M, n < N:
+// W [M][K] bf16 (tensor map ta, box 64 x 128), Bhi / Blo [N][K] bf16 (tensor
+// maps tbh / tbl, box 64 x BN), Y and R fp32 with row stride ldy (R may be
+// Y: an in-place residual add; or NULL). CTA (i, j) computes rows
+// 128i .. 128i+127 of W for tokens BN*j .. BN*j+BN-1. K % 64 == 0.
+// ---------------------------------------------------------------------------
+template <int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_gemm(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tbh,
+            const __grid_constant__ CUtensorMap tbl, int M, int N, int K, float *Y, int ldy, const float *R,
+            int *err) {
+    constexpr int kBTileBytes = BN * 128;
+    constexpr int kStageBytes = kATileBytes + 2 * kBTileBytes;
+    constexpr uint32_t kCols = BN < 32 ? 32 : BN;  // tensor-memory columns (a power of two >= 32)
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *full = reinterpret_cast<uint64_t *>(sm + kStages * kStageBytes);
+    uint64_t *empty = full + kStages;
+    uint64_t *done = empty + kStages;
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(done + 1);
+    int *issued = reinterpret_cast<int *>(tslot + 1);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int m0 = blockIdx.x * 128, n0 = blockIdx.y * BN, nk = K / 64;
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(done, 1);
+        *issued = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(saddr(tslot)),
+                     "r"(kCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+
+    if (warp == 0 && lane == 0) {
+        // TMA issuer: stage s of chunk kc once the MMAs of chunk kc - kStages freed it
+        for (int kc = 0; kc < nk; ++kc) {
+            const int s = kc % kStages;
+            if (kc >= kStages && !mbar_wait(&empty[s], ((kc / kStages) - 1) & 1, err)) break;
+            uint8_t *st = sm + s * kStageBytes;
+            mbar_expect_tx(&full[s], kStageBytes);
+            tma_load_2d(st, &ta, kc * 64, m0, &full[s]);
+            tma_load_2d(st + kATileBytes, &tbh, kc * 64, n0, &full[s]);
+            tma_load_2d(st + kATileBytes + kBTileBytes, &tbl, kc * 64, n0, &full[s]);
+            *issued = kc + 1;
+        }
+    } else if (warp == 1 && lane == 0) {
+        // MMA issuer: 4 k-slices of 16 per chunk, the hi and the lo term each
+        constexpr uint32_t idesc = idesc_bf16_f32<BN>();
+        bool ok = true;
+        for (int kc = 0; kc < nk && ok; ++kc) {
+            const int s = kc % kStages;
+            ok = mbar_wait(&full[s], (kc / kStages) & 1, err);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t a = saddr(sm + s * kStageBytes), bh = a + kATileBytes, bl = bh + kBTileBytes;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                umma_bf16(tmem, sw128_desc(a + kk * 32), sw128_desc(bh + kk * 32), idesc, (kc | kk) != 0);
+                umma_bf16(tmem, sw128_desc(a + kk * 32), sw128_desc(bl + kk * 32), idesc, 1u);
+            }
+            umma_commit(&empty[s]);
+        }
+        if (ok) umma_commit(done);
+    }
+    __syncwarp();
+    // epilogue: warp w reads tensor-memory lanes 32w .. 32w+31 (output rows)
+    const bool have = mbar_wait(done, 0, err);
+    tc_fence_after();
+    if (have) {
+        const int m = m0 + warp * 32 + lane;
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 16) {
+            uint32_t v[16];
+            tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c, v);
+            if (m < M) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int n = n0 + c + i;
+                    if (n < N) {
+                        float y = __uint_as_float(v[i]);
+                        if (R) y += R[(size_t)n * ldy + m];
+                        Y[(size_t)n * ldy + m] = y;
+                    }
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {
+        // a failed CTA still lets its issued copies land before its shared memory goes
+        const int ni = *issued, lo = ni > kStages ? ni - kStages : 0;
+        for (int kc = lo; kc < ni; ++kc) {
+            const uint64_t t0 = gtimer();
+            while (!mbar_try(&full[kc % kStages], (kc / kStages) & 1))
+                if (gtimer() - t0 > kWaitNs) break;
+        }
+    }
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kCols) : "memory");
+    }
+}
+
+template <int BN>
+constexpr int gemm_smem_bytes() {
+    return kStages * (kATileBytes + 2 * BN * 128) + 1024 + 128;
+}
+
+// ---------------------------------------------------------------------------
+// Elementwise and attention kernels of the prefill.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float bf2f(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
+
+// fp32 -> bf16, round to nearest even (finite values).
+__device__ __forceinline__ uint16_t f2bf_rne(float f) {
+    uint32_t u = __float_as_uint(f);
+    if ((u & 0x7F800000u) == 0x7F800000u) return uint16_t((u >> 16) | ((u & 0xFFFFu) ? 0x40u : 0u));
+    u += 0x7FFFu + ((u >> 16) & 1u);
+    return uint16_t(u >> 16);
+}
+
+__device__ __forceinline__ float block_sum(float v, float *red) {
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    const int w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) red[w] = v;
+    __syncthreads();
+    float t = 0.f;
+    for (int i = 0; i < nw; ++i) t += red[i];
+    return t;
+}
+
+// X[t] = float(E[tokens[t]]); a token outside [0, V) sets the error word.
+__global__ void embed_rows(const uint16_t *E, const int32_t *tokens, int n, int d, int V, float *X, int *err) {
+    const int t = blockIdx.x;
+    const int tok = tokens[t];
+    if (tok < 0 || tok >= V) {
+        if (threadIdx.x == 0) atomicExch(err, 2);
+        return;
+    }
+    for (int i = threadIdx.x; i < d; i += blockDim.x) X[(size_t)t * d + i] = bf2f(E[(size_t)tok * d + i]);
+}
+
+// hi/lo bf16 terms of rows of X [rows][K] (fp32), optionally RMSNorm'd with gain g.
+__global__ void norm_split(const float *X, int K, const uint16_t *g, float eps, uint16_t *hi, uint16_t *lo) {
+    __shared__ float red[32];
+    const int t = blockIdx.x;
+    const float *x = X + (size_t)t * K;
+    float scale = 1.f;
+    if (g) {
+        float ss = 0.f;
+        for (int i = threadIdx.x; i < K; i += blockDim.x) ss = fmaf(x[i], x[i], ss);
+        ss = block_sum(ss, red);
+        scale = 1.0f / sqrtf(ss / (float)K + eps);
+    }
+    for (int i = threadIdx.x; i < K; i += blockDim.x) {
+        const float v = g ? x[i] * (scale * bf2f(g[i])) : x[i];
+        const uint16_t h = f2bf_rne(v);
+        hi[(size_t)t * K + i] = h;
+        lo[(size_t)t * K + i] = f2bf_rne(v - bf2f(h));
+    }
+}
+
+// RoPE on q and k of token t (position pos0 + t) from the fp32 QKV rows, q
+// kept (rotated) in place, bf16 k and v written into the cache at the position.
+__global__ void rope_append(float *QKV, int n, int Hq, int Hkv, int hd, int pos0, const float *rope, int max_seq,
+                            uint16_t *kc, uint16_t *vc) {
+    const int t = blockIdx.x, pos = pos0 + t;
+    const int stride = (Hq + 2 * Hkv) * hd, half = hd / 2;
+    float *row = QKV + (size_t)t * stride;
+    for (int idx = threadIdx.x; idx < (Hq + Hkv) * half; idx += blockDim.x) {
+        const int h = idx / half, i = idx % half;
+        float *v = row + (size_t)h * hd;
+        const float c = rope[((size_t)pos * half + i) * 2], s = rope[((size_t)pos * half + i) * 2 + 1];
+        const float a = v[i], b = v[i + half];
+        const float ra = a * c - b * s, rb = b * c + a * s;
+        if (h < Hq) {
+            v[i] = ra;
+            v[i + half] = rb;
+        } else {
+            const int kvh = h - Hq;
+            const size_t off = ((size_t)kvh * max_seq + pos) * hd;
+            kc[off + i] = f2bf_rne(ra);
+            kc[off + i + half] = f2bf_rne(rb);
+        }
+    }
+    for (int idx = threadIdx.x; idx < Hkv * hd; idx += blockDim.x) {
+        const int kvh = idx / hd, i = idx % hd;
+        vc[((size_t)kvh * max_seq + pos) * hd + i] = f2bf_rne(row[(size_t)(Hq + Hkv) * hd + idx]);
+    }
+}
+
+// Causal attention: one warp per (token t, query head h) over cache
+// positions 0 .. pos0 + t of kv head h / G, online softmax in chunks of 32
+// positions (lane = position for the scores, lane = dimension pair for P.V).
+template <int HD>
+__global__ void attend_prefill(const float *QKV, int n, int Hq, int Hkv, int pos0, int max_seq,
+                               const uint16_t *kc, const uint16_t *vc, float *out) {
+    const int warp_global = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (warp_global >= n * Hq) return;
+    const int t = warp_global / Hq, h = warp_global % Hq, G = Hq / Hkv, kvh = h / G;
+    const int T = pos0 + t + 1;
+    const int stride = (Hq + 2 * Hkv) * HD;
+    const float *q = QKV + (size_t)t * stride + (size_t)h * HD;
+    const float scale = rsqrtf((float)HD);
+    float qr[HD];
+#pragma unroll
+    for (int i = 0; i < HD; ++i) qr[i] = q[i] * scale;
+    const uint16_t *K = kc + (size_t)kvh * max_seq * HD, *V = vc + (size_t)kvh * max_seq * HD;
+    constexpr int DP = HD / 32;  // output dims per lane
+    float o[DP], m = -INFINITY, l = 0.f;
+#pragma unroll
+    for (int e = 0; e < DP; ++e) o[e] = 0.f;
+    for (int j0 = 0; j0 < T; j0 += 32) {
+        const int j = j0 + lane;
+        float s = -INFINITY;
+        if (j < T) {
+            const uint4 *kr = reinterpret_cast<const uint4 *>(K + (size_t)j * HD);
+            float acc = 0.f;
+#pragma unroll
+            for (int c = 0; c < HD / 8; ++c) {
+                const uint4 w = kr[c];
+                const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    acc = fmaf(__uint_as_float(u[e] << 16), qr[c * 8 + 2 * e], acc);
+                    acc = fmaf(__uint_as_float(u[e] & 0xFFFF0000u), qr[c * 8 + 2 * e + 1], acc);
+                }
+            }
+            s = acc;
+        }
+        float cm = s;
+        for (int off = 16; off > 0; off >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xFFFFFFFFu, cm, off));
+        const float mn = fmaxf(m, cm);
+        const float corr = __expf(m - mn);
+        const float p = j < T ? __expf(s - mn) : 0.f;
+        float ps = p;
+        for (int off = 16; off > 0; off >>= 1) ps += __shfl_xor_sync(0xFFFFFFFFu, ps, off);
+        l = l * corr + ps;
+        m = mn;
+#pragma unroll
+        for (int e = 0; e < DP; ++e) o[e] *= corr;
+        const int cnt = T - j0 < 32 ? T - j0 : 32;
+        for (int jj = 0; jj < cnt; ++jj) {
+            const float pj = __shfl_sync(0xFFFFFFFFu, p, jj);
+            const uint16_t *vr = V + (size_t)(j0 + jj) * HD + lane * DP;
+#pragma unroll
+            for (int e = 0; e < DP; ++e) o[e] = fmaf(pj, bf2f(vr[e]), o[e]);
+        }
+    }
+    float *dst = out + (size_t)t * Hq * HD + (size_t)h * HD + lane * DP;
+#pragma unroll
+    for (int e = 0; e < DP; ++e) dst[e] = o[e] / l;
+}
+
+// h = silu(G) * U into hi/lo bf16 terms.
+__global__ void silu_split(const float *Gt, const float *U, size_t count, uint16_t *hi, uint16_t *lo) {
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < count; i += (size_t)gridDim.x * blockDim.x) {
+        const float g = Gt[i];
+        const float v = g / (1.0f + expf(-g)) * U[i];
+        const uint16_t h = f2bf_rne(v);
+        hi[i] = h;
+        lo[i] = f2bf_rne(v - bf2f(h));
+    }
+}
+
+// Final RMSNorm of one row into shared memory, then rows of the tied
+// embedding times it (a warp per row), logits and a block argmax key.
+__global__ void lm_head_rows(const float *x, const uint16_t *g, float eps, const uint16_t *E, int V, int d,
+                             float *logits, unsigned long long *keys) {
+    extern __shared__ float xs[];
+    __shared__ float red[32];
+    __shared__ unsigned long long best[32];
+    float ss = 0.f;
+    for (int i = threadIdx.x; i < d; i += blockDim.x) ss = fmaf(x[i], x[i], ss);
+    ss = block_sum(ss, red);
+    const float r = 1.0f / sqrtf(ss / (float)d + eps);
+    for (int i = threadIdx.x; i < d; i += blockDim.x) xs[i] = x[i] * (r * bf2f(g[i]));
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    unsigned long long bk = 0ull;
+    for (int row = blockIdx.x * nw + warp; row < V; row += gridDim.x * nw) {
+        const uint16_t *w = E + (size_t)row * d;
+        float acc = 0.f;
+        for (int c = lane * 8; c < d; c += 256) {
+            const uint4 v = *reinterpret_cast<const uint4 *>(w + c);
+            const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                acc = fmaf(__uint_as_float(u[e] << 16), xs[c + 2 * e], acc);
+                acc = fmaf(__uint_as_float(u[e] & 0xFFFF0000u), xs[c + 2 * e + 1], acc);
+            }
+        }
+        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
+        if (lane == 0) {
+            if (logits) logits[row] = acc;
+            uint32_t u = __float_as_uint(acc);
+            u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+            const unsigned long long k = ((unsigned long long)u << 32) | (0xFFFFFFFFu - (uint32_t)row);
+            bk = k > bk ? k : bk;
+        }
+    }
+    if (lane == 0) best[warp] = bk;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        unsigned long long b = 0ull;
+        for (int i = 0; i < nw; ++i) b = best[i] > b ? best[i] : b;
+        keys[blockIdx.x] = b;
+    }
+}
+
+__global__ void argmax_keys(const unsigned long long *keys, int n, int32_t *out_token) {
+    __shared__ unsigned long long best[32];
+    unsigned long long b = 0ull;
+    for (int i = threadIdx.x; i < n; i += blockDim.x) b = keys[i] > b ? keys[i] : b;
+    for (int o = 16; o > 0; o >>= 1) {
+        const unsigned long long x = __shfl_xor_sync(0xFFFFFFFFu, b, o);
+        b = x > b ? x : b;
+    }
+    if ((threadIdx.x & 31) == 0) best[threadIdx.x >> 5] = b;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < (int)(blockDim.x >> 5); ++i) b = best[i] > b ? best[i] : b;
+        *out_token = (int32_t)(0xFFFFFFFFu - (uint32_t)(b & 0xFFFFFFFFull));
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encoder() {
+    static EncodeTiledFn fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+// Tensor map of a row-major bf16 matrix [rows][K], boxes of 64 x box_rows,
+// 128-byte swizzle (rows past the end read as zeros).
+bool make_map(CUtensorMap *map, const void *ptr, int rows, int K, int box_rows) {
+    EncodeTiledFn enc = encoder();
+    if (!enc) return false;
+    const cuuint64_t gdim[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+    const cuuint64_t gstride[1] = {(cuuint64_t)K * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), gdim, gstride, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int pick_bn(int M, int N, int n_sm) {
+    // the widest token tile that still gives about one CTA per SM
+    const int mt = (M + 127) / 128;
+    for (int bn : {128, 64})
+        if (mt * ((N + bn - 1) / bn) >= n_sm) return bn;
+    return 32;
+}
+
+template <int BN>
+cudaError_t launch_gemm_bn(const CUtensorMap &ta, const void *bhi, const void *blo, int M, int N, int K, float *Y,
+                           int ldy, const float *R, int *err, cudaStream_t s) {
+    CUtensorMap th, tl;
+    if (!make_map(&th, bhi, N, K, BN) || !make_map(&tl, blo, N, K, BN)) return cudaErrorInvalidValue;
+    constexpr int smem = gemm_smem_bytes<BN>();
+    cudaError_t e = cudaFuncSetAttribute(tc_gemm<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    const dim3 grid((M + 127) / 128, (N + BN - 1) / BN);
+    tc_gemm<BN><<<grid, kThreads, smem, s>>>(ta, th, tl, M, N, K, Y, ldy, R, err);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool encode_weight_map(CUtensorMap *map, const void *w, int rows, int K) { return make_map(map, w, rows, K, 128); }
+
+cudaError_t gemm(const CUtensorMap &wmap, const void *bhi, const void *blo, int M, int N, int K, float *Y, int ldy,
+                 const float *R, int *err, int n_sm, cudaStream_t s) {
+    if (K % 64 || M < 1 || N < 1) return cudaErrorInvalidValue;
+    switch (pick_bn(M, N, n_sm)) {
+        case 128: return launch_gemm_bn<128>(wmap, bhi, blo, M, N, K, Y, ldy, R, err, s);
+        case 64: return launch_gemm_bn<64>(wmap, bhi, blo, M, N, K, Y, ldy, R, err, s);
+        default: return launch_gemm_bn<32>(wmap, bhi, blo, M, N, K, Y, ldy, R, err, s);
+    }
+}
+
+cudaError_t run(const Model &m, const Scratch &sc, const int32_t *d_tokens, int n, int pos0, float *out_logits,
+                int32_t *out_token, cudaStream_t s) {
+    const int d = m.d, Hq = m.Hq, Hkv = m.Hkv, hd = m.hd, F = m.F, qd = Hq * hd, kvd = Hkv * hd;
+    const int qkv = qd + 2 * kvd;
+    cudaError_t e = cudaSuccess;
+    auto ok = [&](cudaError_t x) {
+        if (e == cudaSuccess) e = x;
+        return e == cudaSuccess;
+    };
+    embed_rows<<<n, 256, 0, s>>>(m.embed, d_tokens, n, d, m.V, sc.X, sc.err);
+    ok(cudaGetLastError());
+    for (int l = 0; l < m.L && e == cudaSuccess; ++l) {
+        const LayerMaps &lm = m.maps[l];
+        const size_t kv_off = (size_t)l * m.kv_layer_stride;
+        // attention block
+        norm_split<<<n, 256, 0, s>>>(sc.X, d, m.attn_norm[l], m.eps, sc.Ahi, sc.Alo);
+        ok(cudaGetLastError());
+        ok(gemm(lm.wq, sc.Ahi, sc.Alo, qd, n, d, sc.QKV, qkv, nullptr, sc.err, m.n_sm, s));
+        ok(gemm(lm.wk, sc.Ahi, sc.Alo, kvd, n, d, sc.QKV + qd, qkv, nullptr, sc.err, m.n_sm, s));
+        ok(gemm(lm.wv, sc.Ahi, sc.Alo, kvd, n, d, sc.QKV + qd + kvd, qkv, nullptr, sc.err, m.n_sm, s));
+        rope_append<<<n, 256, 0, s>>>(sc.QKV, n, Hq, Hkv, hd, pos0, m.rope, m.max_seq, m.kc + kv_off, m.vc + kv_off);
+        ok(cudaGetLastError());
+        const int warps = n * Hq, wpb = 4;
+        if (hd == 64)
+            attend_prefill<64><<<(warps + wpb - 1) / wpb, wpb * 32, 0, s>>>(sc.QKV, n, Hq, Hkv, pos0, m.max_seq,
+                                                                           m.kc + kv_off, m.vc + kv_off, sc.ATT);
+        else
+            attend_prefill<128><<<(warps + wpb - 1) / wpb, wpb * 32, 0, s>>>(sc.QKV, n, Hq, Hkv, pos0, m.max_seq,
+                                                                            m.kc + kv_off, m.vc + kv_off, sc.ATT);
+        ok(cudaGetLastError());
+        norm_split<<<n, 256, 0, s>>>(sc.ATT, qd, nullptr, 0.f, sc.Ahi, sc.Alo);
+        ok(cudaGetLastError());
+        ok(gemm(lm.wo, sc.Ahi, sc.Alo, d, n, qd, sc.X, d, sc.X, sc.err, m.n_sm, s));
+        // MLP block
+        norm_split<<<n, 256, 0, s>>>(sc.X, d, m.mlp_norm[l], m.eps, sc.Ahi, sc.Alo);
+        ok(cudaGetLastError());
+        ok(gemm(lm.wg, sc.Ahi, sc.Alo, F, n, d, sc.G, F, nullptr, sc.err, m.n_sm, s));
+        ok(gemm(lm.wu, sc.Ahi, sc.Alo, F, n, d, sc.U, F, nullptr, sc.err, m.n_sm, s));
+        silu_split<<<1024, 256, 0, s>>>(sc.G, sc.U, (size_t)n * F, sc.Ahi, sc.Alo);
+        ok(cudaGetLastError());
+        ok(gemm(lm.wd, sc.Ahi, sc.Alo, d, n, F, sc.X, d, sc.X, sc.err, m.n_sm, s));
+    }
+    if (e != cudaSuccess) return e;
+    // LM head of the last prompt position
+    const int blocks = 2 * m.n_sm;
+    lm_head_rows<<<blocks, 512, sizeof(float) * d, s>>>(sc.X + (size_t)(n - 1) * d, m.final_norm, m.eps, m.embed,
+                                                        m.V, d, out_logits, sc.keys);
+    if (!ok(cudaGetLastError())) return e;
+    argmax_keys<<<1, 256, 0, s>>>(sc.keys, blocks, out_token);
+    ok(cudaGetLastError());
+    return e;
+}
+
+}  // namespace mkpf
+
+// Unit entry of the tensor-core contraction (tests and measurement).
+extern "C" int mk_tc_gemm(const void *d_w, int32_t M, int32_t K, const void *d_bhi, const void *d_blo, int32_t N,
+                          float *d_y, const float *d_r, void *stream) {
+    if (!d_w || !d_bhi || !d_blo || !d_y || M < 1 || N < 1 || K < 64 || K % 64) return -1;
+    if ((reinterpret_cast<uintptr_t>(d_w) | reinterpret_cast<uintptr_t>(d_bhi) | reinterpret_cast<uintptr_t>(d_blo)) & 15u)
+        return -1;
+    CUtensorMap wm;
+    if (!mkpf::encode_weight_map(&wm, d_w, M, K)) return -4;
+    int dev = 0, n_sm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return -2;
+    static int *err = nullptr;  // per-process status word of the unit entry
+    if (!err && cudaMalloc(&err, sizeof(int)) != cudaSuccess) return -6;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(err, 0, sizeof(int), s) != cudaSuccess) return -2;
+    const cudaError_t e = mkpf::gemm(wm, d_bhi, d_blo, M, N, K, d_y, M, d_r, err, n_sm, s);
+    if (e != cudaSuccess) return -2;
+    int h = 0;
+    if (cudaMemcpyAsync(&h, err, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return -2;
+    return h ? -5 : 0;
+}

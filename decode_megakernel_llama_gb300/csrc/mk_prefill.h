@@ -1,0 +1,51 @@
+// mk_prefill.h — host-side interface of the prefill kernels (mk_prefill.cu)
+// for the C ABI in mk_host.cpp. Not part of the C ABI.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <vector>
+
+namespace mkpf {
+
+// Tensor maps of one layer's projection weights (bf16 [out][in], boxes of
+// 64 x 128, 128-byte swizzle).
+struct LayerMaps {
+    CUtensorMap wq, wk, wv, wo, wg, wu, wd;
+};
+
+// The model as the prefill reads it (device pointers; borrowed).
+struct Model {
+    int L = 0, d = 0, Hq = 0, Hkv = 0, hd = 0, F = 0, V = 0, max_seq = 0, n_sm = 0;
+    float eps = 0.f;
+    const uint16_t *embed = nullptr, *final_norm = nullptr;
+    std::vector<const uint16_t *> attn_norm, mlp_norm;
+    std::vector<LayerMaps> maps;
+    const float *rope = nullptr;  // [max_seq][hd/2][2] cos, sin
+    uint16_t *kc = nullptr, *vc = nullptr;  // KV cache of batch slot 0 of layer 0
+    size_t kv_layer_stride = 0;             // elements from one layer's slot-0 cache to the next
+};
+
+// Device scratch for up to `cap` prompt tokens.
+struct Scratch {
+    int cap = 0;
+    float *X = nullptr, *QKV = nullptr, *ATT = nullptr, *G = nullptr, *U = nullptr;
+    uint16_t *Ahi = nullptr, *Alo = nullptr;
+    unsigned long long *keys = nullptr;
+    int *err = nullptr;  // 0 ok, 1 a bounded wait expired, 2 a token outside [0, vocab)
+};
+
+bool encode_weight_map(CUtensorMap *map, const void *w, int rows, int K);
+
+// Y[n][m] (+)= W[m][.] . (Bhi[n][.] + Blo[n][.]) on the tensor cores.
+cudaError_t gemm(const CUtensorMap &wmap, const void *bhi, const void *blo, int M, int N, int K, float *Y, int ldy,
+                 const float *R, int *err, int n_sm, cudaStream_t s);
+
+// The prompt d_tokens[0 .. n) at positions pos0 .. pos0+n-1 through every
+// layer: K/V rows of every position into the cache, logits of the last
+// position into out_logits (nullable) and its greedy token into out_token.
+cudaError_t run(const Model &m, const Scratch &sc, const int32_t *d_tokens, int n, int pos0, float *out_logits,
+                int32_t *out_token, cudaStream_t s);
+
+}  // namespace mkpf

@@ -158,6 +158,42 @@ int mk_decode_step_host(mk_handle *h, const int32_t *host_token, int32_t positio
 int mk_decode_step_batch(mk_handle *h, const int32_t *d_tokens, const int32_t *d_positions, int32_t batch,
                          float *out_logits, int32_t *out_tokens, void *stream);
 
+/* Multi-token prefill of batch slot 0: runs the n prompt tokens d_tokens[0 ..
+ * n) (device int32[n]) at positions start_pos .. start_pos + n - 1 through
+ * every layer at once, writes the key/value rows of all n positions into
+ * the KV cache, and writes the logits of the last prompt position to
+ * out_logits (device float[vocab], nullable) and its greedy token to
+ * out_token (device int32[1]). The cache then holds what n consecutive
+ * mk_decode_step calls would have left (to rounding), so decoding continues
+ * at start_pos + n. The projections run as tensor-core contractions
+ * (tcgen05.mma, bf16 weights x the activations split into two bf16 terms,
+ * fp32 accumulation in tensor memory); attention is causal over the cache.
+ * A few launches per layer on `stream` (asynchronous). The first call makes
+ * the weights' tensor maps; a call with more tokens than any before
+ * allocates the scratch for them (on the current device, owned by the
+ * handle). MK_ERR_INVALID_ARG for a NULL pointer, n < 1 or positions past
+ * max_seq; a prompt token outside [0, vocab) or an expired in-kernel wait is
+ * reported by mk_get_status. One call in flight per handle, like the decode
+ * steps (they share the cache).
+ * Source: the article's internal-infrastructure paragraph (the planned
+ * forward pass reused for batch processing): a prompt is such a batch, and
+ * its projections are dense contractions. */
+int mk_prefill(mk_handle *h, const int32_t *d_tokens, int32_t n, int32_t start_pos, float *out_logits,
+               int32_t *out_token, void *stream);
+
+/* The prefill's tensor-core contraction on its own:
+ * d_y[n][m] = sum_k W[m][k] (Bhi[n][k] + Blo[n][k]) (+ d_r[n][m] if d_r is
+ * not NULL; d_r may equal d_y) for m < M, n < N, with W = d_w bf16 [M][K],
+ * Bhi = d_bhi and Blo = d_blo bf16 [N][K], d_y / d_r fp32 [N][M]; K a
+ * multiple of 64, all pointers 16-byte aligned. Synchronous (waits for
+ * `stream`). Returns 0, -1 for bad arguments, -2 for a CUDA error, -4 if
+ * the tensor maps cannot be made, -5 if an in-kernel wait expired, -6 if
+ * its status word cannot be allocated (first call only).
+ * Source: as mk_prefill; a unit entry of this library for tests and
+ * measurement. */
+int mk_tc_gemm(const void *d_w, int32_t M, int32_t K, const void *d_bhi, const void *d_blo, int32_t N, float *d_y,
+               const float *d_r, void *stream);
+
 /* The same step as a chain of separate kernel launches, one per stage
  * (QKV, attention, O-projection, gate/up, down per layer; LM head), with the
  * stream order between launches instead of in-kernel waits. Same results
