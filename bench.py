@@ -38,10 +38,15 @@ def parse():
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--no-comparators", action="store_true",
                     help="skip the unfused-chain timings")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the prefill, tensor-core GEMM and W2A8 GEMV timings")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="budget of each timed oracle CPU-baseline sample (all cores, one thread); 0 skips it")
     ap.add_argument("--profile", action="store_true",
                     help="only W warm-up and K decode steps (for ncu captures); prints one line")
+    ap.add_argument("--profile-gemm", action="store_true",
+                    help="only W + K runs of the prefill's gate contraction (tensor cores) for the "
+                         "workload's prompt (for ncu captures); prints one line")
     ap.add_argument("--trace", default=None,
                     help="also record one traced step and write its summary (JSON) here")
     return ap.parse_args()
@@ -293,6 +298,120 @@ def run_reference(args, ws, rank):
     print(json.dumps(line), flush=True)
 
 
+def projection_params(shape) -> int:
+    """Weights of one layer's seven projections."""
+    d, F, qd, kvd = shape.d_model, shape.ffn_dim, shape.q_dim, shape.kv_dim
+    return qd * d + 2 * kvd * d + d * qd + 3 * F * d
+
+
+def bf16_tensor_peak():
+    """Measured dense bf16 tensor peak (TFLOP/s) and its kind."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            d = json.load(open(path))
+            if d.get("bf16_tflops"):
+                return float(d["bf16_tflops"]), "of measured (burst)"
+        except Exception:
+            pass
+    return 1900.0, "of fallback"
+
+
+def measure_extras(mk, shape, prompt, P, W, dev, stream, decode_us):
+    """Prefill of the P-token prompt (mk_prefill), its gate contraction alone
+    (mk_tc_gemm), and the W2A8 GEMV (mk_w2a8_gemv), timed with CUDA events on
+    the launching stream after W warm-up runs."""
+    import torch
+    from decode_megakernel_llama_gb300 import _lib
+    out = {}
+
+    def timed(fn, reps):
+        for _ in range(W):
+            fn()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record(stream)
+        for _ in range(reps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return 1e3 * a.elapsed_time(b) / reps  # us
+
+    peak_tf, peak_kind = bf16_tensor_peak()
+    # prefill: the prompt at positions 0 .. P-1 (rewrites the same cache rows)
+    toks = prompt.to(dev)
+    tok = torch.zeros(1, dtype=torch.int32, device=dev)
+    us = timed(lambda: mk.prefill(toks, 0, tok, None, stream), 10)
+    if mk.status() != 0:
+        raise SystemExit("prefill status error")
+    flops = 2 * 2 * P * shape.n_layers * projection_params(shape)  # hi and lo terms
+    out["prefill"] = {"prompt_tokens": P, "us_per_prompt": us, "us_per_token": us / P,
+                      "vs_token_by_token_us": decode_us * P,
+                      "projection_tflops": flops / (us * 1e-6) / 1e12,
+                      "note": "tcgen05 bf16 contractions (activations as hi + lo bf16 terms), "
+                              "causal attention, KV append; TFLOP/s counts the projections only, over the whole prefill"}
+    # the gate contraction of that prompt on its own
+    g = torch.Generator(device="cpu").manual_seed(7)
+    F, d = shape.ffn_dim, shape.d_model
+    w = (torch.randn(F, d, generator=g) * 0.02).to(torch.bfloat16).to(dev)
+    x = torch.randn(P, d, generator=g)
+    hi = x.to(torch.bfloat16)
+    lo = (x - hi.float()).to(torch.bfloat16)
+    hi, lo = hi.to(dev), lo.to(dev)
+    y = torch.empty(P, F, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    gus = timed(lambda: _lib.tc_gemm(w, hi, lo, y, status=st, stream=stream), 20)
+    if int(st.item()) != 0:
+        raise SystemExit("tensor-core contraction status error")
+    gflop = 2 * 2 * P * F * d
+    achieved = gflop / (gus * 1e-6) / 1e12
+    out["prefill"]["gate_gemm"] = {"M": F, "K": d, "N": P, "us": gus,
+                                   "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_tf,
+                                                "unit": "TFLOP/s", "frac": achieved / peak_tf,
+                                                "peak_source": peak_kind}}
+    del w, hi, lo, y
+    # W2A8 GEMV over a 134 MB packed matrix (larger than L2)
+    rows, cols = 65536, 8192
+    packed = torch.randint(0, 2 ** 31 - 1, (rows, cols // 16), generator=g, dtype=torch.int32)
+    packed = (packed & 0x55555555).to(dev)  # codes 0 or 1 (weights -1 / 0): valid words
+    xv = torch.randn(cols, generator=g).to(dev)
+    yv = torch.empty(rows, device=dev)
+    wus = timed(lambda: _lib.w2a8_gemv(packed, 0.02, rows, cols, xv, yv, stream=stream), 20)
+    nbytes = rows * cols // 4 + 4 * cols + 4 * rows
+    gbs = nbytes / (wus * 1e-6) / 1e9
+    hbm, hbm_kind = measured_peak()
+    out["w2a8_gemv"] = {"rows": rows, "cols": cols, "us": wus, "weights_per_s": rows * cols / (wus * 1e-6),
+                        "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
+                                     "frac": gbs / hbm, "peak_source": hbm_kind, "bytes_per_launch": nbytes}}
+    return out
+
+
+def run_profile_gemm(args):
+    """W + K launches of the tensor-core contraction of the prompt's gate
+    projection (M = ffn, K = d_model, N = prompt tokens), nothing else."""
+    import torch
+    from decode_megakernel_llama_gb300 import _lib
+    from decode_megakernel_llama_gb300.build import build
+    from decode_megakernel_llama_gb300.configs import WORKLOADS
+    build()
+    dev = torch.device("cuda", 0)
+    wl = WORKLOADS[args.workload]
+    shape, P = wl.shape, wl.prompt_len
+    g = torch.Generator(device="cpu").manual_seed(7)
+    w = (torch.randn(shape.ffn_dim, shape.d_model, generator=g) * 0.02).to(torch.bfloat16).to(dev)
+    x = torch.randn(P, shape.d_model, generator=g)
+    hi = x.to(torch.bfloat16)
+    lo = (x - hi.float()).to(torch.bfloat16)
+    hi, lo = hi.to(dev), lo.to(dev)
+    y = torch.empty(P, shape.ffn_dim, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    for _ in range(args.warmup + args.steps):
+        _lib.tc_gemm(w, hi, lo, y, status=st)
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_gemm": True, "status": int(st.item()), "launches": args.warmup + args.steps}),
+          flush=True)
+
+
 def run_batch(args, ws, rank, local):
     """The batched workload (llama1b_b8): B sequences per step in one launch
     (mk_decode_step_batch), their caches pre-filled with seeded keys/values up
@@ -539,6 +658,10 @@ def run_mk(args, ws, rank, local):
             json.dump(summ, f, indent=1)
         mktrace.to_chrome(rec, os.path.splitext(args.trace)[0] + ".chrome.json")
 
+    # ---- multi-token prefill of the workload's prompt (tensor cores), the
+    # contraction alone, and the W2A8 GEMV
+    extras = None if args.no_extras or ws > 1 else measure_extras(mk, shape, prompt, P, W, dev, stream, us_per_tok_launch)
+
     # ---- roofline of the megakernel (the only kernel)
     mean_bytes = sum(algorithmic_bytes(shape, P0 + s) for s in range(K)) / K
     achieved = mean_bytes / (us_per_tok_launch * 1e-6) / 1e9
@@ -574,6 +697,8 @@ def run_mk(args, ws, rank, local):
             "clocks": clk.summary(),
             "comparators": comp,
             "sampling": sampling_line,
+            "prefill": extras.get("prefill") if extras else None,
+            "w2a8_gemv": extras.get("w2a8_gemv") if extras else None,
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
@@ -589,6 +714,8 @@ def main():
     from decode_megakernel_llama_gb300.configs import WORKLOADS
     if args.impl == "reference":
         run_reference(args, ws, rank)
+    elif args.profile_gemm:
+        run_profile_gemm(args)
     elif WORKLOADS[args.workload].batch > 1:
         run_batch(args, ws, rank, local)
     else:

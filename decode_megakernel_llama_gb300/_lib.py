@@ -95,7 +95,7 @@ def load(path: str | None = None):
     L.mk_w2_unpack.argtypes = [_VP, ctypes.c_int64, ctypes.c_int64, _VP]
     L.mk_w2a8_gemv.argtypes = [_VP, ctypes.c_float, _I32, _I32, _VP, _VP, _VP]
     L.mk_prefill.argtypes = [_VP, _VP, _I32, _I32, _VP, _VP, _VP]
-    L.mk_tc_gemm.argtypes = [_VP, _I32, _I32, _VP, _VP, _I32, _VP, _VP, _VP]
+    L.mk_tc_gemm.argtypes = [_VP, _I32, _I32, _VP, _VP, _I32, _VP, _VP, _VP, _VP]
     L.mk_destroy.argtypes = [_VP]
     L.mk_destroy.restype = None
     _lib = L
@@ -204,15 +204,21 @@ def w2a8_gemv(packed, beta: float, rows: int, cols: int, x, y, stream=None) -> N
                               y.data_ptr(), _stream_ptr(stream)))
 
 
-def tc_gemm(w, bhi, blo, y, r=None, stream=None) -> None:
+def tc_gemm(w, bhi, blo, y, r=None, status=None, stream=None) -> None:
     """mk_tc_gemm on CUDA tensors: w bf16 [M][K], bhi / blo bf16 [N][K], y (and r)
-    float32 [N][M]; y = W (bhi + blo)^T (+ r)."""
+    float32 [N][M]; y = W (bhi + blo)^T (+ r). status: int32 CUDA tensor [1]
+    (zeroed by the caller) that turns non-zero if an in-kernel wait expires;
+    without it, the call synchronises and raises on expiry."""
+    import torch
     M, K = w.shape
     N = bhi.shape[0]
+    st = status if status is not None else torch.zeros(1, dtype=torch.int32, device=y.device)
     rc = load().mk_tc_gemm(w.data_ptr(), int(M), int(K), bhi.data_ptr(), blo.data_ptr(), int(N), y.data_ptr(),
-                           r.data_ptr() if r is not None else None, _stream_ptr(stream))
+                           r.data_ptr() if r is not None else None, st.data_ptr(), _stream_ptr(stream))
     if rc != 0:
         raise MKError(rc, f"mk_tc_gemm returned {rc}")
+    if status is None and int(st.item()) != 0:
+        raise MKError(MK_ERR_TIMEOUT, "a bounded wait of the tensor-core contraction expired")
 
 
 class Megakernel:

@@ -26,7 +26,8 @@ extern "C" cudaError_t mk_kernel_configure(void);
 extern "C" cudaError_t mk_kernel_launch(const mk::Params *p, int n_sm, int cooperative,
                                         cudaStream_t stream);
 extern "C" cudaError_t mk_kernel_occupancy(int *blocks_per_sm);
-extern "C" cudaError_t mk_convert_bf16_f16(const void *src, void *dst, size_t n, cudaStream_t stream);
+extern "C" cudaError_t mk_convert_bf16_f16(const void *src, void *dst, size_t n, unsigned long long *out_of_range,
+                                           cudaStream_t stream);
 extern "C" cudaError_t mk_noise_launch(int n, int pos, int slot, uint64_t seed, const uint32_t *words,
                                        uint32_t *out_words, float *out_noise, cudaStream_t stream);
 
@@ -770,12 +771,20 @@ int mk_create(const mk_config *config, const mk_weights *w, const mk_kv_cache *k
         std::vector<mk_layer_weights> lw16(c.n_layers);
         mk_weights w16 = *w;
         uint16_t *lm16 = nullptr;
-        e = cudaMalloc(&h->w16, n16 * 2);
+        // the copy is exact for magnitudes in fp16's normal range; a weight
+        // beyond fp16's largest finite value would become an infinity, so
+        // such a model keeps sequence-by-sequence batches
+        unsigned long long *d_oor = nullptr;
+        e = cudaMalloc(&h->w16, n16 * 2 + 256);
+        if (e == cudaSuccess) {
+            d_oor = reinterpret_cast<unsigned long long *>(static_cast<char *>(h->w16) + ((n16 * 2 + 255) & ~size_t(255)));
+            e = cudaMemset(d_oor, 0, sizeof(unsigned long long));
+        }
         if (e == cudaSuccess) {
             uint16_t *dst = static_cast<uint16_t *>(h->w16);
             auto copy = [&](const void *src, size_t n) -> const void * {
                 uint16_t *at = dst;
-                if (e == cudaSuccess) e = mk_convert_bf16_f16(src, at, n, nullptr);
+                if (e == cudaSuccess) e = mk_convert_bf16_f16(src, at, n, d_oor, nullptr);
                 dst += n;
                 return at;
             };
@@ -793,6 +802,9 @@ int mk_create(const mk_config *config, const mk_weights *w, const mk_kv_cache *k
             }
             lm16 = const_cast<uint16_t *>(static_cast<const uint16_t *>(copy(w->embed, (size_t)c.vocab * d)));
             if (e == cudaSuccess) e = cudaDeviceSynchronize();
+            unsigned long long oor = 0;
+            if (e == cudaSuccess) e = cudaMemcpy(&oor, d_oor, sizeof oor, cudaMemcpyDeviceToHost);
+            if (e == cudaSuccess && oor != 0) e = cudaErrorInvalidValue;  // out of fp16 range: no fused batches
             w16.layers = lw16.data();
             // the image's layer table points at the copies
             for (int l = 0; l < c.n_layers; ++l) {
@@ -804,7 +816,8 @@ int mk_create(const mk_config *config, const mk_weights *w, const mk_kv_cache *k
         }
         if (e == cudaSuccess) e = cudaMalloc(&h->bdev_mem, h->bim.total);
         if (e != cudaSuccess) {
-            // no room for the batched step: batches run sequence by sequence
+            // no room for the batched step, or a weight beyond fp16's range:
+            // batches run sequence by sequence
             cudaGetLastError();
             if (h->w16) cudaFree(h->w16);
             h->w16 = nullptr;

@@ -50,16 +50,29 @@ extern "C" cudaError_t mk_kernel_occupancy(int *blocks_per_sm) {
 }
 
 namespace {
-// bf16 -> fp16, round to nearest (exact for magnitudes in fp16's normal range)
-__global__ void bf16_to_f16(const uint16_t *__restrict__ src, uint16_t *__restrict__ dst, size_t n) {
-    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
-        dst[i] = __half_as_ushort(__float2half_rn(__uint_as_float((uint32_t)src[i] << 16)));
+// bf16 -> fp16, round to nearest (exact for magnitudes in fp16's normal
+// range); values whose magnitude exceeds fp16's largest finite value (which
+// would become infinities) are counted in *out_of_range.
+__global__ void bf16_to_f16(const uint16_t *__restrict__ src, uint16_t *__restrict__ dst, size_t n,
+                            unsigned long long *out_of_range) {
+    unsigned long long bad = 0;
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+        const float v = __uint_as_float((uint32_t)src[i] << 16);
+        const __half h = __float2half_rn(v);
+        bad += (fabsf(v) <= 3.402823466e38f && __hisinf(h)) ? 1ull : 0ull;
+        dst[i] = __half_as_ushort(h);
+    }
+    if (bad) atomicAdd(out_of_range, bad);
 }
 }  // namespace
 
-// fp16 copy of n bf16 values (device pointers), on `stream`.
-extern "C" cudaError_t mk_convert_bf16_f16(const void *src, void *dst, size_t n, cudaStream_t stream) {
+// fp16 copy of n bf16 values (device pointers), on `stream`; out_of_range
+// (device counter, nullable) accumulates the values beyond fp16's range.
+extern "C" cudaError_t mk_convert_bf16_f16(const void *src, void *dst, size_t n, unsigned long long *out_of_range,
+                                           cudaStream_t stream) {
     if (n == 0) return cudaSuccess;
-    bf16_to_f16<<<1024, 256, 0, stream>>>(static_cast<const uint16_t *>(src), static_cast<uint16_t *>(dst), n);
+    if (!out_of_range) return cudaErrorInvalidValue;
+    bf16_to_f16<<<1024, 256, 0, stream>>>(static_cast<const uint16_t *>(src), static_cast<uint16_t *>(dst), n,
+                                          out_of_range);
     return cudaGetLastError();
 }

@@ -619,8 +619,8 @@ cudaError_t run(const Model &m, const Scratch &sc, const int32_t *d_tokens, int 
 
 // Unit entry of the tensor-core contraction (tests and measurement).
 extern "C" int mk_tc_gemm(const void *d_w, int32_t M, int32_t K, const void *d_bhi, const void *d_blo, int32_t N,
-                          float *d_y, const float *d_r, void *stream) {
-    if (!d_w || !d_bhi || !d_blo || !d_y || M < 1 || N < 1 || K < 64 || K % 64) return -1;
+                          float *d_y, const float *d_r, int32_t *d_status, void *stream) {
+    if (!d_w || !d_bhi || !d_blo || !d_y || !d_status || M < 1 || N < 1 || K < 64 || K % 64) return -1;
     if ((reinterpret_cast<uintptr_t>(d_w) | reinterpret_cast<uintptr_t>(d_bhi) | reinterpret_cast<uintptr_t>(d_blo)) & 15u)
         return -1;
     CUtensorMap wm;
@@ -628,15 +628,7 @@ extern "C" int mk_tc_gemm(const void *d_w, int32_t M, int32_t K, const void *d_b
     int dev = 0, n_sm = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return -2;
-    static int *err = nullptr;  // per-process status word of the unit entry
-    if (!err && cudaMalloc(&err, sizeof(int)) != cudaSuccess) return -6;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (cudaMemsetAsync(err, 0, sizeof(int), s) != cudaSuccess) return -2;
-    const cudaError_t e = mkpf::gemm(wm, d_bhi, d_blo, M, N, K, d_y, M, d_r, err, n_sm, s);
-    if (e != cudaSuccess) return -2;
-    int h = 0;
-    if (cudaMemcpyAsync(&h, err, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
-        cudaStreamSynchronize(s) != cudaSuccess)
-        return -2;
-    return h ? -5 : 0;
+    const cudaError_t e = mkpf::gemm(wm, d_bhi, d_blo, M, N, K, d_y, M, d_r, d_status, n_sm,
+                                     static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? 0 : -2;
 }

@@ -97,8 +97,9 @@ typedef struct mk_handle mk_handle;
  * partials, dependency counters, queues, RoPE table) and uploads them.
  * With max_batch > 1 and head_dim 64 it also plans the fused batched step
  * and keeps, for it, an fp16 copy of every GEMV weight and of the LM head
- * (2 bytes per weight, owned by the handle); if that does not fit, batches
- * run sequence by sequence instead. Synchronous. On success *out receives
+ * (2 bytes per weight, owned by the handle; exact for magnitudes in fp16's
+ * normal range); if that does not fit, or a weight lies beyond fp16's
+ * largest finite value (65504), batches run sequence by sequence instead. Synchronous. On success *out receives
  * the handle.
  * Source: the article "Revolution der KI-Beschleunigung: Wie ein Low-Latency
  * Megakernel den Llama-1B Turbo zündet" (dasgeld.co), paragraph on the
@@ -185,14 +186,14 @@ int mk_prefill(mk_handle *h, const int32_t *d_tokens, int32_t n, int32_t start_p
  * d_y[n][m] = sum_k W[m][k] (Bhi[n][k] + Blo[n][k]) (+ d_r[n][m] if d_r is
  * not NULL; d_r may equal d_y) for m < M, n < N, with W = d_w bf16 [M][K],
  * Bhi = d_bhi and Blo = d_blo bf16 [N][K], d_y / d_r fp32 [N][M]; K a
- * multiple of 64, all pointers 16-byte aligned. Synchronous (waits for
- * `stream`). Returns 0, -1 for bad arguments, -2 for a CUDA error, -4 if
- * the tensor maps cannot be made, -5 if an in-kernel wait expired, -6 if
- * its status word cannot be allocated (first call only).
+ * multiple of 64, all pointers 16-byte aligned. d_status (device int32,
+ * zeroed by the caller) becomes non-zero if an in-kernel wait expires.
+ * Asynchronous on `stream`. Returns 0, -1 for bad arguments, -2 for a CUDA
+ * error, -4 if the tensor maps cannot be made.
  * Source: as mk_prefill; a unit entry of this library for tests and
  * measurement. */
 int mk_tc_gemm(const void *d_w, int32_t M, int32_t K, const void *d_bhi, const void *d_blo, int32_t N, float *d_y,
-               const float *d_r, void *stream);
+               const float *d_r, int32_t *d_status, void *stream);
 
 /* The same step as a chain of separate kernel launches, one per stage
  * (QKV, attention, O-projection, gate/up, down per layer; LM head), with the

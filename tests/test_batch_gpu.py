@@ -181,3 +181,35 @@ def test_tiny_batch4_three_splits_and_a_ragged_tile(cuda_dev):
     prompts = [synth.prompt_tokens(TINY.vocab, 2, seq=b) for b in range(4)]
     run_lockstep(bp, prompts, 4, start_pos=1100)
     bp.close()
+
+
+def test_weights_beyond_fp16_range_keep_sequence_by_sequence_batches(cuda_dev):
+    # One weight beyond fp16's largest finite value (65504) would become an
+    # infinity in the batched step's fp16 copy, so the handle runs batches
+    # one sequence at a time: bit for bit the single-sequence step.
+    build()
+    dev = torch.device("cuda:0")
+    w = synth.make_weights(TINY, dev, 0)
+    w["layers"][1]["w_up"][3, 5] = 70000.0
+    k2, v2 = synth.kv_cache(TINY, 8, 2, dev)
+    k1, v1 = synth.kv_cache(TINY, 8, 1, dev)
+    batched = _lib.Megakernel(TINY, w, k2, v2)
+    single = _lib.Megakernel(TINY, w, k1, v1)
+    toks = torch.tensor([7, 7], dtype=torch.int32, device=dev)
+    pos = torch.zeros(2, dtype=torch.int32, device=dev)
+    out = torch.zeros(2, dtype=torch.int32, device=dev)
+    lb = torch.empty(2, TINY.vocab, device=dev)
+    o1 = torch.zeros(1, dtype=torch.int32, device=dev)
+    l1 = torch.empty(TINY.vocab, device=dev)
+    for step, tok in enumerate([7, 8, 9]):
+        toks.fill_(tok)
+        pos.fill_(step)
+        batched.step_batch(toks, pos, out, lb)
+        single.step(tok, step, o1, l1)
+        torch.cuda.synchronize()
+        assert batched.status() == 0 and single.status() == 0
+        assert torch.isfinite(lb).all()
+        torch.testing.assert_close(lb[0], l1, rtol=0, atol=0)
+        torch.testing.assert_close(lb[1], l1, rtol=0, atol=0)
+    batched.close()
+    single.close()
