@@ -44,6 +44,8 @@ def parse():
                     help="budget of each timed oracle CPU-baseline sample (all cores, one thread); 0 skips it")
     ap.add_argument("--profile", action="store_true",
                     help="only W warm-up and K decode steps (for ncu captures); prints one line")
+    ap.add_argument("--profile-prefill", action="store_true",
+                    help="only W + K prefills of the workload's prompt (for ncu captures); prints one line")
     ap.add_argument("--profile-gemm", action="store_true",
                     help="only W + K runs of the prefill's gate contraction (tensor cores) for the "
                          "workload's prompt (for ncu captures); prints one line")
@@ -412,6 +414,29 @@ def run_profile_gemm(args):
           flush=True)
 
 
+def run_profile_prefill(args):
+    """W + K prefills (mk_prefill) of the workload's prompt, nothing else."""
+    import torch
+    from decode_megakernel_llama_gb300 import _lib, synth
+    from decode_megakernel_llama_gb300.build import build
+    from decode_megakernel_llama_gb300.configs import WORKLOADS
+    build()
+    dev = torch.device("cuda", 0)
+    wl = WORKLOADS[args.workload]
+    shape, P = wl.shape, wl.prompt_len
+    w = synth.make_weights(shape, dev, 0)
+    kc, vc = synth.kv_cache(shape, P + 1, 1, dev)
+    mk = _lib.Megakernel(shape, w, kc, vc)
+    toks = synth.prompt_tokens(shape.vocab, P).to(dev)
+    tok = torch.zeros(1, dtype=torch.int32, device=dev)
+    for _ in range(args.warmup + args.steps):
+        mk.prefill(toks, 0, tok)
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_prefill": True, "status": mk.status(), "prefills": args.warmup + args.steps}),
+          flush=True)
+    mk.close()
+
+
 def run_batch(args, ws, rank, local):
     """The batched workload (llama1b_b8): B sequences per step in one launch
     (mk_decode_step_batch), their caches pre-filled with seeded keys/values up
@@ -716,6 +741,8 @@ def main():
         run_reference(args, ws, rank)
     elif args.profile_gemm:
         run_profile_gemm(args)
+    elif args.profile_prefill:
+        run_profile_prefill(args)
     elif WORKLOADS[args.workload].batch > 1:
         run_batch(args, ws, rank, local)
     else:

@@ -25,9 +25,9 @@
 
 namespace {
 
-constexpr int kW2Warps = 16;
+constexpr int kW2Warps = 8;
 constexpr int kW2Threads = kW2Warps * 32;
-constexpr int kW2Chunks = 8;  // 16-byte weight chunks a lane has in flight (rows x chunks per row)
+constexpr int kW2Rows = 8;  // rows of a batch (one 16-byte chunk of each per lane); two batches in flight
 
 __device__ __forceinline__ float warp_max_f(float v) {
 #pragma unroll
@@ -60,16 +60,36 @@ __device__ __forceinline__ int dot_chunk(const uint4 w, const uint32_t (&xq)[16]
     return acc;
 }
 
-// cols = NC * 2048: lane l of a warp owns elements (c * 32 + l) * 64 .. +64
-// of every row for c < NC, i.e. one 16-byte chunk of packed weights per c,
-// and keeps their 64 activation codes in 16 registers per c.
-template <int NC>
-__global__ void __launch_bounds__(kW2Threads) w2a8_gemv_kernel(const uint4 *__restrict__ W, float beta, int rows,
-                                                              const float *__restrict__ x, float *__restrict__ y) {
-    constexpr int K = NC * 2048;
-    constexpr int R = kW2Chunks / NC;  // rows a warp has in flight
+// Reduce-scatter of 8 per-lane integers over the warp: afterwards lane l
+// holds the warp sum of value (l >> 2) & 7 (9 shuffles for 8 rows).
+__device__ __forceinline__ int warp_reduce8(const int (&a)[8]) {
+    const int lane = threadIdx.x & 31;
+    const bool h16 = (lane & 16) != 0, h8 = (lane & 8) != 0, h4 = (lane & 4) != 0;
+    int b[4], c[2];
+#pragma unroll
+    for (int v = 0; v < 4; ++v) b[v] = (h16 ? a[v + 4] : a[v]) + __shfl_xor_sync(0xFFFFFFFFu, h16 ? a[v] : a[v + 4], 16);
+#pragma unroll
+    for (int v = 0; v < 2; ++v) c[v] = (h8 ? b[v + 2] : b[v]) + __shfl_xor_sync(0xFFFFFFFFu, h8 ? b[v] : b[v + 2], 8);
+    int e = (h4 ? c[1] : c[0]) + __shfl_xor_sync(0xFFFFFFFFu, h4 ? c[0] : c[1], 4);
+    e += __shfl_xor_sync(0xFFFFFFFFu, e, 2);
+    return e + __shfl_xor_sync(0xFFFFFFFFu, e, 1);
+}
+
+// cols = KS * 2048. A row is KS slices of 2048 elements; warp (rg, ks) of a
+// block takes slice ks of kW2Rows rows at a time (row group rg), so each
+// lane holds the 64 activation codes of one 16-byte weight chunk in 16
+// registers and has kW2Rows chunks in flight. The slices' integer sums meet
+// in shared memory (exact), and one scale turns them into y.
+template <int KS>
+__global__ void __launch_bounds__(kW2Threads, 2) w2a8_gemv_kernel(const uint4 *__restrict__ W, float beta, int rows,
+                                                                 const float *__restrict__ x, float *__restrict__ y) {
+    constexpr int K = KS * 2048;
+    constexpr int RG = kW2Warps / KS;  // row groups per block (warps beyond RG * KS idle)
     __shared__ float wmax[kW2Warps];
+    __shared__ int part[kW2Warps][kW2Rows];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int rg = warp / KS, ks = warp % KS;
+    const bool active = rg < RG;
     // per-token absmax of x (every block computes it: x is K floats)
     float am = 0.f;
     for (int i = tid; i < K; i += kW2Threads) am = fmaxf(am, fabsf(x[i]));
@@ -80,12 +100,11 @@ __global__ void __launch_bounds__(kW2Threads) w2a8_gemv_kernel(const uint4 *__re
 #pragma unroll
     for (int w = 0; w < kW2Warps; ++w) am = fmaxf(am, wmax[w]);
     const float s = 127.0f / fmaxf(am, 1e-5f);
-    // this lane's activation codes
-    uint32_t xq[NC][16];
+    // this lane's activation codes: elements ks * 2048 + lane * 64 .. +64
+    uint32_t xq[16];
     int xs = 0;
-#pragma unroll
-    for (int c = 0; c < NC; ++c) {
-        const float4 *src = reinterpret_cast<const float4 *>(x + (c * 32 + lane) * 64);
+    {
+        const float4 *src = reinterpret_cast<const float4 *>(x + ks * 2048 + lane * 64);
 #pragma unroll
         for (int w = 0; w < 16; ++w) {
             const float4 v = src[w];
@@ -97,36 +116,51 @@ __global__ void __launch_bounds__(kW2Threads) w2a8_gemv_kernel(const uint4 *__re
                 xs += q;
                 word |= (uint32_t)(q & 0xFF) << (8 * i);
             }
-            xq[c][w] = word;
+            xq[w] = word;
         }
     }
-    xs = warp_sum_i(xs);  // the warp's lanes cover all K elements
+    xs = warp_sum_i(xs);  // the slice's code sum
     const float fscale = beta / s;
-    // rows, R at a time per warp, all their loads in flight together
-    const int nwarps = gridDim.x * kW2Warps;
-    for (int r0 = (blockIdx.x * kW2Warps + warp) * R; r0 < rows; r0 += nwarps * R) {
-        uint4 wv[R][NC];
+    // rows in batches of kW2Rows per warp; the next batch's loads go out
+    // before the current batch is multiplied (two batches in flight)
+    const int step = gridDim.x * RG * kW2Rows;
+    auto load_batch = [&](int r0, uint4 (&wv)[kW2Rows]) {
+        const int rb = r0 + rg * kW2Rows;
 #pragma unroll
-        for (int k = 0; k < R; ++k) {
-            const int r = r0 + k < rows ? r0 + k : rows - 1;
-            const uint4 *row = W + (size_t)r * (K / 64);
-#pragma unroll
-            for (int c = 0; c < NC; ++c) wv[k][c] = ld_stream(row + c * 32 + lane);
+        for (int k = 0; k < kW2Rows; ++k) {
+            const int r = rb + k < rows ? rb + k : rows - 1;
+            wv[k] = ld_stream(W + (size_t)r * (K / 64) + ks * 32 + lane);
         }
+    };
+    uint4 cur[kW2Rows], nxt[kW2Rows];
+    int r0 = blockIdx.x * RG * kW2Rows;
+    if (active && r0 < rows) load_batch(r0, cur);
+    for (; r0 < rows; r0 += step) {
+        if (active) {
+            if (r0 + step < rows) load_batch(r0 + step, nxt);
+            int acc[kW2Rows];
 #pragma unroll
-        for (int k = 0; k < R; ++k) {
-            int acc = 0;
+            for (int k = 0; k < kW2Rows; ++k) acc[k] = dot_chunk(cur[k], xq, 0);
+            const int sum = warp_reduce8(acc);
+            if ((lane & 3) == 0) part[warp][lane >> 2] = sum - xs;
 #pragma unroll
-            for (int c = 0; c < NC; ++c) acc = dot_chunk(wv[k][c], xq[c], acc);
-            acc = warp_sum_i(acc);
-            if (lane == 0 && r0 + k < rows) y[r0 + k] = (float)(acc - xs) * fscale;
+            for (int k = 0; k < kW2Rows; ++k) cur[k] = nxt[k];
         }
+        __syncthreads();
+        if (tid < RG * kW2Rows) {
+            const int g = tid / kW2Rows, k = tid % kW2Rows, r = r0 + g * kW2Rows + k;
+            int tot = 0;
+#pragma unroll
+            for (int q = 0; q < KS; ++q) tot += part[g * KS + q][k];
+            if (r < rows) y[r] = (float)tot * fscale;
+        }
+        __syncthreads();
     }
 }
 
-template <int NC>
-cudaError_t launch_nc(const uint4 *W, float beta, int rows, const float *x, float *y, int grid, cudaStream_t s) {
-    w2a8_gemv_kernel<NC><<<grid, kW2Threads, 0, s>>>(W, beta, rows, x, y);
+template <int KS>
+cudaError_t launch_ks(const uint4 *W, float beta, int rows, const float *x, float *y, int grid, cudaStream_t s) {
+    w2a8_gemv_kernel<KS><<<grid, kW2Threads, 0, s>>>(W, beta, rows, x, y);
     return cudaGetLastError();
 }
 
@@ -173,17 +207,18 @@ int mk_w2a8_gemv(const uint32_t *d_packed, float beta, int32_t rows, int32_t col
     int dev = 0, n_sm = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return MK_ERR_CUDA;
-    const int per_block = kW2Warps * (kW2Chunks / (cols / 2048));
+    const int ks = cols / 2048;
+    const int per_block = (kW2Warps / ks) * kW2Rows;
     int grid = (rows + per_block - 1) / per_block;
     if (grid > 2 * n_sm) grid = 2 * n_sm;  // two resident blocks per SM, rows strided over them
     const uint4 *W = reinterpret_cast<const uint4 *>(d_packed);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
-    switch (cols / 2048) {
-        case 1: e = launch_nc<1>(W, beta, rows, d_x, d_y, grid, s); break;
-        case 2: e = launch_nc<2>(W, beta, rows, d_x, d_y, grid, s); break;
-        case 3: e = launch_nc<3>(W, beta, rows, d_x, d_y, grid, s); break;
-        default: e = launch_nc<4>(W, beta, rows, d_x, d_y, grid, s); break;
+    switch (ks) {
+        case 1: e = launch_ks<1>(W, beta, rows, d_x, d_y, grid, s); break;
+        case 2: e = launch_ks<2>(W, beta, rows, d_x, d_y, grid, s); break;
+        case 3: e = launch_ks<3>(W, beta, rows, d_x, d_y, grid, s); break;
+        default: e = launch_ks<4>(W, beta, rows, d_x, d_y, grid, s); break;
     }
     return e == cudaSuccess ? MK_OK : MK_ERR_CUDA;
 }
