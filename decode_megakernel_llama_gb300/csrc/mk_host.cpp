@@ -992,8 +992,14 @@ int mk_prefill(mk_handle *h, const int32_t *d_tokens, int32_t n, int32_t start_p
         // scratch for n tokens: residual, q|k|v, attention output, gate, up
         // (fp32) and the hi/lo bf16 operand of the next contraction
         const size_t kmax = std::max(std::max(d, qd), F), qkv = qd + 2 * kvd;
+        // K-split partials: the largest any of the layer's contractions uses
+        const int nsm = h->im.n_sm;
+        size_t work = 0;
+        const int shapes[4][2] = {{qd, d}, {kvd, d}, {d, qd}, {F, d}};
+        for (const auto &mk_ : shapes) work = std::max(work, mkpf::gemm_workspace_floats(mk_[0], n, mk_[1], nsm));
+        work = std::max(work, mkpf::gemm_workspace_floats(d, n, F, nsm));
         const size_t bytes = 4 * (size_t)n * (d + qkv + qd + 2 * (size_t)F) + 2 * 2 * (size_t)n * kmax +
-                             8 * (size_t)2 * h->im.n_sm + 4 * 256;
+                             8 * (size_t)2 * h->im.n_sm + 4 * work + 4 * 512;
         int32_t err_keep = 0;
         if (h->pf.err) cudaMemcpy(&err_keep, h->pf.err, sizeof err_keep, cudaMemcpyDeviceToHost);
         void *mem = nullptr;
@@ -1020,6 +1026,8 @@ int mk_prefill(mk_handle *h, const int32_t *d_tokens, int32_t n, int32_t start_p
         sc.Ahi = reinterpret_cast<uint16_t *>(take(2 * (size_t)n * kmax));
         sc.Alo = reinterpret_cast<uint16_t *>(take(2 * (size_t)n * kmax));
         sc.keys = reinterpret_cast<unsigned long long *>(take(8 * (size_t)2 * h->im.n_sm));
+        sc.work = reinterpret_cast<float *>(take(4 * work));
+        sc.work_floats = work;
         sc.err = reinterpret_cast<int *>(take(4));
         e = cudaMemcpy(sc.err, &err_keep, sizeof err_keep, cudaMemcpyHostToDevice);
         if (e != cudaSuccess) return cuda_fail(e, "prefill status");

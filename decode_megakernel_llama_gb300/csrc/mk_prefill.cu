@@ -29,6 +29,10 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <stdlib.h>
+
+#include <mutex>
+#include <vector>
 
 #include "mk_prefill.h"
 
@@ -36,9 +40,10 @@ namespace mkpf {
 namespace {
 
 constexpr int kThreads = 128;  // 4 warps: TMA issuer, MMA issuer, and all four for the epilogue
-constexpr int kStages = 4;
+constexpr int kRingBytes = 196608;  // the stage ring: 192 KB of shared memory
 constexpr int kATileBytes = 128 * 128;  // 128 rows x 64 bf16
 constexpr uint64_t kWaitNs = 2000000000ull;
+constexpr int kMaxSplits = 16;
 
 __device__ __forceinline__ uint32_t saddr(const void *p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
 
@@ -157,13 +162,22 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
 // Y: an in-place residual add; or NULL). CTA (i, j) computes rows
 // 128i .. 128i+127 of W for tokens BN*j .. BN*j+BN-1. K % 64 == 0.
 // ---------------------------------------------------------------------------
+// Stages of the ring for a token tile of BN: as many as fit in kRingBytes
+// (8 for BN 32, 6 for 64, 4 for 128), so that enough TMA copies are in
+// flight to hide their latency behind the MMAs.
+template <int BN>
+__host__ __device__ constexpr int stages_for() {
+    return kRingBytes / (kATileBytes + 2 * BN * 128) > 8 ? 8 : kRingBytes / (kATileBytes + 2 * BN * 128);
+}
+
 template <int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tbh,
             const __grid_constant__ CUtensorMap tbl, int M, int N, int K, float *Y, int ldy, const float *R,
-            int *err) {
+            float *part, int *err) {
     constexpr int kBTileBytes = BN * 128;
     constexpr int kStageBytes = kATileBytes + 2 * kBTileBytes;
+    constexpr int kStages = stages_for<BN>();
     constexpr uint32_t kCols = BN < 32 ? 32 : BN;  // tensor-memory columns (a power of two >= 32)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -173,7 +187,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t *tslot = reinterpret_cast<uint32_t *>(done + 1);
     int *issued = reinterpret_cast<int *>(tslot + 1);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int m0 = blockIdx.x * 128, n0 = blockIdx.y * BN, nk = K / 64;
+    const int m0 = blockIdx.x * 128, n0 = blockIdx.y * BN;
+    // K split over gridDim.z CTAs: this one takes 64-wide chunks c0 .. c0+nk-1
+    // and writes its partial sums to part[z][N][M] (summed later in a fixed
+    // order), or with one split the result itself
+    const int nk_all = K / 64, z = blockIdx.z, S = gridDim.z;
+    const int c0 = z * nk_all / S, nk = (z + 1) * nk_all / S - c0;
+    if (S > 1) {
+        Y = part + (size_t)z * N * M;
+        ldy = M;
+        R = nullptr;
+    }
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1);
@@ -201,9 +225,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (kc >= kStages && !mbar_wait(&empty[s], ((kc / kStages) - 1) & 1, err)) break;
             uint8_t *st = sm + s * kStageBytes;
             mbar_expect_tx(&full[s], kStageBytes);
-            tma_load_2d(st, &ta, kc * 64, m0, &full[s]);
-            tma_load_2d(st + kATileBytes, &tbh, kc * 64, n0, &full[s]);
-            tma_load_2d(st + kATileBytes + kBTileBytes, &tbl, kc * 64, n0, &full[s]);
+            tma_load_2d(st, &ta, (c0 + kc) * 64, m0, &full[s]);
+            tma_load_2d(st + kATileBytes, &tbh, (c0 + kc) * 64, n0, &full[s]);
+            tma_load_2d(st + kATileBytes + kBTileBytes, &tbl, (c0 + kc) * 64, n0, &full[s]);
             *issued = kc + 1;
         }
     } else if (warp == 1 && lane == 0) {
@@ -266,9 +290,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+// Y[n][m] = R[n][m] (if any) + sum over z of part[z][n][m], z in order.
+__global__ void sum_splits(const float *part, int S, int N, int M, float *Y, int ldy, const float *R) {
+    const size_t total = (size_t)N * M;
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
+        const size_t n = i / M, m = i % M;
+        float y = R ? R[n * ldy + m] : 0.f;
+        for (int z = 0; z < S; ++z) y += part[(size_t)z * total + i];
+        Y[n * ldy + m] = y;
+    }
+}
+
 template <int BN>
 constexpr int gemm_smem_bytes() {
-    return kStages * (kATileBytes + 2 * BN * 128) + 1024 + 128;
+    return stages_for<BN>() * (kATileBytes + 2 * BN * 128) + 1024 + 256;
 }
 
 // ---------------------------------------------------------------------------
@@ -515,7 +550,7 @@ EncodeTiledFn encoder() {
 
 // Tensor map of a row-major bf16 matrix [rows][K], boxes of 64 x box_rows,
 // 128-byte swizzle (rows past the end read as zeros).
-bool make_map(CUtensorMap *map, const void *ptr, int rows, int K, int box_rows) {
+bool encode_map(CUtensorMap *map, const void *ptr, int rows, int K, int box_rows) {
     EncodeTiledFn enc = encoder();
     if (!enc) return false;
     const cuuint64_t gdim[2] = {(cuuint64_t)K, (cuuint64_t)rows};
@@ -527,38 +562,102 @@ bool make_map(CUtensorMap *map, const void *ptr, int rows, int K, int box_rows) 
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int pick_bn(int M, int N, int n_sm) {
-    // the widest token tile that still gives about one CTA per SM
-    const int mt = (M + 127) / 128;
-    for (int bn : {128, 64})
-        if (mt * ((N + bn - 1) / bn) >= n_sm) return bn;
-    return 32;
+// A map depends only on (address, rows, K, box rows), so encoded maps are
+// kept (a small table, most recent first) and reused: encoding costs more
+// host time than a small contraction takes on the GPU.
+bool make_map(CUtensorMap *map, const void *ptr, int rows, int K, int box_rows) {
+    struct Entry {
+        const void *ptr;
+        int rows, K, box;
+        CUtensorMap map;
+    };
+    static std::mutex mu;
+    static std::vector<Entry> cache;
+    std::lock_guard<std::mutex> lock(mu);
+    for (size_t i = 0; i < cache.size(); ++i)
+        if (cache[i].ptr == ptr && cache[i].rows == rows && cache[i].K == K && cache[i].box == box_rows) {
+            *map = cache[i].map;
+            return true;
+        }
+    Entry e{ptr, rows, K, box_rows, {}};
+    if (!encode_map(&e.map, ptr, rows, K, box_rows)) return false;
+    *map = e.map;
+    if (cache.size() >= 512) cache.erase(cache.begin());
+    cache.push_back(e);
+    return true;
+}
+
+// Launch shape of one contraction. A CTA takes one 128-row weight tile and
+// BN tokens, and every CTA streams all K / 64 chunks of its rows unless K is
+// split; the ring of one CTA fills an SM, so more CTAs than SMs run in two
+// waves. Without a split the token tile is the smallest of 32, 64, 128 whose
+// grid still fits one wave (more CTAs in flight at no extra chunks per CTA).
+// A long reduction (K / 64 >= 64 chunks) is split instead, with token tiles
+// of 128, into as many parts as fit one wave, at least 32 chunks each: the
+// chunk count per CTA, not the CTA count, sets the time there.
+struct GemmShape {
+    int bn, S;
+};
+
+GemmShape pick_shape(int M, int N, int K, int n_sm) {
+    const int rt = (M + 127) / 128, nk = K / 64;
+    GemmShape g{128, 1};
+    if (nk >= 64) {
+        const int ctas = rt * ((N + 127) / 128);
+        int S = n_sm / ctas;
+        if (S > nk / 32) S = nk / 32;
+        if (S > kMaxSplits) S = kMaxSplits;
+        g.S = S < 1 ? 1 : S;
+        return g;
+    }
+    for (int bn = 32; bn <= 128; bn *= 2)
+        if (rt * ((N + bn - 1) / bn) <= n_sm || bn == 128) {
+            g.bn = bn;
+            break;
+        }
+    return g;
 }
 
 template <int BN>
 cudaError_t launch_gemm_bn(const CUtensorMap &ta, const void *bhi, const void *blo, int M, int N, int K, float *Y,
-                           int ldy, const float *R, int *err, cudaStream_t s) {
+                           int ldy, const float *R, float *part, int S, int *err, cudaStream_t s) {
     CUtensorMap th, tl;
     if (!make_map(&th, bhi, N, K, BN) || !make_map(&tl, blo, N, K, BN)) return cudaErrorInvalidValue;
     constexpr int smem = gemm_smem_bytes<BN>();
-    cudaError_t e = cudaFuncSetAttribute(tc_gemm<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    const dim3 grid((M + 127) / 128, (N + BN - 1) / BN);
-    tc_gemm<BN><<<grid, kThreads, smem, s>>>(ta, th, tl, M, N, K, Y, ldy, R, err);
-    return cudaGetLastError();
+    static bool configured = false;
+    if (!configured) {
+        const cudaError_t e = cudaFuncSetAttribute(tc_gemm<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    const dim3 grid((M + 127) / 128, (N + BN - 1) / BN, S);
+    tc_gemm<BN><<<grid, kThreads, smem, s>>>(ta, th, tl, M, N, K, Y, ldy, R, part, err);
+    cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess && S > 1) {
+        sum_splits<<<256, 256, 0, s>>>(part, S, N, M, Y, ldy, R);
+        e = cudaGetLastError();
+    }
+    return e;
 }
 
 }  // namespace
 
 bool encode_weight_map(CUtensorMap *map, const void *w, int rows, int K) { return make_map(map, w, rows, K, 128); }
 
+size_t gemm_workspace_floats(int M, int N, int K, int n_sm) {
+    const GemmShape g = pick_shape(M, N, K, n_sm);
+    return g.S > 1 ? (size_t)g.S * N * M : 0;
+}
+
 cudaError_t gemm(const CUtensorMap &wmap, const void *bhi, const void *blo, int M, int N, int K, float *Y, int ldy,
-                 const float *R, int *err, int n_sm, cudaStream_t s) {
+                 const float *R, float *work, size_t work_floats, int *err, int n_sm, cudaStream_t s) {
     if (K % 64 || M < 1 || N < 1) return cudaErrorInvalidValue;
-    switch (pick_bn(M, N, n_sm)) {
-        case 128: return launch_gemm_bn<128>(wmap, bhi, blo, M, N, K, Y, ldy, R, err, s);
-        case 64: return launch_gemm_bn<64>(wmap, bhi, blo, M, N, K, Y, ldy, R, err, s);
-        default: return launch_gemm_bn<32>(wmap, bhi, blo, M, N, K, Y, ldy, R, err, s);
+    const GemmShape g = pick_shape(M, N, K, n_sm);
+    const int S = (size_t)g.S * N * M > work_floats ? 1 : g.S;  // no room for the partials: one pass
+    switch (g.bn) {
+        case 128: return launch_gemm_bn<128>(wmap, bhi, blo, M, N, K, Y, ldy, R, work, S, err, s);
+        case 64: return launch_gemm_bn<64>(wmap, bhi, blo, M, N, K, Y, ldy, R, work, S, err, s);
+        default: return launch_gemm_bn<32>(wmap, bhi, blo, M, N, K, Y, ldy, R, work, S, err, s);
     }
 }
 
@@ -579,9 +678,9 @@ cudaError_t run(const Model &m, const Scratch &sc, const int32_t *d_tokens, int 
         // attention block
         norm_split<<<n, 256, 0, s>>>(sc.X, d, m.attn_norm[l], m.eps, sc.Ahi, sc.Alo);
         ok(cudaGetLastError());
-        ok(gemm(lm.wq, sc.Ahi, sc.Alo, qd, n, d, sc.QKV, qkv, nullptr, sc.err, m.n_sm, s));
-        ok(gemm(lm.wk, sc.Ahi, sc.Alo, kvd, n, d, sc.QKV + qd, qkv, nullptr, sc.err, m.n_sm, s));
-        ok(gemm(lm.wv, sc.Ahi, sc.Alo, kvd, n, d, sc.QKV + qd + kvd, qkv, nullptr, sc.err, m.n_sm, s));
+        ok(gemm(lm.wq, sc.Ahi, sc.Alo, qd, n, d, sc.QKV, qkv, nullptr, sc.work, sc.work_floats, sc.err, m.n_sm, s));
+        ok(gemm(lm.wk, sc.Ahi, sc.Alo, kvd, n, d, sc.QKV + qd, qkv, nullptr, sc.work, sc.work_floats, sc.err, m.n_sm, s));
+        ok(gemm(lm.wv, sc.Ahi, sc.Alo, kvd, n, d, sc.QKV + qd + kvd, qkv, nullptr, sc.work, sc.work_floats, sc.err, m.n_sm, s));
         rope_append<<<n, 256, 0, s>>>(sc.QKV, n, Hq, Hkv, hd, pos0, m.rope, m.max_seq, m.kc + kv_off, m.vc + kv_off);
         ok(cudaGetLastError());
         const int warps = n * Hq, wpb = 4;
@@ -594,15 +693,15 @@ cudaError_t run(const Model &m, const Scratch &sc, const int32_t *d_tokens, int 
         ok(cudaGetLastError());
         norm_split<<<n, 256, 0, s>>>(sc.ATT, qd, nullptr, 0.f, sc.Ahi, sc.Alo);
         ok(cudaGetLastError());
-        ok(gemm(lm.wo, sc.Ahi, sc.Alo, d, n, qd, sc.X, d, sc.X, sc.err, m.n_sm, s));
+        ok(gemm(lm.wo, sc.Ahi, sc.Alo, d, n, qd, sc.X, d, sc.X, sc.work, sc.work_floats, sc.err, m.n_sm, s));
         // MLP block
         norm_split<<<n, 256, 0, s>>>(sc.X, d, m.mlp_norm[l], m.eps, sc.Ahi, sc.Alo);
         ok(cudaGetLastError());
-        ok(gemm(lm.wg, sc.Ahi, sc.Alo, F, n, d, sc.G, F, nullptr, sc.err, m.n_sm, s));
-        ok(gemm(lm.wu, sc.Ahi, sc.Alo, F, n, d, sc.U, F, nullptr, sc.err, m.n_sm, s));
+        ok(gemm(lm.wg, sc.Ahi, sc.Alo, F, n, d, sc.G, F, nullptr, sc.work, sc.work_floats, sc.err, m.n_sm, s));
+        ok(gemm(lm.wu, sc.Ahi, sc.Alo, F, n, d, sc.U, F, nullptr, sc.work, sc.work_floats, sc.err, m.n_sm, s));
         silu_split<<<1024, 256, 0, s>>>(sc.G, sc.U, (size_t)n * F, sc.Ahi, sc.Alo);
         ok(cudaGetLastError());
-        ok(gemm(lm.wd, sc.Ahi, sc.Alo, d, n, F, sc.X, d, sc.X, sc.err, m.n_sm, s));
+        ok(gemm(lm.wd, sc.Ahi, sc.Alo, d, n, F, sc.X, d, sc.X, sc.work, sc.work_floats, sc.err, m.n_sm, s));
     }
     if (e != cudaSuccess) return e;
     // LM head of the last prompt position
@@ -628,7 +727,21 @@ extern "C" int mk_tc_gemm(const void *d_w, int32_t M, int32_t K, const void *d_b
     int dev = 0, n_sm = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return -2;
-    const cudaError_t e = mkpf::gemm(wm, d_bhi, d_blo, M, N, K, d_y, M, d_r, d_status, n_sm,
+    // the K-split partials of this entry live in a workspace it keeps (grown
+    // when a larger contraction needs more; freed at exit)
+    static float *work = nullptr;
+    static size_t work_floats = 0;
+    const size_t need = mkpf::gemm_workspace_floats(M, N, K, n_sm);
+    if (need > work_floats) {
+        if (work) {
+            cudaDeviceSynchronize();
+            cudaFree(work);
+        }
+        work = nullptr;
+        work_floats = 0;
+        if (cudaMalloc(&work, need * sizeof(float)) == cudaSuccess) work_floats = need;
+    }
+    const cudaError_t e = mkpf::gemm(wm, d_bhi, d_blo, M, N, K, d_y, M, d_r, work, work_floats, d_status, n_sm,
                                      static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? 0 : -2;
 }

@@ -33,14 +33,20 @@ struct Scratch {
     float *X = nullptr, *QKV = nullptr, *ATT = nullptr, *G = nullptr, *U = nullptr;
     uint16_t *Ahi = nullptr, *Alo = nullptr;
     unsigned long long *keys = nullptr;
+    float *work = nullptr;   // K-split partial sums of the contractions
+    size_t work_floats = 0;
     int *err = nullptr;  // 0 ok, 1 a bounded wait expired, 2 a token outside [0, vocab)
 };
 
 bool encode_weight_map(CUtensorMap *map, const void *w, int rows, int K);
 
-// Y[n][m] (+)= W[m][.] . (Bhi[n][.] + Blo[n][.]) on the tensor cores.
+// Y[n][m] (+)= W[m][.] . (Bhi[n][.] + Blo[n][.]) on the tensor cores; work
+// (work_floats floats) holds K-split partial sums (one pass if too small).
 cudaError_t gemm(const CUtensorMap &wmap, const void *bhi, const void *blo, int M, int N, int K, float *Y, int ldy,
-                 const float *R, int *err, int n_sm, cudaStream_t s);
+                 const float *R, float *work, size_t work_floats, int *err, int n_sm, cudaStream_t s);
+
+// Floats of K-split workspace gemm() uses for this shape (0: none).
+size_t gemm_workspace_floats(int M, int N, int K, int n_sm);
 
 // The prompt d_tokens[0 .. n) at positions pos0 .. pos0+n-1 through every
 // layer: K/V rows of every position into the cache, logits of the last
