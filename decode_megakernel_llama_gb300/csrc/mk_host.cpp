@@ -91,6 +91,7 @@ bool make_geo_batch(int K, Geo &g) {
 struct Plan {
     int nb = 1;  // sequences of one step
     int n_sm = 0, S = 1, ppt = 0, n_lm = 0, n_stages = 0;
+    int attn_parts = 1;  // instructions sharing one (kv head, split): its query heads split between them
     mk::CtrLayout cl{};
     Geo geo_qkv{}, geo_o{}, geo_gu{}, geo_down{}, geo_lm{};
     std::vector<std::vector<Instr>> q;
@@ -183,9 +184,7 @@ int build_plan(const mk_config *c, int n_sm, Plan &P, int nb) {
             return fail(MK_ERR_UNSUPPORTED, "no batched LM-head geometry for this model");
     } else {
         // input floats per lane: 32 gives the fewest K-slices per row
-        int mnx = 32;
-        if (const char *env = getenv("MK_MAX_NX")) mnx = std::max(8, std::min(32, atoi(env)));
-        auto geo = [&](int K, Geo &g) { return make_geo(K, g, mnx) || make_geo(K, g, 32); };
+        auto geo = [&](int K, Geo &g) { return make_geo(K, g, 32); };
         if (!geo(d, P.geo_qkv) || !geo(qd, P.geo_o) || !geo(d, P.geo_gu) || !geo(F, P.geo_down) ||
             !geo(d, P.geo_lm))
             return fail(MK_ERR_UNSUPPORTED, "no tile geometry for these input lengths");
@@ -236,8 +235,14 @@ int build_plan(const mk_config *c, int n_sm, Plan &P, int nb) {
     // rows, so it starts as soon as q/k/v are published and its cached
     // keys/values are prefetched at the start of the layer. Long contexts
     // spread attention (and its KV streaming) over every SM instead.
-    const double attn_cost = 2.0 * 2.0 * hd * std::ceil((double)c->max_seq / S) + 4096.0;
-    const bool dedicated_attn = Hkv * S * nb * 4 <= n_sm;
+    // A single sequence whose attention fits few SMs splits each kv head's
+    // query heads over two instructions (two SMs): the attention sits on the
+    // critical path between QKV and O-proj, and its time grows with the heads
+    // one SM scores; both read the kv head's keys and values, one appends.
+    P.attn_parts = (nb == 1 && G % 2 == 0 && Hkv * S * 2 * 4 <= n_sm) ? 2 : 1;
+    const int AP = P.attn_parts;
+    const double attn_cost = (2.0 * 2.0 * hd * std::ceil((double)c->max_seq / S) + 4096.0) / AP;
+    const bool dedicated_attn = Hkv * S * nb * AP * 4 <= n_sm;
     int prev_down = 0;
     for (int l = 0; l < L; ++l) {
         const int st = mk::kStagesPerLayer * l;
@@ -248,7 +253,7 @@ int build_plan(const mk_config *c, int n_sm, Plan &P, int nb) {
             std::vector<int> order(n_sm);
             std::iota(order.begin(), order.end(), 0);
             std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return load[a] < load[b]; });
-            for (int i = 0; i < Hkv * S * nb; ++i) {
+            for (int i = 0; i < Hkv * S * nb * AP; ++i) {
                 attn_sm.push_back(order[i]);
                 excluded[order[i]] = 1;
             }
@@ -286,17 +291,20 @@ int build_plan(const mk_config *c, int n_sm, Plan &P, int nb) {
             set_bytes(in, 2ll * in.a1 * d);
             P.q[ch.sm].push_back(in);
         }
-        // ---- attention: Hkv x S splits (x nb sequences; `mat` = sequence)
+        // ---- attention: Hkv x S splits (x nb sequences; `mat` = sequence; x AP
+        // parts of the query heads, `slot` = part)
         for (int b = 0; b < nb; ++b)
         for (int h = 0; h < Hkv; ++h)
-            for (int s = 0; s < S; ++s) {
-                int sm = dedicated_attn ? attn_sm[(b * Hkv + h) * S + s]
+            for (int s = 0; s < S; ++s)
+            for (int a = 0; a < AP; ++a) {
+                int sm = dedicated_attn ? attn_sm[((b * Hkv + h) * S + s) * AP + a]
                                         : (int)(std::min_element(load.begin(), load.end()) - load.begin());
                 load[sm] += attn_cost;
                 Instr in = mk_instr(mk::OP_ATTN, l, st + 1);
                 in.a0 = h;
                 in.a1 = s;
                 in.mat = b;
+                in.slot = a;
                 in.wait_ctr = cl.qkv_grp + l * Hkv + h;
                 in.wait_target = touch[h];
                 P.q[sm].push_back(in);
@@ -509,6 +517,7 @@ void fill_params(const Image &im, const mk_config *config, const mk_weights *w,
     p.L = c.n_layers; p.d = c.d_model; p.Hq = c.n_heads; p.Hkv = c.n_kv_heads; p.hd = c.head_dim;
     p.F = c.ffn_dim; p.V = c.vocab; p.max_seq = c.max_seq; p.max_batch = c.max_batch;
     p.S = P.S; p.G = c.n_heads / c.n_kv_heads; p.ppt = P.ppt; p.eps = c.rms_eps;
+    p.attn_heads = p.G / P.attn_parts;
     p.n_lm = P.n_lm; p.n_stages = P.n_stages;
     p.nb = P.nb;
     p.geo_qkv = P.geo_qkv; p.geo_o = P.geo_o; p.geo_gu = P.geo_gu; p.geo_down = P.geo_down;

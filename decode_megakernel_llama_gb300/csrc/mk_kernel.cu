@@ -35,7 +35,7 @@ extern "C" cudaError_t mk_kernel_configure(void) {
 
 extern "C" cudaError_t mk_kernel_launch(const mk::Params *p, int n_sm, int cooperative,
                                         cudaStream_t stream) {
-    const void *fn = kernel_for(p->hd, p->G, p->nb > 1);
+    const void *fn = kernel_for(p->hd, p->attn_heads, p->nb > 1);
     if (!fn) return cudaErrorInvalidValue;
     void *args[] = {const_cast<mk::Params *>(p)};
     if (cooperative)

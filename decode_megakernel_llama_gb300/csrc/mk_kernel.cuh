@@ -1894,6 +1894,7 @@ template <int HD, int G>
 __device__ void do_attn_hd(const Params &p, const Ctx &cx, const Instr &in, uint32_t &t, bool &bad) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int l = in.layer, kvh = in.a0, split = in.a1;
+    const int gq0 = kvh * p.G + in.slot * G;  // first query head of this instruction
     const int b = seq_of(p, in), pos = pos_of(p, b);  // sequence of a batched step
     const AttnRange r = attn_range(p, split, pos);
     const int seff = attn_seff(p, pos);
@@ -1920,7 +1921,7 @@ __device__ void do_attn_hd(const Params &p, const Ctx &cx, const Instr &in, uint
         const float *rope = p.rope + (size_t)pos * HD;  // [HD/2][2]
         for (int idx = tid; idx < G * (HD / 2); idx += kConsumerThreads) {
             const int g = idx / (HD / 2), i = idx % (HD / 2);
-            const uint2 *qh = qkv + (size_t)(kvh * G + g) * HD;
+            const uint2 *qh = qkv + (size_t)(gq0 + g) * HD;
             const uint2 *srcs[2] = {qh + i, qh + i + HD / 2};
             float ab[2];
             if (bad || !ll_read_n<2>(p, srcs, ep8, ab) || !CHK(rope + 2 * i, 8, 28) ||
@@ -1955,10 +1956,12 @@ __device__ void do_attn_hd(const Params &p, const Ctx &cx, const Instr &in, uint
                 knew[i + HD / 2] = k1;
                 vnew[i] = v0;
                 vnew[i + HD / 2] = v1;
-                p.kc[cache_off + i] = k0;
-                p.kc[cache_off + i + HD / 2] = k1;
-                p.vc[cache_off + i] = v0;
-                p.vc[cache_off + i + HD / 2] = v1;
+                if (in.slot == 0) {  // one instruction of the kv head appends to the cache
+                    p.kc[cache_off + i] = k0;
+                    p.kc[cache_off + i + HD / 2] = k1;
+                    p.vc[cache_off + i] = v0;
+                    p.vc[cache_off + i + HD / 2] = v1;
+                }
             }
         }
         bad = consumer_sync_any(bad);
@@ -2036,11 +2039,11 @@ __device__ void do_attn_hd(const Params &p, const Ctx &cx, const Instr &in, uint
     consumer_sync();
     // output word of element idx of this kv group's heads (batched steps: interleaved)
     // (batched steps: plain fp32, interleaved, released by the attn_done counter)
-    uint2 *const out = p.attll + (size_t)l * p.Hq * HD + (size_t)kvh * G * HD;
+    uint2 *const out = p.attll + (size_t)l * p.Hq * HD + (size_t)gq0 * HD;
     float *const outf = reinterpret_cast<float *>(p.attll) + (size_t)l * kMaxBatch * p.Hq * HD;
     auto put = [&](int idx, float v) {
         if (p.nb > 1) {
-            float *dst = outf + bofs(b, kvh * G * HD + idx);
+            float *dst = outf + bofs(b, gq0 * HD + idx);
             if (CHK(dst, 4, 27)) *dst = v;
         } else if (CHK(out + idx, 8, 27)) {
             ll_store(out + idx, v, ep8);
@@ -2071,7 +2074,7 @@ __device__ void do_attn_hd(const Params &p, const Ctx &cx, const Instr &in, uint
     }
     // Several splits: publish this split's partial (o unnormalised, m, l) ...
     constexpr int PS = HD + 2;  // partial row in global memory: HD outputs, max, sum
-    uint2 *part = p.partll + (((size_t)l * p.nb + b) * p.Hq + (size_t)kvh * G) * p.S * PS;
+    uint2 *part = p.partll + (((size_t)l * p.nb + b) * p.Hq + (size_t)gq0) * p.S * PS;
     for (int idx = tid; idx < G * PS; idx += kConsumerThreads) {
         const int g = idx / PS, e = idx % PS;
         float M = -INFINITY;

@@ -75,7 +75,7 @@ struct alignas(16) Instr {
     int32_t wait_target;    // ... until it reaches this value
     int32_t sig_ctr, sig_n; // counters [sig_ctr, sig_ctr+sig_n) to bump by 1 when done
     int32_t stage;          // topological stage (QKV(l)=5l ... LMHEAD=5L)
-    int32_t slot;           // LMHEAD: argmax partial slot
+    int32_t slot;           // LMHEAD: argmax partial slot.  ATTN: part of the kv head's query heads
     int32_t bytes_lo, bytes_hi;  // weight bytes streamed (host bookkeeping)
     int32_t pad[3];
 };
@@ -109,6 +109,8 @@ struct CtrLayout {
 struct Params {
     // shape
     int32_t L, d, Hq, Hkv, hd, F, V, max_seq, max_batch, S, G, ppt;
+    int32_t attn_heads;     // query heads of one attention instruction (G, or G/2 when a kv head's
+                            // query heads are split over two instructions)
     float eps;
     int32_t n_lm, n_stages;
     Geo geo_qkv, geo_o, geo_gu, geo_down, geo_lm;

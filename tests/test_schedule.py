@@ -54,15 +54,19 @@ def test_every_output_row_exactly_once(shape, n_sm, max_seq):
     for r in instr:
         op, l = int(r[F_OP]), int(r[F_LAYER])
         if op == OP_ATTN:
-            by[(op, l, int(r[F_A0]))].append((int(r[F_A1]), 1))
+            by[(op, l, int(r[F_A0]), int(r[F_SLOT]))].append((int(r[F_A1]), 1))
         else:
             by[(op, l)].append((int(r[F_A0]), int(r[F_A1])))
-    S = len(by[(OP_ATTN, 0, 0)])
+    S = len(by[(OP_ATTN, 0, 0, 0)])
     assert S >= 1
+    # the query heads of a kv head may be split over parts (slot 0 .. AP-1)
+    AP = len({int(r[F_SLOT]) for r in instr if r[F_OP] == OP_ATTN})
+    assert shape.n_heads // shape.n_kv_heads % AP == 0
     for l in range(shape.n_layers):
         cover(by[(OP_QKV, l)], stacked)
         for h in range(shape.n_kv_heads):
-            cover(by[(OP_ATTN, l, h)], S)
+            for a in range(AP):
+                cover(by[(OP_ATTN, l, h, a)], S)
         cover(by[(OP_OPROJ, l)], shape.d_model)
         cover(by[(OP_GATEUP, l)], shape.ffn_dim)
         cover(by[(OP_DOWN, l)], shape.d_model)
@@ -70,6 +74,17 @@ def test_every_output_row_exactly_once(shape, n_sm, max_seq):
     slots = sorted(int(r[F_SLOT]) for r in instr if r[F_OP] == OP_LMHEAD)
     assert slots == list(range(len(slots)))
     assert max(int(r[F_A1]) for r in instr if r[F_OP] != OP_ATTN) <= 2048
+
+
+def test_query_heads_split_where_attention_is_on_the_critical_path():
+    # one sequence, even group size, attention on few SMs: two instructions per
+    # kv head; odd groups (3B-class) and long contexts (every SM busy) keep one
+    parts = lambda *a: len({int(r[F_SLOT]) for r in plan(*a)[0] if r[F_OP] == OP_ATTN})
+    assert parts(LLAMA_1B, 152, 256) == 2
+    assert parts(LLAMA_3B, 152, 384) == 1
+    assert parts(LLAMA_1B, 148, 8256) == 1
+    instr, _, _ = _lib.plan_inspect(LLAMA_1B, 152, 1024, max_batch=8)
+    assert {int(r[F_SLOT]) for r in instr if r[F_OP] == OP_ATTN} == {0}
 
 
 def signal_counts(instr, shape, S):
@@ -203,7 +218,7 @@ def test_tile_copies_stay_in_bounds(shape, n_sm, max_seq):
     mat_rows = {OP_QKV: qd + 2 * kvd, OP_OPROJ: d, OP_GATEUP: F, OP_DOWN: d, OP_LMHEAD: shape.vocab}
     assert d <= STAGED and qd <= STAGED and F <= STAGED_LONG
     ppt = (PAGE // 2) // (hd * 2)
-    S = sum(1 for r in instr if r[F_OP] == OP_ATTN and r[F_LAYER] == 0 and r[F_A0] == 0)
+    S = sum(1 for r in instr if r[F_OP] == OP_ATTN and r[F_LAYER] == 0 and r[F_A0] == 0 and r[F_SLOT] == 0)
     for r in instr:
         op = int(r[F_OP])
         if op == OP_ATTN:
