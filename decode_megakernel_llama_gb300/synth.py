@@ -129,3 +129,16 @@ def host_ternary_weights(w: dict) -> dict:
             h[b] = lw[b]
         out["layers"].append(h)
     return out
+
+
+def sparse_activations(F: int, sparsity: float, seed: int = 5, device="cpu") -> torch.Tensor:
+    """float32 [F]: exactly round(sparsity * F) zeros at seeded random places,
+    the other entries N(0, 1) (a stand-in for the hidden activations of a
+    ReLU-gated FFN block of a trained model, whose sparsity random weights do
+    not reproduce)."""
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    h = torch.randn(F, generator=g, dtype=torch.float32)
+    nz = int(round(sparsity * F))
+    if nz > 0:
+        h[torch.randperm(F, generator=g)[:nz]] = 0.0
+    return h.to(device)

@@ -367,3 +367,28 @@ class OracleModelW2A8(OracleModel):
 
     def full_forward(self, tokens):
         raise NotImplementedError("the W2A8 oracle steps incrementally only")
+
+
+# ---- activation-sparse FFN ------------------------------------------------
+# The TwELL article (iaexpertos.net, "Sakana AI und NVIDIA: TwELL beschleunigt
+# LLMs um bis zu 21,9 %"), sections "Die Herausforderung der von GPUs
+# ignorierten Sparsity" and the list of what TwELL involves: after a ReLU-type
+# activation most hidden units of an FFN block are exactly zero for a given
+# token, and kernels that process only the non-zero elements skip the work of
+# the zeros without changing the model. The oracle is the dense definition;
+# zero terms add nothing to it, so a kernel that skips them reaches the same
+# sum up to rounding order.
+
+def relu_glu(Wg: np.ndarray, Wu: np.ndarray, x) -> np.ndarray:
+    """Hidden activations of a ReLU-gated FFN: h = max(Wg x, 0) * (Wu x)
+    (Wg, Wu bf16 bits [F][d], x float64 [d]); h_i is exactly 0 where the gate
+    is <= 0."""
+    g = matvec(Wg, x)
+    u = matvec(Wu, x)
+    return np.where(g > 0.0, g, 0.0) * u
+
+
+def down_projection(Wd: np.ndarray, h) -> np.ndarray:
+    """y = Wd h for Wd bf16 bits [d][F] (the layout of the model's down
+    projection) and h float64 [F]."""
+    return matvec(Wd, h)
