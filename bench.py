@@ -46,6 +46,9 @@ def parse():
                     help="only W warm-up and K decode steps (for ncu captures); prints one line")
     ap.add_argument("--profile-prefill", action="store_true",
                     help="only W + K prefills of the workload's prompt (for ncu captures); prints one line")
+    ap.add_argument("--profile-twell", action="store_true",
+                    help="only mk_twell_down over 8 W_down^T copies of the workload's FFN shape at 0, 50 "
+                         "and 90%% zero activations (for ncu captures); prints one line")
     ap.add_argument("--profile-gemm", action="store_true",
                     help="only W + K runs of the prefill's gate contraction (tensor cores) for the "
                          "workload's prompt (for ncu captures); prints one line")
@@ -321,8 +324,9 @@ def bf16_tensor_peak():
 
 def measure_extras(mk, shape, prompt, P, W, dev, stream, decode_us):
     """Prefill of the P-token prompt (mk_prefill), its gate contraction alone
-    (mk_tc_gemm), and the W2A8 GEMV (mk_w2a8_gemv), timed with CUDA events on
-    the launching stream after W warm-up runs."""
+    (mk_tc_gemm), the W2A8 GEMV (mk_w2a8_gemv) and the activation-sparse down
+    projection (mk_twell_down), timed with CUDA events on the launching stream
+    after W warm-up runs."""
     import torch
     from decode_megakernel_llama_gb300 import _lib
     out = {}
@@ -385,7 +389,62 @@ def measure_extras(mk, shape, prompt, P, W, dev, stream, decode_us):
     out["w2a8_gemv"] = {"rows": rows, "cols": cols, "us": wus, "weights_per_s": rows * cols / (wus * 1e-6),
                         "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
                                      "frac": gbs / hbm, "peak_source": hbm_kind, "bytes_per_launch": nbytes}}
+    del packed
+    out["twell_down"] = measure_twell(shape, dev, stream, timed, hbm, hbm_kind)
     return out
+
+
+def measure_twell(shape, dev, stream, timed, hbm, hbm_kind):
+    """mk_twell_down at the model's FFN shape over seeded activations with
+    0, 50 and 90 % zeros; copies of W_down^T (about 256 MB in all, larger than
+    L2) are cycled so that every call reads its rows from HBM. The calls over
+    all copies are captured once in a CUDA graph and the graph is replayed, so
+    the time is the device's (two short kernels per call), not the host's
+    launch rate. Bytes per call: the rows of the non-zero units, h, the row
+    blocks' partial sums written and read back, and y."""
+    import math
+    import torch
+    from decode_megakernel_llama_gb300 import _lib, synth
+    F, d = shape.ffn_dim, shape.d_model
+    ncopy = max(2, math.ceil(256e6 / (F * d * 2)))
+    gen = torch.Generator(device=dev).manual_seed(21)
+    wts = [(torch.randn(F, d, generator=gen, device=dev) * 0.02).to(torch.bfloat16) for _ in range(ncopy)]
+    y = torch.empty(d, device=dev)
+    n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
+    R = min(2048, max(1, -(-F // (2 * n_sm))))  # rows per block, as the unit plans them
+    nb = -(-F // R)
+    res = {}
+    for s in (0.0, 0.5, 0.9):
+        h = synth.sparse_activations(F, s, seed=22).to(dev)
+        for w in wts:  # first calls outside the capture (workspace, kernel attributes)
+            _lib.twell_down(w, h, y, stream=stream)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):  # captured on torch's side stream
+            cap = torch.cuda.current_stream(dev)
+            for w in wts:
+                _lib.twell_down(w, h, y, stream=cap)
+        torch.cuda.synchronize()
+
+        def replay():
+            with torch.cuda.stream(stream):
+                graph.replay()
+        us = timed(replay, 8) / ncopy
+        nnz = int((h != 0).sum().item())
+        nbytes = nnz * d * 2 + F * 4 + 2 * nb * d * 4 + d * 4
+        gbs = nbytes / (us * 1e-6) / 1e9
+        res[f"{s:.2f}"] = {"us": us, "nonzero_units": nnz, "bytes_per_call": nbytes, "achieved_gbs": gbs,
+                           "frac": gbs / hbm}
+    dense_us = res["0.00"]["us"]
+    for v in res.values():
+        v["speedup_vs_dense"] = dense_us / v["us"]
+    half = res["0.50"]
+    return {"F": F, "d": d, "by_sparsity": res,
+            "roofline": {"bound": "hbm", "achieved": half["achieved_gbs"], "peak": hbm, "unit": "GB/s",
+                         "frac": half["frac"], "peak_source": hbm_kind, "bytes_per_launch": half["bytes_per_call"],
+                         "at_sparsity": 0.5},
+            "note": "activations are seeded N(0,1) with exact zeros at random units (a stand-in for a "
+                    "ReLU-gated FFN of a trained model); W_down^T copies cycled, every call reads HBM"}
 
 
 def run_profile_gemm(args):
@@ -435,6 +494,29 @@ def run_profile_prefill(args):
     print(json.dumps({"profile_prefill": True, "status": mk.status(), "prefills": args.warmup + args.steps}),
           flush=True)
     mk.close()
+
+
+def run_profile_twell(args):
+    """24 calls of the activation-sparse down projection (mk_twell_down): 8
+    W_down^T copies of the workload's FFN shape, each at 0, 50 and 90 % zero
+    activations; 48 launches (twell_part, twell_reduce), nothing else timed."""
+    import torch
+    from decode_megakernel_llama_gb300 import _lib, synth
+    from decode_megakernel_llama_gb300.build import build
+    from decode_megakernel_llama_gb300.configs import WORKLOADS
+    build()
+    dev = torch.device("cuda", 0)
+    shape = WORKLOADS[args.workload].shape
+    F, d = shape.ffn_dim, shape.d_model
+    gen = torch.Generator(device=dev).manual_seed(21)
+    wts = [(torch.randn(F, d, generator=gen, device=dev) * 0.02).to(torch.bfloat16) for _ in range(8)]
+    y = torch.empty(d, device=dev)
+    for s in (0.0, 0.5, 0.9):
+        h = synth.sparse_activations(F, s, seed=22).to(dev)
+        for w in wts:
+            _lib.twell_down(w, h, y)
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_twell": True, "calls": 24, "F": F, "d": d}), flush=True)
 
 
 def run_batch(args, ws, rank, local):
@@ -724,6 +806,7 @@ def run_mk(args, ws, rank, local):
             "sampling": sampling_line,
             "prefill": extras.get("prefill") if extras else None,
             "w2a8_gemv": extras.get("w2a8_gemv") if extras else None,
+            "twell_down": extras.get("twell_down") if extras else None,
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
@@ -743,6 +826,8 @@ def main():
         run_profile_gemm(args)
     elif args.profile_prefill:
         run_profile_prefill(args)
+    elif args.profile_twell:
+        run_profile_twell(args)
     elif WORKLOADS[args.workload].batch > 1:
         run_batch(args, ws, rank, local)
     else:

@@ -94,6 +94,8 @@ def load(path: str | None = None):
     L.mk_w2_pack.argtypes = [_VP, ctypes.c_int64, ctypes.c_int64, _VP]
     L.mk_w2_unpack.argtypes = [_VP, ctypes.c_int64, ctypes.c_int64, _VP]
     L.mk_w2a8_gemv.argtypes = [_VP, ctypes.c_float, _I32, _I32, _VP, _VP, _VP]
+    L.mk_twell_down.argtypes = [_VP, _I32, _I32, _VP, _VP, _VP]
+    L.mk_twell_ffn.argtypes = [_VP, _VP, _VP, _I32, _I32, _VP, _VP, _VP, _VP]
     L.mk_prefill.argtypes = [_VP, _VP, _I32, _I32, _VP, _VP, _VP]
     L.mk_tc_gemm.argtypes = [_VP, _I32, _I32, _VP, _VP, _I32, _VP, _VP, _VP, _VP]
     L.mk_destroy.argtypes = [_VP]
@@ -202,6 +204,26 @@ def w2a8_gemv(packed, beta: float, rows: int, cols: int, x, y, stream=None) -> N
     x float32 [cols], y float32 [rows]."""
     check(load().mk_w2a8_gemv(packed.data_ptr(), float(beta), int(rows), int(cols), x.data_ptr(),
                               y.data_ptr(), _stream_ptr(stream)))
+
+
+def twell_down(w_down_t, h, y, stream=None) -> None:
+    """mk_twell_down on CUDA tensors: w_down_t bf16 [F][d], h float32 [F],
+    y float32 [d] = W_down h over the non-zero entries of h."""
+    F, d = w_down_t.shape
+    rc = load().mk_twell_down(w_down_t.data_ptr(), int(F), int(d), h.data_ptr(), y.data_ptr(), _stream_ptr(stream))
+    if rc != 0:
+        raise MKError(rc, f"mk_twell_down returned {rc}")
+
+
+def twell_ffn(w_gate, w_up, w_down_t, x, h, y, stream=None) -> None:
+    """mk_twell_ffn on CUDA tensors: w_gate / w_up bf16 [F][d], w_down_t bf16
+    [F][d], x float32 [d]; writes h float32 [F] = relu(W_gate x) * (W_up x) and
+    y float32 [d] = W_down h."""
+    F, d = w_gate.shape
+    rc = load().mk_twell_ffn(w_gate.data_ptr(), w_up.data_ptr(), w_down_t.data_ptr(), int(F), int(d),
+                             x.data_ptr(), h.data_ptr(), y.data_ptr(), _stream_ptr(stream))
+    if rc != 0:
+        raise MKError(rc, f"mk_twell_ffn returned {rc}")
 
 
 def tc_gemm(w, bhi, blo, y, r=None, status=None, stream=None) -> None:

@@ -12,7 +12,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libmk.so")
 LIB_CHECKED = os.path.join(BUILD, "libmk_checked.so")
 SOURCES = ["mk_kernel_hd64.cu", "mk_kernel_hd128.cu", "mk_kernel.cu", "mk_host.cpp", "mk_noalloc.cu", "mk_w2a8.cu",
-           "mk_prefill.cu"]
+           "mk_prefill.cu", "mk_twell.cu"]
 DEPS = SOURCES + ["mk_kernel.cuh", "mk_plan.h", "mk_internal.h", "mk_prefill.h"]
 
 

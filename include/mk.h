@@ -333,6 +333,35 @@ int mk_w2_unpack(const uint32_t *packed, int64_t rows, int64_t cols, int8_t *q);
 int mk_w2a8_gemv(const uint32_t *d_packed, float beta, int32_t rows, int32_t cols, const float *d_x,
                  float *d_y, void *stream);
 
+/* Activation-sparse down projection of one token: y = W_down h, where only
+ * the hidden units with h_i != 0 are read. d_w_down_t: bf16 W_down
+ * transposed, [F][d] (hidden unit i owns the contiguous row i, so a zero
+ * unit costs no weight bytes); d_h: fp32 [F]; d_y: fp32 [d] (written). The
+ * units are listed and their rows gathered per block of rows, and the
+ * blocks' partial sums added in a fixed order: equal inputs give equal bits,
+ * and the result is the dense product up to fp32 rounding order. d a
+ * multiple of 8 up to 4096; weights and y 16-byte aligned.
+ * Asynchronous on `stream`; the partial sums live in a workspace the unit
+ * keeps (allocated on first use, grown for larger shapes). Returns 0, -1
+ * (bad pointer, size or alignment), -3 (unsupported d), -4 (no workspace) or
+ * -2 (launch failed).
+ * Source: the TwELL article (iaexpertos.net, "Sakana AI und NVIDIA: TwELL
+ * beschleunigt LLMs um bis zu 21,9 %"), sections on the sparsity GPUs ignore
+ * and on kernels that process only the non-zero elements of an FFN layer;
+ * the transposed ("twisted", one row per element) layout is the plain reading
+ * of the name the article gives. */
+int mk_twell_down(const void *d_w_down_t, int32_t F, int32_t d, const float *d_h, float *d_y, void *stream);
+
+/* The ReLU-gated FFN of one token with the sparse down projection:
+ * h = max(W_gate x, 0) * (W_up x) (W_gate, W_up bf16 [F][d], x fp32 [d],
+ * h fp32 [F] written), then y = W_down h over the non-zero units as
+ * mk_twell_down. d one of 256, 512, 1024, 2048, 3072, 4096; alignment and
+ * return values as mk_twell_down.
+ * Source: as mk_twell_down (a ReLU-type gate leaves most hidden units
+ * exactly zero, the sparsity the article's kernels exploit). */
+int mk_twell_ffn(const void *d_w_gate, const void *d_w_up, const void *d_w_down_t, int32_t F, int32_t d,
+                 const float *d_x, float *d_h, float *d_y, void *stream);
+
 /* Optional per-instruction timing: when `enable` is non-zero, every step
  * records %globaltimer stamps per instruction into a device buffer that
  * mk_read_trace copies out (see mk_read_trace).

@@ -69,11 +69,11 @@ def test_kernel_hash_covers_every_source_of_the_megakernel():
     # the committed DRAM-traffic record is matched to the kernel by this hash,
     # so every file that shapes the megakernel's code or plan must be in it
     # (the allocation-free entry point's unit only moves its scratch; the
-    # W2A8 GEMV's and the prefill's units are separate kernels)
+    # W2A8 GEMV's, the prefill's and the sparse FFN's units are separate kernels)
     from decode_megakernel_llama_gb300 import build as mkbuild
     import inspect
     src = inspect.getsource(bench.kernel_sha)
     for f in mkbuild.DEPS:
-        if f in ("mk_noalloc.cu", "mk_internal.h", "mk_w2a8.cu", "mk_prefill.cu", "mk_prefill.h"):
+        if f in ("mk_noalloc.cu", "mk_internal.h", "mk_w2a8.cu", "mk_prefill.cu", "mk_prefill.h", "mk_twell.cu"):
             continue
         assert f'"{f}"' in src, f
