@@ -11,17 +11,21 @@
 //   * the weights are the MMA's A operand (M = 128 output features per CTA),
 //     the prompt's activations the B operand (N = 32 .. 128 tokens per CTA);
 //   * both arrive by TMA (cp.async.bulk.tensor) as 128-byte-swizzled K-major
-//     tiles of 64 elements into a 4-stage shared-memory ring with full/empty
-//     mbarriers;
+//     tiles of 64 elements into a ring of 4 to 8 shared-memory stages with
+//     full/empty mbarriers;
 //   * one thread issues tcgen05.mma (kind::f16, bf16 x bf16 -> fp32) into an
 //     accumulator in tensor memory; tcgen05.commit frees a stage when its
 //     MMAs are done;
 //   * the epilogue reads the accumulator with tcgen05.ld and writes fp32
 //     (adding the residual where the layer has one).
 // The activations enter as two bf16 terms, hi = bf16(x) and lo = bf16(x -
-// hi), both multiplied by the same weight tile (twice the MMAs): x is then
-// carried to about 16 significant bits, so the prefill meets the decode
-// step's parity bar while the weights stay in their stored bf16.
+// hi): x is then carried to about 16 significant bits, so the prefill meets
+// the decode step's parity bar while the weights stay in their stored bf16.
+// A stage holds the hi tile and the lo tile back to back, so one MMA with
+// N = 2 BN multiplies the weight tile by both (hi in accumulator columns
+// 0 .. BN-1, lo in BN .. 2BN-1, added in the epilogue): the loop is bound by
+// the count of MMA instructions (a near-fixed cost each at these sizes), and
+// this halves it.
 //
 // Every wait is bounded (%globaltimer, 2 s); on expiry the kernel records an
 // error in a status word, still drains its copies and frees its tensor
@@ -119,10 +123,11 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t smem_byte_addr) {
 
 // Instruction descriptor of tcgen05.mma kind::f16: D fp32 (bits 4-5 = 1),
 // A and B bf16 (7-9 = 1, 10-12 = 1), both K-major (15, 16 = 0), N >> 3
-// (17-22), M >> 4 (24-28).
-template <int BN>
+// (17-22), M >> 4 (24-28); M = 128, N <= 256.
+template <int N>
 __device__ __forceinline__ constexpr uint32_t idesc_bf16_f32() {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+    static_assert(N % 16 == 0 && N >= 16 && N <= 256, "M = 128 needs N a multiple of 16 up to 256");
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
 }
 
 __device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
@@ -178,7 +183,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int kBTileBytes = BN * 128;
     constexpr int kStageBytes = kATileBytes + 2 * kBTileBytes;
     constexpr int kStages = stages_for<BN>();
-    constexpr uint32_t kCols = BN < 32 ? 32 : BN;  // tensor-memory columns (a power of two >= 32)
+    constexpr uint32_t kCols = 2 * BN < 32 ? 32 : 2 * BN;  // tensor-memory columns: hi, then lo (a power of two >= 32)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *full = reinterpret_cast<uint64_t *>(sm + kStages * kStageBytes);
@@ -231,20 +236,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             *issued = kc + 1;
         }
     } else if (warp == 1 && lane == 0) {
-        // MMA issuer: 4 k-slices of 16 per chunk, the hi and the lo term each
-        constexpr uint32_t idesc = idesc_bf16_f32<BN>();
+        // MMA issuer: 4 k-slices of 16 per chunk; B = the hi tile and the lo
+        // tile that follows it (2 BN rows), one MMA for both terms
+        constexpr uint32_t idesc = idesc_bf16_f32<2 * BN>();
         bool ok = true;
         for (int kc = 0; kc < nk && ok; ++kc) {
             const int s = kc % kStages;
             ok = mbar_wait(&full[s], (kc / kStages) & 1, err);
             if (!ok) break;
             tc_fence_after();
-            const uint32_t a = saddr(sm + s * kStageBytes), bh = a + kATileBytes, bl = bh + kBTileBytes;
+            const uint32_t a = saddr(sm + s * kStageBytes), bh = a + kATileBytes;
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
+            for (int kk = 0; kk < 4; ++kk)
                 umma_bf16(tmem, sw128_desc(a + kk * 32), sw128_desc(bh + kk * 32), idesc, (kc | kk) != 0);
-                umma_bf16(tmem, sw128_desc(a + kk * 32), sw128_desc(bl + kk * 32), idesc, 1u);
-            }
             umma_commit(&empty[s]);
         }
         if (ok) umma_commit(done);
@@ -255,16 +259,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     if (have) {
         const int m = m0 + warp * 32 + lane;
+        const uint32_t row = tmem + ((uint32_t)(warp * 32) << 16);
 #pragma unroll 1
         for (int c = 0; c < BN; c += 16) {
-            uint32_t v[16];
-            tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c, v);
+            uint32_t vh[16], vl[16];
+            tmem_ld16(row + (uint32_t)c, vh);
+            tmem_ld16(row + (uint32_t)(BN + c), vl);
             if (m < M) {
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
                     const int n = n0 + c + i;
                     if (n < N) {
-                        float y = __uint_as_float(v[i]);
+                        float y = __uint_as_float(vh[i]) + __uint_as_float(vl[i]);
                         if (R) y += R[(size_t)n * ldy + m];
                         Y[(size_t)n * ldy + m] = y;
                     }
@@ -588,13 +594,15 @@ bool make_map(CUtensorMap *map, const void *ptr, int rows, int K, int box_rows) 
 }
 
 // Launch shape of one contraction. A CTA takes one 128-row weight tile and
-// BN tokens, and every CTA streams all K / 64 chunks of its rows unless K is
-// split; the ring of one CTA fills an SM, so more CTAs than SMs run in two
-// waves. Without a split the token tile is the smallest of 32, 64, 128 whose
-// grid still fits one wave (more CTAs in flight at no extra chunks per CTA).
-// A long reduction (K / 64 >= 64 chunks) is split instead, with token tiles
-// of 128, into as many parts as fit one wave, at least 32 chunks each: the
-// chunk count per CTA, not the CTA count, sets the time there.
+// BN tokens; its loop costs a near-fixed time per 64-wide chunk (about 140
+// cycles per MMA at M = 128, four MMAs a chunk), so the chunk count per CTA
+// sets the time. The ring of one CTA fills an SM, so more CTAs than SMs run
+// in two waves. Without a split the token tile is the smallest of 32, 64,
+// 128 whose grid still fits one wave (more CTAs in flight at no extra chunks
+// per CTA). Only a long reduction (K / 64 >= 64 chunks) is split, with token
+// tiles of 128, into as many parts as fit one wave, at least 32 chunks each:
+// measured, shorter splits lose more to writing and re-reading the partial
+// sums than they gain in parallel chunks.
 struct GemmShape {
     int bn, S;
 };
