@@ -175,11 +175,22 @@ __host__ __device__ constexpr int stages_for() {
     return kRingBytes / (kATileBytes + 2 * BN * 128) > 8 ? 8 : kRingBytes / (kATileBytes + 2 * BN * 128);
 }
 
+// Up to three weight matrices multiplied by the same activations in one
+// launch: CTA row tiles 0 .. tiles[0]-1 take matrix 0 (tensor map ta0),
+// the next tiles[1] matrix 1 (ta1), then matrix 2 (ta2); each has its own
+// rows, output and residual.
+struct Segs {
+    int n;
+    int tiles[3], M[3], ldy[3];
+    float *Y[3];
+    const float *R[3];
+};
+
 template <int BN>
 __global__ void __launch_bounds__(kThreads, 1)
-    tc_gemm(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tbh,
-            const __grid_constant__ CUtensorMap tbl, int M, int N, int K, float *Y, int ldy, const float *R,
-            float *part, int *err) {
+    tc_gemm(const __grid_constant__ CUtensorMap ta0, const __grid_constant__ CUtensorMap ta1,
+            const __grid_constant__ CUtensorMap ta2, const __grid_constant__ CUtensorMap tbh,
+            const __grid_constant__ CUtensorMap tbl, const Segs sg, int N, int K, float *part, int *err) {
     constexpr int kBTileBytes = BN * 128;
     constexpr int kStageBytes = kATileBytes + 2 * kBTileBytes;
     constexpr int kStages = stages_for<BN>();
@@ -192,8 +203,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t *tslot = reinterpret_cast<uint32_t *>(done + 1);
     int *issued = reinterpret_cast<int *>(tslot + 1);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int m0 = blockIdx.x * 128, n0 = blockIdx.y * BN;
-    // K split over gridDim.z CTAs: this one takes 64-wide chunks c0 .. c0+nk-1
+    int bx = blockIdx.x, q = 0;
+    while (q + 1 < sg.n && bx >= sg.tiles[q]) bx -= sg.tiles[q++];
+    const CUtensorMap *ta = q == 0 ? &ta0 : (q == 1 ? &ta1 : &ta2);
+    const int M = sg.M[q];
+    float *Y = sg.Y[q];
+    int ldy = sg.ldy[q];
+    const float *R = sg.R[q];
+    const int m0 = bx * 128, n0 = blockIdx.y * BN;
+    // K split over gridDim.z CTAs (one matrix only): this one takes 64-wide chunks c0 .. c0+nk-1
     // and writes its partial sums to part[z][N][M] (summed later in a fixed
     // order), or with one split the result itself
     const int nk_all = K / 64, z = blockIdx.z, S = gridDim.z;
@@ -230,7 +248,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (kc >= kStages && !mbar_wait(&empty[s], ((kc / kStages) - 1) & 1, err)) break;
             uint8_t *st = sm + s * kStageBytes;
             mbar_expect_tx(&full[s], kStageBytes);
-            tma_load_2d(st, &ta, (c0 + kc) * 64, m0, &full[s]);
+            tma_load_2d(st, ta, (c0 + kc) * 64, m0, &full[s]);
             tma_load_2d(st + kATileBytes, &tbh, (c0 + kc) * 64, n0, &full[s]);
             tma_load_2d(st + kATileBytes + kBTileBytes, &tbl, (c0 + kc) * 64, n0, &full[s]);
             *issued = kc + 1;
@@ -627,8 +645,8 @@ GemmShape pick_shape(int M, int N, int K, int n_sm) {
 }
 
 template <int BN>
-cudaError_t launch_gemm_bn(const CUtensorMap &ta, const void *bhi, const void *blo, int M, int N, int K, float *Y,
-                           int ldy, const float *R, float *part, int S, int *err, cudaStream_t s) {
+cudaError_t launch_gemm_bn(const CUtensorMap *const *tas, const Segs &sg, const void *bhi, const void *blo, int N,
+                           int K, float *part, int S, int *err, cudaStream_t s) {
     CUtensorMap th, tl;
     if (!make_map(&th, bhi, N, K, BN) || !make_map(&tl, blo, N, K, BN)) return cudaErrorInvalidValue;
     constexpr int smem = gemm_smem_bytes<BN>();
@@ -638,14 +656,31 @@ cudaError_t launch_gemm_bn(const CUtensorMap &ta, const void *bhi, const void *b
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    const dim3 grid((M + 127) / 128, (N + BN - 1) / BN, S);
-    tc_gemm<BN><<<grid, kThreads, smem, s>>>(ta, th, tl, M, N, K, Y, ldy, R, part, err);
+    int tiles = 0;
+    for (int i = 0; i < sg.n; ++i) tiles += sg.tiles[i];
+    const dim3 grid(tiles, (N + BN - 1) / BN, S);
+    const CUtensorMap &a0 = *tas[0], &a1 = sg.n > 1 ? *tas[1] : *tas[0], &a2 = sg.n > 2 ? *tas[2] : *tas[0];
+    tc_gemm<BN><<<grid, kThreads, smem, s>>>(a0, a1, a2, th, tl, sg, N, K, part, err);
     cudaError_t e = cudaGetLastError();
     if (e == cudaSuccess && S > 1) {
-        sum_splits<<<256, 256, 0, s>>>(part, S, N, M, Y, ldy, R);
+        sum_splits<<<256, 256, 0, s>>>(part, S, N, sg.M[0], sg.Y[0], sg.ldy[0], sg.R[0]);
         e = cudaGetLastError();
     }
     return e;
+}
+
+template <int BN>
+cudaError_t launch_one(const CUtensorMap &ta, const void *bhi, const void *blo, int M, int N, int K, float *Y, int ldy,
+                       const float *R, float *part, int S, int *err, cudaStream_t s) {
+    Segs sg{};
+    sg.n = 1;
+    sg.tiles[0] = (M + 127) / 128;
+    sg.M[0] = M;
+    sg.Y[0] = Y;
+    sg.ldy[0] = ldy;
+    sg.R[0] = R;
+    const CUtensorMap *tas[1] = {&ta};
+    return launch_gemm_bn<BN>(tas, sg, bhi, blo, N, K, part, S, err, s);
 }
 
 }  // namespace
@@ -663,9 +698,38 @@ cudaError_t gemm(const CUtensorMap &wmap, const void *bhi, const void *blo, int 
     const GemmShape g = pick_shape(M, N, K, n_sm);
     const int S = (size_t)g.S * N * M > work_floats ? 1 : g.S;  // no room for the partials: one pass
     switch (g.bn) {
-        case 128: return launch_gemm_bn<128>(wmap, bhi, blo, M, N, K, Y, ldy, R, work, S, err, s);
-        case 64: return launch_gemm_bn<64>(wmap, bhi, blo, M, N, K, Y, ldy, R, work, S, err, s);
-        default: return launch_gemm_bn<32>(wmap, bhi, blo, M, N, K, Y, ldy, R, work, S, err, s);
+        case 128: return launch_one<128>(wmap, bhi, blo, M, N, K, Y, ldy, R, work, S, err, s);
+        case 64: return launch_one<64>(wmap, bhi, blo, M, N, K, Y, ldy, R, work, S, err, s);
+        default: return launch_one<32>(wmap, bhi, blo, M, N, K, Y, ldy, R, work, S, err, s);
+    }
+}
+
+cudaError_t gemm_multi(int nseg, const CUtensorMap *const *maps, const int *M, float *const *Y, const int *ldy,
+                       const void *bhi, const void *blo, int N, int K, int *err, int n_sm, cudaStream_t s) {
+    if (K % 64 || N < 1 || nseg < 1 || nseg > 3) return cudaErrorInvalidValue;
+    Segs sg{};
+    sg.n = nseg;
+    int tiles = 0;
+    for (int i = 0; i < nseg; ++i) {
+        if (M[i] < 1) return cudaErrorInvalidValue;
+        sg.tiles[i] = (M[i] + 127) / 128;
+        sg.M[i] = M[i];
+        sg.Y[i] = Y[i];
+        sg.ldy[i] = ldy[i];
+        sg.R[i] = nullptr;
+        tiles += sg.tiles[i];
+    }
+    // the smallest token tile whose grid fits one wave (as pick_shape)
+    int bn = 128;
+    for (int b = 32; b < 128; b *= 2)
+        if (tiles * ((N + b - 1) / b) <= n_sm) {
+            bn = b;
+            break;
+        }
+    switch (bn) {
+        case 32: return launch_gemm_bn<32>(maps, sg, bhi, blo, N, K, nullptr, 1, err, s);
+        case 64: return launch_gemm_bn<64>(maps, sg, bhi, blo, N, K, nullptr, 1, err, s);
+        default: return launch_gemm_bn<128>(maps, sg, bhi, blo, N, K, nullptr, 1, err, s);
     }
 }
 
@@ -686,9 +750,12 @@ cudaError_t run(const Model &m, const Scratch &sc, const int32_t *d_tokens, int 
         // attention block
         norm_split<<<n, 256, 0, s>>>(sc.X, d, m.attn_norm[l], m.eps, sc.Ahi, sc.Alo);
         ok(cudaGetLastError());
-        ok(gemm(lm.wq, sc.Ahi, sc.Alo, qd, n, d, sc.QKV, qkv, nullptr, sc.work, sc.work_floats, sc.err, m.n_sm, s));
-        ok(gemm(lm.wk, sc.Ahi, sc.Alo, kvd, n, d, sc.QKV + qd, qkv, nullptr, sc.work, sc.work_floats, sc.err, m.n_sm, s));
-        ok(gemm(lm.wv, sc.Ahi, sc.Alo, kvd, n, d, sc.QKV + qd + kvd, qkv, nullptr, sc.work, sc.work_floats, sc.err, m.n_sm, s));
+        {  // q, k and v in one launch
+            const CUtensorMap *maps[3] = {&lm.wq, &lm.wk, &lm.wv};
+            const int Ms[3] = {qd, kvd, kvd}, lds[3] = {qkv, qkv, qkv};
+            float *Ys[3] = {sc.QKV, sc.QKV + qd, sc.QKV + qd + kvd};
+            ok(gemm_multi(3, maps, Ms, Ys, lds, sc.Ahi, sc.Alo, n, d, sc.err, m.n_sm, s));
+        }
         rope_append<<<n, 256, 0, s>>>(sc.QKV, n, Hq, Hkv, hd, pos0, m.rope, m.max_seq, m.kc + kv_off, m.vc + kv_off);
         ok(cudaGetLastError());
         const int warps = n * Hq, wpb = 4;
@@ -705,8 +772,12 @@ cudaError_t run(const Model &m, const Scratch &sc, const int32_t *d_tokens, int 
         // MLP block
         norm_split<<<n, 256, 0, s>>>(sc.X, d, m.mlp_norm[l], m.eps, sc.Ahi, sc.Alo);
         ok(cudaGetLastError());
-        ok(gemm(lm.wg, sc.Ahi, sc.Alo, F, n, d, sc.G, F, nullptr, sc.work, sc.work_floats, sc.err, m.n_sm, s));
-        ok(gemm(lm.wu, sc.Ahi, sc.Alo, F, n, d, sc.U, F, nullptr, sc.work, sc.work_floats, sc.err, m.n_sm, s));
+        {  // gate and up in one launch
+            const CUtensorMap *maps[2] = {&lm.wg, &lm.wu};
+            const int Ms[2] = {F, F}, lds[2] = {F, F};
+            float *Ys[2] = {sc.G, sc.U};
+            ok(gemm_multi(2, maps, Ms, Ys, lds, sc.Ahi, sc.Alo, n, d, sc.err, m.n_sm, s));
+        }
         silu_split<<<1024, 256, 0, s>>>(sc.G, sc.U, (size_t)n * F, sc.Ahi, sc.Alo);
         ok(cudaGetLastError());
         ok(gemm(lm.wd, sc.Ahi, sc.Alo, d, n, F, sc.X, d, sc.X, sc.work, sc.work_floats, sc.err, m.n_sm, s));
