@@ -88,6 +88,13 @@ def test_tiny_prefill_in_two_parts_and_a_ragged_token_tile(cuda_dev):
     pair.close()
 
 
+def test_tiny_prefill_beyond_the_staged_attention_rows(cuda_dev):
+    # the second part attends to 300 positions, more than the 256 rows the
+    # staged attention kernel holds: the per-pair attention kernel runs it
+    pair, _, _ = prefill_case(TINY, 300, 304, 2, start_split=200)
+    pair.close()
+
+
 def test_llama1b_prefill_of_the_workload_prompt(cuda_dev):
     wl = WORKLOADS["llama1b"]
     pair, _, _ = prefill_case(LLAMA_1B, wl.prompt_len, wl.max_seq, 4)
