@@ -88,9 +88,9 @@ def test_tiny_prefill_in_two_parts_and_a_ragged_token_tile(cuda_dev):
     pair.close()
 
 
-def test_tiny_prefill_beyond_the_staged_attention_rows(cuda_dev):
-    # the second part attends to 300 positions, more than the 256 rows the
-    # staged attention kernel holds: the per-pair attention kernel runs it
+def test_tiny_prefill_of_a_long_second_part(cuda_dev):
+    # the second part starts at position 200 and attends to up to 300
+    # positions: the cached rows of the first part and its own
     pair, _, _ = prefill_case(TINY, 300, 304, 2, start_split=200)
     pair.close()
 
