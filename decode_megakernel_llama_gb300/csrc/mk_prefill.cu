@@ -478,6 +478,100 @@ __global__ void attend_prefill(const float *QKV, int n, int Hq, int Hkv, int pos
     for (int e = 0; e < DP; ++e) dst[e] = o[e] / l;
 }
 
+// The same causal attention with the kv head's cached rows staged in shared
+// memory: CTA (kv head, block of kQB prompt tokens) copies the keys and
+// values of positions 0 .. Tmax-1 (all the block's tokens see), rows padded
+// by 16 bytes so that the lanes' 16-byte key reads spread over the banks;
+// then warp w takes the (token, query head) pairs w, w + 16, ... of the block
+// (one each for G <= 4). Scores use four partial sums per lane and P.V two
+// per output, to shorten the dependent chains.
+constexpr int kQB = 4;
+constexpr int kMaxStagedPos = 256;
+constexpr int kStagedWarps = 16;
+
+template <int HD>
+__global__ void __launch_bounds__(kStagedWarps * 32) attend_prefill_staged(const float *QKV, int n, int Hq, int Hkv,
+                                                                            int pos0, int max_seq, int Tcap,
+                                                                            const uint16_t *kc, const uint16_t *vc,
+                                                                            float *out) {
+    constexpr int RS = HD + 8;  // row stride in bf16 elements (16 bytes of padding)
+    extern __shared__ uint16_t kvs[];
+    uint16_t *Ks = kvs, *Vs = kvs + (size_t)Tcap * RS;
+    const int kvh = blockIdx.x, t0 = blockIdx.y * kQB, G = Hq / Hkv;
+    const int tl = min(n, t0 + kQB);  // tokens t0 .. tl-1
+    const int Tmax = pos0 + tl;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    {
+        const uint4 *Kg = reinterpret_cast<const uint4 *>(kc + (size_t)kvh * max_seq * HD);
+        const uint4 *Vg = reinterpret_cast<const uint4 *>(vc + (size_t)kvh * max_seq * HD);
+        constexpr int CPR = HD / 8;  // 16-byte chunks per row
+        for (int i = tid; i < Tmax * CPR; i += blockDim.x) {
+            const int r = i / CPR, c = i % CPR;
+            *reinterpret_cast<uint4 *>(Ks + (size_t)r * RS + c * 8) = Kg[(size_t)r * CPR + c];
+            *reinterpret_cast<uint4 *>(Vs + (size_t)r * RS + c * 8) = Vg[(size_t)r * CPR + c];
+        }
+    }
+    __syncthreads();
+    const int stride = (Hq + 2 * Hkv) * HD;
+    const float scale = rsqrtf((float)HD);
+    constexpr int DP = HD / 32;
+    for (int pr = warp; pr < (tl - t0) * G; pr += kStagedWarps) {
+        const int t = t0 + pr / G, h = kvh * G + pr % G;
+        const int T = pos0 + t + 1;
+        const float *q = QKV + (size_t)t * stride + (size_t)h * HD;
+        float qr[HD];
+#pragma unroll
+        for (int i = 0; i < HD; ++i) qr[i] = q[i] * scale;
+        float o[2][DP], m = -INFINITY, l = 0.f;
+#pragma unroll
+        for (int e = 0; e < DP; ++e) o[0][e] = o[1][e] = 0.f;
+        for (int j0 = 0; j0 < T; j0 += 32) {
+            const int j = j0 + lane;
+            float s = -INFINITY;
+            if (j < T) {
+                const uint4 *kr = reinterpret_cast<const uint4 *>(Ks + (size_t)j * RS);
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int c = 0; c < HD / 8; ++c) {
+                    const uint4 w = kr[c];
+                    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        acc[e] = fmaf(__uint_as_float(u[e] << 16), qr[c * 8 + 2 * e], acc[e]);
+                        acc[e] = fmaf(__uint_as_float(u[e] & 0xFFFF0000u), qr[c * 8 + 2 * e + 1], acc[e]);
+                    }
+                }
+                s = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+            }
+            float cm = s;
+            for (int off = 16; off > 0; off >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xFFFFFFFFu, cm, off));
+            const float mn = fmaxf(m, cm);
+            const float corr = __expf(m - mn);
+            const float p = j < T ? __expf(s - mn) : 0.f;
+            float ps = p;
+            for (int off = 16; off > 0; off >>= 1) ps += __shfl_xor_sync(0xFFFFFFFFu, ps, off);
+            l = l * corr + ps;
+            m = mn;
+#pragma unroll
+            for (int e = 0; e < DP; ++e) {
+                o[0][e] *= corr;
+                o[1][e] *= corr;
+            }
+            const int cnt = T - j0 < 32 ? T - j0 : 32;
+            const uint16_t *vb = Vs + (size_t)j0 * RS + lane * DP;
+#pragma unroll 8
+            for (int jj = 0; jj < cnt; ++jj) {
+                const float pj = __shfl_sync(0xFFFFFFFFu, p, jj);
+#pragma unroll
+                for (int e = 0; e < DP; ++e) o[jj & 1][e] = fmaf(pj, bf2f(vb[(size_t)jj * RS + e]), o[jj & 1][e]);
+            }
+        }
+        float *dst = out + (size_t)t * Hq * HD + (size_t)h * HD + lane * DP;
+#pragma unroll
+        for (int e = 0; e < DP; ++e) dst[e] = (o[0][e] + o[1][e]) / l;
+    }
+}
+
 // h = silu(G) * U into hi/lo bf16 terms.
 __global__ void silu_split(const float *Gt, const float *U, size_t count, uint16_t *hi, uint16_t *lo) {
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < count; i += (size_t)gridDim.x * blockDim.x) {
@@ -759,12 +853,32 @@ cudaError_t run(const Model &m, const Scratch &sc, const int32_t *d_tokens, int 
         rope_append<<<n, 256, 0, s>>>(sc.QKV, n, Hq, Hkv, hd, pos0, m.rope, m.max_seq, m.kc + kv_off, m.vc + kv_off);
         ok(cudaGetLastError());
         const int warps = n * Hq, wpb = 4;
-        if (hd == 64)
+        if (pos0 + n <= kMaxStagedPos) {
+            // every position the prompt attends to fits the staged rows
+            const int Tcap = pos0 + n;
+            const dim3 grid(Hkv, (n + kQB - 1) / kQB);
+            const size_t smem = 2 * (size_t)Tcap * (hd + 8) * 2;
+            static bool configured = false;
+            if (!configured) {
+                ok(cudaFuncSetAttribute(attend_prefill_staged<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        2 * kMaxStagedPos * (64 + 8) * 2));
+                ok(cudaFuncSetAttribute(attend_prefill_staged<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        2 * kMaxStagedPos * (128 + 8) * 2));
+                configured = e == cudaSuccess;
+            }
+            if (hd == 64)
+                attend_prefill_staged<64><<<grid, kStagedWarps * 32, smem, s>>>(
+                    sc.QKV, n, Hq, Hkv, pos0, m.max_seq, Tcap, m.kc + kv_off, m.vc + kv_off, sc.ATT);
+            else
+                attend_prefill_staged<128><<<grid, kStagedWarps * 32, smem, s>>>(
+                    sc.QKV, n, Hq, Hkv, pos0, m.max_seq, Tcap, m.kc + kv_off, m.vc + kv_off, sc.ATT);
+        } else if (hd == 64) {
             attend_prefill<64><<<(warps + wpb - 1) / wpb, wpb * 32, 0, s>>>(sc.QKV, n, Hq, Hkv, pos0, m.max_seq,
                                                                            m.kc + kv_off, m.vc + kv_off, sc.ATT);
-        else
+        } else {
             attend_prefill<128><<<(warps + wpb - 1) / wpb, wpb * 32, 0, s>>>(sc.QKV, n, Hq, Hkv, pos0, m.max_seq,
                                                                             m.kc + kv_off, m.vc + kv_off, sc.ATT);
+        }
         ok(cudaGetLastError());
         norm_split<<<n, 256, 0, s>>>(sc.ATT, qd, nullptr, 0.f, sc.Ahi, sc.Alo);
         ok(cudaGetLastError());
