@@ -51,6 +51,15 @@ constexpr int kMaxSplits = 16;
 
 __device__ __forceinline__ uint32_t saddr(const void *p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
 
+// Programmatic dependent launch: the prefill's kernels are launched so that
+// the next one in the stream may start once every CTA of the current one has
+// called pdl_trigger (or exited); it does its set-up (and a contraction its
+// first weight-tile loads, which depend on nothing earlier) and then
+// pdl_wait()s, which returns once the previous grid has completed and its
+// writes are visible. Without the launch attribute both are no-ops.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ uint64_t gtimer() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -240,12 +249,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
+    // the weight tiles of the first stages do not depend on the previous
+    // kernel: their copies go out before the wait for its results
+    const int pre = nk < kStages ? nk : kStages;
+    if (warp == 0 && lane == 0)
+        for (int kc = 0; kc < pre; ++kc) {
+            mbar_expect_tx(&full[kc], kStageBytes);
+            tma_load_2d(sm + kc * kStageBytes, ta, (c0 + kc) * 64, m0, &full[kc]);
+        }
+    pdl_wait();
+    pdl_trigger();
 
     if (warp == 0 && lane == 0) {
-        // TMA issuer: stage s of chunk kc once the MMAs of chunk kc - kStages freed it
-        for (int kc = 0; kc < nk; ++kc) {
+        // TMA issuer: the activations of the first stages, then stage s of
+        // chunk kc once the MMAs of chunk kc - kStages freed it
+        for (int kc = 0; kc < pre; ++kc) {
+            uint8_t *st = sm + kc * kStageBytes;
+            tma_load_2d(st + kATileBytes, &tbh, (c0 + kc) * 64, n0, &full[kc]);
+            tma_load_2d(st + kATileBytes + kBTileBytes, &tbl, (c0 + kc) * 64, n0, &full[kc]);
+            *issued = kc + 1;
+        }
+        for (int kc = pre; kc < nk; ++kc) {
             const int s = kc % kStages;
-            if (kc >= kStages && !mbar_wait(&empty[s], ((kc / kStages) - 1) & 1, err)) break;
+            if (!mbar_wait(&empty[s], ((kc / kStages) - 1) & 1, err)) break;
             uint8_t *st = sm + s * kStageBytes;
             mbar_expect_tx(&full[s], kStageBytes);
             tma_load_2d(st, ta, (c0 + kc) * 64, m0, &full[s]);
@@ -316,6 +342,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // Y[n][m] = R[n][m] (if any) + sum over z of part[z][n][m], z in order.
 __global__ void sum_splits(const float *part, int S, int N, int M, float *Y, int ldy, const float *R) {
+    pdl_wait();
+    pdl_trigger();
     const size_t total = (size_t)N * M;
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
         const size_t n = i / M, m = i % M;
@@ -323,6 +351,24 @@ __global__ void sum_splits(const float *part, int S, int N, int M, float *Y, int
         for (int z = 0; z < S; ++z) y += part[(size_t)z * total + i];
         Y[n * ldy + m] = y;
     }
+}
+
+// Launches a prefill kernel with programmatic stream serialization (see
+// pdl_wait): it may start while the previous kernel of the stream finishes.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
 template <int BN>
@@ -356,6 +402,8 @@ __device__ __forceinline__ float block_sum(float v, float *red) {
 
 // X[t] = float(E[tokens[t]]); a token outside [0, V) sets the error word.
 __global__ void embed_rows(const uint16_t *E, const int32_t *tokens, int n, int d, int V, float *X, int *err) {
+    pdl_wait();
+    pdl_trigger();
     const int t = blockIdx.x;
     const int tok = tokens[t];
     if (tok < 0 || tok >= V) {
@@ -368,6 +416,8 @@ __global__ void embed_rows(const uint16_t *E, const int32_t *tokens, int n, int 
 // hi/lo bf16 terms of rows of X [rows][K] (fp32), optionally RMSNorm'd with gain g.
 __global__ void norm_split(const float *X, int K, const uint16_t *g, float eps, uint16_t *hi, uint16_t *lo) {
     __shared__ float red[32];
+    pdl_wait();
+    pdl_trigger();
     const int t = blockIdx.x;
     const float *x = X + (size_t)t * K;
     float scale = 1.f;
@@ -389,6 +439,8 @@ __global__ void norm_split(const float *X, int K, const uint16_t *g, float eps, 
 // kept (rotated) in place, bf16 k and v written into the cache at the position.
 __global__ void rope_append(float *QKV, int n, int Hq, int Hkv, int hd, int pos0, const float *rope, int max_seq,
                             uint16_t *kc, uint16_t *vc) {
+    pdl_wait();
+    pdl_trigger();
     const int t = blockIdx.x, pos = pos0 + t;
     const int stride = (Hq + 2 * Hkv) * hd, half = hd / 2;
     float *row = QKV + (size_t)t * stride;
@@ -420,6 +472,8 @@ __global__ void rope_append(float *QKV, int n, int Hq, int Hkv, int hd, int pos0
 template <int HD>
 __global__ void attend_prefill(const float *QKV, int n, int Hq, int Hkv, int pos0, int max_seq,
                                const uint16_t *kc, const uint16_t *vc, float *out) {
+    pdl_wait();
+    pdl_trigger();
     const int warp_global = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (warp_global >= n * Hq) return;
@@ -496,6 +550,8 @@ __global__ void __launch_bounds__(kStagedWarps * 32) attend_prefill_staged(const
                                                                             float *out) {
     constexpr int RS = HD + 8;  // row stride in bf16 elements (16 bytes of padding)
     extern __shared__ uint16_t kvs[];
+    pdl_wait();
+    pdl_trigger();
     uint16_t *Ks = kvs, *Vs = kvs + (size_t)Tcap * RS;
     const int kvh = blockIdx.x, t0 = blockIdx.y * kQB, G = Hq / Hkv;
     const int tl = min(n, t0 + kQB);  // tokens t0 .. tl-1
@@ -574,6 +630,8 @@ __global__ void __launch_bounds__(kStagedWarps * 32) attend_prefill_staged(const
 
 // h = silu(G) * U into hi/lo bf16 terms.
 __global__ void silu_split(const float *Gt, const float *U, size_t count, uint16_t *hi, uint16_t *lo) {
+    pdl_wait();
+    pdl_trigger();
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < count; i += (size_t)gridDim.x * blockDim.x) {
         const float g = Gt[i];
         const float v = g / (1.0f + expf(-g)) * U[i];
@@ -590,6 +648,8 @@ __global__ void lm_head_rows(const float *x, const uint16_t *g, float eps, const
     extern __shared__ float xs[];
     __shared__ float red[32];
     __shared__ unsigned long long best[32];
+    pdl_wait();
+    pdl_trigger();
     float ss = 0.f;
     for (int i = threadIdx.x; i < d; i += blockDim.x) ss = fmaf(x[i], x[i], ss);
     ss = block_sum(ss, red);
@@ -630,6 +690,8 @@ __global__ void lm_head_rows(const float *x, const uint16_t *g, float eps, const
 
 __global__ void argmax_keys(const unsigned long long *keys, int n, int32_t *out_token) {
     __shared__ unsigned long long best[32];
+    pdl_wait();
+    pdl_trigger();
     unsigned long long b = 0ull;
     for (int i = threadIdx.x; i < n; i += blockDim.x) b = keys[i] > b ? keys[i] : b;
     for (int o = 16; o > 0; o >>= 1) {
@@ -754,12 +816,9 @@ cudaError_t launch_gemm_bn(const CUtensorMap *const *tas, const Segs &sg, const 
     for (int i = 0; i < sg.n; ++i) tiles += sg.tiles[i];
     const dim3 grid(tiles, (N + BN - 1) / BN, S);
     const CUtensorMap &a0 = *tas[0], &a1 = sg.n > 1 ? *tas[1] : *tas[0], &a2 = sg.n > 2 ? *tas[2] : *tas[0];
-    tc_gemm<BN><<<grid, kThreads, smem, s>>>(a0, a1, a2, th, tl, sg, N, K, part, err);
-    cudaError_t e = cudaGetLastError();
-    if (e == cudaSuccess && S > 1) {
-        sum_splits<<<256, 256, 0, s>>>(part, S, N, sg.M[0], sg.Y[0], sg.ldy[0], sg.R[0]);
-        e = cudaGetLastError();
-    }
+    cudaError_t e = launch_pdl(tc_gemm<BN>, grid, dim3(kThreads), smem, s, a0, a1, a2, th, tl, sg, N, K, part, err);
+    if (e == cudaSuccess && S > 1)
+        e = launch_pdl(sum_splits, dim3(256), dim3(256), 0, s, part, S, N, sg.M[0], sg.Y[0], sg.ldy[0], sg.R[0]);
     return e;
 }
 
@@ -836,22 +895,20 @@ cudaError_t run(const Model &m, const Scratch &sc, const int32_t *d_tokens, int 
         if (e == cudaSuccess) e = x;
         return e == cudaSuccess;
     };
-    embed_rows<<<n, 256, 0, s>>>(m.embed, d_tokens, n, d, m.V, sc.X, sc.err);
-    ok(cudaGetLastError());
+    ok(launch_pdl(embed_rows, dim3(n), dim3(256), 0, s, m.embed, d_tokens, n, d, m.V, sc.X, sc.err));
     for (int l = 0; l < m.L && e == cudaSuccess; ++l) {
         const LayerMaps &lm = m.maps[l];
         const size_t kv_off = (size_t)l * m.kv_layer_stride;
         // attention block
-        norm_split<<<n, 256, 0, s>>>(sc.X, d, m.attn_norm[l], m.eps, sc.Ahi, sc.Alo);
-        ok(cudaGetLastError());
+        ok(launch_pdl(norm_split, dim3(n), dim3(256), 0, s, sc.X, d, m.attn_norm[l], m.eps, sc.Ahi, sc.Alo));
         {  // q, k and v in one launch
             const CUtensorMap *maps[3] = {&lm.wq, &lm.wk, &lm.wv};
             const int Ms[3] = {qd, kvd, kvd}, lds[3] = {qkv, qkv, qkv};
             float *Ys[3] = {sc.QKV, sc.QKV + qd, sc.QKV + qd + kvd};
             ok(gemm_multi(3, maps, Ms, Ys, lds, sc.Ahi, sc.Alo, n, d, sc.err, m.n_sm, s));
         }
-        rope_append<<<n, 256, 0, s>>>(sc.QKV, n, Hq, Hkv, hd, pos0, m.rope, m.max_seq, m.kc + kv_off, m.vc + kv_off);
-        ok(cudaGetLastError());
+        ok(launch_pdl(rope_append, dim3(n), dim3(256), 0, s, sc.QKV, n, Hq, Hkv, hd, pos0, m.rope, m.max_seq,
+                      m.kc + kv_off, m.vc + kv_off));
         const int warps = n * Hq, wpb = 4;
         if (pos0 + n <= kMaxStagedPos) {
             // every position the prompt attends to fits the staged rows
@@ -867,43 +924,38 @@ cudaError_t run(const Model &m, const Scratch &sc, const int32_t *d_tokens, int 
                 configured = e == cudaSuccess;
             }
             if (hd == 64)
-                attend_prefill_staged<64><<<grid, kStagedWarps * 32, smem, s>>>(
-                    sc.QKV, n, Hq, Hkv, pos0, m.max_seq, Tcap, m.kc + kv_off, m.vc + kv_off, sc.ATT);
+                ok(launch_pdl(attend_prefill_staged<64>, grid, dim3(kStagedWarps * 32), smem, s, sc.QKV, n, Hq, Hkv,
+                              pos0, m.max_seq, Tcap, m.kc + kv_off, m.vc + kv_off, sc.ATT));
             else
-                attend_prefill_staged<128><<<grid, kStagedWarps * 32, smem, s>>>(
-                    sc.QKV, n, Hq, Hkv, pos0, m.max_seq, Tcap, m.kc + kv_off, m.vc + kv_off, sc.ATT);
+                ok(launch_pdl(attend_prefill_staged<128>, grid, dim3(kStagedWarps * 32), smem, s, sc.QKV, n, Hq, Hkv,
+                              pos0, m.max_seq, Tcap, m.kc + kv_off, m.vc + kv_off, sc.ATT));
         } else if (hd == 64) {
-            attend_prefill<64><<<(warps + wpb - 1) / wpb, wpb * 32, 0, s>>>(sc.QKV, n, Hq, Hkv, pos0, m.max_seq,
-                                                                           m.kc + kv_off, m.vc + kv_off, sc.ATT);
+            ok(launch_pdl(attend_prefill<64>, dim3((warps + wpb - 1) / wpb), dim3(wpb * 32), 0, s, sc.QKV, n, Hq, Hkv,
+                          pos0, m.max_seq, m.kc + kv_off, m.vc + kv_off, sc.ATT));
         } else {
-            attend_prefill<128><<<(warps + wpb - 1) / wpb, wpb * 32, 0, s>>>(sc.QKV, n, Hq, Hkv, pos0, m.max_seq,
-                                                                            m.kc + kv_off, m.vc + kv_off, sc.ATT);
+            ok(launch_pdl(attend_prefill<128>, dim3((warps + wpb - 1) / wpb), dim3(wpb * 32), 0, s, sc.QKV, n, Hq,
+                          Hkv, pos0, m.max_seq, m.kc + kv_off, m.vc + kv_off, sc.ATT));
         }
-        ok(cudaGetLastError());
-        norm_split<<<n, 256, 0, s>>>(sc.ATT, qd, nullptr, 0.f, sc.Ahi, sc.Alo);
-        ok(cudaGetLastError());
+        ok(launch_pdl(norm_split, dim3(n), dim3(256), 0, s, sc.ATT, qd, nullptr, 0.f, sc.Ahi, sc.Alo));
         ok(gemm(lm.wo, sc.Ahi, sc.Alo, d, n, qd, sc.X, d, sc.X, sc.work, sc.work_floats, sc.err, m.n_sm, s));
         // MLP block
-        norm_split<<<n, 256, 0, s>>>(sc.X, d, m.mlp_norm[l], m.eps, sc.Ahi, sc.Alo);
-        ok(cudaGetLastError());
+        ok(launch_pdl(norm_split, dim3(n), dim3(256), 0, s, sc.X, d, m.mlp_norm[l], m.eps, sc.Ahi, sc.Alo));
         {  // gate and up in one launch
             const CUtensorMap *maps[2] = {&lm.wg, &lm.wu};
             const int Ms[2] = {F, F}, lds[2] = {F, F};
             float *Ys[2] = {sc.G, sc.U};
             ok(gemm_multi(2, maps, Ms, Ys, lds, sc.Ahi, sc.Alo, n, d, sc.err, m.n_sm, s));
         }
-        silu_split<<<1024, 256, 0, s>>>(sc.G, sc.U, (size_t)n * F, sc.Ahi, sc.Alo);
-        ok(cudaGetLastError());
+        ok(launch_pdl(silu_split, dim3(1024), dim3(256), 0, s, sc.G, sc.U, (size_t)n * F, sc.Ahi, sc.Alo));
         ok(gemm(lm.wd, sc.Ahi, sc.Alo, d, n, F, sc.X, d, sc.X, sc.work, sc.work_floats, sc.err, m.n_sm, s));
     }
     if (e != cudaSuccess) return e;
     // LM head of the last prompt position
     const int blocks = 2 * m.n_sm;
-    lm_head_rows<<<blocks, 512, sizeof(float) * d, s>>>(sc.X + (size_t)(n - 1) * d, m.final_norm, m.eps, m.embed,
-                                                        m.V, d, out_logits, sc.keys);
-    if (!ok(cudaGetLastError())) return e;
-    argmax_keys<<<1, 256, 0, s>>>(sc.keys, blocks, out_token);
-    ok(cudaGetLastError());
+    if (!ok(launch_pdl(lm_head_rows, dim3(blocks), dim3(512), sizeof(float) * d, s, sc.X + (size_t)(n - 1) * d,
+                       m.final_norm, m.eps, m.embed, m.V, d, out_logits, sc.keys)))
+        return e;
+    ok(launch_pdl(argmax_keys, dim3(1), dim3(256), 0, s, sc.keys, blocks, out_token));
     return e;
 }
 
