@@ -35,6 +35,28 @@ __device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
     return v;
 }
 
+// Programmatic dependent launch (as in the prefill): the reduce may start
+// while the row blocks finish, and a kernel waits for its predecessor's
+// results with pdl_wait; without the launch attribute both are no-ops.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Marks v as used here: called on every loaded vector after a batch of
 // loads, it keeps the compiler from moving arithmetic between the loads, so
 // a thread's loads are all in flight together.
@@ -63,6 +85,8 @@ __global__ void __launch_bounds__(kT) twell_part(const uint16_t *__restrict__ wt
     const int tid = threadIdx.x, lane = tid & 31;
     const int r0 = blockIdx.x * R, n = min(R, F - r0);
     const int nchunk = d / 8;
+    pdl_wait();  // h may come from the kernel before (the FFN's gate/up)
+    pdl_trigger();
     const float mine = lane < n ? h[r0 + lane] : 0.f;
     unsigned left = __ballot_sync(0xFFFFFFFFu, mine != 0.f);
     float2 acc[CPT][4];
@@ -113,6 +137,8 @@ __global__ void __launch_bounds__(kT) twell_part(const uint16_t *__restrict__ wt
 constexpr int kRT = 1024;
 __global__ void __launch_bounds__(kRT) twell_reduce(const float *__restrict__ part, int nb, int D, float *__restrict__ y) {
     __shared__ float ss[kRT / 32][33];
+    pdl_wait();  // the row blocks' partial sums
+    pdl_trigger();
     const int lane = threadIdx.x & 31, s = threadIdx.x >> 5;
     const int c = blockIdx.x * 32 + lane;
     float acc = 0.f;
@@ -138,6 +164,8 @@ __global__ void __launch_bounds__(kT) twell_gateup(const uint16_t *__restrict__ 
                                                    const float *__restrict__ x, int F, float *__restrict__ h) {
     constexpr int D = NC * 256;
     __shared__ float4 xs[D / 4];
+    pdl_wait();
+    pdl_trigger();
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     for (int i = tid; i < D / 4; i += kT) xs[i] = reinterpret_cast<const float4 *>(x)[i];
     __syncthreads();
@@ -181,14 +209,12 @@ __global__ void __launch_bounds__(kT) twell_gateup(const uint16_t *__restrict__ 
 
 template <int CPT>
 cudaError_t launch_part(const uint16_t *wt, const float *h, int F, int d, int R, int nb, float *part, cudaStream_t s) {
-    twell_part<CPT><<<nb, kT, 0, s>>>(wt, h, F, d, R, part);
-    return cudaGetLastError();
+    return launch_pdl(twell_part<CPT>, dim3(nb), dim3(kT), 0, s, wt, h, F, d, R, part);
 }
 
 template <int NC>
 cudaError_t launch_gateup(const uint16_t *wg, const uint16_t *wu, const float *x, int F, float *h, cudaStream_t s) {
-    twell_gateup<NC><<<(F + kWarps - 1) / kWarps, kT, 0, s>>>(wg, wu, x, F, h);
-    return cudaGetLastError();
+    return launch_pdl(twell_gateup<NC>, dim3((F + kWarps - 1) / kWarps), dim3(kT), 0, s, wg, wu, x, F, h);
 }
 
 // Rows per CTA of the down projection: about two CTAs per SM, at most 32
@@ -241,8 +267,7 @@ cudaError_t down(const uint16_t *wt, int F, int d, const float *h, float *y, cud
     const cudaError_t e = d / 8 <= kT ? launch_part<1>(wt, h, F, d, R, nb, part, s)
                                       : launch_part<2>(wt, h, F, d, R, nb, part, s);
     if (e != cudaSuccess) return e;
-    twell_reduce<<<(d + 31) / 32, kRT, 0, s>>>(part, nb, d, y);
-    return cudaGetLastError();
+    return launch_pdl(twell_reduce, dim3((d + 31) / 32), dim3(kRT), 0, s, part, nb, d, y);
 }
 
 }  // namespace
