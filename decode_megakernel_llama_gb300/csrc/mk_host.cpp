@@ -1029,7 +1029,6 @@ int mk_prefill(mk_handle *h, const int32_t *d_tokens, int32_t n, int32_t start_p
         sc.cap = n;
         sc.X = reinterpret_cast<float *>(take(4 * (size_t)n * d));
         sc.QKV = reinterpret_cast<float *>(take(4 * (size_t)n * qkv));
-        sc.ATT = reinterpret_cast<float *>(take(4 * (size_t)n * qd));
         sc.G = reinterpret_cast<float *>(take(4 * (size_t)n * F));
         sc.U = reinterpret_cast<float *>(take(4 * (size_t)n * F));
         sc.Ahi = reinterpret_cast<uint16_t *>(take(2 * (size_t)n * kmax));

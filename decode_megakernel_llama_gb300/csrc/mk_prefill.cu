@@ -469,9 +469,11 @@ __global__ void rope_append(float *QKV, int n, int Hq, int Hkv, int hd, int pos0
 // Causal attention: one warp per (token t, query head h) over cache
 // positions 0 .. pos0 + t of kv head h / G, online softmax in chunks of 32
 // positions (lane = position for the scores, lane = dimension pair for P.V).
+// The output row [n][Hq*HD] is written as the hi/lo bf16 terms the
+// O-projection reads.
 template <int HD>
 __global__ void attend_prefill(const float *QKV, int n, int Hq, int Hkv, int pos0, int max_seq,
-                               const uint16_t *kc, const uint16_t *vc, float *out) {
+                               const uint16_t *kc, const uint16_t *vc, uint16_t *out_hi, uint16_t *out_lo) {
     pdl_wait();
     pdl_trigger();
     const int warp_global = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -527,9 +529,14 @@ __global__ void attend_prefill(const float *QKV, int n, int Hq, int Hkv, int pos
             for (int e = 0; e < DP; ++e) o[e] = fmaf(pj, bf2f(vr[e]), o[e]);
         }
     }
-    float *dst = out + (size_t)t * Hq * HD + (size_t)h * HD + lane * DP;
+    const size_t at = (size_t)t * Hq * HD + (size_t)h * HD + lane * DP;
 #pragma unroll
-    for (int e = 0; e < DP; ++e) dst[e] = o[e] / l;
+    for (int e = 0; e < DP; ++e) {
+        const float v = o[e] / l;
+        const uint16_t hb = f2bf_rne(v);
+        out_hi[at + e] = hb;
+        out_lo[at + e] = f2bf_rne(v - bf2f(hb));
+    }
 }
 
 // The same causal attention with the kv head's cached rows staged in shared
@@ -547,7 +554,7 @@ template <int HD>
 __global__ void __launch_bounds__(kStagedWarps * 32) attend_prefill_staged(const float *QKV, int n, int Hq, int Hkv,
                                                                             int pos0, int max_seq, int Tcap,
                                                                             const uint16_t *kc, const uint16_t *vc,
-                                                                            float *out) {
+                                                                            uint16_t *out_hi, uint16_t *out_lo) {
     constexpr int RS = HD + 8;  // row stride in bf16 elements (16 bytes of padding)
     extern __shared__ uint16_t kvs[];
     pdl_wait();
@@ -622,9 +629,14 @@ __global__ void __launch_bounds__(kStagedWarps * 32) attend_prefill_staged(const
                 for (int e = 0; e < DP; ++e) o[jj & 1][e] = fmaf(pj, bf2f(vb[(size_t)jj * RS + e]), o[jj & 1][e]);
             }
         }
-        float *dst = out + (size_t)t * Hq * HD + (size_t)h * HD + lane * DP;
+        const size_t at = (size_t)t * Hq * HD + (size_t)h * HD + lane * DP;
 #pragma unroll
-        for (int e = 0; e < DP; ++e) dst[e] = (o[0][e] + o[1][e]) / l;
+        for (int e = 0; e < DP; ++e) {
+            const float v = (o[0][e] + o[1][e]) / l;
+            const uint16_t hb = f2bf_rne(v);
+            out_hi[at + e] = hb;
+            out_lo[at + e] = f2bf_rne(v - bf2f(hb));
+        }
     }
 }
 
@@ -925,18 +937,17 @@ cudaError_t run(const Model &m, const Scratch &sc, const int32_t *d_tokens, int 
             }
             if (hd == 64)
                 ok(launch_pdl(attend_prefill_staged<64>, grid, dim3(kStagedWarps * 32), smem, s, sc.QKV, n, Hq, Hkv,
-                              pos0, m.max_seq, Tcap, m.kc + kv_off, m.vc + kv_off, sc.ATT));
+                              pos0, m.max_seq, Tcap, m.kc + kv_off, m.vc + kv_off, sc.Ahi, sc.Alo));
             else
                 ok(launch_pdl(attend_prefill_staged<128>, grid, dim3(kStagedWarps * 32), smem, s, sc.QKV, n, Hq, Hkv,
-                              pos0, m.max_seq, Tcap, m.kc + kv_off, m.vc + kv_off, sc.ATT));
+                              pos0, m.max_seq, Tcap, m.kc + kv_off, m.vc + kv_off, sc.Ahi, sc.Alo));
         } else if (hd == 64) {
             ok(launch_pdl(attend_prefill<64>, dim3((warps + wpb - 1) / wpb), dim3(wpb * 32), 0, s, sc.QKV, n, Hq, Hkv,
-                          pos0, m.max_seq, m.kc + kv_off, m.vc + kv_off, sc.ATT));
+                          pos0, m.max_seq, m.kc + kv_off, m.vc + kv_off, sc.Ahi, sc.Alo));
         } else {
             ok(launch_pdl(attend_prefill<128>, dim3((warps + wpb - 1) / wpb), dim3(wpb * 32), 0, s, sc.QKV, n, Hq,
-                          Hkv, pos0, m.max_seq, m.kc + kv_off, m.vc + kv_off, sc.ATT));
+                          Hkv, pos0, m.max_seq, m.kc + kv_off, m.vc + kv_off, sc.Ahi, sc.Alo));
         }
-        ok(launch_pdl(norm_split, dim3(n), dim3(256), 0, s, sc.ATT, qd, nullptr, 0.f, sc.Ahi, sc.Alo));
         ok(gemm(lm.wo, sc.Ahi, sc.Alo, d, n, qd, sc.X, d, sc.X, sc.work, sc.work_floats, sc.err, m.n_sm, s));
         // MLP block
         ok(launch_pdl(norm_split, dim3(n), dim3(256), 0, s, sc.X, d, m.mlp_norm[l], m.eps, sc.Ahi, sc.Alo));

@@ -30,7 +30,7 @@ struct Model {
 // Device scratch for up to `cap` prompt tokens.
 struct Scratch {
     int cap = 0;
-    float *X = nullptr, *QKV = nullptr, *ATT = nullptr, *G = nullptr, *U = nullptr;
+    float *X = nullptr, *QKV = nullptr, *G = nullptr, *U = nullptr;
     uint16_t *Ahi = nullptr, *Alo = nullptr;
     unsigned long long *keys = nullptr;
     float *work = nullptr;   // K-split partial sums of the contractions
