@@ -991,23 +991,26 @@ int mk_prefill(mk_handle *h, const int32_t *d_tokens, int32_t n, int32_t start_p
             m.mlp_norm[l] = lw.mlp_norm;
             if (!mkpf::encode_weight_map(&lm.wq, lw.wq, qd, d) || !mkpf::encode_weight_map(&lm.wk, lw.wk, kvd, d) ||
                 !mkpf::encode_weight_map(&lm.wv, lw.wv, kvd, d) || !mkpf::encode_weight_map(&lm.wo, lw.wo, d, qd) ||
-                !mkpf::encode_weight_map(&lm.wg, lw.w_gate, F, d) || !mkpf::encode_weight_map(&lm.wu, lw.w_up, F, d) ||
+                !mkpf::encode_gated_map(&lm.wg, lw.w_gate, F, d) || !mkpf::encode_gated_map(&lm.wu, lw.w_up, F, d) ||
                 !mkpf::encode_weight_map(&lm.wd, lw.w_down, d, F))
                 return fail(MK_ERR_UNSUPPORTED, "could not encode the weights' tensor maps");
         }
         h->pf_ready = true;
     }
     if (h->pf.cap < n) {
-        // scratch for n tokens: residual, q|k|v, attention output, gate, up
-        // (fp32) and the hi/lo bf16 operand of the next contraction
-        const size_t kmax = std::max(std::max(d, qd), F), qkv = qd + 2 * kvd;
+        // scratch for n tokens: residual and q|k|v (fp32), the hi/lo bf16
+        // input of the projections from d or Hq hd columns, and that of the
+        // down projection (h = silu(g) * u)
+        const size_t kmax = std::max(d, qd), qkv = qd + 2 * kvd;
         // K-split partials: the largest any of the layer's contractions uses
+        // (gate/up runs in one pass)
         const int nsm = h->im.n_sm;
         size_t work = 0;
-        const int shapes[4][2] = {{qd, d}, {kvd, d}, {d, qd}, {F, d}};
+        const int shapes[3][2] = {{qd, d}, {kvd, d}, {d, qd}};
         for (const auto &mk_ : shapes) work = std::max(work, mkpf::gemm_workspace_floats(mk_[0], n, mk_[1], nsm));
         work = std::max(work, mkpf::gemm_workspace_floats(d, n, F, nsm));
-        const size_t bytes = 4 * (size_t)n * (d + qkv + qd + 2 * (size_t)F) + 2 * 2 * (size_t)n * kmax +
+        // (+ 256 bytes of alignment for each of the 8 pieces)
+        const size_t bytes = 4 * (size_t)n * (d + qkv) + 2 * 2 * (size_t)n * (kmax + F) +
                              8 * (size_t)2 * h->im.n_sm + 4 * work + 4 * 512;
         int32_t err_keep = 0;
         if (h->pf.err) cudaMemcpy(&err_keep, h->pf.err, sizeof err_keep, cudaMemcpyDeviceToHost);
@@ -1029,8 +1032,8 @@ int mk_prefill(mk_handle *h, const int32_t *d_tokens, int32_t n, int32_t start_p
         sc.cap = n;
         sc.X = reinterpret_cast<float *>(take(4 * (size_t)n * d));
         sc.QKV = reinterpret_cast<float *>(take(4 * (size_t)n * qkv));
-        sc.G = reinterpret_cast<float *>(take(4 * (size_t)n * F));
-        sc.U = reinterpret_cast<float *>(take(4 * (size_t)n * F));
+        sc.Hhi = reinterpret_cast<uint16_t *>(take(2 * (size_t)n * F));
+        sc.Hlo = reinterpret_cast<uint16_t *>(take(2 * (size_t)n * F));
         sc.Ahi = reinterpret_cast<uint16_t *>(take(2 * (size_t)n * kmax));
         sc.Alo = reinterpret_cast<uint16_t *>(take(2 * (size_t)n * kmax));
         sc.keys = reinterpret_cast<unsigned long long *>(take(8 * (size_t)2 * h->im.n_sm));

@@ -184,6 +184,16 @@ __host__ __device__ constexpr int stages_for() {
     return kRingBytes / (kATileBytes + 2 * BN * 128) > 8 ? 8 : kRingBytes / (kATileBytes + 2 * BN * 128);
 }
 
+__device__ __forceinline__ float bf2f(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
+
+// fp32 -> bf16, round to nearest even (finite values).
+__device__ __forceinline__ uint16_t f2bf_rne(float f) {
+    uint32_t u = __float_as_uint(f);
+    if ((u & 0x7F800000u) == 0x7F800000u) return uint16_t((u >> 16) | ((u & 0xFFFFu) ? 0x40u : 0u));
+    u += 0x7FFFu + ((u >> 16) & 1u);
+    return uint16_t(u >> 16);
+}
+
 // Up to three weight matrices multiplied by the same activations in one
 // launch: CTA row tiles 0 .. tiles[0]-1 take matrix 0 (tensor map ta0),
 // the next tiles[1] matrix 1 (ta1), then matrix 2 (ta2); each has its own
@@ -193,9 +203,15 @@ struct Segs {
     int tiles[3], M[3], ldy[3];
     float *Y[3];
     const float *R[3];
+    uint16_t *hhi, *hlo;  // gated launches: the hi / lo bf16 terms of h [N][ldy[0]]
 };
 
-template <int BN>
+// GATED: the gate/up projection of the MLP. A CTA takes 64 outputs: its A
+// tile is 64 rows of W_gate (ta0, boxes of 64 rows) over 64 rows of W_up
+// (ta1) for the same outputs, so the accumulator holds g in lanes 0..63 and u
+// in lanes 64..127; the epilogue passes u through shared memory and writes
+// h = silu(g) * u as the hi / lo bf16 terms the down projection reads.
+template <int BN, bool GATED = false>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm(const __grid_constant__ CUtensorMap ta0, const __grid_constant__ CUtensorMap ta1,
             const __grid_constant__ CUtensorMap ta2, const __grid_constant__ CUtensorMap tbh,
@@ -213,13 +229,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     int *issued = reinterpret_cast<int *>(tslot + 1);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     int bx = blockIdx.x, q = 0;
-    while (q + 1 < sg.n && bx >= sg.tiles[q]) bx -= sg.tiles[q++];
+    if (!GATED)
+        while (q + 1 < sg.n && bx >= sg.tiles[q]) bx -= sg.tiles[q++];
     const CUtensorMap *ta = q == 0 ? &ta0 : (q == 1 ? &ta1 : &ta2);
     const int M = sg.M[q];
     float *Y = sg.Y[q];
     int ldy = sg.ldy[q];
     const float *R = sg.R[q];
-    const int m0 = bx * 128, n0 = blockIdx.y * BN;
+    const int m0 = bx * (GATED ? 64 : 128), n0 = blockIdx.y * BN;
     // K split over gridDim.z CTAs (one matrix only): this one takes 64-wide chunks c0 .. c0+nk-1
     // and writes its partial sums to part[z][N][M] (summed later in a fixed
     // order), or with one split the result itself
@@ -230,6 +247,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         ldy = M;
         R = nullptr;
     }
+    // the A tile of chunk kc into stage memory st (gated: gate rows, then up rows)
+    auto load_a = [&](uint8_t *st, int kc, uint64_t *bar) {
+        if (GATED) {
+            tma_load_2d(st, &ta0, (c0 + kc) * 64, m0, bar);
+            tma_load_2d(st + kATileBytes / 2, &ta1, (c0 + kc) * 64, m0, bar);
+        } else {
+            tma_load_2d(st, ta, (c0 + kc) * 64, m0, bar);
+        }
+    };
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1);
@@ -255,7 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0 && lane == 0)
         for (int kc = 0; kc < pre; ++kc) {
             mbar_expect_tx(&full[kc], kStageBytes);
-            tma_load_2d(sm + kc * kStageBytes, ta, (c0 + kc) * 64, m0, &full[kc]);
+            load_a(sm + kc * kStageBytes, kc, &full[kc]);
         }
     pdl_wait();
     pdl_trigger();
@@ -274,7 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!mbar_wait(&empty[s], ((kc / kStages) - 1) & 1, err)) break;
             uint8_t *st = sm + s * kStageBytes;
             mbar_expect_tx(&full[s], kStageBytes);
-            tma_load_2d(st, ta, (c0 + kc) * 64, m0, &full[s]);
+            load_a(st, kc, &full[s]);
             tma_load_2d(st + kATileBytes, &tbh, (c0 + kc) * 64, n0, &full[s]);
             tma_load_2d(st + kATileBytes + kBTileBytes, &tbl, (c0 + kc) * 64, n0, &full[s]);
             *issued = kc + 1;
@@ -301,7 +327,60 @@ __global__ void __launch_bounds__(kThreads, 1)
     // epilogue: warp w reads tensor-memory lanes 32w .. 32w+31 (output rows)
     const bool have = mbar_wait(done, 0, err);
     tc_fence_after();
-    if (have) {
+    if (GATED) {
+        // g sits in tensor-memory lanes 0..63 (warps 0, 1), u in lanes 64..127
+        // (warps 2, 3), row r of each in lane r and r + 64. Each warp hands the
+        // half of its columns the partner warp finishes to shared memory, then
+        // forms h for the other half: gate warps columns 0 .. BN/2-1, up
+        // warps the rest. Every copy has landed and every MMA is done, so the
+        // stage ring is free.
+        constexpr int kH = BN / 2, kUs = kH + 1;  // padded rows: the lanes of a warp hit 32 banks
+        static_assert(2 * 64 * kUs * 4 <= kStages * kStageBytes, "g and u do not fit the stage ring");
+        float *us = reinterpret_cast<float *>(sm);  // [64][kUs] u of columns 0 .. kH-1
+        float *gs = us + 64 * kUs;                  // [64][kUs] g of columns kH .. BN-1
+        const bool up = warp >= 2;
+        const int r = (warp & 1) * 32 + lane;
+        const uint32_t row = tmem + ((uint32_t)(warp * 32) << 16);
+        if (have) {
+            const uint32_t cb = up ? 0 : kH;
+            float *dst = (up ? us : gs) + r * kUs;
+#pragma unroll 1
+            for (int c = 0; c < kH; c += 16) {
+                uint32_t vh[16], vl[16];
+                tmem_ld16(row + cb + (uint32_t)c, vh);
+                tmem_ld16(row + (uint32_t)BN + cb + (uint32_t)c, vl);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) dst[c + i] = __uint_as_float(vh[i]) + __uint_as_float(vl[i]);
+            }
+        }
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        if (have) {
+            const int cb = up ? kH : 0, m = m0 + r;
+            const float *oth = (up ? gs : us) + r * kUs;
+#pragma unroll 1
+            for (int c = 0; c < kH; c += 16) {
+                uint32_t vh[16], vl[16];
+                tmem_ld16(row + (uint32_t)(cb + c), vh);
+                tmem_ld16(row + (uint32_t)(BN + cb + c), vl);
+                if (m < M) {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const int n = n0 + cb + c + i;
+                        if (n < N) {
+                            const float mine = __uint_as_float(vh[i]) + __uint_as_float(vl[i]), o = oth[c + i];
+                            const float g = up ? o : mine, u = up ? mine : o;
+                            const float v = g / (1.0f + expf(-g)) * u;
+                            const uint16_t hb = f2bf_rne(v);
+                            sg.hhi[(size_t)n * ldy + m] = hb;
+                            sg.hlo[(size_t)n * ldy + m] = f2bf_rne(v - bf2f(hb));
+                        }
+                    }
+                }
+            }
+        }
+    } else if (have) {
         const int m = m0 + warp * 32 + lane;
         const uint32_t row = tmem + ((uint32_t)(warp * 32) << 16);
 #pragma unroll 1
@@ -379,16 +458,6 @@ constexpr int gemm_smem_bytes() {
 // ---------------------------------------------------------------------------
 // Elementwise and attention kernels of the prefill.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ float bf2f(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
-
-// fp32 -> bf16, round to nearest even (finite values).
-__device__ __forceinline__ uint16_t f2bf_rne(float f) {
-    uint32_t u = __float_as_uint(f);
-    if ((u & 0x7F800000u) == 0x7F800000u) return uint16_t((u >> 16) | ((u & 0xFFFFu) ? 0x40u : 0u));
-    u += 0x7FFFu + ((u >> 16) & 1u);
-    return uint16_t(u >> 16);
-}
-
 __device__ __forceinline__ float block_sum(float v, float *red) {
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
     const int w = threadIdx.x >> 5, nw = blockDim.x >> 5;
@@ -640,19 +709,6 @@ __global__ void __launch_bounds__(kStagedWarps * 32) attend_prefill_staged(const
     }
 }
 
-// h = silu(G) * U into hi/lo bf16 terms.
-__global__ void silu_split(const float *Gt, const float *U, size_t count, uint16_t *hi, uint16_t *lo) {
-    pdl_wait();
-    pdl_trigger();
-    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < count; i += (size_t)gridDim.x * blockDim.x) {
-        const float g = Gt[i];
-        const float v = g / (1.0f + expf(-g)) * U[i];
-        const uint16_t h = f2bf_rne(v);
-        hi[i] = h;
-        lo[i] = f2bf_rne(v - bf2f(h));
-    }
-}
-
 // Final RMSNorm of one row into shared memory, then rows of the tied
 // embedding times it (a warp per row), logits and a block argmax key.
 __global__ void lm_head_rows(const float *x, const uint16_t *g, float eps, const uint16_t *E, int V, int d,
@@ -812,7 +868,7 @@ GemmShape pick_shape(int M, int N, int K, int n_sm) {
     return g;
 }
 
-template <int BN>
+template <int BN, bool GATED = false>
 cudaError_t launch_gemm_bn(const CUtensorMap *const *tas, const Segs &sg, const void *bhi, const void *blo, int N,
                            int K, float *part, int S, int *err, cudaStream_t s) {
     CUtensorMap th, tl;
@@ -820,15 +876,17 @@ cudaError_t launch_gemm_bn(const CUtensorMap *const *tas, const Segs &sg, const 
     constexpr int smem = gemm_smem_bytes<BN>();
     static bool configured = false;
     if (!configured) {
-        const cudaError_t e = cudaFuncSetAttribute(tc_gemm<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        const cudaError_t e =
+            cudaFuncSetAttribute(tc_gemm<BN, GATED>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
         configured = true;
     }
     int tiles = 0;
     for (int i = 0; i < sg.n; ++i) tiles += sg.tiles[i];
     const dim3 grid(tiles, (N + BN - 1) / BN, S);
-    const CUtensorMap &a0 = *tas[0], &a1 = sg.n > 1 ? *tas[1] : *tas[0], &a2 = sg.n > 2 ? *tas[2] : *tas[0];
-    cudaError_t e = launch_pdl(tc_gemm<BN>, grid, dim3(kThreads), smem, s, a0, a1, a2, th, tl, sg, N, K, part, err);
+    const CUtensorMap &a0 = *tas[0], &a1 = GATED || sg.n > 1 ? *tas[1] : *tas[0], &a2 = sg.n > 2 ? *tas[2] : *tas[0];
+    cudaError_t e =
+        launch_pdl(tc_gemm<BN, GATED>, grid, dim3(kThreads), smem, s, a0, a1, a2, th, tl, sg, N, K, part, err);
     if (e == cudaSuccess && S > 1)
         e = launch_pdl(sum_splits, dim3(256), dim3(256), 0, s, part, S, N, sg.M[0], sg.Y[0], sg.ldy[0], sg.R[0]);
     return e;
@@ -851,6 +909,8 @@ cudaError_t launch_one(const CUtensorMap &ta, const void *bhi, const void *blo, 
 }  // namespace
 
 bool encode_weight_map(CUtensorMap *map, const void *w, int rows, int K) { return make_map(map, w, rows, K, 128); }
+
+bool encode_gated_map(CUtensorMap *map, const void *w, int rows, int K) { return make_map(map, w, rows, K, 64); }
 
 size_t gemm_workspace_floats(int M, int N, int K, int n_sm) {
     const GemmShape g = pick_shape(M, N, K, n_sm);
@@ -895,6 +955,30 @@ cudaError_t gemm_multi(int nseg, const CUtensorMap *const *maps, const int *M, f
         case 32: return launch_gemm_bn<32>(maps, sg, bhi, blo, N, K, nullptr, 1, err, s);
         case 64: return launch_gemm_bn<64>(maps, sg, bhi, blo, N, K, nullptr, 1, err, s);
         default: return launch_gemm_bn<128>(maps, sg, bhi, blo, N, K, nullptr, 1, err, s);
+    }
+}
+
+cudaError_t gemm_gated(const CUtensorMap &wg, const CUtensorMap &wu, int F, const void *bhi, const void *blo, int N,
+                       int K, uint16_t *hhi, uint16_t *hlo, int *err, int n_sm, cudaStream_t s) {
+    if (K % 64 || N < 1 || F < 1) return cudaErrorInvalidValue;
+    Segs sg{};
+    sg.n = 1;
+    sg.tiles[0] = (F + 63) / 64;
+    sg.M[0] = F;
+    sg.ldy[0] = F;
+    sg.hhi = hhi;
+    sg.hlo = hlo;
+    const CUtensorMap *maps[2] = {&wg, &wu};
+    int bn = 128;
+    for (int b = 32; b < 128; b *= 2)
+        if (sg.tiles[0] * ((N + b - 1) / b) <= n_sm) {
+            bn = b;
+            break;
+        }
+    switch (bn) {
+        case 32: return launch_gemm_bn<32, true>(maps, sg, bhi, blo, N, K, nullptr, 1, err, s);
+        case 64: return launch_gemm_bn<64, true>(maps, sg, bhi, blo, N, K, nullptr, 1, err, s);
+        default: return launch_gemm_bn<128, true>(maps, sg, bhi, blo, N, K, nullptr, 1, err, s);
     }
 }
 
@@ -951,14 +1035,9 @@ cudaError_t run(const Model &m, const Scratch &sc, const int32_t *d_tokens, int 
         ok(gemm(lm.wo, sc.Ahi, sc.Alo, d, n, qd, sc.X, d, sc.X, sc.work, sc.work_floats, sc.err, m.n_sm, s));
         // MLP block
         ok(launch_pdl(norm_split, dim3(n), dim3(256), 0, s, sc.X, d, m.mlp_norm[l], m.eps, sc.Ahi, sc.Alo));
-        {  // gate and up in one launch
-            const CUtensorMap *maps[2] = {&lm.wg, &lm.wu};
-            const int Ms[2] = {F, F}, lds[2] = {F, F};
-            float *Ys[2] = {sc.G, sc.U};
-            ok(gemm_multi(2, maps, Ms, Ys, lds, sc.Ahi, sc.Alo, n, d, sc.err, m.n_sm, s));
-        }
-        ok(launch_pdl(silu_split, dim3(1024), dim3(256), 0, s, sc.G, sc.U, (size_t)n * F, sc.Ahi, sc.Alo));
-        ok(gemm(lm.wd, sc.Ahi, sc.Alo, d, n, F, sc.X, d, sc.X, sc.work, sc.work_floats, sc.err, m.n_sm, s));
+        // gate and up in one launch, h = silu(g) * u formed in its epilogue
+        ok(gemm_gated(lm.wg, lm.wu, F, sc.Ahi, sc.Alo, n, d, sc.Hhi, sc.Hlo, sc.err, m.n_sm, s));
+        ok(gemm(lm.wd, sc.Hhi, sc.Hlo, d, n, F, sc.X, d, sc.X, sc.work, sc.work_floats, sc.err, m.n_sm, s));
     }
     if (e != cudaSuccess) return e;
     // LM head of the last prompt position

@@ -10,7 +10,8 @@
 namespace mkpf {
 
 // Tensor maps of one layer's projection weights (bf16 [out][in], boxes of
-// 64 x 128, 128-byte swizzle).
+// 64 x 128, 128-byte swizzle; wg and wu boxes of 64 x 64, as the gated
+// launch takes 64 rows of each).
 struct LayerMaps {
     CUtensorMap wq, wk, wv, wo, wg, wu, wd;
 };
@@ -30,8 +31,9 @@ struct Model {
 // Device scratch for up to `cap` prompt tokens.
 struct Scratch {
     int cap = 0;
-    float *X = nullptr, *QKV = nullptr, *G = nullptr, *U = nullptr;
-    uint16_t *Ahi = nullptr, *Alo = nullptr;
+    float *X = nullptr, *QKV = nullptr;
+    uint16_t *Ahi = nullptr, *Alo = nullptr;  // hi / lo terms of a contraction's input [n][<= max(d, Hq hd)]
+    uint16_t *Hhi = nullptr, *Hlo = nullptr;  // hi / lo terms of h = silu(g) * u [n][F]
     unsigned long long *keys = nullptr;
     float *work = nullptr;   // K-split partial sums of the contractions
     size_t work_floats = 0;
@@ -39,11 +41,18 @@ struct Scratch {
 };
 
 bool encode_weight_map(CUtensorMap *map, const void *w, int rows, int K);
+bool encode_gated_map(CUtensorMap *map, const void *w, int rows, int K);  // W_gate / W_up, for gemm_gated
 
 // Y[n][m] (+)= W[m][.] . (Bhi[n][.] + Blo[n][.]) on the tensor cores; work
 // (work_floats floats) holds K-split partial sums (one pass if too small).
 cudaError_t gemm(const CUtensorMap &wmap, const void *bhi, const void *blo, int M, int N, int K, float *Y, int ldy,
                  const float *R, float *work, size_t work_floats, int *err, int n_sm, cudaStream_t s);
+
+// hi / lo bf16 terms of h[n][f] = silu(g) * u, g and u the rows f of W_gate
+// and W_up (maps from encode_gated_map) times Bhi[n][.] + Blo[n][.]; one
+// pass, no K split.
+cudaError_t gemm_gated(const CUtensorMap &wg, const CUtensorMap &wu, int F, const void *bhi, const void *blo, int N,
+                       int K, uint16_t *hhi, uint16_t *hlo, int *err, int n_sm, cudaStream_t s);
 
 // Floats of K-split workspace gemm() uses for this shape (0: none).
 size_t gemm_workspace_floats(int M, int N, int K, int n_sm);
