@@ -504,6 +504,35 @@ __global__ void norm_split(const float *X, int K, const uint16_t *g, float eps, 
     }
 }
 
+// The split sum of a residual contraction followed by the next RMSNorm:
+// for token n = blockIdx.x, Y[n][m] = R[n][m] + sum over z of part[z][n][m]
+// (z in order), then the RMSNorm of that row with gains g (as norm_split)
+// into hi / lo bf16 terms [n][M]. Each thread reads back only what it wrote.
+__global__ void sum_splits_norm(const float *part, int S, int N, int M, float *Y, int ldy, const float *R,
+                                const uint16_t *g, float eps, uint16_t *hi, uint16_t *lo) {
+    __shared__ float red[32];
+    pdl_wait();
+    pdl_trigger();
+    const int n = blockIdx.x;
+    const size_t total = (size_t)N * M;
+    float *y = Y + (size_t)n * ldy;
+    float ss = 0.f;
+    for (int m = threadIdx.x; m < M; m += blockDim.x) {
+        float v = R ? R[(size_t)n * ldy + m] : 0.f;
+        for (int z = 0; z < S; ++z) v += part[(size_t)z * total + (size_t)n * M + m];
+        y[m] = v;
+        ss = fmaf(v, v, ss);
+    }
+    ss = block_sum(ss, red);
+    const float scale = 1.0f / sqrtf(ss / (float)M + eps);
+    for (int m = threadIdx.x; m < M; m += blockDim.x) {
+        const float v = y[m] * (scale * bf2f(g[m]));
+        const uint16_t h = f2bf_rne(v);
+        hi[(size_t)n * M + m] = h;
+        lo[(size_t)n * M + m] = f2bf_rne(v - bf2f(h));
+    }
+}
+
 // RoPE on q and k of token t (position pos0 + t) from the fp32 QKV rows, q
 // kept (rotated) in place, bf16 k and v written into the cache at the position.
 __global__ void rope_append(float *QKV, int n, int Hq, int Hkv, int hd, int pos0, const float *rope, int max_seq,
@@ -849,7 +878,7 @@ struct GemmShape {
     int bn, S;
 };
 
-GemmShape pick_shape(int M, int N, int K, int n_sm) {
+GemmShape pick_shape(int M, int N, int K, int n_sm, bool norm) {
     const int rt = (M + 127) / 128, nk = K / 64;
     GemmShape g{128, 1};
     if (nk >= 64) {
@@ -858,19 +887,24 @@ GemmShape pick_shape(int M, int N, int K, int n_sm) {
         if (S > nk / 32) S = nk / 32;
         if (S > kMaxSplits) S = kMaxSplits;
         g.S = S < 1 ? 1 : S;
+        if (norm && g.S < 2) g.S = 2;
         return g;
     }
+    // a contraction that feeds an RMSNorm takes two halves of its reduction,
+    // so that the pass summing them also forms the norm
+    const int S = norm && nk >= 2 ? 2 : 1;
     for (int bn = 32; bn <= 128; bn *= 2)
-        if (rt * ((N + bn - 1) / bn) <= n_sm || bn == 128) {
+        if (rt * ((N + bn - 1) / bn) * S <= n_sm || bn == 128) {
             g.bn = bn;
             break;
         }
+    g.S = S;
     return g;
 }
 
 template <int BN, bool GATED = false>
 cudaError_t launch_gemm_bn(const CUtensorMap *const *tas, const Segs &sg, const void *bhi, const void *blo, int N,
-                           int K, float *part, int S, int *err, cudaStream_t s) {
+                           int K, float *part, int S, int *err, cudaStream_t s, const NormOut &nm = NormOut{}) {
     CUtensorMap th, tl;
     if (!make_map(&th, bhi, N, K, BN) || !make_map(&tl, blo, N, K, BN)) return cudaErrorInvalidValue;
     constexpr int smem = gemm_smem_bytes<BN>();
@@ -887,14 +921,19 @@ cudaError_t launch_gemm_bn(const CUtensorMap *const *tas, const Segs &sg, const 
     const CUtensorMap &a0 = *tas[0], &a1 = GATED || sg.n > 1 ? *tas[1] : *tas[0], &a2 = sg.n > 2 ? *tas[2] : *tas[0];
     cudaError_t e =
         launch_pdl(tc_gemm<BN, GATED>, grid, dim3(kThreads), smem, s, a0, a1, a2, th, tl, sg, N, K, part, err);
-    if (e == cudaSuccess && S > 1)
+    if (e == cudaSuccess && S > 1 && nm.g)
+        e = launch_pdl(sum_splits_norm, dim3(N), dim3(256), 0, s, part, S, N, sg.M[0], sg.Y[0], sg.ldy[0], sg.R[0],
+                       nm.g, nm.eps, nm.hi, nm.lo);
+    else if (e == cudaSuccess && S > 1)
         e = launch_pdl(sum_splits, dim3(256), dim3(256), 0, s, part, S, N, sg.M[0], sg.Y[0], sg.ldy[0], sg.R[0]);
+    else if (e == cudaSuccess && nm.g)  // one pass: the norm on its own
+        e = launch_pdl(norm_split, dim3(N), dim3(256), 0, s, sg.Y[0], sg.M[0], nm.g, nm.eps, nm.hi, nm.lo);
     return e;
 }
 
 template <int BN>
 cudaError_t launch_one(const CUtensorMap &ta, const void *bhi, const void *blo, int M, int N, int K, float *Y, int ldy,
-                       const float *R, float *part, int S, int *err, cudaStream_t s) {
+                       const float *R, float *part, int S, int *err, cudaStream_t s, const NormOut &nm) {
     Segs sg{};
     sg.n = 1;
     sg.tiles[0] = (M + 127) / 128;
@@ -903,7 +942,7 @@ cudaError_t launch_one(const CUtensorMap &ta, const void *bhi, const void *blo, 
     sg.ldy[0] = ldy;
     sg.R[0] = R;
     const CUtensorMap *tas[1] = {&ta};
-    return launch_gemm_bn<BN>(tas, sg, bhi, blo, N, K, part, S, err, s);
+    return launch_gemm_bn<BN>(tas, sg, bhi, blo, N, K, part, S, err, s, nm);
 }
 
 }  // namespace
@@ -912,20 +951,21 @@ bool encode_weight_map(CUtensorMap *map, const void *w, int rows, int K) { retur
 
 bool encode_gated_map(CUtensorMap *map, const void *w, int rows, int K) { return make_map(map, w, rows, K, 64); }
 
-size_t gemm_workspace_floats(int M, int N, int K, int n_sm) {
-    const GemmShape g = pick_shape(M, N, K, n_sm);
+size_t gemm_workspace_floats(int M, int N, int K, int n_sm, bool norm) {
+    const GemmShape g = pick_shape(M, N, K, n_sm, norm);
     return g.S > 1 ? (size_t)g.S * N * M : 0;
 }
 
 cudaError_t gemm(const CUtensorMap &wmap, const void *bhi, const void *blo, int M, int N, int K, float *Y, int ldy,
-                 const float *R, float *work, size_t work_floats, int *err, int n_sm, cudaStream_t s) {
-    if (K % 64 || M < 1 || N < 1) return cudaErrorInvalidValue;
-    const GemmShape g = pick_shape(M, N, K, n_sm);
+                 const float *R, float *work, size_t work_floats, int *err, int n_sm, cudaStream_t s,
+                 const NormOut &nm) {
+    if (K % 64 || M < 1 || N < 1 || (nm.g && ldy != M)) return cudaErrorInvalidValue;
+    const GemmShape g = pick_shape(M, N, K, n_sm, nm.g != nullptr);
     const int S = (size_t)g.S * N * M > work_floats ? 1 : g.S;  // no room for the partials: one pass
     switch (g.bn) {
-        case 128: return launch_one<128>(wmap, bhi, blo, M, N, K, Y, ldy, R, work, S, err, s);
-        case 64: return launch_one<64>(wmap, bhi, blo, M, N, K, Y, ldy, R, work, S, err, s);
-        default: return launch_one<32>(wmap, bhi, blo, M, N, K, Y, ldy, R, work, S, err, s);
+        case 128: return launch_one<128>(wmap, bhi, blo, M, N, K, Y, ldy, R, work, S, err, s, nm);
+        case 64: return launch_one<64>(wmap, bhi, blo, M, N, K, Y, ldy, R, work, S, err, s, nm);
+        default: return launch_one<32>(wmap, bhi, blo, M, N, K, Y, ldy, R, work, S, err, s, nm);
     }
 }
 
@@ -996,7 +1036,9 @@ cudaError_t run(const Model &m, const Scratch &sc, const int32_t *d_tokens, int 
         const LayerMaps &lm = m.maps[l];
         const size_t kv_off = (size_t)l * m.kv_layer_stride;
         // attention block
-        ok(launch_pdl(norm_split, dim3(n), dim3(256), 0, s, sc.X, d, m.attn_norm[l], m.eps, sc.Ahi, sc.Alo));
+        // (later layers: the previous down projection's split sum formed the norm)
+        if (l == 0)
+            ok(launch_pdl(norm_split, dim3(n), dim3(256), 0, s, sc.X, d, m.attn_norm[0], m.eps, sc.Ahi, sc.Alo));
         {  // q, k and v in one launch
             const CUtensorMap *maps[3] = {&lm.wq, &lm.wk, &lm.wv};
             const int Ms[3] = {qd, kvd, kvd}, lds[3] = {qkv, qkv, qkv};
@@ -1032,12 +1074,14 @@ cudaError_t run(const Model &m, const Scratch &sc, const int32_t *d_tokens, int 
             ok(launch_pdl(attend_prefill<128>, dim3((warps + wpb - 1) / wpb), dim3(wpb * 32), 0, s, sc.QKV, n, Hq,
                           Hkv, pos0, m.max_seq, m.kc + kv_off, m.vc + kv_off, sc.Ahi, sc.Alo));
         }
-        ok(gemm(lm.wo, sc.Ahi, sc.Alo, d, n, qd, sc.X, d, sc.X, sc.work, sc.work_floats, sc.err, m.n_sm, s));
-        // MLP block
-        ok(launch_pdl(norm_split, dim3(n), dim3(256), 0, s, sc.X, d, m.mlp_norm[l], m.eps, sc.Ahi, sc.Alo));
+        // O-projection + residual, then the MLP's RMSNorm
+        ok(gemm(lm.wo, sc.Ahi, sc.Alo, d, n, qd, sc.X, d, sc.X, sc.work, sc.work_floats, sc.err, m.n_sm, s,
+                NormOut{m.mlp_norm[l], m.eps, sc.Ahi, sc.Alo}));
         // gate and up in one launch, h = silu(g) * u formed in its epilogue
         ok(gemm_gated(lm.wg, lm.wu, F, sc.Ahi, sc.Alo, n, d, sc.Hhi, sc.Hlo, sc.err, m.n_sm, s));
-        ok(gemm(lm.wd, sc.Hhi, sc.Hlo, d, n, F, sc.X, d, sc.X, sc.work, sc.work_floats, sc.err, m.n_sm, s));
+        // down projection + residual, then the next layer's attention RMSNorm
+        const NormOut next = l + 1 < m.L ? NormOut{m.attn_norm[l + 1], m.eps, sc.Ahi, sc.Alo} : NormOut{};
+        ok(gemm(lm.wd, sc.Hhi, sc.Hlo, d, n, F, sc.X, d, sc.X, sc.work, sc.work_floats, sc.err, m.n_sm, s, next));
     }
     if (e != cudaSuccess) return e;
     // LM head of the last prompt position
@@ -1066,7 +1110,7 @@ extern "C" int mk_tc_gemm(const void *d_w, int32_t M, int32_t K, const void *d_b
     // when a larger contraction needs more; freed at exit)
     static float *work = nullptr;
     static size_t work_floats = 0;
-    const size_t need = mkpf::gemm_workspace_floats(M, N, K, n_sm);
+    const size_t need = mkpf::gemm_workspace_floats(M, N, K, n_sm, false);
     if (need > work_floats) {
         if (work) {
             cudaDeviceSynchronize();
@@ -1077,6 +1121,6 @@ extern "C" int mk_tc_gemm(const void *d_w, int32_t M, int32_t K, const void *d_b
         if (cudaMalloc(&work, need * sizeof(float)) == cudaSuccess) work_floats = need;
     }
     const cudaError_t e = mkpf::gemm(wm, d_bhi, d_blo, M, N, K, d_y, M, d_r, work, work_floats, d_status, n_sm,
-                                     static_cast<cudaStream_t>(stream));
+                                     static_cast<cudaStream_t>(stream), mkpf::NormOut{});
     return e == cudaSuccess ? 0 : -2;
 }

@@ -43,10 +43,20 @@ struct Scratch {
 bool encode_weight_map(CUtensorMap *map, const void *w, int rows, int K);
 bool encode_gated_map(CUtensorMap *map, const void *w, int rows, int K);  // W_gate / W_up, for gemm_gated
 
-// Y[n][m] (+)= W[m][.] . (Bhi[n][.] + Blo[n][.]) on the tensor cores; work
-// (work_floats floats) holds K-split partial sums (one pass if too small).
+// An RMSNorm formed from a contraction's output rows: hi / lo bf16 terms
+// [n][M] of RMSNorm(Y[n]) with gains g (g NULL: none).
+struct NormOut {
+    const uint16_t *g = nullptr;
+    float eps = 0.f;
+    uint16_t *hi = nullptr, *lo = nullptr;
+};
+
+// Y[n][m] (+)= W[m][.] . (Bhi[n][.] + Blo[n][.]) on the tensor cores, then
+// the norm nm of Y's rows (ldy == M); work (work_floats floats) holds K-split
+// partial sums (one pass if too small).
 cudaError_t gemm(const CUtensorMap &wmap, const void *bhi, const void *blo, int M, int N, int K, float *Y, int ldy,
-                 const float *R, float *work, size_t work_floats, int *err, int n_sm, cudaStream_t s);
+                 const float *R, float *work, size_t work_floats, int *err, int n_sm, cudaStream_t s,
+                 const NormOut &nm);
 
 // hi / lo bf16 terms of h[n][f] = silu(g) * u, g and u the rows f of W_gate
 // and W_up (maps from encode_gated_map) times Bhi[n][.] + Blo[n][.]; one
@@ -54,8 +64,9 @@ cudaError_t gemm(const CUtensorMap &wmap, const void *bhi, const void *blo, int 
 cudaError_t gemm_gated(const CUtensorMap &wg, const CUtensorMap &wu, int F, const void *bhi, const void *blo, int N,
                        int K, uint16_t *hhi, uint16_t *hlo, int *err, int n_sm, cudaStream_t s);
 
-// Floats of K-split workspace gemm() uses for this shape (0: none).
-size_t gemm_workspace_floats(int M, int N, int K, int n_sm);
+// Floats of K-split workspace gemm() uses for this shape, with or without a
+// norm of its output (0: none).
+size_t gemm_workspace_floats(int M, int N, int K, int n_sm, bool norm);
 
 // The prompt d_tokens[0 .. n) at positions pos0 .. pos0+n-1 through every
 // layer: K/V rows of every position into the cache, logits of the last
