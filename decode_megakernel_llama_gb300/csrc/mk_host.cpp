@@ -1002,11 +1002,13 @@ int mk_prefill(mk_handle *h, const int32_t *d_tokens, int32_t n, int32_t start_p
         // input of the projections from d or Hq hd columns, and that of the
         // down projection (h = silu(g) * u)
         const size_t kmax = std::max(d, qd), qkv = qd + 2 * kvd;
-        // K-split partials: the largest the O and down projections use (both
-        // feed an RMSNorm; q/k/v and gate/up run in one pass)
+        // K-split partials: the largest the q/k/v, O and down projections
+        // use (gate/up runs in one pass)
         const int nsm = h->im.n_sm;
-        const size_t work = std::max(mkpf::gemm_workspace_floats(d, n, qd, nsm, true),
-                                     mkpf::gemm_workspace_floats(d, n, F, nsm, true));
+        const int qkv_rows[3] = {qd, kvd, kvd};
+        const size_t work = std::max(std::max(mkpf::gemm_workspace_floats(d, n, qd, nsm, true),
+                                              mkpf::gemm_workspace_floats(d, n, F, nsm, true)),
+                                     mkpf::gemm_multi_workspace_floats(3, qkv_rows, n, d, nsm));
         // (+ 256 bytes of alignment for each of the 8 pieces)
         const size_t bytes = 4 * (size_t)n * (d + qkv) + 2 * 2 * (size_t)n * (kmax + F) +
                              8 * (size_t)2 * h->im.n_sm + 4 * work + 4 * 512;

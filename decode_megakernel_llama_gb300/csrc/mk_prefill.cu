@@ -35,6 +35,7 @@
 #include <stdint.h>
 #include <stdlib.h>
 
+#include <algorithm>
 #include <mutex>
 #include <vector>
 
@@ -197,12 +198,14 @@ __device__ __forceinline__ uint16_t f2bf_rne(float f) {
 // Up to three weight matrices multiplied by the same activations in one
 // launch: CTA row tiles 0 .. tiles[0]-1 take matrix 0 (tensor map ta0),
 // the next tiles[1] matrix 1 (ta1), then matrix 2 (ta2); each has its own
-// rows, output and residual.
+// rows, output and residual. With a K split the partial sums of split z go
+// to part[z][N][mtot], matrix q's rows from column off[q].
 struct Segs {
     int n;
     int tiles[3], M[3], ldy[3];
     float *Y[3];
     const float *R[3];
+    int mtot, off[3];
     uint16_t *hhi, *hlo;  // gated launches: the hi / lo bf16 terms of h [N][ldy[0]]
 };
 
@@ -237,14 +240,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     int ldy = sg.ldy[q];
     const float *R = sg.R[q];
     const int m0 = bx * (GATED ? 64 : 128), n0 = blockIdx.y * BN;
-    // K split over gridDim.z CTAs (one matrix only): this one takes 64-wide chunks c0 .. c0+nk-1
-    // and writes its partial sums to part[z][N][M] (summed later in a fixed
-    // order), or with one split the result itself
+    // K split over gridDim.z CTAs: this one takes 64-wide chunks c0 .. c0+nk-1
+    // and writes its partial sums to part[z][N][mtot] (summed later in a
+    // fixed order), or with one split the result itself
     const int nk_all = K / 64, z = blockIdx.z, S = gridDim.z;
     const int c0 = z * nk_all / S, nk = (z + 1) * nk_all / S - c0;
     if (S > 1) {
-        Y = part + (size_t)z * N * M;
-        ldy = M;
+        Y = part + (size_t)z * N * sg.mtot + sg.off[q];
+        ldy = sg.mtot;
         R = nullptr;
     }
     // the A tile of chunk kc into stage memory st (gated: gate rows, then up rows)
@@ -507,50 +510,97 @@ __global__ void norm_split(const float *X, int K, const uint16_t *g, float eps, 
 // The split sum of a residual contraction followed by the next RMSNorm:
 // for token n = blockIdx.x, Y[n][m] = R[n][m] + sum over z of part[z][n][m]
 // (z in order), then the RMSNorm of that row with gains g (as norm_split)
-// into hi / lo bf16 terms [n][M]. Each thread reads back only what it wrote.
-__global__ void sum_splits_norm(const float *part, int S, int N, int M, float *Y, int ldy, const float *R,
-                                const uint16_t *g, float eps, uint16_t *hi, uint16_t *lo) {
+// into hi / lo bf16 terms [n][M]. A thread keeps kSnE elements (M <=
+// kSnE * kSnThreads) and loads eight splits' partials of them before it adds
+// any, so a pass waits for about one memory round trip per eight splits.
+constexpr int kSnThreads = 512, kSnE = 8;
+
+__global__ void __launch_bounds__(kSnThreads) sum_splits_norm(const float *__restrict__ part, int S, int N, int M,
+                                                              float *__restrict__ Y, int ldy,
+                                                              const float *__restrict__ R,
+                                                              const uint16_t *__restrict__ g, float eps,
+                                                              uint16_t *__restrict__ hi, uint16_t *__restrict__ lo) {
     __shared__ float red[32];
     pdl_wait();
     pdl_trigger();
-    const int n = blockIdx.x;
+    const int n = blockIdx.x, tid = threadIdx.x;
     const size_t total = (size_t)N * M;
-    float *y = Y + (size_t)n * ldy;
+    const float *pn = part + (size_t)n * M;
+    float v[kSnE];
+#pragma unroll
+    for (int e = 0; e < kSnE; ++e) {
+        const int m = tid + e * kSnThreads;
+        v[e] = R && m < M ? R[(size_t)n * ldy + m] : 0.f;
+    }
+    for (int z0 = 0; z0 < S; z0 += 8) {
+        float w[8][kSnE];
+#pragma unroll
+        for (int dz = 0; dz < 8; ++dz)
+#pragma unroll
+            for (int e = 0; e < kSnE; ++e) {
+                const int m = tid + e * kSnThreads;
+                w[dz][e] = z0 + dz < S && m < M ? pn[(size_t)(z0 + dz) * total + m] : 0.f;
+            }
+#pragma unroll
+        for (int dz = 0; dz < 8; ++dz)
+#pragma unroll
+            for (int e = 0; e < kSnE; ++e)
+                if (z0 + dz < S) v[e] += w[dz][e];
+    }
     float ss = 0.f;
-    for (int m = threadIdx.x; m < M; m += blockDim.x) {
-        float v = R ? R[(size_t)n * ldy + m] : 0.f;
-        for (int z = 0; z < S; ++z) v += part[(size_t)z * total + (size_t)n * M + m];
-        y[m] = v;
-        ss = fmaf(v, v, ss);
+#pragma unroll
+    for (int e = 0; e < kSnE; ++e) {
+        const int m = tid + e * kSnThreads;
+        if (m < M) {
+            Y[(size_t)n * ldy + m] = v[e];
+            ss = fmaf(v[e], v[e], ss);
+        }
     }
     ss = block_sum(ss, red);
     const float scale = 1.0f / sqrtf(ss / (float)M + eps);
-    for (int m = threadIdx.x; m < M; m += blockDim.x) {
-        const float v = y[m] * (scale * bf2f(g[m]));
-        const uint16_t h = f2bf_rne(v);
-        hi[(size_t)n * M + m] = h;
-        lo[(size_t)n * M + m] = f2bf_rne(v - bf2f(h));
+#pragma unroll
+    for (int e = 0; e < kSnE; ++e) {
+        const int m = tid + e * kSnThreads;
+        if (m < M) {
+            const float x = v[e] * (scale * bf2f(g[m]));
+            const uint16_t h = f2bf_rne(x);
+            hi[(size_t)n * M + m] = h;
+            lo[(size_t)n * M + m] = f2bf_rne(x - bf2f(h));
+        }
     }
 }
 
 // RoPE on q and k of token t (position pos0 + t) from the fp32 QKV rows, q
 // kept (rotated) in place, bf16 k and v written into the cache at the position.
-__global__ void rope_append(float *QKV, int n, int Hq, int Hkv, int hd, int pos0, const float *rope, int max_seq,
-                            uint16_t *kc, uint16_t *vc) {
+// With S > 0 the q|k|v row is first summed from the K-split partials
+// part[z][t][.] (z in order) and the sums written back to QKV (q rotated).
+// The blocks of a token (gridDim.y of them) share its pairs.
+__global__ void rope_append(float *__restrict__ QKV, const float *__restrict__ part, int S, int n, int Hq, int Hkv,
+                            int hd, int pos0, const float *__restrict__ rope, int max_seq, uint16_t *__restrict__ kc,
+                            uint16_t *__restrict__ vc) {
     pdl_wait();
     pdl_trigger();
     const int t = blockIdx.x, pos = pos0 + t;
     const int stride = (Hq + 2 * Hkv) * hd, half = hd / 2;
     float *row = QKV + (size_t)t * stride;
-    for (int idx = threadIdx.x; idx < (Hq + Hkv) * half; idx += blockDim.x) {
+    const size_t zs = (size_t)n * stride;
+    const float *prow = part + (size_t)t * stride;
+    auto get = [&](int col) {
+        if (S == 0) return row[col];
+        float v = 0.f;
+        for (int z = 0; z < S; ++z) v += prow[z * zs + col];
+        return v;
+    };
+    const int first = blockIdx.y * blockDim.x + threadIdx.x, step = gridDim.y * blockDim.x;
+    for (int idx = first; idx < (Hq + Hkv) * half; idx += step) {
         const int h = idx / half, i = idx % half;
-        float *v = row + (size_t)h * hd;
+        const int ca = h * hd + i, cb = ca + half;
         const float c = rope[((size_t)pos * half + i) * 2], s = rope[((size_t)pos * half + i) * 2 + 1];
-        const float a = v[i], b = v[i + half];
+        const float a = get(ca), b = get(cb);
         const float ra = a * c - b * s, rb = b * c + a * s;
         if (h < Hq) {
-            v[i] = ra;
-            v[i + half] = rb;
+            row[ca] = ra;
+            row[cb] = rb;
         } else {
             const int kvh = h - Hq;
             const size_t off = ((size_t)kvh * max_seq + pos) * hd;
@@ -558,9 +608,9 @@ __global__ void rope_append(float *QKV, int n, int Hq, int Hkv, int hd, int pos0
             kc[off + i + half] = f2bf_rne(rb);
         }
     }
-    for (int idx = threadIdx.x; idx < Hkv * hd; idx += blockDim.x) {
+    for (int idx = first; idx < Hkv * hd; idx += step) {
         const int kvh = idx / hd, i = idx % hd;
-        vc[((size_t)kvh * max_seq + pos) * hd + i] = f2bf_rne(row[(size_t)(Hq + Hkv) * hd + idx]);
+        vc[((size_t)kvh * max_seq + pos) * hd + i] = f2bf_rne(get((Hq + Hkv) * hd + idx));
     }
 }
 
@@ -878,9 +928,26 @@ struct GemmShape {
     int bn, S;
 };
 
+// A prompt of at most 32 tokens is one token tile: the weights' row tiles
+// alone give too few CTAs to stream them at the memory's rate, so the
+// reduction is split until the grid fills the SMs, with at least 4 chunks
+// per split.
+int small_splits(int tiles, int nk, int n_sm) {
+    int S = n_sm / tiles;
+    if (S > nk / 4) S = nk / 4;
+    if (S > kMaxSplits) S = kMaxSplits;
+    return S < 1 ? 1 : S;
+}
+
 GemmShape pick_shape(int M, int N, int K, int n_sm, bool norm) {
     const int rt = (M + 127) / 128, nk = K / 64;
     GemmShape g{128, 1};
+    if (N <= 32) {
+        g.bn = 32;
+        g.S = small_splits(rt, nk, n_sm);
+        if (norm && g.S < 2 && nk >= 2) g.S = 2;
+        return g;
+    }
     if (nk >= 64) {
         const int ctas = rt * ((N + 127) / 128);
         int S = n_sm / ctas;
@@ -902,9 +969,12 @@ GemmShape pick_shape(int M, int N, int K, int n_sm, bool norm) {
     return g;
 }
 
+// keep_partials: with a K split the partial sums stay in part for the
+// caller's own pass (no split-sum launch).
 template <int BN, bool GATED = false>
 cudaError_t launch_gemm_bn(const CUtensorMap *const *tas, const Segs &sg, const void *bhi, const void *blo, int N,
-                           int K, float *part, int S, int *err, cudaStream_t s, const NormOut &nm = NormOut{}) {
+                           int K, float *part, int S, int *err, cudaStream_t s, const NormOut &nm = NormOut{},
+                           bool keep_partials = false) {
     CUtensorMap th, tl;
     if (!make_map(&th, bhi, N, K, BN) || !make_map(&tl, blo, N, K, BN)) return cudaErrorInvalidValue;
     constexpr int smem = gemm_smem_bytes<BN>();
@@ -921,12 +991,13 @@ cudaError_t launch_gemm_bn(const CUtensorMap *const *tas, const Segs &sg, const 
     const CUtensorMap &a0 = *tas[0], &a1 = GATED || sg.n > 1 ? *tas[1] : *tas[0], &a2 = sg.n > 2 ? *tas[2] : *tas[0];
     cudaError_t e =
         launch_pdl(tc_gemm<BN, GATED>, grid, dim3(kThreads), smem, s, a0, a1, a2, th, tl, sg, N, K, part, err);
-    if (e == cudaSuccess && S > 1 && nm.g)
-        e = launch_pdl(sum_splits_norm, dim3(N), dim3(256), 0, s, part, S, N, sg.M[0], sg.Y[0], sg.ldy[0], sg.R[0],
-                       nm.g, nm.eps, nm.hi, nm.lo);
-    else if (e == cudaSuccess && S > 1)
-        e = launch_pdl(sum_splits, dim3(256), dim3(256), 0, s, part, S, N, sg.M[0], sg.Y[0], sg.ldy[0], sg.R[0]);
-    else if (e == cudaSuccess && nm.g)  // one pass: the norm on its own
+    if (e != cudaSuccess || (S > 1 && keep_partials)) return e;
+    const bool fused = nm.g && sg.M[0] <= kSnE * kSnThreads;
+    if (S > 1 && fused)
+        return launch_pdl(sum_splits_norm, dim3(N), dim3(kSnThreads), 0, s, part, S, N, sg.M[0], sg.Y[0], sg.ldy[0],
+                          sg.R[0], nm.g, nm.eps, nm.hi, nm.lo);
+    if (S > 1) e = launch_pdl(sum_splits, dim3(256), dim3(256), 0, s, part, S, N, sg.M[0], sg.Y[0], sg.ldy[0], sg.R[0]);
+    if (e == cudaSuccess && nm.g)  // the norm on its own
         e = launch_pdl(norm_split, dim3(N), dim3(256), 0, s, sg.Y[0], sg.M[0], nm.g, nm.eps, nm.hi, nm.lo);
     return e;
 }
@@ -941,6 +1012,7 @@ cudaError_t launch_one(const CUtensorMap &ta, const void *bhi, const void *blo, 
     sg.Y[0] = Y;
     sg.ldy[0] = ldy;
     sg.R[0] = R;
+    sg.mtot = M;
     const CUtensorMap *tas[1] = {&ta};
     return launch_gemm_bn<BN>(tas, sg, bhi, blo, N, K, part, S, err, s, nm);
 }
@@ -970,7 +1042,9 @@ cudaError_t gemm(const CUtensorMap &wmap, const void *bhi, const void *blo, int 
 }
 
 cudaError_t gemm_multi(int nseg, const CUtensorMap *const *maps, const int *M, float *const *Y, const int *ldy,
-                       const void *bhi, const void *blo, int N, int K, int *err, int n_sm, cudaStream_t s) {
+                       const void *bhi, const void *blo, int N, int K, int *err, int n_sm, cudaStream_t s, float *work,
+                       size_t work_floats, int *S_used) {
+    *S_used = 1;
     if (K % 64 || N < 1 || nseg < 1 || nseg > 3) return cudaErrorInvalidValue;
     Segs sg{};
     sg.n = nseg;
@@ -982,7 +1056,15 @@ cudaError_t gemm_multi(int nseg, const CUtensorMap *const *maps, const int *M, f
         sg.Y[i] = Y[i];
         sg.ldy[i] = ldy[i];
         sg.R[i] = nullptr;
+        sg.off[i] = sg.mtot;
+        sg.mtot += M[i];
         tiles += sg.tiles[i];
+    }
+    if (N <= 32) {
+        int S = small_splits(tiles, K / 64, n_sm);
+        if ((size_t)S * N * sg.mtot > work_floats) S = 1;
+        *S_used = S;
+        return launch_gemm_bn<32>(maps, sg, bhi, blo, N, K, work, S, err, s, NormOut{}, true);
     }
     // the smallest token tile whose grid fits one wave (as pick_shape)
     int bn = 128;
@@ -998,6 +1080,16 @@ cudaError_t gemm_multi(int nseg, const CUtensorMap *const *maps, const int *M, f
     }
 }
 
+size_t gemm_multi_workspace_floats(int nseg, const int *M, int N, int K, int n_sm) {
+    if (N > 32) return 0;
+    int tiles = 0, mtot = 0;
+    for (int i = 0; i < nseg; ++i) {
+        tiles += (M[i] + 127) / 128;
+        mtot += M[i];
+    }
+    return (size_t)small_splits(tiles, K / 64, n_sm) * N * mtot;
+}
+
 cudaError_t gemm_gated(const CUtensorMap &wg, const CUtensorMap &wu, int F, const void *bhi, const void *blo, int N,
                        int K, uint16_t *hhi, uint16_t *hlo, int *err, int n_sm, cudaStream_t s) {
     if (K % 64 || N < 1 || F < 1) return cudaErrorInvalidValue;
@@ -1006,6 +1098,7 @@ cudaError_t gemm_gated(const CUtensorMap &wg, const CUtensorMap &wu, int F, cons
     sg.tiles[0] = (F + 63) / 64;
     sg.M[0] = F;
     sg.ldy[0] = F;
+    sg.mtot = F;
     sg.hhi = hhi;
     sg.hlo = hlo;
     const CUtensorMap *maps[2] = {&wg, &wu};
@@ -1043,10 +1136,14 @@ cudaError_t run(const Model &m, const Scratch &sc, const int32_t *d_tokens, int 
             const CUtensorMap *maps[3] = {&lm.wq, &lm.wk, &lm.wv};
             const int Ms[3] = {qd, kvd, kvd}, lds[3] = {qkv, qkv, qkv};
             float *Ys[3] = {sc.QKV, sc.QKV + qd, sc.QKV + qd + kvd};
-            ok(gemm_multi(3, maps, Ms, Ys, lds, sc.Ahi, sc.Alo, n, d, sc.err, m.n_sm, s));
+            int Sq = 1;
+            ok(gemm_multi(3, maps, Ms, Ys, lds, sc.Ahi, sc.Alo, n, d, sc.err, m.n_sm, s, sc.work, sc.work_floats,
+                          &Sq));
+            // RoPE and the KV append (a short prompt: from the split partial sums)
+            const int per_tok = n >= 64 ? 1 : std::min(8, (64 + n - 1) / n);
+            ok(launch_pdl(rope_append, dim3(n, per_tok), dim3(256), 0, s, sc.QKV, Sq > 1 ? sc.work : nullptr,
+                          Sq > 1 ? Sq : 0, n, Hq, Hkv, hd, pos0, m.rope, m.max_seq, m.kc + kv_off, m.vc + kv_off));
         }
-        ok(launch_pdl(rope_append, dim3(n), dim3(256), 0, s, sc.QKV, n, Hq, Hkv, hd, pos0, m.rope, m.max_seq,
-                      m.kc + kv_off, m.vc + kv_off));
         const int warps = n * Hq, wpb = 4;
         if (pos0 + n <= kMaxStagedPos) {
             // every position the prompt attends to fits the staged rows

@@ -68,6 +68,10 @@ cudaError_t gemm_gated(const CUtensorMap &wg, const CUtensorMap &wu, int F, cons
 // norm of its output (0: none).
 size_t gemm_workspace_floats(int M, int N, int K, int n_sm, bool norm);
 
+// Floats of K-split partials the prefill's q/k/v launch (nseg matrices of M[i]
+// rows) leaves for its RoPE pass (0: none).
+size_t gemm_multi_workspace_floats(int nseg, const int *M, int N, int K, int n_sm);
+
 // The prompt d_tokens[0 .. n) at positions pos0 .. pos0+n-1 through every
 // layer: K/V rows of every position into the cache, logits of the last
 // position into out_logits (nullable) and its greedy token into out_token.

@@ -101,6 +101,13 @@ def test_llama1b_prefill_of_the_workload_prompt(cuda_dev):
     pair.close()
 
 
+def test_llama1b_prefill_of_a_short_prompt(cuda_dev):
+    # at most 32 tokens: one token tile, every projection's reduction split
+    # over up to 9 CTAs and summed in the RoPE and norm passes
+    pair, _, _ = prefill_case(LLAMA_1B, 11, 24, 2)
+    pair.close()
+
+
 def test_llama3b_prefill_head_dim_128(cuda_dev):
     pair, _, _ = prefill_case(LLAMA_3B, 64, 72, 2)
     pair.close()
