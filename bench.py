@@ -52,6 +52,9 @@ def parse():
     ap.add_argument("--profile-gemm", action="store_true",
                     help="only W + K runs of the prefill's gate contraction (tensor cores) for the "
                          "workload's prompt (for ncu captures); prints one line")
+    ap.add_argument("--profile-w2a8", action="store_true",
+                    help="only W + K launches of the W2A8 GEMV over the bench's 134 MB packed matrix "
+                         "(for ncu captures); prints one line")
     ap.add_argument("--trace", default=None,
                     help="also record one traced step and write its summary (JSON) here")
     return ap.parse_args()
@@ -473,6 +476,26 @@ def run_profile_gemm(args):
           flush=True)
 
 
+def run_profile_w2a8(args):
+    """W + K launches of the W2A8 GEMV over the same 65,536 x 8,192 packed
+    matrix the bench line times, nothing else."""
+    import torch
+    from decode_megakernel_llama_gb300 import _lib
+    from decode_megakernel_llama_gb300.build import build
+    build()
+    dev = torch.device("cuda", 0)
+    g = torch.Generator(device="cpu").manual_seed(7)
+    rows, cols = 65536, 8192
+    packed = torch.randint(0, 2 ** 31 - 1, (rows, cols // 16), generator=g, dtype=torch.int32)
+    packed = (packed & 0x55555555).to(dev)  # codes 0 or 1 (weights -1 / 0): valid words
+    xv = torch.randn(cols, generator=g).to(dev)
+    yv = torch.empty(rows, device=dev)
+    for _ in range(args.warmup + args.steps):
+        _lib.w2a8_gemv(packed, 0.02, rows, cols, xv, yv)
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_w2a8": True, "launches": args.warmup + args.steps}), flush=True)
+
+
 def run_profile_prefill(args):
     """W + K prefills (mk_prefill) of the workload's prompt, nothing else."""
     import torch
@@ -828,6 +851,8 @@ def main():
         run_profile_prefill(args)
     elif args.profile_twell:
         run_profile_twell(args)
+    elif args.profile_w2a8:
+        run_profile_w2a8(args)
     elif WORKLOADS[args.workload].batch > 1:
         run_batch(args, ws, rank, local)
     else:

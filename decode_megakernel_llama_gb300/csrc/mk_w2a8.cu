@@ -50,14 +50,26 @@ __device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
     return v;
 }
 
+// dp4a with unsigned bytes in a and signed bytes in b.
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
 // One 16-byte chunk (4 words, 64 elements) against its 16 words of codes.
+// The codes of bit pair j are taken in place, word & (0x03030303 << 2j):
+// bytes code * 4^j (at most 128, hence unsigned bytes), so pair j's products
+// sum to 4^j times its dot product. The four sums are exact integers and
+// shift back without remainder: no shift per word.
 __device__ __forceinline__ int dot_chunk(const uint4 w, const uint32_t (&xq)[16], int acc) {
     const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+    int a[4] = {0, 0, 0, 0};
 #pragma unroll
     for (int m = 0; m < 4; ++m)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) acc = __dp4a((int)((ws[m] >> (2 * j)) & 0x03030303u), (int)xq[4 * m + j], acc);
-    return acc;
+        for (int j = 0; j < 4; ++j) a[j] = dp4a_us(ws[m] & (0x03030303u << (2 * j)), xq[4 * m + j], a[j]);
+    return acc + a[0] + (a[1] >> 2) + (a[2] >> 4) + (a[3] >> 6);
 }
 
 // Reduce-scatter of 8 per-lane integers over the warp: afterwards lane l
