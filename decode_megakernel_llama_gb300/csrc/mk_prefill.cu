@@ -689,61 +689,70 @@ __global__ void attend_prefill(const float *QKV, int n, int Hq, int Hkv, int pos
 
 // The same causal attention with the kv head's cached rows staged in shared
 // memory: CTA (kv head, block of kQB prompt tokens) copies the keys and
-// values of positions 0 .. Tmax-1 (all the block's tokens see), rows padded
-// by 16 bytes so that the lanes' 16-byte key reads spread over the banks;
-// then warp w takes the (token, query head) pairs w, w + 16, ... of the block
-// (one each for G <= 4). Scores use four partial sums per lane and P.V two
-// per output, to shorten the dependent chains.
+// values of the positions its tokens see, tile by tile of cap rows (cap =
+// kStageTile, or all positions when fewer; rows padded by 16 bytes so that
+// the lanes' 16-byte key reads spread over the banks); warp w takes the
+// (token, query head) pair w of the block (G <= 4 query heads per kv head)
+// and carries its online-softmax state (m, l, o) from tile to tile.
+// Positions go by in chunks of 32 whatever the tiling, so the result does not
+// depend on cap. Scores use four partial sums per lane and P.V two per
+// output, to shorten the dependent chains.
 constexpr int kQB = 4;
-constexpr int kMaxStagedPos = 256;
+constexpr int kStageTile = 256;
 constexpr int kStagedWarps = 16;
+static_assert(kStageTile % 32 == 0, "tiles hold whole chunks of 32 positions");
 
 template <int HD>
 __global__ void __launch_bounds__(kStagedWarps * 32) attend_prefill_staged(const float *QKV, int n, int Hq, int Hkv,
-                                                                            int pos0, int max_seq, int Tcap,
+                                                                            int pos0, int max_seq, int cap,
                                                                             const uint16_t *kc, const uint16_t *vc,
                                                                             uint16_t *out_hi, uint16_t *out_lo) {
     constexpr int RS = HD + 8;  // row stride in bf16 elements (16 bytes of padding)
+    constexpr int CPR = HD / 8; // 16-byte chunks per row
+    constexpr int DP = HD / 32;
     extern __shared__ uint16_t kvs[];
     pdl_wait();
     pdl_trigger();
-    uint16_t *Ks = kvs, *Vs = kvs + (size_t)Tcap * RS;
+    uint16_t *Ks = kvs, *Vs = kvs + (size_t)cap * RS;
     const int kvh = blockIdx.x, t0 = blockIdx.y * kQB, G = Hq / Hkv;
     const int tl = min(n, t0 + kQB);  // tokens t0 .. tl-1
-    const int Tmax = pos0 + tl;
+    const int Tmax = pos0 + tl;       // positions the block's tokens see
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    {
-        const uint4 *Kg = reinterpret_cast<const uint4 *>(kc + (size_t)kvh * max_seq * HD);
-        const uint4 *Vg = reinterpret_cast<const uint4 *>(vc + (size_t)kvh * max_seq * HD);
-        constexpr int CPR = HD / 8;  // 16-byte chunks per row
-        for (int i = tid; i < Tmax * CPR; i += blockDim.x) {
-            const int r = i / CPR, c = i % CPR;
-            *reinterpret_cast<uint4 *>(Ks + (size_t)r * RS + c * 8) = Kg[(size_t)r * CPR + c];
-            *reinterpret_cast<uint4 *>(Vs + (size_t)r * RS + c * 8) = Vg[(size_t)r * CPR + c];
-        }
-    }
-    __syncthreads();
+    const bool active = warp < (tl - t0) * G;
+    const int t = t0 + warp / G, h = kvh * G + warp % G;
+    const int T = pos0 + t + 1;  // positions this pair sees
     const int stride = (Hq + 2 * Hkv) * HD;
-    const float scale = rsqrtf((float)HD);
-    constexpr int DP = HD / 32;
-    for (int pr = warp; pr < (tl - t0) * G; pr += kStagedWarps) {
-        const int t = t0 + pr / G, h = kvh * G + pr % G;
-        const int T = pos0 + t + 1;
+    float qr[HD];
+    if (active) {
+        const float scale = rsqrtf((float)HD);
         const float *q = QKV + (size_t)t * stride + (size_t)h * HD;
-        float qr[HD];
 #pragma unroll
         for (int i = 0; i < HD; ++i) qr[i] = q[i] * scale;
-        float o[2][DP], m = -INFINITY, l = 0.f;
+    }
+    float o[2][DP], m = -INFINITY, l = 0.f;
 #pragma unroll
-        for (int e = 0; e < DP; ++e) o[0][e] = o[1][e] = 0.f;
-        for (int j0 = 0; j0 < T; j0 += 32) {
+    for (int e = 0; e < DP; ++e) o[0][e] = o[1][e] = 0.f;
+    const uint4 *Kg = reinterpret_cast<const uint4 *>(kc + (size_t)kvh * max_seq * HD);
+    const uint4 *Vg = reinterpret_cast<const uint4 *>(vc + (size_t)kvh * max_seq * HD);
+    for (int k0 = 0; k0 < Tmax; k0 += cap) {
+        const int kn = min(cap, Tmax - k0);
+        __syncthreads();  // every warp is done with the previous tile
+        for (int i = tid; i < kn * CPR; i += blockDim.x) {
+            const int r = i / CPR, c = i % CPR;
+            *reinterpret_cast<uint4 *>(Ks + (size_t)r * RS + c * 8) = Kg[(size_t)(k0 + r) * CPR + c];
+            *reinterpret_cast<uint4 *>(Vs + (size_t)r * RS + c * 8) = Vg[(size_t)(k0 + r) * CPR + c];
+        }
+        __syncthreads();
+        if (!active) continue;
+        const int te = min(T, k0 + kn);  // this pair's positions in the tile: k0 .. te-1
+        for (int j0 = k0; j0 < te; j0 += 32) {
             const int j = j0 + lane;
             float s = -INFINITY;
-            if (j < T) {
-                const uint4 *kr = reinterpret_cast<const uint4 *>(Ks + (size_t)j * RS);
+            if (j < te) {
+                const uint4 *kr = reinterpret_cast<const uint4 *>(Ks + (size_t)(j - k0) * RS);
                 float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int c = 0; c < HD / 8; ++c) {
+                for (int c = 0; c < CPR; ++c) {
                     const uint4 w = kr[c];
                     const uint32_t u[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
@@ -758,7 +767,7 @@ __global__ void __launch_bounds__(kStagedWarps * 32) attend_prefill_staged(const
             for (int off = 16; off > 0; off >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xFFFFFFFFu, cm, off));
             const float mn = fmaxf(m, cm);
             const float corr = __expf(m - mn);
-            const float p = j < T ? __expf(s - mn) : 0.f;
+            const float p = j < te ? __expf(s - mn) : 0.f;
             float ps = p;
             for (int off = 16; off > 0; off >>= 1) ps += __shfl_xor_sync(0xFFFFFFFFu, ps, off);
             l = l * corr + ps;
@@ -768,8 +777,8 @@ __global__ void __launch_bounds__(kStagedWarps * 32) attend_prefill_staged(const
                 o[0][e] *= corr;
                 o[1][e] *= corr;
             }
-            const int cnt = T - j0 < 32 ? T - j0 : 32;
-            const uint16_t *vb = Vs + (size_t)j0 * RS + lane * DP;
+            const int cnt = te - j0 < 32 ? te - j0 : 32;
+            const uint16_t *vb = Vs + (size_t)(j0 - k0) * RS + lane * DP;
 #pragma unroll 8
             for (int jj = 0; jj < cnt; ++jj) {
                 const float pj = __shfl_sync(0xFFFFFFFFu, p, jj);
@@ -777,14 +786,15 @@ __global__ void __launch_bounds__(kStagedWarps * 32) attend_prefill_staged(const
                 for (int e = 0; e < DP; ++e) o[jj & 1][e] = fmaf(pj, bf2f(vb[(size_t)jj * RS + e]), o[jj & 1][e]);
             }
         }
-        const size_t at = (size_t)t * Hq * HD + (size_t)h * HD + lane * DP;
+    }
+    if (!active) return;
+    const size_t at = (size_t)t * Hq * HD + (size_t)h * HD + lane * DP;
 #pragma unroll
-        for (int e = 0; e < DP; ++e) {
-            const float v = (o[0][e] + o[1][e]) / l;
-            const uint16_t hb = f2bf_rne(v);
-            out_hi[at + e] = hb;
-            out_lo[at + e] = f2bf_rne(v - bf2f(hb));
-        }
+    for (int e = 0; e < DP; ++e) {
+        const float v = (o[0][e] + o[1][e]) / l;
+        const uint16_t hb = f2bf_rne(v);
+        out_hi[at + e] = hb;
+        out_lo[at + e] = f2bf_rne(v - bf2f(hb));
     }
 }
 
@@ -1145,25 +1155,26 @@ cudaError_t run(const Model &m, const Scratch &sc, const int32_t *d_tokens, int 
                           Sq > 1 ? Sq : 0, n, Hq, Hkv, hd, pos0, m.rope, m.max_seq, m.kc + kv_off, m.vc + kv_off));
         }
         const int warps = n * Hq, wpb = 4;
-        if (pos0 + n <= kMaxStagedPos) {
-            // every position the prompt attends to fits the staged rows
-            const int Tcap = pos0 + n;
+        if ((Hq / Hkv) * kQB <= kStagedWarps) {
+            // one warp per (token, query head) of a block: keys and values
+            // staged tile by tile in shared memory
+            const int cap = std::min(pos0 + n, kStageTile);
             const dim3 grid(Hkv, (n + kQB - 1) / kQB);
-            const size_t smem = 2 * (size_t)Tcap * (hd + 8) * 2;
+            const size_t smem = 2 * (size_t)cap * (hd + 8) * 2;
             static bool configured = false;
             if (!configured) {
                 ok(cudaFuncSetAttribute(attend_prefill_staged<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        2 * kMaxStagedPos * (64 + 8) * 2));
+                                        2 * kStageTile * (64 + 8) * 2));
                 ok(cudaFuncSetAttribute(attend_prefill_staged<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        2 * kMaxStagedPos * (128 + 8) * 2));
+                                        2 * kStageTile * (128 + 8) * 2));
                 configured = e == cudaSuccess;
             }
             if (hd == 64)
                 ok(launch_pdl(attend_prefill_staged<64>, grid, dim3(kStagedWarps * 32), smem, s, sc.QKV, n, Hq, Hkv,
-                              pos0, m.max_seq, Tcap, m.kc + kv_off, m.vc + kv_off, sc.Ahi, sc.Alo));
+                              pos0, m.max_seq, cap, m.kc + kv_off, m.vc + kv_off, sc.Ahi, sc.Alo));
             else
                 ok(launch_pdl(attend_prefill_staged<128>, grid, dim3(kStagedWarps * 32), smem, s, sc.QKV, n, Hq, Hkv,
-                              pos0, m.max_seq, Tcap, m.kc + kv_off, m.vc + kv_off, sc.Ahi, sc.Alo));
+                              pos0, m.max_seq, cap, m.kc + kv_off, m.vc + kv_off, sc.Ahi, sc.Alo));
         } else if (hd == 64) {
             ok(launch_pdl(attend_prefill<64>, dim3((warps + wpb - 1) / wpb), dim3(wpb * 32), 0, s, sc.QKV, n, Hq, Hkv,
                           pos0, m.max_seq, m.kc + kv_off, m.vc + kv_off, sc.Ahi, sc.Alo));

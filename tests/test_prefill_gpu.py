@@ -10,7 +10,7 @@ import torch
 
 from decode_megakernel_llama_gb300 import _lib, synth
 from decode_megakernel_llama_gb300.build import build
-from decode_megakernel_llama_gb300.configs import LLAMA_1B, LLAMA_3B, TINY, WORKLOADS
+from decode_megakernel_llama_gb300.configs import LLAMA_1B, LLAMA_3B, TINY, WORKLOADS, ModelShape
 
 from gpu_helpers import MAX_ABS, Pair, compare, teacher_forced
 
@@ -92,6 +92,14 @@ def test_tiny_prefill_of_a_long_second_part(cuda_dev):
     # the second part starts at position 200 and attends to up to 300
     # positions: the cached rows of the first part and its own
     pair, _, _ = prefill_case(TINY, 300, 304, 2, start_split=200)
+    pair.close()
+
+
+def test_prefill_head_dim_128_over_several_key_tiles(cuda_dev):
+    # head dim 128, three query heads per kv head (as the 3B shape), and a
+    # second part that attends to up to 600 positions: three staged key tiles
+    shape = ModelShape("hd128-g3", 2, 768, 6, 2, 128, 1536, 2048, 1e-5, 5e5)
+    pair, _, _ = prefill_case(shape, 600, 608, 2, start_split=257)
     pair.close()
 
 
