@@ -782,8 +782,20 @@ __global__ void __launch_bounds__(kStagedWarps * 32) attend_prefill_staged(const
 #pragma unroll 8
             for (int jj = 0; jj < cnt; ++jj) {
                 const float pj = __shfl_sync(0xFFFFFFFFu, p, jj);
+                // the lane's DP values of row jj in one 4- or 8-byte load
+                uint32_t u[DP / 2];
+                if constexpr (DP == 2) {
+                    u[0] = *reinterpret_cast<const uint32_t *>(vb + (size_t)jj * RS);
+                } else {
+                    const uint2 w = *reinterpret_cast<const uint2 *>(vb + (size_t)jj * RS);
+                    u[0] = w.x;
+                    u[1] = w.y;
+                }
 #pragma unroll
-                for (int e = 0; e < DP; ++e) o[jj & 1][e] = fmaf(pj, bf2f(vb[(size_t)jj * RS + e]), o[jj & 1][e]);
+                for (int e = 0; e < DP; e += 2) {
+                    o[jj & 1][e] = fmaf(pj, __uint_as_float(u[e / 2] << 16), o[jj & 1][e]);
+                    o[jj & 1][e + 1] = fmaf(pj, __uint_as_float(u[e / 2] & 0xFFFF0000u), o[jj & 1][e + 1]);
+                }
             }
         }
     }
