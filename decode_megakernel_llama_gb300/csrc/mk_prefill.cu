@@ -27,6 +27,12 @@
 // the count of MMA instructions (a near-fixed cost each at these sizes), and
 // this halves it.
 //
+// The causal attention over the prompt (attend_prefill_mma) also runs on the
+// tensor cores, with warp-level mma.sync (its softmax sits between two small
+// products per 64-position tile, row by row in registers): queries and
+// probabilities enter as hi / lo bf16 terms, keys and values are the cache's
+// bf16 rows.
+//
 // Every wait is bounded (%globaltimer, 2 s); on expiry the kernel records an
 // error in a status word, still drains its copies and frees its tensor
 // memory, and returns.
@@ -614,199 +620,194 @@ __global__ void rope_append(float *__restrict__ QKV, const float *__restrict__ p
     }
 }
 
-// Causal attention: one warp per (token t, query head h) over cache
-// positions 0 .. pos0 + t of kv head h / G, online softmax in chunks of 32
-// positions (lane = position for the scores, lane = dimension pair for P.V).
-// The output row [n][Hq*HD] is written as the hi/lo bf16 terms the
-// O-projection reads.
-template <int HD>
-__global__ void attend_prefill(const float *QKV, int n, int Hq, int Hkv, int pos0, int max_seq,
-                               const uint16_t *kc, const uint16_t *vc, uint16_t *out_hi, uint16_t *out_lo) {
-    pdl_wait();
-    pdl_trigger();
-    const int warp_global = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (warp_global >= n * Hq) return;
-    const int t = warp_global / Hq, h = warp_global % Hq, G = Hq / Hkv, kvh = h / G;
-    const int T = pos0 + t + 1;
-    const int stride = (Hq + 2 * Hkv) * HD;
-    const float *q = QKV + (size_t)t * stride + (size_t)h * HD;
-    const float scale = rsqrtf((float)HD);
-    float qr[HD];
-#pragma unroll
-    for (int i = 0; i < HD; ++i) qr[i] = q[i] * scale;
-    const uint16_t *K = kc + (size_t)kvh * max_seq * HD, *V = vc + (size_t)kvh * max_seq * HD;
-    constexpr int DP = HD / 32;  // output dims per lane
-    float o[DP], m = -INFINITY, l = 0.f;
-#pragma unroll
-    for (int e = 0; e < DP; ++e) o[e] = 0.f;
-    for (int j0 = 0; j0 < T; j0 += 32) {
-        const int j = j0 + lane;
-        float s = -INFINITY;
-        if (j < T) {
-            const uint4 *kr = reinterpret_cast<const uint4 *>(K + (size_t)j * HD);
-            float acc = 0.f;
-#pragma unroll
-            for (int c = 0; c < HD / 8; ++c) {
-                const uint4 w = kr[c];
-                const uint32_t u[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    acc = fmaf(__uint_as_float(u[e] << 16), qr[c * 8 + 2 * e], acc);
-                    acc = fmaf(__uint_as_float(u[e] & 0xFFFF0000u), qr[c * 8 + 2 * e + 1], acc);
-                }
-            }
-            s = acc;
-        }
-        float cm = s;
-        for (int off = 16; off > 0; off >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xFFFFFFFFu, cm, off));
-        const float mn = fmaxf(m, cm);
-        const float corr = __expf(m - mn);
-        const float p = j < T ? __expf(s - mn) : 0.f;
-        float ps = p;
-        for (int off = 16; off > 0; off >>= 1) ps += __shfl_xor_sync(0xFFFFFFFFu, ps, off);
-        l = l * corr + ps;
-        m = mn;
-#pragma unroll
-        for (int e = 0; e < DP; ++e) o[e] *= corr;
-        const int cnt = T - j0 < 32 ? T - j0 : 32;
-        for (int jj = 0; jj < cnt; ++jj) {
-            const float pj = __shfl_sync(0xFFFFFFFFu, p, jj);
-            const uint16_t *vr = V + (size_t)(j0 + jj) * HD + lane * DP;
-#pragma unroll
-            for (int e = 0; e < DP; ++e) o[e] = fmaf(pj, bf2f(vr[e]), o[e]);
-        }
-    }
-    const size_t at = (size_t)t * Hq * HD + (size_t)h * HD + lane * DP;
-#pragma unroll
-    for (int e = 0; e < DP; ++e) {
-        const float v = o[e] / l;
-        const uint16_t hb = f2bf_rne(v);
-        out_hi[at + e] = hb;
-        out_lo[at + e] = f2bf_rne(v - bf2f(hb));
-    }
+// Causal attention of the prompt on the tensor cores (mma.sync m16n8k16,
+// bf16 operands, fp32 accumulators), flash-attention style. CTA (kv head,
+// block of QB = 64 / G prompt tokens) holds 64 query rows, row r = (token
+// t0 + r / G, query head kvh * G + r % G); warp w owns rows 16w .. 16w+15.
+// Keys and values go through shared memory in tiles of 64 positions (rows
+// padded by 16 bytes: conflict-free fragment loads). Per tile a warp forms
+// S = (q/sqrt(hd)) K^T from the hi and lo bf16 terms of its scaled queries
+// (two MMAs per fragment), masks the positions past each row's own, updates
+// the rows' running max and sum (online softmax) and adds P V with P as hi
+// and lo bf16 terms; V's fragments come from ldmatrix.trans. The output goes
+// out as the hi / lo bf16 terms the O-projection reads.
+constexpr int kFaWarps = 4;
+constexpr int kFaRows = kFaWarps * 16;
+constexpr int kFaKeys = 64;
+
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// The same causal attention with the kv head's cached rows staged in shared
-// memory: CTA (kv head, block of kQB prompt tokens) copies the keys and
-// values of the positions its tokens see, tile by tile of cap rows (cap =
-// kStageTile, or all positions when fewer; rows padded by 16 bytes so that
-// the lanes' 16-byte key reads spread over the banks); warp w takes the
-// (token, query head) pair w of the block (G <= 4 query heads per kv head)
-// and carries its online-softmax state (m, l, o) from tile to tile.
-// Positions go by in chunks of 32 whatever the tiling, so the result does not
-// depend on cap. Scores use four partial sums per lane and P.V two per
-// output, to shorten the dependent chains.
-constexpr int kQB = 4;
-constexpr int kStageTile = 256;
-constexpr int kStagedWarps = 16;
-static_assert(kStageTile % 32 == 0, "tiles hold whole chunks of 32 positions");
+// bf16 pair (lo element first) of the high terms of (x, y); their low terms in *lo.
+__device__ __forceinline__ uint32_t split2(float x, float y, uint32_t *lo) {
+    const uint16_t hx = f2bf_rne(x), hy = f2bf_rne(y);
+    *lo = (uint32_t)f2bf_rne(x - bf2f(hx)) | ((uint32_t)f2bf_rne(y - bf2f(hy)) << 16);
+    return (uint32_t)hx | ((uint32_t)hy << 16);
+}
 
 template <int HD>
-__global__ void __launch_bounds__(kStagedWarps * 32) attend_prefill_staged(const float *QKV, int n, int Hq, int Hkv,
-                                                                            int pos0, int max_seq, int cap,
-                                                                            const uint16_t *kc, const uint16_t *vc,
-                                                                            uint16_t *out_hi, uint16_t *out_lo) {
-    constexpr int RS = HD + 8;  // row stride in bf16 elements (16 bytes of padding)
-    constexpr int CPR = HD / 8; // 16-byte chunks per row
-    constexpr int DP = HD / 32;
-    extern __shared__ uint16_t kvs[];
+__global__ void __launch_bounds__(kFaWarps * 32) attend_prefill_mma(const float *__restrict__ QKV, int n, int Hq,
+                                                                    int Hkv, int pos0, int max_seq,
+                                                                    const uint16_t *__restrict__ kc,
+                                                                    const uint16_t *__restrict__ vc,
+                                                                    uint16_t *__restrict__ out_hi,
+                                                                    uint16_t *__restrict__ out_lo) {
+    constexpr int RS = HD + 8;       // padded row of a staged tile, in bf16
+    constexpr int KSTEPS = HD / 16;  // k-steps of S = Q K^T
+    constexpr int NT = HD / 8;       // n-tiles of O
+    __shared__ __align__(16) uint16_t Ks[kFaKeys * RS], Vs[kFaKeys * RS];
     pdl_wait();
     pdl_trigger();
-    uint16_t *Ks = kvs, *Vs = kvs + (size_t)cap * RS;
-    const int kvh = blockIdx.x, t0 = blockIdx.y * kQB, G = Hq / Hkv;
-    const int tl = min(n, t0 + kQB);  // tokens t0 .. tl-1
-    const int Tmax = pos0 + tl;       // positions the block's tokens see
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const bool active = warp < (tl - t0) * G;
-    const int t = t0 + warp / G, h = kvh * G + warp % G;
-    const int T = pos0 + t + 1;  // positions this pair sees
+    const int kvh = blockIdx.x, G = Hq / Hkv, QB = kFaRows / G;
+    const int t0 = blockIdx.y * QB;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, c = lane & 3;
     const int stride = (Hq + 2 * Hkv) * HD;
-    float qr[HD];
-    if (active) {
-        const float scale = rsqrtf((float)HD);
-        const float *q = QKV + (size_t)t * stride + (size_t)h * HD;
+    // this lane's two rows (g and g + 8 of the warp's 16)
+    int T[2], tok[2], head[2];
 #pragma unroll
-        for (int i = 0; i < HD; ++i) qr[i] = q[i] * scale;
+    for (int hr = 0; hr < 2; ++hr) {
+        const int r = warp * 16 + g + 8 * hr;
+        tok[hr] = t0 + r / G;
+        head[hr] = kvh * G + r % G;
+        const bool live = r < QB * G && tok[hr] < n;
+        T[hr] = live ? pos0 + tok[hr] + 1 : 0;
     }
-    float o[2][DP], m = -INFINITY, l = 0.f;
+    // the scaled queries as A fragments, hi and lo terms
+    uint32_t qh[KSTEPS][4], ql[KSTEPS][4];
+    {
+        const float scale = rsqrtf((float)HD);
 #pragma unroll
-    for (int e = 0; e < DP; ++e) o[0][e] = o[1][e] = 0.f;
+        for (int hr = 0; hr < 2; ++hr) {
+            const float *q = T[hr] ? QKV + (size_t)tok[hr] * stride + (size_t)head[hr] * HD : nullptr;
+#pragma unroll
+            for (int ks = 0; ks < KSTEPS; ++ks)
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    const int col = ks * 16 + 2 * c + 8 * half;
+                    const float x = q ? q[col] * scale : 0.f, y = q ? q[col + 1] * scale : 0.f;
+                    qh[ks][hr + 2 * half] = split2(x, y, &ql[ks][hr + 2 * half]);
+                }
+        }
+    }
+    float o[NT][4];
+#pragma unroll
+    for (int j = 0; j < NT; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+    float m[2] = {-1e30f, -1e30f}, l[2] = {0.f, 0.f};
+    const int Tblk = pos0 + min(n, t0 + QB);  // positions the block's rows see
+    const int Twarp = max(T[0], T[1]);        // (per lane; the warp's max below)
+    int Tw = Twarp;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) Tw = max(Tw, __shfl_xor_sync(0xFFFFFFFFu, Tw, off));
     const uint4 *Kg = reinterpret_cast<const uint4 *>(kc + (size_t)kvh * max_seq * HD);
     const uint4 *Vg = reinterpret_cast<const uint4 *>(vc + (size_t)kvh * max_seq * HD);
-    for (int k0 = 0; k0 < Tmax; k0 += cap) {
-        const int kn = min(cap, Tmax - k0);
-        __syncthreads();  // every warp is done with the previous tile
-        for (int i = tid; i < kn * CPR; i += blockDim.x) {
-            const int r = i / CPR, c = i % CPR;
-            *reinterpret_cast<uint4 *>(Ks + (size_t)r * RS + c * 8) = Kg[(size_t)(k0 + r) * CPR + c];
-            *reinterpret_cast<uint4 *>(Vs + (size_t)r * RS + c * 8) = Vg[(size_t)(k0 + r) * CPR + c];
+    constexpr int CPR = HD / 8;
+    for (int k0 = 0; k0 < Tblk; k0 += kFaKeys) {
+        const int kn = min(kFaKeys, Tblk - k0);
+        __syncthreads();
+        for (int i = tid; i < kFaKeys * CPR; i += blockDim.x) {
+            const int r = i / CPR, cc = i % CPR;
+            const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+            *reinterpret_cast<uint4 *>(Ks + r * RS + cc * 8) = r < kn ? Kg[(size_t)(k0 + r) * CPR + cc] : z;
+            *reinterpret_cast<uint4 *>(Vs + r * RS + cc * 8) = r < kn ? Vg[(size_t)(k0 + r) * CPR + cc] : z;
         }
         __syncthreads();
-        if (!active) continue;
-        const int te = min(T, k0 + kn);  // this pair's positions in the tile: k0 .. te-1
-        for (int j0 = k0; j0 < te; j0 += 32) {
-            const int j = j0 + lane;
-            float s = -INFINITY;
-            if (j < te) {
-                const uint4 *kr = reinterpret_cast<const uint4 *>(Ks + (size_t)(j - k0) * RS);
-                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        if (k0 >= Tw) continue;  // past every row of this warp
+        // S = Q K^T for the 64 positions (8 n-tiles of 8)
+        float sc[8][4];
 #pragma unroll
-                for (int c = 0; c < CPR; ++c) {
-                    const uint4 w = kr[c];
-                    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+        for (int j = 0; j < 8; ++j) {
+            sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.f;
+            const uint16_t *kr = Ks + (j * 8 + g) * RS + 2 * c;
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        acc[e] = fmaf(__uint_as_float(u[e] << 16), qr[c * 8 + 2 * e], acc[e]);
-                        acc[e] = fmaf(__uint_as_float(u[e] & 0xFFFF0000u), qr[c * 8 + 2 * e + 1], acc[e]);
-                    }
-                }
-                s = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+            for (int ks = 0; ks < KSTEPS; ++ks) {
+                const uint32_t b0 = *reinterpret_cast<const uint32_t *>(kr + ks * 16);
+                const uint32_t b1 = *reinterpret_cast<const uint32_t *>(kr + ks * 16 + 8);
+                mma_bf16(sc[j], qh[ks], b0, b1);
+                mma_bf16(sc[j], ql[ks], b0, b1);
             }
-            float cm = s;
-            for (int off = 16; off > 0; off >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xFFFFFFFFu, cm, off));
-            const float mn = fmaxf(m, cm);
-            const float corr = __expf(m - mn);
-            const float p = j < te ? __expf(s - mn) : 0.f;
-            float ps = p;
-            for (int off = 16; off > 0; off >>= 1) ps += __shfl_xor_sync(0xFFFFFFFFu, ps, off);
-            l = l * corr + ps;
-            m = mn;
+        }
+        // mask, running max and sum, P
+        float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-            for (int e = 0; e < DP; ++e) {
-                o[0][e] *= corr;
-                o[1][e] *= corr;
+        for (int j = 0; j < 8; ++j)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int hr = e >> 1, key = k0 + j * 8 + 2 * c + (e & 1);
+                if (key >= T[hr]) sc[j][e] = -INFINITY;
+                mx[hr] = fmaxf(mx[hr], sc[j][e]);
             }
-            const int cnt = te - j0 < 32 ? te - j0 : 32;
-            const uint16_t *vb = Vs + (size_t)(j0 - k0) * RS + lane * DP;
-#pragma unroll 8
-            for (int jj = 0; jj < cnt; ++jj) {
-                const float pj = __shfl_sync(0xFFFFFFFFu, p, jj);
-                // the lane's DP values of row jj in one 4- or 8-byte load
-                uint32_t u[DP / 2];
-                if constexpr (DP == 2) {
-                    u[0] = *reinterpret_cast<const uint32_t *>(vb + (size_t)jj * RS);
-                } else {
-                    const uint2 w = *reinterpret_cast<const uint2 *>(vb + (size_t)jj * RS);
-                    u[0] = w.x;
-                    u[1] = w.y;
-                }
+        float corr[2];
 #pragma unroll
-                for (int e = 0; e < DP; e += 2) {
-                    o[jj & 1][e] = fmaf(pj, __uint_as_float(u[e / 2] << 16), o[jj & 1][e]);
-                    o[jj & 1][e + 1] = fmaf(pj, __uint_as_float(u[e / 2] & 0xFFFF0000u), o[jj & 1][e + 1]);
-                }
+        for (int hr = 0; hr < 2; ++hr) {
+            mx[hr] = fmaxf(mx[hr], __shfl_xor_sync(0xFFFFFFFFu, mx[hr], 1));
+            mx[hr] = fmaxf(mx[hr], __shfl_xor_sync(0xFFFFFFFFu, mx[hr], 2));
+            const float mn = fmaxf(m[hr], mx[hr]);
+            corr[hr] = __expf(m[hr] - mn);
+            m[hr] = mn;
+        }
+        float ps[2] = {0.f, 0.f};
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int hr = e >> 1;
+                sc[j][e] = __expf(sc[j][e] - m[hr]);  // masked: exp(-inf) = 0
+                ps[hr] += sc[j][e];
+            }
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr) {
+            ps[hr] += __shfl_xor_sync(0xFFFFFFFFu, ps[hr], 1);
+            ps[hr] += __shfl_xor_sync(0xFFFFFFFFu, ps[hr], 2);
+            l[hr] = l[hr] * corr[hr] + ps[hr];
+        }
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+            o[j][0] *= corr[0];
+            o[j][1] *= corr[0];
+            o[j][2] *= corr[1];
+            o[j][3] *= corr[1];
+        }
+        // O += P V: k-step s covers positions 16s .. 16s+15 (n-tiles 2s, 2s+1 of S)
+#pragma unroll
+        for (int s2 = 0; s2 < 4; ++s2) {
+            uint32_t ph[4], pl[4];
+            ph[0] = split2(sc[2 * s2][0], sc[2 * s2][1], &pl[0]);
+            ph[1] = split2(sc[2 * s2][2], sc[2 * s2][3], &pl[1]);
+            ph[2] = split2(sc[2 * s2 + 1][0], sc[2 * s2 + 1][1], &pl[2]);
+            ph[3] = split2(sc[2 * s2 + 1][2], sc[2 * s2 + 1][3], &pl[3]);
+            // lane l addresses row (l % 8) + 8 ((l / 8) & 1) of the tile, columns 8 (l / 16) on
+            const uint16_t *vrow = Vs + (s2 * 16 + (lane & 7) + 8 * ((lane >> 3) & 1)) * RS + 8 * (lane >> 4);
+#pragma unroll
+            for (int j = 0; j < NT; j += 2) {
+                uint32_t b[4];
+                asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                             : "=r"(b[0]), "=r"(b[1]), "=r"(b[2]), "=r"(b[3])
+                             : "r"(saddr(vrow + j * 8)));
+                mma_bf16(o[j], ph, b[0], b[1]);
+                mma_bf16(o[j], pl, b[0], b[1]);
+                mma_bf16(o[j + 1], ph, b[2], b[3]);
+                mma_bf16(o[j + 1], pl, b[2], b[3]);
             }
         }
     }
-    if (!active) return;
-    const size_t at = (size_t)t * Hq * HD + (size_t)h * HD + lane * DP;
+    // O / l as hi / lo bf16 terms
 #pragma unroll
-    for (int e = 0; e < DP; ++e) {
-        const float v = (o[0][e] + o[1][e]) / l;
-        const uint16_t hb = f2bf_rne(v);
-        out_hi[at + e] = hb;
-        out_lo[at + e] = f2bf_rne(v - bf2f(hb));
+    for (int hr = 0; hr < 2; ++hr) {
+        if (!T[hr]) continue;
+        const float inv = 1.0f / l[hr];
+        const size_t at = ((size_t)tok[hr] * Hq + head[hr]) * HD + 2 * c;
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+            uint32_t lo;
+            const uint32_t hi = split2(o[j][2 * hr] * inv, o[j][2 * hr + 1] * inv, &lo);
+            *reinterpret_cast<uint32_t *>(out_hi + at + j * 8) = hi;
+            *reinterpret_cast<uint32_t *>(out_lo + at + j * 8) = lo;
+        }
     }
 }
 
@@ -1166,33 +1167,15 @@ cudaError_t run(const Model &m, const Scratch &sc, const int32_t *d_tokens, int 
             ok(launch_pdl(rope_append, dim3(n, per_tok), dim3(256), 0, s, sc.QKV, Sq > 1 ? sc.work : nullptr,
                           Sq > 1 ? Sq : 0, n, Hq, Hkv, hd, pos0, m.rope, m.max_seq, m.kc + kv_off, m.vc + kv_off));
         }
-        const int warps = n * Hq, wpb = 4;
-        if ((Hq / Hkv) * kQB <= kStagedWarps) {
-            // one warp per (token, query head) of a block: keys and values
-            // staged tile by tile in shared memory
-            const int cap = std::min(pos0 + n, kStageTile);
-            const dim3 grid(Hkv, (n + kQB - 1) / kQB);
-            const size_t smem = 2 * (size_t)cap * (hd + 8) * 2;
-            static bool configured = false;
-            if (!configured) {
-                ok(cudaFuncSetAttribute(attend_prefill_staged<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        2 * kStageTile * (64 + 8) * 2));
-                ok(cudaFuncSetAttribute(attend_prefill_staged<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        2 * kStageTile * (128 + 8) * 2));
-                configured = e == cudaSuccess;
-            }
+        {  // causal attention on the tensor cores (every supported group size: G <= kFaRows)
+            const int QB = kFaRows / (Hq / Hkv);
+            const dim3 grid(Hkv, (n + QB - 1) / QB);
             if (hd == 64)
-                ok(launch_pdl(attend_prefill_staged<64>, grid, dim3(kStagedWarps * 32), smem, s, sc.QKV, n, Hq, Hkv,
-                              pos0, m.max_seq, cap, m.kc + kv_off, m.vc + kv_off, sc.Ahi, sc.Alo));
+                ok(launch_pdl(attend_prefill_mma<64>, grid, dim3(kFaWarps * 32), 0, s, sc.QKV, n, Hq, Hkv, pos0,
+                              m.max_seq, m.kc + kv_off, m.vc + kv_off, sc.Ahi, sc.Alo));
             else
-                ok(launch_pdl(attend_prefill_staged<128>, grid, dim3(kStagedWarps * 32), smem, s, sc.QKV, n, Hq, Hkv,
-                              pos0, m.max_seq, cap, m.kc + kv_off, m.vc + kv_off, sc.Ahi, sc.Alo));
-        } else if (hd == 64) {
-            ok(launch_pdl(attend_prefill<64>, dim3((warps + wpb - 1) / wpb), dim3(wpb * 32), 0, s, sc.QKV, n, Hq, Hkv,
-                          pos0, m.max_seq, m.kc + kv_off, m.vc + kv_off, sc.Ahi, sc.Alo));
-        } else {
-            ok(launch_pdl(attend_prefill<128>, dim3((warps + wpb - 1) / wpb), dim3(wpb * 32), 0, s, sc.QKV, n, Hq,
-                          Hkv, pos0, m.max_seq, m.kc + kv_off, m.vc + kv_off, sc.Ahi, sc.Alo));
+                ok(launch_pdl(attend_prefill_mma<128>, grid, dim3(kFaWarps * 32), 0, s, sc.QKV, n, Hq, Hkv, pos0,
+                              m.max_seq, m.kc + kv_off, m.vc + kv_off, sc.Ahi, sc.Alo));
         }
         // O-projection + residual, then the MLP's RMSNorm
         ok(gemm(lm.wo, sc.Ahi, sc.Alo, d, n, qd, sc.X, d, sc.X, sc.work, sc.work_floats, sc.err, m.n_sm, s,
