@@ -103,6 +103,22 @@ def test_prefill_head_dim_128_over_several_key_tiles(cuda_dev):
     pair.close()
 
 
+@pytest.mark.parametrize("n", [1, 33])
+def test_tiny_prefill_of_one_token_and_of_one_past_the_short_prompt_path(cuda_dev, n):
+    # 1 token: one token tile, one key; 33: the first length past the
+    # short-prompt shapes (at most 32 tokens, every reduction split)
+    pair, _, _ = prefill_case(TINY, n, 40, 2)
+    pair.close()
+
+
+def test_prefill_head_dim_128_short_prompt(cuda_dev):
+    # head dim 128 through the short-prompt shapes (reductions split, q/k/v
+    # partial sums added in the RoPE pass)
+    shape = ModelShape("hd128-g3", 2, 768, 6, 2, 128, 1536, 2048, 1e-5, 5e5)
+    pair, _, _ = prefill_case(shape, 20, 24, 2)
+    pair.close()
+
+
 def test_llama1b_prefill_of_the_workload_prompt(cuda_dev):
     wl = WORKLOADS["llama1b"]
     pair, _, _ = prefill_case(LLAMA_1B, wl.prompt_len, wl.max_seq, 4)
