@@ -917,13 +917,33 @@ int mk_decode_step_host(mk_handle *h, const int32_t *host_token, int32_t positio
     cudaStream_t s = (cudaStream_t)stream;
     cudaError_t e = cudaSetDevice(h->device);
     if (e != cudaSuccess) return cuda_fail(e, "cudaSetDevice");
-    e = cudaMemcpyAsync(h->d_tok_in, host_token, sizeof(int32_t), cudaMemcpyHostToDevice, s);
-    if (e != cudaSuccess) return cuda_fail(e, "token upload");
-    int rc = launch(h, 0, h->d_tok_in, position, host_logits ? h->d_logits : nullptr, h->d_tok_out, s,
-                    false);
+    // Pinned host buffers that the device can address (cudaHostAlloc'd or
+    // registered memory) are used in place: the step reads the token from and
+    // writes the next token to host memory over the chip link, with no copy
+    // operations on the stream. Other host memory goes through copies.
+    const int32_t *tok_in = nullptr;
+    int32_t *tok_out = nullptr;
+    {
+        cudaPointerAttributes ai{}, ao{};
+        if (cudaPointerGetAttributes(&ai, host_token) == cudaSuccess && ai.type == cudaMemoryTypeHost &&
+            ai.devicePointer && cudaPointerGetAttributes(&ao, host_out_token) == cudaSuccess &&
+            ao.type == cudaMemoryTypeHost && ao.devicePointer) {
+            tok_in = static_cast<const int32_t *>(ai.devicePointer);
+            tok_out = static_cast<int32_t *>(ao.devicePointer);
+        }
+        (void)cudaGetLastError();  // an unregistered pointer is not an error of this call
+    }
+    if (!tok_in) {
+        e = cudaMemcpyAsync(h->d_tok_in, host_token, sizeof(int32_t), cudaMemcpyHostToDevice, s);
+        if (e != cudaSuccess) return cuda_fail(e, "token upload");
+    }
+    int rc = launch(h, 0, tok_in ? tok_in : h->d_tok_in, position, host_logits ? h->d_logits : nullptr,
+                    tok_out ? tok_out : h->d_tok_out, s, false);
     if (rc) return rc;
-    e = cudaMemcpyAsync(host_out_token, h->d_tok_out, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
-    if (e != cudaSuccess) return cuda_fail(e, "token download");
+    if (!tok_out) {
+        e = cudaMemcpyAsync(host_out_token, h->d_tok_out, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
+        if (e != cudaSuccess) return cuda_fail(e, "token download");
+    }
     if (host_logits) {
         e = cudaMemcpyAsync(host_logits, h->d_logits, sizeof(float) * h->cfg.vocab,
                             cudaMemcpyDeviceToHost, s);

@@ -2231,6 +2231,12 @@ __global__ void __launch_bounds__(kThreads, 1) mk_megakernel(const Params prm) {
                 sp->posb[b] = CHK(p.d_pos + b, 4, 33) ? *(volatile const int32_t *)(p.d_pos + b) : -1;
             sp->pos = sp->posb[0];
         }
+        // a single sequence's token held in memory is read once as well (it
+        // may sit in host memory; the last CTA may overwrite it at the end)
+        if (p.d_token && p.nb <= 1) {
+            sp->token = CHK(p.d_token, 4, 33) ? *(volatile const int32_t *)p.d_token : -1;
+            sp->d_token = nullptr;
+        }
         uint32_t e = 1;
         if (CHK(p.epoch, 4, 32)) e = *(volatile uint32_t *)p.epoch & 0xFFFFFFu;
         cx.misc->ep8 = (e ? e : 1u) << 8;

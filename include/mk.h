@@ -129,9 +129,12 @@ int mk_decode_step_dev(mk_handle *h, const int32_t *d_token_id, int32_t position
                        float *out_logits, int32_t *out_token, void *stream);
 
 /* Same step through HOST buffers, for callers without device memory of their
- * own: copies *host_token to the device, runs the step, copies the greedy
- * token (and the logits if host_logits is not NULL) back, and waits for the
- * stream. host buffers should be pinned for asynchronous copies.
+ * own: the step reads *host_token and writes the greedy token to
+ * *host_out_token (and the logits to host_logits if not NULL), then waits
+ * for the stream. Pinned buffers the device can address (cudaHostAlloc'd or
+ * registered) are read and written in place by the kernel over the chip
+ * link; other host memory goes through copies on the stream (the logits
+ * always do).
  * Source: as mk_decode_step; the host-buffer form is this library's
  * addition (the pages describe the device step only). */
 int mk_decode_step_host(mk_handle *h, const int32_t *host_token, int32_t position,
