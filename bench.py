@@ -727,11 +727,20 @@ def run_mk(args, ws, rank, local):
     for s in range(W):
         mk.step_dev(tok, P0 + s, tok, None, stream)
     sampled_us = 1e3 * timed_decode() / K
+    # ... and with the top-k / top-p filter on the draw
+    mk.set_sampling_filter(50, 0.9)
+    for s in range(W):
+        mk.step_dev(tok, P0 + s, tok, None, stream)
+    filtered_us = 1e3 * timed_decode() / K
+    mk.set_sampling_filter(0, 1.0)
     mk.set_sampling(0.0)
     if mk.status() != 0:
         raise SystemExit("megakernel status error with sampling")
     sampling_line = {"us_per_token": sampled_us, "temperature": 0.8,
-                     "note": "Gumbel-max draw from softmax(logits/T), Philox4x32-10 noise per vocabulary entry"}
+                     "filtered_us_per_token": filtered_us, "top_k": 50, "top_p": 0.9,
+                     "note": "Gumbel-max draw from softmax(logits/T), Philox4x32-10 noise per vocabulary entry; "
+                             "filtered: the draw among the top_k best logits, cut to the shortest prefix whose "
+                             "softmax mass reaches top_p"}
 
     # ---- comparators: the same kernels as an unfused chain (and as a graph)
     comp = None

@@ -1160,21 +1160,28 @@ __device__ void lm_filtered(const Params &p, const Ctx &cx, const Instr &in, con
     }
     consumer_sync();
     if (!cx.misc->flag) return;
-    // tau = the largest k-th key of any block
-    unsigned long long tau = 0ull;
-    for (int s = tid; s < p.n_lm; s += kConsumerThreads) {
-        const unsigned long long *q = p.lm_cand + (size_t)s * kMaxTopK + (K - 1);
-        const unsigned long long v = CHK(q, 8, 64) ? __ldcg(q) : 0ull;
-        tau = v > tau ? v : tau;
-    }
-    tau = warp_max_u64(tau);
-    if (lane == 0) cx.misc->best8[warp] = tau;
-    consumer_sync();
-    tau = 0ull;
-#pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) tau = cx.misc->best8[w] > tau ? cx.misc->best8[w] : tau;
-    // gather every key >= tau into the (now idle) page ring and sort them
+    // tau = the k-th largest of the blocks' J best keys, J = ceil(k / blocks):
+    // those keys are some of the candidates, so their k-th largest is at most
+    // the k-th largest of all of them, and every key of the global top k is
+    // >= tau. (The largest k-th key of any block is also such a bound, but
+    // with many similar blocks it keeps most candidates.)
     unsigned long long *g = reinterpret_cast<unsigned long long *>(cx.pages);
+    unsigned long long tau = 0ull;
+    {
+        const int J = (K + p.n_lm - 1) / p.n_lm, ns = p.n_lm * J;
+        int npb = 2;
+        while (npb < ns) npb <<= 1;
+        for (int e = tid; e < npb; e += kConsumerThreads) {
+            const unsigned long long *q = p.lm_cand + (size_t)(e / J) * kMaxTopK + e % J;
+            const unsigned long long v = e < ns && CHK(q, 8, 64) ? __ldcg(q) : 0ull;
+            if (CHKS(g + e, 8, 65)) g[e] = v;
+        }
+        consumer_sync();
+        bitonic_desc(g, npb);
+        tau = K - 1 < ns ? g[K - 1] : 0ull;
+        consumer_sync();  // g is reused below
+    }
+    // gather every key >= tau into the (now idle) page ring and sort them
     const int total = p.n_lm * K;
     for (int e = tid; e < total; e += kConsumerThreads) {
         const unsigned long long *q = p.lm_cand + (size_t)(e / K) * kMaxTopK + e % K;
