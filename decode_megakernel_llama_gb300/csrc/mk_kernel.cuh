@@ -1099,34 +1099,101 @@ __device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v)
     return v;
 }
 
-// Sorts keys[0, np) of shared memory into descending order (np a power of
-// two) with a bitonic network run by all consumer threads; ends with a
-// consumer barrier.
-__device__ void bitonic_desc(unsigned long long *keys, int np) {
-    const int tid = threadIdx.x;
-    for (int k = 2; k <= np; k <<= 1)
-        for (int j = k >> 1; j > 0; j >>= 1) {
-            for (int i = tid; i < np; i += kConsumerThreads) {
-                const int l = i ^ j;
-                if (l > i) {
-                    const unsigned long long a = keys[i], b = keys[l];
-                    if ((i & k) == 0 ? a < b : a > b) {
-                        keys[i] = b;
-                        keys[l] = a;
-                    }
-                }
-            }
-            consumer_sync();
-        }
+// 64 keys held by a warp, element e = lane + 32 r in v[r]: one compare-exchange
+// stage of a bitonic network over distance j within blocks of size k
+// (descending overall: blocks with (e & k) == 0 descend).
+__device__ __forceinline__ void bitonic_stage64(unsigned long long (&v)[2], int k, int j) {
+    const int lane = threadIdx.x & 31;
+    if (j == 32) {  // the partner is the lane's other element
+        const bool desc = (lane & k) == 0;  // e = lane and lane + 32 share the block bit for k >= 64
+        const unsigned long long hi = v[0] > v[1] ? v[0] : v[1], lo = v[0] > v[1] ? v[1] : v[0];
+        v[0] = desc ? hi : lo;
+        v[1] = desc ? lo : hi;
+        return;
+    }
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+        const int e = lane + 32 * r;
+        const unsigned long long pv = __shfl_xor_sync(0xFFFFFFFFu, v[r], j);
+        const bool desc = (e & k) == 0, lower = (e & j) == 0;
+        const unsigned long long mx = v[r] > pv ? v[r] : pv, mn = v[r] > pv ? pv : v[r];
+        v[r] = lower == desc ? mx : mn;
+    }
 }
 
-// LM-head epilogue of a filtered draw. Every LM-head instruction sorts the
-// keys (logit, then lowest index) of its rows and publishes its top_k best;
-// the last instruction to arrive gathers the keys no smaller than the
-// largest k-th key of any block (only those can be among the global top_k),
-// sorts them, and with warp 0 cuts the nucleus (the shortest prefix of the
-// top_k whose softmax mass at the temperature reaches top_p) and takes the
-// Gumbel-max among the kept candidates.
+// Sorts the warp's 64 keys descending.
+__device__ __forceinline__ void warp_sort64(unsigned long long (&v)[2]) {
+#pragma unroll
+    for (int k = 2; k <= 64; k <<= 1)
+#pragma unroll
+        for (int j = k >> 1; j > 0; j >>= 1) bitonic_stage64(v, k, j);
+}
+
+// Two descending runs of 64 (a, then b) -> the 64 largest keys of both,
+// descending, in a: the elementwise max of a and reversed b is bitonic and
+// holds them, and a bitonic merge sorts it.
+__device__ __forceinline__ void warp_merge_top64(unsigned long long (&a)[2], const unsigned long long (&b)[2]) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+        const unsigned long long rb = __shfl_sync(0xFFFFFFFFu, b[1 - r], 31 - lane);  // b[63 - e]
+        a[r] = a[r] > rb ? a[r] : rb;
+    }
+#pragma unroll
+    for (int j = 32; j > 0; j >>= 1) bitonic_stage64(a, 64, j);
+}
+
+// The 64 largest of keys[0 .. n), descending, into keys[0 .. 64) (0 pads
+// the rest; no real key is 0), by the consumer warps: each warp sorts runs of
+// 64 in registers and keeps the best 64 of its two runs, then rounds of
+// pairwise keep-the-best-64 merges leave the survivors in run 0. keys must
+// hold max(n, 64) entries. Ends with the consumers synchronised.
+__device__ void block_top64(unsigned long long *keys, int n) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nrun = n > 64 ? (n + 63) / 64 : 1;
+    unsigned long long v[2], w2[2];
+    auto load_run = [&](int run, unsigned long long (&x)[2]) {
+        const int base = run * 64;
+        x[0] = base + lane < n ? keys[base + lane] : 0ull;
+        x[1] = base + lane + 32 < n ? keys[base + lane + 32] : 0ull;
+    };
+    for (int pair = warp; 2 * pair < nrun; pair += kConsumerWarps) {
+        load_run(2 * pair, v);
+        warp_sort64(v);
+        if (2 * pair + 1 < nrun) {
+            load_run(2 * pair + 1, w2);
+            warp_sort64(w2);
+            warp_merge_top64(v, w2);
+        }
+        __syncwarp();
+        keys[2 * pair * 64 + lane] = v[0];
+        keys[2 * pair * 64 + lane + 32] = v[1];
+    }
+    consumer_sync();
+    for (int step = 2; step < nrun; step <<= 1) {  // runs 0, 2 step, 4 step, ... hold the survivors
+        for (int pair = warp; 2 * pair * step < nrun; pair += kConsumerWarps) {
+            const int r0 = 2 * pair * step, r1 = r0 + step;
+            if (r1 < nrun) {
+                load_run(r0, v);
+                load_run(r1, w2);
+                warp_merge_top64(v, w2);
+                __syncwarp();
+                keys[r0 * 64 + lane] = v[0];
+                keys[r0 * 64 + lane + 32] = v[1];
+            }
+        }
+        consumer_sync();
+    }
+}
+
+// LM-head epilogue of a filtered draw. Every LM-head instruction selects the
+// top_k best keys (logit, then lowest index) of its rows, in order, and
+// publishes them; the last instruction to arrive bounds the global top_k from
+// below by the top_k-th largest of the blocks' best keys, gathers the
+// published keys at or above that bound, selects their top_k, and with warp 0
+// cuts the nucleus (the shortest prefix of the top_k whose softmax mass at
+// the temperature reaches top_p) and takes the Gumbel-max among the kept
+// candidates.
 __device__ void lm_filtered(const Params &p, const Ctx &cx, const Instr &in, const float *red, int sw) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int n = in.a1, r0 = in.a0, K = p.top_k;
@@ -1145,7 +1212,7 @@ __device__ void lm_filtered(const Params &p, const Ctx &cx, const Instr &in, con
         if (CHKS(keys + i, 8, 62)) keys[i] = k;
     }
     consumer_sync();
-    bitonic_desc(keys, np);
+    block_top64(keys, np);
     unsigned long long *mine = p.lm_cand + (size_t)in.slot * kMaxTopK;
     for (int j = tid; j < K; j += kConsumerThreads)
         if (CHK(mine + j, 8, 63)) mine[j] = keys[j];
@@ -1169,36 +1236,31 @@ __device__ void lm_filtered(const Params &p, const Ctx &cx, const Instr &in, con
     unsigned long long tau = 0ull;
     {
         const int J = (K + p.n_lm - 1) / p.n_lm, ns = p.n_lm * J;
-        int npb = 2;
-        while (npb < ns) npb <<= 1;
-        for (int e = tid; e < npb; e += kConsumerThreads) {
+        for (int e = tid; e < ns; e += kConsumerThreads) {
             const unsigned long long *q = p.lm_cand + (size_t)(e / J) * kMaxTopK + e % J;
-            const unsigned long long v = e < ns && CHK(q, 8, 64) ? __ldcg(q) : 0ull;
+            const unsigned long long v = CHK(q, 8, 64) ? __ldcg(q) : 0ull;
             if (CHKS(g + e, 8, 65)) g[e] = v;
         }
         consumer_sync();
-        bitonic_desc(g, npb);
+        block_top64(g, ns);
         tau = K - 1 < ns ? g[K - 1] : 0ull;
         consumer_sync();  // g is reused below
     }
-    // gather every key >= tau into the (now idle) page ring and sort them
-    const int total = p.n_lm * K;
-    for (int e = tid; e < total; e += kConsumerThreads) {
-        const unsigned long long *q = p.lm_cand + (size_t)(e / K) * kMaxTopK + e % K;
-        const unsigned long long v = CHK(q, 8, 64) ? __ldcg(q) : 0ull;
-        if (v != 0ull && v >= tau) {
+    // gather every published key >= tau into the (now idle) page ring: a
+    // block's list is in descending order, so its keys >= tau are a prefix
+    // (a thread per block reads until the first key below tau)
+    for (int s = tid; s < p.n_lm; s += kConsumerThreads) {
+        const unsigned long long *q = p.lm_cand + (size_t)s * kMaxTopK;
+        for (int j = 0; j < K; ++j) {
+            const unsigned long long v = CHK(q + j, 8, 64) ? __ldcg(q + j) : 0ull;
+            if (v == 0ull || v < tau) break;
             const int at = atomicAdd(&cx.misc->gcount, 1);
             if (CHKS(g + at, 8, 65)) g[at] = v;
         }
     }
     consumer_sync();
     const int ng = cx.misc->gcount;
-    int np2 = 2;
-    while (np2 < ng || np2 < K) np2 <<= 1;
-    for (int i = ng + tid; i < np2; i += kConsumerThreads)
-        if (CHKS(g + i, 8, 65)) g[i] = 0ull;
-    consumer_sync();
-    bitonic_desc(g, np2);
+    block_top64(g, ng);  // the top k of the candidates, descending, in g[0 .. k)
     if (warp != 0) return;
     // warp 0: candidate j = lane and j = lane + 32 (K <= 64), in key order
     const int nc = ng < K ? ng : K;
