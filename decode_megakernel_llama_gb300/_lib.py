@@ -278,7 +278,8 @@ class Megakernel:
         """d_tokens, d_positions, out_tokens: int32 CUDA tensors [B]; logits: float32 CUDA
         tensor [B][vocab] or None. Sequence b uses batch slot b of the KV cache. With
         B == max_batch (head dim 64) all sequences run in one fused launch that reads
-        every weight tile once (fp16 GEMV inputs); otherwise one launch per sequence."""
+        every weight tile once (fp16 GEMV inputs; with a top-k / top-p filter, two
+        short draw kernels follow it); otherwise one launch per sequence."""
         check(load().mk_decode_step_batch(self.h, d_tokens.data_ptr(), d_positions.data_ptr(),
                                           int(d_tokens.numel()),
                                           logits.data_ptr() if logits is not None else None,

@@ -28,6 +28,10 @@ extern "C" cudaError_t mk_kernel_launch(const mk::Params *p, int n_sm, int coope
 extern "C" cudaError_t mk_kernel_occupancy(int *blocks_per_sm);
 extern "C" cudaError_t mk_convert_bf16_f16(const void *src, void *dst, size_t n, unsigned long long *out_of_range,
                                            cudaStream_t stream);
+extern "C" size_t mk_filter_lists_keys(int B, int V);
+extern "C" cudaError_t mk_filtered_draw_batch(const float *logits, int B, int V, int K, float top_p, float inv_temp,
+                                              const int32_t *positions, uint64_t seed, unsigned long long *lists,
+                                              int32_t *out_tokens, cudaStream_t stream);
 extern "C" cudaError_t mk_noise_launch(int n, int pos, int slot, uint64_t seed, const uint32_t *words,
                                        uint32_t *out_words, float *out_noise, cudaStream_t stream);
 
@@ -682,6 +686,10 @@ struct mk_handle {
     mkpf::Model pf_model;
     mkpf::Scratch pf;
     void *pf_mem = nullptr;
+    // filtered draws of a fused batched step: its logits (when the caller
+    // asks for none) and the candidate lists, made on the first such step
+    float *bf_logits = nullptr;
+    unsigned long long *bf_lists = nullptr;
 };
 
 namespace {
@@ -880,20 +888,42 @@ int mk_decode_step_batch(mk_handle *h, const int32_t *d_tokens, const int32_t *d
         return fail(MK_ERR_INVALID_ARG, "d_tokens, d_positions and out_tokens must not be NULL");
     if (batch < 1 || batch > h->cfg.max_batch) return fail(MK_ERR_INVALID_ARG, "batch outside [1, max_batch]");
     const bool filtered = h->inv_temp > 0.f && (h->top_k > 0 || h->top_p < 1.f);
-    if (h->has_batch && batch == h->cfg.max_batch && !filtered) {
-        // all sequences in one launch: every weight tile read once for all of them
+    if (h->has_batch && batch == h->cfg.max_batch) {
+        // all sequences in one launch: every weight tile read once for all of
+        // them. A filtered draw takes the launch's logits (the launch itself
+        // then picks greedily) and draws every sequence's token after it.
         cudaError_t e = cudaSetDevice(h->device);
         if (e != cudaSuccess) return cuda_fail(e, "cudaSetDevice");
+        const int V = h->cfg.vocab;
+        float *logits = out_logits;
+        if (filtered && (!h->bf_lists || (!logits && !h->bf_logits))) {
+            if (!h->bf_lists) {
+                e = cudaMalloc(&h->bf_lists, sizeof(unsigned long long) * mk_filter_lists_keys(batch, V));
+                if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(filter lists)");
+            }
+            if (!logits && !h->bf_logits) {
+                e = cudaMalloc(&h->bf_logits, sizeof(float) * (size_t)batch * V);
+                if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(batch logits)");
+            }
+        }
+        if (filtered && !logits) logits = h->bf_logits;
         mk::Params p = h->bbase;
         p.timeout_ns = h->timeout_ns;
         p.trace = h->trace_on ? h->d_trace : nullptr;
         p.trace_cap = h->trace_cap;
-        p.inv_temp = h->inv_temp;
+        p.inv_temp = filtered ? 0.f : h->inv_temp;
         p.seed_lo = (uint32_t)(h->seed & 0xFFFFFFFFu);
         p.seed_hi = (uint32_t)(h->seed >> 32);
         if (h->trace_on) h->trace_batch = true;
-        return mkint::launch_step(p, h->bim.n_sm, h->bim.n_stages, 0, d_tokens, 0, out_logits, out_tokens,
-                                  (cudaStream_t)stream, false, d_positions, 0);
+        const int rc = mkint::launch_step(p, h->bim.n_sm, h->bim.n_stages, 0, d_tokens, 0, logits, out_tokens,
+                                          (cudaStream_t)stream, false, d_positions, 0);
+        if (rc || !filtered) return rc;
+        // a filter set with only top_p takes the nucleus among the kMaxTopK best
+        const int K = h->top_k > 0 ? h->top_k : mk::kMaxTopK;
+        e = mk_filtered_draw_batch(logits, batch, V, K, h->top_p, h->inv_temp, d_positions, h->seed, h->bf_lists,
+                                   out_tokens, (cudaStream_t)stream);
+        if (e != cudaSuccess) return cuda_fail(e, "filtered draw of the batch");
+        return MK_OK;
     }
     for (int32_t b = 0; b < batch; ++b) {
         const int rc = launch(h, 0, d_tokens + b, 0, out_logits ? out_logits + (size_t)b * h->cfg.vocab : nullptr,
@@ -1187,6 +1217,8 @@ void mk_destroy(mk_handle *h) {
     if (h->bdev_mem) cudaFree(h->bdev_mem);
     if (h->w16) cudaFree(h->w16);
     if (h->pf_mem) cudaFree(h->pf_mem);
+    if (h->bf_logits) cudaFree(h->bf_logits);
+    if (h->bf_lists) cudaFree(h->bf_lists);
     delete h;
 }
 

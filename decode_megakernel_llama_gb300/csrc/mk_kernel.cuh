@@ -1186,6 +1186,80 @@ __device__ void block_top64(unsigned long long *keys, int n) {
     }
 }
 
+// The filtered draw from nl candidate lists (list s at lists + s * kMaxTopK:
+// the top_k best keys of its part of the vocabulary in descending order, 0
+// where it has fewer), by the consumer threads of one CTA. tau = the top_k-th
+// largest of the lists' J = ceil(top_k / nl) best keys is a lower bound of
+// the global top_k (those keys are some of the candidates); every key >= tau
+// (a prefix of each list) is gathered into g, their top_k selected, and warp 0
+// cuts the nucleus (the shortest prefix of the top_k whose softmax mass at
+// the temperature reaches top_p) and takes the Gumbel-max among the kept
+// candidates with the noise of (entry, pos, slot, seed). g: shared memory for
+// max(nl * top_k, 64) keys; gcount: a shared int. Returns the token in warp 0
+// (-1 in the other warps).
+__device__ int draw_filtered(const unsigned long long *lists, int nl, int K, float top_p, float inv_temp, int pos,
+                             int slot, uint32_t seed_lo, uint32_t seed_hi, unsigned long long *g, int *gcount) {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    unsigned long long tau = 0ull;
+    {
+        const int J = (K + nl - 1) / nl, ns = nl * J;
+        if (tid == 0) *gcount = 0;
+        for (int e = tid; e < ns; e += kConsumerThreads) g[e] = __ldcg(lists + (size_t)(e / J) * kMaxTopK + e % J);
+        consumer_sync();
+        block_top64(g, ns);
+        tau = K - 1 < ns ? g[K - 1] : 0ull;
+        consumer_sync();  // g is reused below
+    }
+    // every list's prefix of keys >= tau (a thread per list)
+    for (int s = tid; s < nl; s += kConsumerThreads) {
+        const unsigned long long *q = lists + (size_t)s * kMaxTopK;
+        for (int j = 0; j < K; ++j) {
+            const unsigned long long v = __ldcg(q + j);
+            if (v == 0ull || v < tau) break;
+            g[atomicAdd(gcount, 1)] = v;
+        }
+    }
+    consumer_sync();
+    const int ng = *(volatile int *)gcount;
+    block_top64(g, ng);  // the top k of the candidates, descending, in g[0 .. k)
+    if (warp != 0) return -1;
+    // warp 0: candidate j = lane and j = lane + 32 (K <= 64), in key order
+    const int nc = ng < K ? ng : K;
+    const float zmax = key_value(g[0]);
+    const bool h0 = lane < nc, h1 = lane + 32 < nc;
+    const float z0 = h0 ? key_value(g[lane]) : 0.f, z1 = h1 ? key_value(g[lane + 32]) : 0.f;
+    const float e0 = h0 ? expf((z0 - zmax) * inv_temp) : 0.f, e1 = h1 ? expf((z1 - zmax) * inv_temp) : 0.f;
+    float c0 = e0, c1 = e1;  // inclusive prefix sums in candidate order
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float a = __shfl_up_sync(0xFFFFFFFFu, c0, o), b = __shfl_up_sync(0xFFFFFFFFu, c1, o);
+        if (lane >= o) {
+            c0 += a;
+            c1 += b;
+        }
+    }
+    c1 += __shfl_sync(0xFFFFFFFFu, c0, 31);
+    const float need = top_p * __shfl_sync(0xFFFFFFFFu, c1, 31);
+    int nkeep = nc;
+    if (top_p < 1.f) {
+        const uint32_t b0 = __ballot_sync(0xFFFFFFFFu, h0 && c0 >= need);
+        const uint32_t b1 = __ballot_sync(0xFFFFFFFFu, h1 && c1 >= need);
+        nkeep = b0 ? __ffs(b0) : (b1 ? 32 + __ffs(b1) : nc);
+    }
+    unsigned long long best = 0ull;
+    if (lane < nkeep) {
+        const uint32_t i = key_index(g[lane]);
+        best = argmax_key(z0 * inv_temp + gumbel_noise(i, pos, slot, seed_lo, seed_hi), i);
+    }
+    if (lane + 32 < nkeep) {
+        const uint32_t i = key_index(g[lane + 32]);
+        const unsigned long long k1 = argmax_key(z1 * inv_temp + gumbel_noise(i, pos, slot, seed_lo, seed_hi), i);
+        best = k1 > best ? k1 : best;
+    }
+    best = warp_max_u64(best);
+    return (int)key_index(best);
+}
+
 // LM-head epilogue of a filtered draw. Every LM-head instruction selects the
 // top_k best keys (logit, then lowest index) of its rows, in order, and
 // publishes them; the last instruction to arrive bounds the global top_k from
@@ -1227,77 +1301,9 @@ __device__ void lm_filtered(const Params &p, const Ctx &cx, const Instr &in, con
     }
     consumer_sync();
     if (!cx.misc->flag) return;
-    // tau = the k-th largest of the blocks' J best keys, J = ceil(k / blocks):
-    // those keys are some of the candidates, so their k-th largest is at most
-    // the k-th largest of all of them, and every key of the global top k is
-    // >= tau. (The largest k-th key of any block is also such a bound, but
-    // with many similar blocks it keeps most candidates.)
-    unsigned long long *g = reinterpret_cast<unsigned long long *>(cx.pages);
-    unsigned long long tau = 0ull;
-    {
-        const int J = (K + p.n_lm - 1) / p.n_lm, ns = p.n_lm * J;
-        for (int e = tid; e < ns; e += kConsumerThreads) {
-            const unsigned long long *q = p.lm_cand + (size_t)(e / J) * kMaxTopK + e % J;
-            const unsigned long long v = CHK(q, 8, 64) ? __ldcg(q) : 0ull;
-            if (CHKS(g + e, 8, 65)) g[e] = v;
-        }
-        consumer_sync();
-        block_top64(g, ns);
-        tau = K - 1 < ns ? g[K - 1] : 0ull;
-        consumer_sync();  // g is reused below
-    }
-    // gather every published key >= tau into the (now idle) page ring: a
-    // block's list is in descending order, so its keys >= tau are a prefix
-    // (a thread per block reads until the first key below tau)
-    for (int s = tid; s < p.n_lm; s += kConsumerThreads) {
-        const unsigned long long *q = p.lm_cand + (size_t)s * kMaxTopK;
-        for (int j = 0; j < K; ++j) {
-            const unsigned long long v = CHK(q + j, 8, 64) ? __ldcg(q + j) : 0ull;
-            if (v == 0ull || v < tau) break;
-            const int at = atomicAdd(&cx.misc->gcount, 1);
-            if (CHKS(g + at, 8, 65)) g[at] = v;
-        }
-    }
-    consumer_sync();
-    const int ng = cx.misc->gcount;
-    block_top64(g, ng);  // the top k of the candidates, descending, in g[0 .. k)
-    if (warp != 0) return;
-    // warp 0: candidate j = lane and j = lane + 32 (K <= 64), in key order
-    const int nc = ng < K ? ng : K;
-    const float zmax = key_value(g[0]);
-    const bool h0 = lane < nc, h1 = lane + 32 < nc;
-    const float z0 = h0 ? key_value(g[lane]) : 0.f, z1 = h1 ? key_value(g[lane + 32]) : 0.f;
-    const float e0 = h0 ? expf((z0 - zmax) * p.inv_temp) : 0.f, e1 = h1 ? expf((z1 - zmax) * p.inv_temp) : 0.f;
-    float c0 = e0, c1 = e1;  // inclusive prefix sums in candidate order
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const float a = __shfl_up_sync(0xFFFFFFFFu, c0, o), b = __shfl_up_sync(0xFFFFFFFFu, c1, o);
-        if (lane >= o) {
-            c0 += a;
-            c1 += b;
-        }
-    }
-    c1 += __shfl_sync(0xFFFFFFFFu, c0, 31);
-    const float need = p.top_p * __shfl_sync(0xFFFFFFFFu, c1, 31);
-    int nkeep = nc;
-    if (p.top_p < 1.f) {
-        const uint32_t b0 = __ballot_sync(0xFFFFFFFFu, h0 && c0 >= need);
-        const uint32_t b1 = __ballot_sync(0xFFFFFFFFu, h1 && c1 >= need);
-        nkeep = b0 ? __ffs(b0) : (b1 ? 32 + __ffs(b1) : nc);
-    }
-    unsigned long long best = 0ull;
-    if (lane < nkeep) {
-        const uint32_t i = key_index(g[lane]);
-        best = argmax_key(z0 * p.inv_temp + gumbel_noise(i, p.pos, p.bslot, p.seed_lo, p.seed_hi), i);
-    }
-    if (lane + 32 < nkeep) {
-        const uint32_t i = key_index(g[lane + 32]);
-        const unsigned long long k1 =
-            argmax_key(z1 * p.inv_temp + gumbel_noise(i, p.pos, p.bslot, p.seed_lo, p.seed_hi), i);
-        best = k1 > best ? k1 : best;
-    }
-    best = warp_max_u64(best);
-    if (lane == 0 && CHK(p.out_token, 4, 21)) *p.out_token = (int32_t)key_index(best);
+    const int tok = draw_filtered(p.lm_cand, p.n_lm, K, p.top_p, p.inv_temp, p.pos, p.bslot, p.seed_lo, p.seed_hi,
+                                  reinterpret_cast<unsigned long long *>(cx.pages), &cx.misc->gcount);
+    if (tid == 0 && CHK(p.out_token, 4, 21)) *p.out_token = tok;
 }
 
 __device__ void do_gemv(const Params &p, const Ctx &cx, const Instr &in, uint32_t &t, bool &bad) {

@@ -49,3 +49,68 @@ extern "C" cudaError_t mk_noise_launch(int n, int pos, int slot, uint64_t seed, 
                                                 words, out_words, out_noise);
     return cudaGetLastError();
 }
+
+// ---------------------------------------------------------------------------
+// Top-k / top-p draws of a fused batched step from its logits [B][V]: the
+// batched LM head writes every sequence's logits, then
+//   filter_lists: CTA (slice j, sequence b) keys entries [1024 j, 1024 j +
+//     1024) of sequence b's logits and publishes its top_k best, in order, as
+//     list j of sequence b;
+//   filter_draw: CTA b draws sequence b's token from its lists with the
+//     single-sequence epilogue's own tail (draw_filtered), on KV slot b's
+//     noise at the sequence's position.
+// ---------------------------------------------------------------------------
+namespace {
+constexpr int kFilterSlice = 1024;
+
+__global__ void __launch_bounds__(mk::kConsumerThreads) filter_lists(const float *logits, int V, int K,
+                                                                     unsigned long long *lists) {
+    __shared__ unsigned long long keys[kFilterSlice];
+    const int b = blockIdx.y, j = blockIdx.x, base = j * kFilterSlice;
+    const float *lg = logits + (size_t)b * V;
+    for (int i = threadIdx.x; i < kFilterSlice; i += blockDim.x) {
+        const int e = base + i;
+        keys[i] = e < V ? mk::argmax_key(lg[e], (uint32_t)e) : 0ull;  // no real key is 0
+    }
+    mk::consumer_sync();
+    mk::block_top64(keys, kFilterSlice);
+    unsigned long long *mine = lists + ((size_t)b * gridDim.x + j) * mk::kMaxTopK;
+    for (int t = threadIdx.x; t < K; t += blockDim.x) mine[t] = keys[t];
+}
+
+__global__ void __launch_bounds__(mk::kConsumerThreads) filter_draw(const unsigned long long *lists, int nl, int K,
+                                                                    float top_p, float inv_temp,
+                                                                    const int32_t *positions, uint32_t seed_lo,
+                                                                    uint32_t seed_hi, int32_t *out_tokens) {
+    extern __shared__ unsigned long long g[];  // max(nl * K, 64) keys
+    __shared__ int gcount;
+    const int b = blockIdx.x;
+    const int tok = mk::draw_filtered(lists + (size_t)b * nl * mk::kMaxTopK, nl, K, top_p, inv_temp, positions[b], b,
+                                      seed_lo, seed_hi, g, &gcount);
+    if (threadIdx.x == 0) out_tokens[b] = tok;
+}
+}  // namespace
+
+// Lists of the filtered draw of a batch: B * ceil(V / 1024) * kMaxTopK keys.
+extern "C" size_t mk_filter_lists_keys(int B, int V) {
+    return (size_t)B * ((V + kFilterSlice - 1) / kFilterSlice) * mk::kMaxTopK;
+}
+
+extern "C" cudaError_t mk_filtered_draw_batch(const float *logits, int B, int V, int K, float top_p, float inv_temp,
+                                              const int32_t *positions, uint64_t seed, unsigned long long *lists,
+                                              int32_t *out_tokens, cudaStream_t stream) {
+    if (B < 1 || V < 1 || K < 1 || K > mk::kMaxTopK) return cudaErrorInvalidValue;
+    const int nl = (V + kFilterSlice - 1) / kFilterSlice;
+    const size_t smem = (size_t)(nl * K > 64 ? nl * K : 64) * sizeof(unsigned long long);
+    static size_t configured = 0;
+    if (smem > configured) {
+        const cudaError_t e = cudaFuncSetAttribute(filter_draw, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        configured = smem;
+    }
+    filter_lists<<<dim3(nl, B), mk::kConsumerThreads, 0, stream>>>(logits, V, K, lists);
+    filter_draw<<<B, mk::kConsumerThreads, smem, stream>>>(lists, nl, K, top_p, inv_temp, positions,
+                                                           (uint32_t)(seed & 0xFFFFFFFFu), (uint32_t)(seed >> 32),
+                                                           out_tokens);
+    return cudaGetLastError();
+}

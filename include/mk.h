@@ -280,8 +280,11 @@ int mk_set_sampling(mk_handle *h, float temperature, uint64_t seed);
  *   3. the token is argmax over the kept set of logit / temperature + g,
  *      with the Gumbel noise g of mk_set_sampling.
  * top_k = 0 and top_p = 1 (the default) switch filtering off. The sums run
- * in fp32. With a filter on, mk_decode_step_batch steps its sequences one
- * launch each. MK_ERR_INVALID_ARG for top_k outside [0, MK_MAX_TOP_K] or
+ * in fp32. With a filter on, a fused batched step (mk_decode_step_batch)
+ * writes every sequence's logits (to an internal buffer if out_logits is
+ * NULL) and two short kernels after it draw each sequence's token; smaller
+ * batches run sequence by sequence as without a filter. MK_ERR_INVALID_ARG
+ * for top_k outside [0, MK_MAX_TOP_K] or
  * top_p outside (0, 1]; MK_ERR_UNSUPPORTED if the model's LM head has more
  * than 256 blocks. Host-only setting, takes effect on the next step.
  * Source: the glossary entry "Megakernel" (synthszr.com), section on

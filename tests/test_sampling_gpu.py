@@ -191,7 +191,8 @@ def test_llama1b_filtered_draws_match_the_oracle(cuda_dev):
     pair.close()
 
 
-def test_filtered_batch_steps_run_per_sequence(cuda_dev):
+def test_fused_batch_filtered_draws_match_the_oracle(cuda_dev):
+    # all sequences in one batched launch, then the draw kernels per sequence
     build()
     dev = torch.device("cuda:0")
     B, T = 3, 0.8
@@ -214,6 +215,34 @@ def test_filtered_batch_steps_run_per_sequence(cuda_dev):
         for b in range(B):
             check_filtered(gl[b], gt[b], T, 10, 0.8, step, b, f"seq {b} step {step}")
         toks.copy_(out)
+    mk.close()
+
+
+def test_llama1b_fused_batch_filtered_draws(cuda_dev):
+    # 8 sequences at the Llama-1B shape: 126 candidate lists of 1,024 entries
+    # per sequence, drawn on each sequence's own slot and position
+    build()
+    dev = torch.device("cuda:0")
+    B, T = 8, 0.7
+    w = synth.make_weights(LLAMA_1B, dev, 0)
+    k, v = synth.kv_cache(LLAMA_1B, 8, B, dev)
+    mk = _lib.Megakernel(LLAMA_1B, w, k, v)
+    mk.set_sampling(T, SEED)
+    toks = torch.arange(100, 100 + B, dtype=torch.int32, device=dev)
+    pos = torch.arange(B, dtype=torch.int32, device=dev) % 3
+    out = torch.zeros(B, dtype=torch.int32, device=dev)
+    logits = torch.empty(B, LLAMA_1B.vocab, dtype=torch.float32, device=dev)
+    for kk, pp in [(50, 0.9), (0, 0.5), (8, 1.0)]:
+        mk.set_sampling_filter(kk, pp)
+        mk.step_batch(toks, pos, out, logits)
+        torch.cuda.synchronize()
+        assert mk.status() == 0
+        gl = logits.double().cpu().numpy()
+        gt = out.cpu().numpy().tolist()
+        for b in range(B):
+            check_filtered(gl[b], gt[b], T, kk, pp, int(pos[b]), b, f"seq {b} k {kk} p {pp}")
+        toks.copy_(out)
+        pos += 1
     mk.close()
 
 
