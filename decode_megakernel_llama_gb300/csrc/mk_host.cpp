@@ -30,8 +30,11 @@ extern "C" cudaError_t mk_convert_bf16_f16(const void *src, void *dst, size_t n,
                                            cudaStream_t stream);
 extern "C" size_t mk_filter_lists_keys(int B, int V);
 extern "C" cudaError_t mk_filtered_draw_batch(const float *logits, int B, int V, int K, float top_p, float inv_temp,
-                                              const int32_t *positions, uint64_t seed, unsigned long long *lists,
-                                              int32_t *out_tokens, cudaStream_t stream);
+                                              const int32_t *positions, int pos0, uint64_t seed,
+                                              unsigned long long *lists, int32_t *out_tokens, cudaStream_t stream);
+extern "C" cudaError_t mk_sampled_draw_batch(const float *logits, int B, int V, float inv_temp,
+                                             const int32_t *positions, int pos0, uint64_t seed,
+                                             unsigned long long *keys, int32_t *out_tokens, cudaStream_t stream);
 extern "C" cudaError_t mk_noise_launch(int n, int pos, int slot, uint64_t seed, const uint32_t *words,
                                        uint32_t *out_words, float *out_noise, cudaStream_t stream);
 
@@ -690,6 +693,10 @@ struct mk_handle {
     // asks for none) and the candidate lists, made on the first such step
     float *bf_logits = nullptr;
     unsigned long long *bf_lists = nullptr;
+    // a sampled draw of the prefill's last position: its logits (when the
+    // caller asks for none) and the candidate lists / slice keys
+    float *pd_logits = nullptr;
+    unsigned long long *pd_lists = nullptr;
 };
 
 namespace {
@@ -920,7 +927,7 @@ int mk_decode_step_batch(mk_handle *h, const int32_t *d_tokens, const int32_t *d
         if (rc || !filtered) return rc;
         // a filter set with only top_p takes the nucleus among the kMaxTopK best
         const int K = h->top_k > 0 ? h->top_k : mk::kMaxTopK;
-        e = mk_filtered_draw_batch(logits, batch, V, K, h->top_p, h->inv_temp, d_positions, h->seed, h->bf_lists,
+        e = mk_filtered_draw_batch(logits, batch, V, K, h->top_p, h->inv_temp, d_positions, 0, h->seed, h->bf_lists,
                                    out_tokens, (cudaStream_t)stream);
         if (e != cudaSuccess) return cuda_fail(e, "filtered draw of the batch");
         return MK_OK;
@@ -1093,8 +1100,34 @@ int mk_prefill(mk_handle *h, const int32_t *d_tokens, int32_t n, int32_t start_p
         e = cudaMemcpy(sc.err, &err_keep, sizeof err_keep, cudaMemcpyHostToDevice);
         if (e != cudaSuccess) return cuda_fail(e, "prefill status");
     }
-    e = mkpf::run(h->pf_model, h->pf, d_tokens, n, start_pos, out_logits, out_token, (cudaStream_t)stream);
+    // with sampling on, the token of the last position is drawn as the decode
+    // step at that position would draw it (same noise, same filter)
+    const bool sampled = h->inv_temp > 0.f;
+    float *logits = out_logits;
+    if (sampled) {
+        if (!h->pd_lists) {
+            e = cudaMalloc(&h->pd_lists, sizeof(unsigned long long) * mk_filter_lists_keys(1, h->cfg.vocab));
+            if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(prefill draw lists)");
+        }
+        if (!logits && !h->pd_logits) {
+            e = cudaMalloc(&h->pd_logits, sizeof(float) * (size_t)h->cfg.vocab);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(prefill logits)");
+        }
+        if (!logits) logits = h->pd_logits;
+    }
+    e = mkpf::run(h->pf_model, h->pf, d_tokens, n, start_pos, logits, out_token, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+    if (sampled) {
+        const int pos = start_pos + n - 1;
+        if (h->top_k > 0 || h->top_p < 1.f)
+            e = mk_filtered_draw_batch(logits, 1, h->cfg.vocab, h->top_k > 0 ? h->top_k : mk::kMaxTopK, h->top_p,
+                                       h->inv_temp, nullptr, pos, h->seed, h->pd_lists, out_token,
+                                       (cudaStream_t)stream);
+        else
+            e = mk_sampled_draw_batch(logits, 1, h->cfg.vocab, h->inv_temp, nullptr, pos, h->seed, h->pd_lists,
+                                      out_token, (cudaStream_t)stream);
+        if (e != cudaSuccess) return cuda_fail(e, "prefill draw");
+    }
     return MK_OK;
 }
 
@@ -1219,6 +1252,8 @@ void mk_destroy(mk_handle *h) {
     if (h->pf_mem) cudaFree(h->pf_mem);
     if (h->bf_logits) cudaFree(h->bf_logits);
     if (h->bf_lists) cudaFree(h->bf_lists);
+    if (h->pd_logits) cudaFree(h->pd_logits);
+    if (h->pd_lists) cudaFree(h->pd_lists);
     delete h;
 }
 

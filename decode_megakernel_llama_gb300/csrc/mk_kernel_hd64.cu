@@ -51,14 +51,17 @@ extern "C" cudaError_t mk_noise_launch(int n, int pos, int slot, uint64_t seed, 
 }
 
 // ---------------------------------------------------------------------------
-// Top-k / top-p draws of a fused batched step from its logits [B][V]: the
-// batched LM head writes every sequence's logits, then
+// Draws from logits [B][V] already in memory, for a fused batched step with a
+// top-k / top-p filter (its LM head writes every sequence's logits) and for a
+// prefill's last position: sequence b draws with KV slot b's noise at
+// position positions[b] (positions NULL: pos0). Filtered:
 //   filter_lists: CTA (slice j, sequence b) keys entries [1024 j, 1024 j +
 //     1024) of sequence b's logits and publishes its top_k best, in order, as
 //     list j of sequence b;
 //   filter_draw: CTA b draws sequence b's token from its lists with the
-//     single-sequence epilogue's own tail (draw_filtered), on KV slot b's
-//     noise at the sequence's position.
+//     single-sequence epilogue's own tail (draw_filtered).
+// Plain (temperature only): sample_slices keys logit / T + noise per slice
+// and keeps the slice's best; sample_reduce takes the best of the slices.
 // ---------------------------------------------------------------------------
 namespace {
 constexpr int kFilterSlice = 1024;
@@ -80,14 +83,50 @@ __global__ void __launch_bounds__(mk::kConsumerThreads) filter_lists(const float
 
 __global__ void __launch_bounds__(mk::kConsumerThreads) filter_draw(const unsigned long long *lists, int nl, int K,
                                                                     float top_p, float inv_temp,
-                                                                    const int32_t *positions, uint32_t seed_lo,
-                                                                    uint32_t seed_hi, int32_t *out_tokens) {
+                                                                    const int32_t *positions, int pos0,
+                                                                    uint32_t seed_lo, uint32_t seed_hi,
+                                                                    int32_t *out_tokens) {
     extern __shared__ unsigned long long g[];  // max(nl * K, 64) keys
     __shared__ int gcount;
     const int b = blockIdx.x;
-    const int tok = mk::draw_filtered(lists + (size_t)b * nl * mk::kMaxTopK, nl, K, top_p, inv_temp, positions[b], b,
+    const int pos = positions ? positions[b] : pos0;
+    const int tok = mk::draw_filtered(lists + (size_t)b * nl * mk::kMaxTopK, nl, K, top_p, inv_temp, pos, b,
                                       seed_lo, seed_hi, g, &gcount);
     if (threadIdx.x == 0) out_tokens[b] = tok;
+}
+
+__global__ void __launch_bounds__(256) sample_slices(const float *logits, int V, float inv_temp,
+                                                     const int32_t *positions, int pos0, uint32_t seed_lo,
+                                                     uint32_t seed_hi, unsigned long long *keys) {
+    __shared__ unsigned long long best8[8];
+    const int b = blockIdx.y, j = blockIdx.x, base = j * kFilterSlice;
+    const int pos = positions ? positions[b] : pos0;
+    const float *lg = logits + (size_t)b * V;
+    unsigned long long best = 0ull;
+    for (int i = threadIdx.x; i < kFilterSlice; i += blockDim.x) {
+        const int e = base + i;
+        if (e < V) {
+            const unsigned long long k =
+                mk::argmax_key(lg[e] * inv_temp + mk::gumbel_noise((uint32_t)e, pos, b, seed_lo, seed_hi), (uint32_t)e);
+            best = k > best ? k : best;
+        }
+    }
+    best = mk::warp_max_u64(best);
+    if ((threadIdx.x & 31) == 0) best8[threadIdx.x >> 5] = best;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (int w = 1; w < 8; ++w) best = best8[w] > best ? best8[w] : best;
+        best = best8[0] > best ? best8[0] : best;
+        keys[(size_t)b * gridDim.x + j] = best;
+    }
+}
+
+__global__ void __launch_bounds__(32) sample_reduce(const unsigned long long *keys, int ns, int32_t *out_tokens) {
+    const int b = blockIdx.x;
+    unsigned long long best = 0ull;
+    for (int j = threadIdx.x; j < ns; j += 32) best = keys[(size_t)b * ns + j] > best ? keys[(size_t)b * ns + j] : best;
+    best = mk::warp_max_u64(best);
+    if (threadIdx.x == 0) out_tokens[b] = (int32_t)mk::key_index(best);
 }
 }  // namespace
 
@@ -97,8 +136,8 @@ extern "C" size_t mk_filter_lists_keys(int B, int V) {
 }
 
 extern "C" cudaError_t mk_filtered_draw_batch(const float *logits, int B, int V, int K, float top_p, float inv_temp,
-                                              const int32_t *positions, uint64_t seed, unsigned long long *lists,
-                                              int32_t *out_tokens, cudaStream_t stream) {
+                                              const int32_t *positions, int pos0, uint64_t seed,
+                                              unsigned long long *lists, int32_t *out_tokens, cudaStream_t stream) {
     if (B < 1 || V < 1 || K < 1 || K > mk::kMaxTopK) return cudaErrorInvalidValue;
     const int nl = (V + kFilterSlice - 1) / kFilterSlice;
     const size_t smem = (size_t)(nl * K > 64 ? nl * K : 64) * sizeof(unsigned long long);
@@ -109,8 +148,21 @@ extern "C" cudaError_t mk_filtered_draw_batch(const float *logits, int B, int V,
         configured = smem;
     }
     filter_lists<<<dim3(nl, B), mk::kConsumerThreads, 0, stream>>>(logits, V, K, lists);
-    filter_draw<<<B, mk::kConsumerThreads, smem, stream>>>(lists, nl, K, top_p, inv_temp, positions,
+    filter_draw<<<B, mk::kConsumerThreads, smem, stream>>>(lists, nl, K, top_p, inv_temp, positions, pos0,
                                                            (uint32_t)(seed & 0xFFFFFFFFu), (uint32_t)(seed >> 32),
                                                            out_tokens);
+    return cudaGetLastError();
+}
+
+// The plain draw (temperature, no filter) of B sequences from their logits;
+// keys: B * ceil(V / 1024) slots of scratch.
+extern "C" cudaError_t mk_sampled_draw_batch(const float *logits, int B, int V, float inv_temp,
+                                             const int32_t *positions, int pos0, uint64_t seed,
+                                             unsigned long long *keys, int32_t *out_tokens, cudaStream_t stream) {
+    if (B < 1 || V < 1 || !(inv_temp > 0.f)) return cudaErrorInvalidValue;
+    const int ns = (V + kFilterSlice - 1) / kFilterSlice;
+    sample_slices<<<dim3(ns, B), 256, 0, stream>>>(logits, V, inv_temp, positions, pos0, (uint32_t)(seed & 0xFFFFFFFFu),
+                                                   (uint32_t)(seed >> 32), keys);
+    sample_reduce<<<B, 32, 0, stream>>>(keys, ns, out_tokens);
     return cudaGetLastError();
 }

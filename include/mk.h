@@ -166,8 +166,10 @@ int mk_decode_step_batch(mk_handle *h, const int32_t *d_tokens, const int32_t *d
  * n) (device int32[n]) at positions start_pos .. start_pos + n - 1 through
  * every layer at once, writes the key/value rows of all n positions into
  * the KV cache, and writes the logits of the last prompt position to
- * out_logits (device float[vocab], nullable) and its greedy token to
- * out_token (device int32[1]). The cache then holds what n consecutive
+ * out_logits (device float[vocab], nullable) and the next token to out_token
+ * (device int32[1]): greedy, or with sampling on (mk_set_sampling,
+ * mk_set_sampling_filter) drawn as the decode step at that position would
+ * draw it (the same noise and filter). The cache then holds what n consecutive
  * mk_decode_step calls would have left (to rounding), so decoding continues
  * at start_pos + n. The projections run as tensor-core contractions
  * (tcgen05.mma, bf16 weights x the activations split into two bf16 terms,

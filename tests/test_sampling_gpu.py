@@ -246,6 +246,36 @@ def test_llama1b_fused_batch_filtered_draws(cuda_dev):
     mk.close()
 
 
+@pytest.mark.parametrize("top_k,top_p", [(0, 1.0), (40, 0.9)])
+def test_prefill_token_is_drawn_like_the_decode_step(cuda_dev, top_k, top_p):
+    # with sampling on, the prefill's token is the draw of its last position
+    # (plain, then filtered) on that position's noise
+    T, n = 0.8, 8
+    pair = Pair(TINY, 16)
+    pair.mk.set_sampling(T, SEED)
+    pair.mk.set_sampling_filter(top_k, top_p)
+    dev = torch.device("cuda:0")
+    prompt = synth.prompt_tokens(TINY.vocab, n)
+    out = torch.zeros(1, dtype=torch.int32, device=dev)
+    logits = torch.empty(TINY.vocab, dtype=torch.float32, device=dev)
+    pair.mk.prefill(prompt.to(dev), 0, out, logits)
+    torch.cuda.synchronize()
+    assert pair.mk.status() == 0
+    for i in range(n):
+        ol, _ = pair.orc.decode_step(int(prompt[i]), i)
+    gl, gt = logits.double().cpu().numpy(), int(out.item())
+    if top_k == 0 and top_p >= 1.0:
+        check_sampled(gl, gt, ol, T, n - 1, 0, "prefill, plain draw")
+    else:
+        check_filtered(gl, gt, T, top_k, top_p, n - 1, 0, "prefill, filtered draw")
+    # and without logits requested (an internal buffer takes them)
+    out2 = torch.zeros(1, dtype=torch.int32, device=dev)
+    pair.mk.prefill(prompt.to(dev), 0, out2)
+    torch.cuda.synchronize()
+    assert int(out2.item()) == gt
+    pair.close()
+
+
 def test_filter_arguments_are_checked(cuda_dev):
     pair = Pair(TINY, 8)
     for k, p in [(-1, 1.0), (65, 1.0), (5, 0.0), (5, 1.5), (5, float("nan"))]:
