@@ -962,13 +962,15 @@ int mk_decode_step_host(mk_handle *h, const int32_t *host_token, int32_t positio
     int32_t *tok_out = nullptr;
     {
         cudaPointerAttributes ai{}, ao{};
-        if (cudaPointerGetAttributes(&ai, host_token) == cudaSuccess && ai.type == cudaMemoryTypeHost &&
-            ai.devicePointer && cudaPointerGetAttributes(&ao, host_out_token) == cudaSuccess &&
+        const cudaError_t qi = cudaPointerGetAttributes(&ai, host_token);
+        const cudaError_t qo = qi == cudaSuccess ? cudaPointerGetAttributes(&ao, host_out_token) : cudaSuccess;
+        // a failed query only means "not usable in place": clear the error it set
+        if (qi != cudaSuccess || qo != cudaSuccess) (void)cudaGetLastError();
+        if (qi == cudaSuccess && qo == cudaSuccess && ai.type == cudaMemoryTypeHost && ai.devicePointer &&
             ao.type == cudaMemoryTypeHost && ao.devicePointer) {
             tok_in = static_cast<const int32_t *>(ai.devicePointer);
             tok_out = static_cast<int32_t *>(ao.devicePointer);
         }
-        (void)cudaGetLastError();  // an unregistered pointer is not an error of this call
     }
     if (!tok_in) {
         e = cudaMemcpyAsync(h->d_tok_in, host_token, sizeof(int32_t), cudaMemcpyHostToDevice, s);

@@ -1151,6 +1151,7 @@ __device__ __forceinline__ void warp_merge_top64(unsigned long long (&a)[2], con
 __device__ void block_top64(unsigned long long *keys, int n) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nrun = n > 64 ? (n + 63) / 64 : 1;
+    const int cap = n > 64 ? n : 64;  // entries that may be written (a short last run keeps its real keys)
     unsigned long long v[2], w2[2];
     auto load_run = [&](int run, unsigned long long (&x)[2]) {
         const int base = run * 64;
@@ -1166,14 +1167,14 @@ __device__ void block_top64(unsigned long long *keys, int n) {
             warp_merge_top64(v, w2);
         }
         __syncwarp();
-        keys[2 * pair * 64 + lane] = v[0];
-        keys[2 * pair * 64 + lane + 32] = v[1];
+        if (2 * pair * 64 + lane < cap) keys[2 * pair * 64 + lane] = v[0];
+        if (2 * pair * 64 + lane + 32 < cap) keys[2 * pair * 64 + lane + 32] = v[1];
     }
     consumer_sync();
     for (int step = 2; step < nrun; step <<= 1) {  // runs 0, 2 step, 4 step, ... hold the survivors
         for (int pair = warp; 2 * pair * step < nrun; pair += kConsumerWarps) {
             const int r0 = 2 * pair * step, r1 = r0 + step;
-            if (r1 < nrun) {
+            if (r1 < nrun) {  // r0 < r1: never the short last run, so 64 entries fit
                 load_run(r0, v);
                 load_run(r1, w2);
                 warp_merge_top64(v, w2);
@@ -1269,7 +1270,7 @@ __device__ int draw_filtered(const unsigned long long *lists, int nl, int K, flo
 // the temperature reaches top_p) and takes the Gumbel-max among the kept
 // candidates.
 __device__ void lm_filtered(const Params &p, const Ctx &cx, const Instr &in, const float *red, int sw) {
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int tid = threadIdx.x;
     const int n = in.a1, r0 = in.a0, K = p.top_k;
     unsigned long long *keys = reinterpret_cast<unsigned long long *>(cx.xbuf);  // n <= 1024 keys (8 KB)
     if (tid == 0) cx.misc->staged_key = -1;  // xbuf stops holding the staged input

@@ -115,8 +115,7 @@ __global__ void __launch_bounds__(256) sample_slices(const float *logits, int V,
     if ((threadIdx.x & 31) == 0) best8[threadIdx.x >> 5] = best;
     __syncthreads();
     if (threadIdx.x == 0) {
-        for (int w = 1; w < 8; ++w) best = best8[w] > best ? best8[w] : best;
-        best = best8[0] > best ? best8[0] : best;
+        for (int w = 0; w < 8; ++w) best = best8[w] > best ? best8[w] : best;
         keys[(size_t)b * gridDim.x + j] = best;
     }
 }

@@ -232,7 +232,8 @@ def test_llama1b_fused_batch_filtered_draws(cuda_dev):
     pos = torch.arange(B, dtype=torch.int32, device=dev) % 3
     out = torch.zeros(B, dtype=torch.int32, device=dev)
     logits = torch.empty(B, LLAMA_1B.vocab, dtype=torch.float32, device=dev)
-    for kk, pp in [(50, 0.9), (0, 0.5), (8, 1.0)]:
+    # top-k 1: 126 lists of one key, fewer keys than a run of 64
+    for kk, pp in [(50, 0.9), (0, 0.5), (8, 1.0), (1, 1.0)]:
         mk.set_sampling_filter(kk, pp)
         mk.step_batch(toks, pos, out, logits)
         torch.cuda.synchronize()
