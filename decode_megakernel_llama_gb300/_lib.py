@@ -91,6 +91,8 @@ def load(path: str | None = None):
                                          ctypes.POINTER(mk_kv_cache), _I32, _I32, _VP, _VP, _VP]
     L.mk_set_sampling_filter.argtypes = [_VP, _I32, ctypes.c_float]
     L.mk_sampling_noise.argtypes = [_I32, _I32, _I32, ctypes.c_uint64, _VP, _VP, _VP, _VP]
+    L.mk_draw_from_logits.argtypes = [_VP, _I32, _I32, ctypes.c_float, _I32, ctypes.c_float, _VP, ctypes.c_uint64,
+                                      _VP, _VP]
     L.mk_w2_pack.argtypes = [_VP, ctypes.c_int64, ctypes.c_int64, _VP]
     L.mk_w2_unpack.argtypes = [_VP, ctypes.c_int64, ctypes.c_int64, _VP]
     L.mk_w2a8_gemv.argtypes = [_VP, ctypes.c_float, _I32, _I32, _VP, _VP, _VP]
@@ -176,6 +178,16 @@ def sampling_noise(n: int, position: int, slot: int, seed: int, out_words=None, 
     ptr = lambda t: t.data_ptr() if t is not None else None
     check(load().mk_sampling_noise(int(n), int(position), int(slot), int(seed) & ((1 << 64) - 1),
                                    ptr(words), ptr(out_words), ptr(out_noise), _stream_ptr(stream)))
+
+
+def draw_from_logits(logits, temperature: float, top_k: int, top_p: float, positions, seed: int, out_tokens,
+                     stream=None) -> None:
+    """mk_draw_from_logits: logits float32 CUDA tensor [B][V]; positions and
+    out_tokens int32 CUDA tensors [B]; sequence b draws on slot b's noise."""
+    B, V = int(logits.shape[0]), int(logits.shape[1])
+    check(load().mk_draw_from_logits(logits.data_ptr(), B, V, float(temperature), int(top_k), float(top_p),
+                                     positions.data_ptr(), int(seed) & ((1 << 64) - 1), out_tokens.data_ptr(),
+                                     _stream_ptr(stream)))
 
 
 def w2_pack(q):

@@ -1172,6 +1172,40 @@ int mk_sampling_noise(int32_t n, int32_t position, int32_t slot, uint64_t seed, 
     return MK_OK;
 }
 
+int mk_draw_from_logits(const float *d_logits, int32_t batch, int32_t vocab, float temperature, int32_t top_k,
+                        float top_p, const int32_t *d_positions, uint64_t seed, int32_t *d_out_tokens, void *stream) {
+    if (!d_logits || !d_positions || !d_out_tokens) return fail(MK_ERR_INVALID_ARG, "NULL pointer");
+    if (batch < 1 || vocab < 1) return fail(MK_ERR_INVALID_ARG, "batch and vocab must be >= 1");
+    if (!(temperature > 0.f) || !std::isfinite(temperature))
+        return fail(MK_ERR_INVALID_ARG, "temperature must be finite and > 0");
+    if (top_k < 0 || top_k > mk::kMaxTopK) return fail(MK_ERR_INVALID_ARG, "top_k outside [0, MK_MAX_TOP_K]");
+    if (!(top_p > 0.f && top_p <= 1.f)) return fail(MK_ERR_INVALID_ARG, "top_p outside (0, 1]");
+    // the kernels' scratch: candidate lists (or slice keys), grown as needed
+    static unsigned long long *work = nullptr;
+    static size_t have = 0;
+    const size_t need = mk_filter_lists_keys(batch, vocab);
+    if (need > have) {
+        if (work) {
+            cudaDeviceSynchronize();
+            cudaFree(work);
+        }
+        work = nullptr;
+        have = 0;
+        const cudaError_t e = cudaMalloc(&work, need * sizeof(unsigned long long));
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(draw scratch)");
+        have = need;
+    }
+    const float inv_temp = 1.0f / temperature;
+    const cudaError_t e =
+        top_k > 0 || top_p < 1.f
+            ? mk_filtered_draw_batch(d_logits, batch, vocab, top_k > 0 ? top_k : mk::kMaxTopK, top_p, inv_temp,
+                                     d_positions, 0, seed, work, d_out_tokens, (cudaStream_t)stream)
+            : mk_sampled_draw_batch(d_logits, batch, vocab, inv_temp, d_positions, 0, seed, work, d_out_tokens,
+                                    (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "draw kernels");
+    return MK_OK;
+}
+
 int mk_set_trace(mk_handle *h, int32_t enable) {
     if (!h) return fail(MK_ERR_INVALID_ARG, "handle is NULL");
     if (enable && !h->d_trace) {

@@ -309,6 +309,21 @@ int mk_set_sampling_filter(mk_handle *h, int32_t top_k, float top_p);
 int mk_sampling_noise(int32_t n, int32_t position, int32_t slot, uint64_t seed, const uint32_t *d_words,
                       uint32_t *d_out_words, float *d_out_noise, void *stream);
 
+/* Tokens drawn from logits already on the device, by the kernels a fused
+ * batched step (with a filter) and a sampled prefill run after their LM
+ * head: for b = 0..batch-1, d_out_tokens[b] (device int32[batch]) is the
+ * draw of mk_set_sampling at `temperature` from d_logits[b*vocab ..
+ * (b+1)*vocab) (device float[batch][vocab]) with the noise of KV slot b at
+ * position d_positions[b] (device int32[batch]), filtered as
+ * mk_set_sampling_filter describes when top_k > 0 or top_p < 1. The library
+ * keeps the kernels' scratch, grown as needed (not thread-safe).
+ * Asynchronous on `stream`. MK_ERR_INVALID_ARG for NULL pointers, batch or
+ * vocab < 1, temperature <= 0 or not finite, top_k outside [0,
+ * MK_MAX_TOP_K] or top_p outside (0, 1].
+ * Source: as mk_set_sampling_filter; a diagnostic of this library. */
+int mk_draw_from_logits(const float *d_logits, int32_t batch, int32_t vocab, float temperature, int32_t top_k,
+                        float top_p, const int32_t *d_positions, uint64_t seed, int32_t *d_out_tokens, void *stream);
+
 
 /* ---- W2A8 GEMV: ternary weights, 8-bit activations ----------------------
  * The GEMV of the page "BitNet 1.58bit GPU Inference Kernel: Revolutionäre

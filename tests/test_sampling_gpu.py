@@ -277,6 +277,42 @@ def test_prefill_token_is_drawn_like_the_decode_step(cuda_dev, top_k, top_p):
     pair.close()
 
 
+@pytest.mark.parametrize("V", [1000, 4096, 50257, 128256])
+@pytest.mark.parametrize("top_k,top_p", [(0, 1.0), (1, 1.0), (5, 1.0), (64, 1.0), (0, 0.9), (40, 0.2), (7, 0.95)])
+def test_draw_from_logits_matches_the_oracle(cuda_dev, V, top_k, top_p):
+    # the draw kernels on their own, over vocabularies that leave short runs
+    # and short lists (1,000 entries: one slice of 1,024; 50,257: a ragged last
+    # slice), with seeded N(0, 9) logits; two sequences on slots 0 and 1
+    T, B = 0.9, 2
+    rng = np.random.default_rng(V * 131 + top_k * 7 + int(top_p * 100))
+    logits = (rng.standard_normal((B, V)) * 3.0).astype(np.float32)
+    pos = np.array([7, 11], dtype=np.int32)
+    out = torch.zeros(B, dtype=torch.int32, device=cuda_dev)
+    _lib.draw_from_logits(torch.from_numpy(logits).to(cuda_dev), T, top_k, top_p,
+                          torch.from_numpy(pos).to(cuda_dev), SEED, out)
+    torch.cuda.synchronize()
+    toks = out.cpu().numpy().tolist()
+    for b in range(B):
+        gl = logits[b].astype(np.float64)
+        if top_k == 0 and top_p >= 1.0:  # the plain draw: the Gumbel-max of the logits
+            z = sampling.sample_scores(gl, T, int(pos[b]), b, SEED)
+            top2 = np.sort(z)[-2:]
+            if top2[1] - top2[0] > 1e-4 * max(1.0, abs(top2[1])):
+                assert toks[b] == int(np.argmax(z)), f"V {V} b {b}"
+        else:
+            check_filtered(gl, toks[b], T, top_k, top_p, int(pos[b]), b, f"V {V} k {top_k} p {top_p} b {b}")
+
+
+def test_draw_from_logits_rejects_bad_arguments(cuda_dev):
+    lg = torch.zeros(1, 10, device=cuda_dev)
+    pos = torch.zeros(1, dtype=torch.int32, device=cuda_dev)
+    out = torch.zeros(1, dtype=torch.int32, device=cuda_dev)
+    for T, k, p in [(0.0, 0, 1.0), (float("nan"), 0, 1.0), (1.0, 65, 1.0), (1.0, 0, 0.0), (1.0, -1, 1.0)]:
+        with pytest.raises(_lib.MKError) as e:
+            _lib.draw_from_logits(lg, T, k, p, pos, SEED, out)
+        assert e.value.code == _lib.MK_ERR_INVALID_ARG
+
+
 def test_filter_arguments_are_checked(cuda_dev):
     pair = Pair(TINY, 8)
     for k, p in [(-1, 1.0), (65, 1.0), (5, 0.0), (5, 1.5), (5, float("nan"))]:
