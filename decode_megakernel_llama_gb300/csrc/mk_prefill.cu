@@ -943,10 +943,11 @@ bool make_map(CUtensorMap *map, const void *ptr, int rows, int K, int box_rows) 
 // sets the time. The ring of one CTA fills an SM, so more CTAs than SMs run
 // in two waves. Without a split the token tile is the smallest of 32, 64,
 // 128 whose grid still fits one wave (more CTAs in flight at no extra chunks
-// per CTA). Only a long reduction (K / 64 >= 64 chunks) is split, with token
-// tiles of 128, into as many parts as fit one wave, at least 32 chunks each:
-// measured, shorter splits lose more to writing and re-reading the partial
-// sums than they gain in parallel chunks.
+// per CTA). A long reduction (K / 64 >= 64 chunks) is split, with token
+// tiles of 128, into as many parts as fit one wave, at least 16 chunks each
+// (measured at 128 tokens: 32-chunk splits 1.57 ms per prefill, 16-chunk
+// 1.51, 8-chunk 1.54: shorter splits lose more to writing and re-reading the
+// partial sums than they gain in parallel chunks).
 struct GemmShape {
     int bn, S;
 };
@@ -974,7 +975,7 @@ GemmShape pick_shape(int M, int N, int K, int n_sm, bool norm) {
     if (nk >= 64) {
         const int ctas = rt * ((N + 127) / 128);
         int S = n_sm / ctas;
-        if (S > nk / 32) S = nk / 32;
+        if (S > nk / 16) S = nk / 16;
         if (S > kMaxSplits) S = kMaxSplits;
         g.S = S < 1 ? 1 : S;
         if (norm && g.S < 2) g.S = 2;
