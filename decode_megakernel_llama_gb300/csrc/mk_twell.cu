@@ -143,8 +143,17 @@ __global__ void __launch_bounds__(kRT) twell_reduce(const float *__restrict__ pa
     const int c = blockIdx.x * 32 + lane;
     float acc = 0.f;
     if (c < D) {
-#pragma unroll 4
-        for (int b = s; b < nb; b += kRT / 32) acc += part[(size_t)b * D + c];
+        // the slice's blocks 16 at a time, all 16 loads in flight before any add
+        for (int b0 = s; b0 < nb; b0 += 16 * (kRT / 32)) {
+            float v[16];
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                const int b = b0 + u * (kRT / 32);
+                v[u] = b < nb ? part[(size_t)b * D + c] : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < 16; ++u) acc += v[u];
+        }
     }
     ss[s][lane] = acc;
     __syncthreads();
