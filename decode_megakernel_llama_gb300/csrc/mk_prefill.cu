@@ -579,8 +579,9 @@ __global__ void __launch_bounds__(kSnThreads) sum_splits_norm(const float *__res
 // RoPE on q and k of token t (position pos0 + t) from the fp32 QKV rows, q
 // kept (rotated) in place, bf16 k and v written into the cache at the position.
 // With S > 0 the q|k|v row is first summed from the K-split partials
-// part[z][t][.] (z in order) and the sums written back to QKV (q rotated).
-// The blocks of a token (gridDim.y of them) share its pairs.
+// part[z][t][.] (z in order): q's sums go to QKV (rotated), k's and v's to
+// the cache as above. The blocks of a token (gridDim.y of them) share its
+// pairs.
 __global__ void rope_append(float *__restrict__ QKV, const float *__restrict__ part, int S, int n, int Hq, int Hkv,
                             int hd, int pos0, const float *__restrict__ rope, int max_seq, uint16_t *__restrict__ kc,
                             uint16_t *__restrict__ vc) {
