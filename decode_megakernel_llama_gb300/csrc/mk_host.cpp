@@ -35,6 +35,8 @@ extern "C" cudaError_t mk_filtered_draw_batch(const float *logits, int B, int V,
 extern "C" cudaError_t mk_sampled_draw_batch(const float *logits, int B, int V, float inv_temp,
                                              const int32_t *positions, int pos0, uint64_t seed,
                                              unsigned long long *keys, int32_t *out_tokens, cudaStream_t stream);
+extern "C" cudaError_t mk_batch_final_norm(const float *x, int B, int d, const uint16_t *gain, float eps, uint16_t *hi,
+                                           uint16_t *lo, cudaStream_t stream);
 extern "C" cudaError_t mk_noise_launch(int n, int pos, int slot, uint64_t seed, const uint32_t *words,
                                        uint32_t *out_words, float *out_noise, cudaStream_t stream);
 
@@ -181,14 +183,11 @@ int build_plan(const mk_config *c, int n_sm, Plan &P, int nb) {
     P.nb = nb;
     if (nb > 1) {
         // batched steps: hd 64 instances
+        // (the LM head of a batched step runs after the launch, on the tensor
+        // cores: no LM-head instructions in this plan)
         if (nb > mk::kMaxBatch || hd != 64 || !make_geo_batch(d, P.geo_qkv) ||
-            !make_geo_batch(qd, P.geo_o) || !make_geo_batch(d, P.geo_gu) || !make_geo_batch(F, P.geo_down) ||
-            !make_geo_batch(d, P.geo_lm))
+            !make_geo_batch(qd, P.geo_o) || !make_geo_batch(d, P.geo_gu) || !make_geo_batch(F, P.geo_down))
             return fail(MK_ERR_UNSUPPORTED, "no batched tile geometry for this model");
-        // LM-head rows per SM beyond the shared accumulators run through a ring
-        // of 8 tiles, which must fit them
-        if ((V + n_sm - 1) / n_sm * mk::kMaxBatch > mk::kBatchAcc && P.geo_lm.rt * 8 * mk::kMaxBatch > mk::kBatchAcc)
-            return fail(MK_ERR_UNSUPPORTED, "no batched LM-head geometry for this model");
     } else {
         // input floats per lane: 32 gives the fewest K-slices per row
         auto geo = [&](int K, Geo &g) { return make_geo(K, g, 32); };
@@ -360,18 +359,21 @@ int build_plan(const mk_config *c, int n_sm, Plan &P, int nb) {
         }
         prev_down = n_down;
     }
-    // ---- final norm + tied LM head + argmax
+    // ---- final norm + tied LM head + argmax (single-sequence steps; a batched
+    // step's LM head follows its launch)
     int slot = 0;
-    for (const Chunk &ch : split_rows(V, 2.0 * d, load, cap_lm)) {
-        Instr in = mk_instr(mk::OP_LMHEAD, L, mk::kStagesPerLayer * L);
-        in.layer = 0;
-        in.a0 = ch.r0;
-        in.a1 = ch.n;
-        in.wait_ctr = cl.down_done + (L - 1);
-        in.wait_target = prev_down;
-        in.slot = slot++;
-        set_bytes(in, 2ll * ch.n * d);
-        P.q[ch.sm].push_back(in);
+    if (nb == 1) {
+        for (const Chunk &ch : split_rows(V, 2.0 * d, load, cap_lm)) {
+            Instr in = mk_instr(mk::OP_LMHEAD, L, mk::kStagesPerLayer * L);
+            in.layer = 0;
+            in.a0 = ch.r0;
+            in.a1 = ch.n;
+            in.wait_ctr = cl.down_done + (L - 1);
+            in.wait_target = prev_down;
+            in.slot = slot++;
+            set_bytes(in, 2ll * ch.n * d);
+            P.q[ch.sm].push_back(in);
+        }
     }
     P.n_lm = slot;
     return MK_OK;
@@ -681,18 +683,24 @@ struct mk_handle {
     mkint::Image bim;
     mk::Params bbase{};
     void *bdev_mem = nullptr;
-    void *w16 = nullptr;  // fp16 copies of the GEMV weights and the LM head (batched steps)
+    void *w16 = nullptr;  // fp16 copies of the GEMV weights (batched steps)
     size_t bzero_bytes = 0;
+    // the batched LM head, after the launch on the tensor cores: the bf16
+    // embedding's tensor map, the final norm's hi / lo terms [2][max_batch][d],
+    // the contraction's wait status, and the logits [max_batch][V] and draw
+    // scratch that the step uses when the caller asks for no logits
+    CUtensorMap emb_map;
+    void *blm_mem = nullptr;
+    uint16_t *blm_hi = nullptr, *blm_lo = nullptr;
+    int *blm_err = nullptr;
+    float *bf_logits = nullptr;
+    unsigned long long *bf_lists = nullptr;
     // multi-token prefill (mk_prefill): tensor maps of the weights, made on
     // the first call, and scratch for the largest prompt so far
     bool pf_ready = false;
     mkpf::Model pf_model;
     mkpf::Scratch pf;
     void *pf_mem = nullptr;
-    // filtered draws of a fused batched step: its logits (when the caller
-    // asks for none) and the candidate lists, made on the first such step
-    float *bf_logits = nullptr;
-    unsigned long long *bf_lists = nullptr;
     // a sampled draw of the prefill's last position: its logits (when the
     // caller asks for none) and the candidate lists / slice keys
     float *pd_logits = nullptr;
@@ -791,10 +799,9 @@ int mk_create(const mk_config *config, const mk_weights *w, const mk_kv_cache *k
         const size_t d = c.d_model, qd = (size_t)c.n_heads * c.head_dim, kvd = (size_t)c.n_kv_heads * c.head_dim,
                      F = c.ffn_dim;
         const size_t per_layer = qd * d + 2 * kvd * d + d * qd + 2 * F * d + d * F;
-        const size_t n16 = per_layer * c.n_layers + (size_t)c.vocab * d;
+        const size_t n16 = per_layer * c.n_layers;  // the LM head runs on the bf16 embedding (tensor cores)
         std::vector<mk_layer_weights> lw16(c.n_layers);
         mk_weights w16 = *w;
-        uint16_t *lm16 = nullptr;
         // the copy is exact for magnitudes in fp16's normal range; a weight
         // beyond fp16's largest finite value would become an infinity, so
         // such a model keeps sequence-by-sequence batches
@@ -824,7 +831,6 @@ int mk_create(const mk_config *config, const mk_weights *w, const mk_kv_cache *k
                 b.w_up = copy(a.w_up, F * d);
                 b.w_down = copy(a.w_down, d * F);
             }
-            lm16 = const_cast<uint16_t *>(static_cast<const uint16_t *>(copy(w->embed, (size_t)c.vocab * d)));
             if (e == cudaSuccess) e = cudaDeviceSynchronize();
             unsigned long long oor = 0;
             if (e == cudaSuccess) e = cudaMemcpy(&oor, d_oor, sizeof oor, cudaMemcpyDeviceToHost);
@@ -839,25 +845,50 @@ int mk_create(const mk_config *config, const mk_weights *w, const mk_kv_cache *k
             }
         }
         if (e == cudaSuccess) e = cudaMalloc(&h->bdev_mem, h->bim.total);
+        // the LM head's block: hi | lo | logits | draw scratch | status
+        const size_t B = c.max_batch, V = c.vocab;
+        const size_t o_lo = B * d * 2, o_lg = (2 * B * d * 2 + 255) & ~size_t(255),
+                     o_ls = (o_lg + B * V * 4 + 255) & ~size_t(255),
+                     o_er = o_ls + sizeof(unsigned long long) * mk_filter_lists_keys((int)B, (int)V);
+        if (e == cudaSuccess && (d % 64 || !mkpf::encode_weight_map(&h->emb_map, w->embed, (int)V, (int)d)))
+            e = cudaErrorInvalidValue;  // no tensor map of the embedding: no fused batches
+        if (e == cudaSuccess) e = cudaMalloc(&h->blm_mem, o_er + sizeof(int));
+        if (e == cudaSuccess) {
+            char *m = static_cast<char *>(h->blm_mem);
+            h->blm_hi = reinterpret_cast<uint16_t *>(m);
+            h->blm_lo = reinterpret_cast<uint16_t *>(m + o_lo);
+            h->bf_logits = reinterpret_cast<float *>(m + o_lg);
+            h->bf_lists = reinterpret_cast<unsigned long long *>(m + o_ls);
+            h->blm_err = reinterpret_cast<int *>(m + o_er);
+            e = cudaMemset(h->blm_err, 0, sizeof(int));
+        }
         if (e != cudaSuccess) {
             // no room for the batched step, or a weight beyond fp16's range:
             // batches run sequence by sequence
             cudaGetLastError();
             if (h->w16) cudaFree(h->w16);
+            if (h->bdev_mem) cudaFree(h->bdev_mem);
+            if (h->blm_mem) cudaFree(h->blm_mem);
             h->w16 = nullptr;
             h->bdev_mem = nullptr;
+            h->blm_mem = nullptr;
+            h->blm_hi = h->blm_lo = nullptr;
+            h->bf_logits = nullptr;
+            h->bf_lists = nullptr;
+            h->blm_err = nullptr;
         } else {
             char *bb = static_cast<char *>(h->bdev_mem);
-            rc = mkint::upload_image(h->bim, config, &w16, kv, bb, nullptr, lm16);
+            rc = mkint::upload_image(h->bim, config, &w16, kv, bb, nullptr, nullptr);
             if (rc) {
                 cudaFree(h->bdev_mem);
+                cudaFree(h->blm_mem);
                 cudaFree(h->w16);
                 cudaFree(h->dev_mem);
                 delete h;
                 return rc;
             }
             mkint::fill_params(h->bim, config, &w16, kv, bb, h->bbase);
-            h->bbase.lm_w = lm16;
+            h->bbase.lm_w = nullptr;  // no LM-head instructions in the batched plan
             h->bzero_bytes = h->bim.o_zero_end - h->bim.o_ctr;
             h->has_batch = true;
         }
@@ -896,40 +927,35 @@ int mk_decode_step_batch(mk_handle *h, const int32_t *d_tokens, const int32_t *d
     if (batch < 1 || batch > h->cfg.max_batch) return fail(MK_ERR_INVALID_ARG, "batch outside [1, max_batch]");
     const bool filtered = h->inv_temp > 0.f && (h->top_k > 0 || h->top_p < 1.f);
     if (h->has_batch && batch == h->cfg.max_batch) {
-        // all sequences in one launch: every weight tile read once for all of
-        // them. A filtered draw takes the launch's logits (the launch itself
-        // then picks greedily) and draws every sequence's token after it.
+        // All sequences in one launch through the last layer: every weight
+        // tile read once for all of them. Then the LM head as one tensor-core
+        // contraction over the bf16 embedding (final RMSNorm first, as hi /
+        // lo bf16 terms) and every sequence's token drawn from its logits.
         cudaError_t e = cudaSetDevice(h->device);
         if (e != cudaSuccess) return cuda_fail(e, "cudaSetDevice");
-        const int V = h->cfg.vocab;
-        float *logits = out_logits;
-        if (filtered && (!h->bf_lists || (!logits && !h->bf_logits))) {
-            if (!h->bf_lists) {
-                e = cudaMalloc(&h->bf_lists, sizeof(unsigned long long) * mk_filter_lists_keys(batch, V));
-                if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(filter lists)");
-            }
-            if (!logits && !h->bf_logits) {
-                e = cudaMalloc(&h->bf_logits, sizeof(float) * (size_t)batch * V);
-                if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(batch logits)");
-            }
-        }
-        if (filtered && !logits) logits = h->bf_logits;
+        const cudaStream_t s = (cudaStream_t)stream;
+        const int V = h->cfg.vocab, d = h->cfg.d_model;
+        float *logits = out_logits ? out_logits : h->bf_logits;
         mk::Params p = h->bbase;
         p.timeout_ns = h->timeout_ns;
         p.trace = h->trace_on ? h->d_trace : nullptr;
         p.trace_cap = h->trace_cap;
-        p.inv_temp = filtered ? 0.f : h->inv_temp;
-        p.seed_lo = (uint32_t)(h->seed & 0xFFFFFFFFu);
-        p.seed_hi = (uint32_t)(h->seed >> 32);
         if (h->trace_on) h->trace_batch = true;
-        const int rc = mkint::launch_step(p, h->bim.n_sm, h->bim.n_stages, 0, d_tokens, 0, logits, out_tokens,
-                                          (cudaStream_t)stream, false, d_positions, 0);
-        if (rc || !filtered) return rc;
+        const int rc = mkint::launch_step(p, h->bim.n_sm, h->bim.n_stages, 0, d_tokens, 0, nullptr, out_tokens, s,
+                                          false, d_positions, 0);
+        if (rc) return rc;
+        e = mk_batch_final_norm(reinterpret_cast<const float *>(h->bbase.xll), batch, d, h->bbase.final_norm,
+                                h->cfg.rms_eps, h->blm_hi, h->blm_lo, s);
+        if (e == cudaSuccess)
+            e = mkpf::gemm(h->emb_map, h->blm_hi, h->blm_lo, V, batch, d, logits, V, nullptr, nullptr, 0, h->blm_err,
+                           h->im.n_sm, s, mkpf::NormOut{});
+        if (e != cudaSuccess) return cuda_fail(e, "LM head of the batch");
         // a filter set with only top_p takes the nucleus among the kMaxTopK best
-        const int K = h->top_k > 0 ? h->top_k : mk::kMaxTopK;
-        e = mk_filtered_draw_batch(logits, batch, V, K, h->top_p, h->inv_temp, d_positions, 0, h->seed, h->bf_lists,
-                                   out_tokens, (cudaStream_t)stream);
-        if (e != cudaSuccess) return cuda_fail(e, "filtered draw of the batch");
+        e = filtered ? mk_filtered_draw_batch(logits, batch, V, h->top_k > 0 ? h->top_k : mk::kMaxTopK, h->top_p,
+                                              h->inv_temp, d_positions, 0, h->seed, h->bf_lists, out_tokens, s)
+                     : mk_sampled_draw_batch(logits, batch, V, h->inv_temp, d_positions, 0, h->seed, h->bf_lists,
+                                             out_tokens, s);
+        if (e != cudaSuccess) return cuda_fail(e, "draw of the batch");
         return MK_OK;
     }
     for (int32_t b = 0; b < batch; ++b) {
@@ -998,11 +1024,17 @@ int mk_get_status(mk_handle *h) {
     cudaError_t e = cudaSetDevice(h->device);
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
-    int32_t st = 0, bst = 0, pst = 0;
+    int32_t st = 0, bst = 0, pst = 0, lst = 0;
     e = cudaMemcpy(&st, h->base.status, sizeof st, cudaMemcpyDeviceToHost);
     if (e == cudaSuccess && h->has_batch) e = cudaMemcpy(&bst, h->bbase.status, sizeof bst, cudaMemcpyDeviceToHost);
     if (e == cudaSuccess && h->pf.err) e = cudaMemcpy(&pst, h->pf.err, sizeof pst, cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess && h->blm_err) e = cudaMemcpy(&lst, h->blm_err, sizeof lst, cudaMemcpyDeviceToHost);
     if (e != cudaSuccess) return cuda_fail(e, "status read");
+    if (lst != 0) {
+        e = cudaMemset(h->blm_err, 0, sizeof(int));
+        if (e != cudaSuccess) return cuda_fail(e, "status reset");
+        return fail(MK_ERR_TIMEOUT, "a bounded wait of the batched LM head expired");
+    }
     if (pst != 0) {
         e = cudaMemset(h->pf.err, 0, sizeof(int));
         if (e != cudaSuccess) return cuda_fail(e, "status reset");
@@ -1286,8 +1318,7 @@ void mk_destroy(mk_handle *h) {
     if (h->bdev_mem) cudaFree(h->bdev_mem);
     if (h->w16) cudaFree(h->w16);
     if (h->pf_mem) cudaFree(h->pf_mem);
-    if (h->bf_logits) cudaFree(h->bf_logits);
-    if (h->bf_lists) cudaFree(h->bf_lists);
+    if (h->blm_mem) cudaFree(h->blm_mem);  // holds bf_logits and bf_lists
     if (h->pd_logits) cudaFree(h->pd_logits);
     if (h->pd_lists) cudaFree(h->pd_lists);
     delete h;

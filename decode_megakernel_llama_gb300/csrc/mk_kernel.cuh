@@ -1517,7 +1517,6 @@ __device__ bool gemv_batch(const Params &p, const Ctx &cx, const Instr &in, uint
     switch (op) {
         case OP_QKV: gain = lw->attn_norm; src = xf; break;
         case OP_GATEUP: gain = lw->mlp_norm; src = xf; break;
-        case OP_LMHEAD: gain = p.final_norm; src = xf; break;
         case OP_OPROJ: src = reinterpret_cast<const float *>(p.attll) + (size_t)l * kMaxBatch * p.Hq * p.hd; break;
         default: src = hf; break;  // OP_DOWN
     }
@@ -1613,7 +1612,6 @@ __device__ bool gemv_batch(const Params &p, const Ctx &cx, const Instr &in, uint
     const uint4 *pages = reinterpret_cast<const uint4 *>(cx.pages);
     const int woff0 = trow0 * row_u4 + ks * 16 + tq, woff1 = trow1 * row_u4 + ks * 16 + tq;  // + 4 * c
     const bool tracing = p.trace != nullptr;
-    unsigned long long best = 0ull;  // LM head: this lane's best key of sequence lane & 7
     // Applies the op's transform to output row o (of the instruction) of
     // sequence b, accumulator row arow, and publishes it.
     auto publish = [&](int o, int b, int arow, float rs) {
@@ -1624,18 +1622,10 @@ __device__ bool gemv_batch(const Params &p, const Ctx &cx, const Instr &in, uint
         } else if (op == OP_OPROJ || op == OP_DOWN) {
             float *dst = xf + bofs(b, r0 + o);
             if (CHK(dst, 4, 15)) *dst = resid[b * n + o] + v;
-        } else if (gu) {
+        } else {  // gate/up
             const float up = acc[(arow + 1) * kMaxBatch + b] * rs;
             float *dst = hf + bofs(b, r0 + o);
             if (CHK(dst, 4, 16)) *dst = v / (1.0f + expf(-v)) * up;
-        } else {  // LM head
-            float *lg = p.out_logits ? p.out_logits + (size_t)b * p.V + r0 + o : nullptr;
-            if (lg && CHK(lg, 4, 18)) *lg = v;
-            const float z = p.inv_temp > 0.f ? v * p.inv_temp + gumbel_noise((uint32_t)(r0 + o), pos_of(p, b), slot_of(p, b),
-                                                                            p.seed_lo, p.seed_hi)
-                                             : v;
-            const unsigned long long key = argmax_key(z, (uint32_t)(r0 + o));
-            best = key > best ? key : best;
         }
     };
     int pg = (int)(t % kPages);
@@ -1727,65 +1717,14 @@ __device__ bool gemv_batch(const Params &p, const Ctx &cx, const Instr &in, uint
         if (b < nb)
             for (int i = tid >> 3; i < n; i += kConsumerThreads / kMaxBatch) publish(i, b, gu ? 2 * i : i, rs);
     }
-    // O-proj, gate/up and down release their completion counters (the
-    // attention of QKV's outputs and the LM head's argmax use their own
-    // protocols)
+    // O-proj, gate/up and down release their completion counters (QKV's
+    // outputs are tagged words that the attention waits on)
     if (op == OP_OPROJ || op == OP_GATEUP || op == OP_DOWN) {
         bad = consumer_sync_any(bad);
         if (bad) return true;
         if (tid == 0) ctr_signal(p, in.sig_ctr, in.sig_n);
     }
     phase_stamp(p, cx, 1);
-    if (op != OP_LMHEAD) return false;
-    // ---- LM head: per-sequence block argmax, then the last block reduces them
-    bad = consumer_sync_any(bad);
-    if (bad) return true;
-#pragma unroll
-    for (int o = 8; o < 32; o <<= 1) {  // lanes with the same sequence (lane & 7)
-        const unsigned long long other = __shfl_xor_sync(0xFFFFFFFFu, best, o);
-        best = other > best ? other : best;
-    }
-    unsigned long long *bw = reinterpret_cast<unsigned long long *>(cx.xbuf);  // [8 warps][kMaxBatch]
-    if (lane < kMaxBatch) bw[warp * kMaxBatch + lane] = best;
-    consumer_sync();
-    if (tid < nb) {
-        unsigned long long bb = 0ull;
-        for (int w = 0; w < kConsumerWarps; ++w) bb = bw[w * kMaxBatch + tid] > bb ? bw[w * kMaxBatch + tid] : bb;
-        if (CHK(p.lm_part + (size_t)tid * p.n_lm + in.slot, 8, 19)) p.lm_part[(size_t)tid * p.n_lm + in.slot] = bb;
-    }
-    consumer_sync();
-    if (tid == 0) {
-        __threadfence();
-        const uint32_t old = CHK(p.ctr + p.cl.lm_arrive, 4, 31) ? atom_acq_rel_add(p.ctr + p.cl.lm_arrive, 1u) : 0u;
-        const bool last = old == (uint32_t)p.n_lm - 1u;
-        if (last) __threadfence();
-        cx.misc->flag = last ? 1 : 0;
-    }
-    consumer_sync();
-    if (cx.misc->flag) {
-        for (int b = 0; b < nb; ++b) {
-            unsigned long long g2 = 0ull;
-            for (int s2 = tid; s2 < p.n_lm; s2 += kConsumerThreads) {
-                const unsigned long long v = CHK(p.lm_part + (size_t)b * p.n_lm + s2, 8, 20)
-                                                 ? __ldcg(p.lm_part + (size_t)b * p.n_lm + s2) : 0ull;
-                g2 = v > g2 ? v : g2;
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                const unsigned long long other = __shfl_xor_sync(0xFFFFFFFFu, g2, o);
-                g2 = other > g2 ? other : g2;
-            }
-            if (lane == 0) cx.misc->best8[warp] = g2;
-            consumer_sync();
-            if (tid == 0) {
-                unsigned long long bb = 0ull;
-                for (int w = 0; w < kConsumerWarps; ++w) bb = cx.misc->best8[w] > bb ? cx.misc->best8[w] : bb;
-                if (CHK(p.out_token + b, 4, 21))
-                    p.out_token[b] = (int32_t)(0xFFFFFFFFu - (uint32_t)(bb & 0xFFFFFFFFull));
-            }
-            consumer_sync();
-        }
-    }
     return false;
 }
 

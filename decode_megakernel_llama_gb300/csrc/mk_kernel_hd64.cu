@@ -95,6 +95,8 @@ __global__ void __launch_bounds__(mk::kConsumerThreads) filter_draw(const unsign
     if (threadIdx.x == 0) out_tokens[b] = tok;
 }
 
+// inv_temp > 0: the key of logit * inv_temp + noise; otherwise of the logit
+// itself (the greedy choice, lowest index on ties).
 __global__ void __launch_bounds__(256) sample_slices(const float *logits, int V, float inv_temp,
                                                      const int32_t *positions, int pos0, uint32_t seed_lo,
                                                      uint32_t seed_hi, unsigned long long *keys) {
@@ -106,8 +108,9 @@ __global__ void __launch_bounds__(256) sample_slices(const float *logits, int V,
     for (int i = threadIdx.x; i < kFilterSlice; i += blockDim.x) {
         const int e = base + i;
         if (e < V) {
-            const unsigned long long k =
-                mk::argmax_key(lg[e] * inv_temp + mk::gumbel_noise((uint32_t)e, pos, b, seed_lo, seed_hi), (uint32_t)e);
+            const float z = inv_temp > 0.f ? lg[e] * inv_temp + mk::gumbel_noise((uint32_t)e, pos, b, seed_lo, seed_hi)
+                                           : lg[e];
+            const unsigned long long k = mk::argmax_key(z, (uint32_t)e);
             best = k > best ? k : best;
         }
     }
@@ -117,6 +120,34 @@ __global__ void __launch_bounds__(256) sample_slices(const float *logits, int V,
     if (threadIdx.x == 0) {
         for (int w = 0; w < 8; ++w) best = best8[w] > best ? best8[w] : best;
         keys[(size_t)b * gridDim.x + j] = best;
+    }
+}
+
+// The final RMSNorm of a batched step's residual stream (x of sequence b at
+// bofs(b, e), fp32) with gains g, as the hi / lo bf16 terms [b][d] of the
+// LM head's input: a CTA per sequence.
+__global__ void __launch_bounds__(256) batch_final_norm(const float *x, int d, const uint16_t *g, float eps,
+                                                        uint16_t *hi, uint16_t *lo) {
+    __shared__ float red[8];
+    const int b = blockIdx.x;
+    float ss = 0.f;
+    for (int e = threadIdx.x; e < d; e += blockDim.x) {
+        const float v = x[mk::bofs(b, e)];
+        ss = fmaf(v, v, ss);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+    __syncthreads();
+    ss = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) ss += red[w];
+    const float r = 1.0f / sqrtf(ss / (float)d + eps);
+    for (int e = threadIdx.x; e < d; e += blockDim.x) {
+        const float v = x[mk::bofs(b, e)] * (r * mk::bf16f(g[e]));
+        const uint16_t h = mk::f2bf(v);
+        hi[(size_t)b * d + e] = h;
+        lo[(size_t)b * d + e] = mk::f2bf(v - mk::bf16f(h));
     }
 }
 
@@ -153,15 +184,24 @@ extern "C" cudaError_t mk_filtered_draw_batch(const float *logits, int B, int V,
     return cudaGetLastError();
 }
 
-// The plain draw (temperature, no filter) of B sequences from their logits;
-// keys: B * ceil(V / 1024) slots of scratch.
+// The plain draw (temperature, no filter; inv_temp = 0: the greedy choice)
+// of B sequences from their logits; keys: B * ceil(V / 1024) slots of scratch.
 extern "C" cudaError_t mk_sampled_draw_batch(const float *logits, int B, int V, float inv_temp,
                                              const int32_t *positions, int pos0, uint64_t seed,
                                              unsigned long long *keys, int32_t *out_tokens, cudaStream_t stream) {
-    if (B < 1 || V < 1 || !(inv_temp > 0.f)) return cudaErrorInvalidValue;
+    if (B < 1 || V < 1 || !(inv_temp >= 0.f)) return cudaErrorInvalidValue;
     const int ns = (V + kFilterSlice - 1) / kFilterSlice;
     sample_slices<<<dim3(ns, B), 256, 0, stream>>>(logits, V, inv_temp, positions, pos0, (uint32_t)(seed & 0xFFFFFFFFu),
                                                    (uint32_t)(seed >> 32), keys);
     sample_reduce<<<B, 32, 0, stream>>>(keys, ns, out_tokens);
+    return cudaGetLastError();
+}
+
+// The final RMSNorm of a batched step's B sequences into the LM head's hi /
+// lo bf16 input [B][d].
+extern "C" cudaError_t mk_batch_final_norm(const float *x, int B, int d, const uint16_t *gain, float eps, uint16_t *hi,
+                                           uint16_t *lo, cudaStream_t stream) {
+    if (B < 1 || B > mk::kMaxBatch || d < 1) return cudaErrorInvalidValue;
+    batch_final_norm<<<B, 256, 0, stream>>>(x, d, gain, eps, hi, lo);
     return cudaGetLastError();
 }

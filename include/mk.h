@@ -95,11 +95,13 @@ typedef struct mk_handle mk_handle;
 /* Plans the per-SM instruction queues for this model on the current device
  * (host scheduler), allocates the library's scratch (activations, attention
  * partials, dependency counters, queues, RoPE table) and uploads them.
- * With max_batch > 1 and head_dim 64 it also plans the fused batched step
- * and keeps, for it, an fp16 copy of every GEMV weight and of the LM head
- * (2 bytes per weight, owned by the handle; exact for magnitudes in fp16's
- * normal range); if that does not fit, or a weight lies beyond fp16's
- * largest finite value (65504), batches run sequence by sequence instead. Synchronous. On success *out receives
+ * With max_batch > 1, head_dim 64 and d_model a multiple of 64 it also plans
+ * the fused batched step and keeps, for it, an fp16 copy of every layer
+ * GEMV weight (2 bytes per weight, owned by the handle; exact for
+ * magnitudes in fp16's normal range) and the LM head's scratch (its logits
+ * and draw lists for max_batch sequences); if that does not fit, or a
+ * weight lies beyond fp16's largest finite value (65504), batches run
+ * sequence by sequence instead. Synchronous. On success *out receives
  * the handle.
  * Source: the article "Revolution der KI-Beschleunigung: Wie ein Low-Latency
  * Megakernel den Llama-1B Turbo zündet" (dasgeld.co), paragraph on the
@@ -149,9 +151,14 @@ int mk_decode_step_host(mk_handle *h, const int32_t *host_token, int32_t positio
  * int32[batch]) and, if out_logits is not NULL, its logits to
  * out_logits[b*vocab .. ] (device float[batch][vocab]).
  * With batch == max_batch and the fused batched step planned (see
- * mk_create), all sequences run in ONE launch that reads every weight tile
- * once for all of them; its GEMVs take fp16 inputs, so its logits agree with
- * the single-sequence step to the parity tolerance, not bit for bit.
+ * mk_create), all sequences run through the last layer in ONE launch that
+ * reads every layer's weight tile once for all of them; then three kernels
+ * on the same stream form the final RMSNorm, the LM head (one tensor-core
+ * contraction over the bf16 embedding for all sequences) and the draw. The
+ * layer GEMVs take fp16 inputs, so the logits agree with the
+ * single-sequence step to the parity tolerance, not bit for bit; a bounded
+ * wait of the LM head that expired is reported by mk_get_status
+ * (MK_ERR_TIMEOUT).
  * Otherwise the sequences run one fused step after another on `stream` (one
  * launch each, in batch order). A device token or position out of range is
  * reported by mk_get_status (MK_ERR_INVALID_ARG) and the step does nothing

@@ -145,9 +145,9 @@ def test_llama1b_batch8_short_lockstep(cuda_dev):
     bp.close()
 
 
-def test_wide_vocab_batch2_lm_head_ring(cuda_dev):
-    # more LM-head rows per SM than the shared accumulators hold for all
-    # sequences: the LM head runs through its ring of accumulator slots
+def test_wide_vocab_batch2(cuda_dev):
+    # a 160000-row vocabulary: 1250 row tiles of the LM head's tensor-core
+    # contraction, and 157 slices per sequence for the token draw
     wide = ModelShape("wide-vocab", 2, 256, 4, 2, 64, 1024, 160000, 1e-5, 1e4)
     bp = BatchPair(wide, 8, 2)
     prompts = [synth.prompt_tokens(wide.vocab, 3, seq=b) for b in range(2)]
