@@ -831,35 +831,65 @@ __device__ __forceinline__ bool stage_units(const Params &p, const Ctx &cx, cons
     }
 }
 
-// Two rows at once: both rows' weights are loaded before any FMA so the two
-// dependent chains overlap. Element e of chunk c of this lane is input index
-// (c*32 + lane)*8 + e of the warp's K-slice; each 32-bit weight word holds
-// elements (2k, 2k+1), multiplied as a pair with one packed fp32 FMA.
+// Packs two floats as bf16x2, round to nearest even: lo goes to the low half.
+__device__ __forceinline__ uint32_t pack_bf2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Dot products of two weight rows with the staged input over the warp's
+// K-slice (NX*32 columns) on the tensor cores: mma.sync m16n8k16, bf16 in,
+// fp32 accumulate. Per 128-column block, A row m < 8 holds the row's
+// 16-byte chunks m (k 0-7) and 8+m (k 8-15) and A row 8+m the same chunks
+// of the second row (one ldmatrix.x4 over four contiguous 128-byte spans,
+// no bank conflicts); B column n holds the inputs of chunks n and 8+n, so
+// the diagonal D[m][m] (D[8+m][m]) is chunk pair m's share of the first
+// (second) row's dot product, and accumulating over the blocks sums them.
+// The input enters as hi and lo bf16 terms (x = hi + lo to 2^-16
+// relative): xb holds, per block, this lane's hi pairs at columns 2*lane
+// and 64+2*lane, then its lo pairs. wa / wb: the rows at the warp's
+// K-slice. On return ra / rb hold the diagonal elements this lane owns (0
+// in the other lanes): their warp sums are the two dot products.
 template <int NX>
-__device__ __forceinline__ void dot_rows2(const uint4 *wa, const uint4 *wb, const float *xr,
+__device__ __forceinline__ void dot_rows2(const uint4 *wa, const uint4 *wb, const uint32_t (&xb)[NX],
                                           float &ra, float &rb) {
-    uint4 va[NX / 8], vb[NX / 8];
+    const int lane = threadIdx.x & 31;
+    const uint4 *src = ((lane & 8) ? wb : wa) + ((lane & 16) ? 8 : 0) + (lane & 7);
+    const uint32_t s0 = smem_u32(src);
+    float d[4][4];
 #pragma unroll
-    for (int c = 0; c < NX / 8; ++c) {
-        va[c] = wa[c * 32];
-        vb[c] = wb[c * 32];
+    for (int c = 0; c < 4; ++c) d[c][0] = d[c][1] = d[c][2] = d[c][3] = 0.f;
+#pragma unroll
+    for (int b = 0; b < NX / 4; ++b) {
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4(s0 + 256u * b, a0, a1, a2, a3);
+        mma_bf16_16816(d[(b & 1) * 2], a0, a1, a2, a3, xb[4 * b], xb[4 * b + 1]);
+        mma_bf16_16816(d[(b & 1) * 2 + 1], a0, a1, a2, a3, xb[4 * b + 2], xb[4 * b + 3]);
     }
-    float2 a[4], b[4];
+    float s[4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) a[k] = b[k] = make_float2(0.f, 0.f);
-#pragma unroll
-    for (int c = 0; c < NX / 8; ++c) {
-        const uint32_t ua[4] = {va[c].x, va[c].y, va[c].z, va[c].w};
-        const uint32_t ub[4] = {vb[c].x, vb[c].y, vb[c].z, vb[c].w};
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const float2 x2 = make_float2(xr[c * 8 + 2 * k], xr[c * 8 + 2 * k + 1]);
-            a[k] = __ffma2_rn(make_float2(bf_lo(ua[k]), bf_hi(ua[k])), x2, a[k]);
-            b[k] = __ffma2_rn(make_float2(bf_lo(ub[k]), bf_hi(ub[k])), x2, b[k]);
-        }
-    }
-    ra = ((a[0].x + a[0].y) + (a[1].x + a[1].y)) + ((a[2].x + a[2].y) + (a[3].x + a[3].y));
-    rb = ((b[0].x + b[0].y) + (b[1].x + b[1].y)) + ((b[2].x + b[2].y) + (b[3].x + b[3].y));
+    for (int i = 0; i < 4; ++i) s[i] = (d[0][i] + d[1][i]) + (d[2][i] + d[3][i]);
+    const int g = lane >> 2, t = lane & 3;
+    const bool diag = t == (g >> 1), odd = (g & 1) != 0;
+    ra = diag ? (odd ? s[1] : s[0]) : 0.f;
+    rb = diag ? (odd ? s[3] : s[2]) : 0.f;
 }
 
 // Warp sums of two values at once: after the call lanes 0-15 hold the sum of
@@ -964,8 +994,8 @@ __device__ void gemv_instr(const Params &p, const Ctx &cx, const Instr &in, cons
                          CHK(p.xll + r0 + tid, 8, 13);
     uint2 rword = make_uint2(0u, 0u);
     if (resid_x) rword = ll_ld8(p.xll + r0 + tid);
-    // this lane's input slice
-    float xr[NX];
+    // this lane's input slice as hi / lo bf16 pairs (see dot_rows2)
+    uint32_t xb[NX];
     float *red = in.op == OP_DOWN ? cx.dred : cx.red;
     const int sbase = ks * g.kslice;
     {
@@ -997,21 +1027,20 @@ __device__ void gemv_instr(const Params &p, const Ctx &cx, const Instr &in, cons
         const float rstd = gain ? 1.0f / sqrtf(ss / (float)g.K + p.eps) : 1.0f;
         const uint16_t *gbuf = reinterpret_cast<const uint16_t *>(cx.xbuf + kMaxStaged);
 #pragma unroll
-        for (int c = 0; c < NX / 8; ++c) {
-            const int idx = sbase + (c * 32 + lane) * 8;
-            const float4 u = *reinterpret_cast<const float4 *>(cx.xbuf + idx);
-            const float4 v = *reinterpret_cast<const float4 *>(cx.xbuf + idx + 4);
-            float *x = xr + c * 8;
-            x[0] = u.x; x[1] = u.y; x[2] = u.z; x[3] = u.w;
-            x[4] = v.x; x[5] = v.y; x[6] = v.z; x[7] = v.w;
-            if (gain) {
-                const uint4 gb = *reinterpret_cast<const uint4 *>(gbuf + idx);
-                x[0] *= rstd * bf_lo(gb.x); x[1] *= rstd * bf_hi(gb.x);
-                x[2] *= rstd * bf_lo(gb.y); x[3] *= rstd * bf_hi(gb.y);
-                x[4] *= rstd * bf_lo(gb.z); x[5] *= rstd * bf_hi(gb.z);
-                x[6] *= rstd * bf_lo(gb.w); x[7] *= rstd * bf_hi(gb.w);
+        for (int b = 0; b < NX / 4; ++b)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int idx = sbase + 128 * b + 64 * h + 2 * lane;
+                float2 v = *reinterpret_cast<const float2 *>(cx.xbuf + idx);
+                if (gain) {
+                    const uint32_t gb = *reinterpret_cast<const uint32_t *>(gbuf + idx);
+                    v.x *= rstd * bf_lo(gb);
+                    v.y *= rstd * bf_hi(gb);
+                }
+                const uint32_t hi = pack_bf2(v.x, v.y);
+                xb[4 * b + h] = hi;
+                xb[4 * b + 2 + h] = pack_bf2(v.x - bf_lo(hi), v.y - bf_hi(hi));
             }
-        }
     }
     phase_stamp(p, cx, 0);
     // Tiles. Warp (rg, ks) owns rows rg*M .. rg*M+M-1 of every tile (M = 64/NX
@@ -1025,7 +1054,7 @@ __device__ void gemv_instr(const Params &p, const Ctx &cx, const Instr &in, cons
     const int row_u4 = g.K / 8;  // 16-byte chunks per row
     const bool tracing = p.trace != nullptr;
     const uint4 *pages = reinterpret_cast<const uint4 *>(cx.pages);
-    const int woff = rg * M * row_u4 + sbase / 8 + lane;
+    const int woff = rg * M * row_u4 + sbase / 8;  // the warp's first row at its K-slice
     const bool second = (lane & 16) != 0;  // lanes 16-31 hold the second row's sum
     // row r of a tile is output row j*per + roff[r] (+ n for the up half of a gate/up tile)
     int roff[M], obase[M];
@@ -1052,9 +1081,9 @@ __device__ void gemv_instr(const Params &p, const Ctx &cx, const Instr &in, cons
                 const uint4 *wa = page + q * row_u4;
                 const uint4 *wb = v1 ? wa + row_u4 : wa;  // an invalid second row re-reads the first
                 float ra = 0.f, rb = 0.f;
-                if (CHKS(wa, 16, 44) && CHKS(wa + (NX / 8 - 1) * 32, 16, 45) && CHKS(wb, 16, 44) &&
-                    CHKS(wb + (NX / 8 - 1) * 32, 16, 45))
-                    dot_rows2<NX>(wa, wb, xr, ra, rb);
+                if (CHKS(wa, 16, 44) && CHKS(wa + 4 * NX - 1, 16, 45) && CHKS(wb, 16, 44) &&
+                    CHKS(wb + 4 * NX - 1, 16, 45))
+                    dot_rows2<NX>(wa, wb, xb, ra, rb);
                 // with one row pair per warp the page is free once the weights are in registers
                 if (M == 2) {
                     __syncwarp();
