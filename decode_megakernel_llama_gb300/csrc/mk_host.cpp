@@ -30,7 +30,7 @@ extern "C" cudaError_t mk_convert_bf16_f16(const void *src, void *dst, size_t n,
                                            cudaStream_t stream);
 extern "C" size_t mk_filter_lists_keys(int B, int V);
 extern "C" cudaError_t mk_filtered_draw_batch(const float *logits, int B, int V, int K, float top_p, float inv_temp,
-                                              const int32_t *positions, int pos0, uint64_t seed,
+                                              const int32_t *positions, int pos0, int slot0, uint64_t seed,
                                               unsigned long long *lists, int32_t *out_tokens, cudaStream_t stream);
 extern "C" cudaError_t mk_sampled_draw_batch(const float *logits, int B, int V, float inv_temp,
                                              const int32_t *positions, int pos0, uint64_t seed,
@@ -709,6 +709,10 @@ struct mk_handle {
 
 namespace {
 
+// The last LM-head block gathers and sorts up to n_lm * kMaxTopK candidate
+// keys in its page ring, padded to a power of two: at most 16384 (128 KB).
+bool filter_in_kernel(const mk_handle *h) { return h->base.n_lm * mk::kMaxTopK <= 16384; }
+
 int launch(mk_handle *h, int32_t token, const int32_t *d_token, int32_t position, float *out_logits,
            int32_t *out_token, cudaStream_t stream, bool unfused, const int32_t *d_pos = nullptr,
            int32_t bslot = 0) {
@@ -728,11 +732,29 @@ int launch(mk_handle *h, int32_t token, const int32_t *d_token, int32_t position
     p.seed_lo = (uint32_t)(h->seed & 0xFFFFFFFFu);
     p.seed_hi = (uint32_t)(h->seed >> 32);
     // a filter set with only top_p takes the nucleus among the kMaxTopK best
-    p.top_k = h->inv_temp > 0.f && (h->top_k > 0 || h->top_p < 1.f) ? (h->top_k > 0 ? h->top_k : mk::kMaxTopK) : 0;
+    const bool filtered = h->inv_temp > 0.f && (h->top_k > 0 || h->top_p < 1.f);
+    const int K = h->top_k > 0 ? h->top_k : mk::kMaxTopK;
+    p.top_k = filtered ? K : 0;
     p.top_p = h->top_p;
+    // More LM-head blocks than the last block can sort the candidates of:
+    // the launch picks greedily and writes the logits, and the filter
+    // kernels of the batched step draw the token after it (same noise:
+    // this step's position and slot).
+    const bool after = filtered && !filter_in_kernel(h);
+    float *logits = out_logits;
+    if (after) {
+        p.top_k = 0;
+        p.inv_temp = 0.f;
+        if (!logits) logits = h->d_logits;
+    }
     if (h->trace_on) h->trace_batch = false;
-    return mkint::launch_step(p, h->im.n_sm, h->im.n_stages, token, d_token, position, out_logits,
-                              out_token, stream, unfused, d_pos, bslot);
+    const int rc = mkint::launch_step(p, h->im.n_sm, h->im.n_stages, token, d_token, position, logits, out_token,
+                                      stream, unfused, d_pos, bslot);
+    if (rc || !after) return rc;
+    e = mk_filtered_draw_batch(logits, 1, h->cfg.vocab, K, h->top_p, h->inv_temp, d_pos, d_pos ? 0 : position, bslot,
+                               h->seed, h->pd_lists, out_token, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "filtered draw");
+    return MK_OK;
 }
 
 }  // namespace
@@ -952,7 +974,7 @@ int mk_decode_step_batch(mk_handle *h, const int32_t *d_tokens, const int32_t *d
         if (e != cudaSuccess) return cuda_fail(e, "LM head of the batch");
         // a filter set with only top_p takes the nucleus among the kMaxTopK best
         e = filtered ? mk_filtered_draw_batch(logits, batch, V, h->top_k > 0 ? h->top_k : mk::kMaxTopK, h->top_p,
-                                              h->inv_temp, d_positions, 0, h->seed, h->bf_lists, out_tokens, s)
+                                              h->inv_temp, d_positions, 0, 0, h->seed, h->bf_lists, out_tokens, s)
                      : mk_sampled_draw_batch(logits, batch, V, h->inv_temp, d_positions, 0, h->seed, h->bf_lists,
                                              out_tokens, s);
         if (e != cudaSuccess) return cuda_fail(e, "draw of the batch");
@@ -1155,7 +1177,7 @@ int mk_prefill(mk_handle *h, const int32_t *d_tokens, int32_t n, int32_t start_p
         const int pos = start_pos + n - 1;
         if (h->top_k > 0 || h->top_p < 1.f)
             e = mk_filtered_draw_batch(logits, 1, h->cfg.vocab, h->top_k > 0 ? h->top_k : mk::kMaxTopK, h->top_p,
-                                       h->inv_temp, nullptr, pos, h->seed, h->pd_lists, out_token,
+                                       h->inv_temp, nullptr, pos, 0, h->seed, h->pd_lists, out_token,
                                        (cudaStream_t)stream);
         else
             e = mk_sampled_draw_batch(logits, 1, h->cfg.vocab, h->inv_temp, nullptr, pos, h->seed, h->pd_lists,
@@ -1185,10 +1207,15 @@ int mk_set_sampling_filter(mk_handle *h, int32_t top_k, float top_p) {
     if (!h) return fail(MK_ERR_INVALID_ARG, "handle is NULL");
     if (top_k < 0 || top_k > mk::kMaxTopK) return fail(MK_ERR_INVALID_ARG, "top_k outside [0, 64]");
     if (!(top_p > 0.f && top_p <= 1.f)) return fail(MK_ERR_INVALID_ARG, "top_p outside (0, 1]");
-    // the last LM-head block gathers and sorts up to n_lm * kMaxTopK keys in
-    // its page ring, padded to a power of two: at most 16384 keys (128 KB)
-    if ((top_k > 0 || top_p < 1.f) && h->base.n_lm * mk::kMaxTopK > 16384)
-        return fail(MK_ERR_UNSUPPORTED, "too many LM-head blocks for the filtered draw");
+    // a model whose candidates do not fit the in-kernel sort draws with the
+    // filter kernels after the launch: their candidate lists are made here
+    if ((top_k > 0 || top_p < 1.f) && !filter_in_kernel(h) && !h->pd_lists) {
+        const cudaError_t e = cudaMalloc(&h->pd_lists, sizeof(unsigned long long) * mk_filter_lists_keys(1, h->cfg.vocab));
+        if (e != cudaSuccess) {
+            h->pd_lists = nullptr;
+            return cuda_fail(e, "cudaMalloc(filter lists)");
+        }
+    }
     h->top_k = top_k;
     h->top_p = top_p;
     return MK_OK;
@@ -1231,7 +1258,7 @@ int mk_draw_from_logits(const float *d_logits, int32_t batch, int32_t vocab, flo
     const cudaError_t e =
         top_k > 0 || top_p < 1.f
             ? mk_filtered_draw_batch(d_logits, batch, vocab, top_k > 0 ? top_k : mk::kMaxTopK, top_p, inv_temp,
-                                     d_positions, 0, seed, work, d_out_tokens, (cudaStream_t)stream)
+                                     d_positions, 0, 0, seed, work, d_out_tokens, (cudaStream_t)stream)
             : mk_sampled_draw_batch(d_logits, batch, vocab, inv_temp, d_positions, 0, seed, work, d_out_tokens,
                                     (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "draw kernels");

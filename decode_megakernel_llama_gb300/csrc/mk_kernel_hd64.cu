@@ -83,15 +83,15 @@ __global__ void __launch_bounds__(mk::kConsumerThreads) filter_lists(const float
 
 __global__ void __launch_bounds__(mk::kConsumerThreads) filter_draw(const unsigned long long *lists, int nl, int K,
                                                                     float top_p, float inv_temp,
-                                                                    const int32_t *positions, int pos0,
+                                                                    const int32_t *positions, int pos0, int slot0,
                                                                     uint32_t seed_lo, uint32_t seed_hi,
                                                                     int32_t *out_tokens) {
     extern __shared__ unsigned long long g[];  // max(nl * K, 64) keys
     __shared__ int gcount;
     const int b = blockIdx.x;
     const int pos = positions ? positions[b] : pos0;
-    const int tok = mk::draw_filtered(lists + (size_t)b * nl * mk::kMaxTopK, nl, K, top_p, inv_temp, pos, b,
-                                      seed_lo, seed_hi, g, &gcount);
+    const int tok = mk::draw_filtered(lists + (size_t)b * nl * mk::kMaxTopK, nl, K, top_p, inv_temp, pos,
+                                      slot0 + b, seed_lo, seed_hi, g, &gcount);
     if (threadIdx.x == 0) out_tokens[b] = tok;
 }
 
@@ -166,7 +166,7 @@ extern "C" size_t mk_filter_lists_keys(int B, int V) {
 }
 
 extern "C" cudaError_t mk_filtered_draw_batch(const float *logits, int B, int V, int K, float top_p, float inv_temp,
-                                              const int32_t *positions, int pos0, uint64_t seed,
+                                              const int32_t *positions, int pos0, int slot0, uint64_t seed,
                                               unsigned long long *lists, int32_t *out_tokens, cudaStream_t stream) {
     if (B < 1 || V < 1 || K < 1 || K > mk::kMaxTopK) return cudaErrorInvalidValue;
     const int nl = (V + kFilterSlice - 1) / kFilterSlice;
@@ -178,7 +178,7 @@ extern "C" cudaError_t mk_filtered_draw_batch(const float *logits, int B, int V,
         configured = smem;
     }
     filter_lists<<<dim3(nl, B), mk::kConsumerThreads, 0, stream>>>(logits, V, K, lists);
-    filter_draw<<<B, mk::kConsumerThreads, smem, stream>>>(lists, nl, K, top_p, inv_temp, positions, pos0,
+    filter_draw<<<B, mk::kConsumerThreads, smem, stream>>>(lists, nl, K, top_p, inv_temp, positions, pos0, slot0,
                                                            (uint32_t)(seed & 0xFFFFFFFFu), (uint32_t)(seed >> 32),
                                                            out_tokens);
     return cudaGetLastError();

@@ -290,12 +290,17 @@ int mk_set_sampling(mk_handle *h, float temperature, uint64_t seed);
  *      with the Gumbel noise g of mk_set_sampling.
  * top_k = 0 and top_p = 1 (the default) switch filtering off. The sums run
  * in fp32. With a filter on, a fused batched step (mk_decode_step_batch)
- * writes every sequence's logits (to an internal buffer if out_logits is
- * NULL) and two short kernels after it draw each sequence's token; smaller
- * batches run sequence by sequence as without a filter. MK_ERR_INVALID_ARG
- * for top_k outside [0, MK_MAX_TOP_K] or
- * top_p outside (0, 1]; MK_ERR_UNSUPPORTED if the model's LM head has more
- * than 256 blocks. Host-only setting, takes effect on the next step.
+ * draws every sequence's token with two short kernels after its LM head;
+ * smaller batches run sequence by sequence as without a filter. A
+ * single-sequence step draws in its LM-head epilogue, unless the model's LM
+ * head has more than 256 blocks (the plan splits the vocabulary into more
+ * instructions than the last block can sort the candidates of, e.g. a
+ * 3B-class d_model of 3072): then the step writes its logits (to an
+ * internal buffer if out_logits is NULL) and the same two kernels draw its
+ * token, with the same noise. The candidate lists of that case are
+ * allocated here (MK_ERR_NOMEM or MK_ERR_CUDA if that fails). MK_ERR_INVALID_ARG for top_k
+ * outside [0, MK_MAX_TOP_K] or top_p outside (0, 1]. Host-only setting,
+ * takes effect on the next step.
  * Source: the glossary entry "Megakernel" (synthszr.com), section on
  * megakernels in chatbots; the pages define no sampler, so the filter
  * follows the nucleus sampling of Holtzman, Buys, Du, Forbes, Choi (ICLR

@@ -13,7 +13,7 @@ import oracle
 from oracle import sampling
 from decode_megakernel_llama_gb300 import _lib, synth
 from decode_megakernel_llama_gb300.build import build
-from decode_megakernel_llama_gb300.configs import LLAMA_1B, TINY
+from decode_megakernel_llama_gb300.configs import LLAMA_1B, TINY, ModelShape
 
 from gpu_helpers import MAX_ABS, Pair, compare, oracle_config
 
@@ -319,4 +319,40 @@ def test_filter_arguments_are_checked(cuda_dev):
         with pytest.raises(_lib.MKError) as e:
             pair.mk.set_sampling_filter(k, p)
         assert e.value.code == _lib.MK_ERR_INVALID_ARG
+    pair.close()
+
+
+# 320,000 rows over 152 SMs at d_model 256: two LM-head instructions per SM
+# (2,048 rows each at most), 304 blocks, more candidates than the last block
+# sorts: the step picks greedily, writes its logits and the filter kernels
+# draw after the launch.
+WIDE = ModelShape("wide-vocab-320k", 2, 256, 4, 2, 64, 1024, 320000, 1e-5, 1e4)
+
+
+@pytest.mark.parametrize("mode", ["mega", "unfused"])
+def test_filtered_draw_after_the_launch_matches_the_oracle(cuda_dev, mode):
+    instr, _, _ = _lib.plan_inspect(WIDE, torch.cuda.get_device_properties(0).multi_processor_count, 16)
+    assert int((instr[:, 0] == 6).sum()) * 64 > 16384
+    T = 0.8
+    pair = Pair(WIDE, 16)
+    pair.mk.set_sampling(T, SEED)
+    prompt = [int(t) for t in synth.prompt_tokens(WIDE.vocab, 3)]
+    tok = prompt[0]
+    for pos, (k, p) in enumerate([(50, 0.9), (0, 0.3), (1, 1.0), (64, 0.99), (5, 1.0)]):
+        pair.mk.set_sampling_filter(k, p)
+        gl, gt = pair.gpu_step(tok, pos, mode)
+        ol, ot = pair.orc.decode_step(tok, pos)
+        compare(gl, int(np.argmax(gl)), ol, ot, f"pos {pos}")
+        check_filtered(gl, gt, T, k, p, pos, 0, f"{mode} k {k} p {p} pos {pos}")
+        if k == 1:
+            assert gt == int(np.argmax(gl))
+        tok = prompt[pos + 1] if pos + 1 < len(prompt) else gt
+    # no logits asked for: the step keeps them in its own buffer
+    pair.mk.set_sampling_filter(40, 0.9)
+    out = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pair.mk.step(tok, 5, out)
+    gl, _ = pair.gpu_step(tok, 5, mode)  # the same position again: the same logits and noise
+    torch.cuda.synchronize()
+    assert pair.mk.status() == 0
+    check_filtered(gl, int(out.item()), T, 40, 0.9, 5, 0, "no logits")
     pair.close()

@@ -394,3 +394,14 @@ def test_batched_plan_falls_back_where_unsupported():
         assert not any(int(r[F_MAT]) > 0 for r in instr if r[F_OP] == OP_ATTN)
         single, _, _ = _lib.plan_inspect(shape, n_sm, 64)
         assert np.array_equal(instr, single)
+
+
+def test_lm_head_blocks_and_the_filtered_draw_path():
+    # The last LM-head block sorts up to 16384 candidate keys (64 per block):
+    # Llama-1B's 152 blocks draw in the epilogue; the 3B-class d_model 3072
+    # splits each SM's 844 rows in two (512 rows per block at most), 304
+    # blocks, so its filtered draw runs after the launch.
+    for shape, inside in ((LLAMA_1B, True), (LLAMA_3B, False)):
+        instr, _, _ = _lib.plan_inspect(shape, 152, 64)
+        n_lm = int((instr[:, F_OP] == OP_LMHEAD).sum())
+        assert (n_lm * 64 <= 16384) == inside, (shape.name, n_lm)
