@@ -1467,7 +1467,8 @@ __device__ void do_gemv(const Params &p, const Ctx &cx, const Instr &in, uint32_
 // applied there too, from the sums of squares the warps gathered while
 // loading their slices.
 // Tile order: K-chunk by K-chunk over all row blocks when the instruction's
-// accumulators fit in shared memory; otherwise (LM head) groups of 8 row
+// accumulators fit in shared memory; otherwise (more rows per instruction
+// than the accumulators hold) groups of 8 row
 // blocks, all K-chunks of a group before the next, through a ring of 8
 // accumulator slots (a warp runs at most kPages tiles ahead of the slowest,
 // and a slot is reused 8 tiles later).
